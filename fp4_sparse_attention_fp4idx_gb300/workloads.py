@@ -1,0 +1,301 @@
+"""Seeded synthetic inputs for the fused FP4 indexer pre-pass.
+
+This module only draws inputs: it holds none of the method's arithmetic, and
+both the CUDA path and the CPU oracle consume what it returns.  Everything is
+generated on the host with numpy's PCG64 (identical streams on x86-64 and
+aarch64); bf16 tensors are returned as uint16 bit patterns, rounded from fp32
+draws with torch's CPU fp32->bf16 conversion.
+
+Workload shapes follow the pages' indexer shapes (head_dim 128, rope_dim 64,
+group 32, kv_block 64; H = 32 or 64 query heads; DeepSeek / GLM-style decode,
+MTP and prefill batches).  The RoPE tables are the caller-side cos/sin cache,
+fp32 [max_pos, 32], theta = pos * base^(-2i/64) evaluated in double.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+HEAD_DIM = 128
+ROPE_HALF = 32
+KV_BLOCK = 64
+PAGE_BYTES = KV_BLOCK * 68
+ROPE_NEOX = 0
+ROPE_INTERLEAVED = 1
+
+# E2M1 midpoints and the group anchor 6 used to build exact-tie rows.
+_MID_PATTERN = [6.0, 0.25, -0.25, 0.75, -0.75, 1.25, -1.25, 1.75, -1.75,
+                2.5, -2.5, 3.5, -3.5, 5.0, -5.0]
+
+
+def to_bf16_bits(x) -> np.ndarray:
+    """fp32/fp64 array -> bf16 bit patterns (uint16), via torch CPU."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def bf16_bits_to_f32(b) -> np.ndarray:
+    return (np.asarray(b, dtype=np.uint32) << 16).view(np.float32)
+
+
+def rope_tables(max_pos: int, base: float = 10000.0):
+    """cos/sin fp32 [max_pos, 32]: theta(p, i) = p * base^(-2i/64)."""
+    i = np.arange(ROPE_HALF, dtype=np.float64)
+    inv_freq = base ** (-2.0 * i / (2 * ROPE_HALF))
+    theta = np.arange(max_pos, dtype=np.float64)[:, None] * inv_freq[None, :]
+    return np.cos(theta).astype(np.float32), np.sin(theta).astype(np.float32)
+
+
+def _normal_bf16(rng, shape, chunk_rows: int = 1 << 22) -> np.ndarray:
+    """N(0,1) bf16 bits, drawn in chunks of rows to bound host memory."""
+    shape = tuple(shape)
+    n = int(np.prod(shape))
+    out = np.empty(n, np.uint16)
+    step = chunk_rows * HEAD_DIM
+    for s in range(0, n, step):
+        e = min(n, s + step)
+        out[s:e] = to_bf16_bits(rng.standard_normal(e - s, dtype=np.float32))
+    return out.reshape(shape)
+
+
+def midpoint_group_values(scale_pow2: int) -> np.ndarray:
+    """32 values 2^k * {6, +-0.25, +-0.75, ..., +-5, 0...}: with anchor 6*2^k
+    the group's scale is exactly 2^k, so every listed value sits on an exact
+    E2M1 midpoint after scaling."""
+    v = np.zeros(32, np.float64)
+    v[:len(_MID_PATTERN)] = _MID_PATTERN
+    return v * (2.0 ** scale_pow2)
+
+
+def midpoint_key_row() -> np.ndarray:
+    """A 128-element key row whose exact midpoints survive RMSNorm when gamma
+    is 1: row = 8 * p where each group of p holds the 15 midpoint/anchor
+    values plus integer fillers (11, 11, 10, 10 sixes; a one in groups 2, 3).
+    The squares of p add up to 2048 exactly, so the mean square of the row is
+    64 * 2048 / 128 = 1024 = 4^5 and the normalised row is exactly p / 4."""
+    p = np.zeros((4, 32), np.float64)
+    sixes = [11, 11, 10, 10]
+    ones = [0, 0, 1, 1]
+    for g in range(4):
+        p[g, :15] = _MID_PATTERN
+        p[g, 15:15 + sixes[g]] = 6.0
+        p[g, 15 + sixes[g]:15 + sixes[g] + ones[g]] = 1.0
+    assert float((p * p).sum()) == 2048.0
+    return (8.0 * p).reshape(-1)
+
+
+def subnormal_bf16(rng, n: int) -> np.ndarray:
+    """Random bf16 subnormals: exponent field 0, mantissa 1..127, random sign."""
+    mant = rng.integers(1, 128, size=n, dtype=np.uint16)
+    sign = rng.integers(0, 2, size=n, dtype=np.uint16) << 15
+    return (mant | sign).astype(np.uint16)
+
+
+@dataclass
+class Workload:
+    name: str
+    T: int
+    H: int
+    rope_style: int
+    q: np.ndarray            # uint16 [T,H,128]
+    w: np.ndarray            # uint16 [T,H]
+    k: np.ndarray            # uint16 [T,128]
+    gamma: np.ndarray        # uint16 [128]
+    eps: float
+    positions: np.ndarray    # int64 [T]
+    cos: np.ndarray          # f32 [max_pos,32]
+    sin: np.ndarray          # f32 [max_pos,32]
+    slot_mapping: np.ndarray  # int64 [T]
+    num_blocks: int
+    cache_init: np.ndarray   # uint8 [num_blocks, 4352] sentinel bytes
+    notes: dict = field(default_factory=dict)
+
+    @property
+    def max_pos(self) -> int:
+        return int(self.cos.shape[0])
+
+
+def _sentinel_cache(rng, num_blocks: int) -> np.ndarray:
+    return rng.integers(0, 256, size=(num_blocks, PAGE_BYTES), dtype=np.uint8)
+
+
+def _gamma(rng) -> np.ndarray:
+    return to_bf16_bits(1.0 + 0.1 * rng.standard_normal(HEAD_DIM))
+
+
+def make_tiny(gamma_one: bool = False) -> Workload:
+    """T=8, H=32, NeoX, seed 0.  Token 1 all zeros, token 2 bf16 subnormals,
+    token 3 exact E2M1 midpoints at position 0 (RoPE is the identity there).
+    With gamma_one the key midpoints survive RMSNorm too."""
+    rng = np.random.Generator(np.random.PCG64(0))
+    T, H = 8, 32
+    q = _normal_bf16(rng, (T, H, HEAD_DIM))
+    k = _normal_bf16(rng, (T, HEAD_DIM))
+    q[1] = 0
+    k[1] = 0
+    q[2] = subnormal_bf16(rng, H * HEAD_DIM).reshape(H, HEAD_DIM)
+    k[2] = subnormal_bf16(rng, HEAD_DIM)
+    for h in range(H):
+        q[3, h] = to_bf16_bits(np.concatenate(
+            [midpoint_group_values(h - 16 + g) for g in range(4)]))
+    k[3] = to_bf16_bits(midpoint_key_row())
+    gamma = to_bf16_bits(np.ones(HEAD_DIM)) if gamma_one else _gamma(rng)
+    if gamma_one:
+        _gamma(rng)  # keep the stream aligned with the gamma~N case
+    positions = rng.integers(0, 4096, size=T, dtype=np.int64)
+    positions[3] = 0
+    cos, sin = rope_tables(4096)
+    w = _normal_bf16(rng, (T, H))
+    num_blocks = 4
+    slots = rng.permutation(num_blocks * KV_BLOCK)[:T].astype(np.int64)
+    cache = _sentinel_cache(rng, num_blocks)
+    return Workload("tiny_gamma1" if gamma_one else "tiny", T, H, ROPE_NEOX,
+                    q, w, k, gamma, 1e-6, positions, cos, sin, slots,
+                    num_blocks, cache)
+
+
+def make_decode() -> Workload:
+    """T=256, H=64, interleaved RoPE, seed 1.  Rows ~N(0,1) times a per-row
+    factor from {1, 40, 1e-3}; positions U[0,131072); 4096 blocks; distinct
+    random slots with 10% set to -1."""
+    rng = np.random.Generator(np.random.PCG64(1))
+    T, H = 256, 64
+    fac = np.array([1.0, 40.0, 1e-3])
+    qf = rng.standard_normal((T, H, HEAD_DIM)) * fac[rng.integers(0, 3, (T, H, 1))]
+    kf = rng.standard_normal((T, HEAD_DIM)) * fac[rng.integers(0, 3, (T, 1))]
+    q = to_bf16_bits(qf)
+    k = to_bf16_bits(kf)
+    gamma = _gamma(rng)
+    max_pos = 131072
+    positions = rng.integers(0, max_pos, size=T, dtype=np.int64)
+    cos, sin = rope_tables(max_pos)
+    w = _normal_bf16(rng, (T, H))
+    num_blocks = 4096
+    slots = rng.choice(num_blocks * KV_BLOCK, size=T, replace=False).astype(np.int64)
+    slots[rng.random(T) < 0.10] = -1
+    cache = _sentinel_cache(rng, num_blocks)
+    return Workload("decode", T, H, ROPE_INTERLEAVED, q, w, k, gamma, 1e-6,
+                    positions, cos, sin, slots, num_blocks, cache)
+
+
+def make_prefill() -> Workload:
+    """T=8192, H=64, NeoX, positions 0..8191, seed 2.  N(0,1) with 1% of the
+    entries (Bernoulli mask) scaled by 50 before the bf16 cast; 8192 blocks,
+    the tokens filling 128 consecutive blocks from a seeded start block."""
+    rng = np.random.Generator(np.random.PCG64(2))
+    T, H = 8192, 64
+
+    def draw(shape):
+        x = rng.standard_normal(shape, dtype=np.float32)
+        x[rng.random(shape, dtype=np.float32) < 0.01] *= 50.0
+        return to_bf16_bits(x)
+
+    q = draw((T, H, HEAD_DIM))
+    k = draw((T, HEAD_DIM))
+    gamma = _gamma(rng)
+    positions = np.arange(T, dtype=np.int64)
+    cos, sin = rope_tables(T)
+    w = _normal_bf16(rng, (T, H))
+    num_blocks = 8192
+    start = int(rng.integers(0, num_blocks - T // KV_BLOCK + 1))
+    slots = start * KV_BLOCK + np.arange(T, dtype=np.int64)
+    cache = _sentinel_cache(rng, num_blocks)
+    return Workload("prefill", T, H, ROPE_NEOX, q, w, k, gamma, 1e-6,
+                    positions, cos, sin, slots, num_blocks, cache)
+
+
+def make_large_prefill(T: int = 65536) -> Workload:
+    """T=65536, H=64, NeoX, positions 0..T-1, N(0,1), seed 3; 16384 blocks,
+    token t -> block perm[t // 64], offset t % 64 (perm a random permutation
+    of the blocks).  A smaller T keeps the same recipe for quick runs."""
+    rng = np.random.Generator(np.random.PCG64(3))
+    H = 64
+    q = _normal_bf16(rng, (T, H, HEAD_DIM))
+    k = _normal_bf16(rng, (T, HEAD_DIM))
+    gamma = _gamma(rng)
+    positions = np.arange(T, dtype=np.int64)
+    cos, sin = rope_tables(T)
+    w = _normal_bf16(rng, (T, H))
+    num_blocks = 16384
+    perm = rng.permutation(num_blocks).astype(np.int64)
+    t = np.arange(T, dtype=np.int64)
+    slots = perm[t // KV_BLOCK] * KV_BLOCK + t % KV_BLOCK
+    cache = _sentinel_cache(rng, num_blocks)
+    return Workload("large_prefill" if T == 65536 else f"large_prefill_T{T}",
+                    T, H, ROPE_NEOX, q, w, k, gamma, 1e-6, positions, cos,
+                    sin, slots, num_blocks, cache)
+
+
+def make_mtp() -> Workload:
+    """1024 sequences x next_n=4 (T=4096), H=32, interleaved RoPE, seed 4.
+    Per-sequence base position U[0,65536) plus offsets 0..3; Laplace(0,1)
+    bf16; 65536 blocks; each sequence's one or two pages drawn without reuse
+    from a random block permutation; 5% of slots set to -1."""
+    rng = np.random.Generator(np.random.PCG64(4))
+    S, NN, H = 1024, 4, 32
+    T = S * NN
+    q = to_bf16_bits(rng.laplace(0.0, 1.0, (T, H, HEAD_DIM)))
+    k = to_bf16_bits(rng.laplace(0.0, 1.0, (T, HEAD_DIM)))
+    gamma = _gamma(rng)
+    base = rng.integers(0, 65536, size=S, dtype=np.int64)
+    positions = (base[:, None] + np.arange(NN, dtype=np.int64)[None, :]).reshape(-1)
+    max_pos = 65536 + NN - 1
+    cos, sin = rope_tables(max_pos)
+    w = _normal_bf16(rng, (T, H))
+    num_blocks = 65536
+    perm = iter(rng.permutation(num_blocks).astype(np.int64).tolist())
+    slots = np.empty(T, np.int64)
+    for s in range(S):
+        table = {}
+        for j in range(NN):
+            p = int(positions[s * NN + j])
+            lb = p // KV_BLOCK
+            if lb not in table:
+                table[lb] = next(perm)
+            slots[s * NN + j] = table[lb] * KV_BLOCK + p % KV_BLOCK
+    slots[rng.random(T) < 0.05] = -1
+    cache = _sentinel_cache(rng, num_blocks)
+    return Workload("mtp", T, H, ROPE_INTERLEAVED, q, w, k, gamma, 1e-6,
+                    positions, cos, sin, slots, num_blocks, cache)
+
+
+def make_random(T: int, H: int, rope_style: int, seed: int, max_pos: int = 512,
+                num_blocks: int | None = None, skip_frac: float = 0.1,
+                scales=(1.0, 40.0, 1e-3)) -> Workload:
+    """Small generic case: per-row scales, random positions, random distinct
+    slots with a fraction skipped."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    fac = np.asarray(scales, np.float64)
+    qf = rng.standard_normal((T, H, HEAD_DIM)) * fac[rng.integers(0, len(fac), (T, H, 1))]
+    kf = rng.standard_normal((T, HEAD_DIM)) * fac[rng.integers(0, len(fac), (T, 1))]
+    q = to_bf16_bits(qf)
+    k = to_bf16_bits(kf)
+    gamma = _gamma(rng)
+    positions = rng.integers(0, max_pos, size=T, dtype=np.int64)
+    cos, sin = rope_tables(max_pos)
+    w = _normal_bf16(rng, (T, H))
+    if num_blocks is None:
+        num_blocks = max(1, (2 * T + KV_BLOCK - 1) // KV_BLOCK)
+    slots = rng.choice(num_blocks * KV_BLOCK, size=T, replace=False).astype(np.int64)
+    slots[rng.random(T) < skip_frac] = -1
+    cache = _sentinel_cache(rng, num_blocks)
+    return Workload(f"random_T{T}_H{H}_s{rope_style}_{seed}", T, H, rope_style,
+                    q, w, k, gamma, 1e-6, positions, cos, sin, slots,
+                    num_blocks, cache)
+
+
+CONFIGS = {
+    "tiny": make_tiny,
+    "decode": make_decode,
+    "prefill": make_prefill,
+    "large_prefill": make_large_prefill,
+    "mtp": make_mtp,
+}
+
+
+def make(name: str) -> Workload:
+    if name == "tiny_gamma1":
+        return make_tiny(gamma_one=True)
+    return CONFIGS[name]()

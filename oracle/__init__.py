@@ -1,0 +1,218 @@
+"""Plain scalar CPU oracle of the fused FP4 indexer pre-pass.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline / reference legs of ``bench.py`` may import this package.
+The product path (``fp4_sparse_attention_fp4idx_gb300``) never does, and this
+package never imports the product.
+
+The arithmetic lives in ``fp4idx_oracle.c`` (plain C, compiled without FP
+contraction); this module only builds it with gcc and marshals numpy arrays.
+bf16 arrays are carried as ``uint16`` bit patterns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fp4idx_oracle.c")
+_LIB = os.path.join(_HERE, "libfp4idx_oracle.so")
+
+HEAD_DIM = 128
+PAYLOAD_BYTES = 64
+EXP_BYTES = 4
+KV_BLOCK = 64
+PAGE_BYTES = KV_BLOCK * (PAYLOAD_BYTES + EXP_BYTES)
+ROPE_NEOX = 0
+ROPE_INTERLEAVED = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no FP contraction, no fast-math)."""
+    hdr = os.path.join(_HERE, "fp4idx_oracle.h")
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= max(os.path.getmtime(_SRC), os.path.getmtime(hdr))):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+           "-fno-strict-aliasing", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
+    P = ctypes.c_void_p
+    i64 = ctypes.c_int64
+    L.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
+    L.oracle_f32_to_bf16.restype = ctypes.c_uint16
+    L.oracle_rmsnorm_row.argtypes = [P, P, ctypes.c_float, P]
+    L.oracle_rmsnorm_row.restype = None
+    L.oracle_rope_row.argtypes = [P, P, P, ctypes.c_int]
+    L.oracle_rope_row.restype = None
+    L.oracle_quant_group.argtypes = [P, ctypes.c_float, P]
+    L.oracle_quant_group.restype = ctypes.c_int
+    L.oracle_dequant.argtypes = [ctypes.c_uint8, ctypes.c_int]
+    L.oracle_dequant.restype = ctypes.c_float
+    L.oracle_quant_pack_row.argtypes = [P, P, P, P, P, P]
+    L.oracle_quant_pack_row.restype = None
+    L.oracle_k_norm_rope_pack_store.argtypes = [
+        P, P, ctypes.c_float, P, P, P, i64, ctypes.c_int, P, P, i64, i64]
+    L.oracle_k_norm_rope_pack_store.restype = ctypes.c_int
+    L.oracle_q_rope_pack_weights.argtypes = [
+        P, P, P, P, P, i64, ctypes.c_int, P, P, P, i64, i64]
+    L.oracle_q_rope_pack_weights.restype = ctypes.c_int
+    return L
+
+
+_lib = None
+_active = None  # set by use_variant(): a planted-mistake build for mutation tests
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _active is not None:
+        return _active
+    if _lib is None:
+        build()
+        _lib = _bind(ctypes.CDLL(_LIB))
+    return _lib
+
+
+def compile_variant(source_text: str, workdir: str) -> ctypes.CDLL:
+    """Compile a modified copy of the oracle's C source (used by the tests to
+    plant a mistake and check that the pins catch it)."""
+    import shutil
+    src = os.path.join(workdir, "fp4idx_oracle.c")
+    shutil.copy(os.path.join(_HERE, "fp4idx_oracle.h"), workdir)
+    with open(src, "w") as f:
+        f.write(source_text)
+    so = os.path.join(workdir, f"libvariant{abs(hash(source_text))}.so")
+    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+                    "-fno-strict-aliasing", "-shared", "-fPIC", "-o", so, src, "-lm"],
+                   check=True)
+    return _bind(ctypes.CDLL(so))
+
+
+class use_variant:
+    """Context manager: route every oracle call to the given library."""
+
+    def __init__(self, L):
+        self.L = L
+
+    def __enter__(self):
+        global _active
+        self.prev, _active = _active, self.L
+        return self.L
+
+    def __exit__(self, *exc):
+        global _active
+        _active = self.prev
+        return False
+
+
+def source_text() -> str:
+    with open(_SRC) as f:
+        return f.read()
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ---------------------------------------------------------------- single steps
+def f32_to_bf16(x: float) -> int:
+    return int(lib().oracle_f32_to_bf16(ctypes.c_float(x)))
+
+
+def rmsnorm_row(x_bits, gamma_bits, eps: float) -> np.ndarray:
+    x = _c(x_bits, np.uint16)
+    g = _c(gamma_bits, np.uint16)
+    assert x.shape == (HEAD_DIM,) and g.shape == (HEAD_DIM,)
+    y = np.empty(HEAD_DIM, np.uint16)
+    lib().oracle_rmsnorm_row(_p(x), _p(g), ctypes.c_float(eps), _p(y))
+    return y
+
+
+def rope_row(y_bits, cos_row, sin_row, rope_style: int) -> np.ndarray:
+    y = _c(y_bits, np.uint16).copy()
+    c = _c(cos_row, np.float32)
+    s = _c(sin_row, np.float32)
+    assert y.shape == (HEAD_DIM,) and c.shape == (32,) and s.shape == (32,)
+    lib().oracle_rope_row(_p(y), _p(c), _p(s), int(rope_style))
+    return y
+
+
+def quant_group(z, floor: float = 2.0 ** -126):
+    """Returns (nibbles uint8[32], exponent)."""
+    z = _c(z, np.float32)
+    assert z.shape == (32,)
+    n = np.empty(32, np.uint8)
+    e = lib().oracle_quant_group(_p(z), ctypes.c_float(floor), _p(n))
+    return n, int(e)
+
+
+def dequant(nibble: int, e: int) -> float:
+    return float(lib().oracle_dequant(ctypes.c_uint8(nibble), int(e)))
+
+
+def quant_pack_row(row_bits):
+    """Returns dict(payload[64], exp[4], e1[4], e2[4], n1[128])."""
+    r = _c(row_bits, np.uint16)
+    assert r.shape == (HEAD_DIM,)
+    payload = np.empty(PAYLOAD_BYTES, np.uint8)
+    ex = np.empty(EXP_BYTES, np.uint8)
+    e1 = np.empty(4, np.int32)
+    e2 = np.empty(4, np.int32)
+    n1 = np.empty(HEAD_DIM, np.uint8)
+    lib().oracle_quant_pack_row(_p(r), _p(payload), _p(ex), _p(e1), _p(e2), _p(n1))
+    return dict(payload=payload, exp=ex, e1=e1, e2=e2, n1=n1)
+
+
+# ------------------------------------------------------------------ full ops
+def k_norm_rope_pack_store(k, gamma, eps, positions, cos_cache, sin_cache,
+                           rope_style, slot_mapping, kv_cache) -> int:
+    """kv_cache (uint8 [num_blocks, 4352]) is updated in place."""
+    k = _c(k, np.uint16)
+    T = k.shape[0]
+    assert k.shape == (T, HEAD_DIM)
+    g = _c(gamma, np.uint16)
+    pos = _c(positions, np.int64)
+    cs = _c(cos_cache, np.float32)
+    sn = _c(sin_cache, np.float32)
+    sl = _c(slot_mapping, np.int64)
+    assert kv_cache.dtype == np.uint8 and kv_cache.flags.c_contiguous
+    assert kv_cache.shape[1:] == (PAGE_BYTES,)
+    assert pos.shape == (T,) and sl.shape == (T,) and cs.shape == sn.shape
+    return int(lib().oracle_k_norm_rope_pack_store(
+        _p(k), _p(g), ctypes.c_float(eps), _p(pos), _p(cs), _p(sn), cs.shape[0],
+        int(rope_style), _p(sl), _p(kv_cache), kv_cache.shape[0], T))
+
+
+def q_rope_pack_weights(q, w, positions, cos_cache, sin_cache, rope_style,
+                        out=None):
+    """Returns (q_fp4 [T,H,64] u8, q_scale [T,H,4] u8, weights [T,H] f32, status)."""
+    q = _c(q, np.uint16)
+    T, H, D = q.shape
+    assert D == HEAD_DIM
+    w = _c(w, np.uint16)
+    assert w.shape == (T, H)
+    pos = _c(positions, np.int64)
+    cs = _c(cos_cache, np.float32)
+    sn = _c(sin_cache, np.float32)
+    if out is None:
+        out = (np.zeros((T, H, PAYLOAD_BYTES), np.uint8),
+               np.zeros((T, H, EXP_BYTES), np.uint8),
+               np.zeros((T, H), np.float32))
+    qf, qs, wt = out
+    st = lib().oracle_q_rope_pack_weights(
+        _p(q), _p(w), _p(pos), _p(cs), _p(sn), cs.shape[0], int(rope_style),
+        _p(qf), _p(qs), _p(wt), T, H)
+    return qf, qs, wt, int(st)

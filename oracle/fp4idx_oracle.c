@@ -1,0 +1,295 @@
+/*
+ * fp4idx_oracle.c -- plain, slow, scalar CPU oracle for the fused FP4
+ * indexer pre-pass.  TEST INFRASTRUCTURE ONLY (see fp4idx_oracle.h).
+ *
+ * Build with no floating-point contraction and no fast-math so that every
+ * fp32 operation below is one IEEE round-to-nearest-even step:
+ *     gcc -O2 -ffp-contract=off -fno-fast-math -shared -fPIC
+ * (fp32 expressions are evaluated in fp32 on x86-64 SSE and on aarch64.)
+ *
+ * Notation used in the comments: rn32(.) is one fp32 rounding, bf16(.) one
+ * fp32 -> bf16 rounding, both to nearest with ties to even.
+ */
+#include "fp4idx_oracle.h"
+
+#include <math.h>
+#include <string.h>
+
+enum {
+  HEAD_DIM = 128,     /* [aiter] API: head_dim = 128 */
+  ROPE_DIM = 64,      /* [aiter] API: rope_dim = 64, dims 0..63 */
+  GROUP = 32,         /* [aiter] API: group_size = 32 (per-32 UE8M0 scales) */
+  KV_BLOCK = 64,      /* [aiter] API: kv_block_size = 64 */
+  PAYLOAD_BYTES = 64, /* [sgl] Summary: 64 e2m1 bytes ... */
+  EXP_BYTES = 4,      /* ... plus four block exponents = 68-byte slot */
+  PAGE_BYTES = KV_BLOCK * (PAYLOAD_BYTES + EXP_BYTES) /* 4352 */
+};
+
+/* The E2M1 grid: magnitude code m in 0..7 encodes GRID[m]. */
+static const double GRID[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+/* Scale floors of the two quantisation stages.  The [sgl] review says the
+ * indexer packer applies its floor after the amax/6 division and that the
+ * packer's floor differs from the fake-quant's; neither value is printed.
+ * Reading taken: both floors are 2^-126 (the smallest normal fp32), applied
+ * after the division.  They only decide the exponent of groups whose amax is
+ * below 6 * 2^-126 (all-zero and subnormal groups get exponent byte 1). */
+static const float STAGE1_FLOOR = 1.17549435082228750797e-38f; /* 2^-126 */
+static const float STAGE2_FLOOR = 1.17549435082228750797e-38f; /* 2^-126 */
+
+static uint32_t f2u(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  return u;
+}
+static float u2f(uint32_t u) {
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+static float bf16_to_f32(uint16_t b) { return u2f((uint32_t)b << 16); }
+
+/* fp32 -> bf16, round to nearest, ties to even, written from the definition:
+ * take the two bf16 neighbours of |x| (truncation, and one bf16 ulp above
+ * it), keep the nearer one, and on a tie the one whose last bit is 0.  The
+ * distances are exact in double.  Finite inputs only. */
+uint16_t oracle_f32_to_bf16(float x) {
+  uint32_t u = f2u(x);
+  uint32_t sign = u & 0x80000000u;
+  uint32_t mag = u & 0x7fffffffu;
+  uint32_t lo = mag & 0xffff0000u;   /* bf16 neighbour toward zero */
+  uint32_t hi = lo + 0x00010000u;    /* next bf16 magnitude up     */
+  double m = (double)u2f(mag);
+  double d_lo = m - (double)u2f(lo);
+  double d_hi = (double)u2f(hi) - m;
+  uint32_t pick;
+  if (d_lo < d_hi)
+    pick = lo;
+  else if (d_hi < d_lo)
+    pick = hi;
+  else
+    pick = ((lo >> 16) & 1u) ? hi : lo; /* tie: even last bit */
+  return (uint16_t)((sign | pick) >> 16);
+}
+
+/* RMSNorm of an index-key row ([sgl] Summary: the key kernel fuses RMSNorm
+ * ahead of RoPE), y = bf16(rn32(rn32(x * r) * gamma)).
+ * Readings (pages silent): fp32 arithmetic, x*r before *gamma, one bf16
+ * rounding at the end (the bf16 round trip after RMSNorm); r is a correctly
+ * rounded sqrt followed by a correctly rounded reciprocal.  The sum of squares
+ * uses one fixed order: 16 partial sums of 8 consecutive squares, accumulated
+ * left to right, then combined pairwise at distances 8, 4, 2, 1 (partial c
+ * plus partial c^d), the total being partial 0. */
+void oracle_rmsnorm_row(const uint16_t* xb, const uint16_t* gamma, float eps,
+                        uint16_t* y) {
+  float x[HEAD_DIM];
+  for (int i = 0; i < HEAD_DIM; ++i) x[i] = bf16_to_f32(xb[i]);
+
+  float p[16];
+  for (int c = 0; c < 16; ++c) {
+    float acc = x[8 * c] * x[8 * c];
+    for (int j = 1; j < 8; ++j) {
+      float sq = x[8 * c + j] * x[8 * c + j];
+      acc = acc + sq;
+    }
+    p[c] = acc;
+  }
+  for (int d = 8; d >= 1; d >>= 1) {
+    float nxt[16];
+    for (int c = 0; c < 16; ++c) nxt[c] = p[c] + p[c ^ d];
+    memcpy(p, nxt, sizeof p);
+  }
+  float sum = p[0];
+  float ms = sum / 128.0f;
+  float den = ms + eps;
+  float root = sqrtf(den);
+  float r = 1.0f / root;
+  for (int i = 0; i < HEAD_DIM; ++i) {
+    float xr = x[i] * r;
+    float xg = xr * bf16_to_f32(gamma[i]);
+    y[i] = oracle_f32_to_bf16(xg);
+  }
+}
+
+/* RoPE on dims 0..63 ([aiter] API: rope_dim = 64 and the is_neox switch;
+ * [sgl] Summary: the bf16 round trip after RoPE).  Pair i (0..31) uses
+ * cos_row[i], sin_row[i]:
+ *   NeoX:        (a, b) = (y[i], y[i+32])
+ *   interleaved: (a, b) = (y[2i], y[2i+1])
+ *   a' = bf16(rn32(rn32(a*c) - rn32(b*s))),  b' = bf16(rn32(rn32(b*c) + rn32(a*s)))
+ * Dims 64..127 pass through unchanged. */
+void oracle_rope_row(uint16_t* y, const float* cos_row, const float* sin_row,
+                     int rope_style) {
+  for (int i = 0; i < ROPE_DIM / 2; ++i) {
+    int ia, ib;
+    if (rope_style == ORACLE_ROPE_NEOX) {
+      ia = i;
+      ib = i + ROPE_DIM / 2;
+    } else {
+      ia = 2 * i;
+      ib = 2 * i + 1;
+    }
+    float a = bf16_to_f32(y[ia]);
+    float b = bf16_to_f32(y[ib]);
+    float c = cos_row[i];
+    float s = sin_row[i];
+    float ac = a * c, bs = b * s, bc = b * c, as = a * s;
+    float na = ac - bs;
+    float nb = bc + as;
+    y[ia] = oracle_f32_to_bf16(na);
+    y[ib] = oracle_f32_to_bf16(nb);
+  }
+}
+
+/* Nearest E2M1 code of a magnitude v >= 0, by brute force over the grid;
+ * on an exact tie the even code wins (round half to even, [sgl] Summary and
+ * [aiter] One deliberate deviation).  Values above 6 land on code 7.  The
+ * distances are exact in double for every v that can sit near a midpoint. */
+static int e2m1_nearest_code(double v) {
+  int best = 0;
+  double best_d = fabs(v - GRID[0]);
+  for (int m = 1; m < 8; ++m) {
+    double d = fabs(v - GRID[m]);
+    if (d < best_d || (d == best_d && (m % 2) == 0 && (best % 2) != 0)) {
+      best = m;
+      best_d = d;
+    }
+  }
+  return best;
+}
+
+/* One per-32 UE8M0 group ([sgl] review, index_pack_exponent and
+ * clear_negative_zero):
+ *   A = max|z|;  t = max(rn32(A / 6), floor)
+ *   e = (bits(t) >> 23) + (mantissa(t) != 0), clamped to [1, 254]
+ *       i.e. the biased exponent of the power of two ceil_pow2(t)
+ *   code = nearest grid point to |z| / 2^(e-127), ties to even
+ *   nibble = code | 8 if z < 0 and code != 0  (no -0 codes). */
+int oracle_quant_group(const float* z, float floor_, uint8_t* nibbles) {
+  float amax = 0.0f;
+  for (int i = 0; i < GROUP; ++i) {
+    float a = fabsf(z[i]);
+    if (a > amax) amax = a;
+  }
+  float t = amax / 6.0f;
+  if (t < floor_) t = floor_;
+  uint32_t bits = f2u(t);
+  int e = (int)(bits >> 23) + ((bits & 0x7fffffu) != 0u ? 1 : 0);
+  if (e < 1) e = 1;
+  if (e > 254) e = 254;
+  double scale = ldexp(1.0, e - 127);
+  for (int i = 0; i < GROUP; ++i) {
+    double v = fabs((double)z[i]) / scale;
+    int m = e2m1_nearest_code(v);
+    int neg = (z[i] < 0.0f) && (m != 0);
+    nibbles[i] = (uint8_t)(m | (neg ? 8 : 0));
+  }
+  return e;
+}
+
+float oracle_dequant(uint8_t nibble, int e) {
+  double v = GRID[nibble & 7] * ldexp(1.0, e - 127);
+  if (nibble & 8) v = -v;
+  return (float)v; /* exact: at most two significant bits */
+}
+
+/* Stage 1 fake-quantises the row to the per-32 UE8M0 E2M1 grid (dequantised
+ * back to bf16, which is exact); stage 2 runs the indexer packer on that
+ * result with its own floor ([sgl] review: "Keep both quantization stages").
+ * Pack: payload byte 16g+j = nibble[32g+2j] | nibble[32g+2j+1] << 4, and
+ * exponent byte g = stage-2 exponent of group g.
+ * Readings (pages silent): even element in the low nibble; group g in byte g
+ * of the little-endian exponent word. */
+void oracle_quant_pack_row(const uint16_t* row, uint8_t* payload64,
+                           uint8_t* exp4, int* stage1_e, int* stage2_e,
+                           uint8_t* stage1_nibbles) {
+  for (int g = 0; g < HEAD_DIM / GROUP; ++g) {
+    float z[GROUP];
+    for (int i = 0; i < GROUP; ++i) z[i] = bf16_to_f32(row[GROUP * g + i]);
+
+    uint8_t n1[GROUP];
+    int e1 = oracle_quant_group(z, STAGE1_FLOOR, n1);
+    float u[GROUP];
+    for (int i = 0; i < GROUP; ++i) {
+      float dq = oracle_dequant(n1[i], e1);
+      u[i] = bf16_to_f32(oracle_f32_to_bf16(dq));
+    }
+
+    uint8_t n2[GROUP];
+    int e2 = oracle_quant_group(u, STAGE2_FLOOR, n2);
+
+    for (int j = 0; j < GROUP / 2; ++j)
+      payload64[16 * g + j] = (uint8_t)(n2[2 * j] | (n2[2 * j + 1] << 4));
+    exp4[g] = (uint8_t)e2;
+    if (stage1_e) stage1_e[g] = e1;
+    if (stage2_e) stage2_e[g] = e2;
+    if (stage1_nibbles) memcpy(stage1_nibbles + GROUP * g, n1, GROUP);
+  }
+}
+
+/* Keys ([sgl] Summary: RMSNorm, RoPE, both quantisation stages and the paged
+ * cache store in one op).  Slot s >= 0 goes to page s/64, offset s%64.
+ * Readings: a negative slot means "skip" (slot 0 is an ordinary slot); the
+ * 68 bytes of a slot are split inside the 4352-byte page into the 64-byte
+ * payload at o*64 and the 4-byte exponent word at 4096 + o*4. */
+int oracle_k_norm_rope_pack_store(const uint16_t* k, const uint16_t* gamma,
+                                  float eps, const int64_t* positions,
+                                  const float* cos_cache,
+                                  const float* sin_cache, int64_t max_pos,
+                                  int rope_style, const int64_t* slot_mapping,
+                                  uint8_t* kv_cache, int64_t num_blocks,
+                                  int64_t num_tokens) {
+  int status = 0;
+  for (int64_t t = 0; t < num_tokens; ++t) {
+    int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    int64_t pos = positions[t];
+    if (pos < 0 || pos >= max_pos || slot >= num_blocks * KV_BLOCK) {
+      status = -1;
+      continue;
+    }
+    uint16_t y[HEAD_DIM];
+    oracle_rmsnorm_row(k + t * HEAD_DIM, gamma, eps, y);
+    oracle_rope_row(y, cos_cache + pos * (ROPE_DIM / 2),
+                    sin_cache + pos * (ROPE_DIM / 2), rope_style);
+    uint8_t payload[PAYLOAD_BYTES], ex[EXP_BYTES];
+    oracle_quant_pack_row(y, payload, ex, NULL, NULL, NULL);
+    int64_t b = slot / KV_BLOCK, o = slot % KV_BLOCK;
+    uint8_t* page = kv_cache + b * PAGE_BYTES;
+    memcpy(page + o * PAYLOAD_BYTES, payload, PAYLOAD_BYTES);
+    memcpy(page + KV_BLOCK * PAYLOAD_BYTES + o * EXP_BYTES, ex, EXP_BYTES);
+  }
+  return status;
+}
+
+/* Queries ([sgl] Summary: the query op rotates, quantises and packs the same
+ * way and computes the head weights in the same launch; [aiter] API: weights
+ * carry the plain weight, fp32 here, nothing folded in). */
+int oracle_q_rope_pack_weights(const uint16_t* q, const uint16_t* w,
+                               const int64_t* positions,
+                               const float* cos_cache, const float* sin_cache,
+                               int64_t max_pos, int rope_style,
+                               uint8_t* q_fp4, uint8_t* q_scale,
+                               float* weights, int64_t num_tokens,
+                               int64_t num_heads) {
+  int status = 0;
+  double wscale = 1.0 / sqrt((double)num_heads * (double)HEAD_DIM);
+  for (int64_t t = 0; t < num_tokens; ++t) {
+    int64_t pos = positions[t];
+    if (pos < 0 || pos >= max_pos) {
+      status = -1;
+      continue;
+    }
+    for (int64_t h = 0; h < num_heads; ++h) {
+      int64_t r = t * num_heads + h;
+      uint16_t y[HEAD_DIM];
+      memcpy(y, q + r * HEAD_DIM, sizeof y);
+      oracle_rope_row(y, cos_cache + pos * (ROPE_DIM / 2),
+                      sin_cache + pos * (ROPE_DIM / 2), rope_style);
+      oracle_quant_pack_row(y, q_fp4 + r * PAYLOAD_BYTES,
+                            q_scale + r * EXP_BYTES, NULL, NULL, NULL);
+      weights[r] = (float)((double)bf16_to_f32(w[r]) * wscale);
+    }
+  }
+  return status;
+}

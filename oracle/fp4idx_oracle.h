@@ -1,0 +1,98 @@
+/*
+ * fp4idx_oracle.h -- plain scalar CPU oracle for the fused FP4 indexer
+ * pre-pass.  TEST INFRASTRUCTURE ONLY: nothing on the product path may link,
+ * load or call this library.  Only the test suite, the smoke check and the
+ * bench's CPU-baseline / reference legs use it.
+ *
+ * It shares no code, header, table or constant with the CUDA library.  Every
+ * buffer is a HOST pointer to a dense, row-major array.  bf16 values are
+ * passed as their 16-bit patterns (uint16_t).
+ *
+ * Sources (web pages on FP4 DSA-indexer keys and queries):
+ *   [sgl]  "dsv4.1: RoPE and FP4 packing kernels" (sglang PR 39656):
+ *          Summary; Verification; review comment on clear_negative_zero,
+ *          index_pack_exponent and inv_scale_ue8m0.
+ *   [aiter] "[HIP] Add FP4 output mode to indexer_qk_rope_quant_and_cache"
+ *          (aiter PR 5484): API; Verification; One deliberate deviation.
+ *
+ * Where the pages leave a step open, the reading used is stated beside the
+ * function that takes it.
+ */
+#ifndef FP4IDX_ORACLE_H
+#define FP4IDX_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* RoPE pairing styles. */
+#define ORACLE_ROPE_NEOX 0        /* pairs (i, i+32), i in 0..31 */
+#define ORACLE_ROPE_INTERLEAVED 1 /* pairs (2i, 2i+1), i in 0..31 */
+
+/* ---- single steps, exported so the tests can pin each one ---- */
+
+/* fp32 -> bf16 bit pattern, round to nearest, ties to even (finite input). */
+uint16_t oracle_f32_to_bf16(float x);
+
+/* RMSNorm of one 128-element key row, bf16 in / bf16 out. */
+void oracle_rmsnorm_row(const uint16_t* x, const uint16_t* gamma, float eps,
+                        uint16_t* y);
+
+/* In-place RoPE of the first 64 dims of a 128-element bf16 row. */
+void oracle_rope_row(uint16_t* y, const float* cos_row, const float* sin_row,
+                     int rope_style);
+
+/* Quantise one 32-element group z (fp32 values) with scale floor `floor_`.
+ * Writes 32 nibbles (bit 3 sign, bits 2..0 E2M1 code) and returns the
+ * biased UE8M0 exponent. */
+int oracle_quant_group(const float* z, float floor_, uint8_t* nibbles);
+
+/* Dequantise a nibble with biased exponent e (exact in fp32). */
+float oracle_dequant(uint8_t nibble, int e);
+
+/* Both quantisation stages + pack for one 128-element bf16 row:
+ * 64 payload bytes and 4 exponent bytes (group g -> byte g).
+ * If stage1_e / stage2_e are non-NULL they receive the 4 exponents of each
+ * stage; stage1_codes (128 nibbles) likewise, for invariant tests. */
+void oracle_quant_pack_row(const uint16_t* row, uint8_t* payload64,
+                           uint8_t* exp4, int* stage1_e, int* stage2_e,
+                           uint8_t* stage1_nibbles);
+
+/* ---- the two operations of the pre-pass ---- */
+
+/* Keys: RMSNorm -> RoPE -> two-stage FP4 -> 68-byte slot -> paged cache.
+ *   k          [T,128] bf16      gamma [128] bf16
+ *   positions  [T] int64         cos_cache, sin_cache [max_pos,32] fp32
+ *   slot_mapping [T] int64 (<0: skip the token)
+ *   kv_cache   [num_blocks, 4352] bytes: page b holds 64 payloads of 64 B
+ *              at b*4352 + o*64, then 64 exponent words at b*4352+4096+o*4.
+ * Returns 0, or -1 if a position or slot is out of range (that row is
+ * skipped, the others are still written). */
+int oracle_k_norm_rope_pack_store(const uint16_t* k, const uint16_t* gamma,
+                                  float eps, const int64_t* positions,
+                                  const float* cos_cache,
+                                  const float* sin_cache, int64_t max_pos,
+                                  int rope_style, const int64_t* slot_mapping,
+                                  uint8_t* kv_cache, int64_t num_blocks,
+                                  int64_t num_tokens);
+
+/* Queries: RoPE -> two-stage FP4 -> pack, plus fp32 head weights.
+ *   q [T,H,128] bf16, w [T,H] bf16
+ *   q_fp4 [T,H,64] bytes, q_scale [T,H,4] bytes, weights [T,H] fp32
+ *   weights[t,h] = w[t,h] * H^-1/2 * D^-1/2 (D = 128), rounded once.
+ * Returns 0, or -1 if a position is out of range (that token's outputs are
+ * left untouched). */
+int oracle_q_rope_pack_weights(const uint16_t* q, const uint16_t* w,
+                               const int64_t* positions,
+                               const float* cos_cache, const float* sin_cache,
+                               int64_t max_pos, int rope_style,
+                               uint8_t* q_fp4, uint8_t* q_scale,
+                               float* weights, int64_t num_tokens,
+                               int64_t num_heads);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FP4IDX_ORACLE_H */

@@ -1,0 +1,112 @@
+"""Each plausible mistake, planted in a copy of the oracle's C source and
+compiled on the CPU, must fail at least one independent pin (the digest test,
+which compares the oracle with its own earlier output, is not counted)."""
+import inspect
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+# (name, text in the oracle source, replacement)
+MUTANTS = [
+    ("tie_to_odd", "(d == best_d && (m % 2) == 0 && (best % 2) != 0)",
+     "(d == best_d && (m % 2) != 0 && (best % 2) == 0)"),
+    ("tie_toward_lower_code", " || (d == best_d && (m % 2) == 0 && (best % 2) != 0)", ""),
+    ("keep_negative_zero", "int neg = (z[i] < 0.0f) && (m != 0);", "int neg = (z[i] < 0.0f);"),
+    ("nibble_order_swapped", "(uint8_t)(n2[2 * j] | (n2[2 * j + 1] << 4))",
+     "(uint8_t)(n2[2 * j + 1] | (n2[2 * j] << 4))"),
+    ("exponent_floor_not_ceil", "+ ((bits & 0x7fffffu) != 0u ? 1 : 0)", "+ 0"),
+    ("amax_over_4", "float t = amax / 6.0f;", "float t = amax / 4.0f;"),
+    ("large_floor", "STAGE1_FLOOR = 1.17549435082228750797e-38f",
+     "STAGE1_FLOOR = 1e-10f"),
+    ("single_stage", "int e2 = oracle_quant_group(u, STAGE2_FLOOR, n2);",
+     "int e2 = e1; memcpy(n2, n1, GROUP);"),
+    ("scale_bias_off_by_one", "double scale = ldexp(1.0, e - 127);",
+     "double scale = ldexp(1.0, e - 128);"),
+    ("amax_signed", "float a = fabsf(z[i]);", "float a = z[i];"),
+    ("exp_bytes_reversed", "exp4[g] = (uint8_t)e2;", "exp4[3 - g] = (uint8_t)e2;"),
+    ("mean_over_64", "float ms = sum / 128.0f;", "float ms = sum / 64.0f;"),
+    ("eps_outside_sqrt", "float den = ms + eps;\n  float root = sqrtf(den);",
+     "float den = ms;\n  float root = sqrtf(den) + eps;"),
+    ("gamma_dropped", "float xg = xr * bf16_to_f32(gamma[i]);", "float xg = xr;"),
+    ("no_reciprocal", "float r = 1.0f / root;", "float r = root;"),
+    ("rope_sign", "float na = ac - bs;", "float na = ac + bs;"),
+    ("rope_cos_sin_swapped", "float c = cos_row[i];\n    float s = sin_row[i];",
+     "float c = sin_row[i];\n    float s = cos_row[i];"),
+    ("rope_neox_partner_half_head", "ib = i + ROPE_DIM / 2;", "ib = i + HEAD_DIM / 2;"),
+    ("rope_interleaved_table_index", "float c = cos_row[i];",
+     "float c = cos_row[rope_style == ORACLE_ROPE_NEOX ? i : (2 * i) % 32];"),
+    ("slot_record_interleaved",
+     "memcpy(page + o * PAYLOAD_BYTES, payload, PAYLOAD_BYTES);\n"
+     "    memcpy(page + KV_BLOCK * PAYLOAD_BYTES + o * EXP_BYTES, ex, EXP_BYTES);",
+     "memcpy(page + o * 68, payload, PAYLOAD_BYTES);\n"
+     "    memcpy(page + o * 68 + PAYLOAD_BYTES, ex, EXP_BYTES);"),
+    ("slot_zero_skipped", "if (slot < 0) continue;", "if (slot <= 0) continue;"),
+    ("weights_scale_no_sqrt_of_heads",
+     "double wscale = 1.0 / sqrt((double)num_heads * (double)HEAD_DIM);",
+     "double wscale = 1.0 / ((double)num_heads * sqrt((double)HEAD_DIM));"),
+    ("bf16_truncate", "if (d_lo < d_hi)\n    pick = lo;", "if (1)\n    pick = lo;"),
+    ("bf16_ties_up", "pick = ((lo >> 16) & 1u) ? hi : lo;", "pick = hi;"),
+    ("q_rope_skipped",
+     "      oracle_rope_row(y, cos_cache + pos * (ROPE_DIM / 2),\n"
+     "                      sin_cache + pos * (ROPE_DIM / 2), rope_style);\n", ""),
+    ("k_rope_skipped",
+     "    oracle_rope_row(y, cos_cache + pos * (ROPE_DIM / 2),\n"
+     "                    sin_cache + pos * (ROPE_DIM / 2), rope_style);\n", ""),
+]
+
+# Independent pins, cheapest first.
+PINS = [
+    pins.test_golden_e2m1_values,
+    pins.test_golden_pack_layout,
+    pins.test_all_zero_group,
+    pins.test_rmsnorm_constant_row_closed_form,
+    pins.test_rmsnorm_midpoint_key_row,
+    pins.test_rmsnorm_eps_inside_sqrt,
+    pins.test_rope_identity_and_quarter_turn,
+    pins.test_rope_single_pair_and_general,
+    pins.test_cache_store_placement_and_skip,
+    pins.test_out_of_range_rows_are_skipped,
+    pins.test_golden_midpoint_key_slot,
+    pins.test_golden_tiny_query_midpoints,
+    pins.test_k_op_closed_form_composition,
+    pins.test_q_op_closed_form_composition,
+    pins.test_weights_closed_form,
+    pins.test_two_stage_invariants,
+    pins.test_group_quant_exact_rational,
+    pins.test_exponent_exhaustive_bf16,
+    pins.test_bf16_rounding_matches_torch,
+    pins.test_rmsnorm_random_rows_vs_fp64,
+    pins.test_codes_exhaustive_bf16,
+]
+
+
+def _run(fn):
+    params = inspect.signature(fn).parameters
+    if "style" in params:
+        for s in (0, 1):
+            fn(style=s)
+    else:
+        fn()
+
+
+def test_unmutated_oracle_passes_all_pins():
+    for fn in PINS:
+        _run(fn)
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_planted_mistake_is_caught(name, old, new, tmp_path):
+    src = oracle.source_text()
+    assert src.count(old) == 1, f"mutation site for {name} not unique"
+    L = oracle.compile_variant(src.replace(old, new), str(tmp_path))
+    caught = None
+    with oracle.use_variant(L):
+        for fn in PINS:
+            try:
+                _run(fn)
+            except AssertionError:
+                caught = fn.__name__
+                break
+    assert caught is not None, f"mutant {name} passed every pin"
