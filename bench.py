@@ -1,0 +1,461 @@
+"""Benchmark of the fused FP4 indexer pre-pass (keys + queries) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload large_prefill] [--mode fused|separate]
+
+One step = the whole hot path over one batch: key RMSNorm/RoPE/FP4/paged
+store for T tokens and query RoPE/FP4/pack/head weights for T x H rows, with
+the inputs resident in HBM.  Prints ONE JSON line (rank 0).
+
+Timing: W untimed warm-up steps, then K timed steps between a barrier and a
+device synchronisation; before every timed step a buffer of twice the L2 size
+is written (outside the step's CUDA events) so no step reads a previous
+step's data from L2.  Per-step device time comes from CUDA events on the
+launching stream.  nvidia-smi samples SM clocks and throttle reasons during
+the timed region.
+
+The reference arm (--impl reference) times the CPU oracle on the host cores
+on a bounded sample of the same workload; under torchrun only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = ("tokens/s and achieved HBM GB/s (fraction of GB300 peak), "
+          "fused indexer K+Q FP4 pack")
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------- bytes model
+def algorithmic_bytes(w, mode: str) -> dict:
+    """Bytes a step must move at minimum.  Per query row: 256 (q) + 2 (w) +
+    64 (q_fp4) + 4 (q_scale) + 4 (weight); per token: 8 (position) + 8 (slot);
+    per distinct position: 256 (cos+sin rows); per stored key row: 256 (k) +
+    68 (slot); once: 256 (gamma).  The separate key call re-reads positions
+    and cos/sin rows for its own rows."""
+    T, H = w.T, w.H
+    valid = (w.slot_mapping >= 0)
+    n_valid = int(valid.sum())
+    d_all = int(np.unique(w.positions).size)
+    d_valid = int(np.unique(w.positions[valid]).size)
+    q_call = T * H * (256 + 2 + 64 + 4 + 4) + T * 8 + 256 * d_all
+    k_call = n_valid * (256 + 68 + 8) + T * 8 + 256 * d_valid + 256
+    fused = T * H * (256 + 2 + 64 + 4 + 4) + T * 16 + 256 * d_all + n_valid * (256 + 68) + 256
+    return {"q_call": q_call, "k_call": k_call, "fused": fused,
+            "step": fused if mode == "fused" else q_call + k_call, "n_valid": n_valid}
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_record(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    src = os.path.join(ROOT, "fp4_sparse_attention_fp4idx_gb300", "csrc", "fp4idx.cu")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        with open(src, "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()
+        rec = d.get(kernel)
+        if rec and rec.get("source_sha256") == h:
+            return rec
+    except Exception:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for ln in f:
+                p = [x.strip() for x in ln.split(",")]
+                if len(p) >= 9:
+                    rows.append(p)
+        os.unlink(self.path)
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------------ distributed
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws: int, backend: str):
+    import torch.distributed as dist
+    if ws > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if ws > 1 else None
+
+
+def max_over_ranks(x: float, dist, device=None) -> float:
+    """Max of a scalar over all ranks (identity when not distributed)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# --------------------------------------------------------------- our arm
+def upload(w, device):
+    import torch
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+    def d(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+    return dict(k=bf(w.k), gamma=bf(w.gamma), slots=d(w.slot_mapping), cache=d(w.cache_init),
+                q=bf(w.q), w=bf(w.w), pos=d(w.positions), cos=d(w.cos), sin=d(w.sin))
+
+
+def make_step(F, D, w, mode, outs):
+    qf, qs, wt = outs
+
+    def step():
+        if mode == "fused":
+            F.indexer_prepass(D["k"], D["gamma"], D["slots"], D["cache"], D["q"], D["w"],
+                              D["pos"], D["cos"], D["sin"], eps=w.eps, rope_style=w.rope_style,
+                              q_fp4=qf, q_scale=qs, weights=wt)
+        else:
+            F.k_norm_rope_pack_store(D["k"], D["gamma"], D["pos"], D["cos"], D["sin"],
+                                     D["slots"], D["cache"], eps=w.eps, rope_style=w.rope_style)
+            F.q_rope_pack_weights(D["q"], D["w"], D["pos"], D["cos"], D["sin"],
+                                  rope_style=w.rope_style, q_fp4=qf, q_scale=qs, weights=wt)
+    return step
+
+
+def time_device(F, w, D, mode, steps, warmup, flush, dist=None, sampler=None):
+    """Returns dict with per-step event times (ms) of the whole step and, in
+    separate mode, of each launch."""
+    import torch
+    dev = D["q"].device
+    T, H = w.T, w.H
+    outs = (torch.empty((T, H, 64), dtype=torch.uint8, device=dev),
+            torch.empty((T, H, 4), dtype=torch.uint8, device=dev),
+            torch.empty((T, H), dtype=torch.float32, device=dev))
+    step = make_step(F, D, w, mode, outs)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    barrier(dist)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.1)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        flush.zero_()
+        a, m, b = ev[i]
+        a.record(stream)
+        if mode == "fused":
+            step()
+        else:
+            F.k_norm_rope_pack_store(D["k"], D["gamma"], D["pos"], D["cos"], D["sin"],
+                                     D["slots"], D["cache"], eps=w.eps, rope_style=w.rope_style)
+            m.record(stream)
+            F.q_rope_pack_weights(D["q"], D["w"], D["pos"], D["cos"], D["sin"],
+                                  rope_style=w.rope_style, q_fp4=outs[0], q_scale=outs[1],
+                                  weights=outs[2])
+        b.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    barrier(dist)
+    clocks = sampler.stop() if sampler else None
+    step_ms = [a.elapsed_time(b) for a, _, b in ev]
+    res = {"step_ms": step_ms, "wall_s": wall, "clocks": clocks}
+    if mode != "fused":
+        res["k_ms"] = [a.elapsed_time(m) for a, m, _ in ev]
+        res["q_ms"] = [m.elapsed_time(b) for _, m, b in ev]
+    return res
+
+
+def time_e2e(F, w, D, mode, steps):
+    """Through the public API with host buffers: per step, copy the step's
+    inputs (q, w, k, positions, slot mapping) from pinned host memory, run
+    the pre-pass, and copy the query outputs back.  The cos/sin tables, gamma
+    and the paged cache stay resident on the device."""
+    import torch
+    dev = D["q"].device
+    names = ("q", "w", "k", "pos", "slots")
+    host = {n: D[n].cpu().pin_memory() for n in names}
+    T, H = w.T, w.H
+    outs = (torch.empty((T, H, 64), dtype=torch.uint8, device=dev),
+            torch.empty((T, H, 4), dtype=torch.uint8, device=dev),
+            torch.empty((T, H), dtype=torch.float32, device=dev))
+    hout = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    step = make_step(F, D, w, mode, outs)
+    stream = torch.cuda.current_stream()
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+
+    def one():
+        for n in names:
+            D[n].copy_(host[n], non_blocking=True)
+        step()
+        for o, h in zip(outs, hout):
+            h.copy_(o, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps, h2d, d2h
+
+
+def cpu_baseline(w, budget_s: float = 12.0):
+    """The oracle as it stands, single-threaded, on the first S tokens of the
+    workload (keys and queries), S grown until about budget_s of CPU work."""
+    import oracle
+    oracle.build()
+    S = 64
+    while True:
+        sub_q, sub_w, pos = w.q[:S], w.w[:S], w.positions[:S]
+        cache = w.cache_init.copy()
+        t0 = time.perf_counter()
+        oracle.k_norm_rope_pack_store(w.k[:S], w.gamma, w.eps, pos, w.cos, w.sin,
+                                      w.rope_style, w.slot_mapping[:S], cache)
+        oracle.q_rope_pack_weights(sub_q, sub_w, pos, w.cos, w.sin, w.rope_style)
+        dt = time.perf_counter() - t0
+        if dt * 4 > budget_s or S >= w.T:
+            break
+        S = min(w.T, S * 4)
+    return {"value": S / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {S} of {w.T} tokens of the {w.name} workload (H={w.H}), "
+                      f"keys and queries, single thread, {dt:.2f} s"}
+
+
+def run_ours(args):
+    import torch
+    from fp4_sparse_attention_fp4idx_gb300 import fp4idx as F
+    from fp4_sparse_attention_fp4idx_gb300 import workloads as wl
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = init_dist(ws, "nccl")
+    dev = torch.device("cuda", local)
+    peak, peak_kind = measured_peak()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+
+    w = wl.make(args.workload)
+    D = upload(w, dev)
+    sampler = ClockSampler(local) if rank == 0 else None
+    r = time_device(F, w, D, args.mode, args.steps, args.warmup, flush, dist, sampler)
+    step_ms = statistics.mean(r["step_ms"])
+    step_ms_all = max_over_ranks(step_ms, dist, dev)
+    ab = algorithmic_bytes(w, args.mode)
+    value = ws * w.T / (step_ms_all / 1e3)
+
+    # dominant kernel: the fused launch, or the query launch in separate mode
+    if args.mode == "fused":
+        kname, kbytes, kms = "prepass_kernel", ab["fused"], step_ms
+    else:
+        kname, kbytes, kms = "q_kernel", ab["q_call"], statistics.mean(r["q_ms"])
+    achieved = kbytes / (kms / 1e3) / 1e9
+    tr = traffic_record(kname)
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                "kernel": kname, "algorithmic_bytes_per_launch": kbytes,
+                "traffic": tr["dram_bytes_per_launch"] if tr else None}
+
+    e2e_ms, h2d, d2h = time_e2e(F, w, D, args.mode, max(3, min(args.steps, 10)))
+    e2e_ms_all = max_over_ranks(e2e_ms, dist, dev)
+
+    extra = {}
+    if rank == 0 and not args.no_extra:
+        for name in ("prefill", "decode", "mtp"):
+            if name == args.workload:
+                continue
+            wx = wl.make(name)
+            Dx = upload(wx, dev)
+            rx = time_device(F, wx, Dx, args.mode, 50, 5, flush)
+            ms = statistics.mean(rx["step_ms"])
+            bx = algorithmic_bytes(wx, args.mode)["step"]
+            extra[name] = {"T": wx.T, "H": wx.H, "ms_per_step": round(ms, 5),
+                           "tokens_per_s": round(wx.T / (ms / 1e3), 1),
+                           "gbs": round(bx / (ms / 1e3) / 1e9, 1),
+                           "frac_of_peak": round(bx / (ms / 1e3) / 1e9 / peak, 4)}
+            del Dx
+
+    base = cpu_baseline(w) if (rank == 0 and ws == 1 and not args.no_cpu) else None
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms_all, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "T": w.T, "H": w.H, "head_dim": 128, "rope_dim": 64,
+                       "rope_style": "neox" if w.rope_style == 0 else "interleaved",
+                       "kv_blocks": w.num_blocks, "mode": args.mode,
+                       "l2": "flushed before every timed step (write of 2x L2 size)"},
+            "gbs": round(ab["step"] / (step_ms_all / 1e3) / 1e9, 1),
+            "frac_of_peak": round(ab["step"] / (step_ms_all / 1e3) / 1e9 / peak, 4),
+            "algorithmic_bytes_per_step": ab["step"],
+            "roofline": roofline,
+            "e2e": {"value": round(ws * w.T / (e2e_ms_all / 1e3), 1), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": round(e2e_ms_all, 4)},
+            "gpu_launches": args.steps * (1 if args.mode == "fused" else 2),
+            "clocks": r["clocks"],
+            "cpu_baseline": base,
+            "timed_wall_s": round(r["wall_s"], 4),
+            "other_configs": extra,
+        }
+        if args.mode != "fused":
+            line["k_ms"] = round(statistics.mean(r["k_ms"]), 5)
+            line["q_ms"] = round(statistics.mean(r["q_ms"]), 5)
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------- reference arm
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from fp4_sparse_attention_fp4idx_gb300 import workloads as wl
+    oracle.build()
+    w = wl.make(args.workload)
+    S = min(w.T, args.ref_tokens)
+    cache = w.cache_init.copy()
+
+    def step():
+        oracle.k_norm_rope_pack_store(w.k[:S], w.gamma, w.eps, w.positions[:S], w.cos, w.sin,
+                                      w.rope_style, w.slot_mapping[:S], cache)
+        oracle.q_rope_pack_weights(w.q[:S], w.w[:S], w.positions[:S], w.cos, w.sin,
+                                   w.rope_style)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = S / dt
+    sample = (f"first {S} of {w.T} tokens of the {w.name} workload (H={w.H}) per step, "
+              "keys and queries, single thread")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "H": w.H, "head_dim": 128, "rope_dim": 64,
+                   "rope_style": "neox" if w.rope_style == 0 else "interleaved",
+                   "kv_blocks": w.num_blocks, "mode": "oracle"},
+        "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": 1,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="large_prefill",
+                    choices=["tiny", "decode", "prefill", "large_prefill", "mtp"])
+    ap.add_argument("--mode", choices=["fused", "separate"], default="fused")
+    ap.add_argument("--ref-tokens", type=int, default=512,
+                    help="tokens per step of the reference (oracle) arm")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

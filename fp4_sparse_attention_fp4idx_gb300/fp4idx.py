@@ -1,0 +1,257 @@
+"""ctypes binding of libfp4idx.so (argument marshalling only).
+
+Importing this module loads the CUDA library and raises ImportError if it is
+missing: there is no CPU path.  Build it with
+``python -m fp4_sparse_attention_fp4idx_gb300.build``.
+
+Two layers:
+  * ``lib()`` -- the raw C ABI (names and argument order of include/fp4idx.h,
+    plain integers for pointers).
+  * torch wrappers with the same names (minus the ``fp4idx_`` prefix) that
+    check dtypes/devices, allocate outputs with torch, pass ``data_ptr()``s
+    and the current CUDA stream, and raise ``Fp4idxError`` on a non-OK
+    status.  Every step of the computation runs in the library's kernels.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfp4idx.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "fp4idx.h")
+
+ROPE_NEOX = 0
+ROPE_INTERLEAVED = 1
+HEAD_DIM = 128
+PAGE_BYTES = 4352
+ERRFLAG_POSITION = 0x1
+ERRFLAG_SLOT = 0x2
+
+OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_ARG, ERR_CUDA = range(6)
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with "
+        "`python -m fp4_sparse_attention_fp4idx_gb300.build` (needs nvcc); "
+        "there is no CPU fallback")
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_F = ctypes.c_float
+_INT = ctypes.c_int
+
+_SIGS = {
+    "fp4idx_k_norm_rope_pack_store": (
+        _INT, [_P, _I64, _P, _F, _P, _P, _P, _I64, _INT, _P, _P, _I64, _I64, _P, _P]),
+    "fp4idx_q_rope_pack_weights": (
+        _INT, [_P, _I64, _I64, _P, _I64, _F, _P, _P, _P, _I64, _INT, _P, _P, _P, _I64,
+               _I64, _P, _P]),
+    "fp4idx_indexer_prepass": (
+        _INT, [_P, _I64, _P, _F, _P, _P, _I64,
+               _P, _I64, _I64, _P, _I64, _F, _P, _P, _P, _I64,
+               _P, _P, _P, _I64, _INT, _I64, _P, _P]),
+    "fp4idx_status_string": (ctypes.c_char_p, [_INT]),
+    "fp4idx_version": (ctypes.c_char_p, []),
+}
+
+_lib = ctypes.CDLL(LIB_PATH)
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+def lib() -> ctypes.CDLL:
+    return _lib
+
+
+def declared_symbols(header: str = HEADER_PATH) -> list:
+    """Names of the functions include/fp4idx.h declares."""
+    with open(header) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    return sorted(set(re.findall(r"\b(fp4idx_[a-z0-9_]+)\s*\(", text)))
+
+
+def status_string(status: int) -> str:
+    return _lib.fp4idx_status_string(int(status)).decode()
+
+
+def version() -> str:
+    return _lib.fp4idx_version().decode()
+
+
+class Fp4idxError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: status {status} ({status_string(status)})")
+        self.status = status
+
+
+def _check(status: int, where: str) -> None:
+    if status != OK:
+        raise Fp4idxError(status, where)
+
+
+def rope_style_code(style) -> int:
+    if style in (ROPE_NEOX, "neox"):
+        return ROPE_NEOX
+    if style in (ROPE_INTERLEAVED, "interleaved", "gptj"):
+        return ROPE_INTERLEAVED
+    raise ValueError(f"unknown rope style {style!r}")
+
+
+def default_weight_scale(num_heads: int, head_dim: int = HEAD_DIM) -> float:
+    """fp32(H^-1/2 * D^-1/2), evaluated in double."""
+    return float(ctypes.c_float(1.0 / math.sqrt(num_heads * head_dim)).value)
+
+
+# ------------------------------------------------------------ torch wrappers
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_ptr(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(int(s.cuda_stream))
+
+
+def _need(t, dtype, name, ndim=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    return t
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def k_norm_rope_pack_store(k, gamma, positions, cos_cache, sin_cache, slot_mapping,
+                           kv_cache, *, eps: float = 1e-6, rope_style="neox",
+                           err_flags=None, stream=None) -> None:
+    """Keys -> paged FP4 index cache, in place.  k bf16 [T,128] (row stride a
+    multiple of 8), gamma bf16 [128], positions/slot_mapping int64 [T],
+    cos/sin fp32 [max_pos,32], kv_cache uint8 [num_blocks, 4352]."""
+    torch = _torch()
+    _need(k, torch.bfloat16, "k", 2)
+    _need(gamma, torch.bfloat16, "gamma", 1)
+    _need(positions, torch.int64, "positions", 1)
+    _need(slot_mapping, torch.int64, "slot_mapping", 1)
+    _need(cos_cache, torch.float32, "cos_cache", 2)
+    _need(sin_cache, torch.float32, "sin_cache", 2)
+    _need(kv_cache, torch.uint8, "kv_cache", 2)
+    T = k.shape[0]
+    if k.shape[1] != HEAD_DIM or k.stride(1) != 1:
+        raise ValueError("k must be [T,128] with unit element stride")
+    if gamma.shape[0] != HEAD_DIM or not gamma.is_contiguous():
+        raise ValueError("gamma must be contiguous [128]")
+    if positions.shape[0] != T or slot_mapping.shape[0] != T:
+        raise ValueError("positions and slot_mapping must have T entries")
+    if not (positions.is_contiguous() and slot_mapping.is_contiguous()):
+        raise ValueError("positions and slot_mapping must be contiguous")
+    if cos_cache.shape != sin_cache.shape or cos_cache.shape[1] != 32:
+        raise ValueError("cos/sin caches must both be [max_pos, 32]")
+    if not (cos_cache.is_contiguous() and sin_cache.is_contiguous()):
+        raise ValueError("cos/sin caches must be contiguous")
+    if kv_cache.shape[1] != PAGE_BYTES or not kv_cache.is_contiguous():
+        raise ValueError("kv_cache must be contiguous [num_blocks, 4352]")
+    st = _lib.fp4idx_k_norm_rope_pack_store(
+        _ptr(k), k.stride(0), _ptr(gamma), float(eps), _ptr(positions), _ptr(cos_cache),
+        _ptr(sin_cache), cos_cache.shape[0], rope_style_code(rope_style), _ptr(slot_mapping),
+        _ptr(kv_cache), kv_cache.shape[0], T, _ptr(err_flags), _stream_ptr(stream))
+    _check(st, "fp4idx_k_norm_rope_pack_store")
+
+
+def _q_outputs(q_fp4, q_scale, weights, T, H, device):
+    torch = _torch()
+    if q_fp4 is None:
+        q_fp4 = torch.empty((T, H, 64), dtype=torch.uint8, device=device)
+    if q_scale is None:
+        q_scale = torch.empty((T, H, 4), dtype=torch.uint8, device=device)
+    if weights is None:
+        weights = torch.empty((T, H), dtype=torch.float32, device=device)
+    for t, shape, dt, name in ((q_fp4, (T, H, 64), torch.uint8, "q_fp4"),
+                               (q_scale, (T, H, 4), torch.uint8, "q_scale"),
+                               (weights, (T, H), torch.float32, "weights")):
+        _need(t, dt, name)
+        if tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous {shape}")
+    return q_fp4, q_scale, weights
+
+
+def _check_q(q, w, positions, cos_cache, sin_cache):
+    torch = _torch()
+    _need(q, torch.bfloat16, "q", 3)
+    _need(w, torch.bfloat16, "w", 2)
+    _need(positions, torch.int64, "positions", 1)
+    _need(cos_cache, torch.float32, "cos_cache", 2)
+    _need(sin_cache, torch.float32, "sin_cache", 2)
+    T, H, D = q.shape
+    if D != HEAD_DIM or q.stride(2) != 1:
+        raise ValueError("q must be [T,H,128] with unit element stride")
+    if tuple(w.shape) != (T, H) or w.stride(1) != 1:
+        raise ValueError("w must be [T,H] with unit head stride")
+    if positions.shape[0] != T or not positions.is_contiguous():
+        raise ValueError("positions must be contiguous [T]")
+    if cos_cache.shape != sin_cache.shape or cos_cache.shape[1] != 32:
+        raise ValueError("cos/sin caches must both be [max_pos, 32]")
+    if not (cos_cache.is_contiguous() and sin_cache.is_contiguous()):
+        raise ValueError("cos/sin caches must be contiguous")
+    return T, H
+
+
+def q_rope_pack_weights(q, w, positions, cos_cache, sin_cache, *, rope_style="neox",
+                        weight_scale=None, q_fp4=None, q_scale=None, weights=None,
+                        err_flags=None, stream=None):
+    """Queries -> (q_fp4 uint8 [T,H,64], q_scale uint8 [T,H,4], weights fp32
+    [T,H]).  q bf16 [T,H,128] (strides multiples of 8), w bf16 [T,H]."""
+    T, H = _check_q(q, w, positions, cos_cache, sin_cache)
+    q_fp4, q_scale, weights = _q_outputs(q_fp4, q_scale, weights, T, H, q.device)
+    ws = default_weight_scale(H) if weight_scale is None else float(weight_scale)
+    st = _lib.fp4idx_q_rope_pack_weights(
+        _ptr(q), q.stride(0), q.stride(1), _ptr(w), w.stride(0), ws, _ptr(positions),
+        _ptr(cos_cache), _ptr(sin_cache), cos_cache.shape[0], rope_style_code(rope_style),
+        _ptr(q_fp4), _ptr(q_scale), _ptr(weights), T, H, _ptr(err_flags), _stream_ptr(stream))
+    _check(st, "fp4idx_q_rope_pack_weights")
+    return q_fp4, q_scale, weights
+
+
+def indexer_prepass(k, gamma, slot_mapping, kv_cache, q, w, positions, cos_cache, sin_cache, *,
+                    eps: float = 1e-6, rope_style="neox", weight_scale=None, q_fp4=None,
+                    q_scale=None, weights=None, err_flags=None, stream=None):
+    """Both halves in one launch; returns (q_fp4, q_scale, weights) and updates
+    kv_cache in place.  Same argument rules as the two separate calls."""
+    torch = _torch()
+    T, H = _check_q(q, w, positions, cos_cache, sin_cache)
+    _need(k, torch.bfloat16, "k", 2)
+    _need(gamma, torch.bfloat16, "gamma", 1)
+    _need(slot_mapping, torch.int64, "slot_mapping", 1)
+    _need(kv_cache, torch.uint8, "kv_cache", 2)
+    if k.shape[0] != T or k.shape[1] != HEAD_DIM or k.stride(1) != 1:
+        raise ValueError("k must be [T,128] with unit element stride")
+    if gamma.shape[0] != HEAD_DIM or not gamma.is_contiguous():
+        raise ValueError("gamma must be contiguous [128]")
+    if slot_mapping.shape[0] != T or not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be contiguous [T]")
+    if kv_cache.shape[1] != PAGE_BYTES or not kv_cache.is_contiguous():
+        raise ValueError("kv_cache must be contiguous [num_blocks, 4352]")
+    q_fp4, q_scale, weights = _q_outputs(q_fp4, q_scale, weights, T, H, q.device)
+    ws = default_weight_scale(H) if weight_scale is None else float(weight_scale)
+    st = _lib.fp4idx_indexer_prepass(
+        _ptr(k), k.stride(0), _ptr(gamma), float(eps), _ptr(slot_mapping), _ptr(kv_cache),
+        kv_cache.shape[0], _ptr(q), q.stride(0), q.stride(1), _ptr(w), w.stride(0), ws,
+        _ptr(q_fp4), _ptr(q_scale), _ptr(weights), H, _ptr(positions), _ptr(cos_cache),
+        _ptr(sin_cache), cos_cache.shape[0], rope_style_code(rope_style), T, _ptr(err_flags),
+        _stream_ptr(stream))
+    _check(st, "fp4idx_indexer_prepass")
+    return q_fp4, q_scale, weights

@@ -1,0 +1,185 @@
+/*
+ * fp4idx.h -- C ABI of libfp4idx.so, the fused FP4 indexer pre-pass of a
+ * DeepSeek-style sparse-attention (DSA) indexer, as CUDA kernels for one
+ * GB300 GPU (sm_103a).
+ *
+ * What it computes (sources are web pages, cited by title and section):
+ *   "dsv4.1: RoPE and FP4 packing kernels" (sglang PR 39656), Summary: keys
+ *   get RMSNorm, RoPE, two quantisation stages to the per-32 UE8M0 E2M1 grid
+ *   (round half to even) and a paged-cache store of the 68-byte index-K slot
+ *   (64 e2m1 bytes + 4 block exponents); queries get the same RoPE and
+ *   quantisation plus fp32 head weights in the same launch.
+ *   "[HIP] Add FP4 output mode to indexer_qk_rope_quant_and_cache" (aiter PR
+ *   5484), API: head_dim 128, rope_dim 64, group 32, kv_block 64; q_out is
+ *   u8 [T, H, 64]; weights carry the plain weight, nothing folded in.
+ *
+ * Fixed geometry (anything else is not representable in these calls):
+ *   head_dim 128, RoPE on dims 0..63, groups of 32 (4 per row), 64 slots per
+ *   cache page.
+ *
+ * Numerics, per 128-element row (all fp32 steps round to nearest even, no
+ * fused multiply-add, subnormals kept):
+ *   RMSNorm (keys only): sum of squares in a fixed order (16 partial sums of
+ *     8 consecutive squares, then pairwise at distances 8, 4, 2, 1),
+ *     r = 1 / sqrt(sum/128 + eps) (correctly rounded sqrt, then correctly
+ *     rounded reciprocal), y = bf16((x * r) * gamma).
+ *   RoPE: pair i in 0..31 is (i, i+32) for NeoX or (2i, 2i+1) interleaved,
+ *     a' = bf16(a*c - b*s), b' = bf16(b*c + a*s) with c, s = cos/sin[pos][i].
+ *   Quantisation, per group of 32 (both stages): e = biased exponent of
+ *     ceil_pow2(max(amax/6, 2^-126)); code = nearest of
+ *     {0,.5,1,1.5,2,3,4,6} to |z| * 2^(127-e), ties to the even code; sign
+ *     bit only on a non-zero code.  Stage 1 dequantises; stage 2 packs.
+ *   Slot: payload byte 16g+j = nib[32g+2j] | nib[32g+2j+1] << 4; exponent
+ *     word byte g = stage-2 exponent of group g.
+ *   Weights: weights[t,h] = fp32(w[t,h]) * weight_scale (one rounding).
+ *
+ * Conventions for every call:
+ *   - All data pointers are DEVICE pointers (cudaMalloc / torch CUDA memory)
+ *     on the current device.  bf16 tensors are passed as const void*.
+ *   - The caller owns every buffer.  The library allocates nothing, keeps no
+ *     per-call state, never synchronises, and enqueues one kernel on
+ *     `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *   - Host-side checks run before anything is enqueued; a failing check
+ *     returns its status and enqueues nothing.  num_tokens == 0 returns
+ *     FP4IDX_OK and enqueues nothing.
+ *   - Device-side range checks: a position outside [0, max_pos) or a slot
+ *     >= num_blocks*64 never causes an out-of-bounds access; the token is
+ *     skipped (its outputs are left untouched) and, if err_flags is not
+ *     NULL, the matching FP4IDX_ERRFLAG_* bit is OR-ed into *err_flags.
+ *   - Inputs must keep every intermediate finite: |x| below ~1.8e19 for
+ *     keys (the fp32 sum of squares), and every 32-element group of the
+ *     rotated row with amax <= 6*2^125 (the stage-1 dequantised values);
+ *     outputs for non-finite intermediates are unspecified.
+ *   - Calls are asynchronous; errors of the kernel itself surface at the
+ *     caller's next synchronisation.  FP4IDX_ERR_CUDA reports a failed
+ *     launch (cudaGetLastError right after it).
+ */
+#ifndef FP4IDX_H
+#define FP4IDX_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fp4idx_status {
+  FP4IDX_OK = 0,
+  FP4IDX_ERR_NULL = 1,  /* a required pointer is NULL (num_tokens > 0)      */
+  FP4IDX_ERR_SHAPE = 2, /* num_tokens < 0, num_heads < 1, max_pos < 1,
+                           num_blocks < 1, or a size product overflows      */
+  FP4IDX_ERR_ALIGN = 3, /* a pointer or stride breaks its alignment rule    */
+  FP4IDX_ERR_ARG = 4,   /* bad rope_style, eps not finite and > 0, or a
+                           non-finite weight_scale                           */
+  FP4IDX_ERR_CUDA = 5   /* the kernel launch failed                          */
+} fp4idx_status;
+
+enum {
+  FP4IDX_ROPE_NEOX = 0,        /* pairs (i, i+32)  */
+  FP4IDX_ROPE_INTERLEAVED = 1  /* pairs (2i, 2i+1) */
+};
+
+enum {
+  FP4IDX_HEAD_DIM = 128,
+  FP4IDX_ROPE_DIM = 64,
+  FP4IDX_GROUP = 32,
+  FP4IDX_KV_BLOCK = 64,
+  FP4IDX_SLOT_PAYLOAD_BYTES = 64,
+  FP4IDX_SLOT_EXP_BYTES = 4,
+  FP4IDX_PAGE_BYTES = 64 * 68 /* 4352 */
+};
+
+/* Bits OR-ed into *err_flags by the device-side range checks. */
+#define FP4IDX_ERRFLAG_POSITION 0x1u /* a position outside [0, max_pos)     */
+#define FP4IDX_ERRFLAG_SLOT 0x2u     /* a slot >= num_blocks * 64           */
+
+/*
+ * Keys: RMSNorm -> RoPE -> two-stage FP4 -> 68-byte slot -> paged cache.
+ * Source: "dsv4.1: RoPE and FP4 packing kernels", Summary
+ * (index_k_norm_rope_pack_store fuses RMSNorm, RoPE, both quantisation
+ * stages and the paged cache store).
+ *
+ *   k            bf16, row t at k + t*k_token_stride elements, 128 elements
+ *                each.  16-byte aligned; k_token_stride a multiple of 8.
+ *   gamma        bf16 [128], 16-byte aligned.
+ *   eps          RMSNorm epsilon, finite and > 0.
+ *   positions    int64 [num_tokens]; the RoPE row of token t.
+ *   cos_cache,   fp32 [max_pos, 32] each, dense, 16-byte aligned.
+ *   sin_cache
+ *   rope_style   FP4IDX_ROPE_NEOX or FP4IDX_ROPE_INTERLEAVED.
+ *   slot_mapping int64 [num_tokens]; slot < 0 skips the token (nothing is
+ *                written); otherwise page slot/64, offset o = slot%64.
+ *                Slots must be distinct (duplicates: unspecified winner).
+ *   kv_cache     bytes [num_blocks, 4352], 16-byte aligned, updated in
+ *                place: the slot's 64-byte payload at page + o*64 and its
+ *                4-byte exponent word at page + 4096 + o*4.  Every other
+ *                byte is left untouched.
+ *   err_flags    optional device uint32 (NULL: no reporting).
+ *   stream       cudaStream_t.
+ */
+fp4idx_status fp4idx_k_norm_rope_pack_store(
+    const void* k, int64_t k_token_stride, const void* gamma, float eps,
+    const int64_t* positions, const float* cos_cache, const float* sin_cache,
+    int64_t max_pos, int rope_style, const int64_t* slot_mapping,
+    uint8_t* kv_cache, int64_t num_blocks, int64_t num_tokens,
+    uint32_t* err_flags, void* stream);
+
+/*
+ * Queries: RoPE -> two-stage FP4 -> pack, plus fp32 head weights, in one
+ * launch.  Source: "dsv4.1: RoPE and FP4 packing kernels", Summary
+ * (index_q_rope_pack_weights); "[HIP] Add FP4 output mode to
+ * indexer_qk_rope_quant_and_cache", API (q_out u8 [T, H, 64]; weights carry
+ * the plain weight).
+ *
+ *   q            bf16, row (t,h) at q + t*q_token_stride + h*q_head_stride
+ *                elements, 128 elements each.  16-byte aligned; both strides
+ *                multiples of 8.
+ *   w            bf16, w[t,h] at w + t*w_token_stride + h elements.
+ *   weight_scale finite fp32; the pages' value is H^-1/2 * D^-1/2 (D = 128).
+ *   positions, cos_cache, sin_cache, max_pos, rope_style: as for keys.
+ *   q_fp4        bytes [num_tokens, num_heads, 64], dense, 16-byte aligned.
+ *   q_scale      bytes [num_tokens, num_heads, 4], dense, 4-byte aligned
+ *                (one exponent word per row, group g in byte g).
+ *   weights_out  fp32 [num_tokens, num_heads], dense, 4-byte aligned.
+ *   err_flags    optional device uint32 (NULL: no reporting).
+ *   stream       cudaStream_t.
+ */
+fp4idx_status fp4idx_q_rope_pack_weights(
+    const void* q, int64_t q_token_stride, int64_t q_head_stride,
+    const void* w, int64_t w_token_stride, float weight_scale,
+    const int64_t* positions, const float* cos_cache, const float* sin_cache,
+    int64_t max_pos, int rope_style, uint8_t* q_fp4, uint8_t* q_scale,
+    float* weights_out, int64_t num_tokens, int64_t num_heads,
+    uint32_t* err_flags, void* stream);
+
+/*
+ * Both halves of the pre-pass in ONE launch: exactly the two calls above
+ * (same arguments, same results, same checks), with the key rows and the
+ * query tokens scheduled over one grid so that the step pays one launch and
+ * one tail.  Source: "dsv4.1: RoPE and FP4 packing kernels", Summary (the
+ * key and query ops of the indexer pre-pass).  positions, cos_cache,
+ * sin_cache, max_pos and rope_style are shared by both halves.
+ */
+fp4idx_status fp4idx_indexer_prepass(
+    /* keys */
+    const void* k, int64_t k_token_stride, const void* gamma, float eps,
+    const int64_t* slot_mapping, uint8_t* kv_cache, int64_t num_blocks,
+    /* queries */
+    const void* q, int64_t q_token_stride, int64_t q_head_stride,
+    const void* w, int64_t w_token_stride, float weight_scale,
+    uint8_t* q_fp4, uint8_t* q_scale, float* weights_out, int64_t num_heads,
+    /* shared */
+    const int64_t* positions, const float* cos_cache, const float* sin_cache,
+    int64_t max_pos, int rope_style, int64_t num_tokens, uint32_t* err_flags,
+    void* stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char* fp4idx_status_string(fp4idx_status status);
+
+/* Static version string of the library ("fp4idx <semver> sm_103a"). */
+const char* fp4idx_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FP4IDX_H */

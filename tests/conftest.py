@@ -11,6 +11,7 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built libfp4idx.so")
     config.addinivalue_line("markers", "slow: long-running CPU test")
+    config.addinivalue_line("markers", "fake_ptr: passes fake device pointers that host checks must reject")
 
 
 def pytest_collection_modifyitems(config, items):

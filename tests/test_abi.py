@@ -1,0 +1,232 @@
+"""CPU-only checks of the boundary: the C-ABI library builds and loads, exports
+every function include/fp4idx.h declares, and its host-side checks return the
+documented status codes before anything touches CUDA.  Also checks that the
+product path and the oracle never import each other."""
+import ctypes
+import os
+import re
+import shutil
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+PKG = os.path.join(ROOT, "fp4_sparse_attention_fp4idx_gb300")
+
+
+@pytest.fixture(scope="module")
+def F():
+    from fp4_sparse_attention_fp4idx_gb300 import build
+    if not os.path.exists(build.LIB):
+        build.build()
+    from fp4_sparse_attention_fp4idx_gb300 import fp4idx
+    return fp4idx
+
+
+def test_exports_every_declared_symbol(F):
+    names = F.declared_symbols()
+    assert set(names) == {"fp4idx_k_norm_rope_pack_store", "fp4idx_q_rope_pack_weights",
+                          "fp4idx_indexer_prepass", "fp4idx_status_string", "fp4idx_version"}
+    out = subprocess.run(["nm", "-D", "--defined-only", F.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (fp4idx_\w+)", out))
+    assert set(names) <= exported
+    for n in names:
+        assert hasattr(F.lib(), n)
+
+
+def test_library_is_built_for_sm103a(F):
+    out = subprocess.run(["cuobjdump", "--list-elf", F.LIB_PATH], capture_output=True,
+                         text=True)
+    if out.returncode != 0:
+        pytest.skip("cuobjdump unavailable")
+    assert "sm_103a" in out.stdout
+
+
+def test_status_strings_and_version(F):
+    texts = [F.status_string(s) for s in range(6)]
+    assert texts[0] == "ok" and len(set(texts)) == 6
+    assert F.status_string(99) == "unknown status"
+    assert F.version().startswith("fp4idx ") and "sm_103a" in F.version()
+
+
+# Fake, aligned "device pointers": only ever passed together with a defect
+# that the host checks reject, so nothing is dereferenced or launched.  As a
+# second guard these tests never run where a CUDA device is visible (there
+# the GPU suite checks the same status codes on real device memory).
+A = [0x100000 * (i + 1) for i in range(20)]
+
+
+@pytest.fixture(autouse=True)
+def _no_visible_gpu(request):
+    if "fake_ptr" in request.keywords:
+        import torch
+        if torch.cuda.is_available():
+            pytest.skip("fake-pointer host-check tests run only where no GPU is visible")
+
+
+def _k_args(**over):
+    a = dict(k=A[0], k_stride=128, gamma=A[1], eps=1e-6, pos=A[2], cos=A[3], sin=A[4],
+             max_pos=64, style=0, slots=A[5], cache=A[6], num_blocks=4, T=8, err=None,
+             stream=None)
+    a.update(over)
+    return a
+
+
+def _call_k(F, a):
+    return F.lib().fp4idx_k_norm_rope_pack_store(
+        a["k"], a["k_stride"], a["gamma"], a["eps"], a["pos"], a["cos"], a["sin"],
+        a["max_pos"], a["style"], a["slots"], a["cache"], a["num_blocks"], a["T"], a["err"],
+        a["stream"])
+
+
+def _q_args(**over):
+    a = dict(q=A[0], qts=64 * 128, qhs=128, w=A[7], wts=64, ws=0.125, pos=A[2], cos=A[3],
+             sin=A[4], max_pos=64, style=1, qf=A[8], qs=A[9], wt=A[10], T=8, H=64, err=None,
+             stream=None)
+    a.update(over)
+    return a
+
+
+def _call_q(F, a):
+    return F.lib().fp4idx_q_rope_pack_weights(
+        a["q"], a["qts"], a["qhs"], a["w"], a["wts"], a["ws"], a["pos"], a["cos"], a["sin"],
+        a["max_pos"], a["style"], a["qf"], a["qs"], a["wt"], a["T"], a["H"], a["err"],
+        a["stream"])
+
+
+def _call_fused(F, ka, qa):
+    return F.lib().fp4idx_indexer_prepass(
+        ka["k"], ka["k_stride"], ka["gamma"], ka["eps"], ka["slots"], ka["cache"],
+        ka["num_blocks"], qa["q"], qa["qts"], qa["qhs"], qa["w"], qa["wts"], qa["ws"],
+        qa["qf"], qa["qs"], qa["wt"], qa["H"], qa["pos"], qa["cos"], qa["sin"],
+        qa["max_pos"], qa["style"], qa["T"], qa["err"], qa["stream"])
+
+
+K_DEFECTS = [
+    (dict(T=-1), "ERR_SHAPE"),
+    (dict(k=None), "ERR_NULL"),
+    (dict(gamma=None), "ERR_NULL"),
+    (dict(pos=None), "ERR_NULL"),
+    (dict(cos=None), "ERR_NULL"),
+    (dict(sin=None), "ERR_NULL"),
+    (dict(slots=None), "ERR_NULL"),
+    (dict(cache=None), "ERR_NULL"),
+    (dict(max_pos=0), "ERR_SHAPE"),
+    (dict(num_blocks=0), "ERR_SHAPE"),
+    (dict(num_blocks=1 << 62), "ERR_SHAPE"),
+    (dict(style=2), "ERR_ARG"),
+    (dict(style=-1), "ERR_ARG"),
+    (dict(eps=0.0), "ERR_ARG"),
+    (dict(eps=-1e-6), "ERR_ARG"),
+    (dict(eps=float("nan")), "ERR_ARG"),
+    (dict(eps=float("inf")), "ERR_ARG"),
+    (dict(k=A[0] + 8), "ERR_ALIGN"),
+    (dict(k_stride=130), "ERR_ALIGN"),
+    (dict(gamma=A[1] + 2), "ERR_ALIGN"),
+    (dict(pos=A[2] + 4), "ERR_ALIGN"),
+    (dict(cos=A[3] + 4), "ERR_ALIGN"),
+    (dict(slots=A[5] + 4), "ERR_ALIGN"),
+    (dict(cache=A[6] + 4), "ERR_ALIGN"),
+    (dict(err=A[11] + 2), "ERR_ALIGN"),
+]
+
+Q_DEFECTS = [
+    (dict(T=-3), "ERR_SHAPE"),
+    (dict(q=None), "ERR_NULL"),
+    (dict(w=None), "ERR_NULL"),
+    (dict(qf=None), "ERR_NULL"),
+    (dict(qs=None), "ERR_NULL"),
+    (dict(wt=None), "ERR_NULL"),
+    (dict(pos=None), "ERR_NULL"),
+    (dict(H=0), "ERR_SHAPE"),
+    (dict(H=1 << 60), "ERR_SHAPE"),
+    (dict(max_pos=-5), "ERR_SHAPE"),
+    (dict(style=7), "ERR_ARG"),
+    (dict(ws=float("inf")), "ERR_ARG"),
+    (dict(ws=float("nan")), "ERR_ARG"),
+    (dict(q=A[0] + 2), "ERR_ALIGN"),
+    (dict(qts=64 * 128 + 4), "ERR_ALIGN"),
+    (dict(qhs=132), "ERR_ALIGN"),
+    (dict(w=A[7] + 1), "ERR_ALIGN"),
+    (dict(qf=A[8] + 4), "ERR_ALIGN"),
+    (dict(qs=A[9] + 2), "ERR_ALIGN"),
+    (dict(wt=A[10] + 2), "ERR_ALIGN"),
+    (dict(sin=A[4] + 8), "ERR_ALIGN"),
+]
+
+
+def _ids(defects):
+    return [f"{list(o)[0]}={list(o.values())[0]}" for o, _ in defects]
+
+
+# Arguments the fused call takes from the key side only; everything else
+# (positions, tables, max_pos, rope_style, T) comes from the query side.
+_KEY_ONLY = {"k", "k_stride", "gamma", "eps", "slots", "cache", "num_blocks", "err"}
+FUSED_K_DEFECTS = [d for d in K_DEFECTS if set(d[0]) <= _KEY_ONLY and "err" not in d[0]]
+FUSED_Q_DEFECTS = Q_DEFECTS
+
+
+@pytest.mark.fake_ptr
+@pytest.mark.parametrize("over,code", K_DEFECTS, ids=_ids(K_DEFECTS))
+def test_key_host_checks(F, over, code):
+    assert _call_k(F, _k_args(**over)) == getattr(F, code)
+
+
+@pytest.mark.fake_ptr
+@pytest.mark.parametrize("over,code", Q_DEFECTS, ids=_ids(Q_DEFECTS))
+def test_query_host_checks(F, over, code):
+    assert _call_q(F, _q_args(**over)) == getattr(F, code)
+
+
+@pytest.mark.fake_ptr
+@pytest.mark.parametrize("over,code", FUSED_K_DEFECTS, ids=_ids(FUSED_K_DEFECTS))
+def test_fused_host_checks_keys(F, over, code):
+    assert _call_fused(F, _k_args(**over), _q_args(style=0)) == getattr(F, code)
+
+
+@pytest.mark.fake_ptr
+@pytest.mark.parametrize("over,code", FUSED_Q_DEFECTS, ids=_ids(FUSED_Q_DEFECTS))
+def test_fused_host_checks_queries(F, over, code):
+    assert _call_fused(F, _k_args(), _q_args(**over)) == getattr(F, code)
+
+
+@pytest.mark.fake_ptr
+def test_zero_tokens_is_ok_without_touching_cuda(F):
+    # All pointers NULL, T == 0: returns OK before any check or CUDA call.
+    assert _call_k(F, _k_args(T=0, k=None, gamma=None, cache=None)) == F.OK
+    assert _call_q(F, _q_args(T=0, q=None, w=None)) == F.OK
+    assert _call_fused(F, _k_args(T=0), _q_args(T=0)) == F.OK
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    """No CPU fallback: importing the binding without libfp4idx.so raises."""
+    pkg = tmp_path / "fp4_sparse_attention_fp4idx_gb300"
+    shutil.copytree(PKG, pkg, ignore=shutil.ignore_patterns("*.so", "__pycache__"))
+    r = subprocess.run([sys.executable, "-c",
+                        "import fp4_sparse_attention_fp4idx_gb300.fp4idx"],
+                       cwd=tmp_path, capture_output=True, text=True)
+    assert r.returncode != 0 and "ImportError" in r.stderr and "no CPU fallback" in r.stderr
+
+
+def _py_sources(d):
+    for dp, _, fs in os.walk(d):
+        for f in fs:
+            if f.endswith((".py", ".cu", ".h", ".c")):
+                yield os.path.join(dp, f)
+
+
+def test_product_and_oracle_are_independent():
+    """The package never imports the oracle, and the oracle never imports the
+    package (they share only the seeded workload generator via the tests)."""
+    for p in _py_sources(PKG):
+        text = open(p).read()
+        assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), p
+        assert "fp4idx_oracle" not in text, p
+    for p in _py_sources(os.path.join(ROOT, "oracle")):
+        text = open(p).read()
+        assert not re.search(r"^\s*(import|from)\s+fp4_sparse_attention_fp4idx_gb300\b",
+                             text, re.M), p
+        assert not re.search(r"#\s*include\s*[<\"]fp4idx\.h", text), p

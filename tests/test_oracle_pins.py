@@ -169,6 +169,23 @@ def test_all_zero_group():
     assert not r["payload"].any() and list(r["exp"]) == [1, 1, 1, 1]
 
 
+def test_domain_boundary_top_binade():
+    """The stage-1 fake-quant dequantises to bf16: for a group amax up to
+    6*2^125 (= 1.5*2^127) every dequantised value is finite; above it the
+    scale is 2^126 and codes 6, 7 dequantise to 2^128 and 1.5*2^128, which
+    overflow.  Inputs that large are outside the finite domain."""
+    a = wl.to_bf16_bits(np.array([6.0 * 2.0 ** 125]))[0]
+    row = np.zeros(128, np.uint16)
+    row[0] = a
+    r = oracle.quant_pack_row(row)
+    assert list(r["e1"]) == [252, 1, 1, 1] and list(r["e2"]) == [252, 1, 1, 1]
+    assert r["payload"][0] == 7
+    assert np.isfinite(oracle.dequant(7, 252))
+    row[0] = a + 1  # next bf16 above 6*2^125
+    r = oracle.quant_pack_row(row)
+    assert r["e1"][0] == 253 and np.isinf(oracle.dequant(6, 253))
+
+
 def test_inverse_scale_equals_division():
     """Multiplying by the exact inverse scale 2^(127-e) equals dividing by
     2^(e-127) in fp32 for every e in [1, 254] (sglang review,
