@@ -12,32 +12,46 @@
 //   5484): API (geometry, q_out layout, plain weights), One deliberate
 //   deviation (round half to even at midpoints).
 //
-// Mapping onto the GPU.  A half-warp owns one 128-element row: lane j holds
-// elements 8j..8j+7 as one 16-byte load, so a 32-element quantisation group
-// is four adjacent lanes and the group amax is two xor-shuffles.  Each lane
-// then produces one 32-bit word of eight nibbles, so the 64-byte payload of a
-// row is one coalesced 64-byte store per half-warp (128 bytes per warp).
-// Queries are processed one token per CTA iteration (the RoPE coefficients
-// are loaded once per token and reused for all heads); each half-warp keeps
-// four 256-byte rows in flight.  Keys are one row per half-warp.
+// ---------------------------------------------------------------- design
+// The pass is HBM-bound (about 2.6 bytes moved per element and a few dozen
+// integer/fp32 operations), so the kernel is organised around two limits:
+// bytes in flight and issue slots per element.
 //
-// Bit-exactness.  Every fp32 step uses an explicit round-to-nearest
-// intrinsic (__fmul_rn, __fadd_rn, __fsqrt_rn, __frcp_rn), which the compiler
-// never fuses into FMA, and the build keeps subnormals (no FTZ).
+// Data movement: one persistent grid; every warp owns a contiguous range of
+// work items and a private ring of kStages shared-memory stages.  A work item
+// is a chunk of up to 8 rows of 128 bf16 (2 KB): 8 heads of one query token,
+// or the key rows of 8 consecutive tokens.  Lane 0 of the warp fetches items
+// kStages ahead with cp.async.bulk (the Blackwell bulk-copy engine), together
+// with the query token's cos/sin rows, and an mbarrier per stage counts the
+// bytes in.  So the bytes in flight cost no registers and no load
+// instructions, and the warp only computes.
 //
-// Quantisation shortcut (derived from the two-stage definition):
-//   * stage-1 exponent: for a bf16 amax A = 1.m * 2^(E-127) (E its biased
-//     exponent field), ceil_pow2(A/6) = 2^(E-129) if 1.m <= 1.5 and 2^(E-128)
-//     otherwise; A/6 rounded to fp32 never crosses a power of two for a bf16
-//     A, so e1 = max(E - 2 + (mantissa > 0x400000), 1) without a division.
+// Compute layout: 8 lanes own a row.  Lane j holds dims 8j..8j+7 (the RoPE
+// half) AND dims 64+8j..64+8j+7 (the pass-through half) as two 16-byte words,
+// so every lane does the same RoPE work (no idle lanes), and every lane sits
+// in two 32-element quantisation groups: group j/4 (dims 0..63) and group
+// 2+j/4 (dims 64..127).  The two group maxima travel as one packed bf16x2
+// word, so both reductions take two shuffles.  A warp works on 4 rows at a
+// time.
+//
+// Bit-exactness: fp32 steps use explicit round-to-nearest operations (scalar
+// intrinsics or packed f32x2 .rn instructions), which are never fused into
+// FMA; subnormals are kept (no FTZ anywhere).
+//
+// Quantisation in closed form (derived from the two-stage definition):
+//   * stage-1 exponent: for a bf16 amax with bits h = E<<7 | m (E biased),
+//     ceil_pow2(amax/6) is 2^(E-129) if m <= 64 (1.m <= 1.5) and 2^(E-128)
+//     otherwise; amax/6 rounded to fp32 never crosses a power of two for a
+//     bf16 amax.  So e1 = max(((h + 63) >> 7) - 2, 1), no division.
 //   * stage-1 codes: the hardware e2m1x2 conversion rounds to nearest even
-//     and saturates, i.e. exactly the grid rule; it may emit -0 codes, which
-//     are cleared at the end.
-//   * stage 2: with e1 > 1 the stage-1 top code is 5, 6 or 7.  If it is 5
-//     (3.0, i.e. A*2^(127-e1) < 3.5) stage 2 halves the scale (e2 = e1 - 1)
-//     and every code m <= 5 maps exactly to the code of 2*grid[m], which is
-//     m + min(m, 2); otherwise (and whenever e1 == 1, where the floor holds)
-//     stage 2 reproduces stage 1.  The dequantised values never change.
+//     and saturates, i.e. exactly the grid rule (it may emit -0 codes, which
+//     are cleared at the end).
+//   * stage 2: with e1 > 1 the group's largest scaled value is 1.m * 4 (m <=
+//     64, code 6 or 7) or 1.m * 2 (m > 64); it lands on code 5 (3.0) exactly
+//     when 64 < m < 96.  Then stage 2 halves the scale (e2 = e1 - 1) and each
+//     code m <= 5 becomes the code of 2*grid[m], i.e. m + min(m, 2);
+//     otherwise (and always when e1 == 1, where the floor holds) stage 2
+//     reproduces stage 1.
 
 #include <cuda_runtime.h>
 #include <math.h>
@@ -47,17 +61,119 @@
 
 namespace {
 
+// Build-time tuning knobs (rows per work item, ring depth, CTAs per SM).
+#ifndef FP4IDX_CHUNK_ROWS
+#define FP4IDX_CHUNK_ROWS 16
+#endif
+#ifndef FP4IDX_STAGES
+#define FP4IDX_STAGES 2
+#endif
+#ifndef FP4IDX_MIN_BLOCKS
+#define FP4IDX_MIN_BLOCKS 1
+#endif
+#ifndef FP4IDX_WARPS
+#define FP4IDX_WARPS 24
+#endif
+
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kThreads = 256;             // 8 warps = 16 half-warp row engines
-constexpr int kEngines = kThreads / 16;   // rows processed side by side
-constexpr int kQRowsInFlight = 4;         // rows per half-warp per batch
-constexpr int kRopeHalf = FP4IDX_ROPE_DIM / 2;  // 32 cos/sin entries per row
+constexpr int kWarps = FP4IDX_WARPS;
+constexpr int kThreads = kWarps * 32;
+constexpr int kChunkRows = FP4IDX_CHUNK_ROWS;  // rows per work item (multiple of 4)
+constexpr int kStages = FP4IDX_STAGES;
+constexpr int kRowBytes = 256;
+constexpr int kStageCos = kChunkRows * kRowBytes;  // 32 fp32 cos values (query item)
+constexpr int kStageSin = kStageCos + 128;         // 32 fp32 sin values (query item)
+constexpr int kStageHdr = kStageSin + 128;         // 4-byte header
+constexpr int kStageBytes = kStageHdr + 16;        // 16-byte multiple
+constexpr int kRingBytes = kStages * kStageBytes;
+constexpr int kSmemBytes = kWarps * kRingBytes;
+constexpr int kMinBlocksPerSm = FP4IDX_MIN_BLOCKS;
+static_assert(kChunkRows % 4 == 0 && kChunkRows <= 16, "chunk rows: multiple of 4, at most 16");
+// A key item reuses the cos/sin area for its tokens' positions and slots.
+static_assert(kChunkRows * 8 <= 128, "positions/slots of a key item must fit in 128 bytes");
+constexpr int kRopeHalf = FP4IDX_ROPE_DIM / 2;     // 32 cos/sin entries per row
 constexpr int kKvBlock = FP4IDX_KV_BLOCK;
 constexpr int kPageBytes = FP4IDX_PAGE_BYTES;
 constexpr int kPayloadBytes = FP4IDX_SLOT_PAYLOAD_BYTES;
 constexpr int kExpOffset = kKvBlock * kPayloadBytes;  // 4096
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per stage wait
 
-// ------------------------------------------------------------------ helpers
+// ------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for a stage with a time limit; false if the limit ran out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    for (int k = 0; k < 32; ++k)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// Bulk copy global -> this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void lds128(uint32_t addr, uint32_t (&w)[4]) {
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ float4 ld_f4(const float* p) {
+  return __ldg(reinterpret_cast<const float4*>(p));
+}
+
+// ---------------------------------------------------- arithmetic helpers
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
@@ -68,17 +184,42 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return d;
 }
 
-// 16-byte streaming load of data read exactly once (no L1 allocation).
-__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
-  uint4 r;
-  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-      : "l"(p));
-  return r;
+// (r0, r1) = (a0*b0, a1*b1), each rounded to nearest even.  Used only where
+// no addition consumes the products (the compiler may fuse a packed
+// multiply with a following packed add).
+__device__ __forceinline__ void mul2(float& r0, float& r1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rr;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rr, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rr;\n\t}"
+      : "=f"(r0), "=f"(r1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
-__device__ __forceinline__ float4 ld_f4(const float* p) {
-  return __ldg(reinterpret_cast<const float4*>(p));
+// Per half: max(|a|, |b|) of two bf16 (sign bit = xor of the signs, ignored).
+__device__ __forceinline__ uint32_t hmax_abs(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t umin16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("min.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t uadd16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("add.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
 }
 
 // Eight fp32 values -> eight E2M1 nibbles (element 2k in the low nibble of
@@ -93,123 +234,136 @@ __device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8]) {
       "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
       "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
       : "=r"(w)
-      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]),
-        "f"(v[6]), "f"(v[7]));
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]),
+        "f"(v[7]));
   return w;
 }
 
-// Per nibble: magnitude m (m <= 5) -> m + min(m, 2), the code of 2*grid[m];
-// sign bits unchanged.
-__device__ __forceinline__ uint32_t double_codes(uint32_t p) {
-  const uint32_t mag = p & 0x77777777u;
-  const uint32_t ge2 = ((mag >> 1) | (mag >> 2)) & 0x11111111u;  // m >= 2
-  const uint32_t add = (ge2 << 1) | (mag & 0x11111111u & ~ge2);   // min(m,2)
-  return (p & 0x88888888u) | (mag + add);
+// Stage-2 fix-up of eight stage-1 nibbles: if `halve`, every magnitude m
+// (m <= 5) becomes m + min(m, 2); then sign bits survive only on non-zero
+// magnitudes (no -0 codes).
+__device__ __forceinline__ uint32_t finish_codes(uint32_t p, bool halve) {
+  const uint32_t ge2 = ((p >> 1) | (p >> 2)) & 0x11111111u;  // magnitude >= 2
+  const uint32_t b0 = p & 0x11111111u;                        // magnitude bit 0
+  uint32_t mag = p & 0x77777777u;
+  if (halve) mag += (ge2 << 1) | (b0 & ~ge2);
+  return (p & ((ge2 | b0) << 3)) | mag;
 }
 
-// Keep a nibble's sign bit only when its magnitude is non-zero.
-__device__ __forceinline__ uint32_t clear_negative_zero(uint32_t p) {
-  const uint32_t nz = (p | (p >> 1) | (p >> 2)) & 0x11111111u;
-  return p & (0x77777777u | (nz << 3));
-}
+// Both stages for this lane's two 8-element parts: a = its slice of group
+// j/4 (dims 8j..8j+7), b = its slice of group 2+j/4 (dims 64+8j..).  All 32
+// lanes must call (shuffles).  Returns the two payload words and the row's
+// exponent word (valid in lanes 0 and 4 of each 8-lane row group).
+// The two groups' exponent arithmetic runs packed, one group per 16 bits.
+__device__ __forceinline__ void quant_lane(const uint32_t (&a)[4], const uint32_t (&b)[4], int j,
+                                           uint32_t& pa, uint32_t& pb, uint32_t& ew) {
+  const uint32_t ma = hmax_abs(hmax_abs(a[0], a[1]), hmax_abs(a[2], a[3]));
+  const uint32_t mb = hmax_abs(hmax_abs(b[0], b[1]), hmax_abs(b[2], b[3]));
+  uint32_t m = hmax_abs(prmt(ma, mb, 0x5410u), prmt(ma, mb, 0x7632u));
+  m = hmax_abs(m, __shfl_xor_sync(kFull, m, 1));
+  m = hmax_abs(m, __shfl_xor_sync(kFull, m, 2));
+  m &= 0x7fff7fffu;  // bf16 amax bits h of (group a, group b)
 
-// Both quantisation stages for this lane's 8 elements (bf16-exact fp32
-// values z).  Must be called by all 32 lanes (group amax uses shuffles).
-// Returns the lane's payload word; *e2 receives the group's exponent.
-__device__ __forceinline__ uint32_t quant_pack_lane(const uint32_t (&w)[4], uint32_t* e2) {
-  float z[8];
+  // Per half: E' = (h + 63) >> 7 is e1 + 2 before the floor, so
+  // 254 - e1 = min(256 - E', 253); it is the biased exponent of 2^(127-e1).
+  const uint32_t ep = ((m + 0x003f003fu) >> 7) & 0x01ff01ffu;
+  const uint32_t ie = umin16x2(0x01000100u - ep, 0x00fd00fdu);
+  const float ia = __uint_as_float(ie << 23);
+  const float ib = __uint_as_float((ie >> 16) << 23);
+  // Stage 2 halves the scale when e1 > 1 (254 - e1 < 253) and the amax
+  // mantissa lies in (64, 96), i.e. the top stage-1 code is 5.
+  const uint32_t mq = uadd16x2(m & 0x007f007fu, 0xffbfffbfu);  // mantissa - 65
+  const bool ha2 = (mq & 0xffffu) < 31u && (ie & 0xffffu) < 253u;
+  const bool hb2 = (mq >> 16) < 31u && (ie >> 16) < 253u;
+
+  float va[8], vb[8];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    z[2 * k] = bf16_lo(w[k]);
-    z[2 * k + 1] = bf16_hi(w[k]);
+    mul2(va[2 * k], va[2 * k + 1], bf16_lo(a[k]), bf16_hi(a[k]), ia, ia);
+    mul2(vb[2 * k], vb[2 * k + 1], bf16_lo(b[k]), bf16_hi(b[k]), ib, ib);
   }
-  float a = fabsf(z[0]);
-#pragma unroll
-  for (int i = 1; i < 8; ++i) a = fmaxf(a, fabsf(z[i]));
-  a = fmaxf(a, __shfl_xor_sync(kFull, a, 1));
-  a = fmaxf(a, __shfl_xor_sync(kFull, a, 2));
-
-  const uint32_t ab = __float_as_uint(a);
-  int e1 = (int)(ab >> 23) - 2 + ((ab & 0x7fffffu) > 0x400000u ? 1 : 0);
-  e1 = e1 < 1 ? 1 : e1;
-  const float inv1 = __uint_as_float((uint32_t)(254 - e1) << 23);  // 2^(127-e1)
-
-  float v[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(z[i], inv1);
-  uint32_t p = e2m1x8(v);
-
-  const bool halve = (e1 > 1) && (__fmul_rn(a, inv1) < 3.5f);
-  if (halve) p = double_codes(p);
-  *e2 = (uint32_t)(e1 - (halve ? 1 : 0));
-  return clear_negative_zero(p);
+  pa = finish_codes(e2m1x8(va), ha2);
+  pb = finish_codes(e2m1x8(vb), hb2);
+  // e2 = e1 - halve, one group per 16 bits (each fits in a byte).
+  const uint32_t e2 = 0x00fe00feu - ie - (ha2 ? 1u : 0u) - (hb2 ? 0x10000u : 0u);
+  const uint32_t x = e2 << (8 * (j >> 2));
+  ew = x | __shfl_xor_sync(kFull, x, 4);
 }
 
-// Exponent word of the row: byte g = exponent of group g (lanes 4g..4g+3).
-__device__ __forceinline__ uint32_t exponent_word(uint32_t e, int j) {
-  uint32_t x = e << (8 * (j >> 2));
-  x |= __shfl_xor_sync(kFull, x, 4);
-  x |= __shfl_xor_sync(kFull, x, 8);
-  return x;
-}
-
-// RoPE coefficients of this lane for one position.  NeoX: lanes 0..7 hold
-// cos/sin[8(j&3) .. +7]; lanes 0..3 own the first element of each pair and
-// take -sin so both halves compute own*c + partner*s.  Interleaved: lanes
-// 0..7 hold cos/sin[4j .. 4j+3].  Lanes 8..15 hold nothing.
+// RoPE coefficients of lane j for one position, as fp32 pairs.
+//   NeoX: lane j owns dims 8j..8j+7, pair index i = 8(j&3)+k; lanes 0..3
+//   hold the first member of each pair and use -sin, so every lane computes
+//   own*cos + partner*sin'.
+//   Interleaved: word k of lane j is the pair i = 4j+k; c = (cos_i, cos_i),
+//   s = (-sin_i, sin_i) so that (a, b)*c + (b, a)*s = (a', b').
 template <int kStyle>
 struct RopeCoef {
   float c[8];
   float s[8];
-  __device__ __forceinline__ void load(const float* cos_row, const float* sin_row, int j) {
-    if (j >= 8) return;
+  __device__ __forceinline__ void set(const float4& c0, const float4& c1, const float4& s0,
+                                      const float4& s1, int j) {
     if (kStyle == FP4IDX_ROPE_NEOX) {
-      const int b = 8 * (j & 3);
-      const float4 c0 = ld_f4(cos_row + b), c1 = ld_f4(cos_row + b + 4);
-      const float4 s0 = ld_f4(sin_row + b), s1 = ld_f4(sin_row + b + 4);
+      const float sg = j < 4 ? -1.0f : 1.0f;
       c[0] = c0.x; c[1] = c0.y; c[2] = c0.z; c[3] = c0.w;
       c[4] = c1.x; c[5] = c1.y; c[6] = c1.z; c[7] = c1.w;
-      s[0] = s0.x; s[1] = s0.y; s[2] = s0.z; s[3] = s0.w;
-      s[4] = s1.x; s[5] = s1.y; s[6] = s1.z; s[7] = s1.w;
-      if (j < 4) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) s[i] = -s[i];
-      }
+      s[0] = sg * s0.x; s[1] = sg * s0.y; s[2] = sg * s0.z; s[3] = sg * s0.w;
+      s[4] = sg * s1.x; s[5] = sg * s1.y; s[6] = sg * s1.z; s[7] = sg * s1.w;
     } else {
-      const float4 c0 = ld_f4(cos_row + 4 * j), s0 = ld_f4(sin_row + 4 * j);
-      c[0] = c0.x; c[1] = c0.y; c[2] = c0.z; c[3] = c0.w;
-      s[0] = s0.x; s[1] = s0.y; s[2] = s0.z; s[3] = s0.w;
+      c[0] = c0.x; c[1] = c0.x; c[2] = c0.y; c[3] = c0.y;
+      c[4] = c0.z; c[5] = c0.z; c[6] = c0.w; c[7] = c0.w;
+      s[0] = -s0.x; s[1] = s0.x; s[2] = -s0.y; s[3] = s0.y;
+      s[4] = -s0.z; s[5] = s0.z; s[6] = -s0.w; s[7] = s0.w;
+    }
+  }
+  // From a cos/sin row pair in shared memory.
+  __device__ __forceinline__ void load_smem(uint32_t cos_row, uint32_t sin_row, int j) {
+    if (kStyle == FP4IDX_ROPE_NEOX) {
+      const uint32_t off = 32u * (uint32_t)(j & 3);
+      set(lds_f4(cos_row + off), lds_f4(cos_row + off + 16), lds_f4(sin_row + off),
+          lds_f4(sin_row + off + 16), j);
+    } else {
+      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      set(lds_f4(cos_row + 16u * j), z, lds_f4(sin_row + 16u * j), z, j);
+    }
+  }
+  // From the global cos/sin tables.
+  __device__ __forceinline__ void load_global(const float* cos_row, const float* sin_row, int j) {
+    if (kStyle == FP4IDX_ROPE_NEOX) {
+      const int off = 8 * (j & 3);
+      set(ld_f4(cos_row + off), ld_f4(cos_row + off + 4), ld_f4(sin_row + off),
+          ld_f4(sin_row + off + 4), j);
+    } else {
+      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      set(ld_f4(cos_row + 4 * j), z, ld_f4(sin_row + 4 * j), z, j);
     }
   }
 };
 
-// In-place RoPE of this lane's words.  Must be called by all 32 lanes (the
-// NeoX partner exchange is a shuffle); only lanes j < 8 change their data.
+// In-place RoPE of the lane's RoPE-half word group `a`.  All 32 lanes must
+// call (the NeoX partner exchange is a shuffle).  Scalar round-to-nearest
+// intrinsics on purpose: a packed f32x2 multiply followed by a packed add
+// may be contracted into a fused multiply-add, which rounds differently.
 template <int kStyle>
-__device__ __forceinline__ void rope_lane(uint32_t (&w)[4], const RopeCoef<kStyle>& rc, int j) {
+__device__ __forceinline__ void rope_lane(uint32_t (&a)[4], const RopeCoef<kStyle>& rc) {
   if (kStyle == FP4IDX_ROPE_NEOX) {
     uint32_t p[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) p[k] = __shfl_xor_sync(kFull, w[k], 4);
-    if (j < 8) {
+    for (int k = 0; k < 4; ++k) p[k] = __shfl_xor_sync(kFull, a[k], 4);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float r0 = __fadd_rn(__fmul_rn(bf16_lo(w[k]), rc.c[2 * k]),
-                                   __fmul_rn(bf16_lo(p[k]), rc.s[2 * k]));
-        const float r1 = __fadd_rn(__fmul_rn(bf16_hi(w[k]), rc.c[2 * k + 1]),
-                                   __fmul_rn(bf16_hi(p[k]), rc.s[2 * k + 1]));
-        w[k] = pack_bf16x2(r0, r1);
-      }
+    for (int k = 0; k < 4; ++k) {
+      const float r0 = __fadd_rn(__fmul_rn(bf16_lo(a[k]), rc.c[2 * k]),
+                                 __fmul_rn(bf16_lo(p[k]), rc.s[2 * k]));
+      const float r1 = __fadd_rn(__fmul_rn(bf16_hi(a[k]), rc.c[2 * k + 1]),
+                                 __fmul_rn(bf16_hi(p[k]), rc.s[2 * k + 1]));
+      a[k] = pack_bf16x2(r0, r1);
     }
   } else {
-    if (j < 8) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float x0 = bf16_lo(w[k]), x1 = bf16_hi(w[k]);
-        const float r0 = __fsub_rn(__fmul_rn(x0, rc.c[k]), __fmul_rn(x1, rc.s[k]));
-        const float r1 = __fadd_rn(__fmul_rn(x1, rc.c[k]), __fmul_rn(x0, rc.s[k]));
-        w[k] = pack_bf16x2(r0, r1);
-      }
+    for (int k = 0; k < 4; ++k) {
+      const float x0 = bf16_lo(a[k]), x1 = bf16_hi(a[k]);
+      const float r0 = __fadd_rn(__fmul_rn(x0, rc.c[2 * k]), __fmul_rn(x1, rc.s[2 * k]));
+      const float r1 = __fadd_rn(__fmul_rn(x1, rc.c[2 * k + 1]), __fmul_rn(x0, rc.s[2 * k + 1]));
+      a[k] = pack_bf16x2(r0, r1);
     }
   }
 }
@@ -227,6 +381,8 @@ struct KArgs {
   const int64_t* slots;
   uint8_t* cache;
   int64_t num_blocks;
+  int meta_bulk;  // positions and slots 16-byte aligned: a full key item's
+                  // positions/slots travel with its rows in the bulk copy
 };
 
 struct QArgs {
@@ -251,151 +407,330 @@ struct Shared {
   uint32_t* err;
 };
 
-// ------------------------------------------------------------- key rows
-// 16 consecutive key rows [row0, row0 + 16), one per half-warp engine.
-template <int kStyle>
-__device__ __forceinline__ void key_rows(const KArgs& ka, const Shared& sh, int64_t row0,
-                                         const float (&g)[8]) {
-  const int j = threadIdx.x & 15;
-  const int64_t t = row0 + (threadIdx.x >> 4);
-  bool live = t < sh.T;
-  int64_t slot = -1, pos = 0;
-  if (live) {
-    slot = __ldg(ka.slots + t);
-    live = slot >= 0;
-  }
-  uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-  if (live) {
-    pos = __ldg(sh.pos + t);
-    raw = ld_stream_v4(ka.k + t * ka.k_stride + 8 * j);
-    const bool pos_ok = pos >= 0 && pos < sh.max_pos;
-    const bool slot_ok = slot < ka.num_blocks * kKvBlock;
-    if (!(pos_ok && slot_ok)) {
-      if (j == 0) flag_error(sh.err, (pos_ok ? 0u : FP4IDX_ERRFLAG_POSITION) |
-                                         (slot_ok ? 0u : FP4IDX_ERRFLAG_SLOT));
-      live = false;
-      pos = 0;
+// Work items, in groups of kChunkRows tokens: each group contributes one
+// key chunk (its key rows, if keys are processed) followed by its query
+// chunks (token t, heads h0 .. h0+kChunkRows-1, ceil(H/kChunkRows) chunks per token, if queries
+// are processed).  Interleaving the two kinds gives every warp's contiguous
+// range the same mix of work.
+struct Work {
+  int64_t per_group;  // items of a full group
+  int64_t total;      // all items
+  int64_t cpt;        // query chunks per token = ceil(H / kChunkRows)
+  int has_k;          // 1 if key chunks are processed
+  int has_q;          // 1 if query chunks are processed
+};
+
+struct ItemIter {
+  int64_t t;     // key: first token of the chunk; query: the token
+  int64_t h0;    // query: first head of the chunk
+  int is_key;
+  __device__ __forceinline__ void seek(int64_t item, const Work& wk) {
+    const int64_t o = item / wk.per_group;
+    const int64_t sub = item - o * wk.per_group;
+    if (wk.has_k && sub == 0) {
+      is_key = 1;
+      t = o * kChunkRows;
+      h0 = 0;
+    } else {
+      const int64_t q = sub - wk.has_k;
+      is_key = 0;
+      t = o * kChunkRows + q / wk.cpt;
+      h0 = (q % wk.cpt) * kChunkRows;
     }
   }
-  RopeCoef<kStyle> rc{};
-  if (live) rc.load(sh.cos + pos * kRopeHalf, sh.sin + pos * kRopeHalf, j);
-
-  // RMSNorm: 8 sequential squares per lane, then the xor butterfly 8,4,2,1.
-  uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-  float x[8];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    x[2 * k] = bf16_lo(w[k]);
-    x[2 * k + 1] = bf16_hi(w[k]);
-  }
-  float ss = __fmul_rn(x[0], x[0]);
-#pragma unroll
-  for (int i = 1; i < 8; ++i) ss = __fadd_rn(ss, __fmul_rn(x[i], x[i]));
-  ss = __fadd_rn(ss, __shfl_xor_sync(kFull, ss, 8));
-  ss = __fadd_rn(ss, __shfl_xor_sync(kFull, ss, 4));
-  ss = __fadd_rn(ss, __shfl_xor_sync(kFull, ss, 2));
-  ss = __fadd_rn(ss, __shfl_xor_sync(kFull, ss, 1));
-  const float ms = __fmul_rn(ss, 0.0078125f);  // /128, exact scaling
-  const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, ka.eps)));
-#pragma unroll
-  for (int k = 0; k < 4; ++k)
-    w[k] = pack_bf16x2(__fmul_rn(__fmul_rn(x[2 * k], r), g[2 * k]),
-                       __fmul_rn(__fmul_rn(x[2 * k + 1], r), g[2 * k + 1]));
-
-  rope_lane<kStyle>(w, rc, j);
-  uint32_t e2;
-  const uint32_t payload = quant_pack_lane(w, &e2);
-  const uint32_t ex = exponent_word(e2, j);
-  if (live) {
-    uint8_t* page = ka.cache + (slot / kKvBlock) * (int64_t)kPageBytes;
-    const int64_t o = slot % kKvBlock;
-    *reinterpret_cast<uint32_t*>(page + o * kPayloadBytes + 4 * j) = payload;
-    if (j == 0) *reinterpret_cast<uint32_t*>(page + kExpOffset + 4 * o) = ex;
-  }
-}
-
-template <int kStyle>
-__device__ __forceinline__ void load_gamma(const KArgs& ka, float (&g)[8]) {
-  const int j = threadIdx.x & 15;
-  const uint4 gr = __ldg(reinterpret_cast<const uint4*>(ka.gamma) + j);
-  const uint32_t gw[4] = {gr.x, gr.y, gr.z, gr.w};
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    g[2 * k] = bf16_lo(gw[k]);
-    g[2 * k + 1] = bf16_hi(gw[k]);
-  }
-}
-
-// ----------------------------------------------------------- query tokens
-template <int kStyle>
-__device__ __forceinline__ void query_token(const QArgs& qa, const Shared& sh, int64_t t) {
-  const int j = threadIdx.x & 15;
-  const int engine = threadIdx.x >> 4;
-  const int64_t pos = __ldg(sh.pos + t);
-  if (pos < 0 || pos >= sh.max_pos) {  // uniform over the CTA
-    if (threadIdx.x == 0) flag_error(sh.err, FP4IDX_ERRFLAG_POSITION);
-    return;
-  }
-  for (int64_t h = threadIdx.x; h < qa.H; h += blockDim.x) {
-    const uint16_t wb = __ldg(qa.w + t * qa.w_tstride + h);
-    qa.weights[t * qa.H + h] = __fmul_rn(__uint_as_float((uint32_t)wb << 16), qa.wscale);
-  }
-  RopeCoef<kStyle> rc;
-  rc.load(sh.cos + pos * kRopeHalf, sh.sin + pos * kRopeHalf, j);
-
-  const uint16_t* qt = qa.q + t * qa.q_tstride + 8 * j;
-  for (int64_t base = 0; base < qa.H; base += kEngines * kQRowsInFlight) {
-    uint4 raw[kQRowsInFlight];
-#pragma unroll
-    for (int i = 0; i < kQRowsInFlight; ++i) {
-      const int64_t h = base + engine + kEngines * i;
-      raw[i] = h < qa.H ? ld_stream_v4(qt + h * qa.q_hstride) : make_uint4(0u, 0u, 0u, 0u);
+  __device__ __forceinline__ void next(const Work& wk, int64_t H) {
+    if (is_key) {
+      if (wk.has_q) {
+        is_key = 0;
+        h0 = 0;
+      } else {
+        t += kChunkRows;
+      }
+      return;
     }
-#pragma unroll
-    for (int i = 0; i < kQRowsInFlight; ++i) {
-      const int64_t h = base + engine + kEngines * i;
-      uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-      rope_lane<kStyle>(w, rc, j);
-      uint32_t e2;
-      const uint32_t payload = quant_pack_lane(w, &e2);
-      const uint32_t ex = exponent_word(e2, j);
-      if (h < qa.H) {
-        const int64_t row = t * qa.H + h;
-        *reinterpret_cast<uint32_t*>(qa.q_fp4 + row * kPayloadBytes + 4 * j) = payload;
-        if (j == 0) *reinterpret_cast<uint32_t*>(qa.q_scale + row * 4) = ex;
+    h0 += kChunkRows;
+    if (h0 >= H) {
+      h0 = 0;
+      ++t;
+      if (wk.has_k && (t % kChunkRows) == 0) is_key = 1;
+    }
+  }
+};
+
+// --------------------------------------------------------- producer side
+// The producer's position lookups: the position of the token after the
+// current one is loaded one token ahead, so issuing never waits for it.
+struct PosCache {
+  int64_t t, v;    // token and its position
+  int64_t nt, nv;  // next token and its position (load in flight)
+  __device__ __forceinline__ void reset() {
+    t = -1;
+    nt = -1;
+    v = 0;
+    nv = 0;
+  }
+  __device__ __forceinline__ int64_t get(int64_t tok, const Shared& sh) {
+    if (tok != t) {
+      v = tok == nt ? nv : __ldg(sh.pos + tok);
+      t = tok;
+      if (tok + 1 < sh.T) {
+        nt = tok + 1;
+        nv = __ldg(sh.pos + tok + 1);
       }
     }
+    return v;
+  }
+};
+
+// Issues the copies of one item into a stage (lane 0 only).
+__device__ __forceinline__ void issue_item(const ItemIter& it, const Work& wk, const KArgs& ka,
+                                           const QArgs& qa, const Shared& sh, uint32_t stage,
+                                           uint32_t bar, PosCache& pc) {
+  if (it.is_key) {
+    const int64_t n = sh.T - it.t < kChunkRows ? sh.T - it.t : kChunkRows;
+    const bool meta = ka.meta_bulk && n == kChunkRows;
+    mbar_arrive_expect_tx(bar, (uint32_t)n * kRowBytes + (meta ? 2u * kChunkRows * 8u : 0u));
+    const uint16_t* src = ka.k + it.t * ka.k_stride;
+    if (ka.k_stride == FP4IDX_HEAD_DIM) {
+      bulk_g2s(stage, src, (uint32_t)n * kRowBytes, bar);
+    } else {
+      for (int64_t r = 0; r < n; ++r)
+        bulk_g2s(stage + (uint32_t)r * kRowBytes, src + r * ka.k_stride, kRowBytes, bar);
+    }
+    if (meta) {
+      bulk_g2s(stage + kStageCos, sh.pos + it.t, kChunkRows * 8u, bar);
+      bulk_g2s(stage + kStageSin, ka.slots + it.t, kChunkRows * 8u, bar);
+    }
+    return;
+  }
+  const int64_t n = qa.H - it.h0 < kChunkRows ? qa.H - it.h0 : kChunkRows;
+  const int64_t pos_v = pc.get(it.t, sh);
+  const bool ok = pos_v >= 0 && pos_v < sh.max_pos;
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(stage + kStageHdr), "r"(ok ? 1u : 0u) : "memory");
+  mbar_arrive_expect_tx(bar, (uint32_t)n * kRowBytes + (ok ? 256u : 0u));
+  const uint16_t* src = qa.q + it.t * qa.q_tstride + it.h0 * qa.q_hstride;
+  if (qa.q_hstride == FP4IDX_HEAD_DIM) {
+    bulk_g2s(stage, src, (uint32_t)n * kRowBytes, bar);
+  } else {
+    for (int64_t r = 0; r < n; ++r)
+      bulk_g2s(stage + (uint32_t)r * kRowBytes, src + r * qa.q_hstride, kRowBytes, bar);
+  }
+  if (ok) {
+    bulk_g2s(stage + kStageCos, sh.cos + pos_v * kRopeHalf, 128u, bar);
+    bulk_g2s(stage + kStageSin, sh.sin + pos_v * kRopeHalf, 128u, bar);
   }
 }
 
-// ------------------------------------------------------------------ kernels
-template <int kStyle>
-__global__ void __launch_bounds__(kThreads) k_kernel(KArgs ka, Shared sh) {
-  float g[8];
-  load_gamma<kStyle>(ka, g);
-  for (int64_t row0 = (int64_t)blockIdx.x * kEngines; row0 < sh.T;
-       row0 += (int64_t)gridDim.x * kEngines)
-    key_rows<kStyle>(ka, sh, row0, g);
+// --------------------------------------------------------- consumer side
+__device__ __forceinline__ int64_t lds_s64(uint32_t addr) {
+  int64_t v;
+  asm volatile("ld.shared.s64 %0, [%1];" : "=l"(v) : "r"(addr));
+  return v;
 }
 
+// A query item: up to kChunkRows heads of token it.t, rows in the stage.
 template <int kStyle>
-__global__ void __launch_bounds__(kThreads) q_kernel(QArgs qa, Shared sh) {
-  for (int64_t t = blockIdx.x; t < sh.T; t += gridDim.x) query_token<kStyle>(qa, sh, t);
+__device__ __forceinline__ void query_chunk(const ItemIter& it, const QArgs& qa, const Shared& sh,
+                                            uint32_t stage) {
+  const int lane = threadIdx.x & 31, j = lane & 7, rg = lane >> 3;
+  const int n = (int)(qa.H - it.h0 < kChunkRows ? qa.H - it.h0 : kChunkRows);
+  uint32_t ok;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(ok) : "r"(stage + kStageHdr));
+  if (!ok) {
+    if (lane == 0) flag_error(sh.err, FP4IDX_ERRFLAG_POSITION);
+    return;  // the whole token is skipped; uniform over the warp
+  }
+  const int64_t row0 = it.t * qa.H + it.h0;
+  uint16_t wb = 0;
+  if (lane < n) wb = __ldg(qa.w + it.t * qa.w_tstride + it.h0 + lane);
+
+  RopeCoef<kStyle> rc;
+  rc.load_smem(stage + kStageCos, stage + kStageSin, j);
+  uint8_t* const out = qa.q_fp4 + row0 * kPayloadBytes + 4 * j;
+  uint8_t* const scl = qa.q_scale + row0 * 4;
+#pragma unroll 1
+  for (int r0 = 0; r0 < n; r0 += 4) {  // uniform over the warp
+    const int r = r0 + rg;
+    uint32_t a[4], b[4];
+    const uint32_t rowaddr = stage + (uint32_t)r * kRowBytes + 16u * j;
+    lds128(rowaddr, a);
+    lds128(rowaddr + 128u, b);
+    rope_lane<kStyle>(a, rc);
+    uint32_t pa, pb, ew;
+    quant_lane(a, b, j, pa, pb, ew);
+    if (r < n) {
+      *reinterpret_cast<uint32_t*>(out + r * kPayloadBytes) = pa;
+      *reinterpret_cast<uint32_t*>(out + r * kPayloadBytes + 32) = pb;
+      if (j == 0) *reinterpret_cast<uint32_t*>(scl + 4 * r) = ew;
+    }
+  }
+  if (lane < n)
+    qa.weights[row0 + lane] = __fmul_rn(__uint_as_float((uint32_t)wb << 16), qa.wscale);
 }
 
-// One grid over both halves: work items [0, nk) are groups of 16 key rows,
-// items [nk, nk + T) are query tokens.
+// Slot and position of one key row (r < n), validated; live = false for a
+// skipped or out-of-range row (then pos = 0, a safe table row).
+struct KeyMeta {
+  int64_t slot, pos;
+  bool live;
+};
+
+__device__ __forceinline__ KeyMeta key_meta(const ItemIter& it, const KArgs& ka, const Shared& sh,
+                                            uint32_t stage, int r, int n, bool meta, int j) {
+  KeyMeta m{-1, 0, false};
+  if (r < n) {
+    if (meta) {
+      m.pos = lds_s64(stage + kStageCos + 8u * r);
+      m.slot = lds_s64(stage + kStageSin + 8u * r);
+    } else {
+      m.pos = __ldg(sh.pos + it.t + r);
+      m.slot = __ldg(ka.slots + it.t + r);
+    }
+    m.live = m.slot >= 0;
+  }
+  if (m.live) {
+    const bool pos_ok = m.pos >= 0 && m.pos < sh.max_pos;
+    const bool slot_ok = m.slot < ka.num_blocks * kKvBlock;
+    if (!(pos_ok && slot_ok)) {
+      if (j == 0)
+        flag_error(sh.err, (pos_ok ? 0u : FP4IDX_ERRFLAG_POSITION) |
+                               (slot_ok ? 0u : FP4IDX_ERRFLAG_SLOT));
+      m.live = false;
+    }
+  }
+  if (!m.live) m.pos = 0;
+  return m;
+}
+
+// A key item: tokens it.t .. it.t + kChunkRows - 1, rows in the stage.
 template <int kStyle>
-__global__ void __launch_bounds__(kThreads) prepass_kernel(KArgs ka, QArgs qa, Shared sh) {
-  float g[8];
-  load_gamma<kStyle>(ka, g);
-  const int64_t nk = (sh.T + kEngines - 1) / kEngines;
-  const int64_t total = nk + sh.T;
-  for (int64_t item = blockIdx.x; item < total; item += gridDim.x) {
-    if (item < nk)
-      key_rows<kStyle>(ka, sh, item * kEngines, g);
+__device__ __forceinline__ void key_chunk(const ItemIter& it, const KArgs& ka, const Shared& sh,
+                                          uint32_t stage) {
+  const int lane = threadIdx.x & 31, j = lane & 7, rg = lane >> 3;
+  const int n = (int)(sh.T - it.t < kChunkRows ? sh.T - it.t : kChunkRows);
+  const bool meta = ka.meta_bulk && n == kChunkRows;  // uniform
+#pragma unroll 1
+  for (int r0 = 0; r0 < n; r0 += 4) {  // uniform over the warp
+    const int r = r0 + rg;
+    const KeyMeta km = key_meta(it, ka, sh, stage, r, n, meta, j);
+    RopeCoef<kStyle> rc;
+    rc.load_global(sh.cos + km.pos * kRopeHalf, sh.sin + km.pos * kRopeHalf, j);
+
+    uint32_t a[4], b[4];
+    const uint32_t rowaddr = stage + (uint32_t)r * kRowBytes + 16u * j;
+    lds128(rowaddr, a);
+    lds128(rowaddr + 128u, b);
+    // RMSNorm.  Lane j holds the 8-element runs j and 8+j of the fixed
+    // summation order; the butterfly's distance-8 step is the local add.
+    float sa = __fmul_rn(bf16_lo(a[0]), bf16_lo(a[0]));
+    float sb = __fmul_rn(bf16_lo(b[0]), bf16_lo(b[0]));
+    sa = __fadd_rn(sa, __fmul_rn(bf16_hi(a[0]), bf16_hi(a[0])));
+    sb = __fadd_rn(sb, __fmul_rn(bf16_hi(b[0]), bf16_hi(b[0])));
+#pragma unroll
+    for (int k = 1; k < 4; ++k) {
+      sa = __fadd_rn(sa, __fmul_rn(bf16_lo(a[k]), bf16_lo(a[k])));
+      sa = __fadd_rn(sa, __fmul_rn(bf16_hi(a[k]), bf16_hi(a[k])));
+      sb = __fadd_rn(sb, __fmul_rn(bf16_lo(b[k]), bf16_lo(b[k])));
+      sb = __fadd_rn(sb, __fmul_rn(bf16_hi(b[k]), bf16_hi(b[k])));
+    }
+    float ss = __fadd_rn(sa, sb);                       // distance 8
+    ss = __fadd_rn(ss, __shfl_xor_sync(kFull, ss, 4));  // distance 4
+    ss = __fadd_rn(ss, __shfl_xor_sync(kFull, ss, 2));  // distance 2
+    ss = __fadd_rn(ss, __shfl_xor_sync(kFull, ss, 1));  // distance 1
+    const float ms = __fmul_rn(ss, 0.0078125f);         // /128, exact scaling
+    const float rr = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, ka.eps)));
+    const uint4 ga = __ldg(reinterpret_cast<const uint4*>(ka.gamma) + j);
+    const uint4 gb = __ldg(reinterpret_cast<const uint4*>(ka.gamma) + 8 + j);
+    const uint32_t gwa[4] = {ga.x, ga.y, ga.z, ga.w}, gwb[4] = {gb.x, gb.y, gb.z, gb.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float u0, u1, y0, y1;
+      mul2(u0, u1, bf16_lo(a[k]), bf16_hi(a[k]), rr, rr);
+      mul2(y0, y1, u0, u1, bf16_lo(gwa[k]), bf16_hi(gwa[k]));
+      a[k] = pack_bf16x2(y0, y1);
+      mul2(u0, u1, bf16_lo(b[k]), bf16_hi(b[k]), rr, rr);
+      mul2(y0, y1, u0, u1, bf16_lo(gwb[k]), bf16_hi(gwb[k]));
+      b[k] = pack_bf16x2(y0, y1);
+    }
+    rope_lane<kStyle>(a, rc);
+    uint32_t pa, pb, ew;
+    quant_lane(a, b, j, pa, pb, ew);
+    if (km.live) {
+      uint8_t* page = ka.cache + (km.slot / kKvBlock) * (int64_t)kPageBytes;
+      const int64_t o = km.slot % kKvBlock;
+      uint8_t* dst = page + o * kPayloadBytes + 4 * j;
+      *reinterpret_cast<uint32_t*>(dst) = pa;
+      *reinterpret_cast<uint32_t*>(dst + 32) = pb;
+      if (j == 0) *reinterpret_cast<uint32_t*>(page + kExpOffset + 4 * o) = ew;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+template <int kStyle>
+__global__ void __launch_bounds__(kThreads, kMinBlocksPerSm)
+    prepass_kernel(KArgs ka, QArgs qa, Shared sh, Work wk) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bars[kWarps * kStages];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t ring = smem_addr(smem) + (uint32_t)warp * kRingBytes;
+  const uint32_t bar0 = smem_addr(&bars[warp * kStages]);
+  if (lane == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8u * s, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  const int64_t G = (int64_t)gridDim.x * kWarps;
+  const int64_t g = (int64_t)blockIdx.x * kWarps + warp;
+  const int64_t lo = g * wk.total / G, hi = (g + 1) * wk.total / G;
+  if (lo >= hi) return;
+
+  ItemIter cons, prod;
+  cons.seek(lo, wk);
+  prod = cons;
+  PosCache pc;  // producer's position lookups (lane 0)
+  pc.reset();
+  const int64_t first = hi - lo < kStages ? hi - lo : kStages;
+  for (int s = 0; s < first; ++s) {
+    if (lane == 0) issue_item(prod, wk, ka, qa, sh, ring + s * kStageBytes, bar0 + 8u * s, pc);
+    prod.next(wk, qa.H);
+  }
+
+  int s = 0;
+  uint32_t phase = 0;
+  for (int64_t i = lo; i < hi; ++i) {
+    const uint32_t stage = ring + (uint32_t)s * kStageBytes;
+    const uint32_t bar = bar0 + 8u * s;
+    if (!mbar_wait_bounded(bar, phase)) {
+      // Give up: report, then wait (bounded) for this warp's other copies so
+      // none is still writing shared memory when the CTA exits.
+      if (lane == 0) flag_error(sh.err, FP4IDX_ERRFLAG_TIMEOUT);
+      int s2 = s;
+      uint32_t p2 = phase;
+      for (int64_t k = 0; k < kStages && i + k < hi; ++k) {
+        mbar_wait_bounded(bar0 + 8u * s2, p2);
+        if (++s2 == kStages) {
+          s2 = 0;
+          p2 ^= 1u;
+        }
+      }
+      return;
+    }
+    if (cons.is_key)
+      key_chunk<kStyle>(cons, ka, sh, stage);
     else
-      query_token<kStyle>(qa, sh, item - nk);
+      query_chunk<kStyle>(cons, qa, sh, stage);
+    __syncwarp();
+    if (i + kStages < hi) {
+      if (lane == 0) issue_item(prod, wk, ka, qa, sh, stage, bar, pc);
+      prod.next(wk, qa.H);
+    }
+    cons.next(wk, qa.H);
+    if (++s == kStages) {
+      s = 0;
+      phase ^= 1u;
+    }
   }
 }
 
@@ -403,21 +738,25 @@ __global__ void __launch_bounds__(kThreads) prepass_kernel(KArgs ka, QArgs qa, S
 constexpr int kMaxDevices = 64;
 struct DeviceInfo {
   int sm_count = 0;
-  int occupancy[3][2] = {{0, 0}, {0, 0}, {0, 0}};  // [kernel][style]
+  int blocks_per_sm[2] = {0, 0};  // [style]
 };
 DeviceInfo g_devices[kMaxDevices];
 
-template <typename Kernel>
-int occupancy_of(Kernel kern) {
+template <int kStyle>
+int setup_kernel() {
+  auto kern = prepass_kernel<kStyle>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+      cudaSuccess)
+    return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, 0) != cudaSuccess || n < 1)
-    n = 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, kSmemBytes) !=
+      cudaSuccess)
+    return 0;
   return n;
 }
 
-// Resident CTAs for a persistent grid (SM count x blocks per SM), cached per
-// device; 0 on a CUDA error.
-int persistent_grid(int which, int style) {
+// CTAs that fit on the device at once, cached per device; 0 on a CUDA error.
+int resident_ctas(int style) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
   DeviceInfo& di = g_devices[dev];
@@ -425,15 +764,14 @@ int persistent_grid(int which, int style) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return 0;
-    di.occupancy[0][0] = occupancy_of(k_kernel<FP4IDX_ROPE_NEOX>);
-    di.occupancy[0][1] = occupancy_of(k_kernel<FP4IDX_ROPE_INTERLEAVED>);
-    di.occupancy[1][0] = occupancy_of(q_kernel<FP4IDX_ROPE_NEOX>);
-    di.occupancy[1][1] = occupancy_of(q_kernel<FP4IDX_ROPE_INTERLEAVED>);
-    di.occupancy[2][0] = occupancy_of(prepass_kernel<FP4IDX_ROPE_NEOX>);
-    di.occupancy[2][1] = occupancy_of(prepass_kernel<FP4IDX_ROPE_INTERLEAVED>);
+    const int n0 = setup_kernel<FP4IDX_ROPE_NEOX>();
+    const int n1 = setup_kernel<FP4IDX_ROPE_INTERLEAVED>();
+    if (n0 < 1 || n1 < 1) return 0;
+    di.blocks_per_sm[0] = n0;
+    di.blocks_per_sm[1] = n1;
     di.sm_count = sms;
   }
-  return di.sm_count * di.occupancy[which][style];
+  return di.sm_count * di.blocks_per_sm[style];
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -473,14 +811,29 @@ fp4idx_status check_queries(const void* q, int64_t q_tstride, int64_t q_hstride,
   return FP4IDX_OK;
 }
 
-fp4idx_status launch_status() {
+fp4idx_status launch(const KArgs& ka, const QArgs& qa, const Shared& sh, bool keys, bool queries,
+                     int rope_style, void* stream) {
+  Work wk;
+  wk.has_k = keys ? 1 : 0;
+  wk.has_q = queries ? 1 : 0;
+  wk.cpt = (qa.H + kChunkRows - 1) / kChunkRows;
+  wk.per_group = wk.has_k + (queries ? kChunkRows * wk.cpt : 0);
+  {
+    const int64_t groups = (sh.T + kChunkRows - 1) / kChunkRows;
+    const int64_t last = sh.T - (groups - 1) * kChunkRows;  // tokens in the last group
+    wk.total = (groups - 1) * wk.per_group + wk.has_k + (queries ? last * wk.cpt : 0);
+  }
+  const int64_t resident = resident_ctas(rope_style);
+  if (resident <= 0) return FP4IDX_ERR_CUDA;
+  const int64_t want = (wk.total + kWarps - 1) / kWarps;  // at least one item per warp
+  const int64_t grid = want < resident ? want : resident;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (rope_style == FP4IDX_ROPE_NEOX)
+    prepass_kernel<FP4IDX_ROPE_NEOX><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(ka, qa, sh, wk);
+  else
+    prepass_kernel<FP4IDX_ROPE_INTERLEAVED>
+        <<<(unsigned)grid, kThreads, kSmemBytes, s>>>(ka, qa, sh, wk);
   return cudaGetLastError() == cudaSuccess ? FP4IDX_OK : FP4IDX_ERR_CUDA;
-}
-
-int64_t grid_for(int64_t items, int which, int style) {
-  const int64_t resident = persistent_grid(which, style);
-  if (resident <= 0) return 0;
-  return items < resident ? items : resident;
 }
 
 }  // namespace
@@ -502,16 +855,12 @@ fp4idx_status fp4idx_k_norm_rope_pack_store(
   if (err_flags && !aligned(err_flags, 4)) return FP4IDX_ERR_ALIGN;
 
   KArgs ka{static_cast<const uint16_t*>(k), k_token_stride, static_cast<const uint16_t*>(gamma),
-           eps, slot_mapping, kv_cache, num_blocks};
+           eps, slot_mapping, kv_cache, num_blocks,
+           aligned(positions, 16) && aligned(slot_mapping, 16) ? 1 : 0};
+  QArgs qa{};
+  qa.H = 1;
   Shared sh{positions, cos_cache, sin_cache, max_pos, num_tokens, err_flags};
-  const int64_t grid = grid_for((num_tokens + kEngines - 1) / kEngines, 0, rope_style);
-  if (grid <= 0) return FP4IDX_ERR_CUDA;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (rope_style == FP4IDX_ROPE_NEOX)
-    k_kernel<FP4IDX_ROPE_NEOX><<<(unsigned)grid, kThreads, 0, s>>>(ka, sh);
-  else
-    k_kernel<FP4IDX_ROPE_INTERLEAVED><<<(unsigned)grid, kThreads, 0, s>>>(ka, sh);
-  return launch_status();
+  return launch(ka, qa, sh, true, false, rope_style, stream);
 }
 
 fp4idx_status fp4idx_q_rope_pack_weights(
@@ -529,18 +878,12 @@ fp4idx_status fp4idx_q_rope_pack_weights(
   if (st != FP4IDX_OK) return st;
   if (err_flags && !aligned(err_flags, 4)) return FP4IDX_ERR_ALIGN;
 
+  KArgs ka{};
   QArgs qa{static_cast<const uint16_t*>(q), q_token_stride, q_head_stride,
            static_cast<const uint16_t*>(w), w_token_stride, weight_scale, q_fp4, q_scale,
            weights_out, num_heads};
   Shared sh{positions, cos_cache, sin_cache, max_pos, num_tokens, err_flags};
-  const int64_t grid = grid_for(num_tokens, 1, rope_style);
-  if (grid <= 0) return FP4IDX_ERR_CUDA;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (rope_style == FP4IDX_ROPE_NEOX)
-    q_kernel<FP4IDX_ROPE_NEOX><<<(unsigned)grid, kThreads, 0, s>>>(qa, sh);
-  else
-    q_kernel<FP4IDX_ROPE_INTERLEAVED><<<(unsigned)grid, kThreads, 0, s>>>(qa, sh);
-  return launch_status();
+  return launch(ka, qa, sh, false, true, rope_style, stream);
 }
 
 fp4idx_status fp4idx_indexer_prepass(
@@ -563,20 +906,13 @@ fp4idx_status fp4idx_indexer_prepass(
   if (err_flags && !aligned(err_flags, 4)) return FP4IDX_ERR_ALIGN;
 
   KArgs ka{static_cast<const uint16_t*>(k), k_token_stride, static_cast<const uint16_t*>(gamma),
-           eps, slot_mapping, kv_cache, num_blocks};
+           eps, slot_mapping, kv_cache, num_blocks,
+           aligned(positions, 16) && aligned(slot_mapping, 16) ? 1 : 0};
   QArgs qa{static_cast<const uint16_t*>(q), q_token_stride, q_head_stride,
            static_cast<const uint16_t*>(w), w_token_stride, weight_scale, q_fp4, q_scale,
            weights_out, num_heads};
   Shared sh{positions, cos_cache, sin_cache, max_pos, num_tokens, err_flags};
-  const int64_t items = (num_tokens + kEngines - 1) / kEngines + num_tokens;
-  const int64_t grid = grid_for(items, 2, rope_style);
-  if (grid <= 0) return FP4IDX_ERR_CUDA;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (rope_style == FP4IDX_ROPE_NEOX)
-    prepass_kernel<FP4IDX_ROPE_NEOX><<<(unsigned)grid, kThreads, 0, s>>>(ka, qa, sh);
-  else
-    prepass_kernel<FP4IDX_ROPE_INTERLEAVED><<<(unsigned)grid, kThreads, 0, s>>>(ka, qa, sh);
-  return launch_status();
+  return launch(ka, qa, sh, true, true, rope_style, stream);
 }
 
 const char* fp4idx_status_string(fp4idx_status status) {
@@ -591,6 +927,6 @@ const char* fp4idx_status_string(fp4idx_status status) {
   return "unknown status";
 }
 
-const char* fp4idx_version(void) { return "fp4idx 0.1.0 sm_103a"; }
+const char* fp4idx_version(void) { return "fp4idx 0.2.0 sm_103a"; }
 
 }  // extern "C"

@@ -29,6 +29,7 @@ HEAD_DIM = 128
 PAGE_BYTES = 4352
 ERRFLAG_POSITION = 0x1
 ERRFLAG_SLOT = 0x2
+ERRFLAG_TIMEOUT = 0x4
 
 OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_ARG, ERR_CUDA = range(6)
 

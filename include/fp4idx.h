@@ -89,9 +89,12 @@ enum {
   FP4IDX_PAGE_BYTES = 64 * 68 /* 4352 */
 };
 
-/* Bits OR-ed into *err_flags by the device-side range checks. */
+/* Bits OR-ed into *err_flags by the device-side checks. */
 #define FP4IDX_ERRFLAG_POSITION 0x1u /* a position outside [0, max_pos)     */
 #define FP4IDX_ERRFLAG_SLOT 0x2u     /* a slot >= num_blocks * 64           */
+#define FP4IDX_ERRFLAG_TIMEOUT 0x4u  /* an input copy did not arrive within
+                                        1 s; that warp's remaining rows were
+                                        left unwritten                       */
 
 /*
  * Keys: RMSNorm -> RoPE -> two-stage FP4 -> 68-byte slot -> paged cache.
