@@ -197,6 +197,33 @@ __device__ __forceinline__ void mul2(float& r0, float& r1, float a0, float a1, f
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+// (r0, r1) = (rn(a0*b0 + z), rn(a1*b1 + z)) with z = -0 supplied at run time:
+// exactly the rounded products rn(a*b) (x + -0 = x, and +0 + -0 = +0).
+// Because z is unknown to the compiler, the products can never be merged
+// with a following addition into one fused operation.
+__device__ __forceinline__ void prod2(float& r0, float& r1, float a0, float a1, float b0, float b1,
+                                      float z) {
+  asm("{\n\t.reg .b64 ra, rb, rz, rr;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rz, {%6, %6};\n\t"
+      "fma.rn.f32x2 rr, ra, rb, rz;\n\t"
+      "mov.b64 {%0, %1}, rr;\n\t}"
+      : "=f"(r0), "=f"(r1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(z));
+}
+
+// (r0, r1) = (rn(a0+b0), rn(a1+b1)).
+__device__ __forceinline__ void sum2(float& r0, float& r1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rr;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rr, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rr;\n\t}"
+      : "=f"(r0), "=f"(r1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // Per half: max(|a|, |b|) of two bf16 (sign bit = xor of the signs, ignored).
 __device__ __forceinline__ uint32_t hmax_abs(uint32_t a, uint32_t b) {
   uint32_t d;
@@ -340,29 +367,31 @@ struct RopeCoef {
 };
 
 // In-place RoPE of the lane's RoPE-half word group `a`.  All 32 lanes must
-// call (the NeoX partner exchange is a shuffle).  Scalar round-to-nearest
-// intrinsics on purpose: a packed f32x2 multiply followed by a packed add
-// may be contracted into a fused multiply-add, which rounds differently.
+// call (the NeoX partner exchange is a shuffle).  Each result is
+// rn(rn(x*c) + rn(y*s')): the products come from prod2 (exactly rounded,
+// never fused with the sum), then one rounded packed addition.
 template <int kStyle>
-__device__ __forceinline__ void rope_lane(uint32_t (&a)[4], const RopeCoef<kStyle>& rc) {
+__device__ __forceinline__ void rope_lane(uint32_t (&a)[4], const RopeCoef<kStyle>& rc, float z) {
   if (kStyle == FP4IDX_ROPE_NEOX) {
     uint32_t p[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) p[k] = __shfl_xor_sync(kFull, a[k], 4);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const float r0 = __fadd_rn(__fmul_rn(bf16_lo(a[k]), rc.c[2 * k]),
-                                 __fmul_rn(bf16_lo(p[k]), rc.s[2 * k]));
-      const float r1 = __fadd_rn(__fmul_rn(bf16_hi(a[k]), rc.c[2 * k + 1]),
-                                 __fmul_rn(bf16_hi(p[k]), rc.s[2 * k + 1]));
+      float m0, m1, n0, n1, r0, r1;
+      prod2(m0, m1, bf16_lo(a[k]), bf16_hi(a[k]), rc.c[2 * k], rc.c[2 * k + 1], z);
+      prod2(n0, n1, bf16_lo(p[k]), bf16_hi(p[k]), rc.s[2 * k], rc.s[2 * k + 1], z);
+      sum2(r0, r1, m0, m1, n0, n1);
       a[k] = pack_bf16x2(r0, r1);
     }
   } else {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const float x0 = bf16_lo(a[k]), x1 = bf16_hi(a[k]);
-      const float r0 = __fadd_rn(__fmul_rn(x0, rc.c[2 * k]), __fmul_rn(x1, rc.s[2 * k]));
-      const float r1 = __fadd_rn(__fmul_rn(x1, rc.c[2 * k + 1]), __fmul_rn(x0, rc.s[2 * k + 1]));
+      float m0, m1, n0, n1, r0, r1;
+      prod2(m0, m1, x0, x1, rc.c[2 * k], rc.c[2 * k + 1], z);
+      prod2(n0, n1, x1, x0, rc.s[2 * k], rc.s[2 * k + 1], z);
+      sum2(r0, r1, m0, m1, n0, n1);
       a[k] = pack_bf16x2(r0, r1);
     }
   }
@@ -405,6 +434,7 @@ struct Shared {
   int64_t max_pos;
   int64_t T;
   uint32_t* err;
+  float neg_zero;  // -0.0f, passed at run time (see prod2)
 };
 
 // Work items, in groups of kChunkRows tokens: each group contributes one
@@ -412,33 +442,37 @@ struct Shared {
 // chunks (token t, heads h0 .. h0+kChunkRows-1, ceil(H/kChunkRows) chunks per token, if queries
 // are processed).  Interleaving the two kinds gives every warp's contiguous
 // range the same mix of work.
+// All item, token and row indices fit in 32 bits: the host rejects
+// T * H >= 2^31, which no query tensor that fits in memory reaches.
 struct Work {
-  int64_t per_group;  // items of a full group
-  int64_t total;      // all items
-  int64_t cpt;        // query chunks per token = ceil(H / kChunkRows)
-  int has_k;          // 1 if key chunks are processed
-  int has_q;          // 1 if query chunks are processed
+  int32_t per_group;  // items of a full group
+  int32_t total;      // all items
+  int32_t cpt;        // query chunks per token = ceil(H / kChunkRows)
+  int32_t H;          // heads
+  int32_t T;          // tokens
+  int32_t has_k;      // 1 if key chunks are processed
+  int32_t has_q;      // 1 if query chunks are processed
 };
 
 struct ItemIter {
-  int64_t t;     // key: first token of the chunk; query: the token
-  int64_t h0;    // query: first head of the chunk
-  int is_key;
-  __device__ __forceinline__ void seek(int64_t item, const Work& wk) {
-    const int64_t o = item / wk.per_group;
-    const int64_t sub = item - o * wk.per_group;
+  int32_t t;   // key: first token of the chunk; query: the token
+  int32_t h0;  // query: first head of the chunk
+  int32_t is_key;
+  __device__ __forceinline__ void seek(int32_t item, const Work& wk) {
+    const int32_t o = item / wk.per_group;
+    const int32_t sub = item - o * wk.per_group;
     if (wk.has_k && sub == 0) {
       is_key = 1;
       t = o * kChunkRows;
       h0 = 0;
     } else {
-      const int64_t q = sub - wk.has_k;
+      const int32_t q = sub - wk.has_k;
       is_key = 0;
       t = o * kChunkRows + q / wk.cpt;
       h0 = (q % wk.cpt) * kChunkRows;
     }
   }
-  __device__ __forceinline__ void next(const Work& wk, int64_t H) {
+  __device__ __forceinline__ void next(const Work& wk) {
     if (is_key) {
       if (wk.has_q) {
         is_key = 0;
@@ -449,7 +483,7 @@ struct ItemIter {
       return;
     }
     h0 += kChunkRows;
-    if (h0 >= H) {
+    if (h0 >= wk.H) {
       h0 = 0;
       ++t;
       if (wk.has_k && (t % kChunkRows) == 0) is_key = 1;
@@ -461,19 +495,19 @@ struct ItemIter {
 // The producer's position lookups: the position of the token after the
 // current one is loaded one token ahead, so issuing never waits for it.
 struct PosCache {
-  int64_t t, v;    // token and its position
-  int64_t nt, nv;  // next token and its position (load in flight)
+  int32_t t, nt;   // token and next token
+  int64_t v, nv;   // their positions (the next one's load in flight)
   __device__ __forceinline__ void reset() {
     t = -1;
     nt = -1;
     v = 0;
     nv = 0;
   }
-  __device__ __forceinline__ int64_t get(int64_t tok, const Shared& sh) {
+  __device__ __forceinline__ int64_t get(int32_t tok, const Shared& sh, int32_t T) {
     if (tok != t) {
       v = tok == nt ? nv : __ldg(sh.pos + tok);
       t = tok;
-      if (tok + 1 < sh.T) {
+      if (tok + 1 < T) {
         nt = tok + 1;
         nv = __ldg(sh.pos + tok + 1);
       }
@@ -487,14 +521,14 @@ __device__ __forceinline__ void issue_item(const ItemIter& it, const Work& wk, c
                                            const QArgs& qa, const Shared& sh, uint32_t stage,
                                            uint32_t bar, PosCache& pc) {
   if (it.is_key) {
-    const int64_t n = sh.T - it.t < kChunkRows ? sh.T - it.t : kChunkRows;
+    const int n = min(wk.T - it.t, kChunkRows);
     const bool meta = ka.meta_bulk && n == kChunkRows;
     mbar_arrive_expect_tx(bar, (uint32_t)n * kRowBytes + (meta ? 2u * kChunkRows * 8u : 0u));
-    const uint16_t* src = ka.k + it.t * ka.k_stride;
+    const uint16_t* src = ka.k + (int64_t)it.t * ka.k_stride;
     if (ka.k_stride == FP4IDX_HEAD_DIM) {
       bulk_g2s(stage, src, (uint32_t)n * kRowBytes, bar);
     } else {
-      for (int64_t r = 0; r < n; ++r)
+      for (int r = 0; r < n; ++r)
         bulk_g2s(stage + (uint32_t)r * kRowBytes, src + r * ka.k_stride, kRowBytes, bar);
     }
     if (meta) {
@@ -503,16 +537,16 @@ __device__ __forceinline__ void issue_item(const ItemIter& it, const Work& wk, c
     }
     return;
   }
-  const int64_t n = qa.H - it.h0 < kChunkRows ? qa.H - it.h0 : kChunkRows;
-  const int64_t pos_v = pc.get(it.t, sh);
+  const int n = min(wk.H - it.h0, kChunkRows);
+  const int64_t pos_v = pc.get(it.t, sh, wk.T);
   const bool ok = pos_v >= 0 && pos_v < sh.max_pos;
   asm volatile("st.shared.u32 [%0], %1;" ::"r"(stage + kStageHdr), "r"(ok ? 1u : 0u) : "memory");
   mbar_arrive_expect_tx(bar, (uint32_t)n * kRowBytes + (ok ? 256u : 0u));
-  const uint16_t* src = qa.q + it.t * qa.q_tstride + it.h0 * qa.q_hstride;
+  const uint16_t* src = qa.q + (int64_t)it.t * qa.q_tstride + (int64_t)it.h0 * qa.q_hstride;
   if (qa.q_hstride == FP4IDX_HEAD_DIM) {
     bulk_g2s(stage, src, (uint32_t)n * kRowBytes, bar);
   } else {
-    for (int64_t r = 0; r < n; ++r)
+    for (int r = 0; r < n; ++r)
       bulk_g2s(stage + (uint32_t)r * kRowBytes, src + r * qa.q_hstride, kRowBytes, bar);
   }
   if (ok) {
@@ -530,32 +564,33 @@ __device__ __forceinline__ int64_t lds_s64(uint32_t addr) {
 
 // A query item: up to kChunkRows heads of token it.t, rows in the stage.
 template <int kStyle>
-__device__ __forceinline__ void query_chunk(const ItemIter& it, const QArgs& qa, const Shared& sh,
-                                            uint32_t stage) {
+__device__ __forceinline__ void query_chunk(const ItemIter& it, const Work& wk, const QArgs& qa,
+                                            const Shared& sh, uint32_t stage) {
   const int lane = threadIdx.x & 31, j = lane & 7, rg = lane >> 3;
-  const int n = (int)(qa.H - it.h0 < kChunkRows ? qa.H - it.h0 : kChunkRows);
+  const int n = min(wk.H - it.h0, kChunkRows);
   uint32_t ok;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(ok) : "r"(stage + kStageHdr));
   if (!ok) {
     if (lane == 0) flag_error(sh.err, FP4IDX_ERRFLAG_POSITION);
     return;  // the whole token is skipped; uniform over the warp
   }
-  const int64_t row0 = it.t * qa.H + it.h0;
+  const int32_t row0 = it.t * wk.H + it.h0;
   uint16_t wb = 0;
-  if (lane < n) wb = __ldg(qa.w + it.t * qa.w_tstride + it.h0 + lane);
+  if (lane < n) wb = __ldg(qa.w + (int64_t)it.t * qa.w_tstride + it.h0 + lane);
 
   RopeCoef<kStyle> rc;
   rc.load_smem(stage + kStageCos, stage + kStageSin, j);
-  uint8_t* const out = qa.q_fp4 + row0 * kPayloadBytes + 4 * j;
-  uint8_t* const scl = qa.q_scale + row0 * 4;
-#pragma unroll 1
-  for (int r0 = 0; r0 < n; r0 += 4) {  // uniform over the warp
+  uint8_t* const out = qa.q_fp4 + (int64_t)row0 * kPayloadBytes + 4 * j;
+  uint8_t* const scl = qa.q_scale + (int64_t)row0 * 4;
+  const uint32_t rows = stage + 16u * j;
+#pragma unroll
+  for (int r0 = 0; r0 < kChunkRows; r0 += 4) {
+    if (r0 >= n) break;  // uniform over the warp
     const int r = r0 + rg;
     uint32_t a[4], b[4];
-    const uint32_t rowaddr = stage + (uint32_t)r * kRowBytes + 16u * j;
-    lds128(rowaddr, a);
-    lds128(rowaddr + 128u, b);
-    rope_lane<kStyle>(a, rc);
+    lds128(rows + (uint32_t)r * kRowBytes, a);
+    lds128(rows + (uint32_t)r * kRowBytes + 128u, b);
+    rope_lane<kStyle>(a, rc, sh.neg_zero);
     uint32_t pa, pb, ew;
     quant_lane(a, b, j, pa, pb, ew);
     if (r < n) {
@@ -577,6 +612,7 @@ struct KeyMeta {
 
 __device__ __forceinline__ KeyMeta key_meta(const ItemIter& it, const KArgs& ka, const Shared& sh,
                                             uint32_t stage, int r, int n, bool meta, int j) {
+  // (it.t + r < T: r < n)
   KeyMeta m{-1, 0, false};
   if (r < n) {
     if (meta) {
@@ -604,10 +640,10 @@ __device__ __forceinline__ KeyMeta key_meta(const ItemIter& it, const KArgs& ka,
 
 // A key item: tokens it.t .. it.t + kChunkRows - 1, rows in the stage.
 template <int kStyle>
-__device__ __forceinline__ void key_chunk(const ItemIter& it, const KArgs& ka, const Shared& sh,
-                                          uint32_t stage) {
+__device__ __forceinline__ void key_chunk(const ItemIter& it, const Work& wk, const KArgs& ka,
+                                          const Shared& sh, uint32_t stage) {
   const int lane = threadIdx.x & 31, j = lane & 7, rg = lane >> 3;
-  const int n = (int)(sh.T - it.t < kChunkRows ? sh.T - it.t : kChunkRows);
+  const int n = min(wk.T - it.t, kChunkRows);
   const bool meta = ka.meta_bulk && n == kChunkRows;  // uniform
 #pragma unroll 1
   for (int r0 = 0; r0 < n; r0 += 4) {  // uniform over the warp
@@ -652,7 +688,7 @@ __device__ __forceinline__ void key_chunk(const ItemIter& it, const KArgs& ka, c
       mul2(y0, y1, u0, u1, bf16_lo(gwb[k]), bf16_hi(gwb[k]));
       b[k] = pack_bf16x2(y0, y1);
     }
-    rope_lane<kStyle>(a, rc);
+    rope_lane<kStyle>(a, rc, sh.neg_zero);
     uint32_t pa, pb, ew;
     quant_lane(a, b, j, pa, pb, ew);
     if (km.live) {
@@ -683,23 +719,24 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSm)
 
   const int64_t G = (int64_t)gridDim.x * kWarps;
   const int64_t g = (int64_t)blockIdx.x * kWarps + warp;
-  const int64_t lo = g * wk.total / G, hi = (g + 1) * wk.total / G;
-  if (lo >= hi) return;
+  const int32_t lo = (int32_t)(g * wk.total / G);
+  const int32_t count = (int32_t)((g + 1) * wk.total / G) - lo;  // items of this warp
+  if (count <= 0) return;
 
   ItemIter cons, prod;
   cons.seek(lo, wk);
   prod = cons;
   PosCache pc;  // producer's position lookups (lane 0)
   pc.reset();
-  const int64_t first = hi - lo < kStages ? hi - lo : kStages;
+  const int first = count < kStages ? count : kStages;
   for (int s = 0; s < first; ++s) {
     if (lane == 0) issue_item(prod, wk, ka, qa, sh, ring + s * kStageBytes, bar0 + 8u * s, pc);
-    prod.next(wk, qa.H);
+    prod.next(wk);
   }
 
   int s = 0;
   uint32_t phase = 0;
-  for (int64_t i = lo; i < hi; ++i) {
+  for (int32_t i = 0; i < count; ++i) {
     const uint32_t stage = ring + (uint32_t)s * kStageBytes;
     const uint32_t bar = bar0 + 8u * s;
     if (!mbar_wait_bounded(bar, phase)) {
@@ -708,7 +745,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSm)
       if (lane == 0) flag_error(sh.err, FP4IDX_ERRFLAG_TIMEOUT);
       int s2 = s;
       uint32_t p2 = phase;
-      for (int64_t k = 0; k < kStages && i + k < hi; ++k) {
+      for (int k = 0; k < kStages && i + k < count; ++k) {
         mbar_wait_bounded(bar0 + 8u * s2, p2);
         if (++s2 == kStages) {
           s2 = 0;
@@ -718,15 +755,15 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSm)
       return;
     }
     if (cons.is_key)
-      key_chunk<kStyle>(cons, ka, sh, stage);
+      key_chunk<kStyle>(cons, wk, ka, sh, stage);
     else
-      query_chunk<kStyle>(cons, qa, sh, stage);
+      query_chunk<kStyle>(cons, wk, qa, sh, stage);
     __syncwarp();
-    if (i + kStages < hi) {
+    if (i + kStages < count) {
       if (lane == 0) issue_item(prod, wk, ka, qa, sh, stage, bar, pc);
-      prod.next(wk, qa.H);
+      prod.next(wk);
     }
-    cons.next(wk, qa.H);
+    cons.next(wk);
     if (++s == kStages) {
       s = 0;
       phase ^= 1u;
@@ -813,14 +850,19 @@ fp4idx_status check_queries(const void* q, int64_t q_tstride, int64_t q_hstride,
 
 fp4idx_status launch(const KArgs& ka, const QArgs& qa, const Shared& sh, bool keys, bool queries,
                      int rope_style, void* stream) {
+  // 32-bit indices: T * H, T * ceil(H/16) + T and T itself below 2^31.
+  const int64_t H = queries ? qa.H : 1;
+  if (sh.T >= INT32_MAX / 2 || H >= INT32_MAX || sh.T * H >= INT32_MAX / 2) return FP4IDX_ERR_SHAPE;
   Work wk;
   wk.has_k = keys ? 1 : 0;
   wk.has_q = queries ? 1 : 0;
-  wk.cpt = (qa.H + kChunkRows - 1) / kChunkRows;
+  wk.H = (int32_t)H;
+  wk.T = (int32_t)sh.T;
+  wk.cpt = (int32_t)((H + kChunkRows - 1) / kChunkRows);
   wk.per_group = wk.has_k + (queries ? kChunkRows * wk.cpt : 0);
   {
-    const int64_t groups = (sh.T + kChunkRows - 1) / kChunkRows;
-    const int64_t last = sh.T - (groups - 1) * kChunkRows;  // tokens in the last group
+    const int32_t groups = (wk.T + kChunkRows - 1) / kChunkRows;
+    const int32_t last = wk.T - (groups - 1) * kChunkRows;  // tokens in the last group
     wk.total = (groups - 1) * wk.per_group + wk.has_k + (queries ? last * wk.cpt : 0);
   }
   const int64_t resident = resident_ctas(rope_style);
@@ -859,7 +901,7 @@ fp4idx_status fp4idx_k_norm_rope_pack_store(
            aligned(positions, 16) && aligned(slot_mapping, 16) ? 1 : 0};
   QArgs qa{};
   qa.H = 1;
-  Shared sh{positions, cos_cache, sin_cache, max_pos, num_tokens, err_flags};
+  Shared sh{positions, cos_cache, sin_cache, max_pos, num_tokens, err_flags, -0.0f};
   return launch(ka, qa, sh, true, false, rope_style, stream);
 }
 
@@ -882,7 +924,7 @@ fp4idx_status fp4idx_q_rope_pack_weights(
   QArgs qa{static_cast<const uint16_t*>(q), q_token_stride, q_head_stride,
            static_cast<const uint16_t*>(w), w_token_stride, weight_scale, q_fp4, q_scale,
            weights_out, num_heads};
-  Shared sh{positions, cos_cache, sin_cache, max_pos, num_tokens, err_flags};
+  Shared sh{positions, cos_cache, sin_cache, max_pos, num_tokens, err_flags, -0.0f};
   return launch(ka, qa, sh, false, true, rope_style, stream);
 }
 
@@ -911,7 +953,7 @@ fp4idx_status fp4idx_indexer_prepass(
   QArgs qa{static_cast<const uint16_t*>(q), q_token_stride, q_head_stride,
            static_cast<const uint16_t*>(w), w_token_stride, weight_scale, q_fp4, q_scale,
            weights_out, num_heads};
-  Shared sh{positions, cos_cache, sin_cache, max_pos, num_tokens, err_flags};
+  Shared sh{positions, cos_cache, sin_cache, max_pos, num_tokens, err_flags, -0.0f};
   return launch(ka, qa, sh, true, true, rope_style, stream);
 }
 
