@@ -116,6 +116,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
+// Adds to the stage's expected byte count without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+// Arrives (release): everything this thread wrote before is visible to a
+// thread whose wait observes the completed phase.
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -442,89 +454,98 @@ struct Shared {
 // chunks (token t, heads h0 .. h0+kChunkRows-1, ceil(H/kChunkRows) chunks per token, if queries
 // are processed).  Interleaving the two kinds gives every warp's contiguous
 // range the same mix of work.
-// All item, token and row indices fit in 32 bits: the host rejects
-// T * H >= 2^31, which no query tensor that fits in memory reaches.
-struct Work {
-  int32_t per_group;  // items of a full group
-  int32_t total;      // all items
-  int32_t cpt;        // query chunks per token = ceil(H / kChunkRows)
-  int32_t H;          // heads
-  int32_t T;          // tokens
-  int32_t has_k;      // 1 if key chunks are processed
-  int32_t has_q;      // 1 if query chunks are processed
+// Unsigned 32-bit division by a run-time invariant d >= 1 with one
+// multiply-high and two shifts (Granlund and Montgomery, "Division by
+// Invariant Integers using Multiplication", PLDI 1994, section 4):
+//   l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1,
+//   t = mulhi(m, n), q = (t + ((n - t) >> min(l, 1))) >> max(l - 1, 0).
+struct FastDiv {
+  uint32_t m, s1, s2;
+  __device__ __forceinline__ uint32_t div(uint32_t n) const {
+    const uint32_t t = __umulhi(m, n);
+    return (t + ((n - t) >> s1)) >> s2;
+  }
 };
 
-struct ItemIter {
-  int32_t t;   // key: first token of the chunk; query: the token
-  int32_t h0;  // query: first head of the chunk
-  int32_t is_key;
-  __device__ __forceinline__ void seek(int32_t item, const Work& wk) {
-    const int32_t o = item / wk.per_group;
-    const int32_t sub = item - o * wk.per_group;
-    if (wk.has_k && sub == 0) {
-      is_key = 1;
-      t = o * kChunkRows;
-      h0 = 0;
-    } else {
-      const int32_t q = sub - wk.has_k;
-      is_key = 0;
-      t = o * kChunkRows + q / wk.cpt;
-      h0 = (q % wk.cpt) * kChunkRows;
-    }
-  }
-  __device__ __forceinline__ void next(const Work& wk) {
-    if (is_key) {
-      if (wk.has_q) {
-        is_key = 0;
-        h0 = 0;
-      } else {
-        t += kChunkRows;
-      }
-      return;
-    }
-    h0 += kChunkRows;
-    if (h0 >= wk.H) {
-      h0 = 0;
-      ++t;
-      if (wk.has_k && (t % kChunkRows) == 0) is_key = 1;
-    }
-  }
+FastDiv make_fastdiv(uint32_t d) {
+  uint32_t l = 0;
+  while ((1ull << l) < d) ++l;
+  FastDiv f;
+  f.m = (uint32_t)((((1ull << l) - d) << 32) / d + 1);
+  f.s1 = l < 1 ? l : 1;
+  f.s2 = l > 1 ? l - 1 : 0;
+  return f;
+}
+
+// The work of one launch, in two item lists: key items (kChunkRows
+// consecutive tokens each) and query items (token t, heads h0 .. h0 +
+// kChunkRows - 1; cpt items per token).  Every CTA gets an equal slice of
+// each list; inside a CTA the warps claim items one at a time from two
+// shared-memory counters (key items first), so a warp that runs ahead
+// simply takes more items.  All indices fit in 32 bits: the host rejects
+// T * H >= 2^30, which no query tensor that fits in memory reaches.
+struct Work {
+  int32_t T, H;
+  int32_t nk;   // key items
+  int32_t nq;   // query items = T * cpt
+  int32_t cpt;  // query items per token = ceil(H / kChunkRows)
+  FastDiv cpt_div;
 };
+
+enum : uint32_t { kItemNone = 0, kItemKey = 1, kItemQuery = 2 };
 
 // --------------------------------------------------------- producer side
-// The producer's position lookups: the position of the token after the
-// current one is loaded one token ahead, so issuing never waits for it.
-struct PosCache {
-  int32_t t, nt;   // token and next token
-  int64_t v, nv;   // their positions (the next one's load in flight)
-  __device__ __forceinline__ void reset() {
-    t = -1;
-    nt = -1;
-    v = 0;
-    nv = 0;
-  }
-  __device__ __forceinline__ int64_t get(int32_t tok, const Shared& sh, int32_t T) {
-    if (tok != t) {
-      v = tok == nt ? nv : __ldg(sh.pos + tok);
-      t = tok;
-      if (tok + 1 < T) {
-        nt = tok + 1;
-        nv = __ldg(sh.pos + tok + 1);
+// Lane 0's view of the items it will issue next: A is ready to issue (its
+// token position was requested one step earlier), B is claimed.
+struct Producer {
+  uint32_t a_kind, b_kind;
+  int32_t a_t, a_h0, b_idx;
+  int64_t a_pos;
+  bool k_done;
+
+  __device__ __forceinline__ void claim(int32_t* sk, int32_t* sq, int32_t k_hi, int32_t q_hi) {
+    if (!k_done) {
+      const int32_t k = atomicAdd(sk, 1);
+      if (k < k_hi) {
+        b_kind = kItemKey;
+        b_idx = k;
+        return;
       }
+      k_done = true;
     }
-    return v;
+    const int32_t q = atomicAdd(sq, 1);
+    b_kind = q < q_hi ? kItemQuery : kItemNone;
+    b_idx = q;
+  }
+  // A <- B (decode it and request its position), then claim a new B.
+  __device__ __forceinline__ void advance(const Work& wk, const Shared& sh, int32_t* sk,
+                                          int32_t* sq, int32_t k_hi, int32_t q_hi) {
+    a_kind = b_kind;
+    if (a_kind == kItemKey) {
+      a_t = b_idx * kChunkRows;
+      a_h0 = 0;
+    } else if (a_kind == kItemQuery) {
+      a_t = (int32_t)wk.cpt_div.div((uint32_t)b_idx);
+      a_h0 = (b_idx - a_t * wk.cpt) * kChunkRows;
+      a_pos = __ldg(sh.pos + a_t);
+    }
+    if (a_kind != kItemNone) claim(sk, sq, k_hi, q_hi);
   }
 };
 
-// Issues the copies of one item into a stage (lane 0 only).
-__device__ __forceinline__ void issue_item(const ItemIter& it, const Work& wk, const KArgs& ka,
+// Issues item A into a stage: its header (kind, token, first head, position
+// ok) and its bulk copies.  Lane 0 only.
+__device__ __forceinline__ void issue_item(const Producer& pr, const Work& wk, const KArgs& ka,
                                            const QArgs& qa, const Shared& sh, uint32_t stage,
-                                           uint32_t bar, PosCache& pc) {
-  if (it.is_key) {
-    const int n = min(wk.T - it.t, kChunkRows);
+                                           uint32_t bar) {
+  if (pr.a_kind == kItemKey) {
+    const int n = min(wk.T - pr.a_t, kChunkRows);
     const bool meta = ka.meta_bulk && n == kChunkRows;
+    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(stage + kStageHdr), "r"(kItemKey),
+                 "r"(pr.a_t)
+                 : "memory");
     mbar_arrive_expect_tx(bar, (uint32_t)n * kRowBytes + (meta ? 2u * kChunkRows * 8u : 0u));
-    const uint16_t* src = ka.k + (int64_t)it.t * ka.k_stride;
+    const uint16_t* src = ka.k + (int64_t)pr.a_t * ka.k_stride;
     if (ka.k_stride == FP4IDX_HEAD_DIM) {
       bulk_g2s(stage, src, (uint32_t)n * kRowBytes, bar);
     } else {
@@ -532,27 +553,32 @@ __device__ __forceinline__ void issue_item(const ItemIter& it, const Work& wk, c
         bulk_g2s(stage + (uint32_t)r * kRowBytes, src + r * ka.k_stride, kRowBytes, bar);
     }
     if (meta) {
-      bulk_g2s(stage + kStageCos, sh.pos + it.t, kChunkRows * 8u, bar);
-      bulk_g2s(stage + kStageSin, ka.slots + it.t, kChunkRows * 8u, bar);
+      bulk_g2s(stage + kStageCos, sh.pos + pr.a_t, kChunkRows * 8u, bar);
+      bulk_g2s(stage + kStageSin, ka.slots + pr.a_t, kChunkRows * 8u, bar);
     }
     return;
   }
-  const int n = min(wk.H - it.h0, kChunkRows);
-  const int64_t pos_v = pc.get(it.t, sh, wk.T);
-  const bool ok = pos_v >= 0 && pos_v < sh.max_pos;
-  asm volatile("st.shared.u32 [%0], %1;" ::"r"(stage + kStageHdr), "r"(ok ? 1u : 0u) : "memory");
-  mbar_arrive_expect_tx(bar, (uint32_t)n * kRowBytes + (ok ? 256u : 0u));
-  const uint16_t* src = qa.q + (int64_t)it.t * qa.q_tstride + (int64_t)it.h0 * qa.q_hstride;
+  // Query item: the row copies go out before the token's position is
+  // needed; the header and the arrive come last, so the consumer sees the
+  // header once the phase completes.  An out-of-range position copies table
+  // row 0 instead (the consumer skips the token).
+  const int n = min(wk.H - pr.a_h0, kChunkRows);
+  mbar_expect_tx(bar, (uint32_t)n * kRowBytes + 256u);
+  const uint16_t* src = qa.q + (int64_t)pr.a_t * qa.q_tstride + (int64_t)pr.a_h0 * qa.q_hstride;
   if (qa.q_hstride == FP4IDX_HEAD_DIM) {
     bulk_g2s(stage, src, (uint32_t)n * kRowBytes, bar);
   } else {
     for (int r = 0; r < n; ++r)
       bulk_g2s(stage + (uint32_t)r * kRowBytes, src + r * qa.q_hstride, kRowBytes, bar);
   }
-  if (ok) {
-    bulk_g2s(stage + kStageCos, sh.cos + pos_v * kRopeHalf, 128u, bar);
-    bulk_g2s(stage + kStageSin, sh.sin + pos_v * kRopeHalf, 128u, bar);
-  }
+  const bool ok = pr.a_pos >= 0 && pr.a_pos < sh.max_pos;
+  const int64_t row = ok ? pr.a_pos : 0;
+  bulk_g2s(stage + kStageCos, sh.cos + row * kRopeHalf, 128u, bar);
+  bulk_g2s(stage + kStageSin, sh.sin + row * kRopeHalf, 128u, bar);
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(stage + kStageHdr),
+               "r"(kItemQuery), "r"(pr.a_t), "r"(pr.a_h0), "r"(ok ? 1u : 0u)
+               : "memory");
+  mbar_arrive(bar);
 }
 
 // --------------------------------------------------------- consumer side
@@ -562,21 +588,20 @@ __device__ __forceinline__ int64_t lds_s64(uint32_t addr) {
   return v;
 }
 
-// A query item: up to kChunkRows heads of token it.t, rows in the stage.
+// A query item: heads h0 .. h0 + kChunkRows - 1 of token t, rows in the
+// stage; `ok` says whether the token's position was in range.
 template <int kStyle>
-__device__ __forceinline__ void query_chunk(const ItemIter& it, const Work& wk, const QArgs& qa,
-                                            const Shared& sh, uint32_t stage) {
+__device__ __forceinline__ void query_chunk(int32_t t, int32_t h0, bool ok, const Work& wk,
+                                            const QArgs& qa, const Shared& sh, uint32_t stage) {
   const int lane = threadIdx.x & 31, j = lane & 7, rg = lane >> 3;
-  const int n = min(wk.H - it.h0, kChunkRows);
-  uint32_t ok;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(ok) : "r"(stage + kStageHdr));
+  const int n = min(wk.H - h0, kChunkRows);
   if (!ok) {
     if (lane == 0) flag_error(sh.err, FP4IDX_ERRFLAG_POSITION);
     return;  // the whole token is skipped; uniform over the warp
   }
-  const int32_t row0 = it.t * wk.H + it.h0;
+  const int32_t row0 = t * wk.H + h0;
   uint16_t wb = 0;
-  if (lane < n) wb = __ldg(qa.w + (int64_t)it.t * qa.w_tstride + it.h0 + lane);
+  if (lane < n) wb = __ldg(qa.w + (int64_t)t * qa.w_tstride + h0 + lane);
 
   RopeCoef<kStyle> rc;
   rc.load_smem(stage + kStageCos, stage + kStageSin, j);
@@ -610,17 +635,16 @@ struct KeyMeta {
   bool live;
 };
 
-__device__ __forceinline__ KeyMeta key_meta(const ItemIter& it, const KArgs& ka, const Shared& sh,
+__device__ __forceinline__ KeyMeta key_meta(int32_t t0, const KArgs& ka, const Shared& sh,
                                             uint32_t stage, int r, int n, bool meta, int j) {
-  // (it.t + r < T: r < n)
   KeyMeta m{-1, 0, false};
   if (r < n) {
     if (meta) {
       m.pos = lds_s64(stage + kStageCos + 8u * r);
       m.slot = lds_s64(stage + kStageSin + 8u * r);
     } else {
-      m.pos = __ldg(sh.pos + it.t + r);
-      m.slot = __ldg(ka.slots + it.t + r);
+      m.pos = __ldg(sh.pos + t0 + r);
+      m.slot = __ldg(ka.slots + t0 + r);
     }
     m.live = m.slot >= 0;
   }
@@ -638,17 +662,17 @@ __device__ __forceinline__ KeyMeta key_meta(const ItemIter& it, const KArgs& ka,
   return m;
 }
 
-// A key item: tokens it.t .. it.t + kChunkRows - 1, rows in the stage.
+// A key item: tokens t0 .. t0 + kChunkRows - 1, rows in the stage.
 template <int kStyle>
-__device__ __forceinline__ void key_chunk(const ItemIter& it, const Work& wk, const KArgs& ka,
+__device__ __forceinline__ void key_chunk(int32_t t0, const Work& wk, const KArgs& ka,
                                           const Shared& sh, uint32_t stage) {
   const int lane = threadIdx.x & 31, j = lane & 7, rg = lane >> 3;
-  const int n = min(wk.T - it.t, kChunkRows);
+  const int n = min(wk.T - t0, kChunkRows);
   const bool meta = ka.meta_bulk && n == kChunkRows;  // uniform
 #pragma unroll 1
   for (int r0 = 0; r0 < n; r0 += 4) {  // uniform over the warp
     const int r = r0 + rg;
-    const KeyMeta km = key_meta(it, ka, sh, stage, r, n, meta, j);
+    const KeyMeta km = key_meta(t0, ka, sh, stage, r, n, meta, j);
     RopeCoef<kStyle> rc;
     rc.load_global(sh.cos + km.pos * kRopeHalf, sh.sin + km.pos * kRopeHalf, j);
 
@@ -708,62 +732,69 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSm)
     prepass_kernel(KArgs ka, QArgs qa, Shared sh, Work wk) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[kWarps * kStages];
+  __shared__ int32_t next_k, next_q;  // this CTA's claim counters
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int32_t k_hi = (int32_t)((int64_t)(blockIdx.x + 1) * wk.nk / gridDim.x);
+  const int32_t q_hi = (int32_t)((int64_t)(blockIdx.x + 1) * wk.nq / gridDim.x);
+  if (threadIdx.x == 0) {
+    next_k = (int32_t)((int64_t)blockIdx.x * wk.nk / gridDim.x);
+    next_q = (int32_t)((int64_t)blockIdx.x * wk.nq / gridDim.x);
+  }
   const uint32_t ring = smem_addr(smem) + (uint32_t)warp * kRingBytes;
   const uint32_t bar0 = smem_addr(&bars[warp * kStages]);
   if (lane == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8u * s, 1);
     fence_mbar_init();
   }
-  __syncwarp();
+  __syncthreads();
 
-  const int64_t G = (int64_t)gridDim.x * kWarps;
-  const int64_t g = (int64_t)blockIdx.x * kWarps + warp;
-  const int32_t lo = (int32_t)(g * wk.total / G);
-  const int32_t count = (int32_t)((g + 1) * wk.total / G) - lo;  // items of this warp
-  if (count <= 0) return;
-
-  ItemIter cons, prod;
-  cons.seek(lo, wk);
-  prod = cons;
-  PosCache pc;  // producer's position lookups (lane 0)
-  pc.reset();
-  const int first = count < kStages ? count : kStages;
-  for (int s = 0; s < first; ++s) {
-    if (lane == 0) issue_item(prod, wk, ka, qa, sh, ring + s * kStageBytes, bar0 + 8u * s, pc);
-    prod.next(wk);
+  Producer pr;  // meaningful in lane 0 only
+  pr.k_done = false;
+  pr.b_kind = kItemNone;
+  if (lane == 0) {
+    pr.claim(&next_k, &next_q, k_hi, q_hi);
+    pr.advance(wk, sh, &next_k, &next_q, k_hi, q_hi);
+  }
+  uint32_t valid = 0;  // bit s: stage s holds an item
+  for (int s = 0; s < kStages; ++s) {
+    bool v = false;
+    if (lane == 0 && pr.a_kind != kItemNone) {
+      issue_item(pr, wk, ka, qa, sh, ring + s * kStageBytes, bar0 + 8u * s);
+      pr.advance(wk, sh, &next_k, &next_q, k_hi, q_hi);
+      v = true;
+    }
+    valid |= (uint32_t)__shfl_sync(kFull, v ? 1 : 0, 0) << s;
   }
 
   int s = 0;
   uint32_t phase = 0;
-  for (int32_t i = 0; i < count; ++i) {
+  while (valid & (1u << s)) {
     const uint32_t stage = ring + (uint32_t)s * kStageBytes;
     const uint32_t bar = bar0 + 8u * s;
     if (!mbar_wait_bounded(bar, phase)) {
       // Give up: report, then wait (bounded) for this warp's other copies so
       // none is still writing shared memory when the CTA exits.
       if (lane == 0) flag_error(sh.err, FP4IDX_ERRFLAG_TIMEOUT);
-      int s2 = s;
-      uint32_t p2 = phase;
-      for (int k = 0; k < kStages && i + k < count; ++k) {
-        mbar_wait_bounded(bar0 + 8u * s2, p2);
-        if (++s2 == kStages) {
-          s2 = 0;
-          p2 ^= 1u;
-        }
+      for (int k = 1; k < kStages; ++k) {
+        const int s2 = (s + k) % kStages;
+        if (valid & (1u << s2)) mbar_wait_bounded(bar0 + 8u * s2, phase ^ (s + k >= kStages ? 1u : 0u));
       }
       return;
     }
-    if (cons.is_key)
-      key_chunk<kStyle>(cons, wk, ka, sh, stage);
+    uint32_t hdr[4];
+    lds128(stage + kStageHdr, hdr);
+    if (hdr[0] == kItemKey)
+      key_chunk<kStyle>((int32_t)hdr[1], wk, ka, sh, stage);
     else
-      query_chunk<kStyle>(cons, wk, qa, sh, stage);
+      query_chunk<kStyle>((int32_t)hdr[1], (int32_t)hdr[2], hdr[3] != 0, wk, qa, sh, stage);
     __syncwarp();
-    if (i + kStages < count) {
-      if (lane == 0) issue_item(prod, wk, ka, qa, sh, stage, bar, pc);
-      prod.next(wk);
+    bool v = false;
+    if (lane == 0 && pr.a_kind != kItemNone) {
+      issue_item(pr, wk, ka, qa, sh, stage, bar);
+      pr.advance(wk, sh, &next_k, &next_q, k_hi, q_hi);
+      v = true;
     }
-    cons.next(wk);
+    valid = (valid & ~(1u << s)) | ((uint32_t)__shfl_sync(kFull, v ? 1 : 0, 0) << s);
     if (++s == kStages) {
       s = 0;
       phase ^= 1u;
@@ -850,24 +881,20 @@ fp4idx_status check_queries(const void* q, int64_t q_tstride, int64_t q_hstride,
 
 fp4idx_status launch(const KArgs& ka, const QArgs& qa, const Shared& sh, bool keys, bool queries,
                      int rope_style, void* stream) {
-  // 32-bit indices: T * H, T * ceil(H/16) + T and T itself below 2^31.
+  // 32-bit indices: T * H and T itself below 2^30.
   const int64_t H = queries ? qa.H : 1;
-  if (sh.T >= INT32_MAX / 2 || H >= INT32_MAX || sh.T * H >= INT32_MAX / 2) return FP4IDX_ERR_SHAPE;
+  if (sh.T >= (1 << 30) || H >= (1 << 30) || sh.T * H >= (1 << 30)) return FP4IDX_ERR_SHAPE;
   Work wk;
-  wk.has_k = keys ? 1 : 0;
-  wk.has_q = queries ? 1 : 0;
-  wk.H = (int32_t)H;
   wk.T = (int32_t)sh.T;
+  wk.H = (int32_t)H;
   wk.cpt = (int32_t)((H + kChunkRows - 1) / kChunkRows);
-  wk.per_group = wk.has_k + (queries ? kChunkRows * wk.cpt : 0);
-  {
-    const int32_t groups = (wk.T + kChunkRows - 1) / kChunkRows;
-    const int32_t last = wk.T - (groups - 1) * kChunkRows;  // tokens in the last group
-    wk.total = (groups - 1) * wk.per_group + wk.has_k + (queries ? last * wk.cpt : 0);
-  }
+  wk.cpt_div = make_fastdiv((uint32_t)wk.cpt);
+  wk.nk = keys ? (wk.T + kChunkRows - 1) / kChunkRows : 0;
+  wk.nq = queries ? wk.T * wk.cpt : 0;
+  const int64_t total = (int64_t)wk.nk + wk.nq;
   const int64_t resident = resident_ctas(rope_style);
   if (resident <= 0) return FP4IDX_ERR_CUDA;
-  const int64_t want = (wk.total + kWarps - 1) / kWarps;  // at least one item per warp
+  const int64_t want = (total + kWarps - 1) / kWarps;  // at least one item per warp
   const int64_t grid = want < resident ? want : resident;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (rope_style == FP4IDX_ROPE_NEOX)
