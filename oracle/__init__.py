@@ -65,6 +65,9 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.oracle_q_rope_pack_weights.argtypes = [
         P, P, P, P, P, i64, ctypes.c_int, P, P, P, i64, i64]
     L.oracle_q_rope_pack_weights.restype = ctypes.c_int
+    L.oracle_paged_mqa_logits.argtypes = [
+        P, P, P, P, i64, P, i64, P, P, i64, i64, i64, i64, i64]
+    L.oracle_paged_mqa_logits.restype = ctypes.c_int
     return L
 
 
@@ -216,3 +219,24 @@ def q_rope_pack_weights(q, w, positions, cos_cache, sin_cache, rope_style,
         _p(q), _p(w), _p(pos), _p(cs), _p(sn), cs.shape[0], int(rope_style),
         _p(qf), _p(qs), _p(wt), T, H)
     return qf, qs, wt, int(st)
+
+
+def paged_mqa_logits(q_fp4, q_scale, weights, kv_cache, block_table, context_lens,
+                     next_n: int, max_context: int):
+    """Returns (logits fp32 [B*next_n, max_context], status)."""
+    qf = _c(q_fp4, np.uint8)
+    qs = _c(q_scale, np.uint8)
+    wt = _c(weights, np.float32)
+    R, H, _ = qf.shape
+    assert qf.shape[2] == PAYLOAD_BYTES and qs.shape == (R, H, EXP_BYTES) and wt.shape == (R, H)
+    cache = _c(kv_cache, np.uint8)
+    assert cache.shape[1:] == (PAGE_BYTES,)
+    bt = _c(block_table, np.int32)
+    cl = _c(context_lens, np.int32)
+    B = cl.shape[0]
+    assert R == B * next_n and bt.shape[0] == B
+    out = np.empty((R, max_context), np.float32)
+    st = lib().oracle_paged_mqa_logits(
+        _p(qf), _p(qs), _p(wt), _p(cache), cache.shape[0], _p(bt), bt.shape[1], _p(cl),
+        _p(out), max_context, B, next_n, H, max_context)
+    return out, int(st)

@@ -293,3 +293,69 @@ int oracle_q_rope_pack_weights(const uint16_t* q, const uint16_t* w,
   }
   return status;
 }
+
+/* The scorer ([aiter] Verification, End-to-end: the FP4 paged MQA-logits
+ * scorer reads the kernel's own bytes; [vllm] Code Review: the scaled E2M1
+ * dot product of packed queries and packed keys with their per-32 block
+ * scales).  The DSA indexer score of a query row against a key is the
+ * head-weighted sum of ReLU'd dot products.  Readings (pages silent): no
+ * causal mask between the next_n rows of one sequence (every row scores
+ * [0, context_len)), -inf for the padding columns, and no extra scalar
+ * (the head weights already carry H^-1/2 D^-1/2). */
+static double dequant_d(uint8_t nibble, int e) {
+  double v = GRID[nibble & 7] * ldexp(1.0, e - 127);
+  return (nibble & 8) ? -v : v;
+}
+
+int oracle_paged_mqa_logits(const uint8_t* q_fp4, const uint8_t* q_scale,
+                            const float* weights, const uint8_t* kv_cache,
+                            int64_t num_blocks, const int32_t* block_table,
+                            int64_t block_table_stride,
+                            const int32_t* context_lens, float* logits,
+                            int64_t logits_stride, int64_t batch,
+                            int64_t next_n, int64_t num_heads,
+                            int64_t max_context) {
+  int status = 0;
+  double kv[HEAD_DIM], qv[HEAD_DIM];
+  for (int64_t b = 0; b < batch; ++b) {
+    int64_t ctx = context_lens[b];
+    for (int64_t j = 0; j < next_n; ++j) {
+      int64_t t = b * next_n + j;
+      for (int64_t s = 0; s < max_context; ++s) {
+        float* out = logits + t * logits_stride + s;
+        if (s >= ctx) {
+          *out = -INFINITY;
+          continue;
+        }
+        int64_t page = block_table[b * block_table_stride + s / KV_BLOCK];
+        if (page < 0 || page >= num_blocks) {
+          *out = -INFINITY;
+          status = -1;
+          continue;
+        }
+        const uint8_t* pg = kv_cache + page * PAGE_BYTES;
+        int64_t o = s % KV_BLOCK;
+        for (int d = 0; d < HEAD_DIM; ++d) {
+          uint8_t kbyte = pg[o * PAYLOAD_BYTES + d / 2];
+          uint8_t knib = (d % 2) ? (kbyte >> 4) : (kbyte & 15);
+          int ke = pg[KV_BLOCK * PAYLOAD_BYTES + o * EXP_BYTES + d / GROUP];
+          kv[d] = dequant_d(knib, ke);
+        }
+        double acc = 0.0;
+        for (int64_t h = 0; h < num_heads; ++h) {
+          int64_t r = t * num_heads + h;
+          for (int d = 0; d < HEAD_DIM; ++d) {
+            uint8_t qbyte = q_fp4[r * PAYLOAD_BYTES + d / 2];
+            uint8_t qnib = (d % 2) ? (qbyte >> 4) : (qbyte & 15);
+            qv[d] = dequant_d(qnib, q_scale[r * EXP_BYTES + d / GROUP]);
+          }
+          double dot = 0.0;
+          for (int d = 0; d < HEAD_DIM; ++d) dot += qv[d] * kv[d];
+          if (dot > 0.0) acc += (double)weights[r] * dot;
+        }
+        *out = (float)acc;
+      }
+    }
+  }
+  return status;
+}

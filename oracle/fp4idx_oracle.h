@@ -92,6 +92,24 @@ int oracle_q_rope_pack_weights(const uint16_t* q, const uint16_t* w,
                                float* weights, int64_t num_tokens,
                                int64_t num_heads);
 
+/* FP4 paged MQA-logits scorer (the consumer of the packed queries and the
+ * paged index-K cache).  Query row t = b*next_n + j of sequence b scores
+ * every cached token s < context_lens[b]:
+ *   logits[t, s] = sum_h weights[t,h] * max(0, sum_d q[t,h,d] * k_s[d])
+ * with q, k the dequantised FP4 values (grid value * 2^(e-127)) and k_s the
+ * slot at page block_table[b, s/64], offset s%64 (page-split layout).
+ * Positions context_lens[b] <= s < max_context get -inf.  Sums in double,
+ * rounded to fp32 once.  Returns 0, or -1 if a page index is out of range
+ * (those logits are -inf). */
+int oracle_paged_mqa_logits(const uint8_t* q_fp4, const uint8_t* q_scale,
+                            const float* weights, const uint8_t* kv_cache,
+                            int64_t num_blocks, const int32_t* block_table,
+                            int64_t block_table_stride,
+                            const int32_t* context_lens, float* logits,
+                            int64_t logits_stride, int64_t batch,
+                            int64_t next_n, int64_t num_heads,
+                            int64_t max_context);
+
 #ifdef __cplusplus
 }
 #endif

@@ -7,6 +7,7 @@ import pytest
 
 import oracle
 from tests import test_oracle_pins as pins
+from tests import test_scorer_oracle as spins
 
 # (name, text in the oracle source, replacement)
 MUTANTS = [
@@ -51,6 +52,20 @@ MUTANTS = [
     ("q_rope_skipped",
      "      oracle_rope_row(y, cos_cache + pos * (ROPE_DIM / 2),\n"
      "                      sin_cache + pos * (ROPE_DIM / 2), rope_style);\n", ""),
+    ("scorer_no_relu", "if (dot > 0.0) acc += (double)weights[r] * dot;",
+     "acc += (double)weights[r] * dot;"),
+    ("scorer_weight_dropped", "if (dot > 0.0) acc += (double)weights[r] * dot;",
+     "if (dot > 0.0) acc += dot;"),
+    ("scorer_slot_offset_off_by_one", "int64_t o = s % KV_BLOCK;\n        for (int d",
+     "int64_t o = (s + 1) % KV_BLOCK;\n        for (int d"),
+    ("scorer_key_group_exponent", "int ke = pg[KV_BLOCK * PAYLOAD_BYTES + o * EXP_BYTES + d / GROUP];",
+     "int ke = pg[KV_BLOCK * PAYLOAD_BYTES + o * EXP_BYTES + (d / GROUP + 1) % 4];"),
+    ("scorer_key_nibble_swap", "uint8_t knib = (d % 2) ? (kbyte >> 4) : (kbyte & 15);",
+     "uint8_t knib = (d % 2) ? (kbyte & 15) : (kbyte >> 4);"),
+    ("scorer_query_exponent_bias", "qv[d] = dequant_d(qnib, q_scale[r * EXP_BYTES + d / GROUP]);",
+     "qv[d] = dequant_d(qnib, q_scale[r * EXP_BYTES + d / GROUP] + 1);"),
+    ("scorer_padding_zero", "        if (s >= ctx) {\n          *out = -INFINITY;",
+     "        if (s >= ctx) {\n          *out = 0.0f;"),
     ("k_rope_skipped",
      "    oracle_rope_row(y, cos_cache + pos * (ROPE_DIM / 2),\n"
      "                    sin_cache + pos * (ROPE_DIM / 2), rope_style);\n", ""),
@@ -73,6 +88,12 @@ PINS = [
     pins.test_k_op_closed_form_composition,
     pins.test_q_op_closed_form_composition,
     pins.test_weights_closed_form,
+    spins.test_single_element_closed_form,
+    spins.test_heads_weighted_relu_sum,
+    spins.test_group_exponents_scale_the_score,
+    spins.test_page_indirection_and_sequences,
+    spins.test_bad_page_reported,
+    spins.test_random_case_exact_rational,
     pins.test_two_stage_invariants,
     pins.test_group_quant_exact_rational,
     pins.test_exponent_exhaustive_bf16,
