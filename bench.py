@@ -345,6 +345,73 @@ def time_e2e(F, w, D, mode, steps):
     return a.elapsed_time(b) / steps, h2d, d2h
 
 
+# ------------------------------------------------------------------ scorer
+def scorer_bytes(sw) -> int:
+    """Bytes one scorer launch must move at minimum: per cached token below
+    its context, its 68-byte slot; per used page, its 4-byte block-table
+    entry; per query row, 64 + 4 bytes of packed query and a 4-byte weight;
+    per sequence its context length; and the fp32 logits written, -inf
+    padding included (batch * next_n * max_context * 4)."""
+    ctx = np.minimum(np.maximum(sw.context_lens.astype(np.int64), 0), sw.max_context)
+    pages = -(-ctx // 64)
+    rows = sw.batch * sw.next_n
+    return int(ctx.sum() * 68 + pages.sum() * 4 + rows * sw.H * 72 + sw.batch * 4
+               + rows * sw.max_context * 4)
+
+
+def run_scorer(F, dev, peak, flush, steps: int, warmup: int = 5) -> dict:
+    """The FP4 paged MQA-logits scorer on the GLM-5.2-style decode workload:
+    CUDA-event time per launch (L2 flushed before each, outside the events)
+    and its HBM roofline."""
+    import torch
+    from fp4_sparse_attention_fp4idx_gb300 import workloads as wl
+    sw = wl.make_scorer_decode()
+
+    def d(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    qf, qs, wt, cache = d(sw.q_fp4), d(sw.q_scale), d(sw.weights), d(sw.kv_cache)
+    bt, ctx = d(sw.block_table), d(sw.context_lens)
+    rows = sw.batch * sw.next_n
+    out = torch.empty((rows, sw.max_context), dtype=torch.float32, device=dev)
+    for _ in range(warmup):
+        flush()
+        F.paged_mqa_logits(qf, qs, wt, cache, bt, ctx, sw.max_context, next_n=sw.next_n,
+                           logits=out)
+    torch.cuda.synchronize()
+    fn = F.lib().fp4idx_paged_mqa_logits
+    stream = torch.cuda.current_stream()
+    args = (qf.data_ptr(), qs.data_ptr(), wt.data_ptr(), cache.data_ptr(), sw.num_blocks,
+            bt.data_ptr(), bt.stride(0), ctx.data_ptr(), out.data_ptr(), out.stride(0),
+            sw.batch, sw.next_n, sw.H, sw.max_context, None, stream.cuda_stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for a, b in ev:
+        flush()
+        a.record(stream)
+        _ok(F, fn(*args))
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    nbytes = scorer_bytes(sw)
+    ctx_tokens = int(np.minimum(np.maximum(sw.context_lens, 0), sw.max_context).sum())
+    achieved = nbytes / (ms / 1e3) / 1e9
+    flops = 2.0 * 128 * sw.next_n * sw.H * ctx_tokens
+    return {
+        "workload": sw.name, "batch": sw.batch, "next_n": sw.next_n, "H": sw.H,
+        "max_context": sw.max_context, "cached_tokens": ctx_tokens,
+        "kv_cache_bytes": int(sw.kv_cache.nbytes), "launches": steps,
+        "ms_per_launch": round(ms, 5),
+        "scored_keys_per_s": round(ctx_tokens * sw.next_n / (ms / 1e3), 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "kernel": "scorer_kernel", "algorithmic_bytes_per_launch": nbytes,
+                     "traffic": None},
+        "mxf4_tflops": round(flops / (ms / 1e3) / 1e12, 1),
+        "l2": "flushed before every launch, outside the CUDA events",
+    }
+
+
 def cpu_baseline(w, budget_s: float = 12.0):
     """The oracle as it stands, single-threaded, on the first S tokens of the
     workload (keys and queries), S grown until about budget_s of CPU work."""
@@ -419,6 +486,10 @@ def run_ours(args):
                            "frac_of_peak": round(bx / (ms / 1e3) / 1e9 / peak, 4)}
             del Dx
 
+    scorer = None
+    if rank == 0 and not args.no_extra:
+        scorer = run_scorer(F, dev, peak, flush, 200)
+
     base = cpu_baseline(w) if (rank == 0 and ws == 1 and not args.no_cpu) else None
     if rank == 0:
         line = {
@@ -444,6 +515,7 @@ def run_ours(args):
             "cpu_baseline": base,
             "timed_wall_s": round(r["wall_s"], 4),
             "other_configs": extra,
+            "scorer": scorer,
         }
         if args.mode != "fused":
             line["k_ms"] = round(statistics.mean(r["k_ms"]), 5)

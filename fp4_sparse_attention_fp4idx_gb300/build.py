@@ -13,7 +13,7 @@ import sys
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SRC = os.path.join(PKG, "csrc", "fp4idx.cu")
+SRCS = [os.path.join(PKG, "csrc", name) for name in ("fp4idx.cu", "fp4idx_scorer.cu")]
 HDR = os.path.join(ROOT, "include", "fp4idx.h")
 LIB = os.path.join(PKG, "libfp4idx.so")
 
@@ -21,7 +21,7 @@ LIB = os.path.join(PKG, "libfp4idx.so")
 NVCC_FLAGS = [
     "-O3", "-std=c++17", "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo",
     "-fmad=false", "-ftz=false", "-prec-div=true", "-prec-sqrt=true",
-    "-Xcompiler", "-fPIC", "-shared",
+    "-Xcompiler", "-fPIC",
 ]
 
 
@@ -33,15 +33,30 @@ def nvcc() -> str:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    if (not force and os.path.exists(LIB)
-            and os.path.getmtime(LIB) >= max(os.path.getmtime(SRC), os.path.getmtime(HDR))):
+    newest = max(os.path.getmtime(f) for f in (*SRCS, HDR))
+    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= newest:
         return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *NVCC_FLAGS, "-I", os.path.join(ROOT, "include"), SRC, "-o", tmp]
-    if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
+    tag = f".tmp{os.getpid()}"
+    objs, procs = [], []
+    for src in SRCS:  # one translation unit per process, compiled in parallel
+        obj = os.path.join(PKG, os.path.basename(src) + tag + ".o")
+        cmd = [nvcc(), *NVCC_FLAGS, "-I", os.path.join(ROOT, "include"), "-c", src, "-o", obj]
+        if verbose:
+            cmd.insert(1, "-Xptxas=-v")
+        objs.append(obj)
+        procs.append((cmd, subprocess.Popen(cmd)))
+    try:
+        for cmd, proc in procs:
+            if proc.wait() != 0:
+                raise subprocess.CalledProcessError(proc.returncode, cmd)
+        tmp = LIB + tag
+        subprocess.run([nvcc(), "-shared", "-gencode", "arch=compute_103a,code=sm_103a", *objs,
+                        "-o", tmp], check=True)
+        os.replace(tmp, LIB)
+    finally:
+        for obj in objs:
+            if os.path.exists(obj):
+                os.remove(obj)
     return LIB
 
 

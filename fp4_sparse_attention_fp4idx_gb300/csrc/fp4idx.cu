@@ -996,6 +996,6 @@ const char* fp4idx_status_string(fp4idx_status status) {
   return "unknown status";
 }
 
-const char* fp4idx_version(void) { return "fp4idx 0.2.0 sm_103a"; }
+const char* fp4idx_version(void) { return "fp4idx 0.3.0 sm_103a"; }
 
 }  // extern "C"

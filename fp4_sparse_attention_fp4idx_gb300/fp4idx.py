@@ -30,6 +30,7 @@ PAGE_BYTES = 4352
 ERRFLAG_POSITION = 0x1
 ERRFLAG_SLOT = 0x2
 ERRFLAG_TIMEOUT = 0x4
+ERRFLAG_PAGE = 0x8
 
 OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_ARG, ERR_CUDA = range(6)
 
@@ -54,6 +55,8 @@ _SIGS = {
         _INT, [_P, _I64, _P, _F, _P, _P, _I64,
                _P, _I64, _I64, _P, _I64, _F, _P, _P, _P, _I64,
                _P, _P, _P, _I64, _INT, _I64, _P, _P]),
+    "fp4idx_paged_mqa_logits": (
+        _INT, [_P, _P, _P, _P, _I64, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _I64, _P, _P]),
     "fp4idx_status_string": (ctypes.c_char_p, [_INT]),
     "fp4idx_version": (ctypes.c_char_p, []),
 }
@@ -256,3 +259,51 @@ def indexer_prepass(k, gamma, slot_mapping, kv_cache, q, w, positions, cos_cache
         _stream_ptr(stream))
     _check(st, "fp4idx_indexer_prepass")
     return q_fp4, q_scale, weights
+
+
+def paged_mqa_logits(q_fp4, q_scale, weights, kv_cache, block_table, context_lens,
+                     max_context: int, *, next_n: int = 1, logits=None, err_flags=None,
+                     stream=None):
+    """FP4 paged MQA logits -> fp32 [batch*next_n, max_context].  q_fp4 uint8
+    [batch*next_n, H, 64], q_scale uint8 [batch*next_n, H, 4], weights fp32
+    [batch*next_n, H] (the pre-pass's query outputs), kv_cache uint8
+    [num_blocks, 4352], block_table int32 [batch, >= ceil(max_context/64)]
+    (unit column stride), context_lens int32 [batch]."""
+    torch = _torch()
+    _need(q_fp4, torch.uint8, "q_fp4", 3)
+    _need(q_scale, torch.uint8, "q_scale", 3)
+    _need(weights, torch.float32, "weights", 2)
+    _need(kv_cache, torch.uint8, "kv_cache", 2)
+    _need(block_table, torch.int32, "block_table", 2)
+    _need(context_lens, torch.int32, "context_lens", 1)
+    T, H, nb = q_fp4.shape
+    if nb != 64 or not q_fp4.is_contiguous():
+        raise ValueError("q_fp4 must be contiguous [batch*next_n, H, 64]")
+    if tuple(q_scale.shape) != (T, H, 4) or not q_scale.is_contiguous():
+        raise ValueError("q_scale must be contiguous [batch*next_n, H, 4]")
+    if tuple(weights.shape) != (T, H) or not weights.is_contiguous():
+        raise ValueError("weights must be contiguous [batch*next_n, H]")
+    if next_n < 1 or T % next_n:
+        raise ValueError("the query rows must be batch*next_n")
+    batch = T // next_n
+    if block_table.shape[0] != batch or block_table.stride(1) != 1:
+        raise ValueError("block_table must be [batch, pages] with unit column stride")
+    if context_lens.shape[0] != batch or not context_lens.is_contiguous():
+        raise ValueError("context_lens must be contiguous [batch]")
+    if kv_cache.shape[1] != PAGE_BYTES or not kv_cache.is_contiguous():
+        raise ValueError("kv_cache must be contiguous [num_blocks, 4352]")
+    if logits is None:
+        logits = torch.empty((T, max_context), dtype=torch.float32, device=q_fp4.device)
+    _need(logits, torch.float32, "logits", 2)
+    if logits.shape[0] != T or logits.shape[1] < max_context or logits.stride(1) != 1:
+        raise ValueError("logits must be [batch*next_n, >= max_context] with unit column stride")
+    # A size-1 leading dimension may carry any stride (numpy gives 0 to a
+    # new axis); the row width is the stride the C ABI's checks expect then.
+    bt_stride = block_table.stride(0) if batch > 1 else block_table.shape[1]
+    out_stride = logits.stride(0) if T > 1 else logits.shape[1]
+    st = _lib.fp4idx_paged_mqa_logits(
+        _ptr(q_fp4), _ptr(q_scale), _ptr(weights), _ptr(kv_cache), kv_cache.shape[0],
+        _ptr(block_table), bt_stride, _ptr(context_lens), _ptr(logits), out_stride, batch,
+        next_n, H, int(max_context), _ptr(err_flags), _stream_ptr(stream))
+    _check(st, "fp4idx_paged_mqa_logits")
+    return logits

@@ -299,3 +299,122 @@ def make(name: str) -> Workload:
     if name == "tiny_gamma1":
         return make_tiny(gamma_one=True)
     return CONFIGS[name]()
+
+
+# ------------------------------------------------------------------ scorer
+@dataclass
+class ScorerWorkload:
+    """Inputs of the FP4 paged MQA-logits scorer: packed queries with their
+    exponent words and fp32 head weights (what the query half of the pre-pass
+    emits) and a paged index-K cache (what the key half writes), drawn
+    directly as bytes."""
+    name: str
+    batch: int
+    next_n: int
+    H: int
+    max_context: int
+    q_fp4: np.ndarray         # uint8 [batch*next_n, H, 64]
+    q_scale: np.ndarray       # uint8 [batch*next_n, H, 4]
+    weights: np.ndarray       # f32 [batch*next_n, H]
+    kv_cache: np.ndarray      # uint8 [num_blocks, 4352]
+    block_table: np.ndarray   # int32 [batch, pages]; -1 past each context
+    context_lens: np.ndarray  # int32 [batch]
+    notes: dict = field(default_factory=dict)
+
+    @property
+    def num_blocks(self) -> int:
+        return int(self.kv_cache.shape[0])
+
+    def rows_of(self, seqs) -> "ScorerWorkload":
+        """The same inputs restricted to the given sequences (for sampled
+        oracle checks at full size); the cache is shared, not copied."""
+        seqs = np.asarray(seqs)
+        rows = (seqs[:, None] * self.next_n + np.arange(self.next_n)[None, :]).reshape(-1)
+        return ScorerWorkload(self.name, len(seqs), self.next_n, self.H, self.max_context,
+                              self.q_fp4[rows], self.q_scale[rows], self.weights[rows],
+                              self.kv_cache, self.block_table[seqs], self.context_lens[seqs],
+                              dict(self.notes, rows=rows))
+
+
+def make_scorer(name: str, batch: int, next_n: int, H: int, context_lens, max_context: int,
+                seed: int, exp_range=(118, 135), spare_blocks: int = 3,
+                extremes: bool = False) -> ScorerWorkload:
+    """Uniform random payload nibbles (every E2M1 code, both signs, -0
+    included), exponent bytes uniform in exp_range, weights ~ N(0,1) *
+    (H*128)^-1/2.  Pages are a random permutation of the pool; block-table
+    entries past a sequence's context are -1 and must never be read.  With
+    `extremes`, some key groups are all-zero at the floor exponent 1 (what the
+    pre-pass writes for a zero group), some sit at exponent 1 with non-zero
+    codes (values 2^-127 .. 6*2^-126), and some use exponents 150..160."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    ctx = np.asarray(context_lens, dtype=np.int32)
+    assert ctx.shape == (batch,)
+    pages_needed = [max(0, -(-int(min(c, max_context)) // KV_BLOCK)) for c in ctx]
+    num_blocks = sum(pages_needed) + spare_blocks
+    width = max(1, -(-max_context // KV_BLOCK))
+    perm = rng.permutation(num_blocks).astype(np.int32)
+    bt = np.full((batch, width), -1, dtype=np.int32)
+    at = 0
+    for b, n in enumerate(pages_needed):
+        bt[b, :n] = perm[at:at + n]
+        at += n
+    lo, hi = exp_range
+    cache = rng.integers(0, 256, size=(num_blocks, PAGE_BYTES), dtype=np.uint8)
+    cache[:, KV_BLOCK * 64:] = rng.integers(lo, hi + 1, size=(num_blocks, KV_BLOCK * 4),
+                                            dtype=np.uint8)
+    rows = batch * next_n
+    q_fp4 = rng.integers(0, 256, size=(rows, H, 64), dtype=np.uint8)
+    q_scale = rng.integers(lo, hi + 1, size=(rows, H, 4), dtype=np.uint8)
+    weights = (rng.standard_normal((rows, H)) / np.sqrt(H * HEAD_DIM)).astype(np.float32)
+    if extremes:
+        n_tok = num_blocks * KV_BLOCK
+        for kind in range(3):
+            picks = rng.choice(n_tok, size=max(1, n_tok // 16), replace=False)
+            for tok in picks:
+                page, o = divmod(int(tok), KV_BLOCK)
+                g = int(rng.integers(0, 4))
+                payload = cache[page, o * 64 + 16 * g:o * 64 + 16 * g + 16]
+                if kind == 0:
+                    payload[:] = 0
+                    cache[page, KV_BLOCK * 64 + 4 * o + g] = 1
+                elif kind == 1:
+                    cache[page, KV_BLOCK * 64 + 4 * o + g] = 1
+                else:
+                    cache[page, KV_BLOCK * 64 + 4 * o + g] = rng.integers(150, 161)
+    return ScorerWorkload(name, batch, next_n, H, max_context, q_fp4, q_scale, weights, cache,
+                          bt, ctx, {"seed": seed, "exp_range": exp_range,
+                                    "extremes": extremes})
+
+
+def _ragged_lens(rng, batch: int, lo: int, hi: int) -> np.ndarray:
+    return rng.integers(lo, hi + 1, size=batch).astype(np.int32)
+
+
+def make_scorer_decode(batch: int = 128, next_n: int = 4, H: int = 32,
+                       max_context: int = 65536, seed: int = 21) -> ScorerWorkload:
+    """GLM-5.2-style decode with multi-token prediction: H = 32 index heads,
+    next_n = 4 query tokens per sequence, 128 sequences with context lengths
+    uniform in [max_context/4, max_context] (about 5.2M cached tokens, 350 MB
+    of index-K cache, 134 MB of logits)."""
+    rng = np.random.Generator(np.random.PCG64(seed + 1000))
+    lens = _ragged_lens(rng, batch, max_context // 4, max_context)
+    return make_scorer("scorer_decode", batch, next_n, H, lens, max_context, seed)
+
+
+SCORER_CONFIGS = {
+    # name: (batch, next_n, H, context_lens, max_context, seed, extremes)
+    "scorer_tiny": (3, 1, 32, [0, 1, 200], 260, 31, True),
+    "scorer_glm_next1": (5, 1, 32, [64, 127, 129, 700, 1000], 1024, 32, True),
+    "scorer_glm_next4": (4, 4, 32, [1, 255, 256, 777], 800, 33, False),
+    "scorer_dsv_next1": (3, 1, 64, [300, 64, 513], 520, 34, True),
+    "scorer_dsv_next2": (3, 2, 64, [128, 5, 640], 700, 35, False),
+    "scorer_r96": (2, 3, 32, [450, 200], 450, 36, False),
+    "scorer_h128": (2, 1, 128, [333, 129], 384, 37, True),
+}
+
+
+def make_scorer_config(name: str) -> ScorerWorkload:
+    if name == "scorer_decode":
+        return make_scorer_decode()
+    b, n, h, lens, mc, seed, ext = SCORER_CONFIGS[name]
+    return make_scorer(name, b, n, h, lens, mc, seed, extremes=ext)

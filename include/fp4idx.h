@@ -4,6 +4,7 @@
  * GB300 GPU (sm_103a).
  *
  * What it computes (sources are web pages, cited by title and section):
+ *   (the pre-pass; the FP4 scorer that reads its bytes is declared last)
  *   "dsv4.1: RoPE and FP4 packing kernels" (sglang PR 39656), Summary: keys
  *   get RMSNorm, RoPE, two quantisation stages to the per-32 UE8M0 E2M1 grid
  *   (round half to even) and a paged-cache store of the 68-byte index-K slot
@@ -95,6 +96,9 @@ enum {
 #define FP4IDX_ERRFLAG_TIMEOUT 0x4u  /* an input copy did not arrive within
                                         1 s; that warp's remaining rows were
                                         left unwritten                       */
+#define FP4IDX_ERRFLAG_PAGE 0x8u     /* scorer: a block-table entry outside
+                                        [0, num_blocks) for a token below its
+                                        context length; its logits are -inf */
 
 /*
  * Keys: RMSNorm -> RoPE -> two-stage FP4 -> 68-byte slot -> paged cache.
@@ -175,6 +179,58 @@ fp4idx_status fp4idx_indexer_prepass(
     const int64_t* positions, const float* cos_cache, const float* sin_cache,
     int64_t max_pos, int rope_style, int64_t num_tokens, uint32_t* err_flags,
     void* stream);
+
+/*
+ * FP4 paged MQA-logits scorer: the consumer of the bytes written above.
+ * Sources: "[HIP] Add FP4 output mode to indexer_qk_rope_quant_and_cache"
+ * (aiter PR 5484), Verification (the paged FP4 MQA-logits scorer reads the
+ * packed keys and their e8m0 exponents from the paged cache; GLM-5.2 shapes
+ * H = 32, kv_block 64, next_n 1 and 4); "[ROCm][Perf] Enabled FP4Indexer for
+ * DSV4" (vLLM PR 42908), Code Review (block-scaled E2M1 dot products of
+ * packed queries and keys, ReLU, head weights, sum over heads).
+ *
+ * Query row t = b*next_n + j (sequence b, its j-th query token) scores every
+ * cached token s of sequence b:
+ *   logits[t, s] = sum_h weights[t,h] * max(0, sum_d q[t,h,d] * k_s[d])
+ *     for s < min(context_lens[b], max_context),
+ *   logits[t, s] = -inf for context_lens[b] <= s < max_context,
+ * with q and k the FP4 values (E2M1 grid value * 2^(e-127), e the row's
+ * exponent byte for the group d/32) and k_s the slot of token s: page
+ * block_table[b, s/64], offset s%64, in the layout fp4idx_k_norm_rope_pack_store
+ * writes.  The products are exact; sums are fp32 (tensor-core accumulation
+ * over d, then the weighted head sum in two interleaved chains), so a logit
+ * is within 2^-17 * sum_h |weights[t,h]| * sum_d |q[t,h,d] k_s[d]| of the
+ * exact value (a bound from the fp32 rounding of at most 128 head terms and
+ * 128 products).
+ *
+ *   q_fp4        bytes [batch*next_n, num_heads, 64], dense, 16-byte aligned
+ *                (the q_fp4 output of the calls above).
+ *   q_scale      bytes [batch*next_n, num_heads, 4], dense, 4-byte aligned.
+ *   weights      fp32 [batch*next_n, num_heads], dense.
+ *   kv_cache     bytes [num_blocks, 4352], 16-byte aligned, read only.
+ *                Exponent bytes must be <= 254 (255 is NaN on the tensor
+ *                core); the pre-pass writes 1..252.
+ *   block_table  int32, entry (b, p) at b*block_table_stride + p; read for
+ *                p < ceil(min(context_lens[b], max_context) / 64) only.
+ *                block_table_stride >= ceil(max_context / 64).
+ *   context_lens int32 [batch]; values < 0 count as 0.
+ *   logits       fp32, row t at logits + t*logits_stride, columns
+ *                [0, max_context) written, the rest untouched;
+ *                logits_stride >= max_context.
+ *   batch >= 0, next_n >= 1, num_heads a multiple of 32,
+ *   next_n * num_heads <= 128, 0 <= max_context < 2^30.
+ *   err_flags    optional device uint32: FP4IDX_ERRFLAG_PAGE for a bad
+ *                block-table entry (those logits are -inf, nothing is read),
+ *                FP4IDX_ERRFLAG_TIMEOUT if a copy or the tensor core did not
+ *                finish within 1 s (that CTA's remaining logits unwritten).
+ * batch == 0 or max_context == 0 returns FP4IDX_OK and enqueues nothing.
+ */
+fp4idx_status fp4idx_paged_mqa_logits(
+    const uint8_t* q_fp4, const uint8_t* q_scale, const float* weights,
+    const uint8_t* kv_cache, int64_t num_blocks, const int32_t* block_table,
+    int64_t block_table_stride, const int32_t* context_lens, float* logits,
+    int64_t logits_stride, int64_t batch, int64_t next_n, int64_t num_heads,
+    int64_t max_context, uint32_t* err_flags, void* stream);
 
 /* Static, NUL-terminated description of a status code. */
 const char* fp4idx_status_string(fp4idx_status status);

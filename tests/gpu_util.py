@@ -108,3 +108,60 @@ def assert_same(w: wl.Workload, gpu, ref, tokens=None):
     assert_bytes_equal(qf, rqf, f"{w.name} q_fp4")
     assert_bytes_equal(qs, rqs, f"{w.name} q_scale")
     assert_weights(wt, rwt, f"{w.name} weights")
+
+
+# ------------------------------------------------------------------ scorer
+# A logit's fp32 error bound: 2^-17 * sum_h |w| * sum_d |q k| (the header's
+# contract for fp4idx_paged_mqa_logits: fp32 rounding of <= 128 products in
+# the tensor core and <= 128 weighted head terms, each <= 2^-24 relative).
+SCORER_TOL = 2.0 ** -17
+
+
+class DeviceScorer:
+    def __init__(self, sw: wl.ScorerWorkload, device="cuda"):
+        self.sw = sw
+        self.q_fp4 = dev(sw.q_fp4, device)
+        self.q_scale = dev(sw.q_scale, device)
+        self.weights = dev(sw.weights, device)
+        self.cache = dev(sw.kv_cache, device)
+        self.bt = dev(sw.block_table, device)
+        self.ctx = dev(sw.context_lens, device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def run(self, logits=None):
+        out = F().paged_mqa_logits(self.q_fp4, self.q_scale, self.weights, self.cache, self.bt,
+                                   self.ctx, self.sw.max_context, next_n=self.sw.next_n,
+                                   logits=logits, err_flags=self.err)
+        torch.cuda.synchronize()
+        return out
+
+
+def scorer_oracle(sw: wl.ScorerWorkload):
+    return oracle.paged_mqa_logits(sw.q_fp4, sw.q_scale, sw.weights, sw.kv_cache,
+                                   sw.block_table, sw.context_lens, sw.next_n, sw.max_context)
+
+
+def scorer_magnitude(sw: wl.ScorerWorkload) -> np.ndarray:
+    """sum_h |w| * sum_d |q k| per logit: the oracle on sign-cleared inputs
+    (every dot product is then >= 0, so ReLU passes it unchanged)."""
+    cache = sw.kv_cache.copy()
+    cache[:, :wl.KV_BLOCK * 64] &= 0x77
+    out, _ = oracle.paged_mqa_logits(sw.q_fp4 & 0x77, sw.q_scale, np.abs(sw.weights), cache,
+                                     sw.block_table, sw.context_lens, sw.next_n,
+                                     sw.max_context)
+    return out
+
+
+def assert_logits_close(got: np.ndarray, want: np.ndarray, mag: np.ndarray, what: str):
+    assert got.shape == want.shape, (what, got.shape, want.shape)
+    ninf_w, ninf_g = np.isneginf(want), np.isneginf(got)
+    assert np.array_equal(ninf_w, ninf_g), (what, "-inf pattern differs",
+                                            np.argwhere(ninf_w != ninf_g)[:5])
+    fin = ~ninf_w
+    assert np.all(np.isfinite(got[fin])), (what, "non-finite logits")
+    err = np.abs(got[fin].astype(np.float64) - want[fin].astype(np.float64))
+    lim = SCORER_TOL * mag[fin].astype(np.float64)
+    bad = err > lim
+    assert not bad.any(), (what, int(bad.sum()), float(err[bad].max()),
+                           np.argwhere(fin)[np.flatnonzero(bad)[:5]].tolist())
+    return float((err / np.maximum(mag[fin], 1e-300)).max()) if err.size else 0.0

@@ -28,7 +28,8 @@ def F():
 def test_exports_every_declared_symbol(F):
     names = F.declared_symbols()
     assert set(names) == {"fp4idx_k_norm_rope_pack_store", "fp4idx_q_rope_pack_weights",
-                          "fp4idx_indexer_prepass", "fp4idx_status_string", "fp4idx_version"}
+                          "fp4idx_indexer_prepass", "fp4idx_paged_mqa_logits",
+                          "fp4idx_status_string", "fp4idx_version"}
     out = subprocess.run(["nm", "-D", "--defined-only", F.LIB_PATH], capture_output=True,
                          text=True, check=True).stdout
     exported = set(re.findall(r"\bT (fp4idx_\w+)", out))
@@ -193,12 +194,64 @@ def test_fused_host_checks_queries(F, over, code):
     assert _call_fused(F, _k_args(), _q_args(**over)) == getattr(F, code)
 
 
+def _s_args(**over):
+    a = dict(qf=A[12], qs=A[13], w=A[14], cache=A[6], nb=16, bt=A[15], bts=8, ctx=A[16],
+             out=A[17], os=512, batch=4, next_n=1, H=32, max_ctx=500, err=None, stream=None)
+    a.update(over)
+    return a
+
+
+def _call_s(F, a):
+    return F.lib().fp4idx_paged_mqa_logits(
+        a["qf"], a["qs"], a["w"], a["cache"], a["nb"], a["bt"], a["bts"], a["ctx"], a["out"],
+        a["os"], a["batch"], a["next_n"], a["H"], a["max_ctx"], a["err"], a["stream"])
+
+
+S_DEFECTS = [
+    (dict(batch=-1), "ERR_SHAPE"),
+    (dict(max_ctx=-1), "ERR_SHAPE"),
+    (dict(qf=None), "ERR_NULL"),
+    (dict(qs=None), "ERR_NULL"),
+    (dict(w=None), "ERR_NULL"),
+    (dict(cache=None), "ERR_NULL"),
+    (dict(bt=None), "ERR_NULL"),
+    (dict(ctx=None), "ERR_NULL"),
+    (dict(out=None), "ERR_NULL"),
+    (dict(next_n=0), "ERR_SHAPE"),
+    (dict(H=16), "ERR_SHAPE"),
+    (dict(H=48), "ERR_SHAPE"),
+    (dict(H=64, next_n=3), "ERR_SHAPE"),
+    (dict(H=160), "ERR_SHAPE"),
+    (dict(nb=0), "ERR_SHAPE"),
+    (dict(nb=1 << 40), "ERR_SHAPE"),
+    (dict(max_ctx=1 << 30), "ERR_SHAPE"),
+    (dict(os=499), "ERR_SHAPE"),
+    (dict(bts=7), "ERR_SHAPE"),
+    (dict(qf=A[12] + 4), "ERR_ALIGN"),
+    (dict(qs=A[13] + 2), "ERR_ALIGN"),
+    (dict(w=A[14] + 2), "ERR_ALIGN"),
+    (dict(cache=A[6] + 8), "ERR_ALIGN"),
+    (dict(bt=A[15] + 2), "ERR_ALIGN"),
+    (dict(ctx=A[16] + 1), "ERR_ALIGN"),
+    (dict(out=A[17] + 2), "ERR_ALIGN"),
+    (dict(err=A[11] + 2), "ERR_ALIGN"),
+]
+
+
+@pytest.mark.fake_ptr
+@pytest.mark.parametrize("over,code", S_DEFECTS, ids=_ids(S_DEFECTS))
+def test_scorer_host_checks(F, over, code):
+    assert _call_s(F, _s_args(**over)) == getattr(F, code)
+
+
 @pytest.mark.fake_ptr
 def test_zero_tokens_is_ok_without_touching_cuda(F):
     # All pointers NULL, T == 0: returns OK before any check or CUDA call.
     assert _call_k(F, _k_args(T=0, k=None, gamma=None, cache=None)) == F.OK
     assert _call_q(F, _q_args(T=0, q=None, w=None)) == F.OK
     assert _call_fused(F, _k_args(T=0), _q_args(T=0)) == F.OK
+    assert _call_s(F, _s_args(batch=0, qf=None, cache=None)) == F.OK
+    assert _call_s(F, _s_args(max_ctx=0, out=None)) == F.OK
 
 
 def test_binding_fails_loudly_without_the_library(tmp_path):
