@@ -15,23 +15,39 @@
 //   "dsv4.1: RoPE and FP4 packing kernels" (sglang PR 39656), Summary: the
 //   68-byte slot (64 payload bytes + 4 exponent bytes).
 //
-// Design.  A CTA (4 warps) owns one sequence b and a contiguous range of
-// 128-token key tiles; a tile is two 64-slot cache pages.  The MMA has the
-// keys as A (M = 128 tokens) and the sequence's R = next_n * H query rows as
-// B (N = R), K = 128 as two MMAs of K = 64:
-//   - the page payloads (64 tokens x 64 bytes) arrive by TMA tensor copies in
-//     the 64-byte swizzled layout the MMA reads, and the exponent words by a
-//     bulk copy, into a ring of stages (one mbarrier each);
-//   - each exponent word is exactly one TMEM scale-factor cell: group g sits
-//     in byte g, and the MMA over groups {0,1} takes bytes 0-1 (scale-factor
-//     id 0), the one over {2,3} bytes 2-3 (id 2).  Row r's cell is TMEM
-//     column base + r/32; the key side reads lane r, the query side lane
-//     r%32 (written to every lane quadrant);
-//   - the accumulator D[token, query row] (R fp32 columns) stays in TMEM;
-//     thread t of the CTA owns token t of the tile (TMEM lane t) and forms
-//     sum_h w * max(D, 0) for each of the next_n query tokens in registers,
-//     so the head sum needs no data exchange between threads.
-// Each E2M1 product is exact; the tensor core accumulates in fp32.
+// Work.  A tile is 128 consecutive tokens (two 64-slot pages) of one
+// sequence; only tiles holding a token below the sequence's context are
+// work.  The persistent grid splits the list of all work tiles (sequence by
+// sequence) into equal contiguous shares, one per CTA, from the context
+// lengths alone; a CTA's share may span several sequences ("segments").
+// Logits of tiles past the context are -inf, written in a final phase.
+//
+// MMA.  Keys are A (M = 128 tokens), the sequence's R = next_n * H query rows
+// are B (N = R), K = 128 as two MMAs of K = 64.  Each exponent word of a slot
+// is exactly one TMEM scale-factor cell: group g sits in byte g; the MMA over
+// groups {0,1} takes bytes 0-1 (scale-factor id 0), the one over {2,3} bytes
+// 2-3 (id 2).  Row r's cell is TMEM column base + r/32; the key side reads
+// lane r, the query side lane r%32 (written to every lane quadrant).
+//
+// Roles (10 warps).
+//   producer (warp 8): TMA tensor copies of the page payloads (64 tokens x
+//     64 bytes, in the 64-byte swizzled layout the MMA reads) and bulk copies
+//     of the exponent words into a ring of S stages;
+//   MMA issuer (warp 9): two MMAs per tile into one of two TMEM
+//     accumulators, committed to the accumulator's "full" barrier and the
+//     stage's "empty" barrier;
+//   two epilogue groups (warps 0-3, 4-7), group e owning the tiles k with
+//     k % 2 == e and accumulator e: for its tile it writes the keys' scale
+//     words into TMEM (and, at the first tile of a segment, the segment's
+//     query operand and scale words), then reads the accumulator (thread =
+//     token = TMEM lane), releases it, and forms sum_h w * max(D, 0) per
+//     query token in registers.  Each warp holds its own copy of the
+//     segment's head weights, so no warp waits on another except through
+//     bounded mbarrier waits.  One group's epilogue overlaps the other
+//     group's MMA.
+// Every wait is bounded (1 s) and a shared abort flag stops every role; in
+// flight copies and MMAs are waited for before TMEM and shared memory are
+// released.  Each E2M1 product is exact; the tensor core accumulates in fp32.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -42,16 +58,19 @@
 
 namespace {
 
-constexpr int kThreads = 128;          // 4 warps = the 128 TMEM lanes
-constexpr int kTile = 128;             // key tokens per tile (MMA M)
+constexpr int kEpiWarps = 8;                 // two groups of four
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 10 * 32;
+constexpr int kTile = 128;                   // key tokens per tile (MMA M)
 constexpr int kKvBlock = FP4IDX_KV_BLOCK;
 constexpr int kPageBytes = FP4IDX_PAGE_BYTES;
 constexpr int kPayloadBytes = kKvBlock * FP4IDX_SLOT_PAYLOAD_BYTES;  // 4096
 constexpr int kExpBytes = kKvBlock * FP4IDX_SLOT_EXP_BYTES;          // 256
 constexpr int kStageA = 2 * kPayloadBytes;                           // 8192
 constexpr int kStageE = 2 * kExpBytes;                               // 512
-constexpr int kMaxRows = 128;          // query rows per sequence (MMA N)
-constexpr int kMaxStages = 12;
+constexpr int kMaxRows = 128;                // query rows per sequence (MMA N)
+constexpr int kMaxStages = 16;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
 struct ScorerParams {
@@ -66,32 +85,39 @@ struct ScorerParams {
   int64_t num_blocks;
   int64_t bt_stride;
   int64_t logits_stride;
+  int32_t batch;
   int32_t next_n;
   int32_t H;
   int32_t R;
   int32_t max_context;
-  int32_t tiles;           // ceil(max_context / 128)
-  int32_t tiles_per_cta;
-  int32_t splits;          // CTAs per sequence
+  int32_t tiles_total;     // ceil(max_context / 128) tiles per sequence
   int32_t stages;
-  uint32_t tmem_cols;      // power of two >= R + 12
+  uint32_t tmem_cols;      // power of two >= 2R + 32
 };
 
 // Shared-memory carve-up (offsets from a 1024-byte aligned base).
 struct Layout {
-  uint32_t a, b, e, w, bars, ok, tmem_slot, total;
+  uint32_t a, q, e, w, bars, ok, misc, scan, total;
 };
 
-__host__ __device__ inline Layout make_layout(int stages, int R) {
+// Barrier indices: full[S], empty[S], sfa_ready[2], acc_full[2], acc_empty[2].
+__host__ __device__ inline int bar_full(int s) { return s; }
+__host__ __device__ inline int bar_empty(int S, int s) { return S + s; }
+__host__ __device__ inline int bar_sfa(int S, int e) { return 2 * S + e; }
+__host__ __device__ inline int bar_accf(int S, int e) { return 2 * S + 2 + e; }
+__host__ __device__ inline int bar_acce(int S, int e) { return 2 * S + 4 + e; }
+
+__host__ __device__ inline Layout make_layout(int S, int R) {
   Layout L;
-  L.a = 0;                                              // stages x 8192, swizzled
-  L.b = L.a + (uint32_t)stages * kStageA;               // R x 64, swizzled
-  L.e = L.b + (uint32_t)R * 64;                         // stages x 512
-  L.w = L.e + (uint32_t)stages * kStageE;               // R floats
-  L.bars = (L.w + (uint32_t)R * 4 + 7u) & ~7u;          // stages + 1 mbarriers
-  L.ok = L.bars + 8u * (uint32_t)(stages + 1);          // stages words
-  L.tmem_slot = L.ok + 4u * (uint32_t)stages;
-  L.total = L.tmem_slot + 4u;
+  L.a = 0;                                     // S x 8192, swizzled payloads
+  L.q = L.a + (uint32_t)S * kStageA;           // 2 x R x 64, swizzled queries
+  L.e = L.q + 2u * (uint32_t)R * 64;           // S x 512 exponent words
+  L.w = L.e + (uint32_t)S * kStageE;           // 8 epilogue warps x R weights
+  L.bars = L.w + (uint32_t)kEpiWarps * R * 4;  // 2S + 6 mbarriers
+  L.ok = L.bars + 8u * (uint32_t)(2 * S + 6);  // S page masks
+  L.misc = L.ok + 4u * (uint32_t)S;            // tmem base, abort, b/t/n start
+  L.scan = L.misc + 32;                        // kThreads + 1 partial sums (int64)
+  L.total = L.scan + 8u * (kThreads + 1);
   return L;
 }
 
@@ -117,15 +143,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete; gives up after 1 s.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// Waits for the phase with the given parity to complete.  Gives up (false)
+// when another role has raised *abort, or after 1 s, raising *abort itself.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
+                                           volatile uint32_t* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (;;) {
-    for (int k = 0; k < 16; ++k)
+    for (int k = 0; k < 8; ++k)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+    if (*abort) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      *abort = 1u;
+      return false;
+    }
   }
+}
+
+// The same wait with no abort flag: used while draining after an abort.
+__device__ __forceinline__ void wait_phase_drain(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > kWaitLimitNs) return;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 // Shared-memory matrix descriptor of a K-major operand in the 64-byte
@@ -163,6 +206,12 @@ __device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64
       : "memory");
 }
 
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
@@ -172,8 +221,8 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
         "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      : "r"(taddr)
+      : "memory");
 }
 
 // Packed fp32 pair: (a.x * b.x + c.x, a.y * b.y + c.y), each rounded once.
@@ -190,227 +239,332 @@ __device__ __forceinline__ void flag_error(uint32_t* err, uint32_t bit) {
   if (err != nullptr) atomicOr(err, bit);
 }
 
-// -inf for every column of tiles [t0, t1) below max_context.
-__device__ void write_padding(const ScorerParams& p, int b, int t0, int t1) {
-  for (int t = t0; t < t1; ++t) {
-    const int s = t * kTile + (int)threadIdx.x;
-    if (s >= p.max_context) continue;
-    for (int j = 0; j < p.next_n; ++j)
-      p.logits[((int64_t)b * p.next_n + j) * p.logits_stride + s] = -INFINITY;
-  }
+__device__ __forceinline__ int ctx_eff(const ScorerParams& p, int b) {
+  return min(max(__ldg(p.ctx_lens + b), 0), p.max_context);
 }
 
-__global__ void __launch_bounds__(kThreads) scorer_kernel(const __grid_constant__ ScorerParams p,
-                                                          const __grid_constant__ CUtensorMap tmap) {
-  extern __shared__ uint8_t smem_raw[];
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int b = blockIdx.x / p.splits;
-  const int split = blockIdx.x - b * p.splits;
-  const int t_lo = split * p.tiles_per_cta;
-  const int t_hi = min(p.tiles, t_lo + p.tiles_per_cta);
-  if (t_lo >= t_hi) return;  // uniform over the CTA
-  const int ctx = min(max(__ldg(p.ctx_lens + b), 0), p.max_context);
-  const int work_hi = min(t_hi, (ctx + kTile - 1) / kTile);  // tiles holding a token < ctx
-  if (work_hi <= t_lo) {  // nothing to score: padding only
-    write_padding(p, b, t_lo, t_hi);
-    return;
-  }
-  const int nwork = work_hi - t_lo;
+__device__ __forceinline__ int work_tiles(int ctx) { return (ctx + kTile - 1) / kTile; }
 
+// Walks a CTA's tiles in order: sequence b, tile t, its context, and the
+// segment index g (how many times b has changed since the first tile).
+struct Walker {
+  int b, t, ctx, g;
+  __device__ void init(const ScorerParams& p, int b0, int t0) {
+    b = b0;
+    t = t0;
+    ctx = ctx_eff(p, b0);
+    g = 0;
+  }
+  __device__ void advance(const ScorerParams& p) {
+    ++t;
+    while (t >= work_tiles(ctx) && b + 1 < p.batch) {
+      ++b;
+      t = 0;
+      ctx = ctx_eff(p, b);
+      ++g;
+    }
+  }
+};
+
+template <int NCHUNK>
+__global__ void __launch_bounds__(kThreads, 1)
+    scorer_kernel(const __grid_constant__ ScorerParams p, const __grid_constant__ CUtensorMap tmap) {
+  extern __shared__ uint8_t smem_raw[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = p.stages, R = p.R;
   uint8_t* const smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const Layout L = make_layout(p.stages, p.R);
+  const Layout L = make_layout(S, R);
   uint8_t* const sA = smem + L.a;
-  uint8_t* const sB = smem + L.b;
+  uint8_t* const sQ = smem + L.q;
   uint8_t* const sE = smem + L.e;
   float* const sW = reinterpret_cast<float*>(smem + L.w);
-  const uint32_t bars = smem_addr(smem + L.bars);  // full[0..S-1], then the MMA barrier
-  const uint32_t mma_bar = bars + 8u * (uint32_t)p.stages;
+  const uint32_t bars = smem_addr(smem + L.bars);
   volatile uint32_t* const stage_ok = reinterpret_cast<volatile uint32_t*>(smem + L.ok);
-  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(smem + L.tmem_slot);
+  uint32_t* const misc = reinterpret_cast<uint32_t*>(smem + L.misc);
+  volatile uint32_t* const abort = misc + 1;
+  int32_t* const start = reinterpret_cast<int32_t*>(misc + 2);  // b, t, n
+  long long* const scan = reinterpret_cast<long long*>(smem + L.scan);
+  auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
 
+  // ---- this CTA's share of the work tiles --------------------------------
+  const int per = (p.batch + kThreads - 1) / kThreads;
+  const int b_lo = min(p.batch, tid * per), b_hi = min(p.batch, b_lo + per);
+  long long part = 0;
+  for (int b = b_lo; b < b_hi; ++b) part += work_tiles(ctx_eff(p, b));
+  scan[tid] = part;
   if (tid == 0) {
-    for (int s = 0; s <= p.stages; ++s)
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bars + 8u * s) : "memory");
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    *abort = 0u;
+    start[2] = 0;
   }
-  if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_addr(tmem_slot)),
-                 "r"(p.tmem_cols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  const uint32_t tmem = *tmem_slot;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-  const uint32_t sfa_col = (uint32_t)p.R, sfb_col = (uint32_t)p.R + 8u;
-
-  // Producer state (thread 0): tiles issued so far.
-  int issued = 0;
-  auto issue = [&](int k) {  // tile t_lo + k into stage k % S
-    const int stage = k % p.stages;
-    const int tile = t_lo + k;
-    uint32_t okmask = 0, bytes = 0;
-    int32_t page[2];
-    for (int half = 0; half < 2; ++half) {
-      const int pidx = tile * 2 + half;
-      page[half] = -1;
-      if (pidx * kKvBlock < ctx) {
-        const int32_t id = __ldg(p.block_table + (int64_t)b * p.bt_stride + pidx);
-        if (id >= 0 && id < p.num_blocks) {
-          page[half] = id;
-          okmask |= 1u << half;
-          bytes += kPayloadBytes + kExpBytes;
-        } else {
-          flag_error(p.err, FP4IDX_ERRFLAG_PAGE);
-        }
+  if (tid == 0) {
+    long long run = 0;
+    for (int i = 0; i < kThreads; ++i) {
+      const long long v = scan[i];
+      scan[i] = run;
+      run += v;
+    }
+    scan[kThreads] = run;
+  }
+  __syncthreads();
+  const long long W = scan[kThreads];
+  const long long lo = W * blockIdx.x / gridDim.x, hi = W * (blockIdx.x + 1) / gridDim.x;
+  if (lo < hi && scan[tid] <= lo && lo < scan[tid] + part) {
+    long long acc = scan[tid];
+    for (int b = b_lo; b < b_hi; ++b) {
+      const int wt = work_tiles(ctx_eff(p, b));
+      if (lo < acc + wt) {
+        start[0] = b;
+        start[1] = (int)(lo - acc);
+        start[2] = (int)(hi - lo);
+        break;
       }
+      acc += wt;
     }
-    stage_ok[stage] = okmask;
-    const uint32_t bar = bars + 8u * stage;
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-    for (int half = 0; half < 2; ++half) {
-      if (page[half] < 0) continue;
-      asm volatile(
-          "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
-          "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(sA + stage * kStageA +
-                                                            half * kPayloadBytes)),
-          "l"(&tmap), "r"(0), "r"(0), "r"(page[half]), "r"(bar)
-          : "memory");
-      const uint8_t* src = p.cache + (int64_t)page[half] * kPageBytes + kPayloadBytes;
-      asm volatile(
-          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
-          "[%3];" ::"r"(smem_addr(sE + stage * kStageE + half * kExpBytes)),
-          "l"(src), "r"(kExpBytes), "r"(bar)
-          : "memory");
-    }
-    issued = k + 1;
-  };
-  if (tid == 0)
-    for (int k = 0; k < min(p.stages, nwork); ++k) issue(k);
-
-  // Query rows of sequence b (rows b*R .. b*R+R-1 of q_fp4), their weights,
-  // and their scale words (row 32j+i in column sfb_col+j, lane i of every
-  // quadrant).
-  const int64_t row0 = (int64_t)b * p.R;
-  if (tid < p.R) {
-    const uint4* src = reinterpret_cast<const uint4*>(p.q_fp4 + (row0 + tid) * 64);
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      *reinterpret_cast<uint4*>(sB + sw64_chunk(tid, c)) = __ldg(src + c);
-    sW[tid] = __ldg(p.weights + row0 + tid);
   }
-  {
-    const int i = tid & 31;
-    uint32_t v[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int r = 32 * j + i;
-      v[j] = r < p.R ? __ldg(reinterpret_cast<const uint32_t*>(p.q_scale) + row0 + r)
-                     : 0x7F7F7F7Fu;
-    }
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                     tmem + lane_base + sfb_col),
-                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
-                 : "memory");
-  }
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // sB -> tensor core
+  __syncthreads();
+  const int n = start[2];
 
-  const uint32_t id0 = mxf4_idesc(p.R, 0), id1 = mxf4_idesc(p.R, 2);
-  const uint32_t a_base = smem_addr(sA), b_base = smem_addr(sB);
-  float* const out0 = p.logits + (int64_t)b * p.next_n * p.logits_stride;
-  bool failed = false, mma_pending = false;
-  int k = 0;
-  for (; k < nwork; ++k) {
-    const int stage = k % p.stages;
-    const uint32_t parity = (uint32_t)(k / p.stages) & 1u;
-    const bool ok = mbar_wait_bounded(bars + 8u * stage, parity);
-    uint32_t okmask = 0;
-    if (ok) {
-      okmask = stage_ok[stage];
-      const uint32_t word = reinterpret_cast<const uint32_t*>(sE + stage * kStageE)[tid];
-      asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(
-                       tmem + lane_base + sfa_col + (uint32_t)warp),
-                   "r"(word)
+  if (n > 0) {
+    const int b0 = start[0], t0 = start[1];
+    if (tid == 0) {
+      for (int i = 0; i < 2 * S + 6; ++i) {
+        // sfa_ready and acc_empty take one arrival per epilogue warp of a group
+        const int cnt = ((i >= 2 * S && i < 2 * S + 2) || i >= 2 * S + 4) ? 4 : 1;
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar(i)), "r"(cnt)
+                     : "memory");
+      }
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_addr(misc)),
+                   "r"(p.tmem_cols)
                    : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    if (__syncthreads_or(!ok)) {
-      failed = true;
-      break;
-    }
-    if (tid == 0) {
-      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint32_t a = a_base + (uint32_t)stage * kStageA;
-      mma_mxf4(tmem, sw64_desc(a), sw64_desc(b_base), id0, tmem + sfa_col, tmem + sfb_col, 0u);
-      mma_mxf4(tmem, sw64_desc(a + 32), sw64_desc(b_base + 32), id1, tmem + sfa_col,
-               tmem + sfb_col, 1u);
-      asm volatile(
-          "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-              mma_bar)
-          : "memory");
-    }
-    mma_pending = true;
-    const bool done = mbar_wait_bounded(mma_bar, (uint32_t)k & 1u);
+    __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    if (__syncthreads_or(!done)) {
-      failed = true;
-      break;
-    }
-    mma_pending = false;
-    if (tid == 0 && k + p.stages < nwork) issue(k + p.stages);
+    const uint32_t tmem = misc[0];
+    // TMEM columns: accumulators [0, R) and [R, 2R); key scale words of
+    // group e at 2R + 8e; query scale words of segment g at 2R + 16 + 8(g%2).
+    const uint32_t sfa_col0 = 2u * R, sfb_col0 = 2u * R + 16u;
+    int issued = 0;  // producer: tiles whose copies were issued
 
-    // Epilogue: token s of this thread, one logit per query token j.
-    const int s = (t_lo + k) * kTile + tid;
-    const bool valid = s < ctx && ((okmask >> (tid >> 6)) & 1u);
-    for (int j = 0; j < p.next_n; ++j) {
-      float2 acc = make_float2(0.0f, 0.0f);
-      for (int c0 = j * p.H; c0 < (j + 1) * p.H; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_base + (uint32_t)c0, r);
-        const float4* w4 = reinterpret_cast<const float4*>(sW + c0);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 w = w4[i];
-          const float2 x0 = make_float2(fmaxf(__uint_as_float(r[4 * i]), 0.0f),
-                                        fmaxf(__uint_as_float(r[4 * i + 1]), 0.0f));
-          const float2 x1 = make_float2(fmaxf(__uint_as_float(r[4 * i + 2]), 0.0f),
-                                        fmaxf(__uint_as_float(r[4 * i + 3]), 0.0f));
-          acc = fma2(make_float2(w.x, w.y), x0, acc);
-          acc = fma2(make_float2(w.z, w.w), x1, acc);
+    if (warp == kProducerWarp) {
+      if (lane == 0) {
+        Walker wk;
+        wk.init(p, b0, t0);
+        for (int k = 0; k < n; ++k) {
+          const int s = k % S;
+          if (!wait_phase(bar(bar_empty(S, s)), ((uint32_t)(k / S) & 1u) ^ 1u, abort)) break;
+          uint32_t okmask = 0, bytes = 0;
+          int32_t page[2];
+          for (int half = 0; half < 2; ++half) {
+            const int pidx = wk.t * 2 + half;
+            page[half] = -1;
+            if (pidx * kKvBlock < wk.ctx) {
+              const int32_t id = __ldg(p.block_table + (int64_t)wk.b * p.bt_stride + pidx);
+              if (id >= 0 && id < p.num_blocks) {
+                page[half] = id;
+                okmask |= 1u << half;
+                bytes += kPayloadBytes + kExpBytes;
+              } else {
+                flag_error(p.err, FP4IDX_ERRFLAG_PAGE);
+              }
+            }
+          }
+          stage_ok[s] = okmask;
+          const uint32_t fb = bar(bar_full(s));
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb),
+                       "r"(bytes)
+                       : "memory");
+          for (int half = 0; half < 2; ++half) {
+            if (page[half] < 0) continue;
+            asm volatile(
+                "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
+                "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(sA + s * kStageA +
+                                                                  half * kPayloadBytes)),
+                "l"(&tmap), "r"(0), "r"(0), "r"(page[half]), "r"(fb)
+                : "memory");
+            const uint8_t* src = p.cache + (int64_t)page[half] * kPageBytes + kPayloadBytes;
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], "
+                "%2, [%3];" ::"r"(smem_addr(sE + s * kStageE + half * kExpBytes)),
+                "l"(src), "r"(kExpBytes), "r"(fb)
+                : "memory");
+          }
+          issued = k + 1;
+          wk.advance(p);
         }
       }
-      if (s < p.max_context)
-        out0[(int64_t)j * p.logits_stride + s] = valid ? __fadd_rn(acc.x, acc.y) : -INFINITY;
+    } else if (warp == kMmaWarp) {
+      if (lane == 0) {
+        Walker wk;
+        wk.init(p, b0, t0);
+        const uint32_t id0 = mxf4_idesc(R, 0), id1 = mxf4_idesc(R, 2);
+        const uint32_t a_base = smem_addr(sA), q_base = smem_addr(sQ);
+        int done = 0;
+        for (int k = 0; k < n; ++k) {
+          const int s = k % S, e = k & 1;
+          const uint32_t ph = (uint32_t)(k >> 1) & 1u;
+          if (!wait_phase(bar(bar_sfa(S, e)), ph, abort)) break;
+          if (!wait_phase(bar(bar_acce(S, e)), ph ^ 1u, abort)) break;
+          if (!wait_phase(bar(bar_full(s)), (uint32_t)(k / S) & 1u, abort)) break;
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint32_t a = a_base + (uint32_t)s * kStageA;
+          const uint32_t q = q_base + (uint32_t)(wk.g & 1) * (uint32_t)R * 64u;
+          const uint32_t d = tmem + (uint32_t)e * (uint32_t)R;
+          const uint32_t sfa = tmem + sfa_col0 + 8u * (uint32_t)e;
+          const uint32_t sfb = tmem + sfb_col0 + 8u * (uint32_t)(wk.g & 1);
+          mma_mxf4(d, sw64_desc(a), sw64_desc(q), id0, sfa, sfb, 0u);
+          mma_mxf4(d, sw64_desc(a + 32), sw64_desc(q + 32), id1, sfa, sfb, 1u);
+          mma_commit(bar(bar_accf(S, e)));
+          mma_commit(bar(bar_empty(S, s)));
+          done = k + 1;
+          wk.advance(p);
+        }
+        if (done > 0)  // the last commits land before the CTA's memory is released
+          wait_phase_drain(bar(bar_empty(S, (done - 1) % S)), (uint32_t)((done - 1) / S) & 1u);
+      }
+    } else {
+      // ---- epilogue group e: tiles k = e, e+2, ... ---------------------------
+      const int e = warp >> 2, quad = warp & 3;
+      const int row = quad * 32 + lane;             // token of the tile = TMEM lane
+      const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+      float* const wts = sW + warp * R;             // this warp's head weights
+      Walker wk;
+      wk.init(p, b0, t0);
+      if (e == 1) wk.advance(p);
+      int wg = -1;                                  // segment of the weights held
+      for (int k = e; k < n; k += 2) {
+        const int s = k % S;
+        // prepare tile k: the keys' scale words (and a new segment's queries)
+        bool ok = wait_phase(bar(bar_full(s)), (uint32_t)(k / S) & 1u, abort);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        const uint32_t okmask = stage_ok[s];
+        const int64_t row0 = ((int64_t)wk.b * p.next_n) * p.H;  // first query row of b
+        if (k == 0 || wk.t == 0) {  // first tile of a segment: its query operand
+          const int gb = wk.g & 1;
+          if (row < R) {
+            const uint4* src = reinterpret_cast<const uint4*>(p.q_fp4 + (row0 + row) * 64);
+            uint8_t* dst = sQ + gb * R * 64;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              *reinterpret_cast<uint4*>(dst + sw64_chunk(row, c)) = __ldg(src + c);
+          }
+          uint32_t v[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int r = 32 * j + lane;
+            v[j] = r < R ? __ldg(reinterpret_cast<const uint32_t*>(p.q_scale) + row0 + r)
+                         : 0x7F7F7F7Fu;
+          }
+          asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                           tmem + lane_base + sfb_col0 + 8u * (uint32_t)gb),
+                       "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
+                       : "memory");
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        {
+          const uint32_t word = reinterpret_cast<const uint32_t*>(sE + s * kStageE)[row];
+          asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(
+                           tmem + lane_base + sfa_col0 + 8u * (uint32_t)e + (uint32_t)quad),
+                       "r"(word)
+                       : "memory");
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(bar_sfa(S, e)));
+        if (wk.g != wg) {  // this warp's copy of the segment's head weights
+          for (int i = lane; i < R; i += 32) wts[i] = __ldg(p.weights + row0 + i);
+          __syncwarp();
+          wg = wk.g;
+        }
+
+        // epilogue of tile k
+        ok = wait_phase(bar(bar_accf(S, e)), (uint32_t)(k >> 1) & 1u, abort);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        uint32_t r[NCHUNK][32];
+#pragma unroll
+        for (int c = 0; c < NCHUNK; ++c)
+          tmem_ld32(tmem + lane_base + (uint32_t)e * (uint32_t)R + 32u * c, r[c]);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(bar_acce(S, e)));
+        float part[NCHUNK];
+#pragma unroll
+        for (int c = 0; c < NCHUNK; ++c) {
+          float2 acc = make_float2(0.0f, 0.0f);
+          const float4* w4 = reinterpret_cast<const float4*>(wts + 32 * c);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 w = w4[i];
+            const float2 x0 = make_float2(fmaxf(__uint_as_float(r[c][4 * i]), 0.0f),
+                                          fmaxf(__uint_as_float(r[c][4 * i + 1]), 0.0f));
+            const float2 x1 = make_float2(fmaxf(__uint_as_float(r[c][4 * i + 2]), 0.0f),
+                                          fmaxf(__uint_as_float(r[c][4 * i + 3]), 0.0f));
+            acc = fma2(make_float2(w.x, w.y), x0, acc);
+            acc = fma2(make_float2(w.z, w.w), x1, acc);
+          }
+          part[c] = __fadd_rn(acc.x, acc.y);
+        }
+        const int s_tok = wk.t * kTile + row;
+        const bool valid = s_tok < wk.ctx && ((okmask >> (row >> 6)) & 1u);
+        if (s_tok < p.max_context) {
+          float* out = p.logits + ((int64_t)wk.b * p.next_n) * p.logits_stride + s_tok;
+          const int cpj = p.H / 32;  // chunks per query token
+#pragma unroll
+          for (int j = 0; j < NCHUNK; ++j) {
+            if (j >= p.next_n) break;
+            float v = 0.0f;
+#pragma unroll
+            for (int c = 0; c < NCHUNK; ++c)
+              if (c / cpj == j) v = (c % cpj == 0) ? part[c] : __fadd_rn(v, part[c]);
+            out[(int64_t)j * p.logits_stride] = valid ? v : -INFINITY;
+          }
+        }
+        wk.advance(p);
+        wk.advance(p);
+      }
     }
+
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (*abort) {  // every role has stopped: let copies in flight land first
+      if (warp == kProducerWarp && lane == 0)
+        for (int q = max(0, issued - S); q < issued; ++q)
+          wait_phase_drain(bar(bar_full(q % S)), (uint32_t)(q / S) & 1u);
+      if (tid == 0) flag_error(p.err, FP4IDX_ERRFLAG_TIMEOUT);
+      __syncthreads();
+    }
+    if (warp == 0)
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                   "r"(p.tmem_cols)
+                   : "memory");
   }
 
-  if (failed) {
-    // Let every copy and the MMA in flight land before the CTA's shared
-    // memory and TMEM are released.  The logits of this CTA's remaining
-    // tiles are left unwritten.
-    if (tid == 0) {
-      flag_error(p.err, FP4IDX_ERRFLAG_TIMEOUT);
-      for (int q = k; q < issued; ++q)
-        mbar_wait_bounded(bars + 8u * (q % p.stages), (uint32_t)(q / p.stages) & 1u);
-      if (mma_pending) mbar_wait_bounded(mma_bar, (uint32_t)k & 1u);
+  // ---- -inf for tiles past each context, spread over the grid's warps ------
+  const long long items = (long long)p.batch * p.tiles_total;
+  const int gwarps = gridDim.x * (kThreads / 32);
+  for (long long it = (long long)blockIdx.x * (kThreads / 32) + warp; it < items; it += gwarps) {
+    const int b = (int)(it / p.tiles_total), t = (int)(it % p.tiles_total);
+    if (t < work_tiles(ctx_eff(p, b))) continue;
+    for (int j = 0; j < p.next_n; ++j) {
+      float* out = p.logits + ((int64_t)b * p.next_n + j) * p.logits_stride;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int s = t * kTile + 32 * m + lane;
+        if (s < p.max_context) out[s] = -INFINITY;
+      }
     }
-  } else {
-    write_padding(p, b, work_hi, t_hi);
   }
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-  __syncthreads();
-  if (warp == 0)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(p.tmem_cols)
-                 : "memory");
 }
 
 bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
@@ -435,10 +589,20 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+typedef void (*ScorerKernel)(ScorerParams, CUtensorMap);
+
+ScorerKernel kernel_for(int nchunk) {
+  switch (nchunk) {
+    case 1: return scorer_kernel<1>;
+    case 2: return scorer_kernel<2>;
+    case 3: return scorer_kernel<3>;
+    default: return scorer_kernel<4>;
+  }
+}
+
 struct DeviceInfo {
   bool ready = false;
   int sms = 0;
-  int smem_per_sm = 0;
   int smem_optin = 0;
 };
 
@@ -469,14 +633,13 @@ extern "C" fp4idx_status fp4idx_paged_mqa_logits(
   DeviceInfo& di = info[dev];
   if (!di.ready) {
     if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&di.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
-                               dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&di.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
             cudaSuccess)
       return FP4IDX_ERR_CUDA;
-    if (cudaFuncSetAttribute(scorer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             di.smem_optin) != cudaSuccess)
-      return FP4IDX_ERR_CUDA;
+    for (int c = 1; c <= 4; ++c)
+      if (cudaFuncSetAttribute(kernel_for(c), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               di.smem_optin) != cudaSuccess)
+        return FP4IDX_ERR_CUDA;
     di.ready = true;
   }
   EncodeTiledFn encode = encode_fn();
@@ -494,43 +657,21 @@ extern "C" fp4idx_status fp4idx_paged_mqa_logits(
   p.num_blocks = num_blocks;
   p.bt_stride = block_table_stride;
   p.logits_stride = logits_stride;
+  p.batch = (int32_t)batch;
   p.next_n = (int32_t)next_n;
   p.H = (int32_t)num_heads;
   p.R = (int32_t)(next_n * num_heads);
   p.max_context = (int32_t)max_context;
-  p.tiles = (int32_t)((max_context + kTile - 1) / kTile);
+  p.tiles_total = (int32_t)((max_context + kTile - 1) / kTile);
   uint32_t cols = 32;
-  while (cols < (uint32_t)p.R + 12u) cols <<= 1;
+  while (cols < 2u * (uint32_t)p.R + 32u) cols <<= 1;
   p.tmem_cols = cols;
-
-  // Stages: the fewest (>= 4) with which shared memory, not TMEM, limits the
-  // CTAs resident on an SM to what TMEM (512 columns) can hold at once.
-  const int tmem_ctas = 512 / (int)cols;
-  const int reserve = 1024;  // per-CTA shared memory the system keeps
-  int stages = 4;
-  for (;; ++stages) {
-    const int bytes = (int)make_layout(stages, p.R).total + 1024;  // + base alignment
-    if (bytes > di.smem_optin) {
-      --stages;
-      break;
-    }
-    if (di.smem_per_sm / (bytes + reserve) <= tmem_ctas || stages == kMaxStages) break;
-  }
-  if (stages < 2) return FP4IDX_ERR_SHAPE;
-  p.stages = stages;
-  const int smem_bytes = (int)make_layout(stages, p.R).total + 1024;
-  int ctas = di.smem_per_sm / (smem_bytes + reserve);
-  if (ctas > tmem_ctas) ctas = tmem_ctas;
-  if (ctas < 1) ctas = 1;
-
-  // Split each sequence's tiles so that the grid covers about four waves.
-  const int64_t want = (int64_t)di.sms * ctas * 4;
-  int64_t per = (batch * p.tiles + want - 1) / want;
-  if (per < 1) per = 1;
-  p.tiles_per_cta = (int32_t)per;
-  p.splits = (int32_t)((p.tiles + per - 1) / per);
-  const int64_t grid = batch * p.splits;
-  if (grid >= (1ll << 31)) return FP4IDX_ERR_SHAPE;
+  // As many stages as fit in one CTA's shared memory (one CTA per SM).
+  int S = kMaxStages;
+  while (S > 2 && (int)make_layout(S, p.R).total + 1024 > di.smem_optin) --S;
+  if ((int)make_layout(S, p.R).total + 1024 > di.smem_optin) return FP4IDX_ERR_SHAPE;
+  p.stages = S;
+  const int smem_bytes = (int)make_layout(S, p.R).total + 1024;
 
   // The cache as a 3-D byte tensor: 64 payload bytes x 64 slots x pages.
   alignas(64) CUtensorMap tmap;
@@ -544,7 +685,7 @@ extern "C" fp4idx_status fp4idx_paged_mqa_logits(
       CUDA_SUCCESS)
     return FP4IDX_ERR_CUDA;
 
-  scorer_kernel<<<(unsigned)grid, kThreads, smem_bytes, static_cast<cudaStream_t>(stream)>>>(p,
-                                                                                            tmap);
+  kernel_for(p.R / 32)<<<(unsigned)di.sms, kThreads, smem_bytes,
+                          static_cast<cudaStream_t>(stream)>>>(p, tmap);
   return cudaGetLastError() == cudaSuccess ? FP4IDX_OK : FP4IDX_ERR_CUDA;
 }
