@@ -32,16 +32,17 @@
 // Roles (10 warps).
 //   producer (warp 8): TMA tensor copies of the page payloads (64 tokens x
 //     64 bytes, in the 64-byte swizzled layout the MMA reads) and bulk copies
-//     of the exponent words into a ring of S stages;
-//   MMA issuer (warp 9): two MMAs per tile into one of two TMEM
-//     accumulators, committed to the accumulator's "full" barrier and the
-//     stage's "empty" barrier;
+//     of the exponent words into a ring of S stages; the warp fetches the
+//     page ids of 16 tiles per load, one batch ahead;
+//   MMA issuer (warp 9, the whole warp waiting, lane 0 issuing): two MMAs
+//     per tile into one of two TMEM accumulators, committed to the
+//     accumulator's "full" barrier and the stage's "empty" barrier;
 //   two epilogue groups (warps 0-3, 4-7), group e owning the tiles k with
 //     k % 2 == e and accumulator e: for its tile it writes the keys' scale
 //     words into TMEM (and, at the first tile of a segment, the segment's
 //     query operand and scale words), then reads the accumulator (thread =
-//     token = TMEM lane), releases it, and forms sum_h w * max(D, 0) per
-//     query token in registers.  Each warp holds its own copy of the
+//     token = TMEM lane) and forms sum_h w * max(D, 0) per query token in
+//     registers.  Each warp holds its own copy of the
 //     segment's head weights, so no warp waits on another except through
 //     bounded mbarrier waits.  One group's epilogue overlaps the other
 //     group's MMA.
@@ -100,12 +101,15 @@ struct Layout {
   uint32_t a, q, e, w, bars, ok, misc, scan, total;
 };
 
-// Barrier indices: full[S], empty[S], sfa_ready[2], acc_full[2], acc_empty[2].
+// Barrier indices: full[S], empty[S], sfa_ready[2], acc_full[2].  There is
+// no "accumulator empty" barrier: an epilogue warp reads accumulator e of
+// tile k-2 to completion before it prepares tile k, so the MMA issuer's wait
+// on sfa_ready for tile k also covers the accumulator's release.
 __host__ __device__ inline int bar_full(int s) { return s; }
 __host__ __device__ inline int bar_empty(int S, int s) { return S + s; }
 __host__ __device__ inline int bar_sfa(int S, int e) { return 2 * S + e; }
 __host__ __device__ inline int bar_accf(int S, int e) { return 2 * S + 2 + e; }
-__host__ __device__ inline int bar_acce(int S, int e) { return 2 * S + 4 + e; }
+constexpr int kExtraBars = 4;
 
 __host__ __device__ inline Layout make_layout(int S, int R) {
   Layout L;
@@ -113,8 +117,8 @@ __host__ __device__ inline Layout make_layout(int S, int R) {
   L.q = L.a + (uint32_t)S * kStageA;           // 2 x R x 64, swizzled queries
   L.e = L.q + 2u * (uint32_t)R * 64;           // S x 512 exponent words
   L.w = L.e + (uint32_t)S * kStageE;           // 8 epilogue warps x R weights
-  L.bars = L.w + (uint32_t)kEpiWarps * R * 4;  // 2S + 6 mbarriers
-  L.ok = L.bars + 8u * (uint32_t)(2 * S + 6);  // S page masks
+  L.bars = L.w + (uint32_t)kEpiWarps * R * 4;  // 2S + 4 mbarriers
+  L.ok = L.bars + 8u * (uint32_t)(2 * S + kExtraBars);  // S page masks
   L.misc = L.ok + 4u * (uint32_t)S;            // tmem base, abort, b/t/n start
   L.scan = L.misc + 32;                        // kThreads + 1 partial sums (int64)
   L.total = L.scan + 8u * (kThreads + 1);
@@ -245,6 +249,37 @@ __device__ __forceinline__ int ctx_eff(const ScorerParams& p, int b) {
 
 __device__ __forceinline__ int work_tiles(int ctx) { return (ctx + kTile - 1) / kTile; }
 
+// sum over the 32 columns of chunk c of w * max(D, 0), for chunks [C0, C1)
+// of the accumulator at column address acc (this thread's TMEM lane).
+template <int C0, int C1>
+__device__ __forceinline__ void epilogue_pass(uint32_t acc, const float* wts, float* part) {
+  uint32_t r[C1 - C0][32];
+  float4 w[C1 - C0][8];
+#pragma unroll
+  for (int c = C0; c < C1; ++c) tmem_ld32(acc + 32u * c, r[c - C0]);
+#pragma unroll
+  for (int c = C0; c < C1; ++c)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[c - C0][i] = reinterpret_cast<const float4*>(wts + 32 * c)[i];
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int c = C0; c < C1; ++c) {
+    float2 a = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 ww = w[c - C0][i];
+      const uint32_t* x = r[c - C0] + 4 * i;
+      a = fma2(make_float2(ww.x, ww.y),
+               make_float2(fmaxf(__uint_as_float(x[0]), 0.0f), fmaxf(__uint_as_float(x[1]), 0.0f)),
+               a);
+      a = fma2(make_float2(ww.z, ww.w),
+               make_float2(fmaxf(__uint_as_float(x[2]), 0.0f), fmaxf(__uint_as_float(x[3]), 0.0f)),
+               a);
+    }
+    part[c] = __fadd_rn(a.x, a.y);
+  }
+}
+
 // Walks a CTA's tiles in order: sequence b, tile t, its context, and the
 // segment index g (how many times b has changed since the first tile).
 struct Walker {
@@ -329,9 +364,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (n > 0) {
     const int b0 = start[0], t0 = start[1];
     if (tid == 0) {
-      for (int i = 0; i < 2 * S + 6; ++i) {
-        // sfa_ready and acc_empty take one arrival per epilogue warp of a group
-        const int cnt = ((i >= 2 * S && i < 2 * S + 2) || i >= 2 * S + 4) ? 4 : 1;
+      for (int i = 0; i < 2 * S + kExtraBars; ++i) {
+        // sfa_ready takes one arrival per epilogue warp of a group
+        const int cnt = (i >= 2 * S && i < 2 * S + 2) ? 4 : 1;
         asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar(i)), "r"(cnt)
                      : "memory");
       }
@@ -354,82 +389,122 @@ __global__ void __launch_bounds__(kThreads, 1)
     int issued = 0;  // producer: tiles whose copies were issued
 
     if (warp == kProducerWarp) {
-      if (lane == 0) {
-        Walker wk;
-        wk.init(p, b0, t0);
-        for (int k = 0; k < n; ++k) {
-          const int s = k % S;
-          if (!wait_phase(bar(bar_empty(S, s)), ((uint32_t)(k / S) & 1u) ^ 1u, abort)) break;
-          uint32_t okmask = 0, bytes = 0;
+      // The page ids of 16 tiles are fetched by the whole warp in one load
+      // (lane L: tile L/2, page L%2), a batch ahead of the tiles issued.
+      Walker fetch_wk;
+      fetch_wk.init(p, b0, t0);
+      auto fetch = [&](int k0, int32_t& id, bool& inctx) {
+        const int mine = lane >> 1;
+        int cb = fetch_wk.b, ct = fetch_wk.t, cctx = fetch_wk.ctx;
+        for (int i = 0; i < 16 && k0 + i < n; ++i) {
+          if (i == mine) {
+            cb = fetch_wk.b;
+            ct = fetch_wk.t;
+            cctx = fetch_wk.ctx;
+          }
+          fetch_wk.advance(p);
+        }
+        const int pidx = ct * 2 + (lane & 1);
+        inctx = k0 + mine < n && pidx * kKvBlock < cctx;
+        id = inctx ? __ldg(p.block_table + (int64_t)cb * p.bt_stride + pidx) : -1;
+      };
+      int32_t cur_id, nxt_id = -1;
+      bool cur_in, nxt_in = false;
+      fetch(0, cur_id, cur_in);
+      bool stop = false;
+      for (int k0 = 0; k0 < n && !stop; k0 += 16) {
+        if (k0 + 16 < n) fetch(k0 + 16, nxt_id, nxt_in);
+        for (int i = 0; i < 16 && k0 + i < n; ++i) {
+          const int k = k0 + i, s = k % S;
           int32_t page[2];
+          bool in[2];
+#pragma unroll
           for (int half = 0; half < 2; ++half) {
-            const int pidx = wk.t * 2 + half;
-            page[half] = -1;
-            if (pidx * kKvBlock < wk.ctx) {
-              const int32_t id = __ldg(p.block_table + (int64_t)wk.b * p.bt_stride + pidx);
-              if (id >= 0 && id < p.num_blocks) {
-                page[half] = id;
-                okmask |= 1u << half;
-                bytes += kPayloadBytes + kExpBytes;
-              } else {
-                flag_error(p.err, FP4IDX_ERRFLAG_PAGE);
+            page[half] = __shfl_sync(0xffffffffu, cur_id, 2 * i + half);
+            in[half] = __shfl_sync(0xffffffffu, (int)cur_in, 2 * i + half) != 0;
+          }
+          int ok = 1;
+          if (lane == 0) {
+            ok = wait_phase(bar(bar_empty(S, s)), ((uint32_t)(k / S) & 1u) ^ 1u, abort);
+            if (ok) {
+              uint32_t okmask = 0, bytes = 0;
+#pragma unroll
+              for (int half = 0; half < 2; ++half) {
+                if (!in[half]) {
+                  page[half] = -1;
+                } else if (page[half] < 0 || page[half] >= p.num_blocks) {
+                  flag_error(p.err, FP4IDX_ERRFLAG_PAGE);
+                  page[half] = -1;
+                } else {
+                  okmask |= 1u << half;
+                  bytes += kPayloadBytes + kExpBytes;
+                }
               }
+              stage_ok[s] = okmask;
+              const uint32_t fb = bar(bar_full(s));
+              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+              asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb),
+                           "r"(bytes)
+                           : "memory");
+#pragma unroll
+              for (int half = 0; half < 2; ++half) {
+                if (page[half] < 0) continue;
+                asm volatile(
+                    "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
+                    "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(sA + s * kStageA +
+                                                                      half * kPayloadBytes)),
+                    "l"(&tmap), "r"(0), "r"(0), "r"(page[half]), "r"(fb)
+                    : "memory");
+                const uint8_t* src = p.cache + (int64_t)page[half] * kPageBytes + kPayloadBytes;
+                asm volatile(
+                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], "
+                    "[%1], %2, [%3];" ::"r"(smem_addr(sE + s * kStageE + half * kExpBytes)),
+                    "l"(src), "r"(kExpBytes), "r"(fb)
+                    : "memory");
+              }
+              issued = k + 1;
             }
           }
-          stage_ok[s] = okmask;
-          const uint32_t fb = bar(bar_full(s));
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb),
-                       "r"(bytes)
-                       : "memory");
-          for (int half = 0; half < 2; ++half) {
-            if (page[half] < 0) continue;
-            asm volatile(
-                "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
-                "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(sA + s * kStageA +
-                                                                  half * kPayloadBytes)),
-                "l"(&tmap), "r"(0), "r"(0), "r"(page[half]), "r"(fb)
-                : "memory");
-            const uint8_t* src = p.cache + (int64_t)page[half] * kPageBytes + kPayloadBytes;
-            asm volatile(
-                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], "
-                "%2, [%3];" ::"r"(smem_addr(sE + s * kStageE + half * kExpBytes)),
-                "l"(src), "r"(kExpBytes), "r"(fb)
-                : "memory");
+          if (!__shfl_sync(0xffffffffu, ok, 0)) {
+            stop = true;
+            break;
           }
-          issued = k + 1;
-          wk.advance(p);
         }
+        cur_id = nxt_id;
+        cur_in = nxt_in;
       }
     } else if (warp == kMmaWarp) {
-      if (lane == 0) {
-        Walker wk;
-        wk.init(p, b0, t0);
-        const uint32_t id0 = mxf4_idesc(R, 0), id1 = mxf4_idesc(R, 2);
-        const uint32_t a_base = smem_addr(sA), q_base = smem_addr(sQ);
-        int done = 0;
-        for (int k = 0; k < n; ++k) {
-          const int s = k % S, e = k & 1;
-          const uint32_t ph = (uint32_t)(k >> 1) & 1u;
-          if (!wait_phase(bar(bar_sfa(S, e)), ph, abort)) break;
-          if (!wait_phase(bar(bar_acce(S, e)), ph ^ 1u, abort)) break;
-          if (!wait_phase(bar(bar_full(s)), (uint32_t)(k / S) & 1u, abort)) break;
-          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-          const uint32_t a = a_base + (uint32_t)s * kStageA;
-          const uint32_t q = q_base + (uint32_t)(wk.g & 1) * (uint32_t)R * 64u;
+      // The whole warp waits (a warp-uniform loop wakes promptly); lane 0
+      // issues the MMAs and commits.
+      Walker wk;
+      wk.init(p, b0, t0);
+      const uint32_t id0 = mxf4_idesc(R, 0), id1 = mxf4_idesc(R, 2);
+      // descriptor start addresses advance in 16-byte units
+      const uint64_t a_desc0 = sw64_desc(smem_addr(sA)), q_desc0 = sw64_desc(smem_addr(sQ));
+      int done = 0;
+      for (int k = 0; k < n; ++k) {
+        const int s = k % S, e = k & 1;
+        bool ok = wait_phase(bar(bar_sfa(S, e)), (uint32_t)(k >> 1) & 1u, abort) &&
+                  wait_phase(bar(bar_full(s)), (uint32_t)(k / S) & 1u, abort);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        if (lane == 0) {
+          const uint64_t a = a_desc0 + (uint64_t)(s * (kStageA >> 4));
+          const uint64_t q = q_desc0 + (uint64_t)((wk.g & 1) * R * (64 >> 4));
           const uint32_t d = tmem + (uint32_t)e * (uint32_t)R;
           const uint32_t sfa = tmem + sfa_col0 + 8u * (uint32_t)e;
           const uint32_t sfb = tmem + sfb_col0 + 8u * (uint32_t)(wk.g & 1);
-          mma_mxf4(d, sw64_desc(a), sw64_desc(q), id0, sfa, sfb, 0u);
-          mma_mxf4(d, sw64_desc(a + 32), sw64_desc(q + 32), id1, sfa, sfb, 1u);
+          mma_mxf4(d, a, q, id0, sfa, sfb, 0u);
+          mma_mxf4(d, a + 2, q + 2, id1, sfa, sfb, 1u);
           mma_commit(bar(bar_accf(S, e)));
           mma_commit(bar(bar_empty(S, s)));
-          done = k + 1;
-          wk.advance(p);
         }
-        if (done > 0)  // the last commits land before the CTA's memory is released
-          wait_phase_drain(bar(bar_empty(S, (done - 1) % S)), (uint32_t)((done - 1) / S) & 1u);
+        __syncwarp();
+        done = k + 1;
+        wk.advance(p);
       }
+      if (done > 0 && lane == 0)  // the last commits land before the memory is released
+        wait_phase_drain(bar(bar_empty(S, (done - 1) % S)), (uint32_t)((done - 1) / S) & 1u);
     } else {
       // ---- epilogue group e: tiles k = e, e+2, ... ---------------------------
       const int e = warp >> 2, quad = warp & 3;
@@ -490,31 +565,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = wait_phase(bar(bar_accf(S, e)), (uint32_t)(k >> 1) & 1u, abort);
         if (!__all_sync(0xffffffffu, ok)) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        uint32_t r[NCHUNK][32];
-#pragma unroll
-        for (int c = 0; c < NCHUNK; ++c)
-          tmem_ld32(tmem + lane_base + (uint32_t)e * (uint32_t)R + 32u * c, r[c]);
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(bar_acce(S, e)));
+        // Two passes over the accumulator's 32-column chunks; each pass
+        // issues its TMEM loads and its weight loads together, so their
+        // latencies overlap.
         float part[NCHUNK];
-#pragma unroll
-        for (int c = 0; c < NCHUNK; ++c) {
-          float2 acc = make_float2(0.0f, 0.0f);
-          const float4* w4 = reinterpret_cast<const float4*>(wts + 32 * c);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float4 w = w4[i];
-            const float2 x0 = make_float2(fmaxf(__uint_as_float(r[c][4 * i]), 0.0f),
-                                          fmaxf(__uint_as_float(r[c][4 * i + 1]), 0.0f));
-            const float2 x1 = make_float2(fmaxf(__uint_as_float(r[c][4 * i + 2]), 0.0f),
-                                          fmaxf(__uint_as_float(r[c][4 * i + 3]), 0.0f));
-            acc = fma2(make_float2(w.x, w.y), x0, acc);
-            acc = fma2(make_float2(w.z, w.w), x1, acc);
-          }
-          part[c] = __fadd_rn(acc.x, acc.y);
-        }
+        constexpr int kFirst = (NCHUNK + 1) / 2;
+        epilogue_pass<0, kFirst>(tmem + lane_base + (uint32_t)e * (uint32_t)R, wts, part);
+        if constexpr (NCHUNK > kFirst)
+          epilogue_pass<kFirst, NCHUNK>(tmem + lane_base + (uint32_t)e * (uint32_t)R, wts, part);
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
         const int s_tok = wk.t * kTile + row;
         const bool valid = s_tok < wk.ctx && ((okmask >> (row >> 6)) & 1u);
         if (s_tok < p.max_context) {
