@@ -65,6 +65,15 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.oracle_q_rope_pack_weights.argtypes = [
         P, P, P, P, P, i64, ctypes.c_int, P, P, P, i64, i64]
     L.oracle_q_rope_pack_weights.restype = ctypes.c_int
+    L.oracle_hadamard_row.argtypes = [P]
+    L.oracle_hadamard_row.restype = None
+    L.oracle_k_norm_rope_pack_store_ex.argtypes = [
+        P, P, ctypes.c_float, P, P, P, i64, ctypes.c_int, P, P, i64, i64, ctypes.c_int,
+        ctypes.c_int]
+    L.oracle_k_norm_rope_pack_store_ex.restype = ctypes.c_int
+    L.oracle_q_rope_pack_weights_ex.argtypes = [
+        P, P, P, P, P, i64, ctypes.c_int, P, P, P, i64, i64, ctypes.c_int]
+    L.oracle_q_rope_pack_weights_ex.restype = ctypes.c_int
     L.oracle_paged_mqa_logits.argtypes = [
         P, P, P, P, i64, P, i64, P, P, i64, i64, i64, i64, i64]
     L.oracle_paged_mqa_logits.restype = ctypes.c_int
@@ -180,8 +189,17 @@ def quant_pack_row(row_bits):
 
 
 # ------------------------------------------------------------------ full ops
+def hadamard_row(y_bits) -> np.ndarray:
+    """Normalised 128-point Walsh-Hadamard rotation of a bf16 row (bits)."""
+    y = _c(y_bits, np.uint16).copy()
+    assert y.shape == (HEAD_DIM,)
+    lib().oracle_hadamard_row(_p(y))
+    return y
+
+
 def k_norm_rope_pack_store(k, gamma, eps, positions, cos_cache, sin_cache,
-                           rope_style, slot_mapping, kv_cache) -> int:
+                           rope_style, slot_mapping, kv_cache, compress_ratio: int = 1,
+                           hadamard: bool = False) -> int:
     """kv_cache (uint8 [num_blocks, 4352]) is updated in place."""
     k = _c(k, np.uint16)
     T = k.shape[0]
@@ -194,13 +212,14 @@ def k_norm_rope_pack_store(k, gamma, eps, positions, cos_cache, sin_cache,
     assert kv_cache.dtype == np.uint8 and kv_cache.flags.c_contiguous
     assert kv_cache.shape[1:] == (PAGE_BYTES,)
     assert pos.shape == (T,) and sl.shape == (T,) and cs.shape == sn.shape
-    return int(lib().oracle_k_norm_rope_pack_store(
+    return int(lib().oracle_k_norm_rope_pack_store_ex(
         _p(k), _p(g), ctypes.c_float(eps), _p(pos), _p(cs), _p(sn), cs.shape[0],
-        int(rope_style), _p(sl), _p(kv_cache), kv_cache.shape[0], T))
+        int(rope_style), _p(sl), _p(kv_cache), kv_cache.shape[0], T, int(compress_ratio),
+        int(bool(hadamard))))
 
 
 def q_rope_pack_weights(q, w, positions, cos_cache, sin_cache, rope_style,
-                        out=None):
+                        out=None, hadamard: bool = False):
     """Returns (q_fp4 [T,H,64] u8, q_scale [T,H,4] u8, weights [T,H] f32, status)."""
     q = _c(q, np.uint16)
     T, H, D = q.shape
@@ -215,9 +234,9 @@ def q_rope_pack_weights(q, w, positions, cos_cache, sin_cache, rope_style,
                np.zeros((T, H, EXP_BYTES), np.uint8),
                np.zeros((T, H), np.float32))
     qf, qs, wt = out
-    st = lib().oracle_q_rope_pack_weights(
+    st = lib().oracle_q_rope_pack_weights_ex(
         _p(q), _p(w), _p(pos), _p(cs), _p(sn), cs.shape[0], int(rope_style),
-        _p(qf), _p(qs), _p(wt), T, H)
+        _p(qf), _p(qs), _p(wt), T, H, int(bool(hadamard)))
     return qf, qs, wt, int(st)
 
 

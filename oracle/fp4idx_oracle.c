@@ -227,18 +227,39 @@ void oracle_quant_pack_row(const uint16_t* row, uint8_t* payload64,
   }
 }
 
+/* Optional rotation of a row before quantisation ([csa] Changes: the
+ * fused kv-cache kernel does RMSNorm + RoPE + optional Hadamard rotate + FP4
+ * quant).  Reading: the normalised 128-point Walsh-Hadamard transform in
+ * Sylvester order, y' = bf16(rn32(H y) * rn32(1/sqrt(128))), with H y formed
+ * by the fast transform's butterfly stages h = 1, 2, 4, ..., 64, each pair
+ * (j, j+h) (bit h of j clear) becoming (rn32(a+b), rn32(a-b)). */
+void oracle_hadamard_row(uint16_t* y) {
+  float x[HEAD_DIM];
+  for (int i = 0; i < HEAD_DIM; ++i) x[i] = bf16_to_f32(y[i]);
+  for (int h = 1; h < HEAD_DIM; h *= 2)
+    for (int i = 0; i < HEAD_DIM; i += 2 * h)
+      for (int j = i; j < i + h; ++j) {
+        float a = x[j], b = x[j + h];
+        x[j] = a + b;
+        x[j + h] = a - b;
+      }
+  const float norm = (float)(1.0 / sqrt((double)HEAD_DIM));
+  for (int i = 0; i < HEAD_DIM; ++i) y[i] = oracle_f32_to_bf16(x[i] * norm);
+}
+
 /* Keys ([sgl] Summary: RMSNorm, RoPE, both quantisation stages and the paged
  * cache store in one op).  Slot s >= 0 goes to page s/64, offset s%64.
  * Readings: a negative slot means "skip" (slot 0 is an ordinary slot); the
  * 68 bytes of a slot are split inside the 4352-byte page into the 64-byte
  * payload at o*64 and the 4-byte exponent word at 4096 + o*4. */
-int oracle_k_norm_rope_pack_store(const uint16_t* k, const uint16_t* gamma,
-                                  float eps, const int64_t* positions,
-                                  const float* cos_cache,
-                                  const float* sin_cache, int64_t max_pos,
-                                  int rope_style, const int64_t* slot_mapping,
-                                  uint8_t* kv_cache, int64_t num_blocks,
-                                  int64_t num_tokens) {
+int oracle_k_norm_rope_pack_store_ex(const uint16_t* k, const uint16_t* gamma,
+                                     float eps, const int64_t* positions,
+                                     const float* cos_cache,
+                                     const float* sin_cache, int64_t max_pos,
+                                     int rope_style, const int64_t* slot_mapping,
+                                     uint8_t* kv_cache, int64_t num_blocks,
+                                     int64_t num_tokens, int compress_ratio,
+                                     int hadamard) {
   int status = 0;
   for (int64_t t = 0; t < num_tokens; ++t) {
     int64_t slot = slot_mapping[t];
@@ -248,10 +269,14 @@ int oracle_k_norm_rope_pack_store(const uint16_t* k, const uint16_t* gamma,
       status = -1;
       continue;
     }
+    /* [sgl] Summary: RoPE at the group's first position; with groups of
+     * compress_ratio consecutive positions that is pos - pos % ratio. */
+    int64_t rope_pos = pos - pos % compress_ratio;
     uint16_t y[HEAD_DIM];
     oracle_rmsnorm_row(k + t * HEAD_DIM, gamma, eps, y);
-    oracle_rope_row(y, cos_cache + pos * (ROPE_DIM / 2),
-                    sin_cache + pos * (ROPE_DIM / 2), rope_style);
+    oracle_rope_row(y, cos_cache + rope_pos * (ROPE_DIM / 2),
+                    sin_cache + rope_pos * (ROPE_DIM / 2), rope_style);
+    if (hadamard) oracle_hadamard_row(y);
     uint8_t payload[PAYLOAD_BYTES], ex[EXP_BYTES];
     oracle_quant_pack_row(y, payload, ex, NULL, NULL, NULL);
     int64_t b = slot / KV_BLOCK, o = slot % KV_BLOCK;
@@ -262,16 +287,29 @@ int oracle_k_norm_rope_pack_store(const uint16_t* k, const uint16_t* gamma,
   return status;
 }
 
+int oracle_k_norm_rope_pack_store(const uint16_t* k, const uint16_t* gamma,
+                                  float eps, const int64_t* positions,
+                                  const float* cos_cache,
+                                  const float* sin_cache, int64_t max_pos,
+                                  int rope_style, const int64_t* slot_mapping,
+                                  uint8_t* kv_cache, int64_t num_blocks,
+                                  int64_t num_tokens) {
+  return oracle_k_norm_rope_pack_store_ex(k, gamma, eps, positions, cos_cache,
+                                          sin_cache, max_pos, rope_style,
+                                          slot_mapping, kv_cache, num_blocks,
+                                          num_tokens, 1, 0);
+}
+
 /* Queries ([sgl] Summary: the query op rotates, quantises and packs the same
  * way and computes the head weights in the same launch; [aiter] API: weights
  * carry the plain weight, fp32 here, nothing folded in). */
-int oracle_q_rope_pack_weights(const uint16_t* q, const uint16_t* w,
-                               const int64_t* positions,
-                               const float* cos_cache, const float* sin_cache,
-                               int64_t max_pos, int rope_style,
-                               uint8_t* q_fp4, uint8_t* q_scale,
-                               float* weights, int64_t num_tokens,
-                               int64_t num_heads) {
+int oracle_q_rope_pack_weights_ex(const uint16_t* q, const uint16_t* w,
+                                  const int64_t* positions,
+                                  const float* cos_cache, const float* sin_cache,
+                                  int64_t max_pos, int rope_style,
+                                  uint8_t* q_fp4, uint8_t* q_scale,
+                                  float* weights, int64_t num_tokens,
+                                  int64_t num_heads, int hadamard) {
   int status = 0;
   double wscale = 1.0 / sqrt((double)num_heads * (double)HEAD_DIM);
   for (int64_t t = 0; t < num_tokens; ++t) {
@@ -286,12 +324,25 @@ int oracle_q_rope_pack_weights(const uint16_t* q, const uint16_t* w,
       memcpy(y, q + r * HEAD_DIM, sizeof y);
       oracle_rope_row(y, cos_cache + pos * (ROPE_DIM / 2),
                       sin_cache + pos * (ROPE_DIM / 2), rope_style);
+      if (hadamard) oracle_hadamard_row(y);
       oracle_quant_pack_row(y, q_fp4 + r * PAYLOAD_BYTES,
                             q_scale + r * EXP_BYTES, NULL, NULL, NULL);
       weights[r] = (float)((double)bf16_to_f32(w[r]) * wscale);
     }
   }
   return status;
+}
+
+int oracle_q_rope_pack_weights(const uint16_t* q, const uint16_t* w,
+                               const int64_t* positions,
+                               const float* cos_cache, const float* sin_cache,
+                               int64_t max_pos, int rope_style,
+                               uint8_t* q_fp4, uint8_t* q_scale,
+                               float* weights, int64_t num_tokens,
+                               int64_t num_heads) {
+  return oracle_q_rope_pack_weights_ex(q, w, positions, cos_cache, sin_cache,
+                                       max_pos, rope_style, q_fp4, q_scale,
+                                       weights, num_tokens, num_heads, 0);
 }
 
 /* The scorer ([aiter] Verification, End-to-end: the FP4 paged MQA-logits

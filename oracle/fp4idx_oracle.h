@@ -14,6 +14,9 @@
  *          index_pack_exponent and inv_scale_ue8m0.
  *   [aiter] "[HIP] Add FP4 output mode to indexer_qk_rope_quant_and_cache"
  *          (aiter PR 5484): API; Verification; One deliberate deviation.
+ *   [csa]  "DeepSeek-V4 FP4: fused_compress FP4 scatter + rmsnorm_rope_rotate
+ *          FP4 KV-cache kernel" (aiter PR 4029): Changes (optional Hadamard
+ *          rotation before the FP4 quantisation).
  *
  * Where the pages leave a step open, the reading used is stated beside the
  * function that takes it.
@@ -91,6 +94,34 @@ int oracle_q_rope_pack_weights(const uint16_t* q, const uint16_t* w,
                                uint8_t* q_fp4, uint8_t* q_scale,
                                float* weights, int64_t num_tokens,
                                int64_t num_heads);
+
+/* ---- stated variants of the same two operations ---- */
+
+/* In-place normalised 128-point Walsh-Hadamard rotation of a bf16 row:
+ * fast-transform butterflies h = 1..64 in fp32, times rn32(1/sqrt(128)),
+ * rounded to bf16. */
+void oracle_hadamard_row(uint16_t* y);
+
+/* Keys with the variants: compress_ratio (1, 2 or 4) moves the RoPE to the
+ * group's first position, pos - pos % ratio; hadamard != 0 rotates the row
+ * after RoPE.  compress_ratio 1 and hadamard 0 is the call above. */
+int oracle_k_norm_rope_pack_store_ex(const uint16_t* k, const uint16_t* gamma,
+                                     float eps, const int64_t* positions,
+                                     const float* cos_cache,
+                                     const float* sin_cache, int64_t max_pos,
+                                     int rope_style, const int64_t* slot_mapping,
+                                     uint8_t* kv_cache, int64_t num_blocks,
+                                     int64_t num_tokens, int compress_ratio,
+                                     int hadamard);
+
+/* Queries with the rotation variant (hadamard != 0: after RoPE). */
+int oracle_q_rope_pack_weights_ex(const uint16_t* q, const uint16_t* w,
+                                  const int64_t* positions,
+                                  const float* cos_cache, const float* sin_cache,
+                                  int64_t max_pos, int rope_style,
+                                  uint8_t* q_fp4, uint8_t* q_scale,
+                                  float* weights, int64_t num_tokens,
+                                  int64_t num_heads, int hadamard);
 
 /* FP4 paged MQA-logits scorer (the consumer of the packed queries and the
  * paged index-K cache).  Query row t = b*next_n + j of sequence b scores

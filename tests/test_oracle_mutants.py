@@ -7,6 +7,7 @@ import pytest
 
 import oracle
 from tests import test_oracle_pins as pins
+from tests import test_oracle_variants as vpins
 from tests import test_scorer_oracle as spins
 
 # (name, text in the oracle source, replacement)
@@ -67,8 +68,22 @@ MUTANTS = [
     ("scorer_padding_zero", "        if (s >= ctx) {\n          *out = -INFINITY;",
      "        if (s >= ctx) {\n          *out = 0.0f;"),
     ("k_rope_skipped",
-     "    oracle_rope_row(y, cos_cache + pos * (ROPE_DIM / 2),\n"
-     "                    sin_cache + pos * (ROPE_DIM / 2), rope_style);\n", ""),
+     "    oracle_rope_row(y, cos_cache + rope_pos * (ROPE_DIM / 2),\n"
+     "                    sin_cache + rope_pos * (ROPE_DIM / 2), rope_style);\n", ""),
+    ("hadamard_sign", "x[j + h] = a - b;", "x[j + h] = b - a;"),
+    ("hadamard_norm_over_128", "(float)(1.0 / sqrt((double)HEAD_DIM))",
+     "(float)(1.0 / (double)HEAD_DIM)"),
+    ("hadamard_stage_dropped", "for (int h = 1; h < HEAD_DIM; h *= 2)",
+     "for (int h = 1; h < HEAD_DIM / 2; h *= 2)"),
+    ("hadamard_pair_distance", "float a = x[j], b = x[j + h];",
+     "float a = x[j], b = x[(j + h + 1) % HEAD_DIM];"),
+    ("compress_divides", "int64_t rope_pos = pos - pos % compress_ratio;",
+     "int64_t rope_pos = pos / compress_ratio;"),
+    ("compress_ignored", "int64_t rope_pos = pos - pos % compress_ratio;",
+     "int64_t rope_pos = pos;"),
+    ("k_hadamard_skipped", "    if (hadamard) oracle_hadamard_row(y);\n    uint8_t payload", "    uint8_t payload"),
+    ("q_hadamard_skipped", "      if (hadamard) oracle_hadamard_row(y);\n      oracle_quant_pack_row",
+     "      oracle_quant_pack_row"),
 ]
 
 # Independent pins, cheapest first.
@@ -94,6 +109,11 @@ PINS = [
     spins.test_page_indirection_and_sequences,
     spins.test_bad_page_reported,
     spins.test_random_case_exact_rational,
+    vpins.test_hadamard_one_hot_rows,
+    vpins.test_hadamard_small_integers_exact,
+    vpins.test_query_rotation_sign_pattern,
+    vpins.test_key_rotation_sign_pattern,
+    vpins.test_compress_ratio_uses_group_first_position,
     pins.test_two_stage_invariants,
     pins.test_group_quant_exact_rational,
     pins.test_exponent_exhaustive_bf16,
@@ -108,6 +128,9 @@ def _run(fn):
     if "style" in params:
         for s in (0, 1):
             fn(style=s)
+    elif "ratio" in params:
+        for r in (2, 4):
+            fn(ratio=r)
     else:
         fn()
 
