@@ -345,6 +345,48 @@ def time_e2e(F, w, D, mode, steps):
     return a.elapsed_time(b) / steps, h2d, d2h
 
 
+# ------------------------------------------------------------- variants
+def run_variants(F, w, D, dev, peak, flush, steps: int = 100, warmup: int = 5) -> dict:
+    """The fused pre-pass with the stated variants (the fp4idx_options block)
+    on the same workload: CUDA-event time per launch, L2 flushed before each,
+    and the fraction of the measured HBM peak (the algorithmic bytes do not
+    change with the options)."""
+    import ctypes
+    import torch
+    T, H = w.T, w.H
+    qf = torch.empty((T, H, 64), dtype=torch.uint8, device=dev)
+    qs = torch.empty((T, H, 4), dtype=torch.uint8, device=dev)
+    wt = torch.empty((T, H), dtype=torch.float32, device=dev)
+    p = {k: v.data_ptr() for k, v in D.items()}
+    st = torch.cuda.current_stream()
+    fn = F.lib().fp4idx_indexer_prepass_ex
+    nbytes = algorithmic_bytes(w, "fused")["fused"]
+    out = {}
+    for name, ratio, had in (("hadamard", 1, 1), ("compress_ratio_4", 4, 0),
+                             ("compress_ratio_4_hadamard", 4, 1)):
+        opts = ctypes.cast(ctypes.pointer(F.Options(ratio, had)), ctypes.c_void_p)
+        args = (p["k"], 128, p["gamma"], w.eps, p["slots"], p["cache"], w.num_blocks, p["q"],
+                H * 128, 128, p["w"], H, F.default_weight_scale(H), qf.data_ptr(),
+                qs.data_ptr(), wt.data_ptr(), H, p["pos"], p["cos"], p["sin"], w.max_pos,
+                w.rope_style, T, opts, None, st.cuda_stream)
+        for _ in range(warmup):
+            flush()
+            _ok(F, fn(*args))
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for a, b in ev:
+            flush()
+            a.record(st)
+            _ok(F, fn(*args))
+            b.record(st)
+        torch.cuda.synchronize()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out[name] = {"ms_per_launch": round(ms, 5), "tokens_per_s": round(T / (ms / 1e3), 1),
+                     "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}
+    return out
+
+
 # ------------------------------------------------------------------ scorer
 def scorer_bytes(sw) -> int:
     """Bytes one scorer launch must move at minimum: per cached token below
@@ -486,7 +528,9 @@ def run_ours(args):
                            "frac_of_peak": round(bx / (ms / 1e3) / 1e9 / peak, 4)}
             del Dx
 
-    scorer = None
+    scorer = variants = None
+    if rank == 0 and not args.no_extra and args.mode == "fused":
+        variants = run_variants(F, w, D, dev, peak, flush)
     if rank == 0 and not args.no_extra:
         scorer = run_scorer(F, dev, peak, flush, 200)
 
@@ -515,6 +559,7 @@ def run_ours(args):
             "cpu_baseline": base,
             "timed_wall_s": round(r["wall_s"], 4),
             "other_configs": extra,
+            "variants": variants,
             "scorer": scorer,
         }
         if args.mode != "fused":

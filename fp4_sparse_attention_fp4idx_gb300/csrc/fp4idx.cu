@@ -409,6 +409,56 @@ __device__ __forceinline__ void rope_lane(uint32_t (&a)[4], const RopeCoef<kStyl
   }
 }
 
+// Normalised 128-point Walsh-Hadamard rotation of the row held by the 8
+// lanes of a row group (lane j: a = dims 8j..8j+7, b = dims 64+8j..64+8j+7).
+// Butterfly stages h = 1, 2, 4 stay inside a lane's 8-element runs, h = 8,
+// 16, 32 pair lane j with lane j ^ (h/8), h = 64 pairs a with b; each
+// butterfly turns (lower, upper) into (rn(lower + upper), rn(lower - upper)).
+// Then one product with rn32(1/sqrt(128)) and the bf16 rounding.  All 32
+// lanes must call (shuffles).
+__device__ __forceinline__ void hadamard_lane(uint32_t (&a)[4], uint32_t (&b)[4], int j) {
+  float x[16];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    x[2 * k] = bf16_lo(a[k]);
+    x[2 * k + 1] = bf16_hi(a[k]);
+    x[8 + 2 * k] = bf16_lo(b[k]);
+    x[8 + 2 * k + 1] = bf16_hi(b[k]);
+  }
+#pragma unroll
+  for (int h = 1; h < 8; h *= 2)
+#pragma unroll
+    for (int run = 0; run < 16; run += 8)
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (!(i & h)) {
+          const float u = x[run + i], v = x[run + i + h];
+          x[run + i] = __fadd_rn(u, v);
+          x[run + i + h] = __fsub_rn(u, v);
+        }
+#pragma unroll
+  for (int m = 1; m < 8; m *= 2) {
+    const bool upper = (j & m) != 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float other = __shfl_xor_sync(kFull, x[i], m);
+      x[i] = upper ? __fsub_rn(other, x[i]) : __fadd_rn(x[i], other);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float u = x[i], v = x[8 + i];
+    x[i] = __fadd_rn(u, v);
+    x[8 + i] = __fsub_rn(u, v);
+  }
+  const float norm = 0.08838834764831845f;  // rn32(1/sqrt(128))
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    a[k] = pack_bf16x2(__fmul_rn(x[2 * k], norm), __fmul_rn(x[2 * k + 1], norm));
+    b[k] = pack_bf16x2(__fmul_rn(x[8 + 2 * k], norm), __fmul_rn(x[8 + 2 * k + 1], norm));
+  }
+}
+
 __device__ __forceinline__ void flag_error(uint32_t* err, uint32_t bit) {
   if (err != nullptr) atomicOr(err, bit);
 }
@@ -424,6 +474,8 @@ struct KArgs {
   int64_t num_blocks;
   int meta_bulk;  // positions and slots 16-byte aligned: a full key item's
                   // positions/slots travel with its rows in the bulk copy
+  int64_t pos_mask;  // ~(compress_ratio - 1): a key takes the RoPE of its
+                     // group's first position, pos - pos % ratio
 };
 
 struct QArgs {
@@ -590,7 +642,7 @@ __device__ __forceinline__ int64_t lds_s64(uint32_t addr) {
 
 // A query item: heads h0 .. h0 + kChunkRows - 1 of token t, rows in the
 // stage; `ok` says whether the token's position was in range.
-template <int kStyle>
+template <int kStyle, bool kRotate>
 __device__ __forceinline__ void query_chunk(int32_t t, int32_t h0, bool ok, const Work& wk,
                                             const QArgs& qa, const Shared& sh, uint32_t stage) {
   const int lane = threadIdx.x & 31, j = lane & 7, rg = lane >> 3;
@@ -616,6 +668,7 @@ __device__ __forceinline__ void query_chunk(int32_t t, int32_t h0, bool ok, cons
     lds128(rows + (uint32_t)r * kRowBytes, a);
     lds128(rows + (uint32_t)r * kRowBytes + 128u, b);
     rope_lane<kStyle>(a, rc, sh.neg_zero);
+    if constexpr (kRotate) hadamard_lane(a, b, j);
     uint32_t pa, pb, ew;
     quant_lane(a, b, j, pa, pb, ew);
     if (r < n) {
@@ -659,11 +712,12 @@ __device__ __forceinline__ KeyMeta key_meta(int32_t t0, const KArgs& ka, const S
     }
   }
   if (!m.live) m.pos = 0;
+  m.pos &= ka.pos_mask;
   return m;
 }
 
 // A key item: tokens t0 .. t0 + kChunkRows - 1, rows in the stage.
-template <int kStyle>
+template <int kStyle, bool kRotate>
 __device__ __forceinline__ void key_chunk(int32_t t0, const Work& wk, const KArgs& ka,
                                           const Shared& sh, uint32_t stage) {
   const int lane = threadIdx.x & 31, j = lane & 7, rg = lane >> 3;
@@ -713,6 +767,7 @@ __device__ __forceinline__ void key_chunk(int32_t t0, const Work& wk, const KArg
       b[k] = pack_bf16x2(y0, y1);
     }
     rope_lane<kStyle>(a, rc, sh.neg_zero);
+    if constexpr (kRotate) hadamard_lane(a, b, j);
     uint32_t pa, pb, ew;
     quant_lane(a, b, j, pa, pb, ew);
     if (km.live) {
@@ -727,7 +782,7 @@ __device__ __forceinline__ void key_chunk(int32_t t0, const Work& wk, const KArg
 }
 
 // ------------------------------------------------------------------ kernel
-template <int kStyle>
+template <int kStyle, bool kRotate>
 __global__ void __launch_bounds__(kThreads, kMinBlocksPerSm)
     prepass_kernel(KArgs ka, QArgs qa, Shared sh, Work wk) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -784,9 +839,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSm)
     uint32_t hdr[4];
     lds128(stage + kStageHdr, hdr);
     if (hdr[0] == kItemKey)
-      key_chunk<kStyle>((int32_t)hdr[1], wk, ka, sh, stage);
+      key_chunk<kStyle, kRotate>((int32_t)hdr[1], wk, ka, sh, stage);
     else
-      query_chunk<kStyle>((int32_t)hdr[1], (int32_t)hdr[2], hdr[3] != 0, wk, qa, sh, stage);
+      query_chunk<kStyle, kRotate>((int32_t)hdr[1], (int32_t)hdr[2], hdr[3] != 0, wk, qa, sh,
+                                   stage);
     __syncwarp();
     bool v = false;
     if (lane == 0 && pr.a_kind != kItemNone) {
@@ -806,13 +862,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSm)
 constexpr int kMaxDevices = 64;
 struct DeviceInfo {
   int sm_count = 0;
-  int blocks_per_sm[2] = {0, 0};  // [style]
+  int blocks_per_sm[2][2] = {{0, 0}, {0, 0}};  // [style][rotate]
 };
 DeviceInfo g_devices[kMaxDevices];
 
-template <int kStyle>
+template <int kStyle, bool kRotate>
 int setup_kernel() {
-  auto kern = prepass_kernel<kStyle>;
+  auto kern = prepass_kernel<kStyle, kRotate>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
       cudaSuccess)
     return 0;
@@ -824,7 +880,7 @@ int setup_kernel() {
 }
 
 // CTAs that fit on the device at once, cached per device; 0 on a CUDA error.
-int resident_ctas(int style) {
+int resident_ctas(int style, int rotate) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
   DeviceInfo& di = g_devices[dev];
@@ -832,14 +888,18 @@ int resident_ctas(int style) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return 0;
-    const int n0 = setup_kernel<FP4IDX_ROPE_NEOX>();
-    const int n1 = setup_kernel<FP4IDX_ROPE_INTERLEAVED>();
-    if (n0 < 1 || n1 < 1) return 0;
-    di.blocks_per_sm[0] = n0;
-    di.blocks_per_sm[1] = n1;
+    const int n[2][2] = {
+        {setup_kernel<FP4IDX_ROPE_NEOX, false>(), setup_kernel<FP4IDX_ROPE_NEOX, true>()},
+        {setup_kernel<FP4IDX_ROPE_INTERLEAVED, false>(),
+         setup_kernel<FP4IDX_ROPE_INTERLEAVED, true>()}};
+    for (int a = 0; a < 2; ++a)
+      for (int b = 0; b < 2; ++b) {
+        if (n[a][b] < 1) return 0;
+        di.blocks_per_sm[a][b] = n[a][b];
+      }
     di.sm_count = sms;
   }
-  return di.sm_count * di.blocks_per_sm[style];
+  return di.sm_count * di.blocks_per_sm[style][rotate];
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -880,7 +940,7 @@ fp4idx_status check_queries(const void* q, int64_t q_tstride, int64_t q_hstride,
 }
 
 fp4idx_status launch(const KArgs& ka, const QArgs& qa, const Shared& sh, bool keys, bool queries,
-                     int rope_style, void* stream) {
+                     int rope_style, int rotate, void* stream) {
   // 32-bit indices: T * H and T itself below 2^30.
   const int64_t H = queries ? qa.H : 1;
   if (sh.T >= (1 << 30) || H >= (1 << 30) || sh.T * H >= (1 << 30)) return FP4IDX_ERR_SHAPE;
@@ -892,17 +952,38 @@ fp4idx_status launch(const KArgs& ka, const QArgs& qa, const Shared& sh, bool ke
   wk.nk = keys ? (wk.T + kChunkRows - 1) / kChunkRows : 0;
   wk.nq = queries ? wk.T * wk.cpt : 0;
   const int64_t total = (int64_t)wk.nk + wk.nq;
-  const int64_t resident = resident_ctas(rope_style);
+  const int64_t resident = resident_ctas(rope_style, rotate);
   if (resident <= 0) return FP4IDX_ERR_CUDA;
   const int64_t want = (total + kWarps - 1) / kWarps;  // at least one item per warp
   const int64_t grid = want < resident ? want : resident;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (rope_style == FP4IDX_ROPE_NEOX)
-    prepass_kernel<FP4IDX_ROPE_NEOX><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(ka, qa, sh, wk);
-  else
-    prepass_kernel<FP4IDX_ROPE_INTERLEAVED>
-        <<<(unsigned)grid, kThreads, kSmemBytes, s>>>(ka, qa, sh, wk);
+  const dim3 g((unsigned)grid);
+  if (rope_style == FP4IDX_ROPE_NEOX) {
+    if (rotate)
+      prepass_kernel<FP4IDX_ROPE_NEOX, true><<<g, kThreads, kSmemBytes, s>>>(ka, qa, sh, wk);
+    else
+      prepass_kernel<FP4IDX_ROPE_NEOX, false><<<g, kThreads, kSmemBytes, s>>>(ka, qa, sh, wk);
+  } else {
+    if (rotate)
+      prepass_kernel<FP4IDX_ROPE_INTERLEAVED, true><<<g, kThreads, kSmemBytes, s>>>(ka, qa, sh, wk);
+    else
+      prepass_kernel<FP4IDX_ROPE_INTERLEAVED, false><<<g, kThreads, kSmemBytes, s>>>(ka, qa, sh,
+                                                                                    wk);
+  }
   return cudaGetLastError() == cudaSuccess ? FP4IDX_OK : FP4IDX_ERR_CUDA;
+}
+
+// Options: NULL means the defaults (compress ratio 1, no rotation).
+fp4idx_status check_options(const fp4idx_options* o, int64_t& pos_mask, int& rotate) {
+  pos_mask = -1;
+  rotate = 0;
+  if (o == nullptr) return FP4IDX_OK;
+  if (o->compress_ratio != 1 && o->compress_ratio != 2 && o->compress_ratio != 4)
+    return FP4IDX_ERR_ARG;
+  if (o->hadamard != 0 && o->hadamard != 1) return FP4IDX_ERR_ARG;
+  pos_mask = ~(int64_t)(o->compress_ratio - 1);
+  rotate = o->hadamard;
+  return FP4IDX_OK;
 }
 
 }  // namespace
@@ -910,26 +991,69 @@ fp4idx_status launch(const KArgs& ka, const QArgs& qa, const Shared& sh, bool ke
 // ------------------------------------------------------------------- C ABI
 extern "C" {
 
-fp4idx_status fp4idx_k_norm_rope_pack_store(
+fp4idx_status fp4idx_k_norm_rope_pack_store_ex(
     const void* k, int64_t k_token_stride, const void* gamma, float eps,
     const int64_t* positions, const float* cos_cache, const float* sin_cache,
     int64_t max_pos, int rope_style, const int64_t* slot_mapping, uint8_t* kv_cache,
-    int64_t num_blocks, int64_t num_tokens, uint32_t* err_flags, void* stream) {
+    int64_t num_blocks, int64_t num_tokens, const fp4idx_options* options,
+    uint32_t* err_flags, void* stream) {
   if (num_tokens < 0) return FP4IDX_ERR_SHAPE;
   if (num_tokens == 0) return FP4IDX_OK;
   fp4idx_status st = check_shared(positions, cos_cache, sin_cache, max_pos, rope_style);
   if (st != FP4IDX_OK) return st;
   st = check_keys(k, k_token_stride, gamma, eps, slot_mapping, kv_cache, num_blocks);
   if (st != FP4IDX_OK) return st;
+  int64_t pos_mask;
+  int rotate;
+  st = check_options(options, pos_mask, rotate);
+  if (st != FP4IDX_OK) return st;
   if (err_flags && !aligned(err_flags, 4)) return FP4IDX_ERR_ALIGN;
 
   KArgs ka{static_cast<const uint16_t*>(k), k_token_stride, static_cast<const uint16_t*>(gamma),
            eps, slot_mapping, kv_cache, num_blocks,
-           aligned(positions, 16) && aligned(slot_mapping, 16) ? 1 : 0};
+           aligned(positions, 16) && aligned(slot_mapping, 16) ? 1 : 0, pos_mask};
   QArgs qa{};
   qa.H = 1;
   Shared sh{positions, cos_cache, sin_cache, max_pos, num_tokens, err_flags, -0.0f};
-  return launch(ka, qa, sh, true, false, rope_style, stream);
+  return launch(ka, qa, sh, true, false, rope_style, rotate, stream);
+}
+
+fp4idx_status fp4idx_k_norm_rope_pack_store(
+    const void* k, int64_t k_token_stride, const void* gamma, float eps,
+    const int64_t* positions, const float* cos_cache, const float* sin_cache,
+    int64_t max_pos, int rope_style, const int64_t* slot_mapping, uint8_t* kv_cache,
+    int64_t num_blocks, int64_t num_tokens, uint32_t* err_flags, void* stream) {
+  return fp4idx_k_norm_rope_pack_store_ex(k, k_token_stride, gamma, eps, positions, cos_cache,
+                                          sin_cache, max_pos, rope_style, slot_mapping, kv_cache,
+                                          num_blocks, num_tokens, nullptr, err_flags, stream);
+}
+
+fp4idx_status fp4idx_q_rope_pack_weights_ex(
+    const void* q, int64_t q_token_stride, int64_t q_head_stride, const void* w,
+    int64_t w_token_stride, float weight_scale, const int64_t* positions,
+    const float* cos_cache, const float* sin_cache, int64_t max_pos, int rope_style,
+    uint8_t* q_fp4, uint8_t* q_scale, float* weights_out, int64_t num_tokens,
+    int64_t num_heads, const fp4idx_options* options, uint32_t* err_flags, void* stream) {
+  if (num_tokens < 0) return FP4IDX_ERR_SHAPE;
+  if (num_tokens == 0) return FP4IDX_OK;
+  fp4idx_status st = check_shared(positions, cos_cache, sin_cache, max_pos, rope_style);
+  if (st != FP4IDX_OK) return st;
+  st = check_queries(q, q_token_stride, q_head_stride, w, weight_scale, q_fp4, q_scale,
+                     weights_out, num_tokens, num_heads);
+  if (st != FP4IDX_OK) return st;
+  int64_t pos_mask;
+  int rotate;
+  st = check_options(options, pos_mask, rotate);
+  if (st != FP4IDX_OK) return st;
+  if (err_flags && !aligned(err_flags, 4)) return FP4IDX_ERR_ALIGN;
+
+  KArgs ka{};
+  ka.pos_mask = -1;
+  QArgs qa{static_cast<const uint16_t*>(q), q_token_stride, q_head_stride,
+           static_cast<const uint16_t*>(w), w_token_stride, weight_scale, q_fp4, q_scale,
+           weights_out, num_heads};
+  Shared sh{positions, cos_cache, sin_cache, max_pos, num_tokens, err_flags, -0.0f};
+  return launch(ka, qa, sh, false, true, rope_style, rotate, stream);
 }
 
 fp4idx_status fp4idx_q_rope_pack_weights(
@@ -938,21 +1062,43 @@ fp4idx_status fp4idx_q_rope_pack_weights(
     const float* cos_cache, const float* sin_cache, int64_t max_pos, int rope_style,
     uint8_t* q_fp4, uint8_t* q_scale, float* weights_out, int64_t num_tokens,
     int64_t num_heads, uint32_t* err_flags, void* stream) {
+  return fp4idx_q_rope_pack_weights_ex(q, q_token_stride, q_head_stride, w, w_token_stride,
+                                       weight_scale, positions, cos_cache, sin_cache, max_pos,
+                                       rope_style, q_fp4, q_scale, weights_out, num_tokens,
+                                       num_heads, nullptr, err_flags, stream);
+}
+
+fp4idx_status fp4idx_indexer_prepass_ex(
+    const void* k, int64_t k_token_stride, const void* gamma, float eps,
+    const int64_t* slot_mapping, uint8_t* kv_cache, int64_t num_blocks, const void* q,
+    int64_t q_token_stride, int64_t q_head_stride, const void* w, int64_t w_token_stride,
+    float weight_scale, uint8_t* q_fp4, uint8_t* q_scale, float* weights_out,
+    int64_t num_heads, const int64_t* positions, const float* cos_cache,
+    const float* sin_cache, int64_t max_pos, int rope_style, int64_t num_tokens,
+    const fp4idx_options* options, uint32_t* err_flags, void* stream) {
   if (num_tokens < 0) return FP4IDX_ERR_SHAPE;
   if (num_tokens == 0) return FP4IDX_OK;
   fp4idx_status st = check_shared(positions, cos_cache, sin_cache, max_pos, rope_style);
   if (st != FP4IDX_OK) return st;
+  st = check_keys(k, k_token_stride, gamma, eps, slot_mapping, kv_cache, num_blocks);
+  if (st != FP4IDX_OK) return st;
   st = check_queries(q, q_token_stride, q_head_stride, w, weight_scale, q_fp4, q_scale,
                      weights_out, num_tokens, num_heads);
   if (st != FP4IDX_OK) return st;
+  int64_t pos_mask;
+  int rotate;
+  st = check_options(options, pos_mask, rotate);
+  if (st != FP4IDX_OK) return st;
   if (err_flags && !aligned(err_flags, 4)) return FP4IDX_ERR_ALIGN;
 
-  KArgs ka{};
+  KArgs ka{static_cast<const uint16_t*>(k), k_token_stride, static_cast<const uint16_t*>(gamma),
+           eps, slot_mapping, kv_cache, num_blocks,
+           aligned(positions, 16) && aligned(slot_mapping, 16) ? 1 : 0, pos_mask};
   QArgs qa{static_cast<const uint16_t*>(q), q_token_stride, q_head_stride,
            static_cast<const uint16_t*>(w), w_token_stride, weight_scale, q_fp4, q_scale,
            weights_out, num_heads};
   Shared sh{positions, cos_cache, sin_cache, max_pos, num_tokens, err_flags, -0.0f};
-  return launch(ka, qa, sh, false, true, rope_style, stream);
+  return launch(ka, qa, sh, true, true, rope_style, rotate, stream);
 }
 
 fp4idx_status fp4idx_indexer_prepass(
@@ -963,25 +1109,11 @@ fp4idx_status fp4idx_indexer_prepass(
     int64_t num_heads, const int64_t* positions, const float* cos_cache,
     const float* sin_cache, int64_t max_pos, int rope_style, int64_t num_tokens,
     uint32_t* err_flags, void* stream) {
-  if (num_tokens < 0) return FP4IDX_ERR_SHAPE;
-  if (num_tokens == 0) return FP4IDX_OK;
-  fp4idx_status st = check_shared(positions, cos_cache, sin_cache, max_pos, rope_style);
-  if (st != FP4IDX_OK) return st;
-  st = check_keys(k, k_token_stride, gamma, eps, slot_mapping, kv_cache, num_blocks);
-  if (st != FP4IDX_OK) return st;
-  st = check_queries(q, q_token_stride, q_head_stride, w, weight_scale, q_fp4, q_scale,
-                     weights_out, num_tokens, num_heads);
-  if (st != FP4IDX_OK) return st;
-  if (err_flags && !aligned(err_flags, 4)) return FP4IDX_ERR_ALIGN;
-
-  KArgs ka{static_cast<const uint16_t*>(k), k_token_stride, static_cast<const uint16_t*>(gamma),
-           eps, slot_mapping, kv_cache, num_blocks,
-           aligned(positions, 16) && aligned(slot_mapping, 16) ? 1 : 0};
-  QArgs qa{static_cast<const uint16_t*>(q), q_token_stride, q_head_stride,
-           static_cast<const uint16_t*>(w), w_token_stride, weight_scale, q_fp4, q_scale,
-           weights_out, num_heads};
-  Shared sh{positions, cos_cache, sin_cache, max_pos, num_tokens, err_flags, -0.0f};
-  return launch(ka, qa, sh, true, true, rope_style, stream);
+  return fp4idx_indexer_prepass_ex(k, k_token_stride, gamma, eps, slot_mapping, kv_cache,
+                                   num_blocks, q, q_token_stride, q_head_stride, w,
+                                   w_token_stride, weight_scale, q_fp4, q_scale, weights_out,
+                                   num_heads, positions, cos_cache, sin_cache, max_pos,
+                                   rope_style, num_tokens, nullptr, err_flags, stream);
 }
 
 const char* fp4idx_status_string(fp4idx_status status) {
@@ -990,12 +1122,12 @@ const char* fp4idx_status_string(fp4idx_status status) {
     case FP4IDX_ERR_NULL: return "a required pointer is NULL";
     case FP4IDX_ERR_SHAPE: return "invalid size (negative count, zero heads/blocks/positions, or overflow)";
     case FP4IDX_ERR_ALIGN: return "a pointer or stride breaks its alignment rule";
-    case FP4IDX_ERR_ARG: return "invalid argument (rope_style, eps or weight_scale)";
+    case FP4IDX_ERR_ARG: return "invalid argument (rope_style, eps, weight_scale or an option)";
     case FP4IDX_ERR_CUDA: return "CUDA launch failed";
   }
   return "unknown status";
 }
 
-const char* fp4idx_version(void) { return "fp4idx 0.3.0 sm_103a"; }
+const char* fp4idx_version(void) { return "fp4idx 0.4.0 sm_103a"; }
 
 }  // extern "C"

@@ -55,6 +55,15 @@ _SIGS = {
         _INT, [_P, _I64, _P, _F, _P, _P, _I64,
                _P, _I64, _I64, _P, _I64, _F, _P, _P, _P, _I64,
                _P, _P, _P, _I64, _INT, _I64, _P, _P]),
+    "fp4idx_k_norm_rope_pack_store_ex": (
+        _INT, [_P, _I64, _P, _F, _P, _P, _P, _I64, _INT, _P, _P, _I64, _I64, _P, _P, _P]),
+    "fp4idx_q_rope_pack_weights_ex": (
+        _INT, [_P, _I64, _I64, _P, _I64, _F, _P, _P, _P, _I64, _INT, _P, _P, _P, _I64,
+               _I64, _P, _P, _P]),
+    "fp4idx_indexer_prepass_ex": (
+        _INT, [_P, _I64, _P, _F, _P, _P, _I64,
+               _P, _I64, _I64, _P, _I64, _F, _P, _P, _P, _I64,
+               _P, _P, _P, _I64, _INT, _I64, _P, _P, _P]),
     "fp4idx_paged_mqa_logits": (
         _INT, [_P, _P, _P, _P, _I64, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _I64, _P, _P]),
     "fp4idx_status_string": (ctypes.c_char_p, [_INT]),
@@ -70,6 +79,19 @@ for _name, (_res, _args) in _SIGS.items():
 
 def lib() -> ctypes.CDLL:
     return _lib
+
+
+class Options(ctypes.Structure):
+    """fp4idx_options of include/fp4idx.h."""
+    _fields_ = [("compress_ratio", ctypes.c_int32), ("hadamard", ctypes.c_int32)]
+
+
+def _options(compress_ratio: int, hadamard: bool):
+    """None for the defaults (the plain entry points are called), else a
+    pointer to an Options block for the _ex entry points."""
+    if compress_ratio == 1 and not hadamard:
+        return None
+    return ctypes.pointer(Options(int(compress_ratio), 1 if hadamard else 0))
 
 
 def declared_symbols(header: str = HEADER_PATH) -> list:
@@ -142,10 +164,12 @@ def _ptr(t):
 
 def k_norm_rope_pack_store(k, gamma, positions, cos_cache, sin_cache, slot_mapping,
                            kv_cache, *, eps: float = 1e-6, rope_style="neox",
+                           compress_ratio: int = 1, hadamard: bool = False,
                            err_flags=None, stream=None) -> None:
     """Keys -> paged FP4 index cache, in place.  k bf16 [T,128] (row stride a
     multiple of 8), gamma bf16 [128], positions/slot_mapping int64 [T],
-    cos/sin fp32 [max_pos,32], kv_cache uint8 [num_blocks, 4352]."""
+    cos/sin fp32 [max_pos,32], kv_cache uint8 [num_blocks, 4352].
+    compress_ratio / hadamard select the stated variants (fp4idx_options)."""
     torch = _torch()
     _need(k, torch.bfloat16, "k", 2)
     _need(gamma, torch.bfloat16, "gamma", 1)
@@ -169,10 +193,15 @@ def k_norm_rope_pack_store(k, gamma, positions, cos_cache, sin_cache, slot_mappi
         raise ValueError("cos/sin caches must be contiguous")
     if kv_cache.shape[1] != PAGE_BYTES or not kv_cache.is_contiguous():
         raise ValueError("kv_cache must be contiguous [num_blocks, 4352]")
-    st = _lib.fp4idx_k_norm_rope_pack_store(
-        _ptr(k), k.stride(0), _ptr(gamma), float(eps), _ptr(positions), _ptr(cos_cache),
-        _ptr(sin_cache), cos_cache.shape[0], rope_style_code(rope_style), _ptr(slot_mapping),
-        _ptr(kv_cache), kv_cache.shape[0], T, _ptr(err_flags), _stream_ptr(stream))
+    args = (_ptr(k), k.stride(0), _ptr(gamma), float(eps), _ptr(positions), _ptr(cos_cache),
+            _ptr(sin_cache), cos_cache.shape[0], rope_style_code(rope_style),
+            _ptr(slot_mapping), _ptr(kv_cache), kv_cache.shape[0], T)
+    opts = _options(compress_ratio, hadamard)
+    if opts is None:
+        st = _lib.fp4idx_k_norm_rope_pack_store(*args, _ptr(err_flags), _stream_ptr(stream))
+    else:
+        st = _lib.fp4idx_k_norm_rope_pack_store_ex(*args, ctypes.cast(opts, _P),
+                                                   _ptr(err_flags), _stream_ptr(stream))
     _check(st, "fp4idx_k_norm_rope_pack_store")
 
 
@@ -216,23 +245,29 @@ def _check_q(q, w, positions, cos_cache, sin_cache):
 
 def q_rope_pack_weights(q, w, positions, cos_cache, sin_cache, *, rope_style="neox",
                         weight_scale=None, q_fp4=None, q_scale=None, weights=None,
-                        err_flags=None, stream=None):
+                        hadamard: bool = False, err_flags=None, stream=None):
     """Queries -> (q_fp4 uint8 [T,H,64], q_scale uint8 [T,H,4], weights fp32
     [T,H]).  q bf16 [T,H,128] (strides multiples of 8), w bf16 [T,H]."""
     T, H = _check_q(q, w, positions, cos_cache, sin_cache)
     q_fp4, q_scale, weights = _q_outputs(q_fp4, q_scale, weights, T, H, q.device)
     ws = default_weight_scale(H) if weight_scale is None else float(weight_scale)
-    st = _lib.fp4idx_q_rope_pack_weights(
-        _ptr(q), q.stride(0), q.stride(1), _ptr(w), w.stride(0), ws, _ptr(positions),
-        _ptr(cos_cache), _ptr(sin_cache), cos_cache.shape[0], rope_style_code(rope_style),
-        _ptr(q_fp4), _ptr(q_scale), _ptr(weights), T, H, _ptr(err_flags), _stream_ptr(stream))
+    args = (_ptr(q), q.stride(0), q.stride(1), _ptr(w), w.stride(0), ws, _ptr(positions),
+            _ptr(cos_cache), _ptr(sin_cache), cos_cache.shape[0], rope_style_code(rope_style),
+            _ptr(q_fp4), _ptr(q_scale), _ptr(weights), T, H)
+    opts = _options(1, hadamard)
+    if opts is None:
+        st = _lib.fp4idx_q_rope_pack_weights(*args, _ptr(err_flags), _stream_ptr(stream))
+    else:
+        st = _lib.fp4idx_q_rope_pack_weights_ex(*args, ctypes.cast(opts, _P), _ptr(err_flags),
+                                                _stream_ptr(stream))
     _check(st, "fp4idx_q_rope_pack_weights")
     return q_fp4, q_scale, weights
 
 
 def indexer_prepass(k, gamma, slot_mapping, kv_cache, q, w, positions, cos_cache, sin_cache, *,
                     eps: float = 1e-6, rope_style="neox", weight_scale=None, q_fp4=None,
-                    q_scale=None, weights=None, err_flags=None, stream=None):
+                    q_scale=None, weights=None, compress_ratio: int = 1,
+                    hadamard: bool = False, err_flags=None, stream=None):
     """Both halves in one launch; returns (q_fp4, q_scale, weights) and updates
     kv_cache in place.  Same argument rules as the two separate calls."""
     torch = _torch()
@@ -251,12 +286,16 @@ def indexer_prepass(k, gamma, slot_mapping, kv_cache, q, w, positions, cos_cache
         raise ValueError("kv_cache must be contiguous [num_blocks, 4352]")
     q_fp4, q_scale, weights = _q_outputs(q_fp4, q_scale, weights, T, H, q.device)
     ws = default_weight_scale(H) if weight_scale is None else float(weight_scale)
-    st = _lib.fp4idx_indexer_prepass(
-        _ptr(k), k.stride(0), _ptr(gamma), float(eps), _ptr(slot_mapping), _ptr(kv_cache),
-        kv_cache.shape[0], _ptr(q), q.stride(0), q.stride(1), _ptr(w), w.stride(0), ws,
-        _ptr(q_fp4), _ptr(q_scale), _ptr(weights), H, _ptr(positions), _ptr(cos_cache),
-        _ptr(sin_cache), cos_cache.shape[0], rope_style_code(rope_style), T, _ptr(err_flags),
-        _stream_ptr(stream))
+    args = (_ptr(k), k.stride(0), _ptr(gamma), float(eps), _ptr(slot_mapping), _ptr(kv_cache),
+            kv_cache.shape[0], _ptr(q), q.stride(0), q.stride(1), _ptr(w), w.stride(0), ws,
+            _ptr(q_fp4), _ptr(q_scale), _ptr(weights), H, _ptr(positions), _ptr(cos_cache),
+            _ptr(sin_cache), cos_cache.shape[0], rope_style_code(rope_style), T)
+    opts = _options(compress_ratio, hadamard)
+    if opts is None:
+        st = _lib.fp4idx_indexer_prepass(*args, _ptr(err_flags), _stream_ptr(stream))
+    else:
+        st = _lib.fp4idx_indexer_prepass_ex(*args, ctypes.cast(opts, _P), _ptr(err_flags),
+                                            _stream_ptr(stream))
     _check(st, "fp4idx_indexer_prepass")
     return q_fp4, q_scale, weights
 

@@ -70,8 +70,8 @@ typedef enum fp4idx_status {
   FP4IDX_ERR_SHAPE = 2, /* num_tokens < 0, num_heads < 1, max_pos < 1,
                            num_blocks < 1, or a size product overflows      */
   FP4IDX_ERR_ALIGN = 3, /* a pointer or stride breaks its alignment rule    */
-  FP4IDX_ERR_ARG = 4,   /* bad rope_style, eps not finite and > 0, or a
-                           non-finite weight_scale                           */
+  FP4IDX_ERR_ARG = 4,   /* bad rope_style, eps not finite and > 0, a
+                           non-finite weight_scale, or a bad option          */
   FP4IDX_ERR_CUDA = 5   /* the kernel launch failed                          */
 } fp4idx_status;
 
@@ -179,6 +179,62 @@ fp4idx_status fp4idx_indexer_prepass(
     const int64_t* positions, const float* cos_cache, const float* sin_cache,
     int64_t max_pos, int rope_style, int64_t num_tokens, uint32_t* err_flags,
     void* stream);
+
+/*
+ * Stated variants of the same two operations, selected by an options block
+ * (NULL = the defaults, identical to the calls above).
+ *
+ *   compress_ratio  1 (default), 2 or 4.  Compressed index keys take their
+ *                   RoPE at the first position of their group of
+ *                   compress_ratio consecutive positions: a key at position
+ *                   p is rotated with table row p - p % compress_ratio.
+ *                   Queries are never moved.  Source: "dsv4.1: RoPE and FP4
+ *                   packing kernels" (sglang PR 39656), Summary (RoPE at the
+ *                   group's first position) and Verification (compress
+ *                   ratios 1, 2, 4).
+ *   hadamard        0 (default) or 1.  After RoPE, every key and query row is
+ *                   rotated by the normalised 128-point Walsh-Hadamard
+ *                   transform (Sylvester order) before quantisation:
+ *                   fast-transform butterflies h = 1, 2, ..., 64 in fp32,
+ *                   each (a, b) -> (rn(a + b), rn(a - b)), then one product
+ *                   with rn32(1/sqrt(128)) and a bf16 rounding.  Rotating
+ *                   both sides keeps every query-key dot product.  Source:
+ *                   "DeepSeek-V4 FP4: fused_compress FP4 scatter +
+ *                   rmsnorm_rope_rotate FP4 KV-cache kernel" (aiter PR 4029),
+ *                   Changes (RMSNorm + RoPE + optional Hadamard rotate + FP4
+ *                   quant + paged KV-cache write).
+ * Any other value returns FP4IDX_ERR_ARG.  All other arguments, checks and
+ * results are those of the corresponding call above.
+ */
+typedef struct fp4idx_options {
+  int32_t compress_ratio;
+  int32_t hadamard;
+} fp4idx_options;
+
+fp4idx_status fp4idx_k_norm_rope_pack_store_ex(
+    const void* k, int64_t k_token_stride, const void* gamma, float eps,
+    const int64_t* positions, const float* cos_cache, const float* sin_cache,
+    int64_t max_pos, int rope_style, const int64_t* slot_mapping,
+    uint8_t* kv_cache, int64_t num_blocks, int64_t num_tokens,
+    const fp4idx_options* options, uint32_t* err_flags, void* stream);
+
+fp4idx_status fp4idx_q_rope_pack_weights_ex(
+    const void* q, int64_t q_token_stride, int64_t q_head_stride,
+    const void* w, int64_t w_token_stride, float weight_scale,
+    const int64_t* positions, const float* cos_cache, const float* sin_cache,
+    int64_t max_pos, int rope_style, uint8_t* q_fp4, uint8_t* q_scale,
+    float* weights_out, int64_t num_tokens, int64_t num_heads,
+    const fp4idx_options* options, uint32_t* err_flags, void* stream);
+
+fp4idx_status fp4idx_indexer_prepass_ex(
+    const void* k, int64_t k_token_stride, const void* gamma, float eps,
+    const int64_t* slot_mapping, uint8_t* kv_cache, int64_t num_blocks,
+    const void* q, int64_t q_token_stride, int64_t q_head_stride,
+    const void* w, int64_t w_token_stride, float weight_scale,
+    uint8_t* q_fp4, uint8_t* q_scale, float* weights_out, int64_t num_heads,
+    const int64_t* positions, const float* cos_cache, const float* sin_cache,
+    int64_t max_pos, int rope_style, int64_t num_tokens,
+    const fp4idx_options* options, uint32_t* err_flags, void* stream);
 
 /*
  * FP4 paged MQA-logits scorer: the consumer of the bytes written above.

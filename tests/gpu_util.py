@@ -40,7 +40,7 @@ class DeviceWorkload:
     def reset_cache(self):
         self.cache.copy_(torch.from_numpy(self.w.cache_init))
 
-    def run(self, mode: str = "fused"):
+    def run(self, mode: str = "fused", compress_ratio: int = 1, hadamard: bool = False):
         """Returns (cache, q_fp4, q_scale, weights) as numpy arrays."""
         f = F()
         w = self.w
@@ -48,31 +48,35 @@ class DeviceWorkload:
         if mode == "fused":
             qf, qs, wt = f.indexer_prepass(self.k, self.gamma, self.slots, self.cache, self.q,
                                            self.wt, self.pos, self.cos, self.sin, eps=w.eps,
-                                           rope_style=w.rope_style, err_flags=self.err)
+                                           rope_style=w.rope_style, err_flags=self.err,
+                                           compress_ratio=compress_ratio, hadamard=hadamard)
         else:
             f.k_norm_rope_pack_store(self.k, self.gamma, self.pos, self.cos, self.sin,
                                      self.slots, self.cache, eps=w.eps,
-                                     rope_style=w.rope_style, err_flags=self.err)
+                                     rope_style=w.rope_style, err_flags=self.err,
+                                     compress_ratio=compress_ratio, hadamard=hadamard)
             qf, qs, wt = f.q_rope_pack_weights(self.q, self.wt, self.pos, self.cos, self.sin,
-                                               rope_style=w.rope_style, err_flags=self.err)
+                                               rope_style=w.rope_style, err_flags=self.err,
+                                               hadamard=hadamard)
         torch.cuda.synchronize()
         return (self.cache.cpu().numpy(), qf.cpu().numpy(), qs.cpu().numpy(),
                 wt.cpu().numpy())
 
 
-def run_oracle(w: wl.Workload, tokens=None):
+def run_oracle(w: wl.Workload, tokens=None, compress_ratio: int = 1, hadamard: bool = False):
     """Oracle outputs; with `tokens`, the query side covers only those tokens
     (rows in the given order) while the key side always covers all tokens."""
     cache = w.cache_init.copy()
     oracle.k_norm_rope_pack_store(w.k, w.gamma, w.eps, w.positions, w.cos, w.sin,
-                                  w.rope_style, w.slot_mapping, cache)
+                                  w.rope_style, w.slot_mapping, cache,
+                                  compress_ratio=compress_ratio, hadamard=hadamard)
     if tokens is None:
         qf, qs, wt, _ = oracle.q_rope_pack_weights(w.q, w.w, w.positions, w.cos, w.sin,
-                                                   w.rope_style)
+                                                   w.rope_style, hadamard=hadamard)
     else:
         qf, qs, wt, _ = oracle.q_rope_pack_weights(w.q[tokens], w.w[tokens],
                                                    w.positions[tokens], w.cos, w.sin,
-                                                   w.rope_style)
+                                                   w.rope_style, hadamard=hadamard)
     return cache, qf, qs, wt
 
 

@@ -29,7 +29,9 @@ def test_exports_every_declared_symbol(F):
     names = F.declared_symbols()
     assert set(names) == {"fp4idx_k_norm_rope_pack_store", "fp4idx_q_rope_pack_weights",
                           "fp4idx_indexer_prepass", "fp4idx_paged_mqa_logits",
-                          "fp4idx_status_string", "fp4idx_version"}
+                          "fp4idx_k_norm_rope_pack_store_ex", "fp4idx_q_rope_pack_weights_ex",
+                          "fp4idx_indexer_prepass_ex", "fp4idx_status_string",
+                          "fp4idx_version"}
     out = subprocess.run(["nm", "-D", "--defined-only", F.LIB_PATH], capture_output=True,
                          text=True, check=True).stdout
     exported = set(re.findall(r"\bT (fp4idx_\w+)", out))
@@ -242,6 +244,29 @@ S_DEFECTS = [
 @pytest.mark.parametrize("over,code", S_DEFECTS, ids=_ids(S_DEFECTS))
 def test_scorer_host_checks(F, over, code):
     assert _call_s(F, _s_args(**over)) == getattr(F, code)
+
+
+@pytest.mark.fake_ptr
+@pytest.mark.parametrize("ratio,had", [(3, 0), (0, 0), (8, 0), (1, 2), (2, -1)])
+def test_option_host_checks(F, ratio, had):
+    """A bad options block is rejected on the host (ERR_ARG) by all three
+    variant entry points."""
+    import ctypes
+    opts = ctypes.cast(ctypes.pointer(F.Options(ratio, had)), ctypes.c_void_p)
+    ka, qa = _k_args(), _q_args(style=0)
+    assert F.lib().fp4idx_k_norm_rope_pack_store_ex(
+        ka["k"], ka["k_stride"], ka["gamma"], ka["eps"], ka["pos"], ka["cos"], ka["sin"],
+        ka["max_pos"], ka["style"], ka["slots"], ka["cache"], ka["num_blocks"], ka["T"], opts,
+        None, None) == F.ERR_ARG
+    assert F.lib().fp4idx_q_rope_pack_weights_ex(
+        qa["q"], qa["qts"], qa["qhs"], qa["w"], qa["wts"], qa["ws"], qa["pos"], qa["cos"],
+        qa["sin"], qa["max_pos"], qa["style"], qa["qf"], qa["qs"], qa["wt"], qa["T"], qa["H"],
+        opts, None, None) == F.ERR_ARG
+    assert F.lib().fp4idx_indexer_prepass_ex(
+        ka["k"], ka["k_stride"], ka["gamma"], ka["eps"], ka["slots"], ka["cache"],
+        ka["num_blocks"], qa["q"], qa["qts"], qa["qhs"], qa["w"], qa["wts"], qa["ws"],
+        qa["qf"], qa["qs"], qa["wt"], qa["H"], qa["pos"], qa["cos"], qa["sin"],
+        qa["max_pos"], qa["style"], qa["T"], opts, None, None) == F.ERR_ARG
 
 
 @pytest.mark.fake_ptr
