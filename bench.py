@@ -75,16 +75,17 @@ def measured_peak():
 
 def traffic_record(kernel: str):
     """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel source changed since the counters were taken."""
+    kernel's source file changed since the counters were taken."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
-    src = os.path.join(ROOT, "fp4_sparse_attention_fp4idx_gb300", "csrc", "fp4idx.cu")
     try:
         with open(p) as f:
             d = json.load(f)
-        with open(src, "rb") as f:
-            h = hashlib.sha256(f.read()).hexdigest()
         rec = d.get(kernel)
-        if rec and rec.get("source_sha256") == h:
+        if not rec:
+            return None
+        with open(os.path.join(ROOT, rec["source_file"]), "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()
+        if rec.get("source_sha256") == h:
             return rec
     except Exception:
         pass
@@ -436,6 +437,7 @@ def run_scorer(F, dev, peak, flush, steps: int, warmup: int = 5) -> dict:
     torch.cuda.synchronize()
     ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     nbytes = scorer_bytes(sw)
+    tr = traffic_record("scorer_kernel")
     ctx_tokens = int(np.minimum(np.maximum(sw.context_lens, 0), sw.max_context).sum())
     achieved = nbytes / (ms / 1e3) / 1e9
     flops = 2.0 * 128 * sw.next_n * sw.H * ctx_tokens
@@ -448,7 +450,7 @@ def run_scorer(F, dev, peak, flush, steps: int, warmup: int = 5) -> dict:
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "kernel": "scorer_kernel", "algorithmic_bytes_per_launch": nbytes,
-                     "traffic": None},
+                     "traffic": tr["dram_bytes_per_launch"] if tr else None},
         "mxf4_tflops": round(flops / (ms / 1e3) / 1e12, 1),
         "l2": "flushed before every launch, outside the CUDA events",
     }
