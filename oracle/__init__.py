@@ -26,6 +26,7 @@ PAYLOAD_BYTES = 64
 EXP_BYTES = 4
 KV_BLOCK = 64
 PAGE_BYTES = KV_BLOCK * (PAYLOAD_BYTES + EXP_BYTES)
+FP8_PAGE_BYTES = KV_BLOCK * (HEAD_DIM + 4)
 ROPE_NEOX = 0
 ROPE_INTERLEAVED = 1
 
@@ -74,6 +75,19 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.oracle_q_rope_pack_weights_ex.argtypes = [
         P, P, P, P, P, i64, ctypes.c_int, P, P, P, i64, i64, ctypes.c_int]
     L.oracle_q_rope_pack_weights_ex.restype = ctypes.c_int
+    L.oracle_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+    L.oracle_e4m3_to_f32.restype = ctypes.c_float
+    L.oracle_f32_to_e4m3.argtypes = [ctypes.c_float]
+    L.oracle_f32_to_e4m3.restype = ctypes.c_uint8
+    L.oracle_fp8_quant_row.argtypes = [P, P]
+    L.oracle_fp8_quant_row.restype = ctypes.c_int
+    L.oracle_k_norm_rope_fp8_store.argtypes = [
+        P, P, ctypes.c_float, P, P, P, i64, ctypes.c_int, P, P, i64, i64, ctypes.c_int,
+        ctypes.c_int]
+    L.oracle_k_norm_rope_fp8_store.restype = ctypes.c_int
+    L.oracle_q_rope_fp8_weights.argtypes = [
+        P, P, P, P, P, i64, ctypes.c_int, P, P, i64, i64, ctypes.c_int]
+    L.oracle_q_rope_fp8_weights.restype = ctypes.c_int
     L.oracle_paged_mqa_logits.argtypes = [
         P, P, P, P, i64, P, i64, P, P, i64, i64, i64, i64, i64]
     L.oracle_paged_mqa_logits.restype = ctypes.c_int
@@ -238,6 +252,62 @@ def q_rope_pack_weights(q, w, positions, cos_cache, sin_cache, rope_style,
         _p(q), _p(w), _p(pos), _p(cs), _p(sn), cs.shape[0], int(rope_style),
         _p(qf), _p(qs), _p(wt), T, H, int(bool(hadamard)))
     return qf, qs, wt, int(st)
+
+
+def e4m3_to_f32(c: int) -> float:
+    return float(lib().oracle_e4m3_to_f32(int(c)))
+
+
+def f32_to_e4m3(v: float) -> int:
+    return int(lib().oracle_f32_to_e4m3(float(v)))
+
+
+def fp8_quant_row(row_bits):
+    """(codes uint8 [128], biased exponent e of the row scale 2^(e-127))."""
+    r = _c(row_bits, np.uint16)
+    assert r.shape == (HEAD_DIM,)
+    codes = np.zeros(HEAD_DIM, np.uint8)
+    e = lib().oracle_fp8_quant_row(_p(r), _p(codes))
+    return codes, int(e)
+
+
+def k_norm_rope_fp8_store(k, gamma, eps, positions, cos_cache, sin_cache, rope_style,
+                          slot_mapping, kv_cache, compress_ratio: int = 1,
+                          hadamard: bool = False) -> int:
+    """FP8 mode; kv_cache (uint8 [num_blocks, 8448]) is updated in place."""
+    k = _c(k, np.uint16)
+    T = k.shape[0]
+    assert k.shape == (T, HEAD_DIM)
+    g = _c(gamma, np.uint16)
+    pos = _c(positions, np.int64)
+    cs = _c(cos_cache, np.float32)
+    sn = _c(sin_cache, np.float32)
+    sl = _c(slot_mapping, np.int64)
+    assert kv_cache.dtype == np.uint8 and kv_cache.flags.c_contiguous
+    assert kv_cache.shape[1:] == (FP8_PAGE_BYTES,)
+    return int(lib().oracle_k_norm_rope_fp8_store(
+        _p(k), _p(g), ctypes.c_float(eps), _p(pos), _p(cs), _p(sn), cs.shape[0],
+        int(rope_style), _p(sl), _p(kv_cache), kv_cache.shape[0], T, int(compress_ratio),
+        int(bool(hadamard))))
+
+
+def q_rope_fp8_weights(q, w, positions, cos_cache, sin_cache, rope_style,
+                       hadamard: bool = False):
+    """FP8 mode: (q_out [T,H,128] u8, weights [T,H] f32 with the scale folded in,
+    status)."""
+    q = _c(q, np.uint16)
+    T, H, D = q.shape
+    assert D == HEAD_DIM
+    w = _c(w, np.uint16)
+    pos = _c(positions, np.int64)
+    cs = _c(cos_cache, np.float32)
+    sn = _c(sin_cache, np.float32)
+    qo = np.zeros((T, H, HEAD_DIM), np.uint8)
+    wt = np.zeros((T, H), np.float32)
+    st = lib().oracle_q_rope_fp8_weights(
+        _p(q), _p(w), _p(pos), _p(cs), _p(sn), cs.shape[0], int(rope_style), _p(qo), _p(wt),
+        T, H, int(bool(hadamard)))
+    return qo, wt, int(st)
 
 
 def paged_mqa_logits(q_fp4, q_scale, weights, kv_cache, block_table, context_lens,

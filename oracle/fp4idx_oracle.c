@@ -252,14 +252,16 @@ void oracle_hadamard_row(uint16_t* y) {
  * Readings: a negative slot means "skip" (slot 0 is an ordinary slot); the
  * 68 bytes of a slot are split inside the 4352-byte page into the 64-byte
  * payload at o*64 and the 4-byte exponent word at 4096 + o*4. */
-int oracle_k_norm_rope_pack_store_ex(const uint16_t* k, const uint16_t* gamma,
-                                     float eps, const int64_t* positions,
-                                     const float* cos_cache,
-                                     const float* sin_cache, int64_t max_pos,
-                                     int rope_style, const int64_t* slot_mapping,
-                                     uint8_t* kv_cache, int64_t num_blocks,
-                                     int64_t num_tokens, int compress_ratio,
-                                     int hadamard) {
+static int fp8_quant_row(const uint16_t* row, uint8_t* codes);
+
+/* Both output modes share every step up to the quantisation: fp8 = 0 packs
+ * the FP4 slot (4352-byte pages), fp8 = 1 the FP8 slot (8448-byte pages). */
+static int key_pass(const uint16_t* k, const uint16_t* gamma, float eps,
+                    const int64_t* positions, const float* cos_cache,
+                    const float* sin_cache, int64_t max_pos, int rope_style,
+                    const int64_t* slot_mapping, uint8_t* kv_cache,
+                    int64_t num_blocks, int64_t num_tokens, int compress_ratio,
+                    int hadamard, int fp8) {
   int status = 0;
   for (int64_t t = 0; t < num_tokens; ++t) {
     int64_t slot = slot_mapping[t];
@@ -277,14 +279,34 @@ int oracle_k_norm_rope_pack_store_ex(const uint16_t* k, const uint16_t* gamma,
     oracle_rope_row(y, cos_cache + rope_pos * (ROPE_DIM / 2),
                     sin_cache + rope_pos * (ROPE_DIM / 2), rope_style);
     if (hadamard) oracle_hadamard_row(y);
+    int64_t b = slot / KV_BLOCK, o = slot % KV_BLOCK;
+    if (fp8) {
+      uint8_t* page = kv_cache + b * (int64_t)KV_BLOCK * (HEAD_DIM + 4);
+      int e = fp8_quant_row(y, page + o * HEAD_DIM);
+      float scale = (float)ldexp(1.0, e - 127);
+      memcpy(page + KV_BLOCK * HEAD_DIM + o * 4, &scale, 4);
+      continue;
+    }
     uint8_t payload[PAYLOAD_BYTES], ex[EXP_BYTES];
     oracle_quant_pack_row(y, payload, ex, NULL, NULL, NULL);
-    int64_t b = slot / KV_BLOCK, o = slot % KV_BLOCK;
     uint8_t* page = kv_cache + b * PAGE_BYTES;
     memcpy(page + o * PAYLOAD_BYTES, payload, PAYLOAD_BYTES);
     memcpy(page + KV_BLOCK * PAYLOAD_BYTES + o * EXP_BYTES, ex, EXP_BYTES);
   }
   return status;
+}
+
+int oracle_k_norm_rope_pack_store_ex(const uint16_t* k, const uint16_t* gamma,
+                                     float eps, const int64_t* positions,
+                                     const float* cos_cache,
+                                     const float* sin_cache, int64_t max_pos,
+                                     int rope_style, const int64_t* slot_mapping,
+                                     uint8_t* kv_cache, int64_t num_blocks,
+                                     int64_t num_tokens, int compress_ratio,
+                                     int hadamard) {
+  return key_pass(k, gamma, eps, positions, cos_cache, sin_cache, max_pos,
+                  rope_style, slot_mapping, kv_cache, num_blocks, num_tokens,
+                  compress_ratio, hadamard, 0);
 }
 
 int oracle_k_norm_rope_pack_store(const uint16_t* k, const uint16_t* gamma,
@@ -303,13 +325,15 @@ int oracle_k_norm_rope_pack_store(const uint16_t* k, const uint16_t* gamma,
 /* Queries ([sgl] Summary: the query op rotates, quantises and packs the same
  * way and computes the head weights in the same launch; [aiter] API: weights
  * carry the plain weight, fp32 here, nothing folded in). */
-int oracle_q_rope_pack_weights_ex(const uint16_t* q, const uint16_t* w,
-                                  const int64_t* positions,
-                                  const float* cos_cache, const float* sin_cache,
-                                  int64_t max_pos, int rope_style,
-                                  uint8_t* q_fp4, uint8_t* q_scale,
-                                  float* weights, int64_t num_tokens,
-                                  int64_t num_heads, int hadamard) {
+/* fp8 = 0: packed FP4 queries, exponent words and plain weights; fp8 = 1:
+ * E4M3 codes, the row's scale folded into its weight ([aiter] Summary: the
+ * FP8 path folds its per-(token, head) q_scale into the weights). */
+static int query_pass(const uint16_t* q, const uint16_t* w,
+                      const int64_t* positions, const float* cos_cache,
+                      const float* sin_cache, int64_t max_pos, int rope_style,
+                      uint8_t* q_out, uint8_t* q_scale, float* weights,
+                      int64_t num_tokens, int64_t num_heads, int hadamard,
+                      int fp8) {
   int status = 0;
   double wscale = 1.0 / sqrt((double)num_heads * (double)HEAD_DIM);
   for (int64_t t = 0; t < num_tokens; ++t) {
@@ -325,12 +349,27 @@ int oracle_q_rope_pack_weights_ex(const uint16_t* q, const uint16_t* w,
       oracle_rope_row(y, cos_cache + pos * (ROPE_DIM / 2),
                       sin_cache + pos * (ROPE_DIM / 2), rope_style);
       if (hadamard) oracle_hadamard_row(y);
-      oracle_quant_pack_row(y, q_fp4 + r * PAYLOAD_BYTES,
-                            q_scale + r * EXP_BYTES, NULL, NULL, NULL);
-      weights[r] = (float)((double)bf16_to_f32(w[r]) * wscale);
+      double folded = 1.0;
+      if (fp8)
+        folded = ldexp(1.0, fp8_quant_row(y, q_out + r * HEAD_DIM) - 127);
+      else
+        oracle_quant_pack_row(y, q_out + r * PAYLOAD_BYTES,
+                              q_scale + r * EXP_BYTES, NULL, NULL, NULL);
+      weights[r] = (float)((double)bf16_to_f32(w[r]) * wscale * folded);
     }
   }
   return status;
+}
+
+int oracle_q_rope_pack_weights_ex(const uint16_t* q, const uint16_t* w,
+                                  const int64_t* positions,
+                                  const float* cos_cache, const float* sin_cache,
+                                  int64_t max_pos, int rope_style,
+                                  uint8_t* q_fp4, uint8_t* q_scale,
+                                  float* weights, int64_t num_tokens,
+                                  int64_t num_heads, int hadamard) {
+  return query_pass(q, w, positions, cos_cache, sin_cache, max_pos, rope_style,
+                    q_fp4, q_scale, weights, num_tokens, num_heads, hadamard, 0);
 }
 
 int oracle_q_rope_pack_weights(const uint16_t* q, const uint16_t* w,
@@ -343,6 +382,89 @@ int oracle_q_rope_pack_weights(const uint16_t* q, const uint16_t* w,
   return oracle_q_rope_pack_weights_ex(q, w, positions, cos_cache, sin_cache,
                                        max_pos, rope_style, q_fp4, q_scale,
                                        weights, num_tokens, num_heads, 0);
+}
+
+/* ---- FP8 output mode ([aiter] Summary and API: the FP8 contract that the
+ * FP4 mode extends; the FP8 path folds its per-(token, head) query scale
+ * into the head weights).  Readings: E4M3 codes (the e4m3fn format: bias 7,
+ * 3 mantissa bits, no infinities, largest finite 448, subnormals m * 2^-9),
+ * one power-of-two (UE8M0) scale per 128-element row, and a key slot of 128
+ * code bytes plus the scale as an fp32 value, page-split like the FP4 slots
+ * (64 x 128 code bytes, then 64 x 4 scale bytes: 8448-byte pages). ---- */
+
+float oracle_e4m3_to_f32(uint8_t c) {
+  int sign = c >> 7, ex = (c >> 3) & 15, man = c & 7;
+  if (ex == 15 && man == 7) return NAN;
+  double v = ex == 0 ? ldexp((double)man, -9) : ldexp(1.0 + man / 8.0, ex - 7);
+  return (float)(sign ? -v : v);
+}
+
+/* Nearest finite E4M3 value by brute force over the 127 non-negative finite
+ * codes; a tie goes to the code with an even mantissa (round half to even);
+ * magnitudes above 448 saturate to 448; the sign is kept, zero included. */
+uint8_t oracle_f32_to_e4m3(float v) {
+  double a = fabs((double)v);
+  int best = 0;
+  double best_d = INFINITY;
+  for (int c = 0; c < 127; ++c) {
+    double d = fabs((double)oracle_e4m3_to_f32((uint8_t)c) - a);
+    if (d < best_d || (d == best_d && (c % 2) == 0 && (best % 2) != 0)) {
+      best = c;
+      best_d = d;
+    }
+  }
+  if (a > 448.0) best = 126;
+  return (uint8_t)(best | (signbit(v) ? 0x80 : 0));
+}
+
+/* One 128-element row: e = biased exponent of ceil_pow2(max(amax/448,
+ * 2^-126)) (the same power-of-two rounding and floor as the FP4 scales),
+ * codes of x * 2^(127 - e).  Returns e. */
+int oracle_fp8_quant_row(const uint16_t* row, uint8_t* codes) {
+  return fp8_quant_row(row, codes);
+}
+
+static int fp8_quant_row(const uint16_t* row, uint8_t* codes) {
+  float amax = 0.0f;
+  for (int i = 0; i < HEAD_DIM; ++i) {
+    float a = fabsf(bf16_to_f32(row[i]));
+    if (a > amax) amax = a;
+  }
+  float t = amax / 448.0f;
+  if (t < STAGE1_FLOOR) t = STAGE1_FLOOR;
+  uint32_t bits = f2u(t);
+  int e = (int)(bits >> 23) + (int)((bits & 0x7fffffu) != 0u);
+  if (e < 1) e = 1;
+  if (e > 254) e = 254;
+  for (int i = 0; i < HEAD_DIM; ++i) {
+    double x = (double)bf16_to_f32(row[i]) * ldexp(1.0, 127 - e);
+    codes[i] = oracle_f32_to_e4m3((float)x);
+  }
+  return e;
+}
+
+enum { FP8_PAGE_BYTES = KV_BLOCK * (HEAD_DIM + 4) /* 8448 */ };
+
+int oracle_k_norm_rope_fp8_store(const uint16_t* k, const uint16_t* gamma,
+                                 float eps, const int64_t* positions,
+                                 const float* cos_cache, const float* sin_cache,
+                                 int64_t max_pos, int rope_style,
+                                 const int64_t* slot_mapping, uint8_t* kv_cache,
+                                 int64_t num_blocks, int64_t num_tokens,
+                                 int compress_ratio, int hadamard) {
+  return key_pass(k, gamma, eps, positions, cos_cache, sin_cache, max_pos,
+                  rope_style, slot_mapping, kv_cache, num_blocks, num_tokens,
+                  compress_ratio, hadamard, 1);
+}
+
+int oracle_q_rope_fp8_weights(const uint16_t* q, const uint16_t* w,
+                              const int64_t* positions, const float* cos_cache,
+                              const float* sin_cache, int64_t max_pos,
+                              int rope_style, uint8_t* q_out, float* weights,
+                              int64_t num_tokens, int64_t num_heads,
+                              int hadamard) {
+  return query_pass(q, w, positions, cos_cache, sin_cache, max_pos, rope_style,
+                    q_out, NULL, weights, num_tokens, num_heads, hadamard, 1);
 }
 
 /* The scorer ([aiter] Verification, End-to-end: the FP4 paged MQA-logits

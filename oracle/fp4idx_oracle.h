@@ -123,6 +123,32 @@ int oracle_q_rope_pack_weights_ex(const uint16_t* q, const uint16_t* w,
                                   float* weights, int64_t num_tokens,
                                   int64_t num_heads, int hadamard);
 
+/* ---- FP8 output mode (E4M3 codes, one power-of-two scale per row) ---- */
+
+float oracle_e4m3_to_f32(uint8_t c);
+/* Nearest E4M3, ties to even mantissa, |v| > 448 saturates, sign kept. */
+uint8_t oracle_f32_to_e4m3(float v);
+/* 128 codes of one bf16 row; returns the biased exponent e of the row's
+ * scale 2^(e-127) = ceil_pow2(max(amax/448, 2^-126)). */
+int oracle_fp8_quant_row(const uint16_t* row, uint8_t* codes);
+/* Keys -> FP8 paged cache [num_blocks, 8448]: page b holds 64 code rows of
+ * 128 bytes at o*128, then 64 fp32 scales at 8192 + o*4. */
+int oracle_k_norm_rope_fp8_store(const uint16_t* k, const uint16_t* gamma,
+                                 float eps, const int64_t* positions,
+                                 const float* cos_cache, const float* sin_cache,
+                                 int64_t max_pos, int rope_style,
+                                 const int64_t* slot_mapping, uint8_t* kv_cache,
+                                 int64_t num_blocks, int64_t num_tokens,
+                                 int compress_ratio, int hadamard);
+/* Queries -> q_out [T,H,128] E4M3 codes and weights [T,H] fp32 with the
+ * row's scale folded in: w * H^-1/2 * D^-1/2 * 2^(e-127), rounded once. */
+int oracle_q_rope_fp8_weights(const uint16_t* q, const uint16_t* w,
+                              const int64_t* positions, const float* cos_cache,
+                              const float* sin_cache, int64_t max_pos,
+                              int rope_style, uint8_t* q_out, float* weights,
+                              int64_t num_tokens, int64_t num_heads,
+                              int hadamard);
+
 /* FP4 paged MQA-logits scorer (the consumer of the packed queries and the
  * paged index-K cache).  Query row t = b*next_n + j of sequence b scores
  * every cached token s < context_lens[b]:

@@ -7,6 +7,7 @@ import pytest
 
 import oracle
 from tests import test_oracle_pins as pins
+from tests import test_oracle_fp8 as fpins
 from tests import test_oracle_variants as vpins
 from tests import test_scorer_oracle as spins
 
@@ -81,9 +82,21 @@ MUTANTS = [
      "int64_t rope_pos = pos / compress_ratio;"),
     ("compress_ignored", "int64_t rope_pos = pos - pos % compress_ratio;",
      "int64_t rope_pos = pos;"),
-    ("k_hadamard_skipped", "    if (hadamard) oracle_hadamard_row(y);\n    uint8_t payload", "    uint8_t payload"),
-    ("q_hadamard_skipped", "      if (hadamard) oracle_hadamard_row(y);\n      oracle_quant_pack_row",
-     "      oracle_quant_pack_row"),
+    ("k_hadamard_skipped", "    if (hadamard) oracle_hadamard_row(y);\n    int64_t b = slot",
+     "    int64_t b = slot"),
+    ("fp8_max_240", "float t = amax / 448.0f;", "float t = amax / 240.0f;"),
+    ("fp8_scale_floor_not_ceil", "+ (int)((bits & 0x7fffffu) != 0u);", "+ 0;"),
+    ("fp8_ties_down", "if (d < best_d || (d == best_d && (c % 2) == 0 && (best % 2) != 0)) {",
+     "if (d < best_d) {"),
+    ("fp8_sign_dropped", "return (uint8_t)(best | (signbit(v) ? 0x80 : 0));",
+     "return (uint8_t)best;"),
+    ("fp8_weight_scale_not_folded",
+     "folded = ldexp(1.0, fp8_quant_row(y, q_out + r * HEAD_DIM) - 127);",
+     "fp8_quant_row(y, q_out + r * HEAD_DIM);"),
+    ("fp8_scale_slot_interleaved", "memcpy(page + KV_BLOCK * HEAD_DIM + o * 4, &scale, 4);",
+     "memcpy(page + KV_BLOCK * HEAD_DIM + (63 - o) * 4, &scale, 4);"),
+    ("q_hadamard_skipped", "      if (hadamard) oracle_hadamard_row(y);\n      double folded",
+     "      double folded"),
 ]
 
 # Independent pins, cheapest first.
@@ -114,6 +127,13 @@ PINS = [
     vpins.test_query_rotation_sign_pattern,
     vpins.test_key_rotation_sign_pattern,
     vpins.test_compress_ratio_uses_group_first_position,
+    fpins.test_encode_saturates_above_448,
+    fpins.test_all_zero_row_floor,
+    fpins.test_key_slot_closed_form,
+    fpins.test_query_weight_folds_scale,
+    fpins.test_decode_all_codes_match_torch,
+    fpins.test_encode_matches_torch_in_range,
+    fpins.test_row_exponent_exact,
     pins.test_two_stage_invariants,
     pins.test_group_quant_exact_rational,
     pins.test_exponent_exhaustive_bf16,
