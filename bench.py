@@ -361,14 +361,24 @@ def run_variants(F, w, D, dev, peak, flush, steps: int = 100, warmup: int = 5) -
     p = {k: v.data_ptr() for k, v in D.items()}
     st = torch.cuda.current_stream()
     fn = F.lib().fp4idx_indexer_prepass_ex
-    nbytes = algorithmic_bytes(w, "fused")["fused"]
+    nbytes4 = algorithmic_bytes(w, "fused")["fused"]
+    # FP8 mode: per query row 256 + 2 + 128 (codes) + 4 (weight), per stored
+    # key row 256 + 132 (slot); no exponent words for queries
+    nv = algorithmic_bytes(w, "fused")["n_valid"]
+    nbytes8 = nbytes4 + T * H * (128 - 64 - 4) + nv * (132 - 68)
+    q8 = torch.empty((T, H, 128), dtype=torch.uint8, device=dev)
+    cache8 = torch.zeros((w.num_blocks, F.FP8_PAGE_BYTES), dtype=torch.uint8, device=dev)
     out = {}
-    for name, ratio, had in (("hadamard", 1, 1), ("compress_ratio_4", 4, 0),
-                             ("compress_ratio_4_hadamard", 4, 1)):
-        opts = ctypes.cast(ctypes.pointer(F.Options(ratio, had)), ctypes.c_void_p)
-        args = (p["k"], 128, p["gamma"], w.eps, p["slots"], p["cache"], w.num_blocks, p["q"],
-                H * 128, 128, p["w"], H, F.default_weight_scale(H), qf.data_ptr(),
-                qs.data_ptr(), wt.data_ptr(), H, p["pos"], p["cos"], p["sin"], w.max_pos,
+    for name, ratio, had, mode in (("hadamard", 1, 1, 0), ("compress_ratio_4", 4, 0, 0),
+                                   ("compress_ratio_4_hadamard", 4, 1, 0), ("fp8", 1, 0, 1),
+                                   ("fp8_hadamard", 1, 1, 1)):
+        opts = ctypes.cast(ctypes.pointer(F.Options(ratio, had, mode)), ctypes.c_void_p)
+        nbytes = nbytes8 if mode else nbytes4
+        args = (p["k"], 128, p["gamma"], w.eps, p["slots"],
+                cache8.data_ptr() if mode else p["cache"], w.num_blocks, p["q"],
+                H * 128, 128, p["w"], H, F.default_weight_scale(H),
+                q8.data_ptr() if mode else qf.data_ptr(), None if mode else qs.data_ptr(),
+                wt.data_ptr(), H, p["pos"], p["cos"], p["sin"], w.max_pos,
                 w.rope_style, T, opts, None, st.cuda_stream)
         for _ in range(warmup):
             flush()
@@ -384,7 +394,8 @@ def run_variants(F, w, D, dev, peak, flush, steps: int = 100, warmup: int = 5) -
         ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
         gbs = nbytes / (ms / 1e3) / 1e9
         out[name] = {"ms_per_launch": round(ms, 5), "tokens_per_s": round(T / (ms / 1e3), 1),
-                     "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}
+                     "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+                     "algorithmic_bytes_per_launch": nbytes}
     return out
 
 

@@ -96,6 +96,10 @@ constexpr int kKvBlock = FP4IDX_KV_BLOCK;
 constexpr int kPageBytes = FP4IDX_PAGE_BYTES;
 constexpr int kPayloadBytes = FP4IDX_SLOT_PAYLOAD_BYTES;
 constexpr int kExpOffset = kKvBlock * kPayloadBytes;  // 4096
+// FP8 output mode: slots of 128 E4M3 codes + a 4-byte fp32 scale, page-split
+// (64 x 128 code bytes, then 64 scales).
+constexpr int kFp8PageBytes = FP4IDX_FP8_PAGE_BYTES;             // 8448
+constexpr int kFp8ScaleOffset = kKvBlock * FP4IDX_HEAD_DIM;      // 8192
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per stage wait
 
 // ------------------------------------------------------------ PTX helpers
@@ -327,6 +331,47 @@ __device__ __forceinline__ void quant_lane(const uint32_t (&a)[4], const uint32_
   const uint32_t e2 = 0x00fe00feu - ie - (ha2 ? 1u : 0u) - (hb2 ? 0x10000u : 0u);
   const uint32_t x = e2 << (8 * (j >> 2));
   ew = x | __shfl_xor_sync(kFull, x, 4);
+}
+
+// Four fp32 values -> four E4M3 codes (round half to even, saturating at
+// 448), element 0 in the low byte.
+__device__ __forceinline__ uint32_t e4m3x4(float v0, float v1, float v2, float v3) {
+  uint32_t w;
+  asm("{\n\t.reg .b16 h0, h1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 h0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 h1, %4, %3;\n\t"
+      "mov.b32 %0, {h0, h1};\n\t}"
+      : "=r"(w)
+      : "f"(v0), "f"(v1), "f"(v2), "f"(v3));
+  return w;
+}
+
+// FP8 mode for this lane's two 8-element parts of its row (a = dims
+// 8j..8j+7, b = dims 64+8j..64+8j+7).  All 32 lanes must call (shuffles).
+// The row's scale is 2^(e-127) = ceil_pow2(max(rn(amax/448), 2^-126)); the
+// codes are E4M3 of x * 2^(127-e) (an exact product).  Returns the codes of
+// a and b (8 bytes each) and e.
+__device__ __forceinline__ void quant_lane_fp8(const uint32_t (&a)[4], const uint32_t (&b)[4],
+                                               uint2& ca, uint2& cb, uint32_t& e) {
+  uint32_t m = hmax_abs(hmax_abs(hmax_abs(a[0], a[1]), hmax_abs(a[2], a[3])),
+                        hmax_abs(hmax_abs(b[0], b[1]), hmax_abs(b[2], b[3])));
+  m = hmax_abs(m, prmt(m, m, 0x1032u));  // both halves
+  m = hmax_abs(m, __shfl_xor_sync(kFull, m, 1));
+  m = hmax_abs(m, __shfl_xor_sync(kFull, m, 2));
+  m = hmax_abs(m, __shfl_xor_sync(kFull, m, 4));
+  const float amax = __uint_as_float((m & 0x7fffu) << 16);
+  const float t = fmaxf(__fdiv_rn(amax, 448.0f), 1.17549435082228750797e-38f);
+  const uint32_t tb = __float_as_uint(t);
+  e = (tb >> 23) + ((tb & 0x7fffffu) != 0u ? 1u : 0u);  // 1 .. 248 for finite bf16
+  const float inv = __uint_as_float((254u - e) << 23);  // 2^(127-e), a normal float
+  float va[8], vb[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    mul2(va[2 * k], va[2 * k + 1], bf16_lo(a[k]), bf16_hi(a[k]), inv, inv);
+    mul2(vb[2 * k], vb[2 * k + 1], bf16_lo(b[k]), bf16_hi(b[k]), inv, inv);
+  }
+  ca = make_uint2(e4m3x4(va[0], va[1], va[2], va[3]), e4m3x4(va[4], va[5], va[6], va[7]));
+  cb = make_uint2(e4m3x4(vb[0], vb[1], vb[2], vb[3]), e4m3x4(vb[4], vb[5], vb[6], vb[7]));
 }
 
 // RoPE coefficients of lane j for one position, as fp32 pairs.
@@ -642,7 +687,7 @@ __device__ __forceinline__ int64_t lds_s64(uint32_t addr) {
 
 // A query item: heads h0 .. h0 + kChunkRows - 1 of token t, rows in the
 // stage; `ok` says whether the token's position was in range.
-template <int kStyle, bool kRotate>
+template <int kStyle, bool kRotate, bool kFp8>
 __device__ __forceinline__ void query_chunk(int32_t t, int32_t h0, bool ok, const Work& wk,
                                             const QArgs& qa, const Shared& sh, uint32_t stage) {
   const int lane = threadIdx.x & 31, j = lane & 7, rg = lane >> 3;
@@ -669,15 +714,30 @@ __device__ __forceinline__ void query_chunk(int32_t t, int32_t h0, bool ok, cons
     lds128(rows + (uint32_t)r * kRowBytes + 128u, b);
     rope_lane<kStyle>(a, rc, sh.neg_zero);
     if constexpr (kRotate) hadamard_lane(a, b, j);
-    uint32_t pa, pb, ew;
-    quant_lane(a, b, j, pa, pb, ew);
-    if (r < n) {
-      *reinterpret_cast<uint32_t*>(out + r * kPayloadBytes) = pa;
-      *reinterpret_cast<uint32_t*>(out + r * kPayloadBytes + 32) = pb;
-      if (j == 0) *reinterpret_cast<uint32_t*>(scl + 4 * r) = ew;
+    if constexpr (kFp8) {
+      // codes at q_out + row*128; the row's scale folded into its weight
+      uint2 ca, cb;
+      uint32_t e;
+      quant_lane_fp8(a, b, ca, cb, e);
+      const float wr = __uint_as_float((uint32_t)__shfl_sync(kFull, (uint32_t)wb, r) << 16);
+      if (r < n) {
+        uint8_t* q8 = qa.q_fp4 + (int64_t)(row0 + r) * FP4IDX_HEAD_DIM + 8 * j;
+        *reinterpret_cast<uint2*>(q8) = ca;
+        *reinterpret_cast<uint2*>(q8 + 64) = cb;
+        if (j == 0)
+          qa.weights[row0 + r] = __fmul_rn(__fmul_rn(wr, qa.wscale), __uint_as_float(e << 23));
+      }
+    } else {
+      uint32_t pa, pb, ew;
+      quant_lane(a, b, j, pa, pb, ew);
+      if (r < n) {
+        *reinterpret_cast<uint32_t*>(out + r * kPayloadBytes) = pa;
+        *reinterpret_cast<uint32_t*>(out + r * kPayloadBytes + 32) = pb;
+        if (j == 0) *reinterpret_cast<uint32_t*>(scl + 4 * r) = ew;
+      }
     }
   }
-  if (lane < n)
+  if (!kFp8 && lane < n)
     qa.weights[row0 + lane] = __fmul_rn(__uint_as_float((uint32_t)wb << 16), qa.wscale);
 }
 
@@ -717,7 +777,7 @@ __device__ __forceinline__ KeyMeta key_meta(int32_t t0, const KArgs& ka, const S
 }
 
 // A key item: tokens t0 .. t0 + kChunkRows - 1, rows in the stage.
-template <int kStyle, bool kRotate>
+template <int kStyle, bool kRotate, bool kFp8>
 __device__ __forceinline__ void key_chunk(int32_t t0, const Work& wk, const KArgs& ka,
                                           const Shared& sh, uint32_t stage) {
   const int lane = threadIdx.x & 31, j = lane & 7, rg = lane >> 3;
@@ -768,6 +828,20 @@ __device__ __forceinline__ void key_chunk(int32_t t0, const Work& wk, const KArg
     }
     rope_lane<kStyle>(a, rc, sh.neg_zero);
     if constexpr (kRotate) hadamard_lane(a, b, j);
+    if constexpr (kFp8) {
+      uint2 ca, cb;
+      uint32_t e;
+      quant_lane_fp8(a, b, ca, cb, e);
+      if (km.live) {
+        uint8_t* page = ka.cache + (km.slot / kKvBlock) * (int64_t)kFp8PageBytes;
+        const int64_t o = km.slot % kKvBlock;
+        uint8_t* dst = page + o * FP4IDX_HEAD_DIM + 8 * j;
+        *reinterpret_cast<uint2*>(dst) = ca;
+        *reinterpret_cast<uint2*>(dst + 64) = cb;
+        if (j == 0) *reinterpret_cast<uint32_t*>(page + kFp8ScaleOffset + 4 * o) = e << 23;
+      }
+      continue;
+    }
     uint32_t pa, pb, ew;
     quant_lane(a, b, j, pa, pb, ew);
     if (km.live) {
@@ -782,7 +856,7 @@ __device__ __forceinline__ void key_chunk(int32_t t0, const Work& wk, const KArg
 }
 
 // ------------------------------------------------------------------ kernel
-template <int kStyle, bool kRotate>
+template <int kStyle, bool kRotate, bool kFp8>
 __global__ void __launch_bounds__(kThreads, kMinBlocksPerSm)
     prepass_kernel(KArgs ka, QArgs qa, Shared sh, Work wk) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -839,10 +913,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSm)
     uint32_t hdr[4];
     lds128(stage + kStageHdr, hdr);
     if (hdr[0] == kItemKey)
-      key_chunk<kStyle, kRotate>((int32_t)hdr[1], wk, ka, sh, stage);
+      key_chunk<kStyle, kRotate, kFp8>((int32_t)hdr[1], wk, ka, sh, stage);
     else
-      query_chunk<kStyle, kRotate>((int32_t)hdr[1], (int32_t)hdr[2], hdr[3] != 0, wk, qa, sh,
-                                   stage);
+      query_chunk<kStyle, kRotate, kFp8>((int32_t)hdr[1], (int32_t)hdr[2], hdr[3] != 0, wk, qa,
+                                         sh, stage);
     __syncwarp();
     bool v = false;
     if (lane == 0 && pr.a_kind != kItemNone) {
@@ -862,13 +936,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSm)
 constexpr int kMaxDevices = 64;
 struct DeviceInfo {
   int sm_count = 0;
-  int blocks_per_sm[2][2] = {{0, 0}, {0, 0}};  // [style][rotate]
+  int blocks_per_sm[2][2][2] = {};  // [style][rotate][fp8]
 };
 DeviceInfo g_devices[kMaxDevices];
 
-template <int kStyle, bool kRotate>
+template <int kStyle, bool kRotate, bool kFp8>
 int setup_kernel() {
-  auto kern = prepass_kernel<kStyle, kRotate>;
+  auto kern = prepass_kernel<kStyle, kRotate, kFp8>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
       cudaSuccess)
     return 0;
@@ -880,7 +954,7 @@ int setup_kernel() {
 }
 
 // CTAs that fit on the device at once, cached per device; 0 on a CUDA error.
-int resident_ctas(int style, int rotate) {
+int resident_ctas(int style, int rotate, int fp8) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
   DeviceInfo& di = g_devices[dev];
@@ -888,18 +962,24 @@ int resident_ctas(int style, int rotate) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return 0;
-    const int n[2][2] = {
-        {setup_kernel<FP4IDX_ROPE_NEOX, false>(), setup_kernel<FP4IDX_ROPE_NEOX, true>()},
-        {setup_kernel<FP4IDX_ROPE_INTERLEAVED, false>(),
-         setup_kernel<FP4IDX_ROPE_INTERLEAVED, true>()}};
+    const int n[2][2][2] = {
+        {{setup_kernel<FP4IDX_ROPE_NEOX, false, false>(),
+          setup_kernel<FP4IDX_ROPE_NEOX, false, true>()},
+         {setup_kernel<FP4IDX_ROPE_NEOX, true, false>(),
+          setup_kernel<FP4IDX_ROPE_NEOX, true, true>()}},
+        {{setup_kernel<FP4IDX_ROPE_INTERLEAVED, false, false>(),
+          setup_kernel<FP4IDX_ROPE_INTERLEAVED, false, true>()},
+         {setup_kernel<FP4IDX_ROPE_INTERLEAVED, true, false>(),
+          setup_kernel<FP4IDX_ROPE_INTERLEAVED, true, true>()}}};
     for (int a = 0; a < 2; ++a)
-      for (int b = 0; b < 2; ++b) {
-        if (n[a][b] < 1) return 0;
-        di.blocks_per_sm[a][b] = n[a][b];
-      }
+      for (int b = 0; b < 2; ++b)
+        for (int c = 0; c < 2; ++c) {
+          if (n[a][b][c] < 1) return 0;
+          di.blocks_per_sm[a][b][c] = n[a][b][c];
+        }
     di.sm_count = sms;
   }
-  return di.sm_count * di.blocks_per_sm[style][rotate];
+  return di.sm_count * di.blocks_per_sm[style][rotate][fp8];
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -918,7 +998,7 @@ fp4idx_status check_shared(const int64_t* positions, const float* cos_cache,
 fp4idx_status check_keys(const void* k, int64_t k_stride, const void* gamma, float eps,
                          const int64_t* slots, const uint8_t* cache, int64_t num_blocks) {
   if (!k || !gamma || !slots || !cache) return FP4IDX_ERR_NULL;
-  if (num_blocks < 1 || num_blocks > INT64_MAX / kPageBytes) return FP4IDX_ERR_SHAPE;
+  if (num_blocks < 1 || num_blocks > INT64_MAX / kFp8PageBytes) return FP4IDX_ERR_SHAPE;
   if (!(eps > 0.0f) || !isfinite(eps)) return FP4IDX_ERR_ARG;
   if (!aligned(k, 16) || (k_stride % 8) != 0 || !aligned(gamma, 16) || !aligned(slots, 8) ||
       !aligned(cache, 16))
@@ -926,21 +1006,30 @@ fp4idx_status check_keys(const void* k, int64_t k_stride, const void* gamma, flo
   return FP4IDX_OK;
 }
 
+// q_scale is not written in the FP8 mode (fp8 != 0) and may be NULL there.
 fp4idx_status check_queries(const void* q, int64_t q_tstride, int64_t q_hstride, const void* w,
                             float wscale, const uint8_t* q_fp4, const uint8_t* q_scale,
-                            const float* weights, int64_t num_tokens, int64_t num_heads) {
-  if (!q || !w || !q_fp4 || !q_scale || !weights) return FP4IDX_ERR_NULL;
-  if (num_heads < 1 || num_heads > INT64_MAX / kPayloadBytes / (num_tokens > 0 ? num_tokens : 1))
+                            const float* weights, int64_t num_tokens, int64_t num_heads,
+                            int fp8 = 0) {
+  if (!q || !w || !q_fp4 || (!q_scale && !fp8) || !weights) return FP4IDX_ERR_NULL;
+  if (num_heads < 1 ||
+      num_heads > INT64_MAX / FP4IDX_HEAD_DIM / (num_tokens > 0 ? num_tokens : 1))
     return FP4IDX_ERR_SHAPE;
   if (!isfinite(wscale)) return FP4IDX_ERR_ARG;
   if (!aligned(q, 16) || (q_tstride % 8) != 0 || (q_hstride % 8) != 0 || !aligned(w, 2) ||
-      !aligned(q_fp4, 16) || !aligned(q_scale, 4) || !aligned(weights, 4))
+      !aligned(q_fp4, 16) || (!fp8 && !aligned(q_scale, 4)) || !aligned(weights, 4))
     return FP4IDX_ERR_ALIGN;
   return FP4IDX_OK;
 }
 
+template <int kStyle, bool kRotate, bool kFp8>
+void launch_one(unsigned grid, cudaStream_t s, const KArgs& ka, const QArgs& qa, const Shared& sh,
+                const Work& wk) {
+  prepass_kernel<kStyle, kRotate, kFp8><<<grid, kThreads, kSmemBytes, s>>>(ka, qa, sh, wk);
+}
+
 fp4idx_status launch(const KArgs& ka, const QArgs& qa, const Shared& sh, bool keys, bool queries,
-                     int rope_style, int rotate, void* stream) {
+                     int rope_style, int rotate, int fp8, void* stream) {
   // 32-bit indices: T * H and T itself below 2^30.
   const int64_t H = queries ? qa.H : 1;
   if (sh.T >= (1 << 30) || H >= (1 << 30) || sh.T * H >= (1 << 30)) return FP4IDX_ERR_SHAPE;
@@ -952,37 +1041,40 @@ fp4idx_status launch(const KArgs& ka, const QArgs& qa, const Shared& sh, bool ke
   wk.nk = keys ? (wk.T + kChunkRows - 1) / kChunkRows : 0;
   wk.nq = queries ? wk.T * wk.cpt : 0;
   const int64_t total = (int64_t)wk.nk + wk.nq;
-  const int64_t resident = resident_ctas(rope_style, rotate);
+  const int64_t resident = resident_ctas(rope_style, rotate, fp8);
   if (resident <= 0) return FP4IDX_ERR_CUDA;
   const int64_t want = (total + kWarps - 1) / kWarps;  // at least one item per warp
   const int64_t grid = want < resident ? want : resident;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const dim3 g((unsigned)grid);
-  if (rope_style == FP4IDX_ROPE_NEOX) {
-    if (rotate)
-      prepass_kernel<FP4IDX_ROPE_NEOX, true><<<g, kThreads, kSmemBytes, s>>>(ka, qa, sh, wk);
-    else
-      prepass_kernel<FP4IDX_ROPE_NEOX, false><<<g, kThreads, kSmemBytes, s>>>(ka, qa, sh, wk);
-  } else {
-    if (rotate)
-      prepass_kernel<FP4IDX_ROPE_INTERLEAVED, true><<<g, kThreads, kSmemBytes, s>>>(ka, qa, sh, wk);
-    else
-      prepass_kernel<FP4IDX_ROPE_INTERLEAVED, false><<<g, kThreads, kSmemBytes, s>>>(ka, qa, sh,
-                                                                                    wk);
+  const unsigned g = (unsigned)grid;
+  const int which = (rope_style == FP4IDX_ROPE_NEOX ? 0 : 4) + (rotate ? 2 : 0) + (fp8 ? 1 : 0);
+  switch (which) {
+    case 0: launch_one<FP4IDX_ROPE_NEOX, false, false>(g, s, ka, qa, sh, wk); break;
+    case 1: launch_one<FP4IDX_ROPE_NEOX, false, true>(g, s, ka, qa, sh, wk); break;
+    case 2: launch_one<FP4IDX_ROPE_NEOX, true, false>(g, s, ka, qa, sh, wk); break;
+    case 3: launch_one<FP4IDX_ROPE_NEOX, true, true>(g, s, ka, qa, sh, wk); break;
+    case 4: launch_one<FP4IDX_ROPE_INTERLEAVED, false, false>(g, s, ka, qa, sh, wk); break;
+    case 5: launch_one<FP4IDX_ROPE_INTERLEAVED, false, true>(g, s, ka, qa, sh, wk); break;
+    case 6: launch_one<FP4IDX_ROPE_INTERLEAVED, true, false>(g, s, ka, qa, sh, wk); break;
+    default: launch_one<FP4IDX_ROPE_INTERLEAVED, true, true>(g, s, ka, qa, sh, wk); break;
   }
   return cudaGetLastError() == cudaSuccess ? FP4IDX_OK : FP4IDX_ERR_CUDA;
 }
 
-// Options: NULL means the defaults (compress ratio 1, no rotation).
-fp4idx_status check_options(const fp4idx_options* o, int64_t& pos_mask, int& rotate) {
+// Options: NULL means the defaults (compress ratio 1, no rotation, FP4).
+fp4idx_status check_options(const fp4idx_options* o, int64_t& pos_mask, int& rotate, int& fp8) {
   pos_mask = -1;
   rotate = 0;
+  fp8 = 0;
   if (o == nullptr) return FP4IDX_OK;
   if (o->compress_ratio != 1 && o->compress_ratio != 2 && o->compress_ratio != 4)
     return FP4IDX_ERR_ARG;
   if (o->hadamard != 0 && o->hadamard != 1) return FP4IDX_ERR_ARG;
+  if (o->output_mode != FP4IDX_OUTPUT_FP4 && o->output_mode != FP4IDX_OUTPUT_FP8)
+    return FP4IDX_ERR_ARG;
   pos_mask = ~(int64_t)(o->compress_ratio - 1);
   rotate = o->hadamard;
+  fp8 = o->output_mode == FP4IDX_OUTPUT_FP8 ? 1 : 0;
   return FP4IDX_OK;
 }
 
@@ -1004,8 +1096,8 @@ fp4idx_status fp4idx_k_norm_rope_pack_store_ex(
   st = check_keys(k, k_token_stride, gamma, eps, slot_mapping, kv_cache, num_blocks);
   if (st != FP4IDX_OK) return st;
   int64_t pos_mask;
-  int rotate;
-  st = check_options(options, pos_mask, rotate);
+  int rotate, fp8;
+  st = check_options(options, pos_mask, rotate, fp8);
   if (st != FP4IDX_OK) return st;
   if (err_flags && !aligned(err_flags, 4)) return FP4IDX_ERR_ALIGN;
 
@@ -1015,7 +1107,7 @@ fp4idx_status fp4idx_k_norm_rope_pack_store_ex(
   QArgs qa{};
   qa.H = 1;
   Shared sh{positions, cos_cache, sin_cache, max_pos, num_tokens, err_flags, -0.0f};
-  return launch(ka, qa, sh, true, false, rope_style, rotate, stream);
+  return launch(ka, qa, sh, true, false, rope_style, rotate, fp8, stream);
 }
 
 fp4idx_status fp4idx_k_norm_rope_pack_store(
@@ -1038,12 +1130,12 @@ fp4idx_status fp4idx_q_rope_pack_weights_ex(
   if (num_tokens == 0) return FP4IDX_OK;
   fp4idx_status st = check_shared(positions, cos_cache, sin_cache, max_pos, rope_style);
   if (st != FP4IDX_OK) return st;
-  st = check_queries(q, q_token_stride, q_head_stride, w, weight_scale, q_fp4, q_scale,
-                     weights_out, num_tokens, num_heads);
-  if (st != FP4IDX_OK) return st;
   int64_t pos_mask;
-  int rotate;
-  st = check_options(options, pos_mask, rotate);
+  int rotate, fp8;
+  st = check_options(options, pos_mask, rotate, fp8);
+  if (st != FP4IDX_OK) return st;
+  st = check_queries(q, q_token_stride, q_head_stride, w, weight_scale, q_fp4, q_scale,
+                     weights_out, num_tokens, num_heads, fp8);
   if (st != FP4IDX_OK) return st;
   if (err_flags && !aligned(err_flags, 4)) return FP4IDX_ERR_ALIGN;
 
@@ -1053,7 +1145,7 @@ fp4idx_status fp4idx_q_rope_pack_weights_ex(
            static_cast<const uint16_t*>(w), w_token_stride, weight_scale, q_fp4, q_scale,
            weights_out, num_heads};
   Shared sh{positions, cos_cache, sin_cache, max_pos, num_tokens, err_flags, -0.0f};
-  return launch(ka, qa, sh, false, true, rope_style, rotate, stream);
+  return launch(ka, qa, sh, false, true, rope_style, rotate, fp8, stream);
 }
 
 fp4idx_status fp4idx_q_rope_pack_weights(
@@ -1082,12 +1174,12 @@ fp4idx_status fp4idx_indexer_prepass_ex(
   if (st != FP4IDX_OK) return st;
   st = check_keys(k, k_token_stride, gamma, eps, slot_mapping, kv_cache, num_blocks);
   if (st != FP4IDX_OK) return st;
-  st = check_queries(q, q_token_stride, q_head_stride, w, weight_scale, q_fp4, q_scale,
-                     weights_out, num_tokens, num_heads);
-  if (st != FP4IDX_OK) return st;
   int64_t pos_mask;
-  int rotate;
-  st = check_options(options, pos_mask, rotate);
+  int rotate, fp8;
+  st = check_options(options, pos_mask, rotate, fp8);
+  if (st != FP4IDX_OK) return st;
+  st = check_queries(q, q_token_stride, q_head_stride, w, weight_scale, q_fp4, q_scale,
+                     weights_out, num_tokens, num_heads, fp8);
   if (st != FP4IDX_OK) return st;
   if (err_flags && !aligned(err_flags, 4)) return FP4IDX_ERR_ALIGN;
 
@@ -1098,7 +1190,7 @@ fp4idx_status fp4idx_indexer_prepass_ex(
            static_cast<const uint16_t*>(w), w_token_stride, weight_scale, q_fp4, q_scale,
            weights_out, num_heads};
   Shared sh{positions, cos_cache, sin_cache, max_pos, num_tokens, err_flags, -0.0f};
-  return launch(ka, qa, sh, true, true, rope_style, rotate, stream);
+  return launch(ka, qa, sh, true, true, rope_style, rotate, fp8, stream);
 }
 
 fp4idx_status fp4idx_indexer_prepass(

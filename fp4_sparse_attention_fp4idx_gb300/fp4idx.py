@@ -81,17 +81,24 @@ def lib() -> ctypes.CDLL:
     return _lib
 
 
+OUTPUT_FP4 = 0
+OUTPUT_FP8 = 1
+FP8_PAGE_BYTES = 8448
+
+
 class Options(ctypes.Structure):
     """fp4idx_options of include/fp4idx.h."""
-    _fields_ = [("compress_ratio", ctypes.c_int32), ("hadamard", ctypes.c_int32)]
+    _fields_ = [("compress_ratio", ctypes.c_int32), ("hadamard", ctypes.c_int32),
+                ("output_mode", ctypes.c_int32)]
 
 
-def _options(compress_ratio: int, hadamard: bool):
+def _options(compress_ratio: int, hadamard: bool, fp8: bool = False):
     """None for the defaults (the plain entry points are called), else a
     pointer to an Options block for the _ex entry points."""
-    if compress_ratio == 1 and not hadamard:
+    if compress_ratio == 1 and not hadamard and not fp8:
         return None
-    return ctypes.pointer(Options(int(compress_ratio), 1 if hadamard else 0))
+    return ctypes.pointer(Options(int(compress_ratio), 1 if hadamard else 0,
+                                  OUTPUT_FP8 if fp8 else OUTPUT_FP4))
 
 
 def declared_symbols(header: str = HEADER_PATH) -> list:
@@ -346,3 +353,85 @@ def paged_mqa_logits(q_fp4, q_scale, weights, kv_cache, block_table, context_len
         next_n, H, int(max_context), _ptr(err_flags), _stream_ptr(stream))
     _check(st, "fp4idx_paged_mqa_logits")
     return logits
+
+
+# ------------------------------------------------------------ FP8 output mode
+def k_norm_rope_fp8_store(k, gamma, positions, cos_cache, sin_cache, slot_mapping, kv_cache, *,
+                          eps: float = 1e-6, rope_style="neox", compress_ratio: int = 1,
+                          hadamard: bool = False, err_flags=None, stream=None) -> None:
+    """Keys -> FP8 paged index cache (uint8 [num_blocks, 8448]), in place:
+    fp4idx_k_norm_rope_pack_store_ex with output_mode FP8."""
+    torch = _torch()
+    _need(k, torch.bfloat16, "k", 2)
+    _need(kv_cache, torch.uint8, "kv_cache", 2)
+    if kv_cache.shape[1] != FP8_PAGE_BYTES or not kv_cache.is_contiguous():
+        raise ValueError("kv_cache must be contiguous [num_blocks, 8448]")
+    T = k.shape[0]
+    if k.shape[1] != HEAD_DIM or k.stride(1) != 1:
+        raise ValueError("k must be [T,128] with unit element stride")
+    opts = _options(compress_ratio, hadamard, fp8=True)
+    st = _lib.fp4idx_k_norm_rope_pack_store_ex(
+        _ptr(k), k.stride(0), _ptr(gamma), float(eps), _ptr(positions), _ptr(cos_cache),
+        _ptr(sin_cache), cos_cache.shape[0], rope_style_code(rope_style), _ptr(slot_mapping),
+        _ptr(kv_cache), kv_cache.shape[0], T, ctypes.cast(opts, _P), _ptr(err_flags),
+        _stream_ptr(stream))
+    _check(st, "fp4idx_k_norm_rope_pack_store_ex (FP8)")
+
+
+def _fp8_q_outputs(q_out, weights, T, H, device):
+    torch = _torch()
+    if q_out is None:
+        q_out = torch.empty((T, H, HEAD_DIM), dtype=torch.uint8, device=device)
+    if weights is None:
+        weights = torch.empty((T, H), dtype=torch.float32, device=device)
+    for t, shape, dt, name in ((q_out, (T, H, HEAD_DIM), torch.uint8, "q_out"),
+                               (weights, (T, H), torch.float32, "weights")):
+        _need(t, dt, name)
+        if tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous {shape}")
+    return q_out, weights
+
+
+def q_rope_fp8_weights(q, w, positions, cos_cache, sin_cache, *, rope_style="neox",
+                       weight_scale=None, q_out=None, weights=None, hadamard: bool = False,
+                       err_flags=None, stream=None):
+    """Queries -> (E4M3 codes uint8 [T,H,128], weights fp32 [T,H] with each
+    row's power-of-two scale folded in)."""
+    T, H = _check_q(q, w, positions, cos_cache, sin_cache)
+    q_out, weights = _fp8_q_outputs(q_out, weights, T, H, q.device)
+    ws = default_weight_scale(H) if weight_scale is None else float(weight_scale)
+    opts = _options(1, hadamard, fp8=True)
+    st = _lib.fp4idx_q_rope_pack_weights_ex(
+        _ptr(q), q.stride(0), q.stride(1), _ptr(w), w.stride(0), ws, _ptr(positions),
+        _ptr(cos_cache), _ptr(sin_cache), cos_cache.shape[0], rope_style_code(rope_style),
+        _ptr(q_out), None, _ptr(weights), T, H, ctypes.cast(opts, _P), _ptr(err_flags),
+        _stream_ptr(stream))
+    _check(st, "fp4idx_q_rope_pack_weights_ex (FP8)")
+    return q_out, weights
+
+
+def indexer_prepass_fp8(k, gamma, slot_mapping, kv_cache, q, w, positions, cos_cache,
+                        sin_cache, *, eps: float = 1e-6, rope_style="neox", weight_scale=None,
+                        q_out=None, weights=None, compress_ratio: int = 1,
+                        hadamard: bool = False, err_flags=None, stream=None):
+    """Both halves in the FP8 mode, one launch; returns (q_out, weights) and
+    updates kv_cache ([num_blocks, 8448]) in place."""
+    torch = _torch()
+    T, H = _check_q(q, w, positions, cos_cache, sin_cache)
+    _need(k, torch.bfloat16, "k", 2)
+    _need(kv_cache, torch.uint8, "kv_cache", 2)
+    if kv_cache.shape[1] != FP8_PAGE_BYTES or not kv_cache.is_contiguous():
+        raise ValueError("kv_cache must be contiguous [num_blocks, 8448]")
+    if k.shape[0] != T or k.shape[1] != HEAD_DIM or k.stride(1) != 1:
+        raise ValueError("k must be [T,128] with unit element stride")
+    q_out, weights = _fp8_q_outputs(q_out, weights, T, H, q.device)
+    ws = default_weight_scale(H) if weight_scale is None else float(weight_scale)
+    opts = _options(compress_ratio, hadamard, fp8=True)
+    st = _lib.fp4idx_indexer_prepass_ex(
+        _ptr(k), k.stride(0), _ptr(gamma), float(eps), _ptr(slot_mapping), _ptr(kv_cache),
+        kv_cache.shape[0], _ptr(q), q.stride(0), q.stride(1), _ptr(w), w.stride(0), ws,
+        _ptr(q_out), None, _ptr(weights), H, _ptr(positions), _ptr(cos_cache), _ptr(sin_cache),
+        cos_cache.shape[0], rope_style_code(rope_style), T, ctypes.cast(opts, _P),
+        _ptr(err_flags), _stream_ptr(stream))
+    _check(st, "fp4idx_indexer_prepass_ex (FP8)")
+    return q_out, weights

@@ -418,3 +418,11 @@ def make_scorer_config(name: str) -> ScorerWorkload:
         return make_scorer_decode()
     b, n, h, lens, mc, seed, ext = SCORER_CONFIGS[name]
     return make_scorer(name, b, n, h, lens, mc, seed, extremes=ext)
+
+
+def fp8_sentinel_cache(w: Workload) -> np.ndarray:
+    """Seeded sentinel bytes for the FP8 output mode's cache: the same number
+    of pages as the workload's FP4 cache, 8448 bytes each."""
+    seed = 7919 + 31 * w.T + w.H + sum(map(ord, w.name))
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return rng.integers(0, 256, size=(w.num_blocks, KV_BLOCK * (HEAD_DIM + 4)), dtype=np.uint8)

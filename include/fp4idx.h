@@ -87,7 +87,13 @@ enum {
   FP4IDX_KV_BLOCK = 64,
   FP4IDX_SLOT_PAYLOAD_BYTES = 64,
   FP4IDX_SLOT_EXP_BYTES = 4,
-  FP4IDX_PAGE_BYTES = 64 * 68 /* 4352 */
+  FP4IDX_PAGE_BYTES = 64 * 68, /* 4352 */
+  FP4IDX_FP8_PAGE_BYTES = 64 * (128 + 4) /* 8448: FP8 output mode */
+};
+
+enum {
+  FP4IDX_OUTPUT_FP4 = 0, /* packed E2M1 + per-32 UE8M0 exponents (default) */
+  FP4IDX_OUTPUT_FP8 = 1  /* E4M3 codes + one power-of-two scale per row   */
 };
 
 /* Bits OR-ed into *err_flags by the device-side checks. */
@@ -203,12 +209,31 @@ fp4idx_status fp4idx_indexer_prepass(
  *                   rmsnorm_rope_rotate FP4 KV-cache kernel" (aiter PR 4029),
  *                   Changes (RMSNorm + RoPE + optional Hadamard rotate + FP4
  *                   quant + paged KV-cache write).
+ *   output_mode     FP4IDX_OUTPUT_FP4 (default) or FP4IDX_OUTPUT_FP8: the
+ *                   FP8 contract that the FP4 mode extends ("[HIP] Add FP4
+ *                   output mode to indexer_qk_rope_quant_and_cache" (aiter
+ *                   PR 5484), Summary and API: the FP8 path folds its
+ *                   per-(token, head) query scale into the head weights).
+ *                   Every 128-element row gets one power-of-two scale
+ *                   s = 2^(e-127) = ceil_pow2(max(rn32(amax/448), 2^-126))
+ *                   and E4M3 (e4m3fn) codes of x / s (an exact division),
+ *                   rounded half to even, saturating at 448, sign of zero
+ *                   kept.  Then:
+ *                     kv_cache is [num_blocks, 8448]: page b holds 64 code
+ *                       rows of 128 bytes at o*128, then 64 fp32 scales s at
+ *                       8192 + o*4 (page-split, like the FP4 pages);
+ *                     q_fp4 receives the codes, [num_tokens, num_heads, 128]
+ *                       bytes (16-byte aligned); q_scale is not written and
+ *                       may be NULL;
+ *                     weights_out[t,h] = rn(fp32(w[t,h]) * weight_scale) * s
+ *                       (s folded in; the product by s is exact).
  * Any other value returns FP4IDX_ERR_ARG.  All other arguments, checks and
  * results are those of the corresponding call above.
  */
 typedef struct fp4idx_options {
   int32_t compress_ratio;
   int32_t hadamard;
+  int32_t output_mode;
 } fp4idx_options;
 
 fp4idx_status fp4idx_k_norm_rope_pack_store_ex(

@@ -247,12 +247,13 @@ def test_scorer_host_checks(F, over, code):
 
 
 @pytest.mark.fake_ptr
-@pytest.mark.parametrize("ratio,had", [(3, 0), (0, 0), (8, 0), (1, 2), (2, -1)])
-def test_option_host_checks(F, ratio, had):
+@pytest.mark.parametrize("ratio,had,mode", [(3, 0, 0), (0, 0, 0), (8, 0, 0), (1, 2, 0),
+                                            (2, -1, 0), (1, 0, 2), (1, 0, -1)])
+def test_option_host_checks(F, ratio, had, mode):
     """A bad options block is rejected on the host (ERR_ARG) by all three
     variant entry points."""
     import ctypes
-    opts = ctypes.cast(ctypes.pointer(F.Options(ratio, had)), ctypes.c_void_p)
+    opts = ctypes.cast(ctypes.pointer(F.Options(ratio, had, mode)), ctypes.c_void_p)
     ka, qa = _k_args(), _q_args(style=0)
     assert F.lib().fp4idx_k_norm_rope_pack_store_ex(
         ka["k"], ka["k_stride"], ka["gamma"], ka["eps"], ka["pos"], ka["cos"], ka["sin"],
