@@ -88,6 +88,10 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.oracle_q_rope_fp8_weights.argtypes = [
         P, P, P, P, P, i64, ctypes.c_int, P, P, i64, i64, ctypes.c_int]
     L.oracle_q_rope_fp8_weights.restype = ctypes.c_int
+    L.oracle_fake_quant_row.argtypes = [P, ctypes.c_int, P]
+    L.oracle_fake_quant_row.restype = None
+    L.oracle_rope_fake_quant.argtypes = [P, i64, P, P, P, i64, ctypes.c_int, ctypes.c_int, P, i64]
+    L.oracle_rope_fake_quant.restype = ctypes.c_int
     L.oracle_paged_mqa_logits.argtypes = [
         P, P, P, P, i64, P, i64, P, P, i64, i64, i64, i64, i64]
     L.oracle_paged_mqa_logits.restype = ctypes.c_int
@@ -308,6 +312,31 @@ def q_rope_fp8_weights(q, w, positions, cos_cache, sin_cache, rope_style,
         _p(q), _p(w), _p(pos), _p(cs), _p(sn), cs.shape[0], int(rope_style), _p(qo), _p(wt),
         T, H, int(bool(hadamard)))
     return qo, wt, int(st)
+
+
+def fake_quant_row(row_bits, mode: int) -> np.ndarray:
+    """Dequantised bf16 row: mode 0 per-32 UE8M0, mode 1 per-16 E4M3."""
+    r = _c(row_bits, np.uint16)
+    assert r.shape == (HEAD_DIM,)
+    out = np.zeros(HEAD_DIM, np.uint16)
+    lib().oracle_fake_quant_row(_p(r), int(mode), _p(out))
+    return out
+
+
+def rope_fake_quant(x, rows_per_token: int, positions, cos_cache, sin_cache, rope_style,
+                    mode: int, out=None):
+    """(out bf16 bits [N,128], status) for rows x [N,128]."""
+    x = _c(x, np.uint16)
+    N = x.shape[0]
+    assert x.shape == (N, HEAD_DIM)
+    pos = _c(positions, np.int64)
+    cs = _c(cos_cache, np.float32)
+    sn = _c(sin_cache, np.float32)
+    if out is None:
+        out = np.zeros((N, HEAD_DIM), np.uint16)
+    st = lib().oracle_rope_fake_quant(_p(x), int(rows_per_token), _p(pos), _p(cs), _p(sn),
+                                      cs.shape[0], int(rope_style), int(mode), _p(out), N)
+    return out, int(st)
 
 
 def paged_mqa_logits(q_fp4, q_scale, weights, kv_cache, block_table, context_lens,

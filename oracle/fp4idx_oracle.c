@@ -467,6 +467,71 @@ int oracle_q_rope_fp8_weights(const uint16_t* q, const uint16_t* w,
                     q_out, NULL, weights, num_tokens, num_heads, hadamard, 1);
 }
 
+/* ---- Torch-shaped fake quantisation ([sgl] Summary: the RoPE tail plus
+ * FP4 fake-quant of the torch-shaped path, per-32 UE8M0 by default and
+ * per-16 E4M3 for compressed KV, keeping the bf16 round trip after RoPE and
+ * round half to even).  Reading: RoPE as in the pre-pass (dims 0..63, bf16
+ * output), then every value is replaced by its dequantised FP4 value, as
+ * bf16 (exact: at most 6 significant bits).
+ *   mode 0 (per-32 UE8M0): stage 1 of the pre-pass.
+ *   mode 1 (per-16 E4M3): s = E4M3(rn32(amax/6)) (the scale rounded to
+ *     E4M3, saturating at 448); code = nearest E2M1 of rn32(x / s) (ties to
+ *     even, saturating at 6); value = code * s; a group whose s rounds to 0
+ *     is all zeros; no -0 (as in the packed path). ---- */
+
+static void fake_quant_group16(const float* z, float* out) {
+  float amax16 = 0.0f;
+  for (int i = 0; i < 16; ++i) amax16 = fmaxf(amax16, fabsf(z[i]));
+  float t16 = amax16 / 6.0f;
+  float sc = oracle_e4m3_to_f32(oracle_f32_to_e4m3(t16));
+  for (int i = 0; i < 16; ++i) {
+    if (sc == 0.0f) {
+      out[i] = 0.0f;
+      continue;
+    }
+    float v = z[i] / sc;
+    int m = e2m1_nearest_code(fabs((double)v));
+    double d = GRID[m] * (double)sc;
+    out[i] = (float)((v < 0.0f && m != 0) ? -d : d);
+  }
+}
+
+void oracle_fake_quant_row(const uint16_t* row, int mode, uint16_t* out) {
+  float z[HEAD_DIM], q[HEAD_DIM];
+  for (int i = 0; i < HEAD_DIM; ++i) z[i] = bf16_to_f32(row[i]);
+  if (mode == 1) {
+    for (int g = 0; g < HEAD_DIM / 16; ++g) fake_quant_group16(z + 16 * g, q + 16 * g);
+  } else {
+    for (int g = 0; g < HEAD_DIM / GROUP; ++g) {
+      uint8_t nib[GROUP];
+      int e = oracle_quant_group(z + GROUP * g, STAGE1_FLOOR, nib);
+      for (int i = 0; i < GROUP; ++i) q[GROUP * g + i] = oracle_dequant(nib[i], e);
+    }
+  }
+  for (int i = 0; i < HEAD_DIM; ++i) out[i] = oracle_f32_to_bf16(q[i]);
+}
+
+int oracle_rope_fake_quant(const uint16_t* x, int64_t rows_per_token,
+                           const int64_t* positions, const float* cos_cache,
+                           const float* sin_cache, int64_t max_pos,
+                           int rope_style, int mode, uint16_t* out,
+                           int64_t num_rows) {
+  int status = 0;
+  for (int64_t r = 0; r < num_rows; ++r) {
+    int64_t pos = positions[r / rows_per_token];
+    if (pos < 0 || pos >= max_pos) {
+      status = -1;
+      continue;
+    }
+    uint16_t y[HEAD_DIM];
+    memcpy(y, x + r * HEAD_DIM, sizeof y);
+    oracle_rope_row(y, cos_cache + pos * (ROPE_DIM / 2),
+                    sin_cache + pos * (ROPE_DIM / 2), rope_style);
+    oracle_fake_quant_row(y, mode, out + r * HEAD_DIM);
+  }
+  return status;
+}
+
 /* The scorer ([aiter] Verification, End-to-end: the FP4 paged MQA-logits
  * scorer reads the kernel's own bytes; [vllm] Code Review: the scaled E2M1
  * dot product of packed queries and packed keys with their per-32 block

@@ -149,6 +149,20 @@ int oracle_q_rope_fp8_weights(const uint16_t* q, const uint16_t* w,
                               int64_t num_tokens, int64_t num_heads,
                               int hadamard);
 
+/* ---- Torch-shaped fake quantisation (bf16 in, dequantised bf16 out) ---- */
+
+/* One 128-element bf16 row: mode 0 = per-32 UE8M0 (stage 1 of the pack),
+ * mode 1 = per-16 groups with E4M3 scales E4M3(amax/6). */
+void oracle_fake_quant_row(const uint16_t* row, int mode, uint16_t* out);
+/* RoPE (as in the pre-pass) then fake quantisation of rows x [num_rows,128];
+ * row r takes positions[r / rows_per_token].  Returns 0, or -1 if a position
+ * is out of range (that row's output is left untouched). */
+int oracle_rope_fake_quant(const uint16_t* x, int64_t rows_per_token,
+                           const int64_t* positions, const float* cos_cache,
+                           const float* sin_cache, int64_t max_pos,
+                           int rope_style, int mode, uint16_t* out,
+                           int64_t num_rows);
+
 /* FP4 paged MQA-logits scorer (the consumer of the packed queries and the
  * paged index-K cache).  Query row t = b*next_n + j of sequence b scores
  * every cached token s < context_lens[b]:

@@ -7,6 +7,7 @@ import pytest
 
 import oracle
 from tests import test_oracle_pins as pins
+from tests import test_oracle_fake_quant as qpins
 from tests import test_oracle_fp8 as fpins
 from tests import test_oracle_variants as vpins
 from tests import test_scorer_oracle as spins
@@ -95,6 +96,16 @@ MUTANTS = [
      "fp8_quant_row(y, q_out + r * HEAD_DIM);"),
     ("fp8_scale_slot_interleaved", "memcpy(page + KV_BLOCK * HEAD_DIM + o * 4, &scale, 4);",
      "memcpy(page + KV_BLOCK * HEAD_DIM + (63 - o) * 4, &scale, 4);"),
+    ("fq16_amax_over_4", "float t16 = amax16 / 6.0f;", "float t16 = amax16 / 4.0f;"),
+    ("fq16_scale_not_e4m3", "float sc = oracle_e4m3_to_f32(oracle_f32_to_e4m3(t16));",
+     "float sc = t16;"),
+    ("fq16_keep_negative_zero", "out[i] = (float)((v < 0.0f && m != 0) ? -d : d);",
+     "out[i] = (float)((v < 0.0f) ? -d : d);"),
+    ("fq16_multiply_not_divide", "float v = z[i] / sc;", "float v = z[i] * sc;"),
+    ("fq_rope_skipped",
+     "    oracle_rope_row(y, cos_cache + pos * (ROPE_DIM / 2),\n"
+     "                    sin_cache + pos * (ROPE_DIM / 2), rope_style);\n"
+     "    oracle_fake_quant_row", "    oracle_fake_quant_row"),
     ("q_hadamard_skipped", "      if (hadamard) oracle_hadamard_row(y);\n      double folded",
      "      double folded"),
 ]
@@ -134,6 +145,11 @@ PINS = [
     fpins.test_decode_all_codes_match_torch,
     fpins.test_encode_matches_torch_in_range,
     fpins.test_row_exponent_exact,
+    qpins.test_mode1_midpoints_closed_form,
+    qpins.test_mode1_tiny_group_is_zero_and_saturation,
+    qpins.test_rope_then_fake_quant_at_position_zero,
+    qpins.test_mode1_per16_e4m3_exact,
+    qpins.test_mode0_is_per32_ue8m0_exact,
     pins.test_two_stage_invariants,
     pins.test_group_quant_exact_rational,
     pins.test_exponent_exhaustive_bf16,
