@@ -396,6 +396,31 @@ def run_variants(F, w, D, dev, peak, flush, steps: int = 100, warmup: int = 5) -
         out[name] = {"ms_per_launch": round(ms, 5), "tokens_per_s": round(T / (ms / 1e3), 1),
                      "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
                      "algorithmic_bytes_per_launch": nbytes}
+    # The torch-shaped RoPE + FP4 fake quantisation of the workload's queries
+    # (T*H rows): 256 B read + 256 B written per row, 8 B of position per
+    # token, 256 B of cos/sin per distinct position.
+    qo = torch.empty((T, H, 128), dtype=torch.bfloat16, device=dev)
+    fq = F.lib().fp4idx_rope_fake_quant
+    nbytes = T * H * 512 + T * 8 + 256 * int(np.unique(w.positions).size)
+    for name, mode in (("fake_quant_ue8m0_32", 0), ("fake_quant_e4m3_16", 1)):
+        args = (p["q"], 128, H, p["pos"], p["cos"], p["sin"], w.max_pos, w.rope_style, mode,
+                qo.data_ptr(), T * H, None, st.cuda_stream)
+        for _ in range(warmup):
+            flush()
+            _ok(F, fq(*args))
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for a, b in ev:
+            flush()
+            a.record(st)
+            _ok(F, fq(*args))
+            b.record(st)
+        torch.cuda.synchronize()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out[name] = {"ms_per_launch": round(ms, 5), "rows_per_s": round(T * H / (ms / 1e3), 1),
+                     "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+                     "algorithmic_bytes_per_launch": nbytes}
     return out
 
 

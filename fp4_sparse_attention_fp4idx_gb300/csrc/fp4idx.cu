@@ -57,6 +57,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <cuda_fp16.h>
+
 #include "fp4idx.h"
 
 namespace {
@@ -932,6 +934,151 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSm)
   }
 }
 
+// ----------------------------------------------------- torch-shaped fake quant
+// RoPE then FP4 fake quantisation of bf16 rows, written back as the
+// dequantised bf16 values.  Source: "dsv4.1: RoPE and FP4 packing kernels"
+// (sglang PR 39656), Summary (the RoPE tail plus FP4 fake-quant of the
+// torch-shaped path: per-32 UE8M0 by default, per-16 E4M3 for compressed
+// KV; bf16 round trip after RoPE; round half to even).
+
+struct FQArgs {
+  const uint16_t* x;
+  int64_t row_stride;       // elements
+  uint32_t rows_per_token;
+  uint32_t N;               // rows
+  const int64_t* pos;
+  const float* cos;
+  const float* sin;
+  int64_t max_pos;
+  uint16_t* out;            // dense [N, 128]
+  uint32_t* err;
+  float neg_zero;
+};
+
+// Eight packed E2M1 codes (element 0 in the low nibble) -> fp32 values at
+// scale 2^0, exactly, by the hardware E2M1 -> f16 conversion.
+__device__ __forceinline__ void e2m1x8_values(uint32_t p, float (&v)[8]) {
+  uint32_t h[4];
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(p));
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    v[2 * k] = __half2float(__ushort_as_half((unsigned short)(h[k] & 0xffffu)));
+    v[2 * k + 1] = __half2float(__ushort_as_half((unsigned short)(h[k] >> 16)));
+  }
+}
+
+// fp32 -> E4M3 (round half to even, saturating) -> fp32, exactly.
+__device__ __forceinline__ float e4m3_round(float t) {
+  uint32_t h;
+  asm("{\n\t.reg .b16 c;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 c, %1, %1;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
+      : "=r"(h)
+      : "f"(t));
+  return __half2float(__ushort_as_half((unsigned short)(h & 0xffffu)));
+}
+
+// Dequantised values of eight codes times `scale` (an exact product),
+// packed as four bf16x2 words.  Codes with a zero magnitude carry no sign.
+__device__ __forceinline__ void dequant8(uint32_t p, float scale, uint32_t (&o)[4]) {
+  float v[8];
+  e2m1x8_values(finish_codes(p, false), v);
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    o[k] = pack_bf16x2(__fmul_rn(v[2 * k], scale), __fmul_rn(v[2 * k + 1], scale));
+}
+
+// Per-32 UE8M0 (stage 1 of the pack) for this lane's two parts; all 32
+// lanes must call (shuffles).
+__device__ __forceinline__ void fake_quant_ue8m0(uint32_t (&a)[4], uint32_t (&b)[4]) {
+  const uint32_t ma = hmax_abs(hmax_abs(a[0], a[1]), hmax_abs(a[2], a[3]));
+  const uint32_t mb = hmax_abs(hmax_abs(b[0], b[1]), hmax_abs(b[2], b[3]));
+  uint32_t m = hmax_abs(prmt(ma, mb, 0x5410u), prmt(ma, mb, 0x7632u));
+  m = hmax_abs(m, __shfl_xor_sync(kFull, m, 1));
+  m = hmax_abs(m, __shfl_xor_sync(kFull, m, 2));
+  m &= 0x7fff7fffu;
+  const uint32_t ep = ((m + 0x003f003fu) >> 7) & 0x01ff01ffu;
+  const uint32_t ie = umin16x2(0x01000100u - ep, 0x00fd00fdu);  // 254 - e1 per half
+  const float ia = __uint_as_float(ie << 23), ib = __uint_as_float((ie >> 16) << 23);
+  const float sa = __uint_as_float((254u - (ie & 0xffffu)) << 23);  // 2^(e1 - 127)
+  const float sb = __uint_as_float((254u - (ie >> 16)) << 23);
+  float va[8], vb[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    mul2(va[2 * k], va[2 * k + 1], bf16_lo(a[k]), bf16_hi(a[k]), ia, ia);
+    mul2(vb[2 * k], vb[2 * k + 1], bf16_lo(b[k]), bf16_hi(b[k]), ib, ib);
+  }
+  dequant8(e2m1x8(va), sa, a);
+  dequant8(e2m1x8(vb), sb, b);
+}
+
+// Per-16 E4M3: a group of 16 is lanes j and j^1 of one part; all 32 lanes
+// must call (shuffles).
+__device__ __forceinline__ void fake_quant_e4m3_16(uint32_t (&a)[4], uint32_t (&b)[4]) {
+  const uint32_t ma = hmax_abs(hmax_abs(a[0], a[1]), hmax_abs(a[2], a[3]));
+  const uint32_t mb = hmax_abs(hmax_abs(b[0], b[1]), hmax_abs(b[2], b[3]));
+  uint32_t m = hmax_abs(prmt(ma, mb, 0x5410u), prmt(ma, mb, 0x7632u));
+  m = hmax_abs(m, __shfl_xor_sync(kFull, m, 1));
+  m &= 0x7fff7fffu;
+  const float sa = e4m3_round(__fdiv_rn(__uint_as_float(m << 16), 6.0f));
+  const float sb = e4m3_round(__fdiv_rn(__uint_as_float(m & 0xffff0000u), 6.0f));
+  float va[8], vb[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    va[2 * k] = sa == 0.0f ? 0.0f : __fdiv_rn(bf16_lo(a[k]), sa);
+    va[2 * k + 1] = sa == 0.0f ? 0.0f : __fdiv_rn(bf16_hi(a[k]), sa);
+    vb[2 * k] = sb == 0.0f ? 0.0f : __fdiv_rn(bf16_lo(b[k]), sb);
+    vb[2 * k + 1] = sb == 0.0f ? 0.0f : __fdiv_rn(bf16_hi(b[k]), sb);
+  }
+  dequant8(e2m1x8(va), sa, a);
+  dequant8(e2m1x8(vb), sb, b);
+}
+
+template <int kStyle, int kMode>
+__global__ void __launch_bounds__(256) fake_quant_kernel(FQArgs fa) {
+  const int lane = threadIdx.x & 31, j = lane & 7, rg = lane >> 3;
+  const uint32_t nwarps = gridDim.x * (blockDim.x / 32);
+  const uint32_t warp = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  for (uint32_t r0 = 4 * warp; r0 < fa.N; r0 += 4 * nwarps) {  // uniform over the warp
+    const uint32_t row = r0 + rg;
+    const bool in = row < fa.N;
+    int64_t pos = 0;
+    bool ok = false;
+    if (in) {
+      pos = __ldg(fa.pos + row / fa.rows_per_token);
+      ok = pos >= 0 && pos < fa.max_pos;
+      if (!ok && j == 0) flag_error(fa.err, FP4IDX_ERRFLAG_POSITION);
+    }
+    if (!ok) pos = 0;
+    RopeCoef<kStyle> rc;
+    rc.load_global(fa.cos + pos * kRopeHalf, fa.sin + pos * kRopeHalf, j);
+    uint32_t a[4] = {0u, 0u, 0u, 0u}, b[4] = {0u, 0u, 0u, 0u};
+    if (ok) {
+      const uint4* src = reinterpret_cast<const uint4*>(fa.x + (int64_t)row * fa.row_stride);
+      const uint4 va = __ldg(src + j), vb = __ldg(src + 8 + j);
+      a[0] = va.x; a[1] = va.y; a[2] = va.z; a[3] = va.w;
+      b[0] = vb.x; b[1] = vb.y; b[2] = vb.z; b[3] = vb.w;
+    }
+    rope_lane<kStyle>(a, rc, fa.neg_zero);
+    if (kMode == FP4IDX_FAKE_QUANT_E4M3_16)
+      fake_quant_e4m3_16(a, b);
+    else
+      fake_quant_ue8m0(a, b);
+    if (ok) {
+      uint4* dst = reinterpret_cast<uint4*>(fa.out + (int64_t)row * FP4IDX_HEAD_DIM);
+      dst[j] = make_uint4(a[0], a[1], a[2], a[3]);
+      dst[8 + j] = make_uint4(b[0], b[1], b[2], b[3]);
+    }
+  }
+}
+
 // --------------------------------------------------------------- host side
 constexpr int kMaxDevices = 64;
 struct DeviceInfo {
@@ -1206,6 +1353,45 @@ fp4idx_status fp4idx_indexer_prepass(
                                    w_token_stride, weight_scale, q_fp4, q_scale, weights_out,
                                    num_heads, positions, cos_cache, sin_cache, max_pos,
                                    rope_style, num_tokens, nullptr, err_flags, stream);
+}
+
+fp4idx_status fp4idx_rope_fake_quant(const void* x, int64_t row_stride, int64_t rows_per_token,
+                                     const int64_t* positions, const float* cos_cache,
+                                     const float* sin_cache, int64_t max_pos, int rope_style,
+                                     int scale_mode, void* out, int64_t num_rows,
+                                     uint32_t* err_flags, void* stream) {
+  if (num_rows < 0) return FP4IDX_ERR_SHAPE;
+  if (num_rows == 0) return FP4IDX_OK;
+  fp4idx_status st = check_shared(positions, cos_cache, sin_cache, max_pos, rope_style);
+  if (st != FP4IDX_OK) return st;
+  if (!x || !out) return FP4IDX_ERR_NULL;
+  if (rows_per_token < 1 || num_rows >= (1ll << 31) || rows_per_token >= (1ll << 31) ||
+      row_stride < FP4IDX_HEAD_DIM)
+    return FP4IDX_ERR_SHAPE;
+  if (scale_mode != FP4IDX_FAKE_QUANT_UE8M0_32 && scale_mode != FP4IDX_FAKE_QUANT_E4M3_16)
+    return FP4IDX_ERR_ARG;
+  if (!aligned(x, 16) || (row_stride % 8) != 0 || !aligned(out, 16) ||
+      (err_flags && !aligned(err_flags, 4)))
+    return FP4IDX_ERR_ALIGN;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return FP4IDX_ERR_CUDA;
+  FQArgs fa{static_cast<const uint16_t*>(x), row_stride, (uint32_t)rows_per_token,
+            (uint32_t)num_rows, positions, cos_cache, sin_cache, max_pos,
+            static_cast<uint16_t*>(out), err_flags, -0.0f};
+  const int64_t quads = (num_rows + 3) / 4;  // one warp-iteration per 4 rows
+  int64_t grid = (quads + 7) / 8;
+  if (grid > (int64_t)sms * 8) grid = (int64_t)sms * 8;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int which = (rope_style == FP4IDX_ROPE_NEOX ? 0 : 2) + scale_mode;
+  switch (which) {
+    case 0: fake_quant_kernel<FP4IDX_ROPE_NEOX, 0><<<(unsigned)grid, 256, 0, s>>>(fa); break;
+    case 1: fake_quant_kernel<FP4IDX_ROPE_NEOX, 1><<<(unsigned)grid, 256, 0, s>>>(fa); break;
+    case 2: fake_quant_kernel<FP4IDX_ROPE_INTERLEAVED, 0><<<(unsigned)grid, 256, 0, s>>>(fa); break;
+    default: fake_quant_kernel<FP4IDX_ROPE_INTERLEAVED, 1><<<(unsigned)grid, 256, 0, s>>>(fa);
+  }
+  return cudaGetLastError() == cudaSuccess ? FP4IDX_OK : FP4IDX_ERR_CUDA;
 }
 
 const char* fp4idx_status_string(fp4idx_status status) {

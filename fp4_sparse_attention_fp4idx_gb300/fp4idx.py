@@ -64,6 +64,8 @@ _SIGS = {
         _INT, [_P, _I64, _P, _F, _P, _P, _I64,
                _P, _I64, _I64, _P, _I64, _F, _P, _P, _P, _I64,
                _P, _P, _P, _I64, _INT, _I64, _P, _P, _P]),
+    "fp4idx_rope_fake_quant": (
+        _INT, [_P, _I64, _I64, _P, _P, _P, _I64, _INT, _INT, _P, _I64, _P, _P]),
     "fp4idx_paged_mqa_logits": (
         _INT, [_P, _P, _P, _P, _I64, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _I64, _P, _P]),
     "fp4idx_status_string": (ctypes.c_char_p, [_INT]),
@@ -435,3 +437,44 @@ def indexer_prepass_fp8(k, gamma, slot_mapping, kv_cache, q, w, positions, cos_c
         _ptr(err_flags), _stream_ptr(stream))
     _check(st, "fp4idx_indexer_prepass_ex (FP8)")
     return q_out, weights
+
+
+# ------------------------------------------------------ torch-shaped fake quant
+FAKE_QUANT_UE8M0_32 = 0
+FAKE_QUANT_E4M3_16 = 1
+
+
+def rope_fake_quant(x, positions, cos_cache, sin_cache, *, rope_style="neox",
+                    scale_mode: int = FAKE_QUANT_UE8M0_32, out=None, err_flags=None,
+                    stream=None):
+    """RoPE + FP4 fake quantisation -> bf16 of x's shape.  x bf16 [T,128]
+    (keys, one position per row) or [T,H,128] (queries, one position per
+    token), unit element stride, row stride a multiple of 8."""
+    torch = _torch()
+    _need(x, torch.bfloat16, "x")
+    if x.dim() == 2:
+        T, D = x.shape
+        rows, per, stride = T, 1, x.stride(0)
+    elif x.dim() == 3:
+        T, H, D = x.shape
+        if x.stride(0) != H * x.stride(1):
+            raise ValueError("x [T,H,128] must have token stride H * head stride")
+        rows, per, stride = T * H, H, x.stride(1)
+    else:
+        raise ValueError("x must be [T,128] or [T,H,128]")
+    if D != HEAD_DIM or x.stride(-1) != 1:
+        raise ValueError("rows must be 128 elements with unit stride")
+    _need(positions, torch.int64, "positions", 1)
+    if positions.shape[0] != T or not positions.is_contiguous():
+        raise ValueError("positions must be contiguous [T]")
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
+    _need(out, torch.bfloat16, "out")
+    if tuple(out.shape) != tuple(x.shape) or not out.is_contiguous():
+        raise ValueError("out must be contiguous with x's shape")
+    st = _lib.fp4idx_rope_fake_quant(
+        _ptr(x), stride, per, _ptr(positions), _ptr(cos_cache), _ptr(sin_cache),
+        cos_cache.shape[0], rope_style_code(rope_style), int(scale_mode), _ptr(out), rows,
+        _ptr(err_flags), _stream_ptr(stream))
+    _check(st, "fp4idx_rope_fake_quant")
+    return out

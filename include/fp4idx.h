@@ -262,6 +262,42 @@ fp4idx_status fp4idx_indexer_prepass_ex(
     const fp4idx_options* options, uint32_t* err_flags, void* stream);
 
 /*
+ * Torch-shaped fake quantisation: RoPE, then every value replaced by its
+ * dequantised FP4 value, written as bf16.  Source: "dsv4.1: RoPE and FP4
+ * packing kernels" (sglang PR 39656), Summary (the RoPE tail plus FP4
+ * fake-quant of the torch-shaped path, per-32 UE8M0 by default and per-16
+ * E4M3 for compressed KV, keeping the bf16 round trip after RoPE and round
+ * half to even).
+ *
+ *   x            bf16 rows, row r at x + r*row_stride elements (16-byte
+ *                aligned, row_stride a multiple of 8 and >= 128).
+ *   rows_per_token  row r takes positions[r / rows_per_token] (1 for keys
+ *                [T,128], H for queries [T,H,128]).
+ *   positions, cos_cache, sin_cache, max_pos, rope_style: as above; RoPE
+ *                on dims 0..63 with the bf16 round trip.
+ *   scale_mode   FP4IDX_FAKE_QUANT_UE8M0_32: groups of 32 with the
+ *                pre-pass's stage-1 scale (the values its stage 1 produces);
+ *                FP4IDX_FAKE_QUANT_E4M3_16: groups of 16 with the scale
+ *                s = E4M3(rn32(amax/6)) (round half to even, saturating at
+ *                448), codes the nearest E2M1 of rn32(x/s) (ties to even,
+ *                saturating at 6), values code*s; a group whose s rounds to
+ *                0 becomes zeros.  No output is -0.
+ *   out          bf16 [num_rows, 128], dense, 16-byte aligned.
+ *   err_flags    FP4IDX_ERRFLAG_POSITION for a row whose position is out of
+ *                range (that row is left untouched).
+ */
+enum {
+  FP4IDX_FAKE_QUANT_UE8M0_32 = 0,
+  FP4IDX_FAKE_QUANT_E4M3_16 = 1
+};
+
+fp4idx_status fp4idx_rope_fake_quant(
+    const void* x, int64_t row_stride, int64_t rows_per_token,
+    const int64_t* positions, const float* cos_cache, const float* sin_cache,
+    int64_t max_pos, int rope_style, int scale_mode, void* out,
+    int64_t num_rows, uint32_t* err_flags, void* stream);
+
+/*
  * FP4 paged MQA-logits scorer: the consumer of the bytes written above.
  * Sources: "[HIP] Add FP4 output mode to indexer_qk_rope_quant_and_cache"
  * (aiter PR 5484), Verification (the paged FP4 MQA-logits scorer reads the

@@ -30,8 +30,8 @@ def test_exports_every_declared_symbol(F):
     assert set(names) == {"fp4idx_k_norm_rope_pack_store", "fp4idx_q_rope_pack_weights",
                           "fp4idx_indexer_prepass", "fp4idx_paged_mqa_logits",
                           "fp4idx_k_norm_rope_pack_store_ex", "fp4idx_q_rope_pack_weights_ex",
-                          "fp4idx_indexer_prepass_ex", "fp4idx_status_string",
-                          "fp4idx_version"}
+                          "fp4idx_indexer_prepass_ex", "fp4idx_rope_fake_quant",
+                          "fp4idx_status_string", "fp4idx_version"}
     out = subprocess.run(["nm", "-D", "--defined-only", F.LIB_PATH], capture_output=True,
                          text=True, check=True).stdout
     exported = set(re.findall(r"\bT (fp4idx_\w+)", out))
@@ -268,6 +268,34 @@ def test_option_host_checks(F, ratio, had, mode):
         ka["num_blocks"], qa["q"], qa["qts"], qa["qhs"], qa["w"], qa["wts"], qa["ws"],
         qa["qf"], qa["qs"], qa["wt"], qa["H"], qa["pos"], qa["cos"], qa["sin"],
         qa["max_pos"], qa["style"], qa["T"], opts, None, None) == F.ERR_ARG
+
+
+FQ_DEFECTS = [
+    (dict(n=-1), "ERR_SHAPE"),
+    (dict(x=None), "ERR_NULL"),
+    (dict(out=None), "ERR_NULL"),
+    (dict(pos=None), "ERR_NULL"),
+    (dict(per=0), "ERR_SHAPE"),
+    (dict(stride=64), "ERR_SHAPE"),
+    (dict(n=1 << 31), "ERR_SHAPE"),
+    (dict(mode=2), "ERR_ARG"),
+    (dict(style=3), "ERR_ARG"),
+    (dict(x=A[0] + 8), "ERR_ALIGN"),
+    (dict(stride=132), "ERR_ALIGN"),
+    (dict(out=A[18] + 2), "ERR_ALIGN"),
+    (dict(max_pos=0), "ERR_SHAPE"),
+]
+
+
+@pytest.mark.fake_ptr
+@pytest.mark.parametrize("over,code", FQ_DEFECTS, ids=_ids(FQ_DEFECTS))
+def test_fake_quant_host_checks(F, over, code):
+    a = dict(x=A[0], stride=128, per=1, pos=A[2], cos=A[3], sin=A[4], max_pos=64, style=0,
+             mode=1, out=A[18], n=64, err=None, stream=None)
+    a.update(over)
+    assert F.lib().fp4idx_rope_fake_quant(
+        a["x"], a["stride"], a["per"], a["pos"], a["cos"], a["sin"], a["max_pos"], a["style"],
+        a["mode"], a["out"], a["n"], a["err"], a["stream"]) == getattr(F, code)
 
 
 @pytest.mark.fake_ptr
