@@ -13,8 +13,9 @@ import sys
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SRCS = [os.path.join(PKG, "csrc", name) for name in ("fp4idx.cu", "fp4idx_scorer.cu")]
-HDR = os.path.join(ROOT, "include", "fp4idx.h")
+SRCS = [os.path.join(PKG, "csrc", name)
+        for name in ("fp4idx.cu", "fp4idx_stream.cu", "fp4idx_scorer.cu")]
+HDRS = [os.path.join(ROOT, "include", "fp4idx.h"), os.path.join(PKG, "csrc", "fp4idx_common.cuh")]
 LIB = os.path.join(PKG, "libfp4idx.so")
 
 # Bit-exact fp32: no FMA contraction, IEEE division/sqrt, subnormals kept.
@@ -33,7 +34,7 @@ def nvcc() -> str:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    newest = max(os.path.getmtime(f) for f in (*SRCS, HDR))
+    newest = max(os.path.getmtime(f) for f in (*SRCS, *HDRS))
     if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= newest:
         return LIB
     tag = f".tmp{os.getpid()}"

@@ -1,0 +1,131 @@
+"""GPU parity of the streaming pre-pass kernel (64-row work units fed by a
+producer warp, four lanes per row): the path taken for FP4 output without
+the rotation when the head count is a multiple of 16, and for every
+key-only call.  The cases leave ragged units and slices, use every
+query-row layout the producer copies (contiguous rows, contiguous heads
+under a larger token stride, one copy per row), put the quantiser's edge
+rows at both row parities of a quarter-warp, and feed out-of-range
+positions.  Bytes must equal the oracle's; weights within 1 ulp."""
+import numpy as np
+import pytest
+import torch
+
+from fp4_sparse_attention_fp4idx_gb300 import workloads as wl
+from tests.gpu_util import (DeviceWorkload, F, assert_bytes_equal, assert_same, assert_weights,
+                            run_oracle)
+
+pytestmark = pytest.mark.gpu
+
+STYLES = [wl.ROPE_NEOX, wl.ROPE_INTERLEAVED]
+
+
+@pytest.mark.parametrize("style", STYLES)
+@pytest.mark.parametrize("T,H", [(1, 16), (3, 16), (5, 48), (63, 32), (64, 16), (65, 64),
+                                 (130, 128), (301, 32)])
+def test_stream_ragged(T, H, style):
+    """Units that end mid-slice (T*H not a multiple of 64), key units that
+    end mid-unit (T not a multiple of 64), one token, 128 heads."""
+    w = wl.make_random(T, H, style, seed=2000 + 13 * T + H)
+    for mode in ("fused", "separate"):
+        d = DeviceWorkload(w)
+        assert_same(w, d.run(mode), run_oracle(w))
+        assert int(d.err.item()) == 0
+
+
+@pytest.mark.parametrize("style", STYLES)
+@pytest.mark.parametrize("scale", [1.0, 40.0, 1e-3, 3e4])
+def test_stream_special_rows(style, scale):
+    """All-zero, subnormal and exact-midpoint query rows on even and odd rows
+    of a unit (the two part orders), with the keys of the same tokens."""
+    w = wl.make_random(70, 16, style, seed=int(scale * 7) + 31 * style + 5, scales=(scale,))
+    rng = np.random.Generator(np.random.PCG64(17 + style))
+    w.q[0] = 0
+    w.k[0] = 0
+    w.q[1] = wl.subnormal_bf16(rng, 16 * 128).reshape(16, 128)
+    w.k[1] = wl.subnormal_bf16(rng, 128)
+    for t in (2, 3):
+        for h in range(16):
+            w.q[t, h] = wl.to_bf16_bits(np.concatenate(
+                [wl.midpoint_group_values(h - 8 + g + t) for g in range(4)]))
+        w.positions[t] = 0
+    w.k[4] = wl.to_bf16_bits(wl.midpoint_key_row())
+    d = DeviceWorkload(w)
+    assert_same(w, d.run("fused"), run_oracle(w))
+    assert int(d.err.item()) == 0
+
+
+@pytest.mark.parametrize("style", STYLES)
+def test_stream_query_layouts(style):
+    """The producer's three ways of copying query rows: one copy per unit
+    (dense), one per 16-row slice (heads contiguous, token stride larger than
+    H*128), one per row (head stride 256); keys with a row stride too."""
+    w = wl.make_random(50, 32, style, seed=88 + style)
+    d = DeviceWorkload(w)
+    f = F()
+    rc, rqf, rqs, rwt = run_oracle(w)
+    big1 = torch.zeros((50, 40, 128), dtype=torch.bfloat16, device="cuda")
+    big1[:, 3:35] = d.q
+    big2 = torch.zeros((50, 64, 128), dtype=torch.bfloat16, device="cuda")
+    big2[:, ::2] = d.q
+    bigk = torch.zeros((50, 2, 128), dtype=torch.bfloat16, device="cuda")
+    bigk[:, 1] = d.k
+    kv = bigk[:, 1]
+    for qv in (d.q, big1[:, 3:35], big2[:, ::2]):
+        qf, qs, wt = f.q_rope_pack_weights(qv, d.wt, d.pos, d.cos, d.sin,
+                                           rope_style=w.rope_style)
+        torch.cuda.synchronize()
+        assert_bytes_equal(qf.cpu().numpy(), rqf, f"q_fp4 strides {qv.stride()}")
+        assert_bytes_equal(qs.cpu().numpy(), rqs, f"q_scale strides {qv.stride()}")
+        assert_weights(wt.cpu().numpy(), rwt)
+        d.reset_cache()
+        qf, qs, wt = f.indexer_prepass(kv, d.gamma, d.slots, d.cache, qv, d.wt, d.pos, d.cos,
+                                       d.sin, eps=w.eps, rope_style=w.rope_style)
+        torch.cuda.synchronize()
+        assert_same(w, (d.cache.cpu().numpy(), qf.cpu().numpy(), qs.cpu().numpy(),
+                        wt.cpu().numpy()), (rc, rqf, rqs, rwt))
+
+
+def test_stream_out_of_range_positions():
+    """A query token whose position is outside [0, max_pos) is skipped as a
+    whole (its slices are flagged, nothing of it is written); the key rows
+    of such tokens are skipped and flagged; the rest is exact."""
+    w = wl.make_random(40, 32, wl.ROPE_INTERLEAVED, seed=23, max_pos=100)
+    w.positions[3] = 100
+    w.positions[17] = -1
+    w.positions[39] = 1 << 40
+    for mode in ("fused", "separate"):
+        d = DeviceWorkload(w)
+        sentinel = torch.full((40, 32, 64), 0xA5, dtype=torch.uint8, device="cuda")
+        d.reset_cache()
+        if mode == "fused":
+            qf, qs, wt = F().indexer_prepass(d.k, d.gamma, d.slots, d.cache, d.q, d.wt, d.pos,
+                                             d.cos, d.sin, eps=w.eps, rope_style=w.rope_style,
+                                             q_fp4=sentinel, err_flags=d.err)
+        else:
+            F().k_norm_rope_pack_store(d.k, d.gamma, d.pos, d.cos, d.sin, d.slots, d.cache,
+                                       eps=w.eps, rope_style=w.rope_style, err_flags=d.err)
+            qf, qs, wt = F().q_rope_pack_weights(d.q, d.wt, d.pos, d.cos, d.sin,
+                                                 rope_style=w.rope_style, q_fp4=sentinel,
+                                                 err_flags=d.err)
+        torch.cuda.synchronize()
+        assert int(d.err.item()) & F().ERRFLAG_POSITION
+        rc, rqf, rqs, rwt = run_oracle(w)
+        assert_bytes_equal(d.cache.cpu().numpy(), rc, "cache")
+        good = np.setdiff1d(np.arange(40), [3, 17, 39])
+        qfn = qf.cpu().numpy()
+        assert_bytes_equal(qfn[good], rqf[good], "q_fp4")
+        assert_bytes_equal(qs.cpu().numpy()[good], rqs[good], "q_scale")
+        assert_weights(wt.cpu().numpy()[good], rwt[good])
+        assert np.all(qfn[[3, 17, 39]] == 0xA5)
+
+
+def test_stream_repeat_and_reuse():
+    """Two launches in a row on the prefill workload give the same bytes (no
+    state carried between launches)."""
+    w = wl.make("prefill")
+    d = DeviceWorkload(w)
+    a = d.run("fused")
+    b = d.run("fused")
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+    assert int(d.err.item()) == 0
