@@ -64,7 +64,7 @@ namespace {
 #define FP4IDX_STREAM_STAGES 12
 #endif
 #ifndef FP4IDX_STREAM_PRODUCERS
-#define FP4IDX_STREAM_PRODUCERS 2
+#define FP4IDX_STREAM_PRODUCERS 4
 #endif
 
 constexpr int kUnitRows = 64;
@@ -79,7 +79,7 @@ static_assert(kStagesS % kProducers == 0, "each producer owns kStagesS / kProduc
 // 4: slices never straddle tokens), or 64 positions and 64 slots (key unit)
 // | header | 64 head weights (query unit).
 constexpr int kCoefOff = kUnitRows * kRowBytes;
-constexpr int kHdrOff = kCoefOff + kSlices * 256;  // {kind, first row/token, rows, flags}
+constexpr int kHdrOff = kCoefOff + kSlices * 256;  // {unit << 2 | kind, first, rows, flags}
 constexpr int kWOff = kHdrOff + 16;
 constexpr int kStageBytesS = kWOff + kUnitRows * 2;  // 17552, a 16-byte multiple
 constexpr int kSmemS = kStagesS * kStageBytesS;
@@ -88,6 +88,7 @@ static_assert(kSmemS <= 227 * 1024, "the ring must fit in shared memory");
 static_assert(kStageBytesS % 16 == 0, "bulk-copy destinations must be 16-byte aligned");
 
 enum : uint32_t { kUnitKey = 1, kUnitQuery = 2 };
+constexpr uint32_t kNoUnit = 0xffffffffu;  // header word 0 before a stage's first unit
 // Header flags: bits 0..3 = slice k's position is valid (query unit); bit 4 =
 // the unit's weights (query) or positions and slots (key) are in the stage.
 constexpr uint32_t kInStage = 1u << 4;
@@ -144,6 +145,37 @@ __device__ __forceinline__ bool lane_wait(uint32_t bar, uint32_t parity,
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
                                               const volatile int* abort) {
   return __all_sync(kFull, lane_wait(bar, parity, abort));
+}
+
+__device__ __forceinline__ uint32_t lds_volatile(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// A consumer's wait for unit i in stage `stage` (all 32 lanes call).  Slices
+// are claimed ahead of the producers, so the stage may still be waiting for
+// unit i - kStagesS or older; a parity wait alone would then alias an older
+// phase.  So first wait (bounded) until the producer has tagged the stage's
+// header with i -- it does so only after the previous unit in the stage was
+// released, i.e. once the stage's barrier is in unit i's phase -- and only
+// then wait for that phase.
+__device__ __forceinline__ bool wait_unit(uint32_t stage, uint32_t bar, int i,
+                                          const volatile int* abort) {
+  bool ok = (lds_volatile(stage + kHdrOff) >> 2) == (uint32_t)i;
+  if (!ok) {
+    const unsigned long long t0 = global_ns();
+    for (;;) {
+      __nanosleep(64);
+      if ((lds_volatile(stage + kHdrOff) >> 2) == (uint32_t)i) {
+        ok = true;
+        break;
+      }
+      if (*abort != 0 || global_ns() - t0 > kWaitLimitNs) break;
+    }
+  }
+  if (!__all_sync(kFull, ok)) return false;
+  return wait_or_abort(bar, (uint32_t)((i / kStagesS) & 1), abort);
 }
 
 // RoPE coefficients of one lane, in the order of its registers A (parts
@@ -562,7 +594,8 @@ __device__ __forceinline__ void issue_meta(int i, int kb, const Units& u, const 
         bulk_g2s(stage + kCoefOff + 512u, ka.slots + t0, kUnitRows * 8u, bar);
       }
       asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(stage + kHdrOff),
-                   "r"(kUnitKey), "r"(t0), "r"(n), "r"(meta ? kInStage : 0u)
+                   "r"(((uint32_t)i << 2) | kUnitKey), "r"(t0), "r"(n),
+                   "r"(meta ? kInStage : 0u)
                    : "memory");
       mbar_arrive_expect_tx(bar, meta ? 2u * kUnitRows * 8u : 0u);
     }
@@ -593,7 +626,8 @@ __device__ __forceinline__ void issue_meta(int i, int kb, const Units& u, const 
     const bool wst = wk.w_bulk && n == kUnitRows;
     if (wst) bulk_g2s(stage + kWOff, qa.w + row0, kUnitRows * 2u, bar);
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(stage + kHdrOff),
-                 "r"(kUnitQuery), "r"(row0), "r"(n), "r"(okbits | (wst ? kInStage : 0u))
+                 "r"(((uint32_t)i << 2) | kUnitQuery), "r"(row0), "r"(n),
+                 "r"(okbits | (wst ? kInStage : 0u))
                  : "memory");
     mbar_arrive_expect_tx(bar, (uint32_t)ntok * 256u + (wst ? kUnitRows * 2u : 0u));
   }
@@ -618,6 +652,9 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     for (int s = 0; s < kStagesS; ++s) {
       mbar_init(full0 + 8u * s, 1);
       mbar_init(empty0 + 8u * s, kSlices);
+      asm volatile("st.shared.u32 [%0], %1;" ::"r"(ring + (uint32_t)s * kStageBytesS + kHdrOff),
+                   "r"(kNoUnit)
+                   : "memory");
     }
     abort_flag = 0;
     next_slice = 0;
@@ -663,10 +700,12 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     // before the CTA's shared memory is released (bounded).  Every unit whose
     // rows were issued also had its metadata issued: the loop can stop only
     // at an empty-stage wait, which precedes both.
+    // The drain ignores the abort flag: only the time limit ends it.
     __syncthreads();
+    const int no_abort = 0;
     for (int m = max(issued - kStagesS / kProducers, 0); m < issued; ++m) {
       const int i = p + kProducers * m;
-      wait_or_abort(full0 + 8u * (i % kStagesS), (uint32_t)((i / kStagesS) & 1), &abort_flag);
+      wait_or_abort(full0 + 8u * (i % kStagesS), (uint32_t)((i / kStagesS) & 1), &no_abort);
     }
     return;
   }
@@ -680,7 +719,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     if (i >= n_units) break;
     const int s = i % kStagesS;
     const uint32_t stage = ring + (uint32_t)s * kStageBytesS;
-    if (!wait_or_abort(full0 + 8u * s, (uint32_t)((i / kStagesS) & 1), &abort_flag)) {
+    if (!wait_unit(stage, full0 + 8u * s, i, &abort_flag)) {
       if (lane == 0) {
         flag_error(sh.err, FP4IDX_ERRFLAG_TIMEOUT);
         abort_flag = 1;
@@ -689,7 +728,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     }
     uint32_t hdr[4];
     lds128(stage + kHdrOff, hdr);
-    if (hdr[0] == kUnitKey)
+    if ((hdr[0] & 3u) == kUnitKey)
       key_slice<kStyle>(stage, (int32_t)hdr[1], (int)hdr[2], hdr[3], sl, ka, sh);
     else
       query_slice<kStyle>(stage, (int32_t)hdr[1], (int)hdr[2], hdr[3], sl, wk, qa, sh);
