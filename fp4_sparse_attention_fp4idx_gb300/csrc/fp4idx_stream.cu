@@ -66,8 +66,11 @@ namespace {
 #ifndef FP4IDX_STREAM_PRODUCERS
 #define FP4IDX_STREAM_PRODUCERS 4
 #endif
+#ifndef FP4IDX_STREAM_UNIT_ROWS
+#define FP4IDX_STREAM_UNIT_ROWS 64
+#endif
 
-constexpr int kUnitRows = 64;
+constexpr int kUnitRows = FP4IDX_STREAM_UNIT_ROWS;
 constexpr int kSliceRows = 16;
 constexpr int kSlices = kUnitRows / kSliceRows;
 constexpr int kConsumers = FP4IDX_STREAM_CONSUMERS;
@@ -81,9 +84,13 @@ static_assert(kStagesS % kProducers == 0, "each producer owns kStagesS / kProduc
 constexpr int kCoefOff = kUnitRows * kRowBytes;
 constexpr int kHdrOff = kCoefOff + kSlices * 256;  // {unit << 2 | kind, first, rows, flags}
 constexpr int kWOff = kHdrOff + 16;
-constexpr int kStageBytesS = kWOff + kUnitRows * 2;  // 17552, a 16-byte multiple
+constexpr int kStageBytesS = kWOff + kUnitRows * 2;  // 17552 for 64-row units
 constexpr int kSmemS = kStagesS * kStageBytesS;
 constexpr int kBatch = 32 / kSlices;  // units per position lookup
+constexpr int kSlotsOff = kCoefOff + kUnitRows * 8;  // key unit: slots after positions
+static_assert(kUnitRows % kSliceRows == 0 && kSlices <= 4 && 32 % kSlices == 0,
+              "a unit is 1, 2 or 4 slices");
+static_assert(2 * kUnitRows * 8 <= kSlices * 256, "key positions and slots fit the area");
 static_assert(kSmemS <= 227 * 1024, "the ring must fit in shared memory");
 static_assert(kStageBytesS % 16 == 0, "bulk-copy destinations must be 16-byte aligned");
 
@@ -462,7 +469,7 @@ __device__ __forceinline__ void key_slice(uint32_t stage, int32_t t0, int n, uin
     if (have) {
       if (flags & kInStage) {
         pos = lds_s64(stage + kCoefOff + 8u * r);
-        slot = lds_s64(stage + kCoefOff + 512u + 8u * r);
+        slot = lds_s64(stage + kSlotsOff + 8u * r);
       } else {
         pos = __ldg(sh.pos + t0 + r);
         slot = __ldg(ka.slots + t0 + r);
@@ -591,7 +598,7 @@ __device__ __forceinline__ void issue_meta(int i, int kb, const Units& u, const 
       const bool meta = wk.meta_bulk && n == kUnitRows;
       if (meta) {
         bulk_g2s(stage + kCoefOff, sh.pos + t0, kUnitRows * 8u, bar);
-        bulk_g2s(stage + kCoefOff + 512u, ka.slots + t0, kUnitRows * 8u, bar);
+        bulk_g2s(stage + kSlotsOff, ka.slots + t0, kUnitRows * 8u, bar);
       }
       asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(stage + kHdrOff),
                    "r"(((uint32_t)i << 2) | kUnitKey), "r"(t0), "r"(n),
@@ -648,6 +655,11 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   u.nq = (int32_t)((int64_t)(blockIdx.x + 1) * wk.nq / gridDim.x) - u.q_lo;
   const uint32_t ring = smem_addr(smem);
   const uint32_t full0 = smem_addr(&full[0]), empty0 = smem_addr(&empty[0]);
+  // The producers' first position lookups go out before anything else: the
+  // cos/sin copies of the first units depend on them, and once the row
+  // copies of every SM are queued a load waits behind all of them.
+  int64_t pos_first = 0;
+  if (warp >= kConsumers) pos_first = slice_pos(warp - kConsumers, 0, u, wk, sh);
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStagesS; ++s) {
       mbar_init(full0 + 8u * s, 1);
@@ -668,12 +680,11 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     const int p = warp - kConsumers;
     const int n_own = n_units > p ? (n_units - p + kProducers - 1) / kProducers : 0;
     int issued = 0;  // own units issued
-    int64_t pos_cur = slice_pos(p, 0, u, wk, sh), pos_next = 0;
-    const int pre = min(kStagesS / kProducers, n_own);
-    for (int m = 0; m < pre; ++m) {
-      const int i = p + kProducers * m;
-      issue_rows(i, u, wk, ka, qa, ring + (uint32_t)i * kStageBytesS, full0 + 8u * i);
-    }
+    int64_t pos_cur = pos_first, pos_next = 0;
+    // The first own unit's rows go out at once; every later unit's rows go
+    // out together with its metadata (the first metadata waits for the
+    // positions, and should not queue behind a whole ring of rows).
+    if (n_own > 0) issue_rows(p, u, wk, ka, qa, ring + (uint32_t)p * kStageBytesS, full0 + 8u * p);
     for (int m = 0; m < n_own; ++m) {
       if (m % kBatch == 0) {
         if (m > 0) pos_cur = pos_next;
@@ -690,8 +701,8 @@ __global__ void __launch_bounds__(kThreadsS, 1)
           }
           break;
         }
-        issue_rows(i, u, wk, ka, qa, stage, bar);
       }
+      if (m > 0) issue_rows(i, u, wk, ka, qa, stage, bar);
       issue_meta(i, m % kBatch, u, wk, ka, qa, sh, pos_cur, stage, bar);
       issued = m + 1;
     }
