@@ -29,23 +29,24 @@
 // 2-3 (id 2).  Row r's cell is TMEM column base + r/32; the key side reads
 // lane r, the query side lane r%32 (written to every lane quadrant).
 //
-// Roles (10 warps).
-//   producer (warp 8): TMA tensor copies of the page payloads (64 tokens x
+// Roles (18 warps).
+//   producer (warp 16): TMA tensor copies of the page payloads (64 tokens x
 //     64 bytes, in the 64-byte swizzled layout the MMA reads) and bulk copies
 //     of the exponent words into a ring of S stages; the warp fetches the
 //     page ids of 16 tiles per load, one batch ahead;
-//   MMA issuer (warp 9, the whole warp waiting, lane 0 issuing): two MMAs
-//     per tile into one of two TMEM accumulators, committed to the
-//     accumulator's "full" barrier and the stage's "empty" barrier;
-//   two epilogue groups (warps 0-3, 4-7), group e owning the tiles k with
-//     k % 2 == e and accumulator e: for its tile it writes the keys' scale
-//     words into TMEM (and, at the first tile of a segment, the segment's
-//     query operand and scale words), then reads the accumulator (thread =
-//     token = TMEM lane) and forms sum_h w * max(D, 0) per query token in
-//     registers.  Each warp holds its own copy of the
-//     segment's head weights, so no warp waits on another except through
-//     bounded mbarrier waits.  One group's epilogue overlaps the other
-//     group's MMA.
+//   MMA issuer (warp 17, the whole warp waiting, lane 0 issuing): two MMAs
+//     per tile into TMEM accumulator k % 3, committed to the tile's
+//     acc_full barrier and the stage's empty barrier;
+//   two epilogue groups of 8 warps (0-7, 8-15), group e owning the tiles k
+//     with k % 2 == e.  Warps q and q+4 of a group share TMEM lane quadrant q
+//     and split the accumulator's 32-column chunks.  For a tile a group
+//     first prepares its next tile (the keys' scale words into TMEM and, at
+//     the first tile of a segment, the segment's query operand and scale
+//     words), then reads its tile's accumulator chunk by chunk (thread =
+//     token = TMEM lane), releases the accumulator and stores
+//     sum_h w * max(D, 0) per query token.  With three accumulators the MMAs
+//     of the next tiles run while a group reads and reduces.  Each warp holds
+//     its own copy of the segment's head weights.
 // Every wait is bounded (1 s) and a shared abort flag stops every role; in
 // flight copies and MMAs are waited for before TMEM and shared memory are
 // released.  Each E2M1 product is exact; the tensor core accumulates in fp32.
@@ -59,10 +60,12 @@
 
 namespace {
 
-constexpr int kEpiWarps = 8;                 // two groups of four
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 10 * 32;
+constexpr int kEpiWarps = 16;                // two groups of eight
+constexpr int kGroupWarps = 8;
+constexpr int kProducerWarp = 16;
+constexpr int kMmaWarp = 17;
+constexpr int kThreads = 18 * 32;
+constexpr int kMaxNext = 4;                  // next_n <= kMaxRows / 32
 constexpr int kTile = 128;                   // key tokens per tile (MMA M)
 constexpr int kKvBlock = FP4IDX_KV_BLOCK;
 constexpr int kPageBytes = FP4IDX_PAGE_BYTES;
@@ -93,12 +96,12 @@ struct ScorerParams {
   int32_t max_context;
   int32_t tiles_total;     // ceil(max_context / 128) tiles per sequence
   int32_t stages;
-  uint32_t tmem_cols;      // power of two >= 2R + 32
+  uint32_t tmem_cols;      // power of two >= 3R + 40
 };
 
 // Shared-memory carve-up (offsets from a 1024-byte aligned base).
 struct Layout {
-  uint32_t a, q, e, w, bars, ok, misc, scan, total;
+  uint32_t a, q, e, w, x, bars, ok, misc, scan, total;
 };
 
 // Barrier indices: full[S], empty[S], sfa_ready[2], acc_full[2].  There is
@@ -107,17 +110,30 @@ struct Layout {
 // on sfa_ready for tile k also covers the accumulator's release.
 __host__ __device__ inline int bar_full(int s) { return s; }
 __host__ __device__ inline int bar_empty(int S, int s) { return S + s; }
+// sfa_ready[e]: group e has prepared its next tile (8 arrivals).
 __host__ __device__ inline int bar_sfa(int S, int e) { return 2 * S + e; }
-__host__ __device__ inline int bar_accf(int S, int e) { return 2 * S + 2 + e; }
-constexpr int kExtraBars = 4;
+// acc_full[k % 6]: the MMAs of tile k are complete.  Tile k uses accumulator
+// k % 3 and belongs to group k % 2, so each of the six barriers is waited on
+// by one group only, one phase after another.
+__host__ __device__ inline int bar_accf(int S, int k6) { return 2 * S + 2 + k6; }
+// acc_empty[a]: the group that read accumulator a has its values (8 arrivals).
+__host__ __device__ inline int bar_acce(int S, int a) { return 2 * S + 8 + a; }
+// Partial-sum hand-off between the two warps of a lane quadrant (group e,
+// quadrant q, buffer b), used when a query token's heads span both halves.
+__host__ __device__ inline int bar_xch(int S, int e, int q, int b) {
+  return 2 * S + 11 + (e * 4 + q) * 2 + b;
+}
+constexpr int kExtraBars = 2 + 6 + 3 + 16;
+constexpr int kAccs = 3;  // TMEM accumulators
 
 __host__ __device__ inline Layout make_layout(int S, int R) {
   Layout L;
   L.a = 0;                                     // S x 8192, swizzled payloads
   L.q = L.a + (uint32_t)S * kStageA;           // 2 x R x 64, swizzled queries
   L.e = L.q + 2u * (uint32_t)R * 64;           // S x 512 exponent words
-  L.w = L.e + (uint32_t)S * kStageE;           // 8 epilogue warps x R weights
-  L.bars = L.w + (uint32_t)kEpiWarps * R * 4;  // 2S + 4 mbarriers
+  L.w = L.e + (uint32_t)S * kStageE;           // 16 epilogue warps x R weights
+  L.x = L.w + (uint32_t)kEpiWarps * R * 4;     // partial sums: 2 groups x 2 x next_n x 128
+  L.bars = L.x + 2u * 2u * kMaxNext * kTile * 4u;  // 2S + 4 mbarriers
   L.ok = L.bars + 8u * (uint32_t)(2 * S + kExtraBars);  // S page masks
   L.misc = L.ok + 4u * (uint32_t)S;            // tmem base, abort, b/t/n start
   L.scan = L.misc + 32;                        // kThreads + 1 partial sums (int64)
@@ -249,36 +265,41 @@ __device__ __forceinline__ int ctx_eff(const ScorerParams& p, int b) {
 
 __device__ __forceinline__ int work_tiles(int ctx) { return (ctx + kTile - 1) / kTile; }
 
-// sum over the 32 columns of chunk c of w * max(D, 0), for chunks [C0, C1)
-// of the accumulator at column address acc (this thread's TMEM lane).
+// Chunks [C0, C1) of an accumulator (this thread's TMEM lane, 32 columns
+// each), one chunk in registers at a time: part[c - C0] = sum over chunk c's
+// columns of w * max(D, 0).  Returns once every TMEM load has completed.
 template <int C0, int C1>
-__device__ __forceinline__ void epilogue_pass(uint32_t acc, const float* wts, float* part) {
-  uint32_t r[C1 - C0][32];
-  float4 w[C1 - C0][8];
+struct HalfAcc {
+  __device__ __forceinline__ void run(uint32_t acc, const float* wts, float* part) const {
 #pragma unroll
-  for (int c = C0; c < C1; ++c) tmem_ld32(acc + 32u * c, r[c - C0]);
+    for (int c = C0; c < C1; ++c) {
+      uint32_t r[32];
+      tmem_ld32(acc + 32u * c, r);
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      // two independent packed chains, then a fixed combining order
+      float2 a0 = make_float2(0.0f, 0.0f), a1 = a0;
 #pragma unroll
-  for (int c = C0; c < C1; ++c)
-#pragma unroll
-    for (int i = 0; i < 8; ++i) w[c - C0][i] = reinterpret_cast<const float4*>(wts + 32 * c)[i];
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int c = C0; c < C1; ++c) {
-    float2 a = make_float2(0.0f, 0.0f);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float4 ww = w[c - C0][i];
-      const uint32_t* x = r[c - C0] + 4 * i;
-      a = fma2(make_float2(ww.x, ww.y),
-               make_float2(fmaxf(__uint_as_float(x[0]), 0.0f), fmaxf(__uint_as_float(x[1]), 0.0f)),
-               a);
-      a = fma2(make_float2(ww.z, ww.w),
-               make_float2(fmaxf(__uint_as_float(x[2]), 0.0f), fmaxf(__uint_as_float(x[3]), 0.0f)),
-               a);
+      for (int i = 0; i < 8; ++i) {
+        const float4 ww = reinterpret_cast<const float4*>(wts + 32 * c)[i];
+        const uint32_t* x = r + 4 * i;
+        a0 = fma2(make_float2(ww.x, ww.y),
+                  make_float2(fmaxf(__uint_as_float(x[0]), 0.0f),
+                              fmaxf(__uint_as_float(x[1]), 0.0f)),
+                  a0);
+        a1 = fma2(make_float2(ww.z, ww.w),
+                  make_float2(fmaxf(__uint_as_float(x[2]), 0.0f),
+                              fmaxf(__uint_as_float(x[3]), 0.0f)),
+                  a1);
+      }
+      part[c - C0] = __fadd_rn(__fadd_rn(a0.x, a0.y), __fadd_rn(a1.x, a1.y));
     }
-    part[c] = __fadd_rn(a.x, a.y);
   }
-}
+};
+
+template <int C0, int C1>
+struct HalfAccT : HalfAcc<C0, C1> {
+  static constexpr int kC0 = C0, kC1 = C1;
+};
 
 // Walks a CTA's tiles in order: sequence b, tile t, its context, and the
 // segment index g (how many times b has changed since the first tile).
@@ -365,8 +386,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int b0 = start[0], t0 = start[1];
     if (tid == 0) {
       for (int i = 0; i < 2 * S + kExtraBars; ++i) {
-        // sfa_ready takes one arrival per epilogue warp of a group
-        const int cnt = (i >= 2 * S && i < 2 * S + 2) ? 4 : 1;
+        // sfa_ready and acc_empty take one arrival per epilogue warp of a group
+        const int cnt = ((i >= bar_sfa(S, 0) && i < bar_sfa(S, 2)) ||
+                         (i >= bar_acce(S, 0) && i < bar_acce(S, kAccs)))
+                            ? kGroupWarps
+                            : 1;
         asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar(i)), "r"(cnt)
                      : "memory");
       }
@@ -385,7 +409,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = misc[0];
     // TMEM columns: accumulators [0, R) and [R, 2R); key scale words of
     // group e at 2R + 8e; query scale words of segment g at 2R + 16 + 8(g%2).
-    const uint32_t sfa_col0 = 2u * R, sfb_col0 = 2u * R + 16u;
+    // TMEM columns: accumulator a at aR (a < 3); the keys' scale words of
+    // accumulator a's tile at 3R + 8a; the query scale words of segment g at
+    // 3R + 24 + 8(g%2).
+    const uint32_t sfa_col0 = (uint32_t)kAccs * R, sfb_col0 = (uint32_t)kAccs * R + 24u;
     int issued = 0;  // producer: tiles whose copies were issued
 
     if (warp == kProducerWarp) {
@@ -483,20 +510,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t a_desc0 = sw64_desc(smem_addr(sA)), q_desc0 = sw64_desc(smem_addr(sQ));
       int done = 0;
       for (int k = 0; k < n; ++k) {
-        const int s = k % S, e = k & 1;
+        const int s = k % S, e = k & 1, a = k % kAccs;
         bool ok = wait_phase(bar(bar_sfa(S, e)), (uint32_t)(k >> 1) & 1u, abort) &&
-                  wait_phase(bar(bar_full(s)), (uint32_t)(k / S) & 1u, abort);
+                  wait_phase(bar(bar_full(s)), (uint32_t)(k / S) & 1u, abort) &&
+                  (k < kAccs ||
+                   wait_phase(bar(bar_acce(S, a)), (uint32_t)(k / kAccs - 1) & 1u, abort));
         if (!__all_sync(0xffffffffu, ok)) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         if (lane == 0) {
-          const uint64_t a = a_desc0 + (uint64_t)(s * (kStageA >> 4));
-          const uint64_t q = q_desc0 + (uint64_t)((wk.g & 1) * R * (64 >> 4));
-          const uint32_t d = tmem + (uint32_t)e * (uint32_t)R;
-          const uint32_t sfa = tmem + sfa_col0 + 8u * (uint32_t)e;
+          const uint64_t adesc = a_desc0 + (uint64_t)(s * (kStageA >> 4));
+          const uint64_t qdesc = q_desc0 + (uint64_t)((wk.g & 1) * R * (64 >> 4));
+          const uint32_t d = tmem + (uint32_t)a * (uint32_t)R;
+          const uint32_t sfa = tmem + sfa_col0 + 8u * (uint32_t)a;
           const uint32_t sfb = tmem + sfb_col0 + 8u * (uint32_t)(wk.g & 1);
-          mma_mxf4(d, a, q, id0, sfa, sfb, 0u);
-          mma_mxf4(d, a + 2, q + 2, id1, sfa, sfb, 1u);
-          mma_commit(bar(bar_accf(S, e)));
+          mma_mxf4(d, adesc, qdesc, id0, sfa, sfb, 0u);
+          mma_mxf4(d, adesc + 2, qdesc + 2, id1, sfa, sfb, 1u);
+          mma_commit(bar(bar_accf(S, k % 6)));
           mma_commit(bar(bar_empty(S, s)));
         }
         __syncwarp();
@@ -506,91 +535,150 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (done > 0 && lane == 0)  // the last commits land before the memory is released
         wait_phase_drain(bar(bar_empty(S, (done - 1) % S)), (uint32_t)((done - 1) / S) & 1u);
     } else {
-      // ---- epilogue group e: tiles k = e, e+2, ... ---------------------------
-      const int e = warp >> 2, quad = warp & 3;
-      const int row = quad * 32 + lane;             // token of the tile = TMEM lane
+      // ---- epilogue group e (warps 8e .. 8e+7): tiles k = e, e+2, ... --------
+      // Warps q and q+4 of a group share TMEM lane quadrant q (tokens
+      // 32q .. 32q+31) and split the accumulator's 32-column chunks: the
+      // lower half takes chunks [0, kC1), the upper half [kC1, NCHUNK).  Per
+      // tile a warp first prepares the group's next tile, then reads and
+      // reduces its chunks, releases the accumulator (acc_empty) and stores
+      // the logits.
+      constexpr int kC1 = (NCHUNK + 1) / 2;
+      const int e = warp / kGroupWarps, gw = warp % kGroupWarps;
+      const int quad = gw & 3, half = gw >> 2;
+      const int row = quad * 32 + lane;  // token of the tile = TMEM lane
       const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-      float* const wts = sW + warp * R;             // this warp's head weights
-      Walker wk;
-      wk.init(p, b0, t0);
-      if (e == 1) wk.advance(p);
-      int wg = -1;                                  // segment of the weights held
-      for (int k = e; k < n; k += 2) {
+      float* const wts = sW + warp * R;  // this warp's head weights
+      float* const xch = reinterpret_cast<float*>(smem + L.x) + e * 2 * kMaxNext * kTile;
+      const int cpj = p.H / 32;          // chunks per query token
+      // a query token whose heads span both halves (its partial sums are
+      // handed from the upper to the lower warp through shared memory)
+      const bool split = kC1 < NCHUNK && kC1 % cpj != 0;
+      const int js = kC1 / cpj;
+
+      // Prepare tile k (walker w): wait for its stage; the lower half writes
+      // the keys' scale words and, at the first tile of a segment, the
+      // segment's query operand and query scale words; every warp arrives on
+      // sfa_ready[e].
+      auto prepare = [&](int k, const Walker& w, uint32_t& okmask) -> bool {
         const int s = k % S;
-        // prepare tile k: the keys' scale words (and a new segment's queries)
-        bool ok = wait_phase(bar(bar_full(s)), (uint32_t)(k / S) & 1u, abort);
-        if (!__all_sync(0xffffffffu, ok)) break;
-        const uint32_t okmask = stage_ok[s];
-        const int64_t row0 = ((int64_t)wk.b * p.next_n) * p.H;  // first query row of b
-        if (k == 0 || wk.t == 0) {  // first tile of a segment: its query operand
-          const int gb = wk.g & 1;
-          if (row < R) {
-            const uint4* src = reinterpret_cast<const uint4*>(p.q_fp4 + (row0 + row) * 64);
-            uint8_t* dst = sQ + gb * R * 64;
+        const bool ok = wait_phase(bar(bar_full(s)), (uint32_t)(k / S) & 1u, abort);
+        if (!__all_sync(0xffffffffu, ok)) return false;
+        okmask = stage_ok[s];
+        if (half == 0) {
+          if (k == 0 || w.t == 0) {  // first tile of a segment: its query operand
+            const int64_t row0 = ((int64_t)w.b * p.next_n) * p.H;  // first query row of b
+            const int gb = w.g & 1;
+            if (row < R) {
+              const uint4* src = reinterpret_cast<const uint4*>(p.q_fp4 + (row0 + row) * 64);
+              uint8_t* dst = sQ + gb * R * 64;
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-              *reinterpret_cast<uint4*>(dst + sw64_chunk(row, c)) = __ldg(src + c);
-          }
-          uint32_t v[4];
+              for (int c = 0; c < 4; ++c)
+                *reinterpret_cast<uint4*>(dst + sw64_chunk(row, c)) = __ldg(src + c);
+            }
+            uint32_t v[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int r = 32 * j + lane;
-            v[j] = r < R ? __ldg(reinterpret_cast<const uint32_t*>(p.q_scale) + row0 + r)
-                         : 0x7F7F7F7Fu;
+            for (int j = 0; j < 4; ++j) {
+              const int r = 32 * j + lane;
+              v[j] = r < R ? __ldg(reinterpret_cast<const uint32_t*>(p.q_scale) + row0 + r)
+                           : 0x7F7F7F7Fu;
+            }
+            asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             tmem + lane_base + sfb_col0 + 8u * (uint32_t)gb),
+                         "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
+                         : "memory");
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           }
-          asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                           tmem + lane_base + sfb_col0 + 8u * (uint32_t)gb),
-                       "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
-                       : "memory");
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        }
-        {
           const uint32_t word = reinterpret_cast<const uint32_t*>(sE + s * kStageE)[row];
           asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(
-                           tmem + lane_base + sfa_col0 + 8u * (uint32_t)e + (uint32_t)quad),
+                           tmem + lane_base + sfa_col0 + 8u * (uint32_t)(k % kAccs) +
+                           (uint32_t)quad),
                        "r"(word)
                        : "memory");
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         }
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(bar_sfa(S, e)));
+        return true;
+      };
+
+      // Tile k, chunks [C0, C1) of accumulator k % 3: load and reduce chunk
+      // by chunk, release the accumulator, store (or hand off) the logits.
+      auto tile = [&](auto acc, int k, const Walker& w, uint32_t okmask, bool& live) {
+        constexpr int C0 = decltype(acc)::kC0, C1 = decltype(acc)::kC1;
+        const int a = k % kAccs;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        float part[C1 > C0 ? C1 - C0 : 1];
+        acc.run(tmem + lane_base + (uint32_t)a * (uint32_t)R, wts, part);
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(bar_acce(S, a)));
+        const int s_tok = w.t * kTile + row;
+        const bool valid = s_tok < w.ctx && ((okmask >> (row >> 6)) & 1u);
+        float* const xb = xch + ((k >> 1) & 1) * kMaxNext * kTile;
+        const uint32_t xbar = bar(bar_xch(S, e, quad, (k >> 1) & 1));
+        float* const out = p.logits + ((int64_t)w.b * p.next_n) * p.logits_stride + s_tok;
+#pragma unroll
+        for (int j = 0; j < kMaxNext; ++j) {
+          if (j >= p.next_n) break;
+          float v = 0.0f;
+          bool any = false;
+#pragma unroll
+          for (int c = C0; c < C1; ++c)
+            if (c / cpj == j) {
+              v = any ? __fadd_rn(v, part[c - C0]) : part[c - C0];
+              any = true;
+            }
+          if (split && j == js) {
+            if (half == 1) {  // hand the upper part to the lower warp
+              xb[j * kTile + row] = v;
+              __syncwarp();
+              if (lane == 0) mbar_arrive(xbar);
+              continue;
+            }
+            if (!__all_sync(0xffffffffu, wait_phase(xbar, (uint32_t)(k >> 2) & 1u, abort))) {
+              live = false;
+              return;
+            }
+            v = __fadd_rn(v, xb[j * kTile + row]);
+          } else if (!any) {
+            continue;
+          }
+          if (s_tok < p.max_context) out[(int64_t)j * p.logits_stride] = valid ? v : -INFINITY;
+        }
+      };
+
+      Walker wk;
+      wk.init(p, b0, t0);
+      if (e == 1) wk.advance(p);
+      Walker nw = wk;
+      nw.advance(p);
+      nw.advance(p);
+      uint32_t okm = 0, okm_next = 0;
+      bool live = e < n && prepare(e, wk, okm);
+      int wg = -1;  // segment of the weights held
+      for (int k = e; k < n && live; k += 2) {
+        if (!__all_sync(0xffffffffu,
+                        wait_phase(bar(bar_accf(S, k % 6)), (uint32_t)(k / 6) & 1u, abort)))
+          break;
+        // The next tile of this group first: its scale words go to the slot
+        // of accumulator (k+2) % 3, whose last MMAs (tile k-1) are complete
+        // because tile k's are.
+        if (k + 2 < n) live = prepare(k + 2, nw, okm_next);
         if (wk.g != wg) {  // this warp's copy of the segment's head weights
+          const int64_t row0 = ((int64_t)wk.b * p.next_n) * p.H;
           for (int i = lane; i < R; i += 32) wts[i] = __ldg(p.weights + row0 + i);
           __syncwarp();
           wg = wk.g;
         }
-
-        // epilogue of tile k
-        ok = wait_phase(bar(bar_accf(S, e)), (uint32_t)(k >> 1) & 1u, abort);
-        if (!__all_sync(0xffffffffu, ok)) break;
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        // Two passes over the accumulator's 32-column chunks; each pass
-        // issues its TMEM loads and its weight loads together, so their
-        // latencies overlap.
-        float part[NCHUNK];
-        constexpr int kFirst = (NCHUNK + 1) / 2;
-        epilogue_pass<0, kFirst>(tmem + lane_base + (uint32_t)e * (uint32_t)R, wts, part);
-        if constexpr (NCHUNK > kFirst)
-          epilogue_pass<kFirst, NCHUNK>(tmem + lane_base + (uint32_t)e * (uint32_t)R, wts, part);
-        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-        const int s_tok = wk.t * kTile + row;
-        const bool valid = s_tok < wk.ctx && ((okmask >> (row >> 6)) & 1u);
-        if (s_tok < p.max_context) {
-          float* out = p.logits + ((int64_t)wk.b * p.next_n) * p.logits_stride + s_tok;
-          const int cpj = p.H / 32;  // chunks per query token
-#pragma unroll
-          for (int j = 0; j < NCHUNK; ++j) {
-            if (j >= p.next_n) break;
-            float v = 0.0f;
-#pragma unroll
-            for (int c = 0; c < NCHUNK; ++c)
-              if (c / cpj == j) v = (c % cpj == 0) ? part[c] : __fadd_rn(v, part[c]);
-            out[(int64_t)j * p.logits_stride] = valid ? v : -INFINITY;
-          }
-        }
-        wk.advance(p);
-        wk.advance(p);
+        if (half == 0)
+          tile(HalfAccT<0, kC1>(), k, wk, okm, live);
+        else
+          tile(HalfAccT<kC1, NCHUNK>(), k, wk, okm, live);
+        okm = okm_next;
+        wk = nw;
+        nw.advance(p);
+        nw.advance(p);
       }
     }
 
@@ -723,7 +811,7 @@ extern "C" fp4idx_status fp4idx_paged_mqa_logits(
   p.max_context = (int32_t)max_context;
   p.tiles_total = (int32_t)((max_context + kTile - 1) / kTile);
   uint32_t cols = 32;
-  while (cols < 2u * (uint32_t)p.R + 32u) cols <<= 1;
+  while (cols < (uint32_t)kAccs * (uint32_t)p.R + 40u) cols <<= 1;
   p.tmem_cols = cols;
   // As many stages as fit in one CTA's shared memory (one CTA per SM).
   int S = kMaxStages;
