@@ -29,24 +29,26 @@
 // 2-3 (id 2).  Row r's cell is TMEM column base + r/32; the key side reads
 // lane r, the query side lane r%32 (written to every lane quadrant).
 //
-// Roles (18 warps).
-//   producer (warp 16): TMA tensor copies of the page payloads (64 tokens x
-//     64 bytes, in the 64-byte swizzled layout the MMA reads) and bulk copies
-//     of the exponent words into a ring of S stages; the warp fetches the
-//     page ids of 16 tiles per load, one batch ahead;
-//   MMA issuer (warp 17, the whole warp waiting, lane 0 issuing): two MMAs
-//     per tile into TMEM accumulator k % 3, committed to the tile's
-//     acc_full barrier and the stage's empty barrier;
+// Roles (17 + P warps, P = kProducers producer warps).
+//   producers (warps 16 .. 16+P-1): TMA tensor copies of the page payloads
+//     (64 tokens x 64 bytes, in the 64-byte swizzled layout the MMA reads)
+//     and bulk copies of the exponent words into a ring of S stages;
+//     producer i issues tiles i, i+P, ...; each warp fetches the page ids
+//     of 16 of its tiles per load, one batch ahead;
+//   MMA issuer (warp 16+P): per tile it waits for the data and for a free
+//     accumulator, stages the keys' exponent words (and, at the first tile
+//     of a segment, the segment's query operand and query scale words) in
+//     shared memory as a 32 x 128-bit transpose, and lane 0 issues
+//     tcgen05.cp of those words into the scale-factor columns of TMEM, the
+//     two MMAs into accumulator k % 3 and the commits -- all in order in
+//     the tensor pipe, so no thread waits for the copies;
 //   two epilogue groups of 8 warps (0-7, 8-15), group e owning the tiles k
 //     with k % 2 == e.  Warps q and q+4 of a group share TMEM lane quadrant q
-//     and split the accumulator's 32-column chunks.  For a tile a group
-//     first prepares its next tile (the keys' scale words into TMEM and, at
-//     the first tile of a segment, the segment's query operand and scale
-//     words), then reads its tile's accumulator chunk by chunk (thread =
-//     token = TMEM lane), releases the accumulator and stores
-//     sum_h w * max(D, 0) per query token.  With three accumulators the MMAs
-//     of the next tiles run while a group reads and reduces.  Each warp holds
-//     its own copy of the segment's head weights.
+//     and split the accumulator's 32-column chunks.  Per tile a warp reads
+//     its chunks one at a time (thread = token = TMEM lane), releases the
+//     accumulator (acc_empty) and stores sum_h w * max(D, 0) per query
+//     token; a page's validity comes from the block table, fetched a tile
+//     ahead.  Each warp holds its own copy of the segment's head weights.
 // Every wait is bounded (1 s) and a shared abort flag stops every role; in
 // flight copies and MMAs are waited for before TMEM and shared memory are
 // released.  Each E2M1 product is exact; the tensor core accumulates in fp32.
@@ -62,10 +64,16 @@ namespace {
 
 constexpr int kEpiWarps = 16;                // two groups of eight
 constexpr int kGroupWarps = 8;
-constexpr int kProducerWarp = 16;
-constexpr int kMmaWarp = 17;
-constexpr int kThreads = 18 * 32;
+#ifndef FP4IDX_SCORER_PRODUCERS
+#define FP4IDX_SCORER_PRODUCERS 1
+#endif
+constexpr int kProducers = FP4IDX_SCORER_PRODUCERS;  // producer warps
+constexpr int kProducerWarp = 16;                    // the first of them
+constexpr int kMmaWarp = kProducerWarp + kProducers;
+constexpr int kThreads = (kMmaWarp + 1) * 32;
 constexpr int kMaxNext = 4;                  // next_n <= kMaxRows / 32
+constexpr int kAccs = 3;                     // TMEM accumulators (tile k: k % 3)
+constexpr int kQBufs = 4;                    // query operands (segment g: g % 4)
 constexpr int kTile = 128;                   // key tokens per tile (MMA M)
 constexpr int kKvBlock = FP4IDX_KV_BLOCK;
 constexpr int kPageBytes = FP4IDX_PAGE_BYTES;
@@ -101,41 +109,36 @@ struct ScorerParams {
 
 // Shared-memory carve-up (offsets from a 1024-byte aligned base).
 struct Layout {
-  uint32_t a, q, e, w, x, bars, ok, misc, scan, total;
+  uint32_t a, q, e, w, x, sf, bars, ok, misc, scan, total;
 };
 
-// Barrier indices: full[S], empty[S], sfa_ready[2], acc_full[2].  There is
-// no "accumulator empty" barrier: an epilogue warp reads accumulator e of
-// tile k-2 to completion before it prepares tile k, so the MMA issuer's wait
-// on sfa_ready for tile k also covers the accumulator's release.
+// Barrier indices: full[S], empty[S], then the ones below.
 __host__ __device__ inline int bar_full(int s) { return s; }
 __host__ __device__ inline int bar_empty(int S, int s) { return S + s; }
-// sfa_ready[e]: group e has prepared its next tile (8 arrivals).
-__host__ __device__ inline int bar_sfa(int S, int e) { return 2 * S + e; }
 // acc_full[k % 6]: the MMAs of tile k are complete.  Tile k uses accumulator
 // k % 3 and belongs to group k % 2, so each of the six barriers is waited on
 // by one group only, one phase after another.
-__host__ __device__ inline int bar_accf(int S, int k6) { return 2 * S + 2 + k6; }
+__host__ __device__ inline int bar_accf(int S, int k6) { return 2 * S + k6; }
 // acc_empty[a]: the group that read accumulator a has its values (8 arrivals).
-__host__ __device__ inline int bar_acce(int S, int a) { return 2 * S + 8 + a; }
+__host__ __device__ inline int bar_acce(int S, int a) { return 2 * S + 6 + a; }
 // Partial-sum hand-off between the two warps of a lane quadrant (group e,
 // quadrant q, buffer b), used when a query token's heads span both halves.
 __host__ __device__ inline int bar_xch(int S, int e, int q, int b) {
-  return 2 * S + 11 + (e * 4 + q) * 2 + b;
+  return 2 * S + 9 + (e * 4 + q) * 2 + b;
 }
-constexpr int kExtraBars = 2 + 6 + 3 + 16;
-constexpr int kAccs = 3;  // TMEM accumulators
+constexpr int kExtraBars = 6 + 3 + 16;
 
 __host__ __device__ inline Layout make_layout(int S, int R) {
   Layout L;
   L.a = 0;                                     // S x 8192, swizzled payloads
-  L.q = L.a + (uint32_t)S * kStageA;           // 2 x R x 64, swizzled queries
-  L.e = L.q + 2u * (uint32_t)R * 64;           // S x 512 exponent words
+  L.q = L.a + (uint32_t)S * kStageA;           // 4 x R x 64, swizzled queries
+  L.e = L.q + (uint32_t)kQBufs * R * 64;       // S x 512 exponent words
   L.w = L.e + (uint32_t)S * kStageE;           // 16 epilogue warps x R weights
   L.x = L.w + (uint32_t)kEpiWarps * R * 4;     // partial sums: 2 groups x 2 x next_n x 128
-  L.bars = L.x + 2u * 2u * kMaxNext * kTile * 4u;  // 2S + 4 mbarriers
-  L.ok = L.bars + 8u * (uint32_t)(2 * S + kExtraBars);  // S page masks
-  L.misc = L.ok + 4u * (uint32_t)S;            // tmem base, abort, b/t/n start
+  L.sf = L.x + 2u * 2u * kMaxNext * kTile * 4u;  // scale-word copy sources
+  L.bars = L.sf + (uint32_t)(kAccs + kQBufs) * 512u;  // 2S + extra mbarriers
+  L.ok = L.bars + 8u * (uint32_t)(2 * S + kExtraBars);
+  L.misc = L.ok;                               // tmem base, abort, b/t/n start
   L.scan = L.misc + 32;                        // kThreads + 1 partial sums (int64)
   L.total = L.scan + 8u * (kThreads + 1);
   return L;
@@ -224,6 +227,24 @@ __device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64
       "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
+}
+
+// Shared-memory descriptor of a tcgen05.cp source without swizzle: rows of
+// 16 bytes, 8-row core matrices 128 bytes apart.
+__device__ __forceinline__ uint64_t cp_desc(uint32_t addr) {
+  uint64_t d = (uint64_t)((addr >> 4) & 0x3FFFu);
+  d |= (uint64_t)(128 >> 4) << 16;         // leading byte offset
+  d |= (uint64_t)(128 >> 4) << 32;         // stride byte offset: 8 rows
+  d |= (uint64_t)1 << 46;                  // descriptor version
+  return d;                                // no swizzle
+}
+
+// 32 rows x 128 bits from shared memory into TMEM columns taddr .. taddr+3
+// of every lane quadrant (row l -> lane 32q + l): the scale-word layout the
+// block-scaled MMA reads (row r's word at lane r, column r / 32).
+__device__ __forceinline__ void cp_32x128b_x4(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc)
+               : "memory");
 }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -336,7 +357,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* const sE = smem + L.e;
   float* const sW = reinterpret_cast<float*>(smem + L.w);
   const uint32_t bars = smem_addr(smem + L.bars);
-  volatile uint32_t* const stage_ok = reinterpret_cast<volatile uint32_t*>(smem + L.ok);
   uint32_t* const misc = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile uint32_t* const abort = misc + 1;
   int32_t* const start = reinterpret_cast<int32_t*>(misc + 2);  // b, t, n
@@ -386,11 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int b0 = start[0], t0 = start[1];
     if (tid == 0) {
       for (int i = 0; i < 2 * S + kExtraBars; ++i) {
-        // sfa_ready and acc_empty take one arrival per epilogue warp of a group
-        const int cnt = ((i >= bar_sfa(S, 0) && i < bar_sfa(S, 2)) ||
-                         (i >= bar_acce(S, 0) && i < bar_acce(S, kAccs)))
-                            ? kGroupWarps
-                            : 1;
+        // acc_empty takes one arrival per epilogue warp of a group
+        const int cnt = (i >= bar_acce(S, 0) && i < bar_acce(S, kAccs)) ? kGroupWarps : 1;
         asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar(i)), "r"(cnt)
                      : "memory");
       }
@@ -411,38 +428,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     // group e at 2R + 8e; query scale words of segment g at 2R + 16 + 8(g%2).
     // TMEM columns: accumulator a at aR (a < 3); the keys' scale words of
     // accumulator a's tile at 3R + 8a; the query scale words of segment g at
-    // 3R + 24 + 8(g%2).
+    // 3R + 24 + 8(g%4).
     const uint32_t sfa_col0 = (uint32_t)kAccs * R, sfb_col0 = (uint32_t)kAccs * R + 24u;
+    uint8_t* const sSF = smem + L.sf;  // copy sources: 3 key + 4 query, 512 B each
     int issued = 0;  // producer: tiles whose copies were issued
 
-    if (warp == kProducerWarp) {
-      // The page ids of 16 tiles are fetched by the whole warp in one load
-      // (lane L: tile L/2, page L%2), a batch ahead of the tiles issued.
-      Walker fetch_wk;
-      fetch_wk.init(p, b0, t0);
-      auto fetch = [&](int k0, int32_t& id, bool& inctx) {
+    if (warp >= kProducerWarp && warp < kMmaWarp) {
+      // Producer pi issues the tiles k = pi, pi + kProducers, ... and so owns
+      // the stages s = k % S (S is a multiple of kProducers).  A warp waits a
+      // few hundred cycles for each copy it issues, so the copies are spread
+      // over several warps.  The page ids of 16 of its tiles are fetched by
+      // the whole warp in one load (lane L: own tile L/2, page L%2), a batch
+      // ahead of the tiles issued.
+      const int pi = warp - kProducerWarp;
+      const int n_own = n > pi ? (n - pi + kProducers - 1) / kProducers : 0;
+      Walker fw;  // at tile fk
+      fw.init(p, b0, t0);
+      int fk = 0;
+      auto fetch = [&](int m0, int32_t& id, bool& inctx) {
         const int mine = lane >> 1;
-        int cb = fetch_wk.b, ct = fetch_wk.t, cctx = fetch_wk.ctx;
-        for (int i = 0; i < 16 && k0 + i < n; ++i) {
-          if (i == mine) {
-            cb = fetch_wk.b;
-            ct = fetch_wk.t;
-            cctx = fetch_wk.ctx;
+        int cb = 0, ct = 0, cctx = 0;
+        for (int i = 0; i < 16 && m0 + i < n_own; ++i) {
+          const int k = pi + kProducers * (m0 + i);
+          while (fk < k) {
+            fw.advance(p);
+            ++fk;
           }
-          fetch_wk.advance(p);
+          if (i == mine) {
+            cb = fw.b;
+            ct = fw.t;
+            cctx = fw.ctx;
+          }
         }
         const int pidx = ct * 2 + (lane & 1);
-        inctx = k0 + mine < n && pidx * kKvBlock < cctx;
+        inctx = m0 + mine < n_own && pidx * kKvBlock < cctx;
         id = inctx ? __ldg(p.block_table + (int64_t)cb * p.bt_stride + pidx) : -1;
       };
       int32_t cur_id, nxt_id = -1;
       bool cur_in, nxt_in = false;
       fetch(0, cur_id, cur_in);
       bool stop = false;
-      for (int k0 = 0; k0 < n && !stop; k0 += 16) {
-        if (k0 + 16 < n) fetch(k0 + 16, nxt_id, nxt_in);
-        for (int i = 0; i < 16 && k0 + i < n; ++i) {
-          const int k = k0 + i, s = k % S;
+      for (int m0 = 0; m0 < n_own && !stop; m0 += 16) {
+        if (m0 + 16 < n_own) fetch(m0 + 16, nxt_id, nxt_in);
+        for (int i = 0; i < 16 && m0 + i < n_own; ++i) {
+          const int k = pi + kProducers * (m0 + i), s = k % S;
           int32_t page[2];
           bool in[2];
 #pragma unroll
@@ -454,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) {
             ok = wait_phase(bar(bar_empty(S, s)), ((uint32_t)(k / S) & 1u) ^ 1u, abort);
             if (ok) {
-              uint32_t okmask = 0, bytes = 0;
+              uint32_t bytes = 0;
 #pragma unroll
               for (int half = 0; half < 2; ++half) {
                 if (!in[half]) {
@@ -463,13 +492,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                   flag_error(p.err, FP4IDX_ERRFLAG_PAGE);
                   page[half] = -1;
                 } else {
-                  okmask |= 1u << half;
                   bytes += kPayloadBytes + kExpBytes;
                 }
               }
-              stage_ok[s] = okmask;
               const uint32_t fb = bar(bar_full(s));
-              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
               asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb),
                            "r"(bytes)
                            : "memory");
@@ -501,8 +527,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         cur_in = nxt_in;
       }
     } else if (warp == kMmaWarp) {
-      // The whole warp waits (a warp-uniform loop wakes promptly); lane 0
-      // issues the MMAs and commits.
+      // The whole warp waits (a warp-uniform loop wakes promptly) and stages
+      // the scale words; lane 0 issues the copies into TMEM, the MMAs and the
+      // commits, in that order in the tensor pipe.
       Walker wk;
       wk.init(p, b0, t0);
       const uint32_t id0 = mxf4_idesc(R, 0), id1 = mxf4_idesc(R, 2);
@@ -510,19 +537,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t a_desc0 = sw64_desc(smem_addr(sA)), q_desc0 = sw64_desc(smem_addr(sQ));
       int done = 0;
       for (int k = 0; k < n; ++k) {
-        const int s = k % S, e = k & 1, a = k % kAccs;
-        bool ok = wait_phase(bar(bar_sfa(S, e)), (uint32_t)(k >> 1) & 1u, abort) &&
-                  wait_phase(bar(bar_full(s)), (uint32_t)(k / S) & 1u, abort) &&
+        const int s = k % S, a = k % kAccs, gq = wk.g % kQBufs;
+        // Tile k's data, and accumulator a free again: tile k-3 read out,
+        // which also means every MMA up to tile k-3 -- and the copies and
+        // operands those MMAs used -- is complete.
+        bool ok = wait_phase(bar(bar_full(s)), (uint32_t)(k / S) & 1u, abort) &&
                   (k < kAccs ||
                    wait_phase(bar(bar_acce(S, a)), (uint32_t)(k / kAccs - 1) & 1u, abort));
         if (!__all_sync(0xffffffffu, ok)) break;
+        const bool seg_start = k == 0 || wk.t == 0;
+        if (seg_start) {
+          // The segment's query operand and query scale words.  Buffer gq was
+          // last used by segment g-4, whose tiles all precede tile k-3.
+          const int64_t row0 = ((int64_t)wk.b * p.next_n) * p.H;  // first query row of b
+          uint8_t* dst = sQ + gq * R * 64;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = lane + 32 * i;
+            if (r < R) {
+              const uint4* src = reinterpret_cast<const uint4*>(p.q_fp4 + (row0 + r) * 64);
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                *reinterpret_cast<uint4*>(dst + sw64_chunk(r, c)) = __ldg(src + c);
+            }
+          }
+          uint32_t v[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int r = 32 * j + lane;
+            v[j] = r < R ? __ldg(reinterpret_cast<const uint32_t*>(p.q_scale) + row0 + r)
+                         : 0x7F7F7F7Fu;
+          }
+          *reinterpret_cast<uint4*>(sSF + (kAccs + gq) * 512 + 16 * lane) =
+              make_uint4(v[0], v[1], v[2], v[3]);
+        }
+        {  // the keys' exponent words, token 32c + l at row l, column c
+          const uint32_t* ew = reinterpret_cast<const uint32_t*>(sE + s * kStageE);
+          *reinterpret_cast<uint4*>(sSF + a * 512 + 16 * lane) =
+              make_uint4(ew[lane], ew[lane + 32], ew[lane + 64], ew[lane + 96]);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         if (lane == 0) {
-          const uint64_t adesc = a_desc0 + (uint64_t)(s * (kStageA >> 4));
-          const uint64_t qdesc = q_desc0 + (uint64_t)((wk.g & 1) * R * (64 >> 4));
-          const uint32_t d = tmem + (uint32_t)a * (uint32_t)R;
           const uint32_t sfa = tmem + sfa_col0 + 8u * (uint32_t)a;
-          const uint32_t sfb = tmem + sfb_col0 + 8u * (uint32_t)(wk.g & 1);
+          const uint32_t sfb = tmem + sfb_col0 + 8u * (uint32_t)gq;
+          cp_32x128b_x4(sfa, cp_desc(smem_addr(sSF + a * 512)));
+          if (seg_start) cp_32x128b_x4(sfb, cp_desc(smem_addr(sSF + (kAccs + gq) * 512)));
+          const uint64_t adesc = a_desc0 + (uint64_t)(s * (kStageA >> 4));
+          const uint64_t qdesc = q_desc0 + (uint64_t)(gq * R * (64 >> 4));
+          const uint32_t d = tmem + (uint32_t)a * (uint32_t)R;
           mma_mxf4(d, adesc, qdesc, id0, sfa, sfb, 0u);
           mma_mxf4(d, adesc + 2, qdesc + 2, id1, sfa, sfb, 1u);
           mma_commit(bar(bar_accf(S, k % 6)));
@@ -539,9 +603,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Warps q and q+4 of a group share TMEM lane quadrant q (tokens
       // 32q .. 32q+31) and split the accumulator's 32-column chunks: the
       // lower half takes chunks [0, kC1), the upper half [kC1, NCHUNK).  Per
-      // tile a warp first prepares the group's next tile, then reads and
-      // reduces its chunks, releases the accumulator (acc_empty) and stores
-      // the logits.
+      // tile a warp reads and reduces its chunks, releases the accumulator
+      // (acc_empty) and stores the logits.
       constexpr int kC1 = (NCHUNK + 1) / 2;
       const int e = warp / kGroupWarps, gw = warp % kGroupWarps;
       const int quad = gw & 3, half = gw >> 2;
@@ -555,56 +618,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool split = kC1 < NCHUNK && kC1 % cpj != 0;
       const int js = kC1 / cpj;
 
-      // Prepare tile k (walker w): wait for its stage; the lower half writes
-      // the keys' scale words and, at the first tile of a segment, the
-      // segment's query operand and query scale words; every warp arrives on
-      // sfa_ready[e].
-      auto prepare = [&](int k, const Walker& w, uint32_t& okmask) -> bool {
-        const int s = k % S;
-        const bool ok = wait_phase(bar(bar_full(s)), (uint32_t)(k / S) & 1u, abort);
-        if (!__all_sync(0xffffffffu, ok)) return false;
-        okmask = stage_ok[s];
-        if (half == 0) {
-          if (k == 0 || w.t == 0) {  // first tile of a segment: its query operand
-            const int64_t row0 = ((int64_t)w.b * p.next_n) * p.H;  // first query row of b
-            const int gb = w.g & 1;
-            if (row < R) {
-              const uint4* src = reinterpret_cast<const uint4*>(p.q_fp4 + (row0 + row) * 64);
-              uint8_t* dst = sQ + gb * R * 64;
-#pragma unroll
-              for (int c = 0; c < 4; ++c)
-                *reinterpret_cast<uint4*>(dst + sw64_chunk(row, c)) = __ldg(src + c);
-            }
-            uint32_t v[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int r = 32 * j + lane;
-              v[j] = r < R ? __ldg(reinterpret_cast<const uint32_t*>(p.q_scale) + row0 + r)
-                           : 0x7F7F7F7Fu;
-            }
-            asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                             tmem + lane_base + sfb_col0 + 8u * (uint32_t)gb),
-                         "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
-                         : "memory");
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          }
-          const uint32_t word = reinterpret_cast<const uint32_t*>(sE + s * kStageE)[row];
-          asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(
-                           tmem + lane_base + sfa_col0 + 8u * (uint32_t)(k % kAccs) +
-                           (uint32_t)quad),
-                       "r"(word)
-                       : "memory");
-          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-        }
-        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(bar_sfa(S, e)));
-        return true;
+      // The validity of this warp's page of tile (w.b, w.t) -- the same rule
+      // the producer applies: inside the context and a page id in range.
+      auto page_id = [&](const Walker& w) -> int32_t {
+        const int pidx = w.t * 2 + (quad >> 1);
+        return pidx * kKvBlock < w.ctx
+                   ? __ldg(p.block_table + (int64_t)w.b * p.bt_stride + pidx)
+                   : -1;
       };
 
       // Tile k, chunks [C0, C1) of accumulator k % 3: load and reduce chunk
       // by chunk, release the accumulator, store (or hand off) the logits.
-      auto tile = [&](auto acc, int k, const Walker& w, uint32_t okmask, bool& live) {
+      auto tile = [&](auto acc, int k, const Walker& w, bool page_ok, bool& live) {
         constexpr int C0 = decltype(acc)::kC0, C1 = decltype(acc)::kC1;
         const int a = k % kAccs;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -614,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(bar_acce(S, a)));
         const int s_tok = w.t * kTile + row;
-        const bool valid = s_tok < w.ctx && ((okmask >> (row >> 6)) & 1u);
+        const bool valid = s_tok < w.ctx && page_ok;
         float* const xb = xch + ((k >> 1) & 1) * kMaxNext * kTile;
         const uint32_t xbar = bar(bar_xch(S, e, quad, (k >> 1) & 1));
         float* const out = p.logits + ((int64_t)w.b * p.next_n) * p.logits_stride + s_tok;
@@ -654,28 +679,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       Walker nw = wk;
       nw.advance(p);
       nw.advance(p);
-      uint32_t okm = 0, okm_next = 0;
-      bool live = e < n && prepare(e, wk, okm);
+      int32_t pid = e < n ? page_id(wk) : -1, pid_next = -1;
+      bool live = true;
       int wg = -1;  // segment of the weights held
       for (int k = e; k < n && live; k += 2) {
+        if (k + 2 < n) pid_next = page_id(nw);  // a tile ahead
         if (!__all_sync(0xffffffffu,
                         wait_phase(bar(bar_accf(S, k % 6)), (uint32_t)(k / 6) & 1u, abort)))
           break;
-        // The next tile of this group first: its scale words go to the slot
-        // of accumulator (k+2) % 3, whose last MMAs (tile k-1) are complete
-        // because tile k's are.
-        if (k + 2 < n) live = prepare(k + 2, nw, okm_next);
         if (wk.g != wg) {  // this warp's copy of the segment's head weights
           const int64_t row0 = ((int64_t)wk.b * p.next_n) * p.H;
           for (int i = lane; i < R; i += 32) wts[i] = __ldg(p.weights + row0 + i);
           __syncwarp();
           wg = wk.g;
         }
+        const bool page_ok = pid >= 0 && pid < p.num_blocks;
         if (half == 0)
-          tile(HalfAccT<0, kC1>(), k, wk, okm, live);
+          tile(HalfAccT<0, kC1>(), k, wk, page_ok, live);
         else
-          tile(HalfAccT<kC1, NCHUNK>(), k, wk, okm, live);
-        okm = okm_next;
+          tile(HalfAccT<kC1, NCHUNK>(), k, wk, page_ok, live);
+        pid = pid_next;
         wk = nw;
         nw.advance(p);
         nw.advance(p);
@@ -685,8 +708,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     if (*abort) {  // every role has stopped: let copies in flight land first
-      if (warp == kProducerWarp && lane == 0)
-        for (int q = max(0, issued - S); q < issued; ++q)
+      if (warp >= kProducerWarp && warp < kMmaWarp && lane == 0)  // its own stages
+        for (int q = issued - 1; q >= 0 && q >= issued - S; q -= kProducers)
           wait_phase_drain(bar(bar_full(q % S)), (uint32_t)(q / S) & 1u);
       if (tid == 0) flag_error(p.err, FP4IDX_ERRFLAG_TIMEOUT);
       __syncthreads();
@@ -811,11 +834,12 @@ extern "C" fp4idx_status fp4idx_paged_mqa_logits(
   p.max_context = (int32_t)max_context;
   p.tiles_total = (int32_t)((max_context + kTile - 1) / kTile);
   uint32_t cols = 32;
-  while (cols < (uint32_t)kAccs * (uint32_t)p.R + 40u) cols <<= 1;
+  while (cols < (uint32_t)kAccs * (uint32_t)p.R + 24u + 8u * kQBufs) cols <<= 1;
   p.tmem_cols = cols;
   // As many stages as fit in one CTA's shared memory (one CTA per SM).
-  int S = kMaxStages;
-  while (S > 2 && (int)make_layout(S, p.R).total + 1024 > di.smem_optin) --S;
+  int S = kMaxStages - kMaxStages % kProducers;  // a multiple of the producer count
+  while (S > kProducers && (int)make_layout(S, p.R).total + 1024 > di.smem_optin)
+    S -= kProducers;
   if ((int)make_layout(S, p.R).total + 1024 > di.smem_optin) return FP4IDX_ERR_SHAPE;
   p.stages = S;
   const int smem_bytes = (int)make_layout(S, p.R).total + 1024;
