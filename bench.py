@@ -316,10 +316,13 @@ def time_device(F, w, D, mode, steps, warmup, flush, dist=None, sampler=None):
 
 
 def time_e2e(F, w, D, mode, steps):
-    """Through the public API with host buffers: per step, copy the step's
-    inputs (q, w, k, positions, slot mapping) from pinned host memory, run
-    the pre-pass, and copy the query outputs back.  The cos/sin tables, gamma
-    and the paged cache stay resident on the device."""
+    """Through the public API with host buffers: per step, the step's inputs
+    (q, w, k, positions, slot mapping) come from pinned host memory and the
+    query outputs go back to pinned host memory.  Fused mode uses
+    indexer_prepass_host (chunked, uploads / launches / downloads
+    overlapped); separate mode copies, runs the two calls and copies back.
+    The cos/sin tables, gamma and the paged cache stay resident on the
+    device."""
     import torch
     dev = D["q"].device
     names = ("q", "w", "k", "pos", "slots")
@@ -335,6 +338,12 @@ def time_e2e(F, w, D, mode, steps):
     d2h = sum(o.numel() * o.element_size() for o in outs)
 
     def one():
+        if mode == "fused":
+            F.indexer_prepass_host(host["k"], D["gamma"], host["slots"], D["cache"], host["q"],
+                                   host["w"], host["pos"], D["cos"], D["sin"], eps=w.eps,
+                                   rope_style=w.rope_style, q_fp4=hout[0], q_scale=hout[1],
+                                   weights=hout[2])
+            return
         for n in names:
             D[n].copy_(host[n], non_blocking=True)
         step()

@@ -309,6 +309,127 @@ def indexer_prepass(k, gamma, slot_mapping, kv_cache, q, w, positions, cos_cache
     return q_fp4, q_scale, weights
 
 
+# ------------------------------------------------------- host-buffer pipeline
+class _HostPipe:
+    """Device staging for two chunks, three streams and their events."""
+
+    def __init__(self, device, chunk: int, H: int):
+        torch = _torch()
+        self.s_in, self.s_run, self.s_out = (torch.cuda.Stream(device) for _ in range(3))
+
+        def two(shape, dt):
+            return [torch.empty(shape, dtype=dt, device=device) for _ in range(2)]
+
+        self.q = two((chunk, H, HEAD_DIM), torch.bfloat16)
+        self.k = two((chunk, HEAD_DIM), torch.bfloat16)
+        self.w = two((chunk, H), torch.bfloat16)
+        self.pos = two((chunk,), torch.int64)
+        self.slots = two((chunk,), torch.int64)
+        self.qf = two((chunk, H, 64), torch.uint8)
+        self.qs = two((chunk, H, 4), torch.uint8)
+        self.wt = two((chunk, H), torch.float32)
+        self.ev_in = [torch.cuda.Event() for _ in range(2)]
+        self.ev_run = [torch.cuda.Event() for _ in range(2)]
+        self.ev_out = [torch.cuda.Event() for _ in range(2)]
+
+
+_HOST_PIPES = {}
+
+
+def _need_host(t, dtype, name, ndim):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-D tensor")
+    return t
+
+
+def indexer_prepass_host(k, gamma, slot_mapping, kv_cache, q, w, positions, cos_cache,
+                         sin_cache, *, eps: float = 1e-6, rope_style="neox", weight_scale=None,
+                         q_fp4=None, q_scale=None, weights=None, chunk_tokens: int = 4096,
+                         err_flags=None, stream=None):
+    """indexer_prepass for inputs and outputs in host memory: k [T,128], q
+    [T,H,128], w [T,H] (bf16), positions and slot_mapping [T] (int64) are
+    contiguous host tensors, pinned for the copies to overlap; gamma, the
+    cos/sin caches and kv_cache are device tensors.  The tokens go through in
+    chunks of chunk_tokens on three streams, so that the upload of chunk c+1,
+    the fused pre-pass of chunk c (one C-ABI launch) and the download of
+    chunk c-1 overlap.  Returns host tensors (q_fp4, q_scale, weights),
+    allocated pinned when not given; they are complete once the caller's
+    stream (which waits for the pipeline) has reached this point."""
+    torch = _torch()
+    _need_host(k, torch.bfloat16, "k", 2)
+    _need_host(q, torch.bfloat16, "q", 3)
+    _need_host(w, torch.bfloat16, "w", 2)
+    _need_host(positions, torch.int64, "positions", 1)
+    _need_host(slot_mapping, torch.int64, "slot_mapping", 1)
+    _need(kv_cache, torch.uint8, "kv_cache", 2)
+    T, H, D = q.shape
+    if D != HEAD_DIM or tuple(k.shape) != (T, HEAD_DIM) or tuple(w.shape) != (T, H):
+        raise ValueError("k must be [T,128], q [T,H,128], w [T,H]")
+    if positions.shape[0] != T or slot_mapping.shape[0] != T:
+        raise ValueError("positions and slot_mapping must have T entries")
+    if chunk_tokens < 1:
+        raise ValueError("chunk_tokens must be >= 1")
+    outs = []
+    for t, shape, dt, name in ((q_fp4, (T, H, 64), torch.uint8, "q_fp4"),
+                               (q_scale, (T, H, 4), torch.uint8, "q_scale"),
+                               (weights, (T, H), torch.float32, "weights")):
+        if t is None:
+            t = torch.empty(shape, dtype=dt).pin_memory()
+        _need_host(t, dt, name, len(shape))
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{name} must be {shape}")
+        outs.append(t)
+    q_fp4, q_scale, weights = outs
+    dev = kv_cache.device
+    chunk = min(int(chunk_tokens), max(T, 1))
+    key = (dev.index, chunk, H)
+    pipe = _HOST_PIPES.get(key)
+    if pipe is None:
+        pipe = _HOST_PIPES[key] = _HostPipe(dev, chunk, H)
+    caller = stream if stream is not None else torch.cuda.current_stream(dev)
+    # everything already queued on the caller's stream comes first
+    for s in (pipe.s_in, pipe.s_run, pipe.s_out):
+        s.wait_stream(caller)
+    for c in range((T + chunk - 1) // chunk):
+        b, t0 = c & 1, c * chunk
+        t1 = min(T, t0 + chunk)
+        n = t1 - t0
+        if c >= 2:  # slot b's inputs are free once chunk c-2 has run
+            pipe.s_in.wait_event(pipe.ev_run[b])
+        with torch.cuda.stream(pipe.s_in):
+            pipe.q[b][:n].copy_(q[t0:t1], non_blocking=True)
+            pipe.k[b][:n].copy_(k[t0:t1], non_blocking=True)
+            pipe.w[b][:n].copy_(w[t0:t1], non_blocking=True)
+            pipe.pos[b][:n].copy_(positions[t0:t1], non_blocking=True)
+            pipe.slots[b][:n].copy_(slot_mapping[t0:t1], non_blocking=True)
+            pipe.ev_in[b].record(pipe.s_in)
+        pipe.s_run.wait_event(pipe.ev_in[b])
+        if c >= 2:  # slot b's outputs are free once chunk c-2 is downloaded
+            pipe.s_run.wait_event(pipe.ev_out[b])
+        indexer_prepass(pipe.k[b][:n], gamma, pipe.slots[b][:n], kv_cache, pipe.q[b][:n],
+                        pipe.w[b][:n], pipe.pos[b][:n], cos_cache, sin_cache, eps=eps,
+                        rope_style=rope_style, weight_scale=weight_scale, q_fp4=pipe.qf[b][:n],
+                        q_scale=pipe.qs[b][:n], weights=pipe.wt[b][:n], err_flags=err_flags,
+                        stream=pipe.s_run)
+        pipe.ev_run[b].record(pipe.s_run)
+        pipe.s_out.wait_event(pipe.ev_run[b])
+        with torch.cuda.stream(pipe.s_out):
+            q_fp4[t0:t1].copy_(pipe.qf[b][:n], non_blocking=True)
+            q_scale[t0:t1].copy_(pipe.qs[b][:n], non_blocking=True)
+            weights[t0:t1].copy_(pipe.wt[b][:n], non_blocking=True)
+            pipe.ev_out[b].record(pipe.s_out)
+    caller.wait_stream(pipe.s_run)
+    caller.wait_stream(pipe.s_out)
+    return q_fp4, q_scale, weights
+
+
 def paged_mqa_logits(q_fp4, q_scale, weights, kv_cache, block_table, context_lens,
                      max_context: int, *, next_n: int = 1, logits=None, err_flags=None,
                      stream=None):
