@@ -913,8 +913,8 @@ void launch_one(unsigned grid, cudaStream_t s, const KArgs& ka, const QArgs& qa,
 
 fp4idx_status launch(const KArgs& ka, const QArgs& qa, const Shared& sh, bool keys, bool queries,
                      int rope_style, int rotate, int fp8, void* stream) {
-  if (stream_eligible(queries, qa.H, rotate, fp8))
-    return launch_stream(ka, qa, sh, keys, queries, rope_style, stream);
+  if (stream_eligible(queries, qa.H, fp8))
+    return launch_stream(ka, qa, sh, keys, queries, rope_style, rotate, stream);
   // 32-bit indices: T * H and T itself below 2^30.
   const int64_t H = queries ? qa.H : 1;
   if (sh.T >= (1 << 30) || H >= (1 << 30) || sh.T * H >= (1 << 30)) return FP4IDX_ERR_SHAPE;

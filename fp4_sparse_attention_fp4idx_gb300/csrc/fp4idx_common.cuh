@@ -274,9 +274,9 @@ inline FastDiv make_fastdiv(uint32_t d) {
 }  // namespace fp4idx_impl
 
 namespace fp4idx_impl {
-// The streaming kernel (fp4idx_stream.cu): FP4 output, no rotation, and
-// for queries a head count that is a multiple of 16.
-bool stream_eligible(bool queries, int64_t H, int rotate, int fp8);
+// The streaming kernel (fp4idx_stream.cu): FP4 output, with or without the
+// rotation, and for queries a head count that is a multiple of 16.
+bool stream_eligible(bool queries, int64_t H, int fp8);
 fp4idx_status launch_stream(const KArgs& ka, const QArgs& qa, const Shared& sh, bool keys,
-                            bool queries, int rope_style, void* stream);
+                            bool queries, int rope_style, int rotate, void* stream);
 }  // namespace fp4idx_impl

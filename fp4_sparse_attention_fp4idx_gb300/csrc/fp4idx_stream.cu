@@ -284,6 +284,137 @@ __device__ __forceinline__ void rope4(uint32_t (&a)[4], uint32_t (&b)[4], const 
   }
 }
 
+__device__ __forceinline__ void unpack8(const uint32_t (&x)[4], float (&v)[8]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    v[2 * k] = bf16_lo(x[k]);
+    v[2 * k + 1] = bf16_hi(x[k]);
+  }
+}
+
+// x = bf16(rn(v * rn32(1/sqrt(128)))), the rotation's normalisation; the
+// products packed over the element pairs (i, i + PS).
+template <int PS>
+__device__ __forceinline__ void scale_pack8(const float (&v)[8], uint32_t (&x)[4]) {
+  const float norm = 0.08838834764831845f;
+  float y[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if (!(i & PS)) mul2(y[i], y[i + PS], v[i], v[i + PS], norm, norm);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) x[k] = pack_bf16x2(y[2 * k], y[2 * k + 1]);
+}
+
+// (r0, r1) = (rn(a0*s + c0), rn(a1*s + c1)) for s = +-1: exactly rn(c +- a).
+__device__ __forceinline__ void pm2(float& r0, float& r1, float a0, float a1, float s, float c0,
+                                    float c1) {
+  asm("{\n\t.reg .b64 ra, rs, rc, rr;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rs, {%4, %4};\n\t"
+      "mov.b64 rc, {%5, %6};\n\t"
+      "fma.rn.f32x2 rr, ra, rs, rc;\n\t"
+      "mov.b64 {%0, %1}, rr;\n\t}"
+      : "=f"(r0), "=f"(r1)
+      : "f"(a0), "f"(a1), "f"(s), "f"(c0), "f"(c1));
+}
+
+// The rotation's packed fp32 operations pair elements (i, i + kPairStride)
+// of a part in every stage, so that each pair stays in one aligned register
+// pair throughout; the stage h == kPairStride runs on scalars.  (Pairing
+// differently in one stage costs register moves: 9% of the rotated
+// pre-pass's time.)
+constexpr int kPairStride = 1;
+
+// In-lane butterfly stage h of one 8-element part; packed over the element
+// pairs (i, i + PS), scalar for h == PS.
+template <int PS>
+__device__ __forceinline__ void part_stage(float (&v)[8], int h) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (i & h) continue;
+    if (h == PS) {
+      const float a = v[i], b = v[i + h];
+      v[i] = __fadd_rn(a, b);
+      v[i + h] = __fsub_rn(a, b);
+    } else if (!(i & PS)) {
+      float s0, s1, d0, d1;
+      sum2(s0, s1, v[i], v[i + PS], v[i + h], v[i + h + PS]);
+      diff2(d0, d1, v[i], v[i + PS], v[i + h], v[i + h + PS]);
+      v[i] = s0;
+      v[i + PS] = s1;
+      v[i + h] = d0;
+      v[i + h + PS] = d1;
+    }
+  }
+}
+
+// Normalised 128-point Walsh-Hadamard rotation of a row held by 4 lanes
+// (register p = part p ^ par, part q = dims 32q + 8j .. 32q + 8j + 7).  The
+// butterfly stages run in the order h = 1, 2, ..., 64, each pair (lower,
+// upper) becoming (rn(lower + upper), rn(lower - upper)): h = 1, 2, 4 inside
+// a part, h = 8 and 16 with lanes j^1 and j^2 (a lane computes rn(partner
+// +- own) as one exact-product fma), h = 32 between registers 0/1 and 2/3
+// (the part swap of odd rows folded into the sign), h = 64 between
+// registers 0/2 and 1/3.  Then one product with rn32(1/sqrt(128)) and the
+// bf16 rounding.  All 32 lanes call (shuffles).
+__device__ __forceinline__ void rotate4(uint32_t (&x0)[4], uint32_t (&x1)[4], uint32_t (&x2)[4],
+                                        uint32_t (&x3)[4], int j, bool par) {
+  constexpr int PS = kPairStride;
+  float v[4][8];
+  unpack8(x0, v[0]);
+  unpack8(x1, v[1]);
+  unpack8(x2, v[2]);
+  unpack8(x3, v[3]);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    part_stage<PS>(v[q], 1);
+    part_stage<PS>(v[q], 2);
+    part_stage<PS>(v[q], 4);
+  }
+#pragma unroll
+  for (int m = 1; m <= 2; m *= 2) {  // h = 8, 16: lower lane own + other, upper other - own
+    const float sg = (j & m) ? -1.0f : 1.0f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (i & PS) continue;
+        const float o0 = __shfl_xor_sync(kFull, v[q][i], m);
+        const float o1 = __shfl_xor_sync(kFull, v[q][i + PS], m);
+        pm2(v[q][i], v[q][i + PS], v[q][i], v[q][i + PS], sg, o0, o1);
+      }
+  }
+  {  // h = 32: register 0 is the lower part for even rows, the upper for odd
+    const float sg = par ? -1.0f : 1.0f;
+#pragma unroll
+    for (int q = 0; q < 4; q += 2)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (i & PS) continue;
+        const float a0 = v[q][i], a1 = v[q][i + PS], b0 = v[q + 1][i], b1 = v[q + 1][i + PS];
+        pm2(v[q][i], v[q][i + PS], a0, a1, sg, b0, b1);           // rn(b +- a)
+        pm2(v[q + 1][i], v[q + 1][i + PS], b0, b1, -sg, a0, a1);  // rn(a -+ b)
+      }
+  }
+#pragma unroll
+  for (int q = 0; q < 2; ++q)  // h = 64: registers 0/1 lower, 2/3 upper
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (i & PS) continue;
+      float s0, s1, d0, d1;
+      sum2(s0, s1, v[q][i], v[q][i + PS], v[q + 2][i], v[q + 2][i + PS]);
+      diff2(d0, d1, v[q][i], v[q][i + PS], v[q + 2][i], v[q + 2][i + PS]);
+      v[q][i] = s0;
+      v[q][i + PS] = s1;
+      v[q + 2][i] = d0;
+      v[q + 2][i + PS] = d1;
+    }
+  scale_pack8<PS>(v[0], x0);
+  scale_pack8<PS>(v[1], x1);
+  scale_pack8<PS>(v[2], x2);
+  scale_pack8<PS>(v[3], x3);
+}
+
 // Lane-local max(|x|) of two 8-element parts, packed: low half = part x,
 // high half = part y (bf16 bits; the sign bits are garbage).
 __device__ __forceinline__ uint32_t pair_amax(const uint32_t (&x)[4], const uint32_t (&y)[4]) {
@@ -408,7 +539,7 @@ struct Lanes {
 
 // --------------------------------------------------------- consumer side
 // Rows 16*sl .. of a query unit (first flattened row row0, n rows).
-template <int kStyle>
+template <int kStyle, bool kRotate>
 __device__ __forceinline__ void query_slice(uint32_t stage, int32_t row0, int n, uint32_t flags,
                                             int sl, const SWork& wk, const QArgs& qa,
                                             const Shared& sh) {
@@ -440,6 +571,7 @@ __device__ __forceinline__ void query_slice(uint32_t stage, int32_t row0, int n,
     uint32_t x0[4], x1[4], x2[4], x3[4];
     ln.load(stage + (uint32_t)(r_first + r) * kRowBytes, x0, x1, x2, x3);
     rope4<kStyle>(x0, x1, cf, sh.neg_zero);
+    if constexpr (kRotate) rotate4(x0, x1, x2, x3, ln.j, ln.par);
     uint32_t code[4], ew;
     quant4(x0, x1, x2, x3, ln.par, code, ew);
     if (r < ns) {
@@ -453,7 +585,7 @@ __device__ __forceinline__ void query_slice(uint32_t stage, int32_t row0, int n,
 }
 
 // Rows 16*sl .. of a key unit (tokens t0 .. t0 + n - 1).
-template <int kStyle>
+template <int kStyle, bool kRotate>
 __device__ __forceinline__ void key_slice(uint32_t stage, int32_t t0, int n, uint32_t flags,
                                           int sl, const KArgs& ka, const Shared& sh) {
   const Lanes ln;
@@ -508,6 +640,7 @@ __device__ __forceinline__ void key_slice(uint32_t stage, int32_t t0, int n, uin
     norm8(x2, rr, __ldg(g + 4 * (2 ^ pa) + ln.j));
     norm8(x3, rr, __ldg(g + 4 * (3 ^ pa) + ln.j));
     rope4<kStyle>(x0, x1, cf, sh.neg_zero);
+    if constexpr (kRotate) rotate4(x0, x1, x2, x3, ln.j, ln.par);
     uint32_t code[4], ew;
     quant4(x0, x1, x2, x3, ln.par, code, ew);
     if (live) {
@@ -641,7 +774,7 @@ __device__ __forceinline__ void issue_meta(int i, int kb, const Units& u, const 
 }
 
 // ------------------------------------------------------------------ kernel
-template <int kStyle>
+template <int kStyle, bool kRotate>
 __global__ void __launch_bounds__(kThreadsS, 1)
     stream_kernel(KArgs ka, QArgs qa, Shared sh, SWork wk) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -740,9 +873,9 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     uint32_t hdr[4];
     lds128(stage + kHdrOff, hdr);
     if ((hdr[0] & 3u) == kUnitKey)
-      key_slice<kStyle>(stage, (int32_t)hdr[1], (int)hdr[2], hdr[3], sl, ka, sh);
+      key_slice<kStyle, kRotate>(stage, (int32_t)hdr[1], (int)hdr[2], hdr[3], sl, ka, sh);
     else
-      query_slice<kStyle>(stage, (int32_t)hdr[1], (int)hdr[2], hdr[3], sl, wk, qa, sh);
+      query_slice<kStyle, kRotate>(stage, (int32_t)hdr[1], (int)hdr[2], hdr[3], sl, wk, qa, sh);
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8u * s);
   }
@@ -753,9 +886,9 @@ __global__ void __launch_bounds__(kThreadsS, 1)
 constexpr int kMaxDevicesS = 64;
 int g_sms[kMaxDevicesS];  // 0: not set up yet; -1: set-up failed
 
-template <int kStyle>
+template <int kStyle, bool kRotate>
 bool setup_stream() {
-  auto kern = stream_kernel<kStyle>;
+  auto kern = stream_kernel<kStyle, kRotate>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemS) !=
       cudaSuccess)
     return false;
@@ -771,7 +904,9 @@ int stream_sms() {
   if (g_sms[dev] == 0) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        !setup_stream<FP4IDX_ROPE_NEOX>() || !setup_stream<FP4IDX_ROPE_INTERLEAVED>())
+        !setup_stream<FP4IDX_ROPE_NEOX, false>() ||
+        !setup_stream<FP4IDX_ROPE_INTERLEAVED, false>() ||
+        !setup_stream<FP4IDX_ROPE_NEOX, true>() || !setup_stream<FP4IDX_ROPE_INTERLEAVED, true>())
       return 0;
     g_sms[dev] = sms;
   }
@@ -780,12 +915,12 @@ int stream_sms() {
 
 }  // namespace
 
-bool stream_eligible(bool queries, int64_t H, int rotate, int fp8) {
-  return !rotate && !fp8 && (!queries || H % kSliceRows == 0);
+bool stream_eligible(bool queries, int64_t H, int fp8) {
+  return !fp8 && (!queries || H % kSliceRows == 0);
 }
 
 fp4idx_status launch_stream(const KArgs& ka, const QArgs& qa, const Shared& sh, bool keys,
-                            bool queries, int rope_style, void* stream) {
+                            bool queries, int rope_style, int rotate, void* stream) {
   const int64_t H = queries ? qa.H : 0;
   if (sh.T >= (1 << 30) || H >= (1 << 30) || sh.T * H >= (1 << 30)) return FP4IDX_ERR_SHAPE;
   SWork wk;
@@ -808,10 +943,15 @@ fp4idx_status launch_stream(const KArgs& ka, const QArgs& qa, const Shared& sh, 
   if (sms <= 0) return FP4IDX_ERR_CUDA;
   const unsigned grid = (unsigned)(total < sms ? total : sms);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (rope_style == FP4IDX_ROPE_NEOX)
-    stream_kernel<FP4IDX_ROPE_NEOX><<<grid, kThreadsS, kSmemS, s>>>(ka, qa, sh, wk);
+  const bool neox = rope_style == FP4IDX_ROPE_NEOX;
+  if (neox && !rotate)
+    stream_kernel<FP4IDX_ROPE_NEOX, false><<<grid, kThreadsS, kSmemS, s>>>(ka, qa, sh, wk);
+  else if (!rotate)
+    stream_kernel<FP4IDX_ROPE_INTERLEAVED, false><<<grid, kThreadsS, kSmemS, s>>>(ka, qa, sh, wk);
+  else if (neox)
+    stream_kernel<FP4IDX_ROPE_NEOX, true><<<grid, kThreadsS, kSmemS, s>>>(ka, qa, sh, wk);
   else
-    stream_kernel<FP4IDX_ROPE_INTERLEAVED><<<grid, kThreadsS, kSmemS, s>>>(ka, qa, sh, wk);
+    stream_kernel<FP4IDX_ROPE_INTERLEAVED, true><<<grid, kThreadsS, kSmemS, s>>>(ka, qa, sh, wk);
   return cudaGetLastError() == cudaSuccess ? FP4IDX_OK : FP4IDX_ERR_CUDA;
 }
 

@@ -1,7 +1,7 @@
 """GPU parity of the streaming pre-pass kernel (64-row work units fed by a
-producer warp, four lanes per row): the path taken for FP4 output without
-the rotation when the head count is a multiple of 16, and for every
-key-only call.  The cases leave ragged units and slices, use every
+producer warp, four lanes per row): the path taken for FP4 output, with
+or without the 128-point rotation, when the head count is a multiple of 16,
+and for every key-only call.  The cases leave ragged units and slices, use every
 query-row layout the producer copies (contiguous rows, contiguous heads
 under a larger token stride, one copy per row), put the quantiser's edge
 rows at both row parities of a quarter-warp, and feed out-of-range
@@ -19,22 +19,25 @@ pytestmark = pytest.mark.gpu
 STYLES = [wl.ROPE_NEOX, wl.ROPE_INTERLEAVED]
 
 
+@pytest.mark.parametrize("hadamard", [False, True], ids=["plain", "rotated"])
 @pytest.mark.parametrize("style", STYLES)
 @pytest.mark.parametrize("T,H", [(1, 16), (3, 16), (5, 48), (63, 32), (64, 16), (65, 64),
                                  (130, 128), (301, 32)])
-def test_stream_ragged(T, H, style):
+def test_stream_ragged(T, H, style, hadamard):
     """Units that end mid-slice (T*H not a multiple of 64), key units that
     end mid-unit (T not a multiple of 64), one token, 128 heads."""
     w = wl.make_random(T, H, style, seed=2000 + 13 * T + H)
+    ref = run_oracle(w, hadamard=hadamard)
     for mode in ("fused", "separate"):
         d = DeviceWorkload(w)
-        assert_same(w, d.run(mode), run_oracle(w))
+        assert_same(w, d.run(mode, hadamard=hadamard), ref)
         assert int(d.err.item()) == 0
 
 
+@pytest.mark.parametrize("hadamard", [False, True], ids=["plain", "rotated"])
 @pytest.mark.parametrize("style", STYLES)
 @pytest.mark.parametrize("scale", [1.0, 40.0, 1e-3, 3e4])
-def test_stream_special_rows(style, scale):
+def test_stream_special_rows(style, scale, hadamard):
     """All-zero, subnormal and exact-midpoint query rows on even and odd rows
     of a unit (the two part orders), with the keys of the same tokens."""
     w = wl.make_random(70, 16, style, seed=int(scale * 7) + 31 * style + 5, scales=(scale,))
@@ -50,7 +53,7 @@ def test_stream_special_rows(style, scale):
         w.positions[t] = 0
     w.k[4] = wl.to_bf16_bits(wl.midpoint_key_row())
     d = DeviceWorkload(w)
-    assert_same(w, d.run("fused"), run_oracle(w))
+    assert_same(w, d.run("fused", hadamard=hadamard), run_oracle(w, hadamard=hadamard))
     assert int(d.err.item()) == 0
 
 
@@ -119,13 +122,14 @@ def test_stream_out_of_range_positions():
         assert np.all(qfn[[3, 17, 39]] == 0xA5)
 
 
-def test_stream_repeat_and_reuse():
+@pytest.mark.parametrize("hadamard", [False, True], ids=["plain", "rotated"])
+def test_stream_repeat_and_reuse(hadamard):
     """Two launches in a row on the prefill workload give the same bytes (no
     state carried between launches)."""
     w = wl.make("prefill")
     d = DeviceWorkload(w)
-    a = d.run("fused")
-    b = d.run("fused")
+    a = d.run("fused", hadamard=hadamard)
+    b = d.run("fused", hadamard=hadamard)
     for x, y in zip(a, b):
         assert np.array_equal(x, y)
     assert int(d.err.item()) == 0
