@@ -64,11 +64,11 @@ def algorithmic_bytes(w, mode: str) -> dict:
 
 
 def prepass_kernel_name(H: int, fp8: bool = False, hadamard: bool = False) -> str:
-    """The kernel an FP4 pre-pass launch runs: the streaming kernel for FP4
-    output (with or without the rotation) when the head count is a multiple
-    of 16, otherwise the per-warp kernel."""
-    del hadamard  # both forms run in the streaming kernel
-    return "stream_kernel" if H % 16 == 0 and not fp8 else "prepass_kernel"
+    """The kernel a pre-pass launch runs: the streaming kernel (every output
+    mode, with or without the rotation) when the head count is a multiple of
+    16, otherwise the per-warp kernel."""
+    del fp8, hadamard  # every form runs in the streaming kernel
+    return "stream_kernel" if H % 16 == 0 else "prepass_kernel"
 
 
 def measured_peak():

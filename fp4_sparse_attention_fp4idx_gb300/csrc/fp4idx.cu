@@ -140,19 +140,6 @@ __device__ __forceinline__ void quant_lane(const uint32_t (&a)[4], const uint32_
   ew = x | __shfl_xor_sync(kFull, x, 4);
 }
 
-// Four fp32 values -> four E4M3 codes (round half to even, saturating at
-// 448), element 0 in the low byte.
-__device__ __forceinline__ uint32_t e4m3x4(float v0, float v1, float v2, float v3) {
-  uint32_t w;
-  asm("{\n\t.reg .b16 h0, h1;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f32 h0, %2, %1;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f32 h1, %4, %3;\n\t"
-      "mov.b32 %0, {h0, h1};\n\t}"
-      : "=r"(w)
-      : "f"(v0), "f"(v1), "f"(v2), "f"(v3));
-  return w;
-}
-
 // FP8 mode for this lane's two 8-element parts of its row (a = dims
 // 8j..8j+7, b = dims 64+8j..64+8j+7).  All 32 lanes must call (shuffles).
 // The row's scale is 2^(e-127) = ceil_pow2(max(rn(amax/448), 2^-126)); the
@@ -913,8 +900,8 @@ void launch_one(unsigned grid, cudaStream_t s, const KArgs& ka, const QArgs& qa,
 
 fp4idx_status launch(const KArgs& ka, const QArgs& qa, const Shared& sh, bool keys, bool queries,
                      int rope_style, int rotate, int fp8, void* stream) {
-  if (stream_eligible(queries, qa.H, fp8))
-    return launch_stream(ka, qa, sh, keys, queries, rope_style, rotate, stream);
+  if (stream_eligible(queries, qa.H))
+    return launch_stream(ka, qa, sh, keys, queries, rope_style, rotate, fp8, stream);
   // 32-bit indices: T * H and T itself below 2^30.
   const int64_t H = queries ? qa.H : 1;
   if (sh.T >= (1 << 30) || H >= (1 << 30) || sh.T * H >= (1 << 30)) return FP4IDX_ERR_SHAPE;

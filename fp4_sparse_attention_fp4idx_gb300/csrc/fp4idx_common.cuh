@@ -190,6 +190,19 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return d;
 }
 
+// Four fp32 values -> four E4M3 codes (round half to even, saturating at
+// 448), element 0 in the low byte.
+__device__ __forceinline__ uint32_t e4m3x4(float v0, float v1, float v2, float v3) {
+  uint32_t w;
+  asm("{\n\t.reg .b16 h0, h1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 h0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 h1, %4, %3;\n\t"
+      "mov.b32 %0, {h0, h1};\n\t}"
+      : "=r"(w)
+      : "f"(v0), "f"(v1), "f"(v2), "f"(v3));
+  return w;
+}
+
 // Eight fp32 values -> eight E2M1 nibbles (element 2k in the low nibble of
 // byte k), round to nearest even, saturating at 6.  The conversion writes
 // its first source operand to the high nibble.
@@ -274,9 +287,9 @@ inline FastDiv make_fastdiv(uint32_t d) {
 }  // namespace fp4idx_impl
 
 namespace fp4idx_impl {
-// The streaming kernel (fp4idx_stream.cu): FP4 output, with or without the
-// rotation, and for queries a head count that is a multiple of 16.
-bool stream_eligible(bool queries, int64_t H, int fp8);
+// The streaming kernel (fp4idx_stream.cu): every output mode, with or
+// without the rotation; for queries a head count that is a multiple of 16.
+bool stream_eligible(bool queries, int64_t H);
 fp4idx_status launch_stream(const KArgs& ka, const QArgs& qa, const Shared& sh, bool keys,
-                            bool queries, int rope_style, int rotate, void* stream);
+                            bool queries, int rope_style, int rotate, int fp8, void* stream);
 }  // namespace fp4idx_impl

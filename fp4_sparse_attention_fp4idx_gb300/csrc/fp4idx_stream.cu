@@ -482,6 +482,37 @@ __device__ __forceinline__ void quant4(const uint32_t (&x0)[4], const uint32_t (
   ew = prmt(e01, e23, par ? 0x4602u : 0x6420u);
 }
 
+// The 8 E4M3 codes of one 8-element part: x * inv (an exact product by a
+// power of two), round half to even, saturating at 448.
+__device__ __forceinline__ uint2 codes8_fp8(const uint32_t (&x)[4], float inv) {
+  float v[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) mul2(v[2 * k], v[2 * k + 1], bf16_lo(x[k]), bf16_hi(x[k]), inv, inv);
+  return make_uint2(e4m3x4(v[0], v[1], v[2], v[3]), e4m3x4(v[4], v[5], v[6], v[7]));
+}
+
+// FP8 output mode for a row held by 4 lanes (all 32 lanes call): the row's
+// amax over its 128 elements, one power-of-two scale 2^(e-127) =
+// ceil_pow2(max(rn(amax/448), 2^-126)), and the E4M3 codes of x * 2^(127-e),
+// 8 bytes per register.
+__device__ __forceinline__ void quant4_fp8(const uint32_t (&x0)[4], const uint32_t (&x1)[4],
+                                           const uint32_t (&x2)[4], const uint32_t (&x3)[4],
+                                           uint2 (&code)[4], uint32_t& e) {
+  uint32_t m = hmax_abs(pair_amax(x0, x1), pair_amax(x2, x3));
+  m = hmax_abs(m, prmt(m, m, 0x1032u));  // both halves
+  m = hmax_abs(m, __shfl_xor_sync(kFull, m, 1));
+  m = hmax_abs(m, __shfl_xor_sync(kFull, m, 2));
+  const float amax = __uint_as_float((m & 0x7fffu) << 16);
+  const float t = fmaxf(__fdiv_rn(amax, 448.0f), 1.17549435082228750797e-38f);
+  const uint32_t tb = __float_as_uint(t);
+  e = (tb >> 23) + ((tb & 0x7fffffu) != 0u ? 1u : 0u);  // 1 .. 248 for finite bf16
+  const float inv = __uint_as_float((254u - e) << 23);  // 2^(127-e), a normal float
+  code[0] = codes8_fp8(x0, inv);
+  code[1] = codes8_fp8(x1, inv);
+  code[2] = codes8_fp8(x2, inv);
+  code[3] = codes8_fp8(x3, inv);
+}
+
 // Sum of the squares of 8 elements, left to right, each step rounded.
 __device__ __forceinline__ float sumsq8(const uint32_t (&x)[4]) {
   float acc = __fmul_rn(bf16_lo(x[0]), bf16_lo(x[0]));
@@ -535,11 +566,20 @@ struct Lanes {
     *reinterpret_cast<uint32_t*>(slot + 32 + st_a) = code[2];
     *reinterpret_cast<uint32_t*>(slot + 32 + st_b) = code[3];
   }
+  // FP8 codes of register p (part p ^ par) at bytes 32 (p ^ par) + 8j of a
+  // 128-byte code row.
+  __device__ __forceinline__ void store8(uint8_t* row, const uint2 (&code)[4]) const {
+    const uint32_t a = 2u * st_a, b = 2u * st_b;
+    *reinterpret_cast<uint2*>(row + a) = code[0];
+    *reinterpret_cast<uint2*>(row + b) = code[1];
+    *reinterpret_cast<uint2*>(row + 64 + a) = code[2];
+    *reinterpret_cast<uint2*>(row + 64 + b) = code[3];
+  }
 };
 
 // --------------------------------------------------------- consumer side
 // Rows 16*sl .. of a query unit (first flattened row row0, n rows).
-template <int kStyle, bool kRotate>
+template <int kStyle, bool kRotate, bool kFp8>
 __device__ __forceinline__ void query_slice(uint32_t stage, int32_t row0, int n, uint32_t flags,
                                             int sl, const SWork& wk, const QArgs& qa,
                                             const Shared& sh) {
@@ -572,20 +612,34 @@ __device__ __forceinline__ void query_slice(uint32_t stage, int32_t row0, int n,
     ln.load(stage + (uint32_t)(r_first + r) * kRowBytes, x0, x1, x2, x3);
     rope4<kStyle>(x0, x1, cf, sh.neg_zero);
     if constexpr (kRotate) rotate4(x0, x1, x2, x3, ln.j, ln.par);
-    uint32_t code[4], ew;
-    quant4(x0, x1, x2, x3, ln.par, code, ew);
-    if (r < ns) {
-      const int64_t row = rs + r;
-      ln.store(qa.q_fp4 + row * kPayloadBytes, code);
-      if (ln.j == 0) *reinterpret_cast<uint32_t*>(qa.q_scale + row * 4) = ew;
+    if constexpr (kFp8) {
+      // codes at q_fp4 + row*128; the row's scale folded into its weight
+      uint2 code[4];
+      uint32_t e;
+      quant4_fp8(x0, x1, x2, x3, code, e);
+      const float wr = __uint_as_float(__shfl_sync(kFull, wb, r) << 16);
+      if (r < ns) {
+        const int64_t row = rs + r;
+        ln.store8(qa.q_fp4 + row * FP4IDX_HEAD_DIM, code);
+        if (ln.j == 0)
+          qa.weights[row] = __fmul_rn(__fmul_rn(wr, qa.wscale), __uint_as_float(e << 23));
+      }
+    } else {
+      uint32_t code[4], ew;
+      quant4(x0, x1, x2, x3, ln.par, code, ew);
+      if (r < ns) {
+        const int64_t row = rs + r;
+        ln.store(qa.q_fp4 + row * kPayloadBytes, code);
+        if (ln.j == 0) *reinterpret_cast<uint32_t*>(qa.q_scale + row * 4) = ew;
+      }
     }
   }
-  if (ln.lane < ns)
+  if (!kFp8 && ln.lane < ns)
     qa.weights[rs + ln.lane] = __fmul_rn(__uint_as_float(wb << 16), qa.wscale);
 }
 
 // Rows 16*sl .. of a key unit (tokens t0 .. t0 + n - 1).
-template <int kStyle, bool kRotate>
+template <int kStyle, bool kRotate, bool kFp8>
 __device__ __forceinline__ void key_slice(uint32_t stage, int32_t t0, int n, uint32_t flags,
                                           int sl, const KArgs& ka, const Shared& sh) {
   const Lanes ln;
@@ -641,6 +695,19 @@ __device__ __forceinline__ void key_slice(uint32_t stage, int32_t t0, int n, uin
     norm8(x3, rr, __ldg(g + 4 * (3 ^ pa) + ln.j));
     rope4<kStyle>(x0, x1, cf, sh.neg_zero);
     if constexpr (kRotate) rotate4(x0, x1, x2, x3, ln.j, ln.par);
+    if constexpr (kFp8) {
+      // a 128-byte code row at o*128 of the page, the fp32 scale at 8192 + o*4
+      uint2 code[4];
+      uint32_t e;
+      quant4_fp8(x0, x1, x2, x3, code, e);
+      if (live) {
+        uint8_t* page = ka.cache + (slot / kKvBlock) * (int64_t)kFp8PageBytes;
+        const int64_t o = slot % kKvBlock;
+        ln.store8(page + o * FP4IDX_HEAD_DIM, code);
+        if (ln.j == 0) *reinterpret_cast<uint32_t*>(page + kFp8ScaleOffset + 4 * o) = e << 23;
+      }
+      continue;
+    }
     uint32_t code[4], ew;
     quant4(x0, x1, x2, x3, ln.par, code, ew);
     if (live) {
@@ -774,7 +841,7 @@ __device__ __forceinline__ void issue_meta(int i, int kb, const Units& u, const 
 }
 
 // ------------------------------------------------------------------ kernel
-template <int kStyle, bool kRotate>
+template <int kStyle, bool kRotate, bool kFp8>
 __global__ void __launch_bounds__(kThreadsS, 1)
     stream_kernel(KArgs ka, QArgs qa, Shared sh, SWork wk) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -873,9 +940,9 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     uint32_t hdr[4];
     lds128(stage + kHdrOff, hdr);
     if ((hdr[0] & 3u) == kUnitKey)
-      key_slice<kStyle, kRotate>(stage, (int32_t)hdr[1], (int)hdr[2], hdr[3], sl, ka, sh);
+      key_slice<kStyle, kRotate, kFp8>(stage, (int32_t)hdr[1], (int)hdr[2], hdr[3], sl, ka, sh);
     else
-      query_slice<kStyle, kRotate>(stage, (int32_t)hdr[1], (int)hdr[2], hdr[3], sl, wk, qa, sh);
+      query_slice<kStyle, kRotate, kFp8>(stage, (int32_t)hdr[1], (int)hdr[2], hdr[3], sl, wk, qa, sh);
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8u * s);
   }
@@ -886,9 +953,9 @@ __global__ void __launch_bounds__(kThreadsS, 1)
 constexpr int kMaxDevicesS = 64;
 int g_sms[kMaxDevicesS];  // 0: not set up yet; -1: set-up failed
 
-template <int kStyle, bool kRotate>
+template <int kStyle, bool kRotate, bool kFp8>
 bool setup_stream() {
-  auto kern = stream_kernel<kStyle, kRotate>;
+  auto kern = stream_kernel<kStyle, kRotate, kFp8>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemS) !=
       cudaSuccess)
     return false;
@@ -898,15 +965,33 @@ bool setup_stream() {
          n >= 1;
 }
 
+template <int kStyle>
+bool setup_style() {
+  return setup_stream<kStyle, false, false>() && setup_stream<kStyle, false, true>() &&
+         setup_stream<kStyle, true, false>() && setup_stream<kStyle, true, true>();
+}
+
+// The kernel for (rotate, fp8).
+template <int kStyle>
+void launch_style(unsigned grid, cudaStream_t s, const KArgs& ka, const QArgs& qa,
+                  const Shared& sh, const SWork& wk, int rotate, int fp8) {
+  if (!rotate && !fp8)
+    stream_kernel<kStyle, false, false><<<grid, kThreadsS, kSmemS, s>>>(ka, qa, sh, wk);
+  else if (!rotate)
+    stream_kernel<kStyle, false, true><<<grid, kThreadsS, kSmemS, s>>>(ka, qa, sh, wk);
+  else if (!fp8)
+    stream_kernel<kStyle, true, false><<<grid, kThreadsS, kSmemS, s>>>(ka, qa, sh, wk);
+  else
+    stream_kernel<kStyle, true, true><<<grid, kThreadsS, kSmemS, s>>>(ka, qa, sh, wk);
+}
+
 int stream_sms() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesS) return 0;
   if (g_sms[dev] == 0) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        !setup_stream<FP4IDX_ROPE_NEOX, false>() ||
-        !setup_stream<FP4IDX_ROPE_INTERLEAVED, false>() ||
-        !setup_stream<FP4IDX_ROPE_NEOX, true>() || !setup_stream<FP4IDX_ROPE_INTERLEAVED, true>())
+        !setup_style<FP4IDX_ROPE_NEOX>() || !setup_style<FP4IDX_ROPE_INTERLEAVED>())
       return 0;
     g_sms[dev] = sms;
   }
@@ -915,12 +1000,10 @@ int stream_sms() {
 
 }  // namespace
 
-bool stream_eligible(bool queries, int64_t H, int fp8) {
-  return !fp8 && (!queries || H % kSliceRows == 0);
-}
+bool stream_eligible(bool queries, int64_t H) { return !queries || H % kSliceRows == 0; }
 
 fp4idx_status launch_stream(const KArgs& ka, const QArgs& qa, const Shared& sh, bool keys,
-                            bool queries, int rope_style, int rotate, void* stream) {
+                            bool queries, int rope_style, int rotate, int fp8, void* stream) {
   const int64_t H = queries ? qa.H : 0;
   if (sh.T >= (1 << 30) || H >= (1 << 30) || sh.T * H >= (1 << 30)) return FP4IDX_ERR_SHAPE;
   SWork wk;
@@ -943,15 +1026,10 @@ fp4idx_status launch_stream(const KArgs& ka, const QArgs& qa, const Shared& sh, 
   if (sms <= 0) return FP4IDX_ERR_CUDA;
   const unsigned grid = (unsigned)(total < sms ? total : sms);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const bool neox = rope_style == FP4IDX_ROPE_NEOX;
-  if (neox && !rotate)
-    stream_kernel<FP4IDX_ROPE_NEOX, false><<<grid, kThreadsS, kSmemS, s>>>(ka, qa, sh, wk);
-  else if (!rotate)
-    stream_kernel<FP4IDX_ROPE_INTERLEAVED, false><<<grid, kThreadsS, kSmemS, s>>>(ka, qa, sh, wk);
-  else if (neox)
-    stream_kernel<FP4IDX_ROPE_NEOX, true><<<grid, kThreadsS, kSmemS, s>>>(ka, qa, sh, wk);
+  if (rope_style == FP4IDX_ROPE_NEOX)
+    launch_style<FP4IDX_ROPE_NEOX>(grid, s, ka, qa, sh, wk, rotate, fp8);
   else
-    stream_kernel<FP4IDX_ROPE_INTERLEAVED, true><<<grid, kThreadsS, kSmemS, s>>>(ka, qa, sh, wk);
+    launch_style<FP4IDX_ROPE_INTERLEAVED>(grid, s, ka, qa, sh, wk, rotate, fp8);
   return cudaGetLastError() == cudaSuccess ? FP4IDX_OK : FP4IDX_ERR_CUDA;
 }
 

@@ -1,7 +1,7 @@
 """GPU parity of the streaming pre-pass kernel (64-row work units fed by a
-producer warp, four lanes per row): the path taken for FP4 output, with
-or without the 128-point rotation, when the head count is a multiple of 16,
-and for every key-only call.  The cases leave ragged units and slices, use every
+producer warp, four lanes per row): the path taken for both output modes
+(FP4 and FP8), with or without the 128-point rotation, when the head count
+is a multiple of 16, and for every key-only call.  The cases leave ragged units and slices, use every
 query-row layout the producer copies (contiguous rows, contiguous heads
 under a larger token stride, one copy per row), put the quantiser's edge
 rows at both row parities of a quarter-warp, and feed out-of-range
@@ -13,6 +13,7 @@ import torch
 from fp4_sparse_attention_fp4idx_gb300 import workloads as wl
 from tests.gpu_util import (DeviceWorkload, F, assert_bytes_equal, assert_same, assert_weights,
                             run_oracle)
+from tests.test_fp8_gpu import assert_fp8_same, run_gpu as run_fp8, run_ref as run_fp8_ref
 
 pytestmark = pytest.mark.gpu
 
@@ -132,4 +133,43 @@ def test_stream_repeat_and_reuse(hadamard):
     b = d.run("fused", hadamard=hadamard)
     for x, y in zip(a, b):
         assert np.array_equal(x, y)
+    assert int(d.err.item()) == 0
+
+
+@pytest.mark.parametrize("hadamard", [False, True], ids=["plain", "rotated"])
+@pytest.mark.parametrize("style", STYLES)
+@pytest.mark.parametrize("T,H", [(1, 16), (5, 48), (63, 32), (65, 64), (130, 128), (301, 32)])
+def test_stream_fp8_ragged(T, H, style, hadamard):
+    """The FP8 output mode: 8448-byte cache pages and 128-byte query code
+    rows byte for byte, the weights (row scale folded in) within 1 ulp, on
+    ragged units and slices, with and without the rotation."""
+    w = wl.make_random(T, H, style, seed=3000 + 13 * T + H)
+    ref = run_fp8_ref(w, hadamard=hadamard)
+    for mode in ("fused", "separate"):
+        d = DeviceWorkload(w)
+        assert_fp8_same(f"T={T} H={H} {mode}", run_fp8(d, mode, hadamard=hadamard), ref)
+        assert int(d.err.item()) == 0
+
+
+@pytest.mark.parametrize("style", STYLES)
+@pytest.mark.parametrize("scale", [1.0, 1e-3, 3e4])
+def test_stream_fp8_special_rows(style, scale):
+    """FP8 rows at the scale's edges on both row parities: all-zero and
+    subnormal rows (the 2^-126 floor), and query rows whose amax/448 is an
+    exact power of two (no rounding up of the scale), at position 0."""
+    w = wl.make_random(70, 16, style, seed=int(scale * 11) + 31 * style + 9, scales=(scale,))
+    rng = np.random.Generator(np.random.PCG64(29 + style))
+    w.q[0] = 0
+    w.k[0] = 0
+    w.q[1] = wl.subnormal_bf16(rng, 16 * 128).reshape(16, 128)
+    w.k[1] = wl.subnormal_bf16(rng, 128)
+    for t in (2, 3):
+        for h in range(16):
+            top = 448.0 * 2.0 ** (h - 8)
+            row = rng.uniform(-0.9, 0.9, 128) * top
+            row[(7 * h + t) % 128] = top if h % 2 else -top
+            w.q[t, h] = wl.to_bf16_bits(row)
+        w.positions[t] = 0
+    d = DeviceWorkload(w)
+    assert_fp8_same("special rows", run_fp8(d, "fused"), run_fp8_ref(w))
     assert int(d.err.item()) == 0
