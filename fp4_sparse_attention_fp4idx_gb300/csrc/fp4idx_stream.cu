@@ -1,13 +1,18 @@
 // fp4idx_stream.cu -- the streaming kernel of the fused FP4 indexer pre-pass
-// (sm_103a): the path taken for FP4 output without the Hadamard rotation when
-// the head count is a multiple of 16 (or only keys are processed).
+// (sm_103a): the path taken, in both output modes and with or without the
+// Hadamard rotation, when the head count is a multiple of 16 (or only keys
+// are processed).
 //
 // Sources (web pages, by title and section): "dsv4.1: RoPE and FP4 packing
 // kernels" (sglang PR 39656), Summary (key op = RMSNorm + RoPE + both
 // quantisation stages + paged store; query op = RoPE + quantisation + head
 // weights in one launch); "[HIP] Add FP4 output mode to
 // indexer_qk_rope_quant_and_cache" (aiter PR 5484), API (geometry, q_out
-// layout, plain weights) and One deliberate deviation (round half to even).
+// layout, plain weights), One deliberate deviation (round half to even) and
+// Summary (the FP8 contract, its query scale folded into the weights);
+// "DeepSeek-V4 FP4: fused_compress FP4 scatter + rmsnorm_rope_rotate FP4
+// KV-cache kernel" (aiter PR 4029), Changes (the optional Hadamard rotation
+// between RoPE and quantisation).
 // The arithmetic is fp4idx.cu's, operation for operation (the same closed
 // form of the two quantisation stages, the same explicitly rounded fp32
 // steps); only the distribution of the work differs.
