@@ -173,3 +173,48 @@ def test_stream_fp8_special_rows(style, scale):
     d = DeviceWorkload(w)
     assert_fp8_same("special rows", run_fp8(d, "fused"), run_fp8_ref(w))
     assert int(d.err.item()) == 0
+
+
+def test_stream_fp8_query_layouts():
+    """The FP8 mode under the producer's three query-row copy layouts (one
+    copy per unit, per 16-row slice, per row) and a key row stride of 256."""
+    w = wl.make_random(50, 32, wl.ROPE_NEOX, seed=90)
+    d = DeviceWorkload(w)
+    f = F()
+    rc, rq, rw = run_fp8_ref(w)
+    big1 = torch.zeros((50, 40, 128), dtype=torch.bfloat16, device="cuda")
+    big1[:, 3:35] = d.q
+    big2 = torch.zeros((50, 64, 128), dtype=torch.bfloat16, device="cuda")
+    big2[:, ::2] = d.q
+    bigk = torch.zeros((50, 2, 128), dtype=torch.bfloat16, device="cuda")
+    bigk[:, 1] = d.k
+    for qv in (d.q, big1[:, 3:35], big2[:, ::2]):
+        cache = torch.from_numpy(wl.fp8_sentinel_cache(w)).cuda()
+        qo, wt = f.indexer_prepass_fp8(bigk[:, 1], d.gamma, d.slots, cache, qv, d.wt, d.pos,
+                                       d.cos, d.sin, eps=w.eps, rope_style=w.rope_style)
+        torch.cuda.synchronize()
+        assert_fp8_same(f"strides {qv.stride()}", (cache.cpu().numpy(), qo.cpu().numpy(),
+                                                   wt.cpu().numpy()), (rc, rq, rw))
+
+
+def test_stream_fp8_out_of_range_positions():
+    """FP8 mode: a query token whose position is out of range is skipped
+    whole and flagged; its key row is skipped and flagged; the rest is exact."""
+    w = wl.make_random(40, 32, wl.ROPE_INTERLEAVED, seed=24, max_pos=100)
+    w.positions[5] = 100
+    w.positions[30] = -3
+    d = DeviceWorkload(w)
+    cache = torch.from_numpy(wl.fp8_sentinel_cache(w)).cuda()
+    sentinel = torch.full((40, 32, 128), 0xA5, dtype=torch.uint8, device="cuda")
+    qo, wt = F().indexer_prepass_fp8(d.k, d.gamma, d.slots, cache, d.q, d.wt, d.pos, d.cos,
+                                     d.sin, eps=w.eps, rope_style=w.rope_style, q_out=sentinel,
+                                     err_flags=d.err)
+    torch.cuda.synchronize()
+    assert int(d.err.item()) & F().ERRFLAG_POSITION
+    rc, rq, rw = run_fp8_ref(w)
+    assert_bytes_equal(cache.cpu().numpy(), rc, "fp8 cache")
+    good = np.setdiff1d(np.arange(40), [5, 30])
+    qn = qo.cpu().numpy()
+    assert_bytes_equal(qn[good], rq[good], "fp8 q codes")
+    assert_weights(wt.cpu().numpy()[good], rw[good])
+    assert np.all(qn[[5, 30]] == 0xA5)
