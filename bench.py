@@ -63,11 +63,10 @@ def algorithmic_bytes(w, mode: str) -> dict:
             "step": fused if mode == "fused" else q_call + k_call, "n_valid": n_valid}
 
 
-def prepass_kernel_name(H: int, fp8: bool = False, hadamard: bool = False) -> str:
-    """The kernel a pre-pass launch runs: the streaming kernel (every output
-    mode, with or without the rotation) when the head count is a multiple of
-    16, otherwise the per-warp kernel."""
-    del fp8, hadamard  # every form runs in the streaming kernel
+def prepass_kernel_name(H: int) -> str:
+    """The kernel a pre-pass launch runs, in every output mode and with or
+    without the rotation: the streaming kernel when the head count is a
+    multiple of 16, otherwise the per-warp kernel."""
     return "stream_kernel" if H % 16 == 0 else "prepass_kernel"
 
 
@@ -413,7 +412,7 @@ def run_variants(F, w, D, dev, peak, flush, steps: int = 100, warmup: int = 5) -
         out[name] = {"ms_per_launch": round(ms, 5), "tokens_per_s": round(T / (ms / 1e3), 1),
                      "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
                      "algorithmic_bytes_per_launch": nbytes,
-                     "kernel": prepass_kernel_name(H, fp8=bool(mode), hadamard=bool(had))}
+                     "kernel": prepass_kernel_name(H)}
     # The torch-shaped RoPE + FP4 fake quantisation of the workload's queries
     # (T*H rows): 256 B read + 256 B written per row, 8 B of position per
     # token, 256 B of cos/sin per distinct position.
