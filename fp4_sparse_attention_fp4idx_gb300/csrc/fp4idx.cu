@@ -13,6 +13,11 @@
 //   deviation (round half to even at midpoints).
 //
 // ---------------------------------------------------------------- design
+// Routing: this file's pre-pass kernel (prepass_kernel) serves query calls
+// whose head count is not a multiple of 16; every other launch runs the
+// streaming kernel of fp4idx_stream.cu, which performs the same operations
+// in the same order (shared helpers in fp4idx_common.cuh).
+//
 // The pass is HBM-bound (about 2.6 bytes moved per element and a few dozen
 // integer/fp32 operations), so the kernel is organised around two limits:
 // bytes in flight and issue slots per element.

@@ -54,6 +54,11 @@
 //    which puts the two rows in different halves of the 128-byte bank
 //    window.  The swap is undone where it shows: the NeoX sine sign, the
 //    interleaved coefficients, the exponent byte order and the store offsets.
+//  * The rotation and the FP8 output mode are template flags on the same
+//    layout.  The 128-point Walsh-Hadamard butterflies (rotate4) need lane
+//    shuffles only at distances 8 and 16; the FP8 quantiser (quant4_fp8)
+//    reduces one amax per row over its 4 lanes and stores 8 code bytes per
+//    part.
 //  * Every wait is bounded (1 s); a timeout sets FP4IDX_ERRFLAG_TIMEOUT and
 //    the CTA drains its copies in flight before it exits.
 
@@ -956,7 +961,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
 
 // --------------------------------------------------------------- host side
 constexpr int kMaxDevicesS = 64;
-int g_sms[kMaxDevicesS];  // 0: not set up yet; -1: set-up failed
+int g_sms[kMaxDevicesS];  // 0: not set up yet (a failed set-up is retried)
 
 template <int kStyle, bool kRotate, bool kFp8>
 bool setup_stream() {
