@@ -22,10 +22,11 @@
 // integer/fp32 operations), so the kernel is organised around two limits:
 // bytes in flight and issue slots per element.
 //
-// Data movement: one persistent grid; every warp owns a contiguous range of
-// work items and a private ring of kStages shared-memory stages.  A work item
-// is a chunk of up to 8 rows of 128 bf16 (2 KB): 8 heads of one query token,
-// or the key rows of 8 consecutive tokens.  Lane 0 of the warp fetches items
+// Data movement: one persistent grid of 24-warp CTAs; the warps of a CTA
+// claim work items from shared counters, each warp with a private ring of
+// kStages shared-memory stages.  A work item is a chunk of up to kChunkRows
+// (16) rows of 128 bf16 (4 KB): up to 16 heads of one query token, or the key
+// rows of 16 consecutive tokens.  Lane 0 of the warp fetches items
 // kStages ahead with cp.async.bulk (the Blackwell bulk-copy engine), together
 // with the query token's cos/sin rows, and an mbarrier per stage counts the
 // bytes in.  So the bytes in flight cost no registers and no load
