@@ -56,3 +56,49 @@ def test_weak_scaling_value_single_rank():
     import bench
     assert bench.weak_scaling_value(1, 65536, 0.25) == pytest.approx(65536 / 0.25e-3)
     assert bench.max_over_ranks(3.5, None) == 3.5
+
+
+def test_prepass_bytes_match_array_sizes():
+    """The pre-pass roofline numerator recounted from the byte sizes of what
+    one fused launch must read and write on a small workload: every query
+    row, head weight, position and slot entry, gamma, the key rows that have
+    a slot, the cos/sin rows of the distinct positions, and the oracle's
+    outputs plus one 68-byte slot per stored key."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+
+    import bench
+    import oracle
+    from fp4_sparse_attention_fp4idx_gb300 import workloads as wl
+    w = wl.make_random(300, 32, wl.ROPE_NEOX, seed=5)
+    qf, qs, wt, _ = oracle.q_rope_pack_weights(w.q, w.w, w.positions, w.cos, w.sin,
+                                               w.rope_style)
+    valid = w.slot_mapping >= 0
+    pos = np.unique(w.positions)
+    assert 0 < pos.size < w.T and 0 < valid.sum() < w.T  # both counts are exercised
+    reads = (w.q.nbytes + w.w.nbytes + w.positions.nbytes + w.slot_mapping.nbytes
+             + w.gamma.nbytes + w.k[valid].nbytes + w.cos[pos].nbytes + w.sin[pos].nbytes)
+    slot_bytes = w.cache_init.shape[1] // wl.KV_BLOCK
+    writes = qf.nbytes + qs.nbytes + wt.nbytes + int(valid.sum()) * slot_bytes
+    assert bench.algorithmic_bytes(w, "fused")["fused"] == reads + writes
+
+
+def test_scorer_bytes_match_array_sizes():
+    """The scorer roofline numerator recounted from array sizes: the slots of
+    the cached tokens below each context, the block-table entries of the
+    pages they occupy, the packed queries, scales, weights and context
+    lengths, and the fp32 logits including the -inf padding."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+
+    import bench
+    from fp4_sparse_attention_fp4idx_gb300 import workloads as wl
+    sw = wl.make_scorer_config("scorer_glm_next4")
+    slot_bytes = sw.kv_cache.shape[1] // wl.KV_BLOCK
+    reads = sw.q_fp4.nbytes + sw.q_scale.nbytes + sw.weights.nbytes + sw.context_lens.nbytes
+    for b in range(sw.batch):
+        ctx = min(max(int(sw.context_lens[b]), 0), sw.max_context)
+        pages = sw.block_table[b, :-(-ctx // wl.KV_BLOCK)] if ctx else sw.block_table[b, :0]
+        reads += ctx * slot_bytes + pages.nbytes
+    logits = np.empty((sw.batch * sw.next_n, sw.max_context), np.float32)
+    assert bench.scorer_bytes(sw) == reads + logits.nbytes
