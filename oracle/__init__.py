@@ -31,6 +31,21 @@ ROPE_NEOX = 0
 ROPE_INTERLEAVED = 1
 
 
+_CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fno-strict-aliasing",
+           "-shared", "-fPIC"]
+
+
+def _gcc(src: str, out: str) -> None:
+    """gcc with OpenMP (token-parallel loops) when the toolchain has it, else
+    without (the pragmas are then ignored and the oracle runs one thread)."""
+    try:
+        subprocess.run(["gcc", *_CFLAGS, "-fopenmp", "-o", out, src, "-lm"], check=True,
+                       stderr=subprocess.DEVNULL)
+    except subprocess.CalledProcessError:
+        subprocess.run(["gcc", *_CFLAGS, "-Wno-unknown-pragmas", "-o", out, src, "-lm"],
+                       check=True)
+
+
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc (no FP contraction, no fast-math)."""
     hdr = os.path.join(_HERE, "fp4idx_oracle.h")
@@ -38,9 +53,7 @@ def build(force: bool = False) -> str:
             and os.path.getmtime(_LIB) >= max(os.path.getmtime(_SRC), os.path.getmtime(hdr))):
         return _LIB
     tmp = _LIB + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
-           "-fno-strict-aliasing", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"]
-    subprocess.run(cmd, check=True)
+    _gcc(_SRC, tmp)
     os.replace(tmp, _LIB)
     return _LIB
 
@@ -56,6 +69,11 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.oracle_rope_row.restype = None
     L.oracle_quant_group.argtypes = [P, ctypes.c_float, P]
     L.oracle_quant_group.restype = ctypes.c_int
+    L.oracle_quant_group_floors.argtypes = [P, ctypes.c_float, ctypes.c_float, P]
+    L.oracle_quant_group_floors.restype = ctypes.c_int
+    L.oracle_quant_pack_row_floors.argtypes = [P, ctypes.c_float, ctypes.c_float,
+                                               ctypes.c_float, ctypes.c_float, P, P, P, P, P]
+    L.oracle_quant_pack_row_floors.restype = None
     L.oracle_dequant.argtypes = [ctypes.c_uint8, ctypes.c_int]
     L.oracle_dequant.restype = ctypes.c_float
     L.oracle_quant_pack_row.argtypes = [P, P, P, P, P, P]
@@ -95,6 +113,14 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.oracle_paged_mqa_logits.argtypes = [
         P, P, P, P, i64, P, i64, P, P, i64, i64, i64, i64, i64]
     L.oracle_paged_mqa_logits.restype = ctypes.c_int
+    L.oracle_mqa_logits_prefill.argtypes = [P, P, P, P, i64, P, P, P, i64, i64, i64]
+    L.oracle_mqa_logits_prefill.restype = ctypes.c_int
+    L.oracle_set_threads.argtypes = [ctypes.c_int]
+    L.oracle_set_threads.restype = None
+    L.oracle_get_threads.argtypes = []
+    L.oracle_get_threads.restype = ctypes.c_int
+    L.oracle_threads_available.argtypes = []
+    L.oracle_threads_available.restype = ctypes.c_int
     return L
 
 
@@ -121,9 +147,7 @@ def compile_variant(source_text: str, workdir: str) -> ctypes.CDLL:
     with open(src, "w") as f:
         f.write(source_text)
     so = os.path.join(workdir, f"libvariant{abs(hash(source_text))}.so")
-    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
-                    "-fno-strict-aliasing", "-shared", "-fPIC", "-o", so, src, "-lm"],
-                   check=True)
+    _gcc(src, so)
     return _bind(ctypes.CDLL(so))
 
 
@@ -187,6 +211,63 @@ def quant_group(z, floor: float = 2.0 ** -126):
     n = np.empty(32, np.uint8)
     e = lib().oracle_quant_group(_p(z), ctypes.c_float(floor), _p(n))
     return n, int(e)
+
+
+def quant_group_floors(z, amax_floor: float, quot_floor: float):
+    """(nibbles uint8[32], exponent) with a floor on the amax (before the
+    division by 6) and one on the quotient (after it); 0 = no floor."""
+    z = _c(z, np.float32)
+    assert z.shape == (32,)
+    n = np.empty(32, np.uint8)
+    e = lib().oracle_quant_group_floors(_p(z), ctypes.c_float(amax_floor),
+                                        ctypes.c_float(quot_floor), _p(n))
+    return n, int(e)
+
+
+def quant_pack_row_floors(row_bits, s1_amax: float, s1_quot: float, s2_amax: float,
+                          s2_quot: float):
+    """quant_pack_row with explicit floors for both stages."""
+    r = _c(row_bits, np.uint16)
+    assert r.shape == (HEAD_DIM,)
+    payload = np.empty(PAYLOAD_BYTES, np.uint8)
+    ex = np.empty(EXP_BYTES, np.uint8)
+    e1 = np.empty(4, np.int32)
+    e2 = np.empty(4, np.int32)
+    n1 = np.empty(HEAD_DIM, np.uint8)
+    lib().oracle_quant_pack_row_floors(_p(r), ctypes.c_float(s1_amax), ctypes.c_float(s1_quot),
+                                       ctypes.c_float(s2_amax), ctypes.c_float(s2_quot),
+                                       _p(payload), _p(ex), _p(e1), _p(e2), _p(n1))
+    return dict(payload=payload, exp=ex, e1=e1, e2=e2, n1=n1)
+
+
+def set_threads(n: int) -> None:
+    """Host threads for the oracle's token / row loops (1 = single-threaded)."""
+    lib().oracle_set_threads(int(n))
+
+
+def get_threads() -> int:
+    return int(lib().oracle_get_threads())
+
+
+def threads_available() -> int:
+    """Cores the oracle can use (1 if it was built without OpenMP)."""
+    return int(lib().oracle_threads_available())
+
+
+class threads:
+    """Context manager: run the oracle on n host threads (default: all)."""
+
+    def __init__(self, n: int | None = None):
+        self.n = n
+
+    def __enter__(self):
+        self.prev = get_threads()
+        set_threads(self.n or threads_available())
+        return get_threads()
+
+    def __exit__(self, *exc):
+        set_threads(self.prev)
+        return False
 
 
 def dequant(nibble: int, e: int) -> float:
@@ -357,4 +438,24 @@ def paged_mqa_logits(q_fp4, q_scale, weights, kv_cache, block_table, context_len
     st = lib().oracle_paged_mqa_logits(
         _p(qf), _p(qs), _p(wt), _p(cache), cache.shape[0], _p(bt), bt.shape[1], _p(cl),
         _p(out), max_context, B, next_n, H, max_context)
+    return out, int(st)
+
+
+def mqa_logits_prefill(q_fp4, q_scale, weights, kv_cache, ks, ke, num_keys: int):
+    """Prefill scorer: (logits fp32 [T, num_keys], status) for query tokens
+    q_fp4 [T,H,64] against the consecutive keys 0..num_keys-1 of kv_cache
+    (key s at page s/64, offset s%64), token t scoring [ks[t], ke[t])."""
+    qf = _c(q_fp4, np.uint8)
+    qs = _c(q_scale, np.uint8)
+    wt = _c(weights, np.float32)
+    T, H, _ = qf.shape
+    assert qf.shape[2] == PAYLOAD_BYTES and qs.shape == (T, H, EXP_BYTES) and wt.shape == (T, H)
+    cache = _c(kv_cache, np.uint8)
+    assert cache.shape[1:] == (PAGE_BYTES,) and cache.shape[0] * KV_BLOCK >= num_keys
+    a = _c(ks, np.int32)
+    b = _c(ke, np.int32)
+    assert a.shape == (T,) and b.shape == (T,)
+    out = np.empty((T, num_keys), np.float32)
+    st = lib().oracle_mqa_logits_prefill(_p(qf), _p(qs), _p(wt), _p(cache), int(num_keys),
+                                         _p(a), _p(b), _p(out), num_keys, T, H)
     return out, int(st)

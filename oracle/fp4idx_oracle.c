@@ -13,7 +13,28 @@
 #include "fp4idx_oracle.h"
 
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Tokens (and scorer rows) are independent, so the top-level loops may run
+ * on several host threads; the arithmetic of each row is the same scalar
+ * code whatever the thread count.  Default: one thread. */
+static int g_threads = 1;
+
+void oracle_set_threads(int n) { g_threads = n < 1 ? 1 : n; }
+
+int oracle_get_threads(void) { return g_threads; }
+
+int oracle_threads_available(void) {
+#ifdef _OPENMP
+  return omp_get_num_procs();
+#else
+  return 1;
+#endif
+}
 
 enum {
   HEAD_DIM = 128,     /* [aiter] API: head_dim = 128 */
@@ -28,14 +49,29 @@ enum {
 /* The E2M1 grid: magnitude code m in 0..7 encodes GRID[m]. */
 static const double GRID[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
 
-/* Scale floors of the two quantisation stages.  The [sgl] review says the
- * indexer packer applies its floor after the amax/6 division and that the
- * packer's floor differs from the fake-quant's; neither value is printed.
- * Reading taken: both floors are 2^-126 (the smallest normal fp32), applied
- * after the division.  They only decide the exponent of groups whose amax is
- * below 6 * 2^-126 (all-zero and subnormal groups get exponent byte 1). */
-static const float STAGE1_FLOOR = 1.17549435082228750797e-38f; /* 2^-126 */
-static const float STAGE2_FLOOR = 1.17549435082228750797e-38f; /* 2^-126 */
+/* Scale floors of the two quantisation stages.
+ *   Stage 1 is the fake quantisation (fake_quant_fp4 / fp4::block_scale).
+ *     Its floor guards the amax of an all-zero group BEFORE the division by
+ *     6 ([csa] review: the FP4 quantiser's amax has an all-zero-group eps
+ *     floor).
+ *   Stage 2 is the indexer packer.  It divides first and floors the
+ *     quotient ([sgl] review: index_pack_exponent keeps amax / 6.0f and a
+ *     post-divide floor rather than reusing fp4::block_scale).
+ * So the two scale floors differ, as the [sgl] review states (the packer
+ * "has a different scale floor from fake_quant_fp4"): one acts on the amax,
+ * the other on amax/6.  Neither value is printed.  Reading taken: both
+ * constants are 2^-126, the smallest normal fp32 -- the smallest floor that
+ * does the one job the pages give it (an all-zero group).
+ * Which bytes hang on this reading: none, for any amax floor in
+ * (0, 6 * 2^-126] and any quotient floor in (0, 2^-126].  Every quotient at
+ * or below 2^-126 already has biased exponent 1 after the ceiling (and 1 is
+ * the clamp's lower bound), so every such floor pair gives every group the
+ * same exponent.  A larger floor F would change exactly the groups whose
+ * stage amax is below 6 * F. */
+static const float STAGE1_AMAX_FLOOR = 1.17549435082228750797e-38f; /* 2^-126 */
+static const float STAGE2_QUOT_FLOOR = 1.17549435082228750797e-38f; /* 2^-126 */
+/* The FP8 row scale's floor (reading F2: ceil_pow2(max(amax/448, 2^-126))). */
+static const float FP8_QUOT_FLOOR = 1.17549435082228750797e-38f; /* 2^-126 */
 
 static uint32_t f2u(float f) {
   uint32_t u;
@@ -160,19 +196,22 @@ static int e2m1_nearest_code(double v) {
 
 /* One per-32 UE8M0 group ([sgl] review, index_pack_exponent and
  * clear_negative_zero):
- *   A = max|z|;  t = max(rn32(A / 6), floor)
+ *   A = max(max|z|, amax_floor);  t = max(rn32(A / 6), quot_floor)
  *   e = (bits(t) >> 23) + (mantissa(t) != 0), clamped to [1, 254]
  *       i.e. the biased exponent of the power of two ceil_pow2(t)
  *   code = nearest grid point to |z| / 2^(e-127), ties to even
- *   nibble = code | 8 if z < 0 and code != 0  (no -0 codes). */
-int oracle_quant_group(const float* z, float floor_, uint8_t* nibbles) {
+ *   nibble = code | 8 if z < 0 and code != 0  (no -0 codes).
+ * A floor of 0 is no floor. */
+int oracle_quant_group_floors(const float* z, float amax_floor, float quot_floor,
+                              uint8_t* nibbles) {
   float amax = 0.0f;
   for (int i = 0; i < GROUP; ++i) {
     float a = fabsf(z[i]);
     if (a > amax) amax = a;
   }
+  if (amax < amax_floor) amax = amax_floor;
   float t = amax / 6.0f;
-  if (t < floor_) t = floor_;
+  if (t < quot_floor) t = quot_floor;
   uint32_t bits = f2u(t);
   int e = (int)(bits >> 23) + ((bits & 0x7fffffu) != 0u ? 1 : 0);
   if (e < 1) e = 1;
@@ -185,6 +224,11 @@ int oracle_quant_group(const float* z, float floor_, uint8_t* nibbles) {
     nibbles[i] = (uint8_t)(m | (neg ? 8 : 0));
   }
   return e;
+}
+
+/* The same group quantiser with only a quotient floor (the packer's form). */
+int oracle_quant_group(const float* z, float floor_, uint8_t* nibbles) {
+  return oracle_quant_group_floors(z, 0.0f, floor_, nibbles);
 }
 
 float oracle_dequant(uint8_t nibble, int e) {
@@ -200,15 +244,20 @@ float oracle_dequant(uint8_t nibble, int e) {
  * exponent byte g = stage-2 exponent of group g.
  * Readings (pages silent): even element in the low nibble; group g in byte g
  * of the little-endian exponent word. */
-void oracle_quant_pack_row(const uint16_t* row, uint8_t* payload64,
-                           uint8_t* exp4, int* stage1_e, int* stage2_e,
-                           uint8_t* stage1_nibbles) {
+/* The pack with the four floors as arguments (stage-1 amax and quotient
+ * floors, stage-2 amax and quotient floors): lets the tests show which
+ * floor readings give the same bytes.  The pre-pass uses
+ * (STAGE1_AMAX_FLOOR, 0, 0, STAGE2_QUOT_FLOOR). */
+void oracle_quant_pack_row_floors(const uint16_t* row, float s1_amax, float s1_quot,
+                                  float s2_amax, float s2_quot, uint8_t* payload64,
+                                  uint8_t* exp4, int* stage1_e, int* stage2_e,
+                                  uint8_t* stage1_nibbles) {
   for (int g = 0; g < HEAD_DIM / GROUP; ++g) {
     float z[GROUP];
     for (int i = 0; i < GROUP; ++i) z[i] = bf16_to_f32(row[GROUP * g + i]);
 
     uint8_t n1[GROUP];
-    int e1 = oracle_quant_group(z, STAGE1_FLOOR, n1);
+    int e1 = oracle_quant_group_floors(z, s1_amax, s1_quot, n1);
     float u[GROUP];
     for (int i = 0; i < GROUP; ++i) {
       float dq = oracle_dequant(n1[i], e1);
@@ -216,7 +265,7 @@ void oracle_quant_pack_row(const uint16_t* row, uint8_t* payload64,
     }
 
     uint8_t n2[GROUP];
-    int e2 = oracle_quant_group(u, STAGE2_FLOOR, n2);
+    int e2 = oracle_quant_group_floors(u, s2_amax, s2_quot, n2);
 
     for (int j = 0; j < GROUP / 2; ++j)
       payload64[16 * g + j] = (uint8_t)(n2[2 * j] | (n2[2 * j + 1] << 4));
@@ -225,6 +274,13 @@ void oracle_quant_pack_row(const uint16_t* row, uint8_t* payload64,
     if (stage2_e) stage2_e[g] = e2;
     if (stage1_nibbles) memcpy(stage1_nibbles + GROUP * g, n1, GROUP);
   }
+}
+
+void oracle_quant_pack_row(const uint16_t* row, uint8_t* payload64,
+                           uint8_t* exp4, int* stage1_e, int* stage2_e,
+                           uint8_t* stage1_nibbles) {
+  oracle_quant_pack_row_floors(row, STAGE1_AMAX_FLOOR, 0.0f, 0.0f, STAGE2_QUOT_FLOOR,
+                               payload64, exp4, stage1_e, stage2_e, stage1_nibbles);
 }
 
 /* Optional rotation of a row before quantisation ([csa] Changes: the
@@ -262,13 +318,25 @@ static int key_pass(const uint16_t* k, const uint16_t* gamma, float eps,
                     const int64_t* slot_mapping, uint8_t* kv_cache,
                     int64_t num_blocks, int64_t num_tokens, int compress_ratio,
                     int hadamard, int fp8) {
-  int status = 0;
+  /* Each token's slot bytes are formed first (in parallel when threads are
+   * enabled), then stored in token order, so a repeated slot keeps the last
+   * token's bytes whatever the thread count. */
+  enum { REC = HEAD_DIM + 4 }; /* 132 >= 68 */
+  uint8_t* rec = (uint8_t*)malloc((size_t)(num_tokens > 0 ? num_tokens : 1) * REC);
+  signed char* state = (signed char*)malloc((size_t)(num_tokens > 0 ? num_tokens : 1));
+  if (!rec || !state) {
+    free(rec);
+    free(state);
+    return -2;
+  }
+#pragma omp parallel for num_threads(g_threads) schedule(dynamic, 64)
   for (int64_t t = 0; t < num_tokens; ++t) {
     int64_t slot = slot_mapping[t];
+    state[t] = 0; /* skipped */
     if (slot < 0) continue;
     int64_t pos = positions[t];
     if (pos < 0 || pos >= max_pos || slot >= num_blocks * KV_BLOCK) {
-      status = -1;
+      state[t] = -1;
       continue;
     }
     /* [sgl] Summary: RoPE at the group's first position; with groups of
@@ -279,20 +347,35 @@ static int key_pass(const uint16_t* k, const uint16_t* gamma, float eps,
     oracle_rope_row(y, cos_cache + rope_pos * (ROPE_DIM / 2),
                     sin_cache + rope_pos * (ROPE_DIM / 2), rope_style);
     if (hadamard) oracle_hadamard_row(y);
+    uint8_t* r = rec + t * REC;
+    if (fp8) {
+      int e = fp8_quant_row(y, r);
+      float scale = (float)ldexp(1.0, e - 127);
+      memcpy(r + HEAD_DIM, &scale, 4);
+    } else {
+      oracle_quant_pack_row(y, r, r + PAYLOAD_BYTES, NULL, NULL, NULL);
+    }
+    state[t] = 1;
+  }
+  int status = 0;
+  for (int64_t t = 0; t < num_tokens; ++t) {
+    if (state[t] < 0) status = -1;
+    if (state[t] <= 0) continue;
+    int64_t slot = slot_mapping[t];
     int64_t b = slot / KV_BLOCK, o = slot % KV_BLOCK;
+    const uint8_t* r = rec + t * REC;
     if (fp8) {
       uint8_t* page = kv_cache + b * (int64_t)KV_BLOCK * (HEAD_DIM + 4);
-      int e = fp8_quant_row(y, page + o * HEAD_DIM);
-      float scale = (float)ldexp(1.0, e - 127);
-      memcpy(page + KV_BLOCK * HEAD_DIM + o * 4, &scale, 4);
+      memcpy(page + o * HEAD_DIM, r, HEAD_DIM);
+      memcpy(page + KV_BLOCK * HEAD_DIM + o * 4, r + HEAD_DIM, 4);
       continue;
     }
-    uint8_t payload[PAYLOAD_BYTES], ex[EXP_BYTES];
-    oracle_quant_pack_row(y, payload, ex, NULL, NULL, NULL);
     uint8_t* page = kv_cache + b * PAGE_BYTES;
-    memcpy(page + o * PAYLOAD_BYTES, payload, PAYLOAD_BYTES);
-    memcpy(page + KV_BLOCK * PAYLOAD_BYTES + o * EXP_BYTES, ex, EXP_BYTES);
+    memcpy(page + o * PAYLOAD_BYTES, r, PAYLOAD_BYTES);
+    memcpy(page + KV_BLOCK * PAYLOAD_BYTES + o * EXP_BYTES, r + PAYLOAD_BYTES, EXP_BYTES);
   }
+  free(rec);
+  free(state);
   return status;
 }
 
@@ -336,6 +419,7 @@ static int query_pass(const uint16_t* q, const uint16_t* w,
                       int fp8) {
   int status = 0;
   double wscale = 1.0 / sqrt((double)num_heads * (double)HEAD_DIM);
+#pragma omp parallel for num_threads(g_threads) schedule(dynamic, 16) reduction(min : status)
   for (int64_t t = 0; t < num_tokens; ++t) {
     int64_t pos = positions[t];
     if (pos < 0 || pos >= max_pos) {
@@ -431,7 +515,7 @@ static int fp8_quant_row(const uint16_t* row, uint8_t* codes) {
     if (a > amax) amax = a;
   }
   float t = amax / 448.0f;
-  if (t < STAGE1_FLOOR) t = STAGE1_FLOOR;
+  if (t < FP8_QUOT_FLOOR) t = FP8_QUOT_FLOOR;
   uint32_t bits = f2u(t);
   int e = (int)(bits >> 23) + (int)((bits & 0x7fffffu) != 0u);
   if (e < 1) e = 1;
@@ -504,7 +588,7 @@ void oracle_fake_quant_row(const uint16_t* row, int mode, uint16_t* out) {
   } else {
     for (int g = 0; g < HEAD_DIM / GROUP; ++g) {
       uint8_t nib[GROUP];
-      int e = oracle_quant_group(z + GROUP * g, STAGE1_FLOOR, nib);
+      int e = oracle_quant_group_floors(z + GROUP * g, STAGE1_AMAX_FLOOR, 0.0f, nib);
       for (int i = 0; i < GROUP; ++i) q[GROUP * g + i] = oracle_dequant(nib[i], e);
     }
   }
@@ -517,6 +601,7 @@ int oracle_rope_fake_quant(const uint16_t* x, int64_t rows_per_token,
                            int rope_style, int mode, uint16_t* out,
                            int64_t num_rows) {
   int status = 0;
+#pragma omp parallel for num_threads(g_threads) schedule(dynamic, 256) reduction(min : status)
   for (int64_t r = 0; r < num_rows; ++r) {
     int64_t pos = positions[r / rows_per_token];
     if (pos < 0 || pos >= max_pos) {
@@ -545,6 +630,38 @@ static double dequant_d(uint8_t nibble, int e) {
   return (nibble & 8) ? -v : v;
 }
 
+/* The dequantised key of one 68-byte slot (payload at pg + o*64, exponent
+ * word at pg + 4096 + o*4). */
+static void key_values(const uint8_t* pg, int64_t o, double* kv) {
+  for (int d = 0; d < HEAD_DIM; ++d) {
+    uint8_t kbyte = pg[o * PAYLOAD_BYTES + d / 2];
+    uint8_t knib = (d % 2) ? (kbyte >> 4) : (kbyte & 15);
+    int ke = pg[KV_BLOCK * PAYLOAD_BYTES + o * EXP_BYTES + d / GROUP];
+    kv[d] = dequant_d(knib, ke);
+  }
+}
+
+/* sum_h w[h] * max(0, q_h . k) in fp64 over the H query rows starting at
+ * query row r0 (each product of two E2M1 values with power-of-two scales is
+ * exact in fp64; the sums round in fp64). */
+static double score(const uint8_t* q_fp4, const uint8_t* q_scale, const float* weights,
+                    int64_t r0, int64_t num_heads, const double* kv) {
+  double qv[HEAD_DIM];
+  double acc = 0.0;
+  for (int64_t h = 0; h < num_heads; ++h) {
+    int64_t r = r0 + h;
+    for (int d = 0; d < HEAD_DIM; ++d) {
+      uint8_t qbyte = q_fp4[r * PAYLOAD_BYTES + d / 2];
+      uint8_t qnib = (d % 2) ? (qbyte >> 4) : (qbyte & 15);
+      qv[d] = dequant_d(qnib, q_scale[r * EXP_BYTES + d / GROUP]);
+    }
+    double dot = 0.0;
+    for (int d = 0; d < HEAD_DIM; ++d) dot += qv[d] * kv[d];
+    if (dot > 0.0) acc += (double)weights[r] * dot;
+  }
+  return acc;
+}
+
 int oracle_paged_mqa_logits(const uint8_t* q_fp4, const uint8_t* q_scale,
                             const float* weights, const uint8_t* kv_cache,
                             int64_t num_blocks, const int32_t* block_table,
@@ -554,46 +671,56 @@ int oracle_paged_mqa_logits(const uint8_t* q_fp4, const uint8_t* q_scale,
                             int64_t next_n, int64_t num_heads,
                             int64_t max_context) {
   int status = 0;
-  double kv[HEAD_DIM], qv[HEAD_DIM];
-  for (int64_t b = 0; b < batch; ++b) {
+#pragma omp parallel for num_threads(g_threads) schedule(dynamic, 1) reduction(min : status)
+  for (int64_t t = 0; t < batch * next_n; ++t) {
+    int64_t b = t / next_n;
     int64_t ctx = context_lens[b];
-    for (int64_t j = 0; j < next_n; ++j) {
-      int64_t t = b * next_n + j;
-      for (int64_t s = 0; s < max_context; ++s) {
-        float* out = logits + t * logits_stride + s;
-        if (s >= ctx) {
-          *out = -INFINITY;
-          continue;
-        }
-        int64_t page = block_table[b * block_table_stride + s / KV_BLOCK];
-        if (page < 0 || page >= num_blocks) {
-          *out = -INFINITY;
-          status = -1;
-          continue;
-        }
-        const uint8_t* pg = kv_cache + page * PAGE_BYTES;
-        int64_t o = s % KV_BLOCK;
-        for (int d = 0; d < HEAD_DIM; ++d) {
-          uint8_t kbyte = pg[o * PAYLOAD_BYTES + d / 2];
-          uint8_t knib = (d % 2) ? (kbyte >> 4) : (kbyte & 15);
-          int ke = pg[KV_BLOCK * PAYLOAD_BYTES + o * EXP_BYTES + d / GROUP];
-          kv[d] = dequant_d(knib, ke);
-        }
-        double acc = 0.0;
-        for (int64_t h = 0; h < num_heads; ++h) {
-          int64_t r = t * num_heads + h;
-          for (int d = 0; d < HEAD_DIM; ++d) {
-            uint8_t qbyte = q_fp4[r * PAYLOAD_BYTES + d / 2];
-            uint8_t qnib = (d % 2) ? (qbyte >> 4) : (qbyte & 15);
-            qv[d] = dequant_d(qnib, q_scale[r * EXP_BYTES + d / GROUP]);
-          }
-          double dot = 0.0;
-          for (int d = 0; d < HEAD_DIM; ++d) dot += qv[d] * kv[d];
-          if (dot > 0.0) acc += (double)weights[r] * dot;
-        }
-        *out = (float)acc;
+    double kv[HEAD_DIM];
+    for (int64_t s = 0; s < max_context; ++s) {
+      float* out = logits + t * logits_stride + s;
+      if (s >= ctx) {
+        *out = -INFINITY;
+        continue;
       }
+      int64_t page = block_table[b * block_table_stride + s / KV_BLOCK];
+      if (page < 0 || page >= num_blocks) {
+        *out = -INFINITY;
+        status = -1;
+        continue;
+      }
+      int64_t o = s % KV_BLOCK;
+      key_values(kv_cache + page * PAGE_BYTES, o, kv);
+      *out = (float)score(q_fp4, q_scale, weights, t * num_heads, num_heads, kv);
     }
   }
   return status;
+}
+
+/* The prefill variant of the scorer ([aiter] Summary: the FP4 paged scorer
+ * "and its prefill variant" read the packed keys straight out of the
+ * cache).  Readings (pages silent on its arguments): the keys of the
+ * prefill chunk are consecutive -- key s sits in page s/64 at offset s%64,
+ * which is what the key op writes with slot_mapping[s] = s -- so there is
+ * no block table; query token t scores the keys s with ks[t] <= s < ke[t];
+ * every other column of [0, num_keys) is -inf.  The score is the decode
+ * scorer's: sum_h w * max(0, q . k). */
+int oracle_mqa_logits_prefill(const uint8_t* q_fp4, const uint8_t* q_scale,
+                              const float* weights, const uint8_t* kv_cache,
+                              int64_t num_keys, const int32_t* ks, const int32_t* ke,
+                              float* logits, int64_t logits_stride, int64_t num_tokens,
+                              int64_t num_heads) {
+#pragma omp parallel for num_threads(g_threads) schedule(dynamic, 1)
+  for (int64_t t = 0; t < num_tokens; ++t) {
+    double kv[HEAD_DIM];
+    for (int64_t s = 0; s < num_keys; ++s) {
+      float* out = logits + t * logits_stride + s;
+      if (s < ks[t] || s >= ke[t]) {
+        *out = -INFINITY;
+        continue;
+      }
+      key_values(kv_cache + (s / KV_BLOCK) * PAGE_BYTES, s % KV_BLOCK, kv);
+      *out = (float)score(q_fp4, q_scale, weights, t * num_heads, num_heads, kv);
+    }
+  }
+  return 0;
 }

@@ -52,6 +52,12 @@ void oracle_rope_row(uint16_t* y, const float* cos_row, const float* sin_row,
  * biased UE8M0 exponent. */
 int oracle_quant_group(const float* z, float floor_, uint8_t* nibbles);
 
+/* The same with a floor on the amax (before the division by 6) and one on
+ * the quotient (after it); 0 means no floor.  Stage 1 of the pre-pass uses
+ * the amax floor, stage 2 the quotient floor. */
+int oracle_quant_group_floors(const float* z, float amax_floor, float quot_floor,
+                              uint8_t* nibbles);
+
 /* Dequantise a nibble with biased exponent e (exact in fp32). */
 float oracle_dequant(uint8_t nibble, int e);
 
@@ -62,6 +68,13 @@ float oracle_dequant(uint8_t nibble, int e);
 void oracle_quant_pack_row(const uint16_t* row, uint8_t* payload64,
                            uint8_t* exp4, int* stage1_e, int* stage2_e,
                            uint8_t* stage1_nibbles);
+
+/* The pack with explicit floors: stage-1 amax and quotient floors, stage-2
+ * amax and quotient floors (the pre-pass: 2^-126, 0, 0, 2^-126). */
+void oracle_quant_pack_row_floors(const uint16_t* row, float s1_amax, float s1_quot,
+                                  float s2_amax, float s2_quot, uint8_t* payload64,
+                                  uint8_t* exp4, int* stage1_e, int* stage2_e,
+                                  uint8_t* stage1_nibbles);
 
 /* ---- the two operations of the pre-pass ---- */
 
@@ -180,6 +193,23 @@ int oracle_paged_mqa_logits(const uint8_t* q_fp4, const uint8_t* q_scale,
                             int64_t logits_stride, int64_t batch,
                             int64_t next_n, int64_t num_heads,
                             int64_t max_context);
+
+/* Prefill scorer: query token t (rows t*H .. t*H+H-1 of q_fp4/q_scale,
+ * weights[t, :]) against the consecutive keys s = 0 .. num_keys-1 (page
+ * s/64, offset s%64 of kv_cache [>= ceil(num_keys/64), 4352]):
+ * logits[t*logits_stride + s] = sum_h w * max(0, q . k_s) for
+ * ks[t] <= s < ke[t], -inf for the other s < num_keys.  Returns 0. */
+int oracle_mqa_logits_prefill(const uint8_t* q_fp4, const uint8_t* q_scale,
+                              const float* weights, const uint8_t* kv_cache,
+                              int64_t num_keys, const int32_t* ks, const int32_t* ke,
+                              float* logits, int64_t logits_stride, int64_t num_tokens,
+                              int64_t num_heads);
+
+/* Host threads used by the token / row loops (default 1), and the number
+ * the machine offers (1 when built without OpenMP). */
+void oracle_set_threads(int n);
+int oracle_get_threads(void);
+int oracle_threads_available(void);
 
 #ifdef __cplusplus
 }

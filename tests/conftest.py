@@ -12,6 +12,11 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built libfp4idx.so")
     config.addinivalue_line("markers", "slow: long-running CPU test")
     config.addinivalue_line("markers", "fake_ptr: passes fake device pointers that host checks must reject")
+    config.addinivalue_line(
+        "markers",
+        "floor_reading: some compared bytes (all-zero or subnormal groups) are decided by the "
+        "scale-floor reading, a value the pages do not print; tests/test_oracle_floors.py shows "
+        "which floors give the same bytes")
 
 
 def pytest_collection_modifyitems(config, items):

@@ -8,6 +8,7 @@ import pytest
 import oracle
 from tests import test_oracle_pins as pins
 from tests import test_oracle_fake_quant as qpins
+from tests import test_oracle_floors as flpins
 from tests import test_oracle_fp8 as fpins
 from tests import test_oracle_variants as vpins
 from tests import test_scorer_oracle as spins
@@ -22,9 +23,11 @@ MUTANTS = [
      "(uint8_t)(n2[2 * j + 1] | (n2[2 * j] << 4))"),
     ("exponent_floor_not_ceil", "+ ((bits & 0x7fffffu) != 0u ? 1 : 0)", "+ 0"),
     ("amax_over_4", "float t = amax / 6.0f;", "float t = amax / 4.0f;"),
-    ("large_floor", "STAGE1_FLOOR = 1.17549435082228750797e-38f",
-     "STAGE1_FLOOR = 1e-10f"),
-    ("single_stage", "int e2 = oracle_quant_group(u, STAGE2_FLOOR, n2);",
+    ("large_stage1_amax_floor", "STAGE1_AMAX_FLOOR = 1.17549435082228750797e-38f",
+     "STAGE1_AMAX_FLOOR = 1e-10f"),
+    ("large_stage2_quotient_floor", "STAGE2_QUOT_FLOOR = 1.17549435082228750797e-38f",
+     "STAGE2_QUOT_FLOOR = 1e-10f"),
+    ("single_stage", "int e2 = oracle_quant_group_floors(u, s2_amax, s2_quot, n2);",
      "int e2 = e1; memcpy(n2, n1, GROUP);"),
     ("scale_bias_off_by_one", "double scale = ldexp(1.0, e - 127);",
      "double scale = ldexp(1.0, e - 128);"),
@@ -42,10 +45,10 @@ MUTANTS = [
     ("rope_interleaved_table_index", "float c = cos_row[i];",
      "float c = cos_row[rope_style == ORACLE_ROPE_NEOX ? i : (2 * i) % 32];"),
     ("slot_record_interleaved",
-     "memcpy(page + o * PAYLOAD_BYTES, payload, PAYLOAD_BYTES);\n"
-     "    memcpy(page + KV_BLOCK * PAYLOAD_BYTES + o * EXP_BYTES, ex, EXP_BYTES);",
-     "memcpy(page + o * 68, payload, PAYLOAD_BYTES);\n"
-     "    memcpy(page + o * 68 + PAYLOAD_BYTES, ex, EXP_BYTES);"),
+     "memcpy(page + o * PAYLOAD_BYTES, r, PAYLOAD_BYTES);\n"
+     "    memcpy(page + KV_BLOCK * PAYLOAD_BYTES + o * EXP_BYTES, r + PAYLOAD_BYTES, EXP_BYTES);",
+     "memcpy(page + o * 68, r, PAYLOAD_BYTES);\n"
+     "    memcpy(page + o * 68 + PAYLOAD_BYTES, r + PAYLOAD_BYTES, EXP_BYTES);"),
     ("slot_zero_skipped", "if (slot < 0) continue;", "if (slot <= 0) continue;"),
     ("weights_scale_no_sqrt_of_heads",
      "double wscale = 1.0 / sqrt((double)num_heads * (double)HEAD_DIM);",
@@ -59,16 +62,16 @@ MUTANTS = [
      "acc += (double)weights[r] * dot;"),
     ("scorer_weight_dropped", "if (dot > 0.0) acc += (double)weights[r] * dot;",
      "if (dot > 0.0) acc += dot;"),
-    ("scorer_slot_offset_off_by_one", "int64_t o = s % KV_BLOCK;\n        for (int d",
-     "int64_t o = (s + 1) % KV_BLOCK;\n        for (int d"),
+    ("scorer_slot_offset_off_by_one", "int64_t o = s % KV_BLOCK;\n      key_values(",
+     "int64_t o = (s + 1) % KV_BLOCK;\n      key_values("),
     ("scorer_key_group_exponent", "int ke = pg[KV_BLOCK * PAYLOAD_BYTES + o * EXP_BYTES + d / GROUP];",
      "int ke = pg[KV_BLOCK * PAYLOAD_BYTES + o * EXP_BYTES + (d / GROUP + 1) % 4];"),
     ("scorer_key_nibble_swap", "uint8_t knib = (d % 2) ? (kbyte >> 4) : (kbyte & 15);",
      "uint8_t knib = (d % 2) ? (kbyte & 15) : (kbyte >> 4);"),
     ("scorer_query_exponent_bias", "qv[d] = dequant_d(qnib, q_scale[r * EXP_BYTES + d / GROUP]);",
      "qv[d] = dequant_d(qnib, q_scale[r * EXP_BYTES + d / GROUP] + 1);"),
-    ("scorer_padding_zero", "        if (s >= ctx) {\n          *out = -INFINITY;",
-     "        if (s >= ctx) {\n          *out = 0.0f;"),
+    ("scorer_padding_zero", "      if (s >= ctx) {\n        *out = -INFINITY;",
+     "      if (s >= ctx) {\n        *out = 0.0f;"),
     ("k_rope_skipped",
      "    oracle_rope_row(y, cos_cache + rope_pos * (ROPE_DIM / 2),\n"
      "                    sin_cache + rope_pos * (ROPE_DIM / 2), rope_style);\n", ""),
@@ -83,8 +86,8 @@ MUTANTS = [
      "int64_t rope_pos = pos / compress_ratio;"),
     ("compress_ignored", "int64_t rope_pos = pos - pos % compress_ratio;",
      "int64_t rope_pos = pos;"),
-    ("k_hadamard_skipped", "    if (hadamard) oracle_hadamard_row(y);\n    int64_t b = slot",
-     "    int64_t b = slot"),
+    ("k_hadamard_skipped", "    if (hadamard) oracle_hadamard_row(y);\n    uint8_t* r = rec",
+     "    uint8_t* r = rec"),
     ("fp8_max_240", "float t = amax / 448.0f;", "float t = amax / 240.0f;"),
     ("fp8_scale_floor_not_ceil", "+ (int)((bits & 0x7fffffu) != 0u);", "+ 0;"),
     ("fp8_ties_down", "if (d < best_d || (d == best_d && (c % 2) == 0 && (best % 2) != 0)) {",
@@ -94,8 +97,8 @@ MUTANTS = [
     ("fp8_weight_scale_not_folded",
      "folded = ldexp(1.0, fp8_quant_row(y, q_out + r * HEAD_DIM) - 127);",
      "fp8_quant_row(y, q_out + r * HEAD_DIM);"),
-    ("fp8_scale_slot_interleaved", "memcpy(page + KV_BLOCK * HEAD_DIM + o * 4, &scale, 4);",
-     "memcpy(page + KV_BLOCK * HEAD_DIM + (63 - o) * 4, &scale, 4);"),
+    ("fp8_scale_slot_interleaved", "memcpy(page + KV_BLOCK * HEAD_DIM + o * 4, r + HEAD_DIM, 4);",
+     "memcpy(page + KV_BLOCK * HEAD_DIM + (63 - o) * 4, r + HEAD_DIM, 4);"),
     ("fq16_amax_over_4", "float t16 = amax16 / 6.0f;", "float t16 = amax16 / 4.0f;"),
     ("fq16_scale_not_e4m3", "float sc = oracle_e4m3_to_f32(oracle_f32_to_e4m3(t16));",
      "float sc = t16;"),
@@ -106,6 +109,10 @@ MUTANTS = [
      "    oracle_rope_row(y, cos_cache + pos * (ROPE_DIM / 2),\n"
      "                    sin_cache + pos * (ROPE_DIM / 2), rope_style);\n"
      "    oracle_fake_quant_row", "    oracle_fake_quant_row"),
+    ("prefill_range_end_inclusive", "if (s < ks[t] || s >= ke[t]) {",
+     "if (s < ks[t] || s > ke[t]) {"),
+    ("prefill_key_page_shifted", "key_values(kv_cache + (s / KV_BLOCK) * PAGE_BYTES, s % KV_BLOCK, kv);",
+     "key_values(kv_cache + ((s + 64) / KV_BLOCK % 2) * PAGE_BYTES, s % KV_BLOCK, kv);"),
     ("q_hadamard_skipped", "      if (hadamard) oracle_hadamard_row(y);\n      double folded",
      "      double folded"),
 ]
@@ -133,6 +140,9 @@ PINS = [
     spins.test_page_indirection_and_sequences,
     spins.test_bad_page_reported,
     spins.test_random_case_exact_rational,
+    spins.test_prefill_single_element_closed_form,
+    spins.test_prefill_ranges_and_exact_values,
+    flpins.test_tiny_groups_two_stage_exact,
     vpins.test_hadamard_one_hot_rows,
     vpins.test_hadamard_small_integers_exact,
     vpins.test_query_rotation_sign_pattern,

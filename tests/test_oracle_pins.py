@@ -473,6 +473,7 @@ def test_weights_closed_form():
             assert np.all(ulp_diff_f32(wt.ravel(), want.astype(np.float32)) == 0)
 
 
+@pytest.mark.floor_reading
 def test_oracle_tiny_digest():
     """Drift guard: the oracle's Tiny outputs hash to the committed digest
     written by tests/golden/make_oracle_digest.py (which calls only the

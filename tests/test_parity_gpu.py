@@ -18,7 +18,9 @@ MODES = ["fused", "separate"]
 
 
 @pytest.mark.parametrize("mode", MODES)
-@pytest.mark.parametrize("name", ["tiny", "tiny_gamma1", "decode", "mtp", "prefill"])
+@pytest.mark.parametrize("name", [pytest.param("tiny", marks=pytest.mark.floor_reading),
+                                  pytest.param("tiny_gamma1", marks=pytest.mark.floor_reading),
+                                  "decode", "mtp", "prefill"])
 def test_config_parity(name, mode):
     w = wl.make(name)
     dw = DeviceWorkload(w)
@@ -115,6 +117,7 @@ def test_ragged_shapes(T, H, style):
 @pytest.mark.parametrize("style", [wl.ROPE_NEOX, wl.ROPE_INTERLEAVED])
 @pytest.mark.parametrize("rows", [1, 5, 64, 300])
 @pytest.mark.parametrize("scale", [1.0, 40.0, 1e-3])
+@pytest.mark.floor_reading
 def test_row_scale_grid(rows, scale, style):
     """Rows x input scales with an all-zero row, a subnormal row and an exact
     half-way row mixed in (the byte-comparison grid of the sglang PR's

@@ -161,3 +161,63 @@ def test_random_case_exact_rational():
         got = out[t, s]
         assert abs(int(np.float32(got).view(np.int32)) - int(want.view(np.int32))) <= 1, (t, s)
     assert np.all(np.isneginf(out[2:, ctx - 9:]))
+
+
+# ----------------------------------------------------------------- prefill
+def exact_logit(q, qs, w, cache, t, page, o):
+    """sum_h w * max(0, q . k) by exact rationals, rounded once to fp32."""
+    kv = []
+    for d in range(128):
+        byte = int(cache[page, o * 64 + d // 2])
+        nib = byte >> 4 if d % 2 else byte & 15
+        kv.append(value(nib, int(cache[page, 4096 + 4 * o + d // 32])))
+    acc = Fr(0)
+    for h in range(q.shape[1]):
+        dot = Fr(0)
+        for d in range(128):
+            byte = int(q[t, h, d // 2])
+            nib = byte >> 4 if d % 2 else byte & 15
+            dot += value(nib, int(qs[t, h, d // 32])) * kv[d]
+        if dot > 0:
+            acc += Fr(float(w[t, h])) * dot
+    return np.float32(float(acc))
+
+
+def test_prefill_ranges_and_exact_values():
+    """The prefill scorer: token t scores the consecutive keys s in
+    [ks[t], ke[t]) (key s in page s/64 at offset s%64), -inf elsewhere;
+    sampled logits equal the exact rational value (within 1 ulp)."""
+    rng = np.random.Generator(np.random.PCG64(44))
+    T, H, nk = 6, 3, 150
+    cache = rng.integers(0, 256, (3, 4352), dtype=np.uint8)
+    cache[:, 4096:] = rng.integers(118, 137, (3, 256), dtype=np.uint8)
+    q = rng.integers(0, 256, (T, H, 64), dtype=np.uint8)
+    qs = rng.integers(118, 137, (T, H, 4), dtype=np.uint8)
+    w = rng.standard_normal((T, H)).astype(np.float32)
+    ks = np.array([0, 10, 64, 149, 30, 5], np.int32)
+    ke = np.array([150, 11, 128, 150, 30, 2], np.int32)   # t=4, t=5: empty ranges
+    out, st = oracle.mqa_logits_prefill(q, qs, w, cache, ks, ke, nk)
+    assert st == 0 and out.shape == (T, nk)
+    for t in range(T):
+        inside = (np.arange(nk) >= ks[t]) & (np.arange(nk) < ke[t])
+        assert np.all(np.isneginf(out[t, ~inside])) and np.all(np.isfinite(out[t, inside]))
+    for (t, s) in [(0, 0), (0, 149), (1, 10), (2, 64), (2, 127), (3, 149), (0, 65)]:
+        want = exact_logit(q, qs, w, cache, t, s // 64, s % 64)
+        got = np.float32(out[t, s])
+        assert abs(int(got.view(np.int32)) - int(want.view(np.int32))) <= 1, (t, s)
+
+
+def test_prefill_single_element_closed_form():
+    """q = 1.0 at dim 9 for one head of weight 2; key 70 (page 1, offset 6)
+    holds 1.5 * 2^2 = 6 at dim 9, key 71 holds -6: logits 12 and 0."""
+    qp, qe = one_hot(9, 2)
+    kp, ke_ = one_hot(9, 3, 129)
+    kn, _ = one_hot(9, 3 | 8, 129)
+    cache = np.zeros((2, 4352), np.uint8)
+    put_slot(cache, 70, kp, ke_)
+    put_slot(cache, 71, kn, ke_)
+    out, _ = oracle.mqa_logits_prefill(qp[None, None], qe[None, None],
+                                       np.array([[2.0]], np.float32), cache,
+                                       np.array([70], np.int32), np.array([72], np.int32), 80)
+    assert out[0, 70] == 12.0 and out[0, 71] == 0.0
+    assert np.all(np.isneginf(out[0, :70])) and np.all(np.isneginf(out[0, 72:]))

@@ -38,6 +38,7 @@ def test_stream_ragged(T, H, style, hadamard):
 @pytest.mark.parametrize("hadamard", [False, True], ids=["plain", "rotated"])
 @pytest.mark.parametrize("style", STYLES)
 @pytest.mark.parametrize("scale", [1.0, 40.0, 1e-3, 3e4])
+@pytest.mark.floor_reading
 def test_stream_special_rows(style, scale, hadamard):
     """All-zero, subnormal and exact-midpoint query rows on even and odd rows
     of a unit (the two part orders), with the keys of the same tokens."""
@@ -153,6 +154,7 @@ def test_stream_fp8_ragged(T, H, style, hadamard):
 
 @pytest.mark.parametrize("style", STYLES)
 @pytest.mark.parametrize("scale", [1.0, 1e-3, 3e4])
+@pytest.mark.floor_reading
 def test_stream_fp8_special_rows(style, scale):
     """FP8 rows at the scale's edges on both row parities: all-zero and
     subnormal rows (the 2^-126 floor), and query rows whose amax/448 is an
