@@ -1,149 +1,157 @@
-// fp4idx_scorer.cu -- FP4 paged MQA-logits scorer on the block-scaled FP4
-// tensor cores of sm_103a (tcgen05.mma kind::mxf4).  It consumes the bytes
-// the pre-pass writes: packed E2M1 queries with their per-32 UE8M0 exponent
-// words, and the paged 68-byte index-K slots.  The operation and the argument
-// contract are in include/fp4idx.h.
+// fp4idx_scorer.cu -- FP4 MQA-logits scorers on the block-scaled FP4 tensor
+// cores of sm_103a (tcgen05.mma kind::mxf4): the paged decode scorer and its
+// prefill variant.  They consume the bytes the pre-pass writes: packed E2M1
+// queries with their per-32 UE8M0 exponent words, and the 68-byte index-K
+// slots of the paged cache.  The operations and argument contracts are in
+// include/fp4idx.h.
 //
 // Sources (web pages, by title and section):
 //   "[HIP] Add FP4 output mode to indexer_qk_rope_quant_and_cache" (aiter PR
-//   5484), Verification: the paged FP4 MQA-logits scorer reads the packed
-//   E2M1 keys and their e8m0 block exponents straight from the paged cache,
-//   at GLM-5.2 shapes (H = 32, D = 128, kv_block = 64) with next_n 1 and 4.
+//   5484), Summary and Verification: the paged FP4 MQA-logits scorer "and its
+//   prefill variant" read the packed E2M1 keys and their e8m0 exponents
+//   straight out of the cache; GLM-5.2 shapes (H = 32, D = 128, kv_block =
+//   64), next_n 1 and 4.
 //   "[ROCm][Perf] Enabled FP4Indexer for DSV4" (vLLM PR 42908), Code Review:
 //   the score of a key is the block-scaled E2M1 dot product with each query
 //   head, through ReLU, times the head weight, summed over the heads.
 //   "dsv4.1: RoPE and FP4 packing kernels" (sglang PR 39656), Summary: the
 //   68-byte slot (64 payload bytes + 4 exponent bytes).
 //
-// Work.  A tile is 128 consecutive tokens (two 64-slot pages) of one
-// sequence; only tiles holding a token below the sequence's context are
-// work.  The persistent grid splits the list of all work tiles (sequence by
-// sequence) into equal contiguous shares, one per CTA, from the context
-// lengths alone; a CTA's share may span several sequences ("segments").
-// Logits of tiles past the context are -inf, written in a final phase.
+// Work.  A segment is a set of query rows sharing one key range: a sequence
+// (next_n tokens) in the decode scorer, a block of consecutive query tokens
+// in the prefill scorer; R = tokens x H rows (R <= 256) form the MMA's N.  A
+// tile is 128 consecutive keys (two 64-slot pages) of a segment's range.
+// The persistent grid splits the list of all (segment, tile) work items into
+// equal contiguous shares, one per CTA, from the context lengths / key ranges
+// alone; a share may span several segments.  Columns outside the ranges
+// (-inf) are split the same way and written alongside by one warp.
 //
-// MMA.  Keys are A (M = 128 tokens), the sequence's R = next_n * H query rows
-// are B (N = R), K = 128 as two MMAs of K = 64.  Each exponent word of a slot
-// is exactly one TMEM scale-factor cell: group g sits in byte g; the MMA over
-// groups {0,1} takes bytes 0-1 (scale-factor id 0), the one over {2,3} bytes
-// 2-3 (id 2).  Row r's cell is TMEM column base + r/32; the key side reads
-// lane r, the query side lane r%32 (written to every lane quadrant).
+// MMA.  Keys are A (M = 128), the segment's query rows B (N = R), K = 128 as
+// two MMAs of K = 64 into an fp32 TMEM accumulator.  Each exponent word of a
+// slot is exactly one TMEM scale-factor cell (group g in byte g; the K halves
+// use bytes 0-1 and 2-3).
 //
-// Roles (17 + P warps, P = kProducers producer warps).
-//   producers (warps 16 .. 16+P-1): TMA tensor copies of the page payloads
-//     (64 tokens x 64 bytes, in the 64-byte swizzled layout the MMA reads)
-//     and bulk copies of the exponent words into a ring of S stages;
-//     producer i issues tiles i, i+P, ...; each warp fetches the page ids
-//     of 16 of its tiles per load, one batch ahead;
-//   MMA issuer (warp 16+P): per tile it waits for the data and for a free
-//     accumulator, stages the keys' exponent words (and, at the first tile
-//     of a segment, the segment's query operand and query scale words) in
-//     shared memory as a 32 x 128-bit transpose, and lane 0 issues
-//     tcgen05.cp of those words into the scale-factor columns of TMEM, the
-//     two MMAs into accumulator k % 3 and the commits -- all in order in
-//     the tensor pipe, so no thread waits for the copies;
-//   two epilogue groups of 8 warps (0-7, 8-15), group e owning the tiles k
-//     with k % 2 == e.  Warps q and q+4 of a group share TMEM lane quadrant q
-//     and split the accumulator's 32-column chunks.  Per tile a warp reads
-//     its chunks one at a time (thread = token = TMEM lane), releases the
-//     accumulator (acc_empty) and stores sum_h w * max(D, 0) per query
-//     token; a page's validity comes from the block table, fetched a tile
-//     ahead.  Each warp holds its own copy of the segment's head weights.
-// Every wait is bounded (1 s) and a shared abort flag stops every role; in
-// flight copies and MMAs are waited for before TMEM and shared memory are
-// released.  Each E2M1 product is exact; the tensor core accumulates in fp32.
+// Roles (20 warps, five per SM sub-partition, so 96 registers a thread).
+// Every role keeps its per-tile chain short: the tile rate of a
+// one-CTA-per-SM pipeline is set by the longest serial chain of dependent
+// instructions in any one warp, not by the copy latency.
+//   warps 2-3    producers: tile k belongs to producer k % 2.  Lane 0 waits
+//                for the stage (and at a segment start issues the TMA copy of
+//                the segment's query operand); lanes 0 and 1 then issue, one
+//                page each, the TMA tensor copies of the page payloads
+//                (64-byte swizzled, the layout the MMA reads) and bulk copies
+//                of their exponent words.  The warp fetches the page ids of
+//                16 of its tiles per load, a batch ahead.  While it waits for
+//                free stages it writes this CTA's share of the -inf columns
+//                outside every segment's range.
+//   warps 0-1    issuers: tile k belongs to issuer k % 2.  Once a tile has
+//                landed, the warp transposes its 128 exponent words (and at
+//                its first tile of a segment the queries' words) into the
+//                32 x 128-bit blocks tcgen05.cp reads; lane 0 then issues
+//                tcgen05.cp into TMEM, the two MMAs into accumulator k % A
+//                and the commit.
+//   warps 4-19   epilogue: warp w reads TMEM lane quadrant w % 4 (tokens
+//                32(w%4) .. +31, one per thread) and a fixed run of the
+//                accumulator's 32-column chunks, chosen so that a query
+//                token's heads never span two warps; every warp takes every
+//                tile, so a tile's read-out is spread over all 16 warps.
+//                Warp 4 frees a tile's stage (and at a segment's last tile its
+//                query buffer) once the tile's MMAs have completed.
+// Every wait is bounded (1 s) and a shared abort flag stops every role;
+// copies and MMAs in flight are waited for before TMEM and shared memory are
+// released.  Each E2M1 product is exact; the tensor core accumulates in
+// fp32, and the weighted head sum is fp32.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "fp4idx.h"
 
 namespace {
 
-constexpr int kEpiWarps = 16;                // two groups of eight
-constexpr int kGroupWarps = 8;
-#ifndef FP4IDX_SCORER_PRODUCERS
-#define FP4IDX_SCORER_PRODUCERS 1
-#endif
-constexpr int kProducers = FP4IDX_SCORER_PRODUCERS;  // producer warps
-constexpr int kProducerWarp = 16;                    // the first of them
-constexpr int kMmaWarp = kProducerWarp + kProducers;
-constexpr int kThreads = (kMmaWarp + 1) * 32;
-constexpr int kMaxNext = 4;                  // next_n <= kMaxRows / 32
-constexpr int kAccs = 3;                     // TMEM accumulators (tile k: k % 3)
-constexpr int kQBufs = 4;                    // query operands (segment g: g % 4)
-constexpr int kTile = 128;                   // key tokens per tile (MMA M)
+// Warp roles.  The warps on a tile's critical chains (issuers, producers)
+// take the lowest warp ids: among ready warps the schedulers favour the
+// oldest, so the epilogue's bulk work does not delay them.
+constexpr int kIssuers = 2;
+constexpr int kIssuerWarp = 0;                            // warps 0-1
+constexpr int kProducers = 2;
+constexpr int kProducerWarp = kIssuerWarp + kIssuers;     // warps 2-3
+constexpr int kEpiWarp = kProducerWarp + kProducers;      // warps 4-19
+constexpr int kEpiWarps = 16;
+constexpr int kWarps = kEpiWarp + kEpiWarps;              // 20: five per SM sub-partition
+constexpr int kThreads = kWarps * 32;                    // 640
+constexpr int kTile = 128;                               // keys per tile (MMA M)
 constexpr int kKvBlock = FP4IDX_KV_BLOCK;
 constexpr int kPageBytes = FP4IDX_PAGE_BYTES;
 constexpr int kPayloadBytes = kKvBlock * FP4IDX_SLOT_PAYLOAD_BYTES;  // 4096
 constexpr int kExpBytes = kKvBlock * FP4IDX_SLOT_EXP_BYTES;          // 256
-constexpr int kStageA = 2 * kPayloadBytes;                           // 8192
-constexpr int kStageE = 2 * kExpBytes;                               // 512
-constexpr int kMaxRows = 128;                // query rows per sequence (MMA N)
+constexpr int kMaxRows = 128;                  // query rows per segment (MMA N)
+constexpr int kMaxChunks = kMaxRows / 32;
+constexpr int kMaxAccs = 3;                    // TMEM accumulators
+constexpr int kQBufs = 4;                      // query operand buffers
 constexpr int kMaxStages = 16;
+constexpr int kSegTab = 512;                   // segment ranges kept in shared memory
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSfCols = 8;                // TMEM columns per scale-word slot
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
+// Offsets inside a stage.
+constexpr uint32_t kStPayload = 0;             // 2 x 4096, swizzled payloads
+constexpr uint32_t kStExp = 2 * kPayloadBytes; // 2 x 256 exponent words
+constexpr uint32_t kStSfa = kStExp + 2 * kExpBytes;  // 512: keys' words, transposed
+constexpr uint32_t kStSfb = kStSfa + 512;      // 512: queries' words
+constexpr uint32_t kStageBytes = kStSfb + 512; // 9728, a multiple of the 512-byte swizzle span
+
+enum { kModeDecode = 0, kModePrefill = 1 };
+
 struct ScorerParams {
-  const uint8_t* q_fp4;
   const uint8_t* q_scale;
   const float* weights;
   const uint8_t* cache;
-  const int32_t* block_table;
-  const int32_t* ctx_lens;
+  const int32_t* block_table;  // decode
+  const int32_t* ctx_lens;     // decode
+  const int32_t* ks;           // prefill
+  const int32_t* ke;           // prefill
   float* logits;
   uint32_t* err;
   int64_t num_blocks;
   int64_t bt_stride;
   int64_t logits_stride;
-  int32_t batch;
-  int32_t next_n;
+  int32_t mode;
+  int32_t nseg;         // segments
+  int32_t tps;          // query tokens per segment (at most; R = tps * H <= 128)
+  int32_t next_n;       // decode: query tokens per sequence
+  int32_t ngroups;      // decode: segments per sequence, ceil(next_n / tps)
+  int32_t num_q;        // query tokens
   int32_t H;
-  int32_t R;
-  int32_t max_context;
-  int32_t tiles_total;     // ceil(max_context / 128) tiles per sequence
+  int32_t R;            // tps * H
+  int32_t ncols;        // logits columns (decode max_context, prefill key count)
+  int32_t tiles_total;  // ceil(ncols / 128)
   int32_t stages;
-  uint32_t tmem_cols;      // power of two >= 3R + 40
+  int32_t cpw;          // accumulator chunks per epilogue warp
 };
 
-// Shared-memory carve-up (offsets from a 1024-byte aligned base).
 struct Layout {
-  uint32_t a, q, e, w, x, sf, bars, ok, misc, scan, total;
+  uint32_t q, w, tab, bars, misc, total;
 };
-
-// Barrier indices: full[S], empty[S], then the ones below.
-__host__ __device__ inline int bar_full(int s) { return s; }
-__host__ __device__ inline int bar_empty(int S, int s) { return S + s; }
-// acc_full[k % 6]: the MMAs of tile k are complete.  Tile k uses accumulator
-// k % 3 and belongs to group k % 2, so each of the six barriers is waited on
-// by one group only, one phase after another.
-__host__ __device__ inline int bar_accf(int S, int k6) { return 2 * S + k6; }
-// acc_empty[a]: the group that read accumulator a has its values (8 arrivals).
-__host__ __device__ inline int bar_acce(int S, int a) { return 2 * S + 6 + a; }
-// Partial-sum hand-off between the two warps of a lane quadrant (group e,
-// quadrant q, buffer b), used when a query token's heads span both halves.
-__host__ __device__ inline int bar_xch(int S, int e, int q, int b) {
-  return 2 * S + 9 + (e * 4 + q) * 2 + b;
-}
-constexpr int kExtraBars = 6 + 3 + 16;
 
 __host__ __device__ inline Layout make_layout(int S, int R) {
   Layout L;
-  L.a = 0;                                     // S x 8192, swizzled payloads
-  L.q = L.a + (uint32_t)S * kStageA;           // 4 x R x 64, swizzled queries
-  L.e = L.q + (uint32_t)kQBufs * R * 64;       // S x 512 exponent words
-  L.w = L.e + (uint32_t)S * kStageE;           // 16 epilogue warps x R weights
-  L.x = L.w + (uint32_t)kEpiWarps * R * 4;     // partial sums: 2 groups x 2 x next_n x 128
-  L.sf = L.x + 2u * 2u * kMaxNext * kTile * 4u;  // scale-word copy sources
-  L.bars = L.sf + (uint32_t)(kAccs + kQBufs) * 512u;  // 2S + extra mbarriers
-  L.ok = L.bars + 8u * (uint32_t)(2 * S + kExtraBars);
-  L.misc = L.ok;                               // tmem base, abort, b/t/n start
-  L.scan = L.misc + 32;                        // kThreads + 1 partial sums (int64)
-  L.total = L.scan + 8u * (kThreads + 1);
+  L.q = (uint32_t)S * kStageBytes;                  // kQBufs x R x 64 swizzled queries
+  L.w = L.q + (uint32_t)kQBufs * R * 64;            // 4 quads x 4 chunks x 32 weights
+  L.tab = L.w + 4u * kMaxChunks * 32u * 4u;         // kSegTab x (lo, hi, lim)
+  L.bars = L.tab + (uint32_t)kSegTab * 12u;         // 2S + 2 x 3 + 2 x 4 mbarriers
+  L.misc = L.bars + 8u * (uint32_t)(2 * S + 2 * kMaxAccs + 8);
+  L.total = L.misc + 64u;
   return L;
 }
 
+
+// ---------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -194,6 +202,38 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                       uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                       uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // Shared-memory matrix descriptor of a K-major operand in the 64-byte
 // swizzled layout: rows of 64 bytes, 8-row groups 512 bytes apart.
 __device__ __forceinline__ uint64_t sw64_desc(uint32_t addr) {
@@ -203,11 +243,6 @@ __device__ __forceinline__ uint64_t sw64_desc(uint32_t addr) {
   d |= (uint64_t)1 << 46;                  // descriptor version
   d |= (uint64_t)4 << 61;                  // 64-byte swizzle
   return d;
-}
-
-// Byte offset of 16-byte chunk c of row r in the 64-byte swizzled layout.
-__device__ __forceinline__ uint32_t sw64_chunk(int r, int c) {
-  return (uint32_t)(r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
 }
 
 // Instruction descriptor of kind::mxf4: E2M1 A and B, UE8M0 scales, both
@@ -280,135 +315,336 @@ __device__ __forceinline__ void flag_error(uint32_t* err, uint32_t bit) {
   if (err != nullptr) atomicOr(err, bit);
 }
 
-__device__ __forceinline__ int ctx_eff(const ScorerParams& p, int b) {
-  return min(max(__ldg(p.ctx_lens + b), 0), p.max_context);
+// sum over 32 columns of w[i] * max(x[i], 0): four packed chains, then a
+// fixed combining order.
+__device__ __forceinline__ float weighted_relu_sum(const uint32_t (&x)[32], const float* w) {
+  float2 a0 = make_float2(0.0f, 0.0f), a1 = a0, a2 = a0, a3 = a0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 w0 = reinterpret_cast<const float4*>(w)[2 * i];
+    const float4 w1 = reinterpret_cast<const float4*>(w)[2 * i + 1];
+    const uint32_t* v = x + 8 * i;
+    a0 = fma2(make_float2(w0.x, w0.y),
+              make_float2(fmaxf(__uint_as_float(v[0]), 0.0f), fmaxf(__uint_as_float(v[1]), 0.0f)),
+              a0);
+    a1 = fma2(make_float2(w0.z, w0.w),
+              make_float2(fmaxf(__uint_as_float(v[2]), 0.0f), fmaxf(__uint_as_float(v[3]), 0.0f)),
+              a1);
+    a2 = fma2(make_float2(w1.x, w1.y),
+              make_float2(fmaxf(__uint_as_float(v[4]), 0.0f), fmaxf(__uint_as_float(v[5]), 0.0f)),
+              a2);
+    a3 = fma2(make_float2(w1.z, w1.w),
+              make_float2(fmaxf(__uint_as_float(v[6]), 0.0f), fmaxf(__uint_as_float(v[7]), 0.0f)),
+              a3);
+  }
+  return __fadd_rn(__fadd_rn(__fadd_rn(a0.x, a0.y), __fadd_rn(a1.x, a1.y)),
+                   __fadd_rn(__fadd_rn(a2.x, a2.y), __fadd_rn(a3.x, a3.y)));
 }
 
-__device__ __forceinline__ int work_tiles(int ctx) { return (ctx + kTile - 1) / kTile; }
+// ---------------------------------------------------------------- segments
+// A segment's work tiles [lo, hi) and its column limit: decode -- tiles
+// below the effective context c = clamp(ctx, 0, max_context), limit c;
+// prefill -- the tiles covering the union of its tokens' clamped key
+// ranges, limit the key count.
+struct SegRange {
+  int lo, hi, lim;
+};
 
-// Chunks [C0, C1) of an accumulator (this thread's TMEM lane, 32 columns
-// each), one chunk in registers at a time: part[c - C0] = sum over chunk c's
-// columns of w * max(D, 0).  Returns once every TMEM load has completed.
-template <int C0, int C1>
-struct HalfAcc {
-  __device__ __forceinline__ void run(uint32_t acc, const float* wts, float* part) const {
-#pragma unroll
-    for (int c = C0; c < C1; ++c) {
-      uint32_t r[32];
-      tmem_ld32(acc + 32u * c, r);
-      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-      // two independent packed chains, then a fixed combining order
-      float2 a0 = make_float2(0.0f, 0.0f), a1 = a0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 ww = reinterpret_cast<const float4*>(wts + 32 * c)[i];
-        const uint32_t* x = r + 4 * i;
-        a0 = fma2(make_float2(ww.x, ww.y),
-                  make_float2(fmaxf(__uint_as_float(x[0]), 0.0f),
-                              fmaxf(__uint_as_float(x[1]), 0.0f)),
-                  a0);
-        a1 = fma2(make_float2(ww.z, ww.w),
-                  make_float2(fmaxf(__uint_as_float(x[2]), 0.0f),
-                              fmaxf(__uint_as_float(x[3]), 0.0f)),
-                  a1);
+// The query tokens of segment g: decode -- tokens j0 .. j0 + ntok - 1 of
+// sequence b = g / ngroups (j0 = (g % ngroups) * tps), whose key range and
+// block-table row it uses; prefill -- tokens g*tps .. of the chunk.
+struct SegQ {
+  int b, qt0, ntok;  // key-range owner (decode: sequence), first query token, tokens
+};
+
+__device__ __forceinline__ SegQ seg_q(const ScorerParams& p, int g) {
+  SegQ q;
+  if (p.mode == kModeDecode) {
+    q.b = g / p.ngroups;
+    const int j0 = (g - q.b * p.ngroups) * p.tps;
+    q.qt0 = q.b * p.next_n + j0;
+    q.ntok = min(p.tps, p.next_n - j0);
+  } else {
+    q.b = g;
+    q.qt0 = g * p.tps;
+    q.ntok = min(p.tps, p.num_q - q.qt0);
+  }
+  return q;
+}
+
+__device__ __forceinline__ SegRange seg_load(const ScorerParams& p, int g) {
+  SegRange r;
+  if (p.mode == kModeDecode) {
+    const int c = min(max(__ldg(p.ctx_lens + g / p.ngroups), 0), p.ncols);
+    r.lo = 0;
+    r.hi = (c + kTile - 1) / kTile;
+    r.lim = c;
+  } else {
+    int mn = p.ncols, mx = 0;
+    const int t0 = g * p.tps;
+    for (int j = 0; j < p.tps; ++j) {
+      const int t = t0 + j;
+      if (t >= p.num_q) break;
+      const int a = min(max(__ldg(p.ks + t), 0), p.ncols);
+      const int b = min(max(__ldg(p.ke + t), 0), p.ncols);
+      if (a < b) {
+        mn = min(mn, a);
+        mx = max(mx, b);
       }
-      part[c - C0] = __fadd_rn(__fadd_rn(a0.x, a0.y), __fadd_rn(a1.x, a1.y));
+    }
+    if (mn < mx) {
+      r.lo = mn / kTile;
+      r.hi = (mx + kTile - 1) / kTile;
+    } else {
+      r.lo = r.hi = 0;
+    }
+    r.lim = p.ncols;
+  }
+  return r;
+}
+
+struct SegTable {
+  const int* tab;  // kSegTab x (lo, hi, lim) for segments g0 .. g0 + kSegTab - 1
+  int g0;
+  __device__ __forceinline__ SegRange get(const ScorerParams& p, int g) const {
+    const int i = g - g0;
+    if (i >= 0 && i < kSegTab) {
+      SegRange r;
+      r.lo = tab[3 * i];
+      r.hi = tab[3 * i + 1];
+      r.lim = tab[3 * i + 2];
+      return r;
+    }
+    if (g >= p.nseg) return SegRange{0, 0, 0};
+    return seg_load(p, g);
+  }
+  // the next segment after g with work tiles (p.nseg if none)
+  __device__ __forceinline__ int next(const ScorerParams& p, int g, SegRange& r) const {
+    for (++g; g < p.nseg; ++g) {
+      r = get(p, g);
+      if (r.lo < r.hi) return g;
+    }
+    r = SegRange{0, 0, 0};
+    return p.nseg;
+  }
+};
+
+// Walks a CTA's work tiles in order: segment g, tile t in [lo, hi), the
+// segment's ordinal qi in this CTA (its query buffer is qi % qbufs) and
+// whether t is the first tile of the segment in this CTA.
+struct Walk {
+  int g, t, hi, lim, qi, pos;  // pos: tiles of the segment before t in this CTA
+  SegQ q;
+  bool first;
+  __device__ __forceinline__ void init(const ScorerParams& p, const SegTable& st, int g0,
+                                       int toff) {
+    const SegRange r = st.get(p, g0);
+    g = g0;
+    t = r.lo + toff;
+    hi = r.hi;
+    lim = r.lim;
+    qi = 0;
+    pos = 0;
+    q = seg_q(p, g0);
+    first = true;
+  }
+  // Only called while tiles remain, so a later segment with work exists.
+  __device__ __forceinline__ void advance(const ScorerParams& p, const SegTable& st) {
+    first = false;
+    ++pos;
+    if (++t < hi) return;
+    SegRange r;
+    g = st.next(p, g, r);
+    t = r.lo;
+    hi = r.hi;
+    lim = r.lim;
+    ++qi;
+    pos = 0;
+    q = seg_q(p, g);
+    first = true;
+  }
+  __device__ __forceinline__ bool last_of_segment() const { return t + 1 >= hi; }
+};
+
+// Writes -inf over a CTA's share of the tiles outside every segment's range
+// (for each such (segment, tile): the segment's query rows x 128 columns),
+// a few tiles at a time, one warp.
+struct Filler {
+  int g, off, left;
+  SegRange r;
+  __device__ __forceinline__ void init(const ScorerParams& p, const SegTable& st, int g0,
+                                       int off0, int count) {
+    g = g0;
+    off = off0;
+    left = count;
+    if (count > 0) r = st.get(p, g);
+  }
+  // write (store) or step over (!store) the next `items` tiles
+  __device__ __forceinline__ void run(const ScorerParams& p, const SegTable& st, int items,
+                                      int lane, bool store = true) {
+    for (; items > 0 && left > 0; --items, --left) {
+      int np = p.tiles_total - (r.hi - r.lo);
+      while (off >= np && g + 1 < p.nseg) {  // the next segment with -inf tiles
+        off = 0;
+        r = st.get(p, ++g);
+        np = p.tiles_total - (r.hi - r.lo);
+      }
+      if (off >= np) {
+        left = 0;
+        return;
+      }
+      const int tile = off < r.lo ? off : r.hi + (off - r.lo);
+      const SegQ q = seg_q(p, g);
+      for (int j = 0; j < q.ntok && store; ++j) {
+        float* const out = p.logits + (int64_t)(q.qt0 + j) * p.logits_stride;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int s = tile * kTile + 32 * m + lane;
+          if (s < p.ncols) __stcs(out + s, -INFINITY);
+        }
+      }
+      ++off;
     }
   }
 };
 
-template <int C0, int C1>
-struct HalfAccT : HalfAcc<C0, C1> {
-  static constexpr int kC0 = C0, kC1 = C1;
-};
-
-// Walks a CTA's tiles in order: sequence b, tile t, its context, and the
-// segment index g (how many times b has changed since the first tile).
-struct Walker {
-  int b, t, ctx, g;
-  __device__ void init(const ScorerParams& p, int b0, int t0) {
-    b = b0;
-    t = t0;
-    ctx = ctx_eff(p, b0);
-    g = 0;
-  }
-  __device__ void advance(const ScorerParams& p) {
-    ++t;
-    while (t >= work_tiles(ctx) && b + 1 < p.batch) {
-      ++b;
-      t = 0;
-      ctx = ctx_eff(p, b);
-      ++g;
+// Inclusive warp scan of two 64-bit values.
+__device__ __forceinline__ void warp_scan2(long long& a, long long& b, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long ya = __shfl_up_sync(0xffffffffu, a, o);
+    const long long yb = __shfl_up_sync(0xffffffffu, b, o);
+    if (lane >= o) {
+      a += ya;
+      b += yb;
     }
   }
-};
+}
 
-template <int NCHUNK>
+// ---------------------------------------------------------------- the kernel
+// CPW: the largest number of accumulator chunks an epilogue warp reads
+// (1, 2 or 4; p.cpw <= CPW): one query token's heads, H / 32 chunks.
+template <int CPW>
 __global__ void __launch_bounds__(kThreads, 1)
-    scorer_kernel(const __grid_constant__ ScorerParams p, const __grid_constant__ CUtensorMap tmap) {
+    scorer_kernel(const __grid_constant__ ScorerParams p, const __grid_constant__ CUtensorMap kmap,
+                  const __grid_constant__ CUtensorMap qmap) {
   extern __shared__ uint8_t smem_raw[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = p.stages, R = p.R;
+  constexpr int A = kMaxAccs, QB = kQBufs;
   uint8_t* const smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const Layout L = make_layout(S, R);
-  uint8_t* const sA = smem + L.a;
   uint8_t* const sQ = smem + L.q;
-  uint8_t* const sE = smem + L.e;
   float* const sW = reinterpret_cast<float*>(smem + L.w);
+  int* const tab = reinterpret_cast<int*>(smem + L.tab);
   const uint32_t bars = smem_addr(smem + L.bars);
   uint32_t* const misc = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile uint32_t* const abort = misc + 1;
-  int32_t* const start = reinterpret_cast<int32_t*>(misc + 2);  // b, t, n
-  long long* const scan = reinterpret_cast<long long*>(smem + L.scan);
-  auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
+  int32_t* const start = reinterpret_cast<int32_t*>(misc + 2);  // g0, toff, n, pg0, poff, pn
+  auto stage = [&](int s) { return smem + (uint32_t)s * kStageBytes; };
+  auto bar_full = [&](int s) { return bars + 8u * (uint32_t)s; };
+  auto bar_empty = [&](int s) { return bars + 8u * (uint32_t)(S + s); };
+  auto bar_accf = [&](int a) { return bars + 8u * (uint32_t)(2 * S + a); };
+  auto bar_acce = [&](int a) { return bars + 8u * (uint32_t)(2 * S + kMaxAccs + a); };
+  auto bar_qempty = [&](int b) { return bars + 8u * (uint32_t)(2 * S + 2 * kMaxAccs + b); };
+  auto bar_qfull = [&](int b) { return bars + 8u * (uint32_t)(2 * S + 2 * kMaxAccs + 4 + b); };
 
-  // ---- this CTA's share of the work tiles --------------------------------
-  const int per = (p.batch + kThreads - 1) / kThreads;
-  const int b_lo = min(p.batch, tid * per), b_hi = min(p.batch, b_lo + per);
-  long long part = 0;
-  for (int b = b_lo; b < b_hi; ++b) part += work_tiles(ctx_eff(p, b));
-  scan[tid] = part;
-  if (tid == 0) {
-    *abort = 0u;
-    start[2] = 0;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    long long run = 0;
-    for (int i = 0; i < kThreads; ++i) {
-      const long long v = scan[i];
-      scan[i] = run;
-      run += v;
+  // ---- this CTA's shares of the work tiles and of the -inf tiles ----------
+  // (the scan scratch lives in the stage area, unused until the copies start)
+  long long* const scanw = reinterpret_cast<long long*>(smem);   // kWarps (prefix of work)
+  long long* const scanp = scanw + 32;                           // kWarps (prefix of pads)
+  {
+    const int per = (p.nseg + kThreads - 1) / kThreads;
+    const int g_lo = min(p.nseg, tid * per), g_hi = min(p.nseg, g_lo + per);
+    long long wpart = 0, ppart = 0;
+    for (int g = g_lo; g < g_hi; ++g) {
+      const SegRange r = seg_load(p, g);
+      wpart += r.hi - r.lo;
+      ppart += p.tiles_total - (r.hi - r.lo);
     }
-    scan[kThreads] = run;
-  }
-  __syncthreads();
-  const long long W = scan[kThreads];
-  const long long lo = W * blockIdx.x / gridDim.x, hi = W * (blockIdx.x + 1) / gridDim.x;
-  if (lo < hi && scan[tid] <= lo && lo < scan[tid] + part) {
-    long long acc = scan[tid];
-    for (int b = b_lo; b < b_hi; ++b) {
-      const int wt = work_tiles(ctx_eff(p, b));
-      if (lo < acc + wt) {
-        start[0] = b;
-        start[1] = (int)(lo - acc);
-        start[2] = (int)(hi - lo);
-        break;
-      }
-      acc += wt;
-    }
-  }
-  __syncthreads();
-  const int n = start[2];
-
-  if (n > 0) {
-    const int b0 = start[0], t0 = start[1];
+    long long wi = wpart, pi = ppart;
+    warp_scan2(wi, pi, lane);
     if (tid == 0) {
-      for (int i = 0; i < 2 * S + kExtraBars; ++i) {
-        // acc_empty takes one arrival per epilogue warp of a group
-        const int cnt = (i >= bar_acce(S, 0) && i < bar_acce(S, kAccs)) ? kGroupWarps : 1;
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar(i)), "r"(cnt)
+      *abort = 0u;
+      start[2] = 0;
+      start[5] = 0;
+      misc[8] = misc[9] = 0u;
+    }
+    if (lane == 31) {
+      scanw[warp] = wi;
+      scanp[warp] = pi;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      long long a = lane < kWarps ? scanw[lane] : 0, b = lane < kWarps ? scanp[lane] : 0;
+      const long long a0 = a, b0 = b;
+      warp_scan2(a, b, lane);
+      __syncwarp();
+      if (lane < kWarps) {
+        scanw[lane] = a - a0;  // exclusive prefix of each warp
+        scanp[lane] = b - b0;
+      }
+      if (lane == kWarps - 1) {
+        scanw[kWarps] = a;  // totals
+        scanp[kWarps] = b;
+      }
+    }
+    __syncthreads();
+    const long long wex = scanw[warp] + wi - wpart, pex = scanp[warp] + pi - ppart;
+    const long long W = scanw[kWarps], P = scanp[kWarps];
+    const long long lo = W * blockIdx.x / gridDim.x, hi = W * (blockIdx.x + 1) / gridDim.x;
+    if (lo < hi && wex <= lo && lo < wex + wpart) {
+      long long acc = wex;
+      for (int g = g_lo; g < g_hi; ++g) {
+        const SegRange r = seg_load(p, g);
+        if (lo < acc + (r.hi - r.lo)) {
+          start[0] = g;
+          start[1] = (int)(lo - acc);
+          start[2] = (int)(hi - lo);
+          break;
+        }
+        acc += r.hi - r.lo;
+      }
+    }
+    const long long plo = P * blockIdx.x / gridDim.x, phi = P * (blockIdx.x + 1) / gridDim.x;
+    if (plo < phi && pex <= plo && plo < pex + ppart) {
+      long long acc = pex;
+      for (int g = g_lo; g < g_hi; ++g) {
+        const SegRange r = seg_load(p, g);
+        const int np = p.tiles_total - (r.hi - r.lo);
+        if (plo < acc + np) {
+          start[3] = g;
+          start[4] = (int)(plo - acc);
+          start[5] = (int)(phi - plo);
+          break;
+        }
+        acc += np;
+      }
+    }
+    __syncthreads();
+  }
+  const int n = start[2];
+  SegTable st;
+  st.tab = tab;
+  st.g0 = n > 0 ? start[0] : -2 * kSegTab;  // no table without work tiles
+  for (int i = tid; i < kSegTab; i += kThreads) {
+    const int g = st.g0 + i;
+    SegRange r = SegRange{0, 0, 0};
+    if (n > 0 && g < p.nseg) r = seg_load(p, g);
+    tab[3 * i] = r.lo;
+    tab[3 * i + 1] = r.hi;
+    tab[3 * i + 2] = r.lim;
+  }
+
+  uint32_t tmem = 0;
+  if (n > 0) {
+    if (tid == 0) {
+      for (int i = 0; i < 2 * S + 2 * kMaxAccs + 8; ++i) {
+        // acc_empty takes one arrival per active epilogue warp
+        const bool acce = i >= 2 * S + kMaxAccs && i < 2 * S + 2 * kMaxAccs;
+        const int cnt = acce ? 4 * ((R / 32 + p.cpw - 1) / p.cpw) : 1;
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bars + 8u * i), "r"(cnt)
                      : "memory");
       }
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -416,327 +652,391 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
       asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                        smem_addr(misc)),
-                   "r"(p.tmem_cols)
+                   "r"(kTmemCols)
                    : "memory");
       asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    __syncthreads();
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    const uint32_t tmem = misc[0];
-    // TMEM columns: accumulators [0, R) and [R, 2R); key scale words of
-    // group e at 2R + 8e; query scale words of segment g at 2R + 16 + 8(g%2).
-    // TMEM columns: accumulator a at aR (a < 3); the keys' scale words of
-    // accumulator a's tile at 3R + 8a; the query scale words of segment g at
-    // 3R + 24 + 8(g%4).
-    const uint32_t sfa_col0 = (uint32_t)kAccs * R, sfb_col0 = (uint32_t)kAccs * R + 24u;
-    uint8_t* const sSF = smem + L.sf;  // copy sources: 3 key + 4 query, 512 B each
-    int issued = 0;  // producer: tiles whose copies were issued
+  }
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  if (n > 0) tmem = misc[0];
+  // TMEM columns: accumulator a at a*R; the keys' scale words of
+  // accumulator a at A*R + 8a; the queries' words of buffer b for issuer m
+  // at A*R + 24 + 8(m*QB + b) (each issuer copies its own).
+  const uint32_t sfa_col0 = (uint32_t)A * R, sfb_col0 = sfa_col0 + kMaxAccs * kSfCols;
+  int last_issued = -1;  // producers: the last tile whose copies were issued
+  int q_issued[4] = {-1, -1, -1, -1};  // producers: parity of the last query copy per buffer
 
-    if (warp >= kProducerWarp && warp < kMmaWarp) {
-      // Producer pi issues the tiles k = pi, pi + kProducers, ... and so owns
-      // the stages s = k % S (S is a multiple of kProducers).  A warp waits a
-      // few hundred cycles for each copy it issues, so the copies are spread
-      // over several warps.  The page ids of 16 of its tiles are fetched by
-      // the whole warp in one load (lane L: own tile L/2, page L%2), a batch
-      // ahead of the tiles issued.
-      const int pi = warp - kProducerWarp;
-      const int n_own = n > pi ? (n - pi + kProducers - 1) / kProducers : 0;
-      Walker fw;  // at tile fk
-      fw.init(p, b0, t0);
-      int fk = 0;
-      auto fetch = [&](int m0, int32_t& id, bool& inctx) {
-        const int mine = lane >> 1;
-        int cb = 0, ct = 0, cctx = 0;
-        for (int i = 0; i < 16 && m0 + i < n_own; ++i) {
-          const int k = pi + kProducers * (m0 + i);
-          while (fk < k) {
-            fw.advance(p);
-            ++fk;
-          }
-          if (i == mine) {
-            cb = fw.b;
-            ct = fw.t;
-            cctx = fw.ctx;
+  if (n > 0 && warp >= kProducerWarp && warp < kProducerWarp + kProducers) {
+    // ---- producers: tile k belongs to producer k % 2 ------------------------
+    const int pi = warp - kProducerWarp;
+    if (pi < n) {
+      // Lane L fetches the page id of half L % 2 of the producer's own tile
+      // m0 + L / 2 (m0: the first own tile of the batch), a batch ahead.
+      Walk lw;  // this lane's walker, at its tile of the batch being fetched
+      lw.init(p, st, start[0], start[1]);
+      int lk = 0;  // lw's tile index
+      const int n_own = (n - pi + kProducers - 1) / kProducers;
+      auto walk_to = [&](int k) {
+        while (lk < k && lk < n - 1) {
+          lw.advance(p, st);
+          ++lk;
+        }
+      };
+      auto fetch = [&](int m0, int32_t& id, int& inrange) {
+        const int m = m0 + (lane >> 1);
+        id = -1;
+        inrange = 0;
+        if (m < n_own) {
+          walk_to(pi + kProducers * m);
+          const int pidx = lw.t * 2 + (lane & 1);
+          if (pidx * kKvBlock < lw.lim) {
+            inrange = 1;
+            id = p.mode == kModeDecode
+                     ? __ldg(p.block_table + (int64_t)lw.q.b * p.bt_stride + pidx)
+                     : pidx;
           }
         }
-        const int pidx = ct * 2 + (lane & 1);
-        inctx = m0 + mine < n_own && pidx * kKvBlock < cctx;
-        id = inctx ? __ldg(p.block_table + (int64_t)cb * p.bt_stride + pidx) : -1;
       };
+      // this producer's half of the -inf tiles (the first half for producer
+      // 0, the second for producer 1), spread over its tiles: a producer
+      // mostly waits for a free stage, so the stores cost the pipeline nothing
+      const int pn_all = start[5], pn = pi == 0 ? pn_all / 2 : pn_all - pn_all / 2;
+      Filler fill;
+      fill.init(p, st, start[3], start[4], pi == 0 ? pn : pn_all);
+      if (pi == 1) fill.run(p, st, pn_all / 2, lane, false);  // step over producer 0's half
+      Walk w;  // lane 0's walker at the tile being issued
+      w.init(p, st, start[0], start[1]);
+      int wk = 0;
       int32_t cur_id, nxt_id = -1;
-      bool cur_in, nxt_in = false;
+      int cur_in, nxt_in = 0;
       fetch(0, cur_id, cur_in);
+      int s = pi;
+      uint32_t ph = 0;
+      const uint32_t q_bytes = (uint32_t)R * 64u;
       bool stop = false;
       for (int m0 = 0; m0 < n_own && !stop; m0 += 16) {
         if (m0 + 16 < n_own) fetch(m0 + 16, nxt_id, nxt_in);
         for (int i = 0; i < 16 && m0 + i < n_own; ++i) {
-          const int k = pi + kProducers * (m0 + i), s = k % S;
-          int32_t page[2];
-          bool in[2];
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            page[half] = __shfl_sync(0xffffffffu, cur_id, 2 * i + half);
-            in[half] = __shfl_sync(0xffffffffu, (int)cur_in, 2 * i + half) != 0;
+          const int k = pi + kProducers * (m0 + i);
+          {
+            const long long f0 = (long long)pn * (m0 + i) / n_own;
+            const long long f1 = (long long)pn * (m0 + i + 1) / n_own;
+            fill.run(p, st, (int)(f1 - f0), lane);
           }
-          int ok = 1;
-          if (lane == 0) {
-            ok = wait_phase(bar(bar_empty(S, s)), ((uint32_t)(k / S) & 1u) ^ 1u, abort);
+          int32_t page[2];
+          int in[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            page[h] = __shfl_sync(0xffffffffu, cur_id, 2 * i + h);
+            in[h] = __shfl_sync(0xffffffffu, cur_in, 2 * i + h);
+          }
+          while (wk < k) {
+            w.advance(p, st);
+            ++wk;
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h)  // a page outside the cache is not read
+            if (in[h] && (page[h] < 0 || page[h] >= p.num_blocks)) {
+              if (lane == 0) flag_error(p.err, FP4IDX_ERRFLAG_PAGE);
+              in[h] = 0;
+            }
+          const uint32_t fb = bar_full(s);
+          // lanes 0 and 1 both write the stage, so both observe its release
+          int ok = __all_sync(0xffffffffu, lane >= 2 || wait_phase(bar_empty(s), ph ^ 1u, abort));
+          if (lane == 0 && ok) {
+            const int qb = w.qi % QB;
+            if (w.first)
+              ok = wait_phase(bar_qempty(qb), (((uint32_t)(w.qi / QB)) & 1u) ^ 1u, abort);
             if (ok) {
-              uint32_t bytes = 0;
-#pragma unroll
-              for (int half = 0; half < 2; ++half) {
-                if (!in[half]) {
-                  page[half] = -1;
-                } else if (page[half] < 0 || page[half] >= p.num_blocks) {
-                  flag_error(p.err, FP4IDX_ERRFLAG_PAGE);
-                  page[half] = -1;
-                } else {
-                  bytes += kPayloadBytes + kExpBytes;
-                }
+              if (w.first) {  // the segment's query operand, on its own barrier
+                const uint32_t qf = bar_qfull(qb);
+                mbar_expect_tx(qf, q_bytes);
+                tma_2d(smem_addr(sQ + (uint32_t)qb * q_bytes), &qmap, 0, w.q.qt0 * p.H, qf);
+                q_issued[qb & 3] = (w.qi / QB) & 1;
               }
-              const uint32_t fb = bar(bar_full(s));
-              asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb),
-                           "r"(bytes)
-                           : "memory");
-#pragma unroll
-              for (int half = 0; half < 2; ++half) {
-                if (page[half] < 0) continue;
-                asm volatile(
-                    "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
-                    "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(sA + s * kStageA +
-                                                                      half * kPayloadBytes)),
-                    "l"(&tmap), "r"(0), "r"(0), "r"(page[half]), "r"(fb)
-                    : "memory");
-                const uint8_t* src = p.cache + (int64_t)page[half] * kPageBytes + kPayloadBytes;
-                asm volatile(
-                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], "
-                    "[%1], %2, [%3];" ::"r"(smem_addr(sE + s * kStageE + half * kExpBytes)),
-                    "l"(src), "r"(kExpBytes), "r"(fb)
-                    : "memory");
-              }
-              issued = k + 1;
+              mbar_expect_tx(fb, (uint32_t)(in[0] + in[1]) * (kPayloadBytes + kExpBytes));
+              last_issued = k;
             }
           }
           if (!__shfl_sync(0xffffffffu, ok, 0)) {
             stop = true;
             break;
           }
+          // lanes 0 and 1 issue one page each
+          const int32_t my_page = lane == 0 ? page[0] : page[1];
+          const int my_in = lane == 0 ? in[0] : in[1];
+          if (lane < 2 && my_in) {
+            uint8_t* const sp = stage(s);
+            tma_3d(smem_addr(sp + kStPayload + lane * kPayloadBytes), &kmap, 0, 0, my_page, fb);
+            bulk_copy(smem_addr(sp + kStExp + lane * kExpBytes),
+                      p.cache + (int64_t)my_page * kPageBytes + kPayloadBytes, kExpBytes, fb);
+          }
+          s += kProducers;
+          if (s >= S) {
+            s -= S;
+            ph ^= 1u;
+          }
         }
         cur_id = nxt_id;
         cur_in = nxt_in;
       }
-    } else if (warp == kMmaWarp) {
-      // The whole warp waits (a warp-uniform loop wakes promptly) and stages
-      // the scale words; lane 0 issues the copies into TMEM, the MMAs and the
-      // commits, in that order in the tensor pipe.
-      Walker wk;
-      wk.init(p, b0, t0);
-      const uint32_t id0 = mxf4_idesc(R, 0), id1 = mxf4_idesc(R, 2);
-      // descriptor start addresses advance in 16-byte units
-      const uint64_t a_desc0 = sw64_desc(smem_addr(sA)), q_desc0 = sw64_desc(smem_addr(sQ));
-      int done = 0;
-      for (int k = 0; k < n; ++k) {
-        const int s = k % S, a = k % kAccs, gq = wk.g % kQBufs;
-        // Tile k's data, and accumulator a free again: tile k-3 read out,
-        // which also means every MMA up to tile k-3 -- and the copies and
-        // operands those MMAs used -- is complete.
-        bool ok = wait_phase(bar(bar_full(s)), (uint32_t)(k / S) & 1u, abort) &&
-                  (k < kAccs ||
-                   wait_phase(bar(bar_acce(S, a)), (uint32_t)(k / kAccs - 1) & 1u, abort));
-        if (!__all_sync(0xffffffffu, ok)) break;
-        const bool seg_start = k == 0 || wk.t == 0;
-        if (seg_start) {
-          // The segment's query operand and query scale words.  Buffer gq was
-          // last used by segment g-4, whose tiles all precede tile k-3.
-          const int64_t row0 = ((int64_t)wk.b * p.next_n) * p.H;  // first query row of b
-          uint8_t* dst = sQ + gq * R * 64;
+      fill.run(p, st, pn, lane);  // any left (an aborted loop)
+    } else if (pi == 1) {  // no work tiles for this producer: its -inf half only
+      const int pn_all = start[5];
+      Filler fill;
+      fill.init(p, st, start[3], start[4], pn_all);
+      fill.run(p, st, pn_all / 2, lane, false);
+      fill.run(p, st, pn_all, lane);
+    }
+  } else if (n > 0 && warp >= kIssuerWarp && warp < kIssuerWarp + kIssuers) {
+    // ---- issuers: tile k belongs to issuer k % 2 ----------------------------
+    const int m = warp - kIssuerWarp;
+    Walk w;
+    w.init(p, st, start[0], start[1]);
+    int wk = 0;
+    uint32_t qv[4];  // this lane's query words of segment qv_g
+    int qv_g = -1;
+    auto load_qwords = [&](int g) {
+      const SegQ q = seg_q(p, g);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int r = lane + 32 * i;
-            if (r < R) {
-              const uint4* src = reinterpret_cast<const uint4*>(p.q_fp4 + (row0 + r) * 64);
-#pragma unroll
-              for (int c = 0; c < 4; ++c)
-                *reinterpret_cast<uint4*>(dst + sw64_chunk(r, c)) = __ldg(src + c);
-            }
+      for (int j = 0; j < 4; ++j) {
+        const int r = 32 * j + lane;
+        qv[j] = (g < p.nseg && r < q.ntok * p.H)
+                    ? __ldg(reinterpret_cast<const uint32_t*>(p.q_scale) + (int64_t)q.qt0 * p.H + r)
+                    : 0x7F7F7F7Fu;
+      }
+      qv_g = g;
+    };
+    const int n_own = n > m ? (n - m + 1) / 2 : 0;
+    const uint32_t id0 = mxf4_idesc(R, 0), id1 = mxf4_idesc(R, 2);
+    const uint32_t q_bytes = (uint32_t)R * 64u;
+    int s = m, a = m % A, last = -1;
+    uint32_t ph = 0, pa = (uint32_t)(m / A) & 1u;
+    for (int i = 0; i < n_own; ++i) {
+      const int k = m + 2 * i;
+      while (wk < k) {
+        w.advance(p, st);
+        ++wk;
+      }
+      // Every lane reads the landed exponent words, so every lane observes
+      // the barrier's completion itself (acquire); a wait by one lane alone
+      // does not order the other lanes' reads after the copy.
+      int ok = __all_sync(0xffffffffu, wait_phase(bar_full(s), ph, abort));
+      if (!ok) break;
+      uint8_t* const sp = stage(s);
+      {  // the keys' words: row l holds tokens l, l+32, l+64, l+96
+        const uint32_t* ew = reinterpret_cast<const uint32_t*>(sp + kStExp);
+        *reinterpret_cast<uint4*>(sp + kStSfa + 16 * lane) =
+            make_uint4(ew[lane], ew[lane + 32], ew[lane + 64], ew[lane + 96]);
+      }
+      const bool seg_first = w.pos < 2;  // this issuer's first tile of the segment
+      if (seg_first) {  // the queries' words, rows 0-127 then 128-255
+        if (qv_g != w.g) load_qwords(w.g);
+        *reinterpret_cast<uint4*>(sp + kStSfb + 16 * lane) = make_uint4(qv[0], qv[1], qv[2], qv[3]);
+        SegRange r;
+        load_qwords(st.next(p, w.g, r));  // the next segment's, ahead of time
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) {
+        const int qb = w.qi % QB;
+        ok = (k < A || wait_phase(bar_acce(a), pa ^ 1u, abort)) &&
+             (!seg_first || wait_phase(bar_qfull(qb), (uint32_t)(w.qi / QB) & 1u, abort));
+        if (ok) {
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint32_t sfa = tmem + sfa_col0 + kSfCols * (uint32_t)a;
+          const uint32_t sfb = tmem + sfb_col0 + kSfCols * (uint32_t)(m * QB + qb);
+          cp_32x128b_x4(sfa, cp_desc(smem_addr(sp + kStSfa)));
+          if (seg_first) {
+            cp_32x128b_x4(sfb, cp_desc(smem_addr(sp + kStSfb)));
           }
-          uint32_t v[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int r = 32 * j + lane;
-            v[j] = r < R ? __ldg(reinterpret_cast<const uint32_t*>(p.q_scale) + row0 + r)
-                         : 0x7F7F7F7Fu;
-          }
-          *reinterpret_cast<uint4*>(sSF + (kAccs + gq) * 512 + 16 * lane) =
-              make_uint4(v[0], v[1], v[2], v[3]);
-        }
-        {  // the keys' exponent words, token 32c + l at row l, column c
-          const uint32_t* ew = reinterpret_cast<const uint32_t*>(sE + s * kStageE);
-          *reinterpret_cast<uint4*>(sSF + a * 512 + 16 * lane) =
-              make_uint4(ew[lane], ew[lane + 32], ew[lane + 64], ew[lane + 96]);
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        if (lane == 0) {
-          const uint32_t sfa = tmem + sfa_col0 + 8u * (uint32_t)a;
-          const uint32_t sfb = tmem + sfb_col0 + 8u * (uint32_t)gq;
-          cp_32x128b_x4(sfa, cp_desc(smem_addr(sSF + a * 512)));
-          if (seg_start) cp_32x128b_x4(sfb, cp_desc(smem_addr(sSF + (kAccs + gq) * 512)));
-          const uint64_t adesc = a_desc0 + (uint64_t)(s * (kStageA >> 4));
-          const uint64_t qdesc = q_desc0 + (uint64_t)(gq * R * (64 >> 4));
+          // operand descriptors built from the buffers' own addresses
+          const uint64_t adesc = sw64_desc(smem_addr(sp + kStPayload));
+          const uint64_t qdesc = sw64_desc(smem_addr(sQ + (uint32_t)qb * q_bytes));
           const uint32_t d = tmem + (uint32_t)a * (uint32_t)R;
           mma_mxf4(d, adesc, qdesc, id0, sfa, sfb, 0u);
           mma_mxf4(d, adesc + 2, qdesc + 2, id1, sfa, sfb, 1u);
-          mma_commit(bar(bar_accf(S, k % 6)));
-          mma_commit(bar(bar_empty(S, s)));
+          mma_commit(bar_accf(a));
+          last = k;
         }
-        __syncwarp();
-        done = k + 1;
-        wk.advance(p);
       }
-      if (done > 0 && lane == 0)  // the last commits land before the memory is released
-        wait_phase_drain(bar(bar_empty(S, (done - 1) % S)), (uint32_t)((done - 1) / S) & 1u);
-    } else {
-      // ---- epilogue group e (warps 8e .. 8e+7): tiles k = e, e+2, ... --------
-      // Warps q and q+4 of a group share TMEM lane quadrant q (tokens
-      // 32q .. 32q+31) and split the accumulator's 32-column chunks: the
-      // lower half takes chunks [0, kC1), the upper half [kC1, NCHUNK).  Per
-      // tile a warp reads and reduces its chunks, releases the accumulator
-      // (acc_empty) and stores the logits.
-      constexpr int kC1 = (NCHUNK + 1) / 2;
-      const int e = warp / kGroupWarps, gw = warp % kGroupWarps;
-      const int quad = gw & 3, half = gw >> 2;
-      const int row = quad * 32 + lane;  // token of the tile = TMEM lane
-      const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-      float* const wts = sW + warp * R;  // this warp's head weights
-      float* const xch = reinterpret_cast<float*>(smem + L.x) + e * 2 * kMaxNext * kTile;
-      const int cpj = p.H / 32;          // chunks per query token
-      // a query token whose heads span both halves (its partial sums are
-      // handed from the upper to the lower warp through shared memory)
-      const bool split = kC1 < NCHUNK && kC1 % cpj != 0;
-      const int js = kC1 / cpj;
-
-      // The validity of this warp's page of tile (w.b, w.t) -- the same rule
-      // the producer applies: inside the context and a page id in range.
-      auto page_id = [&](const Walker& w) -> int32_t {
-        const int pidx = w.t * 2 + (quad >> 1);
-        return pidx * kKvBlock < w.ctx
-                   ? __ldg(p.block_table + (int64_t)w.b * p.bt_stride + pidx)
-                   : -1;
-      };
-
-      // Tile k, chunks [C0, C1) of accumulator k % 3: load and reduce chunk
-      // by chunk, release the accumulator, store (or hand off) the logits.
-      auto tile = [&](auto acc, int k, const Walker& w, bool page_ok, bool& live) {
-        constexpr int C0 = decltype(acc)::kC0, C1 = decltype(acc)::kC1;
-        const int a = k % kAccs;
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        float part[C1 > C0 ? C1 - C0 : 1];
-        acc.run(tmem + lane_base + (uint32_t)a * (uint32_t)R, wts, part);
-        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(bar_acce(S, a)));
-        const int s_tok = w.t * kTile + row;
-        const bool valid = s_tok < w.ctx && page_ok;
-        float* const xb = xch + ((k >> 1) & 1) * kMaxNext * kTile;
-        const uint32_t xbar = bar(bar_xch(S, e, quad, (k >> 1) & 1));
-        float* const out = p.logits + ((int64_t)w.b * p.next_n) * p.logits_stride + s_tok;
-#pragma unroll
-        for (int j = 0; j < kMaxNext; ++j) {
-          if (j >= p.next_n) break;
-          float v = 0.0f;
-          bool any = false;
-#pragma unroll
-          for (int c = C0; c < C1; ++c)
-            if (c / cpj == j) {
-              v = any ? __fadd_rn(v, part[c - C0]) : part[c - C0];
-              any = true;
-            }
-          if (split && j == js) {
-            if (half == 1) {  // hand the upper part to the lower warp
-              xb[j * kTile + row] = v;
-              __syncwarp();
-              if (lane == 0) mbar_arrive(xbar);
-              continue;
-            }
-            if (!__all_sync(0xffffffffu, wait_phase(xbar, (uint32_t)(k >> 2) & 1u, abort))) {
-              live = false;
-              return;
-            }
-            v = __fadd_rn(v, xb[j * kTile + row]);
-          } else if (!any) {
-            continue;
-          }
-          if (s_tok < p.max_context) out[(int64_t)j * p.logits_stride] = valid ? v : -INFINITY;
-        }
-      };
-
-      Walker wk;
-      wk.init(p, b0, t0);
-      if (e == 1) wk.advance(p);
-      Walker nw = wk;
-      nw.advance(p);
-      nw.advance(p);
-      int32_t pid = e < n ? page_id(wk) : -1, pid_next = -1;
-      bool live = true;
-      int wg = -1;  // segment of the weights held
-      for (int k = e; k < n && live; k += 2) {
-        if (k + 2 < n) pid_next = page_id(nw);  // a tile ahead
-        if (!__all_sync(0xffffffffu,
-                        wait_phase(bar(bar_accf(S, k % 6)), (uint32_t)(k / 6) & 1u, abort)))
-          break;
-        if (wk.g != wg) {  // this warp's copy of the segment's head weights
-          const int64_t row0 = ((int64_t)wk.b * p.next_n) * p.H;
-          for (int i = lane; i < R; i += 32) wts[i] = __ldg(p.weights + row0 + i);
-          __syncwarp();
-          wg = wk.g;
-        }
-        const bool page_ok = pid >= 0 && pid < p.num_blocks;
-        if (half == 0)
-          tile(HalfAccT<0, kC1>(), k, wk, page_ok, live);
-        else
-          tile(HalfAccT<kC1, NCHUNK>(), k, wk, page_ok, live);
-        pid = pid_next;
-        wk = nw;
-        nw.advance(p);
-        nw.advance(p);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      s += 2;
+      if (s >= S) {
+        s -= S;
+        ph ^= 1u;
+      }
+      a += 2;
+      while (a >= A) {
+        a -= A;
+        pa ^= 1u;
       }
     }
+    if (lane == 0) misc[8 + m] = (uint32_t)(last + 1);  // for the drain after an abort
+  } else if (n > 0 && warp >= kEpiWarp) {
+    // ---- epilogue -------------------------------------------------------------
+    // Warp (quad, wq) reads chunks [c0, c1) of every accumulator for the 32
+    // tokens of its lane quadrant.  Its chunks hold whole query tokens: one
+    // token, or two single-chunk tokens when H = 32 (cpj == 1, CPW <= 2).
+    const int quad = warp & 3, wq = (warp - kEpiWarp) >> 2;  // TMEM lanes: warp id % 4
+    const int nch = R / 32, cpj = p.H / 32;
+    const int c0 = wq * p.cpw, cw = min(p.cpw, nch - c0);
+    if (cw > 0) {
+      const int row = quad * 32 + lane;  // the tile's token = TMEM lane
+      const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+      float* const wts = sW + (quad * kMaxChunks + c0) * 32;  // this warp's chunk weights
+      const int tok0 = c0 / cpj;                               // first query token
+      const bool two = cpj == 1 && cw == 2;
+      Walk w;
+      w.init(p, st, start[0], start[1]);
+      // per segment: this warp's weights (and in prefill its tokens' key
+      // ranges), the next segment's loaded one segment ahead
+      float wn[CPW];
+      int an[2], bn[2], ac[2] = {0, 0}, bc[2] = {0, 0};
+      auto load_seg = [&](int g) {
+        const SegQ q = seg_q(p, g);
+        const bool live = g < p.nseg;
+#pragma unroll
+        for (int i = 0; i < CPW; ++i) {
+          const int r = 32 * (c0 + i) + lane;  // the segment's query row
+          wn[i] = (i < cw && live && r < q.ntok * p.H)
+                      ? __ldg(p.weights + (int64_t)q.qt0 * p.H + r)
+                      : 0.0f;
+        }
+        if (p.mode == kModePrefill) {
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int t = q.qt0 + tok0 + i;
+            const bool in = live && tok0 + i < q.ntok;
+            an[i] = in ? min(max(__ldg(p.ks + t), 0), p.ncols) : 0;
+            bn[i] = in ? min(max(__ldg(p.ke + t), 0), p.ncols) : 0;
+          }
+        }
+      };
+      auto enter_seg = [&](int g) {
+#pragma unroll
+        for (int i = 0; i < CPW; ++i)
+          if (i < cw) wts[i * 32 + lane] = wn[i];
+        ac[0] = an[0];
+        ac[1] = an[1];
+        bc[0] = bn[0];
+        bc[1] = bn[1];
+        __syncwarp();
+        SegRange r;
+        load_seg(st.next(p, g, r));
+      };
+      // decode: this warp's page of the tile (-1 past the context), loaded a
+      // tile ahead and only compared when the tile is stored, so the load's
+      // latency stays off the per-tile chain
+      auto page_id = [&](const Walk& x) -> int32_t {
+        if (p.mode != kModeDecode) return 0;
+        const int pidx = x.t * 2 + (quad >> 1);
+        if (pidx * kKvBlock >= x.lim) return -1;
+        return __ldg(p.block_table + (int64_t)x.q.b * p.bt_stride + pidx);
+      };
+      load_seg(w.g);
+      Walk nw = w;
+      int32_t pid = page_id(w), pid_next = -1;
+      int a = 0, se = 0;
+      uint32_t pa = 0;
+      for (int k = 0; k < n; ++k) {
+        if (w.first) enter_seg(w.g);
+        if (k + 1 < n) {
+          nw.advance(p, st);
+          pid_next = page_id(nw);
+        }
+        if (!__all_sync(0xffffffffu, wait_phase(bar_accf(a), pa, abort))) break;
+        // The tile's MMAs have completed, so its stage (and, after a
+        // segment's last tile, the segment's query buffer) can be refilled.
+        if (warp == kEpiWarp && lane == 0) {
+          mbar_arrive(bar_empty(se));
+          if (k + 1 == n || w.last_of_segment()) mbar_arrive(bar_qempty(w.qi % QB));
+        }
+        if (++se == S) se = 0;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        float v0 = 0.0f, v1 = 0.0f;
+        const uint32_t col = lane_base + (uint32_t)a * (uint32_t)R + 32u * (uint32_t)c0;
+#pragma unroll
+        for (int i = 0; i < CPW; ++i) {
+          if (i < cw) {
+            uint32_t x[32];
+            tmem_ld32(tmem + col + 32u * i, x);
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            if (i == cw - 1) {  // every load of the tile done: release the accumulator
+              asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar_acce(a));
+            }
+            const float part = weighted_relu_sum(x, wts + i * 32);
+            if (i == 0)
+              v0 = part;
+            else if (two)
+              v1 = part;
+            else
+              v0 = __fadd_rn(v0, part);
+          }
+        }
+        const int s_tok = w.t * kTile + row;
+        const bool pok = pid >= 0 && pid < p.num_blocks;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          if (i == 1 && !two) break;
+          const int qt = w.q.qt0 + tok0 + i;  // query token
+          const bool valid = p.mode == kModeDecode ? (s_tok < w.lim && pok)
+                                                   : (s_tok >= ac[i] && s_tok < bc[i]);
+          if (tok0 + i < w.q.ntok && s_tok < p.ncols)
+            __stcs(p.logits + (int64_t)qt * p.logits_stride + s_tok,
+                   valid ? (i == 0 ? v0 : v1) : -INFINITY);
+        }
+        if (++a == A) {
+          a = 0;
+          pa ^= 1u;
+        }
+        w = nw;
+        pid = pid_next;
+      }
+    }
+  } else if (n == 0 && warp == kProducerWarp) {
+    // ---- no work tiles: only this CTA's share of the -inf tiles -------------
+    Filler fill;
+    fill.init(p, st, start[3], start[4], start[5]);
+    fill.run(p, st, start[5], lane);
+  }
 
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    __syncthreads();
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (n > 0) {
     if (*abort) {  // every role has stopped: let copies in flight land first
-      if (warp >= kProducerWarp && warp < kMmaWarp && lane == 0)  // its own stages
-        for (int q = issued - 1; q >= 0 && q >= issued - S; q -= kProducers)
-          wait_phase_drain(bar(bar_full(q % S)), (uint32_t)(q / S) & 1u);
+      if (warp >= kProducerWarp && warp < kProducerWarp + kProducers && lane == 0) {
+        for (int q = last_issued; q >= 0 && q > last_issued - S; q -= kProducers)
+          wait_phase_drain(bar_full(q % S), (uint32_t)(q / S) & 1u);
+        for (int b = 0; b < QB; ++b)
+          if (q_issued[b] >= 0) wait_phase_drain(bar_qfull(b), (uint32_t)q_issued[b]);
+      }
+      // MMAs in flight land before TMEM is released.  (Without an abort the
+      // epilogue has waited for every one.)  With one accumulator, tile k's
+      // MMAs start only after tile k-1's completed, so only the later of the
+      // two issuers' last tiles can be in flight: waiting on the other's
+      // phase could match a newer phase of the same parity.
+      if (warp >= kIssuerWarp && warp < kIssuerWarp + kIssuers && lane == 0) {
+        const int m = warp - kIssuerWarp;
+        const int last = (int)misc[8 + m] - 1, other = (int)misc[9 - m] - 1;
+        if (last >= 0 && (A > 1 || last > other))
+          wait_phase_drain(bar_accf(last % A), (uint32_t)(last / A) & 1u);
+      }
       if (tid == 0) flag_error(p.err, FP4IDX_ERRFLAG_TIMEOUT);
       __syncthreads();
     }
     if (warp == 0)
       asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                   "r"(p.tmem_cols)
+                   "r"(kTmemCols)
                    : "memory");
-  }
-
-  // ---- -inf for tiles past each context, spread over the grid's warps ------
-  const long long items = (long long)p.batch * p.tiles_total;
-  const int gwarps = gridDim.x * (kThreads / 32);
-  for (long long it = (long long)blockIdx.x * (kThreads / 32) + warp; it < items; it += gwarps) {
-    const int b = (int)(it / p.tiles_total), t = (int)(it % p.tiles_total);
-    if (t < work_tiles(ctx_eff(p, b))) continue;
-    for (int j = 0; j < p.next_n; ++j) {
-      float* out = p.logits + ((int64_t)b * p.next_n + j) * p.logits_stride;
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int s = t * kTile + 32 * m + lane;
-        if (s < p.max_context) out[s] = -INFINITY;
-      }
-    }
   }
 }
 
+// ---------------------------------------------------------------- host side
 bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -744,37 +1044,108 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-    tried = true;
-  }
-  return fn;
-}
-
-typedef void (*ScorerKernel)(ScorerParams, CUtensorMap);
-
-ScorerKernel kernel_for(int nchunk) {
-  switch (nchunk) {
-    case 1: return scorer_kernel<1>;
-    case 2: return scorer_kernel<2>;
-    case 3: return scorer_kernel<3>;
-    default: return scorer_kernel<4>;
-  }
-}
-
 struct DeviceInfo {
   bool ready = false;
   int sms = 0;
   int smem_optin = 0;
 };
+
+std::mutex g_setup_mutex;
+DeviceInfo g_info[64];
+EncodeTiledFn g_encode = nullptr;
+bool g_encode_tried = false;
+
+// One-time per-device set-up (SM count, shared-memory opt-in) and the driver
+// entry point of cuTensorMapEncodeTiled, under a lock.
+fp4idx_status device_setup(DeviceInfo& out, EncodeTiledFn& enc) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP4IDX_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  if (!g_encode_tried) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(f);
+    g_encode_tried = true;
+  }
+  DeviceInfo& di = g_info[dev];
+  if (!di.ready) {
+    DeviceInfo t;
+    if (cudaDeviceGetAttribute(&t.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&t.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(scorer_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             t.smem_optin) != cudaSuccess ||
+        cudaFuncSetAttribute(scorer_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             t.smem_optin) != cudaSuccess ||
+        cudaFuncSetAttribute(scorer_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             t.smem_optin) != cudaSuccess)
+      return FP4IDX_ERR_CUDA;
+    t.ready = true;
+    di = t;
+  }
+  out = di;
+  enc = g_encode;
+  return enc ? FP4IDX_OK : FP4IDX_ERR_CUDA;
+}
+
+// Heads both scorers accept: a multiple of 32, at most 128 (a segment holds
+// at least one query token's heads).
+bool heads_ok(int64_t H) { return H >= 32 && H % 32 == 0 && H <= kMaxRows; }
+
+// Fills the launch-shape fields of p (accumulators, query buffers, chunks
+// per epilogue warp, stages) and launches.
+fp4idx_status launch(ScorerParams& p, const uint8_t* q_fp4, const uint8_t* kv_cache,
+                     cudaStream_t stream) {
+  DeviceInfo di;
+  EncodeTiledFn encode = nullptr;
+  const fp4idx_status ds = device_setup(di, encode);
+  if (ds != FP4IDX_OK) return ds;
+  const int R = p.R;  // <= 128: 3 accumulators + scale words fit 512 TMEM columns
+  const int nch = R / 32, cpj = p.H / 32;
+  (void)nch;
+  p.cpw = cpj;  // chunks per epilogue warp: one query token's heads
+  int S = kMaxStages;
+  while (S > kProducers && (int)make_layout(S, R).total + 1024 > di.smem_optin) S -= kProducers;
+  if ((int)make_layout(S, R).total + 1024 > di.smem_optin) return FP4IDX_ERR_SHAPE;
+  p.stages = S;
+  const int smem_bytes = (int)make_layout(S, R).total + 1024;
+  p.tiles_total = (p.ncols + kTile - 1) / kTile;
+
+  // The cache as a 3-D byte tensor: 64 payload bytes x 64 slots x pages.
+  alignas(64) CUtensorMap kmap;
+  {
+    const cuuint64_t gdim[3] = {64, 64, (cuuint64_t)p.num_blocks};
+    const cuuint64_t gstride[2] = {64, (cuuint64_t)kPageBytes};
+    const cuuint32_t box[3] = {64, 64, 1};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    if (encode(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(kv_cache), gdim,
+               gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+        CUDA_SUCCESS)
+      return FP4IDX_ERR_CUDA;
+  }
+  // The queries as rows of 64 bytes; a segment's R rows are one box (rows
+  // past the last query row read as zeros).
+  alignas(64) CUtensorMap qmap;
+  {
+    const cuuint64_t gdim[2] = {64, (cuuint64_t)p.num_q * (cuuint64_t)p.H};
+    const cuuint64_t gstride[1] = {64};
+    const cuuint32_t box[2] = {64, (cuuint32_t)R};
+    const cuuint32_t estride[2] = {1, 1};
+    if (encode(&qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(q_fp4), gdim,
+               gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+        CUDA_SUCCESS)
+      return FP4IDX_ERR_CUDA;
+  }
+  if (cudaPeekAtLastError() != cudaSuccess) return FP4IDX_ERR_CUDA;  // an earlier error
+  auto kern = p.cpw <= 1 ? scorer_kernel<1> : p.cpw <= 2 ? scorer_kernel<2> : scorer_kernel<4>;
+  kern<<<(unsigned)di.sms, kThreads, smem_bytes, stream>>>(p, kmap, qmap);
+  return cudaPeekAtLastError() == cudaSuccess ? FP4IDX_OK : FP4IDX_ERR_CUDA;
+}
 
 }  // namespace
 
@@ -787,36 +1158,17 @@ extern "C" fp4idx_status fp4idx_paged_mqa_logits(
   if (batch == 0 || max_context == 0) return FP4IDX_OK;
   if (!q_fp4 || !q_scale || !weights || !kv_cache || !block_table || !context_lens || !logits)
     return FP4IDX_ERR_NULL;
-  if (next_n < 1 || num_heads < 32 || num_heads % 32 != 0 || next_n * num_heads > kMaxRows ||
-      num_blocks < 1 || num_blocks >= (1ll << 31) || max_context >= (1 << 30) ||
-      batch >= (1 << 30) || logits_stride < max_context ||
+  if (next_n < 1 || !heads_ok(num_heads) || num_blocks < 1 || num_blocks >= (1ll << 31) ||
+      max_context >= (1 << 30) || next_n >= (1 << 20) ||
+      batch * next_n >= (1ll << 31) / num_heads ||
+      logits_stride < max_context ||
       block_table_stride < (max_context + kKvBlock - 1) / kKvBlock)
     return FP4IDX_ERR_SHAPE;
   if (!aligned(q_fp4, 16) || !aligned(q_scale, 4) || !aligned(weights, 4) ||
       !aligned(kv_cache, 16) || !aligned(block_table, 4) || !aligned(context_lens, 4) ||
       !aligned(logits, 4) || (err_flags && !aligned(err_flags, 4)))
     return FP4IDX_ERR_ALIGN;
-
-  static DeviceInfo info[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP4IDX_ERR_CUDA;
-  DeviceInfo& di = info[dev];
-  if (!di.ready) {
-    if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&di.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
-            cudaSuccess)
-      return FP4IDX_ERR_CUDA;
-    for (int c = 1; c <= 4; ++c)
-      if (cudaFuncSetAttribute(kernel_for(c), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               di.smem_optin) != cudaSuccess)
-        return FP4IDX_ERR_CUDA;
-    di.ready = true;
-  }
-  EncodeTiledFn encode = encode_fn();
-  if (encode == nullptr) return FP4IDX_ERR_CUDA;
-
-  ScorerParams p;
-  p.q_fp4 = q_fp4;
+  ScorerParams p = {};
   p.q_scale = q_scale;
   p.weights = weights;
   p.cache = kv_cache;
@@ -827,36 +1179,56 @@ extern "C" fp4idx_status fp4idx_paged_mqa_logits(
   p.num_blocks = num_blocks;
   p.bt_stride = block_table_stride;
   p.logits_stride = logits_stride;
-  p.batch = (int32_t)batch;
+  p.mode = kModeDecode;
+  // A sequence's next_n tokens form one segment when their rows fit the MMA's
+  // N = 128, otherwise groups of 128 / H tokens sharing the sequence's keys.
+  p.tps = (int32_t)(next_n * num_heads <= kMaxRows ? next_n : kMaxRows / num_heads);
   p.next_n = (int32_t)next_n;
+  p.ngroups = (int32_t)((next_n + p.tps - 1) / p.tps);
+  p.nseg = (int32_t)(batch * p.ngroups);
+  p.num_q = (int32_t)(batch * next_n);
   p.H = (int32_t)num_heads;
-  p.R = (int32_t)(next_n * num_heads);
-  p.max_context = (int32_t)max_context;
-  p.tiles_total = (int32_t)((max_context + kTile - 1) / kTile);
-  uint32_t cols = 32;
-  while (cols < (uint32_t)kAccs * (uint32_t)p.R + 24u + 8u * kQBufs) cols <<= 1;
-  p.tmem_cols = cols;
-  // As many stages as fit in one CTA's shared memory (one CTA per SM).
-  int S = kMaxStages - kMaxStages % kProducers;  // a multiple of the producer count
-  while (S > kProducers && (int)make_layout(S, p.R).total + 1024 > di.smem_optin)
-    S -= kProducers;
-  if ((int)make_layout(S, p.R).total + 1024 > di.smem_optin) return FP4IDX_ERR_SHAPE;
-  p.stages = S;
-  const int smem_bytes = (int)make_layout(S, p.R).total + 1024;
+  p.R = p.tps * p.H;
+  p.ncols = (int32_t)max_context;
+  return launch(p, q_fp4, kv_cache, static_cast<cudaStream_t>(stream));
+}
 
-  // The cache as a 3-D byte tensor: 64 payload bytes x 64 slots x pages.
-  alignas(64) CUtensorMap tmap;
-  const cuuint64_t gdim[3] = {64, 64, (cuuint64_t)num_blocks};
-  const cuuint64_t gstride[2] = {64, (cuuint64_t)kPageBytes};
-  const cuuint32_t box[3] = {64, 64, 1};
-  const cuuint32_t estride[3] = {1, 1, 1};
-  if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(kv_cache), gdim,
-             gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
-      CUDA_SUCCESS)
-    return FP4IDX_ERR_CUDA;
-
-  kernel_for(p.R / 32)<<<(unsigned)di.sms, kThreads, smem_bytes,
-                          static_cast<cudaStream_t>(stream)>>>(p, tmap);
-  return cudaGetLastError() == cudaSuccess ? FP4IDX_OK : FP4IDX_ERR_CUDA;
+extern "C" fp4idx_status fp4idx_mqa_logits_prefill(
+    const uint8_t* q_fp4, const uint8_t* q_scale, const float* weights, const uint8_t* kv_cache,
+    int64_t num_blocks, int64_t num_keys, const int32_t* ks, const int32_t* ke, float* logits,
+    int64_t logits_stride, int64_t num_tokens, int64_t num_heads, uint32_t* err_flags,
+    void* stream) {
+  if (num_tokens < 0 || num_keys < 0) return FP4IDX_ERR_SHAPE;
+  if (num_tokens == 0 || num_keys == 0) return FP4IDX_OK;
+  if (!q_fp4 || !q_scale || !weights || !kv_cache || !ks || !ke || !logits)
+    return FP4IDX_ERR_NULL;
+  if (!heads_ok(num_heads) || num_blocks < 1 ||
+      num_blocks >= (1ll << 31) || num_keys >= (1 << 30) ||
+      num_keys > num_blocks * (int64_t)kKvBlock || num_tokens >= (1ll << 31) / num_heads ||
+      logits_stride < num_keys)
+    return FP4IDX_ERR_SHAPE;
+  if (!aligned(q_fp4, 16) || !aligned(q_scale, 4) || !aligned(weights, 4) ||
+      !aligned(kv_cache, 16) || !aligned(ks, 4) || !aligned(ke, 4) || !aligned(logits, 4) ||
+      (err_flags && !aligned(err_flags, 4)))
+    return FP4IDX_ERR_ALIGN;
+  ScorerParams p = {};
+  p.q_scale = q_scale;
+  p.weights = weights;
+  p.cache = kv_cache;
+  p.ks = ks;
+  p.ke = ke;
+  p.logits = logits;
+  p.err = err_flags;
+  p.num_blocks = num_blocks;
+  p.logits_stride = logits_stride;
+  p.mode = kModePrefill;
+  p.tps = (int32_t)(kMaxRows / num_heads);  // query tokens per segment
+  p.next_n = p.tps;
+  p.ngroups = 1;
+  p.nseg = (int32_t)((num_tokens + p.tps - 1) / p.tps);
+  p.num_q = (int32_t)num_tokens;
+  p.H = (int32_t)num_heads;
+  p.R = p.tps * p.H;
+  p.ncols = (int32_t)num_keys;
+  return launch(p, q_fp4, kv_cache, static_cast<cudaStream_t>(stream));
 }

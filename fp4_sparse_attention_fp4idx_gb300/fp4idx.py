@@ -68,6 +68,8 @@ _SIGS = {
         _INT, [_P, _I64, _I64, _P, _P, _P, _I64, _INT, _INT, _P, _I64, _P, _P]),
     "fp4idx_paged_mqa_logits": (
         _INT, [_P, _P, _P, _P, _I64, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _I64, _P, _P]),
+    "fp4idx_mqa_logits_prefill": (
+        _INT, [_P, _P, _P, _P, _I64, _I64, _P, _P, _P, _I64, _I64, _I64, _P, _P]),
     "fp4idx_status_string": (ctypes.c_char_p, [_INT]),
     "fp4idx_version": (ctypes.c_char_p, []),
 }
@@ -475,6 +477,46 @@ def paged_mqa_logits(q_fp4, q_scale, weights, kv_cache, block_table, context_len
         _ptr(block_table), bt_stride, _ptr(context_lens), _ptr(logits), out_stride, batch,
         next_n, H, int(max_context), _ptr(err_flags), _stream_ptr(stream))
     _check(st, "fp4idx_paged_mqa_logits")
+    return logits
+
+
+def mqa_logits_prefill(q_fp4, q_scale, weights, kv_cache, ks, ke, num_keys: int, *,
+                       logits=None, err_flags=None, stream=None):
+    """FP4 prefill MQA logits -> fp32 [T, num_keys]: query token t (q_fp4
+    uint8 [T, H, 64], q_scale uint8 [T, H, 4], weights fp32 [T, H]) against
+    the consecutive keys 0 .. num_keys-1 of kv_cache uint8 [num_blocks, 4352]
+    (key s at page s/64, offset s%64), over the keys in [ks[t], ke[t])
+    (int32 [T]); -inf elsewhere."""
+    torch = _torch()
+    _need(q_fp4, torch.uint8, "q_fp4", 3)
+    _need(q_scale, torch.uint8, "q_scale", 3)
+    _need(weights, torch.float32, "weights", 2)
+    _need(kv_cache, torch.uint8, "kv_cache", 2)
+    _need(ks, torch.int32, "ks", 1)
+    _need(ke, torch.int32, "ke", 1)
+    T, H, nb = q_fp4.shape
+    if nb != 64 or not q_fp4.is_contiguous():
+        raise ValueError("q_fp4 must be contiguous [T, H, 64]")
+    if tuple(q_scale.shape) != (T, H, 4) or not q_scale.is_contiguous():
+        raise ValueError("q_scale must be contiguous [T, H, 4]")
+    if tuple(weights.shape) != (T, H) or not weights.is_contiguous():
+        raise ValueError("weights must be contiguous [T, H]")
+    if tuple(ks.shape) != (T,) or tuple(ke.shape) != (T,) or not (
+            ks.is_contiguous() and ke.is_contiguous()):
+        raise ValueError("ks and ke must be contiguous [T]")
+    if kv_cache.shape[1] != PAGE_BYTES or not kv_cache.is_contiguous():
+        raise ValueError("kv_cache must be contiguous [num_blocks, 4352]")
+    if logits is None:
+        logits = torch.empty((T, num_keys), dtype=torch.float32, device=q_fp4.device)
+    _need(logits, torch.float32, "logits", 2)
+    if logits.shape[0] != T or logits.shape[1] < num_keys or logits.stride(1) != 1:
+        raise ValueError("logits must be [T, >= num_keys] with unit column stride")
+    out_stride = logits.stride(0) if T > 1 else logits.shape[1]
+    st = _lib.fp4idx_mqa_logits_prefill(
+        _ptr(q_fp4), _ptr(q_scale), _ptr(weights), _ptr(kv_cache), kv_cache.shape[0],
+        int(num_keys), _ptr(ks), _ptr(ke), _ptr(logits), out_stride, T, H, _ptr(err_flags),
+        _stream_ptr(stream))
+    _check(st, "fp4idx_mqa_logits_prefill")
     return logits
 
 

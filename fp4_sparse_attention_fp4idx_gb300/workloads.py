@@ -410,12 +410,33 @@ SCORER_CONFIGS = {
     "scorer_dsv_next2": (3, 2, 64, [128, 5, 640], 700, 35, False),
     "scorer_r96": (2, 3, 32, [450, 200], 450, 36, False),
     "scorer_h128": (2, 1, 128, [333, 129], 384, 37, True),
+    # more than 128 query rows per sequence: groups of 128 / H tokens
+    "scorer_dsv_next4": (3, 4, 64, [300, 64, 513], 520, 38, True),
+    "scorer_h64_next3": (2, 3, 64, [200, 450], 450, 39, False),
+    "scorer_h128_next2": (2, 2, 128, [129, 333], 384, 40, True),
+    "scorer_h96_next3": (2, 3, 96, [100, 200], 256, 42, False),
+    "scorer_h32_next8": (2, 8, 32, [130, 64], 200, 43, False),
+}
+
+
+# Many short sequences: every CTA spans several sequences, so the query
+# operand buffers are reused within a launch.
+SCORER_MANY = {
+    # name: (batch, next_n, H, max_context, seed)
+    "scorer_many_short": (900, 4, 32, 130, 81),
+    "scorer_many_short_r256": (700, 4, 64, 200, 82),
+    "scorer_many_short_r192": (800, 3, 64, 256, 83),
+    "scorer_many_short_r96": (900, 3, 32, 200, 84),
 }
 
 
 def make_scorer_config(name: str) -> ScorerWorkload:
     if name == "scorer_decode":
         return make_scorer_decode()
+    if name in SCORER_MANY:
+        b, n, h, mc, seed = SCORER_MANY[name]
+        rng = np.random.Generator(np.random.PCG64(seed + 1000))
+        return make_scorer(name, b, n, h, _ragged_lens(rng, b, 0, mc), mc, seed)
     b, n, h, lens, mc, seed, ext = SCORER_CONFIGS[name]
     return make_scorer(name, b, n, h, lens, mc, seed, extremes=ext)
 
@@ -426,3 +447,90 @@ def fp8_sentinel_cache(w: Workload) -> np.ndarray:
     seed = 7919 + 31 * w.T + w.H + sum(map(ord, w.name))
     rng = np.random.Generator(np.random.PCG64(seed))
     return rng.integers(0, 256, size=(w.num_blocks, KV_BLOCK * (HEAD_DIM + 4)), dtype=np.uint8)
+
+
+@dataclass
+class PrefillScorerWorkload:
+    """Inputs of the FP4 prefill MQA-logits scorer: T query tokens (packed
+    queries, exponent words, fp32 head weights) against num_keys consecutive
+    keys (key s at page s/64, offset s%64 of the cache), token t over the
+    keys [ks[t], ke[t])."""
+    name: str
+    T: int
+    H: int
+    num_keys: int
+    q_fp4: np.ndarray     # uint8 [T, H, 64]
+    q_scale: np.ndarray   # uint8 [T, H, 4]
+    weights: np.ndarray   # f32 [T, H]
+    kv_cache: np.ndarray  # uint8 [num_blocks, 4352]
+    ks: np.ndarray        # int32 [T]
+    ke: np.ndarray        # int32 [T]
+
+    @property
+    def num_blocks(self) -> int:
+        return int(self.kv_cache.shape[0])
+
+
+def make_prefill_scorer(name: str, T: int, H: int, num_keys: int, seed: int,
+                        ranges: str = "causal", exp_range=(118, 135),
+                        spare_blocks: int = 2) -> PrefillScorerWorkload:
+    """Bytes drawn as in make_scorer.  Key ranges:
+      causal  -- a prefill chunk whose T tokens are the last T of the
+                 num_keys keys: token t scores keys [0, num_keys - T + t + 1);
+      windows -- random ranges [a, b) inside [0, num_keys), some empty;
+      edges   -- ranges that need clamping or are empty: negative starts,
+                 ends past num_keys, a == b, a > b, tile-boundary ends."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    nb = -(-num_keys // KV_BLOCK) + spare_blocks
+    lo, hi = exp_range
+    cache = rng.integers(0, 256, size=(nb, PAGE_BYTES), dtype=np.uint8)
+    cache[:, KV_BLOCK * 64:] = rng.integers(lo, hi + 1, size=(nb, KV_BLOCK * 4), dtype=np.uint8)
+    q_fp4 = rng.integers(0, 256, size=(T, H, 64), dtype=np.uint8)
+    q_scale = rng.integers(lo, hi + 1, size=(T, H, 4), dtype=np.uint8)
+    weights = (rng.standard_normal((T, H)) / np.sqrt(H * HEAD_DIM)).astype(np.float32)
+    t = np.arange(T)
+    if ranges == "causal":
+        ks = np.zeros(T, np.int64)
+        ke = num_keys - T + t + 1
+    elif ranges == "windows":
+        a = rng.integers(0, num_keys, T)
+        b = rng.integers(0, num_keys + 1, T)
+        ks, ke = np.minimum(a, b), np.maximum(a, b)
+        ke[::7] = ks[::7]  # some empty ranges
+    elif ranges == "edges":
+        cands = [(-5, 10), (0, num_keys + 100), (-3, num_keys + 3), (7, 7), (50, 20),
+                 (128, 256), (127, 129), (num_keys - 1, num_keys), (num_keys, num_keys + 5),
+                 (-10, -2), (64, 65), (0, 1)]
+        pick = [cands[i % len(cands)] for i in range(T)]
+        ks = np.array([c[0] for c in pick], np.int64)
+        ke = np.array([c[1] for c in pick], np.int64)
+    else:
+        raise ValueError(ranges)
+    return PrefillScorerWorkload(name, T, H, num_keys, q_fp4, q_scale, weights, cache,
+                                 ks.astype(np.int32), ke.astype(np.int32))
+
+
+PREFILL_SCORER_CONFIGS = {
+    # name: (T, H, num_keys, seed, ranges)
+    "prefill_tiny_causal": (5, 32, 70, 61, "causal"),
+    "prefill_h32_causal": (300, 32, 300, 62, "causal"),
+    "prefill_h64_windows": (77, 64, 1000, 63, "windows"),
+    "prefill_h64_edges": (24, 64, 300, 64, "edges"),
+    "prefill_h128_causal": (33, 128, 500, 65, "causal"),
+    "prefill_h128_windows": (9, 128, 260, 66, "windows"),
+    "prefill_h96_edges": (13, 96, 129, 67, "edges"),
+}
+
+
+def make_prefill_scorer_config(name: str) -> PrefillScorerWorkload:
+    T, H, nk, seed, ranges = PREFILL_SCORER_CONFIGS[name]
+    return make_prefill_scorer(name, T, H, nk, seed, ranges)
+
+
+def make_prefill_scorer_chunk(T: int = 4096, H: int = 64, num_keys: int = 16384,
+                              seed: int = 71) -> PrefillScorerWorkload:
+    """A DeepSeek-shaped prefill chunk: H = 64 index heads, the last 4096
+    tokens of a 16384-token prompt, causal key ranges (about 12K keys per
+    token, 268 MB of logits)."""
+    return make_prefill_scorer("prefill_chunk", T, H, num_keys, seed, "causal")
+

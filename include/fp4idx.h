@@ -315,10 +315,11 @@ fp4idx_status fp4idx_rope_fake_quant(
  * exponent byte for the group d/32) and k_s the slot of token s: page
  * block_table[b, s/64], offset s%64, in the layout fp4idx_k_norm_rope_pack_store
  * writes.  The products are exact; sums are fp32 (tensor-core accumulation
- * over d, then the weighted head sum in two interleaved chains), so a logit
- * is within 2^-17 * sum_h |weights[t,h]| * sum_d |q[t,h,d] k_s[d]| of the
- * exact value (a bound from the fp32 rounding of at most 128 head terms and
- * 128 products).
+ * over d, then the weighted head sum in fixed-order packed chains), so a
+ * logit is within 2^-17 * sum_h |weights[t,h]| * sum_d |q[t,h,d] k_s[d]| of
+ * the exact value (a bound from the fp32 roundings of the tensor core's sum
+ * of 128 products and of the head sum, whose chains are at most 15
+ * additions deep; the tests hold every logit to it).
  *
  *   q_fp4        bytes [batch*next_n, num_heads, 64], dense, 16-byte aligned
  *                (the q_fp4 output of the calls above).
@@ -334,8 +335,10 @@ fp4idx_status fp4idx_rope_fake_quant(
  *   logits       fp32, row t at logits + t*logits_stride, columns
  *                [0, max_context) written, the rest untouched;
  *                logits_stride >= max_context.
- *   batch >= 0, next_n >= 1, num_heads a multiple of 32,
- *   next_n * num_heads <= 128, 0 <= max_context < 2^30.
+ *   batch >= 0, next_n >= 1, num_heads one of 32, 64, 96, 128 (a sequence
+ *   whose next_n * num_heads query rows exceed 128 is scored in groups of
+ *   128 / num_heads tokens, each group reading the sequence's keys once),
+ *   0 <= max_context < 2^30, batch * next_n * num_heads < 2^31.
  *   err_flags    optional device uint32: FP4IDX_ERRFLAG_PAGE for a bad
  *                block-table entry (those logits are -inf, nothing is read),
  *                FP4IDX_ERRFLAG_TIMEOUT if a copy or the tensor core did not
@@ -348,6 +351,40 @@ fp4idx_status fp4idx_paged_mqa_logits(
     int64_t block_table_stride, const int32_t* context_lens, float* logits,
     int64_t logits_stride, int64_t batch, int64_t next_n, int64_t num_heads,
     int64_t max_context, uint32_t* err_flags, void* stream);
+
+/*
+ * The prefill variant of the scorer: query tokens of a prefill chunk against
+ * the chunk's keys, each token over its own key range.  Source: "[HIP] Add
+ * FP4 output mode to indexer_qk_rope_quant_and_cache" (aiter PR 5484),
+ * Summary (the FP4 paged scorer "and its prefill variant" read the packed
+ * keys straight out of the cache).  The page prints no signature; reading
+ * taken: the keys are consecutive -- key s is the slot at page s/64, offset
+ * s%64 of kv_cache, which is what fp4idx_k_norm_rope_pack_store writes with
+ * slot_mapping[s] = s -- so there is no block table, and query token t
+ * scores the keys in [ks[t], ke[t]):
+ *   logits[t, s] = sum_h weights[t,h] * max(0, sum_d q[t,h,d] * k_s[d])
+ *     for max(ks[t], 0) <= s < min(ke[t], num_keys),
+ *   logits[t, s] = -inf for every other s < num_keys
+ * (an empty range gives a row of -inf), with the decode scorer's arithmetic
+ * and error bound.
+ *
+ *   q_fp4, q_scale, weights  as above, [num_tokens, num_heads, ...].
+ *   kv_cache     bytes [num_blocks, 4352], 16-byte aligned, read only;
+ *                num_keys <= num_blocks * 64.  Exponent bytes <= 254.
+ *   ks, ke       int32 [num_tokens].
+ *   logits       fp32, row t at logits + t*logits_stride, columns
+ *                [0, num_keys) written, the rest untouched;
+ *                logits_stride >= num_keys.
+ *   num_heads one of 32, 64, 96, 128; 0 <= num_keys < 2^30;
+ *   num_tokens * num_heads < 2^31.
+ *   err_flags    optional: FP4IDX_ERRFLAG_TIMEOUT as above.
+ * num_tokens == 0 or num_keys == 0 returns FP4IDX_OK and enqueues nothing.
+ */
+fp4idx_status fp4idx_mqa_logits_prefill(
+    const uint8_t* q_fp4, const uint8_t* q_scale, const float* weights,
+    const uint8_t* kv_cache, int64_t num_blocks, int64_t num_keys,
+    const int32_t* ks, const int32_t* ke, float* logits, int64_t logits_stride,
+    int64_t num_tokens, int64_t num_heads, uint32_t* err_flags, void* stream);
 
 /* Static, NUL-terminated description of a status code. */
 const char* fp4idx_status_string(fp4idx_status status);

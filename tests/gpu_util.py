@@ -169,3 +169,38 @@ def assert_logits_close(got: np.ndarray, want: np.ndarray, mag: np.ndarray, what
     assert not bad.any(), (what, int(bad.sum()), float(err[bad].max()),
                            np.argwhere(fin)[np.flatnonzero(bad)[:5]].tolist())
     return float((err / np.maximum(mag[fin], 1e-300)).max()) if err.size else 0.0
+
+
+# ---------------------------------------------------------- prefill scorer
+def prefill_oracle(pw: wl.PrefillScorerWorkload):
+    return oracle.mqa_logits_prefill(pw.q_fp4, pw.q_scale, pw.weights, pw.kv_cache, pw.ks,
+                                     pw.ke, pw.num_keys)
+
+
+def prefill_magnitude(pw: wl.PrefillScorerWorkload) -> np.ndarray:
+    """sum_h |w| * sum_d |q k| per logit (the oracle on sign-cleared inputs)."""
+    cache = pw.kv_cache.copy()
+    cache[:, :wl.KV_BLOCK * 64] &= 0x77
+    out, _ = oracle.mqa_logits_prefill(pw.q_fp4 & 0x77, pw.q_scale, np.abs(pw.weights), cache,
+                                       pw.ks, pw.ke, pw.num_keys)
+    return out
+
+
+class DevicePrefillScorer:
+    def __init__(self, pw: wl.PrefillScorerWorkload, device="cuda"):
+        self.pw = pw
+        self.q_fp4 = dev(pw.q_fp4, device)
+        self.q_scale = dev(pw.q_scale, device)
+        self.weights = dev(pw.weights, device)
+        self.cache = dev(pw.kv_cache, device)
+        self.ks = dev(pw.ks, device)
+        self.ke = dev(pw.ke, device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def run(self, logits=None):
+        out = F().mqa_logits_prefill(self.q_fp4, self.q_scale, self.weights, self.cache, self.ks,
+                                     self.ke, self.pw.num_keys, logits=logits,
+                                     err_flags=self.err)
+        torch.cuda.synchronize()
+        return out
+

@@ -31,7 +31,8 @@ def test_exports_every_declared_symbol(F):
                           "fp4idx_indexer_prepass", "fp4idx_paged_mqa_logits",
                           "fp4idx_k_norm_rope_pack_store_ex", "fp4idx_q_rope_pack_weights_ex",
                           "fp4idx_indexer_prepass_ex", "fp4idx_rope_fake_quant",
-                          "fp4idx_status_string", "fp4idx_version"}
+                          "fp4idx_mqa_logits_prefill", "fp4idx_status_string",
+                          "fp4idx_version"}
     out = subprocess.run(["nm", "-D", "--defined-only", F.LIB_PATH], capture_output=True,
                          text=True, check=True).stdout
     exported = set(re.findall(r"\bT (fp4idx_\w+)", out))
@@ -222,8 +223,8 @@ S_DEFECTS = [
     (dict(next_n=0), "ERR_SHAPE"),
     (dict(H=16), "ERR_SHAPE"),
     (dict(H=48), "ERR_SHAPE"),
-    (dict(H=64, next_n=3), "ERR_SHAPE"),
     (dict(H=160), "ERR_SHAPE"),
+    (dict(H=288), "ERR_SHAPE"),
     (dict(nb=0), "ERR_SHAPE"),
     (dict(nb=1 << 40), "ERR_SHAPE"),
     (dict(max_ctx=1 << 30), "ERR_SHAPE"),
@@ -244,6 +245,50 @@ S_DEFECTS = [
 @pytest.mark.parametrize("over,code", S_DEFECTS, ids=_ids(S_DEFECTS))
 def test_scorer_host_checks(F, over, code):
     assert _call_s(F, _s_args(**over)) == getattr(F, code)
+
+
+def _p_args(**over):
+    a = dict(qf=A[12], qs=A[13], w=A[14], cache=A[6], nb=16, nk=1000, ks=A[15], ke=A[16],
+             out=A[17], os=1000, T=7, H=64, err=None, stream=None)
+    a.update(over)
+    return a
+
+
+def _call_p(F, a):
+    return F.lib().fp4idx_mqa_logits_prefill(
+        a["qf"], a["qs"], a["w"], a["cache"], a["nb"], a["nk"], a["ks"], a["ke"], a["out"],
+        a["os"], a["T"], a["H"], a["err"], a["stream"])
+
+
+P_DEFECTS = [
+    (dict(T=-1), "ERR_SHAPE"),
+    (dict(nk=-1), "ERR_SHAPE"),
+    (dict(qf=None), "ERR_NULL"),
+    (dict(ks=None), "ERR_NULL"),
+    (dict(ke=None), "ERR_NULL"),
+    (dict(out=None), "ERR_NULL"),
+    (dict(H=16), "ERR_SHAPE"),
+    (dict(H=80), "ERR_SHAPE"),
+    (dict(H=288), "ERR_SHAPE"),
+    (dict(H=160), "ERR_SHAPE"),
+    (dict(nb=0), "ERR_SHAPE"),
+    (dict(nk=16 * 64 + 1), "ERR_SHAPE"),
+    (dict(os=999), "ERR_SHAPE"),
+    (dict(qf=A[12] + 4), "ERR_ALIGN"),
+    (dict(cache=A[6] + 8), "ERR_ALIGN"),
+    (dict(ks=A[15] + 2), "ERR_ALIGN"),
+    (dict(out=A[17] + 2), "ERR_ALIGN"),
+]
+
+
+@pytest.mark.fake_ptr
+@pytest.mark.parametrize("over,code", P_DEFECTS, ids=_ids(P_DEFECTS))
+def test_prefill_scorer_host_checks(F, over, code):
+    assert _call_p(F, _p_args(**over)) == getattr(F, code)
+
+
+def test_prefill_scorer_empty_is_a_no_op(F):
+    assert _call_p(F, _p_args(T=0)) == F.OK and _call_p(F, _p_args(nk=0)) == F.OK
 
 
 @pytest.mark.fake_ptr

@@ -17,7 +17,7 @@ from tests.gpu_util import (DeviceScorer, DeviceWorkload, F, SCORER_TOL,
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("name", sorted(wl.SCORER_CONFIGS))
+@pytest.mark.parametrize("name", sorted(wl.SCORER_CONFIGS) + sorted(wl.SCORER_MANY))
 def test_scorer_parity(name):
     sw = wl.make_scorer_config(name)
     got = DeviceScorer(sw)
@@ -91,7 +91,8 @@ def test_scorer_host_checks_on_device():
         return lib.fp4idx_paged_mqa_logits(*a)
 
     assert call(H=48) == f.ERR_SHAPE
-    assert call(H=64, next_n=3) == f.ERR_SHAPE
+    assert call(H=160) == f.ERR_SHAPE   # more heads than one segment holds
+    assert call(H=288) == f.ERR_SHAPE
     assert call(next_n=0) == f.ERR_SHAPE
     assert call(os=sw.max_context - 1) == f.ERR_SHAPE
     assert call(bts=1) == f.ERR_SHAPE
