@@ -99,6 +99,32 @@ def traffic_record(kernel: str):
     return None
 
 
+def spread(ms) -> dict:
+    """Median, min, 90th percentile and mean of per-launch times (ms)."""
+    a = np.asarray(list(ms), np.float64)
+    return {"median": round(float(np.median(a)), 5), "min": round(float(a.min()), 5),
+            "p90": round(float(np.percentile(a, 90)), 5), "mean": round(float(a.mean()), 5),
+            "n": int(a.size)}
+
+
+def time_launches(launch, flush, steps: int, warmup: int, stream) -> list:
+    """CUDA-event time (ms) of `steps` launches on `stream`, the L2 flushed
+    before each (outside its events), after `warmup` untimed launches."""
+    import torch
+    for _ in range(warmup):
+        flush()
+        launch()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for a, b in ev:
+        flush()
+        a.record(stream)
+        launch()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -396,20 +422,11 @@ def run_variants(F, w, D, dev, peak, flush, steps: int = 100, warmup: int = 5) -
                 q8.data_ptr() if mode else qf.data_ptr(), None if mode else qs.data_ptr(),
                 wt.data_ptr(), H, p["pos"], p["cos"], p["sin"], w.max_pos,
                 w.rope_style, T, opts, None, st.cuda_stream)
-        for _ in range(warmup):
-            flush()
-            _ok(F, fn(*args))
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(steps)]
-        for a, b in ev:
-            flush()
-            a.record(st)
-            _ok(F, fn(*args))
-            b.record(st)
-        torch.cuda.synchronize()
-        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        sp = spread(time_launches(lambda: _ok(F, fn(*args)), flush, steps, warmup, st))
+        ms = sp["median"]
         gbs = nbytes / (ms / 1e3) / 1e9
-        out[name] = {"ms_per_launch": round(ms, 5), "tokens_per_s": round(T / (ms / 1e3), 1),
+        out[name] = {"ms_per_launch": ms, "ms_spread": sp,
+                     "tokens_per_s": round(T / (ms / 1e3), 1),
                      "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
                      "algorithmic_bytes_per_launch": nbytes,
                      "kernel": prepass_kernel_name(H)}
@@ -422,20 +439,11 @@ def run_variants(F, w, D, dev, peak, flush, steps: int = 100, warmup: int = 5) -
     for name, mode in (("fake_quant_ue8m0_32", 0), ("fake_quant_e4m3_16", 1)):
         args = (p["q"], 128, H, p["pos"], p["cos"], p["sin"], w.max_pos, w.rope_style, mode,
                 qo.data_ptr(), T * H, None, st.cuda_stream)
-        for _ in range(warmup):
-            flush()
-            _ok(F, fq(*args))
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(steps)]
-        for a, b in ev:
-            flush()
-            a.record(st)
-            _ok(F, fq(*args))
-            b.record(st)
-        torch.cuda.synchronize()
-        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        sp = spread(time_launches(lambda: _ok(F, fq(*args)), flush, steps, warmup, st))
+        ms = sp["median"]
         gbs = nbytes / (ms / 1e3) / 1e9
-        out[name] = {"ms_per_launch": round(ms, 5), "rows_per_s": round(T * H / (ms / 1e3), 1),
+        out[name] = {"ms_per_launch": ms, "ms_spread": sp,
+                     "rows_per_s": round(T * H / (ms / 1e3), 1),
                      "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
                      "algorithmic_bytes_per_launch": nbytes, "kernel": "fake_quant_kernel"}
     return out
@@ -455,13 +463,36 @@ def scorer_bytes(sw) -> int:
                + rows * sw.max_context * 4)
 
 
-def run_scorer(F, dev, peak, flush, steps: int, warmup: int = 5) -> dict:
-    """The FP4 paged MQA-logits scorer on the GLM-5.2-style decode workload:
-    CUDA-event time per launch (L2 flushed before each, outside the events)
-    and its HBM roofline."""
+def prefill_scorer_bytes(pw) -> int:
+    """Bytes one prefill-scorer launch must move at minimum: every key's
+    68-byte slot once, per query row 64 + 4 + 4 bytes, per token its two
+    int32 range bounds, and the fp32 logits written (num_tokens * num_keys
+    * 4, -inf outside the ranges included)."""
+    return int(pw.num_keys * 68 + pw.T * pw.H * 72 + pw.T * 8 + pw.T * pw.num_keys * 4)
+
+
+def _scorer_record(name, ms_list, nbytes, flops, peak, extra):
+    sp = spread(ms_list)
+    ms = sp["median"]
+    achieved = nbytes / (ms / 1e3) / 1e9
+    tr = traffic_record(name)
+    rec = dict(extra)
+    rec.update({
+        "ms_per_launch": ms, "ms_spread": sp,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "kernel": name,
+                     "algorithmic_bytes_per_launch": nbytes,
+                     "traffic": tr["dram_bytes_per_launch"] if tr else None},
+        "mxf4_tflops": round(flops / (ms / 1e3) / 1e12, 1),
+        "l2": "flushed before every launch, outside the CUDA events"})
+    return rec
+
+
+def run_decode_scorer(F, sw, dev, peak, flush, steps: int, warmup: int = 5) -> dict:
+    """One paged-scorer workload: CUDA-event time per launch and its HBM
+    roofline (algorithmic bytes count every cached key once, also where a
+    sequence's query rows are scored in several groups)."""
     import torch
-    from fp4_sparse_attention_fp4idx_gb300 import workloads as wl
-    sw = wl.make_scorer_decode()
 
     def d(a):
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
@@ -470,65 +501,209 @@ def run_scorer(F, dev, peak, flush, steps: int, warmup: int = 5) -> dict:
     bt, ctx = d(sw.block_table), d(sw.context_lens)
     rows = sw.batch * sw.next_n
     out = torch.empty((rows, sw.max_context), dtype=torch.float32, device=dev)
-    for _ in range(warmup):
-        flush()
-        F.paged_mqa_logits(qf, qs, wt, cache, bt, ctx, sw.max_context, next_n=sw.next_n,
-                           logits=out)
+    F.paged_mqa_logits(qf, qs, wt, cache, bt, ctx, sw.max_context, next_n=sw.next_n, logits=out)
     torch.cuda.synchronize()
     fn = F.lib().fp4idx_paged_mqa_logits
     stream = torch.cuda.current_stream()
     args = (qf.data_ptr(), qs.data_ptr(), wt.data_ptr(), cache.data_ptr(), sw.num_blocks,
             bt.data_ptr(), bt.stride(0), ctx.data_ptr(), out.data_ptr(), out.stride(0),
             sw.batch, sw.next_n, sw.H, sw.max_context, None, stream.cuda_stream)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(steps)]
-    for a, b in ev:
-        flush()
-        a.record(stream)
-        _ok(F, fn(*args))
-        b.record(stream)
-    torch.cuda.synchronize()
-    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    nbytes = scorer_bytes(sw)
-    tr = traffic_record("scorer_kernel")
+    ms = time_launches(lambda: _ok(F, fn(*args)), flush, steps, warmup, stream)
     ctx_tokens = int(np.minimum(np.maximum(sw.context_lens, 0), sw.max_context).sum())
-    achieved = nbytes / (ms / 1e3) / 1e9
-    flops = 2.0 * 128 * sw.next_n * sw.H * ctx_tokens
-    return {
+    med = float(np.median(ms))
+    groups = max(1, -(-sw.next_n * sw.H // 128))
+    return _scorer_record("scorer_kernel", ms, scorer_bytes(sw),
+                          2.0 * 128 * sw.next_n * sw.H * ctx_tokens, peak, {
         "workload": sw.name, "batch": sw.batch, "next_n": sw.next_n, "H": sw.H,
         "max_context": sw.max_context, "cached_tokens": ctx_tokens,
         "kv_cache_bytes": int(sw.kv_cache.nbytes), "launches": steps,
-        "ms_per_launch": round(ms, 5),
-        "scored_keys_per_s": round(ctx_tokens * sw.next_n / (ms / 1e3), 1),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "kernel": "scorer_kernel", "algorithmic_bytes_per_launch": nbytes,
-                     "traffic": tr["dram_bytes_per_launch"] if tr else None},
-        "mxf4_tflops": round(flops / (ms / 1e3) / 1e12, 1),
-        "l2": "flushed before every launch, outside the CUDA events",
-    }
+        "query_groups_per_sequence": groups,
+        "scored_keys_per_s": round(ctx_tokens * sw.next_n / (med / 1e3), 1)})
+
+
+def run_prefill_scorer(F, pw, dev, peak, flush, steps: int, warmup: int = 5) -> dict:
+    """The prefill scorer on a prefill chunk: CUDA-event time per launch and
+    its HBM roofline (algorithmic bytes count every key once)."""
+    import torch
+
+    def d(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    qf, qs, wt, cache = d(pw.q_fp4), d(pw.q_scale), d(pw.weights), d(pw.kv_cache)
+    ks, ke = d(pw.ks), d(pw.ke)
+    out = torch.empty((pw.T, pw.num_keys), dtype=torch.float32, device=dev)
+    F.mqa_logits_prefill(qf, qs, wt, cache, ks, ke, pw.num_keys, logits=out)
+    torch.cuda.synchronize()
+    fn = F.lib().fp4idx_mqa_logits_prefill
+    stream = torch.cuda.current_stream()
+    args = (qf.data_ptr(), qs.data_ptr(), wt.data_ptr(), cache.data_ptr(), pw.num_blocks,
+            pw.num_keys, ks.data_ptr(), ke.data_ptr(), out.data_ptr(), out.stride(0), pw.T,
+            pw.H, None, stream.cuda_stream)
+    ms = time_launches(lambda: _ok(F, fn(*args)), flush, steps, warmup, stream)
+    lo = np.clip(pw.ks.astype(np.int64), 0, pw.num_keys)
+    hi = np.clip(pw.ke.astype(np.int64), 0, pw.num_keys)
+    scored = int(np.maximum(hi - lo, 0).sum())
+    med = float(np.median(ms))
+    return _scorer_record("scorer_kernel", ms, prefill_scorer_bytes(pw),
+                          2.0 * 128 * pw.H * scored, peak, {
+        "workload": pw.name, "T": pw.T, "H": pw.H, "num_keys": pw.num_keys,
+        "scored_pairs": scored, "launches": steps,
+        "scored_keys_per_s": round(scored / (med / 1e3), 1)})
+
+
+def run_scorer(F, dev, peak, flush, steps: int) -> dict:
+    """The FP4 scorer on three workloads: GLM-5.2-style decode (H 32,
+    next_n 4, 128 sequences up to 64K tokens), DeepSeek-style decode with
+    H 64 and next_n 4 (256 query rows per sequence, scored in two groups of
+    128), and a DeepSeek-shaped prefill chunk (4096 query tokens, 16384
+    keys, causal)."""
+    from fp4_sparse_attention_fp4idx_gb300 import workloads as wl
+    out = {"decode": run_decode_scorer(F, wl.make_scorer_decode(), dev, peak, flush, steps)}
+    out["decode_h64_next4"] = run_decode_scorer(
+        F, wl.make_scorer_decode(batch=64, H=64, name="scorer_decode_h64"), dev, peak, flush,
+        steps)
+    out["prefill_chunk"] = run_prefill_scorer(F, wl.make_prefill_scorer_chunk(), dev, peak,
+                                              flush, max(20, steps // 4))
+    return out
+
+
+# ------------------------------------------------------------ accuracy
+def unquantised_logits(e) -> np.ndarray:
+    """The indexer score without any quantisation, in fp64: keys RMSNorm'd
+    (gamma, eps) and rotated, queries rotated (exact angles p * 10000^(-2i/64)
+    on dims 0..63), then sum_h w * max(0, q_h . k) with the head weights
+    w * H^-1/2 * 128^-1/2.  Logits [batch*next_n, ctx]."""
+    f = lambda b: (np.asarray(b, np.uint32) << 16).view(np.float32).astype(np.float64)
+    i = np.arange(32, dtype=np.float64)
+    inv = 10000.0 ** (-2.0 * i / 64)
+
+    def rope(x, pos):
+        th = pos[:, None].astype(np.float64) * inv[None, :]
+        c, s_ = np.cos(th), np.sin(th)
+        if x.ndim == 3:
+            c, s_ = c[:, None, :], s_[:, None, :]
+        y = x.copy()
+        if e.rope_style == 0:
+            a, b = x[..., :32], x[..., 32:64]
+            y[..., :32], y[..., 32:64] = a * c - b * s_, b * c + a * s_
+        else:
+            a, b = x[..., 0:64:2], x[..., 1:64:2]
+            y[..., 0:64:2], y[..., 1:64:2] = a * c - b * s_, b * c + a * s_
+        return y
+
+    k = f(e.k)
+    k = k / np.sqrt((k * k).mean(axis=1, keepdims=True) + e.eps) * f(e.gamma)[None, :]
+    k = rope(k, e.k_positions)
+    q = rope(f(e.q), e.q_positions)
+    w = f(e.w) / np.sqrt(e.H * 128.0)
+    out = np.empty((e.batch * e.next_n, e.ctx))
+    for b in range(e.batch):
+        kb = k[b * e.ctx:(b + 1) * e.ctx]
+        for j in range(e.next_n):
+            t = b * e.next_n + j
+            dots = q[t] @ kb.T  # [H, ctx]
+            out[t] = (w[t][:, None] * np.maximum(dots, 0.0)).sum(axis=0)
+    return out
+
+
+def score_agreement(got: np.ndarray, ref: np.ndarray, k: int = 64) -> dict:
+    """Cosine similarity of two logit arrays (over all entries), the mean
+    top-k overlap per row (a pick counts when its reference value reaches the
+    reference's k-th largest, so ties do not count against it), and the max
+    absolute difference."""
+    g, r = got.astype(np.float64).ravel(), ref.astype(np.float64).ravel()
+    cos = float(g @ r / (np.linalg.norm(g) * np.linalg.norm(r)))
+    ov = []
+    for gr, rr in zip(got, ref):
+        kk = min(k, rr.size)
+        thresh = np.partition(rr, -kk)[-kk]
+        picks = np.argpartition(gr, -kk)[-kk:]
+        ov.append(float(np.mean(rr[picks] >= thresh)))
+    return {"cosine": round(cos, 7), f"top{k}_overlap": round(float(np.mean(ov)), 4),
+            "max_abs_err": float(np.max(np.abs(g - r)))}
+
+
+def indexer_pipeline(F, e, device):
+    """The whole path on the GPU through the public API: keys into the paged
+    cache, queries packed with their head weights, then the paged scorer.
+    Returns (logits [batch*next_n, ctx] fp32, cache, q_fp4, q_scale, weights)
+    as numpy arrays."""
+    import torch
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+    def d(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+    cache = torch.zeros((e.num_blocks, F.PAGE_BYTES), dtype=torch.uint8, device=device)
+    cs, sn = d(e.cos), d(e.sin)
+    F.k_norm_rope_pack_store(bf(e.k), bf(e.gamma), d(e.k_positions), cs, sn, d(e.slot_mapping),
+                             cache, eps=e.eps, rope_style=e.rope_style)
+    qf, qs, wt = F.q_rope_pack_weights(bf(e.q), bf(e.w), d(e.q_positions), cs, sn,
+                                       rope_style=e.rope_style)
+    logits = F.paged_mqa_logits(qf, qs, wt, cache, d(e.block_table), d(e.context_lens), e.ctx,
+                                next_n=e.next_n)
+    torch.cuda.synchronize()
+    return tuple(x.cpu().numpy() for x in (logits, cache, qf, qs, wt))
+
+
+def run_accuracy(F, device) -> dict:
+    """The FP4 indexer path (pre-pass then scorer, all on the GPU) against
+    the unquantised fp64 score, at GLM-5.2 shapes (H 32, D 128, kv_block 64),
+    next_n 1 and 4: 4 sequences of 2048 tokens."""
+    from fp4_sparse_attention_fp4idx_gb300 import workloads as wl
+    out = {}
+    for nn in (1, 4):
+        e = wl.make_indexer_e2e(next_n=nn)
+        got = indexer_pipeline(F, e, device)[0]
+        out[f"next_n_{nn}"] = score_agreement(got, unquantised_logits(e))
+    out["reference"] = ("unquantised fp64 indexer score from the same bf16 inputs (RMSNorm, "
+                        "RoPE at exact angles, no FP4 rounding); the FP4 path against its own "
+                        "oracle is held to cosine >= 0.999999 and top-64 overlap 1.0 by "
+                        "tests/test_e2e_accuracy_gpu.py")
+    return out
+
+
+def _oracle_rate(w, S: int) -> float:
+    """Seconds the oracle takes for the keys and queries of the first S
+    tokens of the workload."""
+    import oracle
+    cache = w.cache_init.copy()
+    t0 = time.perf_counter()
+    oracle.k_norm_rope_pack_store(w.k[:S], w.gamma, w.eps, w.positions[:S], w.cos, w.sin,
+                                  w.rope_style, w.slot_mapping[:S], cache)
+    oracle.q_rope_pack_weights(w.q[:S], w.w[:S], w.positions[:S], w.cos, w.sin, w.rope_style)
+    return time.perf_counter() - t0
+
+
+def _oracle_sample(w, budget_s: float):
+    """(S, seconds): S grown by 4x from 64 tokens until a run takes about a
+    quarter of budget_s."""
+    S = 64
+    while True:
+        dt = _oracle_rate(w, S)
+        if dt * 4 > budget_s or S >= w.T:
+            return S, dt
+        S = min(w.T, S * 4)
 
 
 def cpu_baseline(w, budget_s: float = 12.0):
-    """The oracle as it stands, single-threaded, on the first S tokens of the
-    workload (keys and queries), S grown until about budget_s of CPU work."""
+    """The oracle as it stands on the host cores: on all of them (its token
+    loops run in parallel; this is the reported value) and on one, each on
+    the first S tokens of the workload (keys and queries), S grown until
+    about budget_s of work."""
     import oracle
     oracle.build()
-    S = 64
-    while True:
-        sub_q, sub_w, pos = w.q[:S], w.w[:S], w.positions[:S]
-        cache = w.cache_init.copy()
-        t0 = time.perf_counter()
-        oracle.k_norm_rope_pack_store(w.k[:S], w.gamma, w.eps, pos, w.cos, w.sin,
-                                      w.rope_style, w.slot_mapping[:S], cache)
-        oracle.q_rope_pack_weights(sub_q, sub_w, pos, w.cos, w.sin, w.rope_style)
-        dt = time.perf_counter() - t0
-        if dt * 4 > budget_s or S >= w.T:
-            break
-        S = min(w.T, S * 4)
-    return {"value": S / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+    with oracle.threads() as n:
+        S, dt = _oracle_sample(w, budget_s)
+    with oracle.threads(1):
+        S1, dt1 = _oracle_sample(w, budget_s / 2)
+    return {"value": round(S / dt, 1), "unit": "tokens/s", "cores": n, "kind": "oracle",
             "sample": f"first {S} of {w.T} tokens of the {w.name} workload (H={w.H}), "
-                      f"keys and queries, single thread, {dt:.2f} s"}
+                      f"keys and queries, {n} threads, {dt:.2f} s",
+            "single_thread": {"value": round(S1 / dt1, 1), "unit": "tokens/s", "cores": 1,
+                              "sample": f"first {S1} tokens, 1 thread, {dt1:.2f} s"}}
 
 
 def run_ours(args):
@@ -547,7 +722,8 @@ def run_ours(args):
     D = upload(w, dev)
     sampler = ClockSampler(local) if rank == 0 else None
     r = time_device(F, w, D, args.mode, args.steps, args.warmup, flush, dist, sampler)
-    step_ms = statistics.mean(r["step_ms"])
+    step_sp = spread(r["step_ms"])
+    step_ms = step_sp["median"]
     step_ms_all = max_over_ranks(step_ms, dist, dev)
     ab = algorithmic_bytes(w, args.mode)
     value = weak_scaling_value(ws, w.T, step_ms_all)
@@ -557,7 +733,7 @@ def run_ours(args):
     if args.mode == "fused":
         kbytes, kms = ab["fused"], step_ms
     else:
-        kbytes, kms = ab["q_call"], statistics.mean(r["q_ms"])
+        kbytes, kms = ab["q_call"], float(np.median(r["q_ms"]))
     achieved = kbytes / (kms / 1e3) / 1e9
     tr = traffic_record(kname)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -575,26 +751,29 @@ def run_ours(args):
                 continue
             wx = wl.make(name)
             Dx = upload(wx, dev)
-            rx = time_device(F, wx, Dx, args.mode, 100, 5, flush)
-            ms = statistics.mean(rx["step_ms"])
+            rx = time_device(F, wx, Dx, args.mode, 200, 5, flush)
+            sp = spread(rx["step_ms"])
+            ms = sp["median"]
             bx = algorithmic_bytes(wx, args.mode)["step"]
-            extra[name] = {"T": wx.T, "H": wx.H, "ms_per_step": round(ms, 5),
+            extra[name] = {"T": wx.T, "H": wx.H, "ms_per_step": ms, "ms_spread": sp,
                            "tokens_per_s": round(wx.T / (ms / 1e3), 1),
                            "gbs": round(bx / (ms / 1e3) / 1e9, 1),
                            "frac_of_peak": round(bx / (ms / 1e3) / 1e9 / peak, 4)}
             del Dx
 
-    scorer = variants = None
+    scorer = variants = accuracy = None
     if rank == 0 and not args.no_extra and args.mode == "fused":
         variants = run_variants(F, w, D, dev, peak, flush)
     if rank == 0 and not args.no_extra:
         scorer = run_scorer(F, dev, peak, flush, 200)
+        accuracy = run_accuracy(F, dev)
 
     base = cpu_baseline(w) if (rank == 0 and ws == 1 and not args.no_cpu) else None
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms_all, 5),
+            "ms_per_step_spread": step_sp,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.name, "T": w.T, "H": w.H, "head_dim": 128, "rope_dim": 64,
@@ -617,10 +796,11 @@ def run_ours(args):
             "other_configs": extra,
             "variants": variants,
             "scorer": scorer,
+            "accuracy": accuracy,
         }
         if args.mode != "fused":
-            line["k_ms"] = round(statistics.mean(r["k_ms"]), 5)
-            line["q_ms"] = round(statistics.mean(r["q_ms"]), 5)
+            line["k_ms"] = round(float(np.median(r["k_ms"])), 5)
+            line["q_ms"] = round(float(np.median(r["q_ms"])), 5)
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -634,6 +814,8 @@ def run_reference(args):
     import oracle
     from fp4_sparse_attention_fp4idx_gb300 import workloads as wl
     oracle.build()
+    oracle.set_threads(oracle.threads_available())
+    cores = oracle.get_threads()
     w = wl.make(args.workload)
     S = min(w.T, args.ref_tokens)
     cache = w.cache_init.copy()
@@ -652,7 +834,7 @@ def run_reference(args):
     dt = (time.perf_counter() - t0) / args.steps
     value = S / dt
     sample = (f"first {S} of {w.T} tokens of the {w.name} workload (H={w.H}) per step, "
-              "keys and queries, single thread")
+              f"keys and queries, {cores} threads")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
@@ -661,7 +843,7 @@ def run_reference(args):
         "config": {"workload": w.name, "T": w.T, "H": w.H, "head_dim": 128, "rope_dim": 64,
                    "rope_style": "neox" if w.rope_style == 0 else "interleaved",
                    "kv_blocks": w.num_blocks, "mode": "oracle"},
-        "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": 1,
+        "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": cores,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -677,7 +859,7 @@ def main(argv=None):
     ap.add_argument("--workload", default="large_prefill",
                     choices=["tiny", "decode", "prefill", "large_prefill", "mtp"])
     ap.add_argument("--mode", choices=["fused", "separate"], default="fused")
-    ap.add_argument("--ref-tokens", type=int, default=512,
+    ap.add_argument("--ref-tokens", type=int, default=4096,
                     help="tokens per step of the reference (oracle) arm")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")

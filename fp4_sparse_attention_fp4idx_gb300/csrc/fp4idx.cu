@@ -1137,6 +1137,13 @@ const char* fp4idx_status_string(fp4idx_status status) {
   return "unknown status";
 }
 
-const char* fp4idx_version(void) { return "fp4idx 0.4.0 sm_103a"; }
+const char* fp4idx_version(void) { return "fp4idx 0.5.0 sm_103a"; }
+
+// H^-1/2 * D^-1/2 with D = 128, evaluated in double and rounded once to fp32;
+// 0 for a non-positive head count.
+float fp4idx_default_weight_scale(int64_t num_heads) {
+  if (num_heads < 1) return 0.0f;
+  return (float)(1.0 / sqrt((double)num_heads * (double)FP4IDX_HEAD_DIM));
+}
 
 }  // extern "C"

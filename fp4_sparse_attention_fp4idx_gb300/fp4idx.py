@@ -15,7 +15,6 @@ Two layers:
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 import re
 
@@ -70,6 +69,7 @@ _SIGS = {
         _INT, [_P, _P, _P, _P, _I64, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _I64, _P, _P]),
     "fp4idx_mqa_logits_prefill": (
         _INT, [_P, _P, _P, _P, _I64, _I64, _P, _P, _P, _I64, _I64, _I64, _P, _P]),
+    "fp4idx_default_weight_scale": (_F, [_I64]),
     "fp4idx_status_string": (ctypes.c_char_p, [_INT]),
     "fp4idx_version": (ctypes.c_char_p, []),
 }
@@ -139,9 +139,9 @@ def rope_style_code(style) -> int:
     raise ValueError(f"unknown rope style {style!r}")
 
 
-def default_weight_scale(num_heads: int, head_dim: int = HEAD_DIM) -> float:
-    """fp32(H^-1/2 * D^-1/2), evaluated in double."""
-    return float(ctypes.c_float(1.0 / math.sqrt(num_heads * head_dim)).value)
+def default_weight_scale(num_heads: int) -> float:
+    """The library's head-weight scale, fp32(H^-1/2 * 128^-1/2)."""
+    return float(_lib.fp4idx_default_weight_scale(int(num_heads)))
 
 
 # ------------------------------------------------------------ torch wrappers

@@ -391,14 +391,15 @@ def _ragged_lens(rng, batch: int, lo: int, hi: int) -> np.ndarray:
 
 
 def make_scorer_decode(batch: int = 128, next_n: int = 4, H: int = 32,
-                       max_context: int = 65536, seed: int = 21) -> ScorerWorkload:
+                       max_context: int = 65536, seed: int = 21,
+                       name: str = "scorer_decode") -> ScorerWorkload:
     """GLM-5.2-style decode with multi-token prediction: H = 32 index heads,
     next_n = 4 query tokens per sequence, 128 sequences with context lengths
     uniform in [max_context/4, max_context] (about 5.2M cached tokens, 350 MB
     of index-K cache, 134 MB of logits)."""
     rng = np.random.Generator(np.random.PCG64(seed + 1000))
     lens = _ragged_lens(rng, batch, max_context // 4, max_context)
-    return make_scorer("scorer_decode", batch, next_n, H, lens, max_context, seed)
+    return make_scorer(name, batch, next_n, H, lens, max_context, seed)
 
 
 SCORER_CONFIGS = {
@@ -534,3 +535,56 @@ def make_prefill_scorer_chunk(T: int = 4096, H: int = 64, num_keys: int = 16384,
     token, 268 MB of logits)."""
     return make_prefill_scorer("prefill_chunk", T, H, num_keys, seed, "causal")
 
+
+
+@dataclass
+class IndexerE2E:
+    """Raw bf16 inputs of the whole indexer path for `batch` sequences of
+    `ctx` tokens: every token's key (to be normalised, rotated, quantised and
+    stored through slot_mapping into shuffled pages), and the last next_n
+    tokens' queries and head weights.  Keys of sequence b are tokens
+    b*ctx .. b*ctx + ctx - 1 at positions 0 .. ctx-1; its query token j sits
+    at position ctx - next_n + j."""
+    name: str
+    batch: int
+    ctx: int
+    next_n: int
+    H: int
+    rope_style: int
+    k: np.ndarray            # bf16 bits [batch*ctx, 128]
+    k_positions: np.ndarray  # int64 [batch*ctx]
+    slot_mapping: np.ndarray  # int64 [batch*ctx]
+    gamma: np.ndarray        # bf16 bits [128]
+    eps: float
+    q: np.ndarray            # bf16 bits [batch*next_n, H, 128]
+    w: np.ndarray            # bf16 bits [batch*next_n, H]
+    q_positions: np.ndarray  # int64 [batch*next_n]
+    cos: np.ndarray
+    sin: np.ndarray
+    num_blocks: int
+    block_table: np.ndarray  # int32 [batch, ctx/64]
+    context_lens: np.ndarray  # int32 [batch]
+
+
+def make_indexer_e2e(batch: int = 4, ctx: int = 2048, next_n: int = 4, H: int = 32,
+                     rope_style: int = ROPE_NEOX, seed: int = 91) -> IndexerE2E:
+    """GLM-5.2-shaped indexer inputs (H = 32, D = 128, kv_block 64): N(0,1)
+    bf16 keys, queries and head weights, gamma ~ 1 + 0.1 N(0,1), each
+    sequence's pages a random permutation of the pool."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    assert ctx % KV_BLOCK == 0
+    pages = ctx // KV_BLOCK
+    nb = batch * pages
+    perm = rng.permutation(nb).astype(np.int64)
+    bt = perm.reshape(batch, pages).astype(np.int32)
+    tok = np.arange(batch * ctx)
+    b, s = tok // ctx, tok % ctx
+    slots = perm.reshape(batch, pages)[b, s // KV_BLOCK] * KV_BLOCK + s % KV_BLOCK
+    cos, sin = rope_tables(ctx)
+    qpos = np.tile(np.arange(ctx - next_n, ctx, dtype=np.int64), batch)
+    return IndexerE2E(f"indexer_e2e_b{batch}_c{ctx}_n{next_n}_h{H}", batch, ctx, next_n, H,
+                      rope_style, _normal_bf16(rng, (batch * ctx, HEAD_DIM)),
+                      s.astype(np.int64), slots.astype(np.int64), _gamma(rng), 1e-6,
+                      _normal_bf16(rng, (batch * next_n, H, HEAD_DIM)),
+                      _normal_bf16(rng, (batch * next_n, H)), qpos, cos, sin, nb, bt,
+                      np.full(batch, ctx, np.int32))

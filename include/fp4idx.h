@@ -386,6 +386,17 @@ fp4idx_status fp4idx_mqa_logits_prefill(
     const int32_t* ks, const int32_t* ke, float* logits, int64_t logits_stride,
     int64_t num_tokens, int64_t num_heads, uint32_t* err_flags, void* stream);
 
+/*
+ * The head-weight scale the pages use: H^-1/2 * D^-1/2 with D = 128,
+ * evaluated in double and rounded once to fp32 (0 when num_heads < 1).  Pass
+ * it as weight_scale to the query calls above.  Sources: "[HIP] Add FP4
+ * output mode to indexer_qk_rope_quant_and_cache" (aiter PR 5484), API (the
+ * head weights carry the plain weight; the scorer applies its own scalar);
+ * "dsv4.1: RoPE and FP4 packing kernels" (sglang PR 39656), Summary (the
+ * indexer head weights of the query op).
+ */
+float fp4idx_default_weight_scale(int64_t num_heads);
+
 /* Static, NUL-terminated description of a status code. */
 const char* fp4idx_status_string(fp4idx_status status);
 

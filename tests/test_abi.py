@@ -31,8 +31,8 @@ def test_exports_every_declared_symbol(F):
                           "fp4idx_indexer_prepass", "fp4idx_paged_mqa_logits",
                           "fp4idx_k_norm_rope_pack_store_ex", "fp4idx_q_rope_pack_weights_ex",
                           "fp4idx_indexer_prepass_ex", "fp4idx_rope_fake_quant",
-                          "fp4idx_mqa_logits_prefill", "fp4idx_status_string",
-                          "fp4idx_version"}
+                          "fp4idx_mqa_logits_prefill", "fp4idx_default_weight_scale",
+                          "fp4idx_status_string", "fp4idx_version"}
     out = subprocess.run(["nm", "-D", "--defined-only", F.LIB_PATH], capture_output=True,
                          text=True, check=True).stdout
     exported = set(re.findall(r"\bT (fp4idx_\w+)", out))
@@ -382,3 +382,20 @@ def test_product_and_oracle_are_independent():
         assert not re.search(r"^\s*(import|from)\s+fp4_sparse_attention_fp4idx_gb300\b",
                              text, re.M), p
         assert not re.search(r"#\s*include\s*[<\"]fp4idx\.h", text), p
+
+
+def test_default_weight_scale_closed_form(F):
+    """The library's head-weight scale is H^-1/2 * 128^-1/2 rounded once to
+    fp32 (aiter PR 5484, API; sglang PR 39656, Summary); exact powers of two
+    where H * 128 is a power of four."""
+    import numpy as np
+    from fractions import Fraction
+    assert F.default_weight_scale(32) == 1.0 / 64 and F.default_weight_scale(128) == 1.0 / 128
+    for H in (1, 8, 12, 17, 32, 48, 64, 96, 128, 1000):
+        got = F.default_weight_scale(H)
+        want = np.float32(1.0 / np.sqrt(np.float64(H) * 128.0))
+        assert got == float(want), H
+        # within half an fp32 ulp of the exact value
+        exact = 1.0 / (H * 128) ** 0.5
+        assert abs(Fraction(got) - Fraction(exact)) <= Fraction(float(np.spacing(want))) / 2 * (1 + 1e-9)
+    assert F.default_weight_scale(0) == 0.0

@@ -74,17 +74,13 @@ def test_fp8_random_scales_both_styles():
         assert_fp8_same(w.name, run_gpu(dw, "fused"), run_ref(w))
 
 
-def test_fp8_large_prefill_cache_full_size():
-    """The bench workload (T = 65536, H = 64) in the FP8 mode, keys only:
-    the whole 16384-page cache against the oracle."""
+def test_fp8_large_prefill_full_size():
+    """The bench workload (T = 65536, H = 64) in the FP8 mode, one fused
+    launch: the whole 16384-page cache, every query code and every weight
+    against the oracle (run on all host cores)."""
     w = wl.make("large_prefill")
     dw = DeviceWorkload(w)
-    f = F()
-    cache = dev(wl.fp8_sentinel_cache(w))
-    f.k_norm_rope_fp8_store(dw.k, dw.gamma, dw.pos, dw.cos, dw.sin, dw.slots, cache, eps=w.eps,
-                            rope_style=w.rope_style)
-    torch.cuda.synchronize()
-    want = wl.fp8_sentinel_cache(w)
-    oracle.k_norm_rope_fp8_store(w.k, w.gamma, w.eps, w.positions, w.cos, w.sin, w.rope_style,
-                                 w.slot_mapping, want)
-    assert_bytes_equal(cache.cpu().numpy(), want, "large_prefill fp8 kv_cache")
+    got = run_gpu(dw, "fused")
+    with oracle.threads():
+        want = run_ref(w)
+    assert_fp8_same("large_prefill", got, want)

@@ -105,9 +105,9 @@ def test_scorer_host_checks_on_device():
 
 def test_scorer_full_size_sampled():
     """The full decode workload (128 sequences, next_n 4, H 32, contexts up to
-    65,536) in the bench's launch configuration; 3 sequences checked against
-    the oracle (the shortest, the longest and one more), the -inf padding of
-    all sequences checked everywhere."""
+    65,536) in the bench's launch configuration; 12 sequences checked against
+    the oracle on all host cores (the shortest, the longest and ten more),
+    the -inf padding of all sequences checked everywhere."""
     sw = wl.make_scorer_decode()
     ds = DeviceScorer(sw)
     out = ds.run().cpu().numpy()
@@ -117,11 +117,15 @@ def test_scorer_full_size_sampled():
         r = slice(b * sw.next_n, (b + 1) * sw.next_n)
         assert np.all(np.isneginf(out[r, lens[b]:]))
         assert np.all(np.isfinite(out[r, :lens[b]]))
-    seqs = [int(np.argmin(lens)), int(np.argmax(lens)), 77]
+    rng = np.random.Generator(np.random.PCG64(78))
+    seqs = sorted({int(np.argmin(lens)), int(np.argmax(lens)),
+                   *rng.choice(sw.batch, 10, replace=False).tolist()})
     sub = sw.rows_of(seqs)
-    want, st = scorer_oracle(sub)
+    with oracle.threads():
+        want, st = scorer_oracle(sub)
+        mag = scorer_magnitude(sub)
     assert st == 0
-    assert_logits_close(out[sub.notes["rows"]], want, scorer_magnitude(sub), "decode sampled")
+    assert_logits_close(out[sub.notes["rows"]], want, mag, "decode sampled")
 
 
 def test_prepass_then_scorer_pipeline():

@@ -11,6 +11,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from fp4_sparse_attention_fp4idx_gb300 import workloads as wl
 from tests.gpu_util import DeviceWorkload, F, assert_same, run_oracle
 
@@ -41,15 +42,15 @@ def test_variant_random_both_styles(style):
     assert_same(w, gpu, run_oracle(w, compress_ratio=2, hadamard=True))
 
 
-def test_prefill_hadamard_sampled():
-    """The prefill workload (8,192 tokens, H = 64) with the rotation: whole
-    cache, queries of 512 sampled tokens."""
+def test_prefill_hadamard_full():
+    """The prefill workload (8,192 tokens, H = 64) with the rotation: the
+    whole cache and every query output (the oracle on all host cores)."""
     w = wl.make("prefill")
     dw = DeviceWorkload(w)
     gpu = dw.run("fused", hadamard=True)
-    rng = np.random.Generator(np.random.PCG64(62))
-    tokens = np.unique(np.concatenate([np.arange(32), rng.choice(w.T, 480, replace=False)]))
-    assert_same(w, gpu, run_oracle(w, tokens, hadamard=True), tokens)
+    with oracle.threads():
+        ref = run_oracle(w, hadamard=True)
+    assert_same(w, gpu, ref)
 
 
 def test_default_options_match_plain_calls():
