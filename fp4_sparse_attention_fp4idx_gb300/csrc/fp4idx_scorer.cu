@@ -19,44 +19,55 @@
 //
 // Work.  A segment is a set of query rows sharing one key range: a sequence
 // (next_n tokens) in the decode scorer, a block of consecutive query tokens
-// in the prefill scorer; R = tokens x H rows (R <= 256) form the MMA's N.  A
-// tile is 128 consecutive keys (two 64-slot pages) of a segment's range.
-// The persistent grid splits the list of all (segment, tile) work items into
-// equal contiguous shares, one per CTA, from the context lengths / key ranges
-// alone; a share may span several segments.  Columns outside the ranges
-// (-inf) are split the same way and written alongside by one warp.
+// in the prefill scorer; R = tokens x H <= 128 rows form the MMA's N (a
+// sequence with more rows is split into groups of 128 / H tokens).  A tile
+// is 128 consecutive keys (two 64-slot pages) of a segment's range.  The
+// persistent grid splits the list of all (segment, tile) work items into
+// equal contiguous shares, one per CTA, from the context lengths / key
+// ranges alone; a share may span several segments.  Columns outside the
+// ranges (-inf) are split the same way.
 //
 // MMA.  Keys are A (M = 128), the segment's query rows B (N = R), K = 128 as
 // two MMAs of K = 64 into an fp32 TMEM accumulator.  Each exponent word of a
 // slot is exactly one TMEM scale-factor cell (group g in byte g; the K halves
 // use bytes 0-1 and 2-3).
 //
-// Roles (20 warps, five per SM sub-partition, so 96 registers a thread).
-// Every role keeps its per-tile chain short: the tile rate of a
-// one-CTA-per-SM pipeline is set by the longest serial chain of dependent
-// instructions in any one warp, not by the copy latency.
-//   warps 2-3    producers: tile k belongs to producer k % 2.  Lane 0 waits
-//                for the stage (and at a segment start issues the TMA copy of
-//                the segment's query operand); lanes 0 and 1 then issue, one
-//                page each, the TMA tensor copies of the page payloads
-//                (64-byte swizzled, the layout the MMA reads) and bulk copies
-//                of their exponent words.  The warp fetches the page ids of
-//                16 of its tiles per load, a batch ahead.  While it waits for
-//                free stages it writes this CTA's share of the -inf columns
-//                outside every segment's range.
-//   warps 0-1    issuers: tile k belongs to issuer k % 2.  Once a tile has
-//                landed, the warp transposes its 128 exponent words (and at
-//                its first tile of a segment the queries' words) into the
-//                32 x 128-bit blocks tcgen05.cp reads; lane 0 then issues
-//                tcgen05.cp into TMEM, the two MMAs into accumulator k % A
-//                and the commit.
-//   warps 4-19   epilogue: warp w reads TMEM lane quadrant w % 4 (tokens
-//                32(w%4) .. +31, one per thread) and a fixed run of the
-//                accumulator's 32-column chunks, chosen so that a query
-//                token's heads never span two warps; every warp takes every
-//                tile, so a tile's read-out is spread over all 16 warps.
-//                Warp 4 frees a tile's stage (and at a segment's last tile its
-//                query buffer) once the tile's MMAs have completed.
+// Roles (16 warps, four per SM sub-partition, so 128 registers a thread).
+// The tile rate of a one-CTA-per-SM pipeline is set by the longest serial
+// chain of dependent instructions that one warp runs per tile, not by the
+// copy latency: an mbarrier operation costs one thread on the order of a
+// hundred cycles and a copy issue about fifty.  So consecutive tiles are
+// taken in pairs that share one stage and one full / empty barrier pair,
+// and issuer m, accumulator m and epilogue group m form a private pipeline
+// for the tiles k = m (mod 3).
+//   warp 3       producer, a pair per step.  Every 16 tiles, a batch ahead,
+//                its lanes describe the batch's tiles in parallel (page ids,
+//                a header word per tile, the segment's first query row).  Per
+//                pair, lanes 4h .. 4h + 3 wait for the stage, then issue the
+//                TMA tensor copies of tile h's two page payloads (64-byte
+//                swizzled, the layout the MMA reads) and the bulk copies of
+//                their exponent words; lane 0 first writes the two header
+//                words and, at a segment's first tile, loads the segment's
+//                query operand and scale words into a query buffer (in
+//                segment order) and makes the buffer releases of the issuers
+//                that have no tile in the segment.
+//   warps 0-2    issuers: tile k belongs to issuer m = k % 3.  Once the pair
+//                has landed, the warp transposes the tile's 128 exponent
+//                words (and at its first tile of a segment the queries'
+//                words) into the 32 x 128-bit blocks tcgen05.cp reads; lane
+//                0 then issues tcgen05.cp into TMEM, the two MMAs into
+//                accumulator m and commits that mark the accumulator full,
+//                the tile's half of the stage free and, after the issuer's
+//                last tile of a segment, its share of the segment's query
+//                buffer free (a buffer is free once three releases came).
+//   warps 4-15   epilogue: group m = (w - 4) / 4 reads accumulator m; one
+//                warp of the group waits for it while the others wait at the
+//                group's named barrier; warp w of the group reads TMEM lane
+//                quadrant w % 4 (keys 32(w%4) .. +31 of the tile, one per
+//                thread) over every query row, frees the accumulator once its
+//                loads are done, then forms and stores the logits.  Between
+//                tiles each warp writes its share of the -inf columns outside
+//                every segment's range.
 // Every wait is bounded (1 s) and a shared abort flag stops every role;
 // copies and MMAs in flight are waited for before TMEM and shared memory are
 // released.  Each E2M1 product is exact; the tensor core accumulates in
@@ -73,17 +84,18 @@
 
 namespace {
 
-// Warp roles.  The warps on a tile's critical chains (issuers, producers)
-// take the lowest warp ids: among ready warps the schedulers favour the
-// oldest, so the epilogue's bulk work does not delay them.
-constexpr int kIssuers = 2;
-constexpr int kIssuerWarp = 0;                            // warps 0-1
-constexpr int kProducers = 2;
-constexpr int kProducerWarp = kIssuerWarp + kIssuers;     // warps 2-3
-constexpr int kEpiWarp = kProducerWarp + kProducers;      // warps 4-19
-constexpr int kEpiWarps = 16;
-constexpr int kWarps = kEpiWarp + kEpiWarps;              // 20: five per SM sub-partition
-constexpr int kThreads = kWarps * 32;                    // 640
+// Warp roles.  The warps on a tile's critical chains (issuer, stager,
+// producers) take the lowest warp ids: among ready warps the schedulers
+// favour the oldest, so the epilogue's bulk work does not delay them.
+constexpr int kIssuers = 3;                               // one per accumulator
+constexpr int kIssuerWarp = 0;                            // warps 0-2
+constexpr int kProducers = 1;
+constexpr int kProducerWarp = kIssuerWarp + kIssuers;     // warp 3
+constexpr int kEpiWarp = kProducerWarp + kProducers;      // warps 4-15
+constexpr int kEpiGroups = kIssuers;                      // one per accumulator
+constexpr int kEpiWarps = 4 * kEpiGroups;
+constexpr int kWarps = kEpiWarp + kEpiWarps;              // 16: four per SM sub-partition
+constexpr int kThreads = kWarps * 32;                    // 512
 constexpr int kTile = 128;                               // keys per tile (MMA M)
 constexpr int kKvBlock = FP4IDX_KV_BLOCK;
 constexpr int kPageBytes = FP4IDX_PAGE_BYTES;
@@ -91,20 +103,29 @@ constexpr int kPayloadBytes = kKvBlock * FP4IDX_SLOT_PAYLOAD_BYTES;  // 4096
 constexpr int kExpBytes = kKvBlock * FP4IDX_SLOT_EXP_BYTES;          // 256
 constexpr int kMaxRows = 128;                  // query rows per segment (MMA N)
 constexpr int kMaxChunks = kMaxRows / 32;
-constexpr int kMaxAccs = 3;                    // TMEM accumulators
+constexpr int kMaxTps = kMaxRows / 32;         // query tokens per segment (H >= 32)
+constexpr int kMaxAccs = kEpiGroups;           // TMEM accumulators
 constexpr int kQBufs = 4;                      // query operand buffers
-constexpr int kMaxStages = 16;
+constexpr int kMaxPairs = 8;                   // pair stages (two tiles each)
 constexpr int kSegTab = 512;                   // segment ranges kept in shared memory
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCols = 8;                // TMEM columns per scale-word slot
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
-// Offsets inside a stage.
-constexpr uint32_t kStPayload = 0;             // 2 x 4096, swizzled payloads
-constexpr uint32_t kStExp = 2 * kPayloadBytes; // 2 x 256 exponent words
-constexpr uint32_t kStSfa = kStExp + 2 * kExpBytes;  // 512: keys' words, transposed
-constexpr uint32_t kStSfb = kStSfa + 512;      // 512: queries' words
-constexpr uint32_t kStageBytes = kStSfb + 512; // 9728, a multiple of the 512-byte swizzle span
+// Offsets inside a pair stage: tiles h = 0, 1 of a pair share one stage,
+// one full and one empty barrier.
+constexpr uint32_t kTilePayload = 2 * kPayloadBytes;  // 8192: tile h's two swizzled payloads at +8192h
+constexpr uint32_t kPsExp = 2 * kTilePayload;         // tile h's 2 x 256 exponent words at +512h
+constexpr uint32_t kPsSfa = kPsExp + 1024;            // tile h's keys' words, transposed, at +512h
+constexpr uint32_t kPsSfb = kPsSfa + 1024;            // tile h's queries' words, transposed, at +512h
+constexpr uint32_t kPsHdr = kPsSfb + 1024;            // one header word per tile
+constexpr uint32_t kPairBytes = 20480;                // a multiple of 1024
+// A tile's header word (written by the producer, read by the tile's issuer):
+// query buffer (bits 0-1), its fill parity (bit 2), the issuer's first
+// (bit 3) and last (bit 4) tile of the segment here, the segment's first
+// tile here (bit 5), the number of issuers with tiles in the segment here
+// (bits 6-7), the segment's query rows (bits 8-15).
+constexpr uint32_t kHdrFirst = 1u << 3, kHdrLast = 1u << 4, kHdrSegFirst = 1u << 5;
 
 enum { kModeDecode = 0, kModePrefill = 1 };
 
@@ -131,22 +152,26 @@ struct ScorerParams {
   int32_t R;            // tps * H
   int32_t ncols;        // logits columns (decode max_context, prefill key count)
   int32_t tiles_total;  // ceil(ncols / 128)
-  int32_t stages;
-  int32_t cpw;          // accumulator chunks per epilogue warp
+  int32_t stages;       // pair stages
 };
 
 struct Layout {
-  uint32_t q, w, tab, bars, misc, total;
+  uint32_t q, qs, w, tab, bars, misc, total;
 };
 
-__host__ __device__ inline Layout make_layout(int S, int R) {
+// mbarriers: full and empty per pair stage; full and empty per accumulator;
+// empty and full per query buffer.
+__host__ __device__ constexpr int kBarriers(int P) { return 2 * P + 2 * kMaxAccs + 2 * kQBufs; }
+
+__host__ __device__ inline Layout make_layout(int P, int R) {
   Layout L;
-  L.q = (uint32_t)S * kStageBytes;                  // kQBufs x R x 64 swizzled queries
-  L.w = L.q + (uint32_t)kQBufs * R * 64;            // 4 quads x 4 chunks x 32 weights
-  L.tab = L.w + 4u * kMaxChunks * 32u * 4u;         // kSegTab x (lo, hi, lim)
-  L.bars = L.tab + (uint32_t)kSegTab * 12u;         // 2S + 2 x 3 + 2 x 4 mbarriers
-  L.misc = L.bars + 8u * (uint32_t)(2 * S + 2 * kMaxAccs + 8);
-  L.total = L.misc + 64u;
+  L.q = (uint32_t)P * kPairBytes;                   // kQBufs x R x 64 swizzled queries
+  L.qs = L.q + (uint32_t)kQBufs * R * 64;           // kQBufs x 128 query scale words
+  L.w = L.qs + (uint32_t)kQBufs * 512u;             // per epilogue warp: kMaxRows weights
+  L.tab = L.w + (uint32_t)kEpiWarps * kMaxRows * 4u;  // kSegTab x (lo, hi, lim)
+  L.bars = L.tab + (uint32_t)kSegTab * 12u;
+  L.misc = L.bars + 8u * (uint32_t)kBarriers(P);
+  L.total = L.misc + 128u;
   return L;
 }
 
@@ -463,7 +488,6 @@ struct Walk {
     q = seg_q(p, g);
     first = true;
   }
-  __device__ __forceinline__ bool last_of_segment() const { return t + 1 >= hi; }
 };
 
 // Writes -inf over a CTA's share of the tiles outside every segment's range
@@ -522,9 +546,8 @@ __device__ __forceinline__ void warp_scan2(long long& a, long long& b, int lane)
 }
 
 // ---------------------------------------------------------------- the kernel
-// CPW: the largest number of accumulator chunks an epilogue warp reads
-// (1, 2 or 4; p.cpw <= CPW): one query token's heads, H / 32 chunks.
-template <int CPW>
+// CPJ: accumulator chunks of 32 columns per query token, H / 32.
+template <int CPJ>
 __global__ void __launch_bounds__(kThreads, 1)
     scorer_kernel(const __grid_constant__ ScorerParams p, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap qmap) {
@@ -536,19 +559,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const Layout L = make_layout(S, R);
   uint8_t* const sQ = smem + L.q;
+  const uint32_t* const sQs = reinterpret_cast<const uint32_t*>(smem + L.qs);
   float* const sW = reinterpret_cast<float*>(smem + L.w);
   int* const tab = reinterpret_cast<int*>(smem + L.tab);
   const uint32_t bars = smem_addr(smem + L.bars);
   uint32_t* const misc = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile uint32_t* const abort = misc + 1;
   int32_t* const start = reinterpret_cast<int32_t*>(misc + 2);  // g0, toff, n, pg0, poff, pn
-  auto stage = [&](int s) { return smem + (uint32_t)s * kStageBytes; };
+  auto stage = [&](int s) { return smem + (uint32_t)s * kPairBytes; };
   auto bar_full = [&](int s) { return bars + 8u * (uint32_t)s; };
   auto bar_empty = [&](int s) { return bars + 8u * (uint32_t)(S + s); };
   auto bar_accf = [&](int a) { return bars + 8u * (uint32_t)(2 * S + a); };
   auto bar_acce = [&](int a) { return bars + 8u * (uint32_t)(2 * S + kMaxAccs + a); };
   auto bar_qempty = [&](int b) { return bars + 8u * (uint32_t)(2 * S + 2 * kMaxAccs + b); };
-  auto bar_qfull = [&](int b) { return bars + 8u * (uint32_t)(2 * S + 2 * kMaxAccs + 4 + b); };
+  auto bar_qfull = [&](int b) {
+    return bars + 8u * (uint32_t)(2 * S + 2 * kMaxAccs + kQBufs + b);
+  };
 
   // ---- this CTA's shares of the work tiles and of the -inf tiles ----------
   // (the scan scratch lives in the stage area, unused until the copies start)
@@ -569,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       *abort = 0u;
       start[2] = 0;
       start[5] = 0;
-      misc[8] = misc[9] = 0u;
+      misc[8] = misc[9] = misc[10] = 0u;
     }
     if (lane == 31) {
       scanw[warp] = wi;
@@ -640,16 +666,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t tmem = 0;
   if (n > 0) {
     if (tid == 0) {
-      for (int i = 0; i < 2 * S + 2 * kMaxAccs + 8; ++i) {
-        // acc_empty takes one arrival per active epilogue warp
-        const bool acce = i >= 2 * S + kMaxAccs && i < 2 * S + 2 * kMaxAccs;
-        const int cnt = acce ? 4 * ((R / 32 + p.cpw - 1) / p.cpw) : 1;
+      for (int i = 0; i < kBarriers(S); ++i) {
+        // a pair stage's empty takes one arrival per tile, acc_empty one per
+        // warp of its epilogue group, a query buffer's empty one per issuer
+        const int j = i - 2 * S;
+        const int cnt = i >= S && i < 2 * S                             ? 2
+                        : j >= kMaxAccs && j < 2 * kMaxAccs                ? 4
+                        : j >= 2 * kMaxAccs && j < 2 * kMaxAccs + kQBufs ? kIssuers
+                                                                         : 1;
         asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bars + 8u * i), "r"(cnt)
                      : "memory");
       }
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 0) {
+    if (warp == kIssuerWarp) {
       asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                        smem_addr(misc)),
                    "r"(kTmemCols)
@@ -663,341 +693,309 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (n > 0) tmem = misc[0];
   // TMEM columns: accumulator a at a*R; the keys' scale words of
   // accumulator a at A*R + 8a; the queries' words of buffer b for issuer m
-  // at A*R + 24 + 8(m*QB + b) (each issuer copies its own).
+  // at A*R + 8A + 8(m*QB + b) (each issuer copies its own).
   const uint32_t sfa_col0 = (uint32_t)A * R, sfb_col0 = sfa_col0 + kMaxAccs * kSfCols;
-  int last_issued = -1;  // producers: the last tile whose copies were issued
+  int last_issued = -1;  // producer: the last pair whose copies were issued
   int q_issued[4] = {-1, -1, -1, -1};  // producers: parity of the last query copy per buffer
 
-  if (n > 0 && warp >= kProducerWarp && warp < kProducerWarp + kProducers) {
-    // ---- producers: tile k belongs to producer k % 2 ------------------------
-    const int pi = warp - kProducerWarp;
-    if (pi < n) {
-      // Lane L fetches the page id of half L % 2 of the producer's own tile
-      // m0 + L / 2 (m0: the first own tile of the batch), a batch ahead.
-      Walk lw;  // this lane's walker, at its tile of the batch being fetched
-      lw.init(p, st, start[0], start[1]);
-      int lk = 0;  // lw's tile index
-      const int n_own = (n - pi + kProducers - 1) / kProducers;
-      auto walk_to = [&](int k) {
-        while (lk < k && lk < n - 1) {
-          lw.advance(p, st);
-          ++lk;
+  if (n > 0 && warp == kProducerWarp) {
+    // ---- producer: a pair of tiles per step -----------------------------------
+    // Per batch of 16 tiles, a batch ahead, lane L describes half L % 2 of
+    // tile m0 + L / 2: the page id (and whether the page is read), the tile's
+    // header word and the first query row of its segment.
+    Walk lw;  // this lane's walker, at its tile of the batch being described
+    lw.init(p, st, start[0], start[1]);
+    int lk = 0;  // lw's tile index
+    struct Desc {
+      int32_t id, in;
+      uint32_t hdr;
+      int32_t qrow;
+    };
+    auto describe = [&](int m0) -> Desc {
+      const int m = m0 + (lane >> 1);
+      Desc dsc = {-1, 0, 0u, 0};
+      if (m < n) {
+        for (; lk < m; ++lk) lw.advance(p, st);
+        const int pidx = lw.t * 2 + (lane & 1);
+        if (pidx * kKvBlock < lw.lim) {
+          dsc.in = 1;
+          dsc.id = p.mode == kModeDecode
+                       ? __ldg(p.block_table + (int64_t)lw.q.b * p.bt_stride + pidx)
+                       : pidx;
         }
-      };
-      auto fetch = [&](int m0, int32_t& id, int& inrange) {
-        const int m = m0 + (lane >> 1);
-        id = -1;
-        inrange = 0;
-        if (m < n_own) {
-          walk_to(pi + kProducers * m);
-          const int pidx = lw.t * 2 + (lane & 1);
-          if (pidx * kKvBlock < lw.lim) {
-            inrange = 1;
-            id = p.mode == kModeDecode
-                     ? __ldg(p.block_table + (int64_t)lw.q.b * p.bt_stride + pidx)
-                     : pidx;
-          }
-        }
-      };
-      // this producer's half of the -inf tiles (the first half for producer
-      // 0, the second for producer 1), spread over its tiles: a producer
-      // mostly waits for a free stage, so the stores cost the pipeline nothing
-      const int pn_all = start[5], pn = pi == 0 ? pn_all / 2 : pn_all - pn_all / 2;
-      Filler fill;
-      fill.init(p, st, start[3], start[4], pi == 0 ? pn : pn_all);
-      if (pi == 1) fill.run(p, st, pn_all / 2, lane, false);  // step over producer 0's half
-      Walk w;  // lane 0's walker at the tile being issued
-      w.init(p, st, start[0], start[1]);
-      int wk = 0;
-      int32_t cur_id, nxt_id = -1;
-      int cur_in, nxt_in = 0;
-      fetch(0, cur_id, cur_in);
-      int s = pi;
-      uint32_t ph = 0;
-      const uint32_t q_bytes = (uint32_t)R * 64u;
-      bool stop = false;
-      for (int m0 = 0; m0 < n_own && !stop; m0 += 16) {
-        if (m0 + 16 < n_own) fetch(m0 + 16, nxt_id, nxt_in);
-        for (int i = 0; i < 16 && m0 + i < n_own; ++i) {
-          const int k = pi + kProducers * (m0 + i);
-          {
-            const long long f0 = (long long)pn * (m0 + i) / n_own;
-            const long long f1 = (long long)pn * (m0 + i + 1) / n_own;
-            fill.run(p, st, (int)(f1 - f0), lane);
-          }
-          int32_t page[2];
-          int in[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            page[h] = __shfl_sync(0xffffffffu, cur_id, 2 * i + h);
-            in[h] = __shfl_sync(0xffffffffu, cur_in, 2 * i + h);
-          }
-          while (wk < k) {
-            w.advance(p, st);
-            ++wk;
-          }
-#pragma unroll
-          for (int h = 0; h < 2; ++h)  // a page outside the cache is not read
-            if (in[h] && (page[h] < 0 || page[h] >= p.num_blocks)) {
-              if (lane == 0) flag_error(p.err, FP4IDX_ERRFLAG_PAGE);
-              in[h] = 0;
-            }
-          const uint32_t fb = bar_full(s);
-          // lanes 0 and 1 both write the stage, so both observe its release
-          int ok = __all_sync(0xffffffffu, lane >= 2 || wait_phase(bar_empty(s), ph ^ 1u, abort));
-          if (lane == 0 && ok) {
-            const int qb = w.qi % QB;
-            if (w.first)
-              ok = wait_phase(bar_qempty(qb), (((uint32_t)(w.qi / QB)) & 1u) ^ 1u, abort);
-            if (ok) {
-              if (w.first) {  // the segment's query operand, on its own barrier
-                const uint32_t qf = bar_qfull(qb);
-                mbar_expect_tx(qf, q_bytes);
-                tma_2d(smem_addr(sQ + (uint32_t)qb * q_bytes), &qmap, 0, w.q.qt0 * p.H, qf);
-                q_issued[qb & 3] = (w.qi / QB) & 1;
-              }
-              mbar_expect_tx(fb, (uint32_t)(in[0] + in[1]) * (kPayloadBytes + kExpBytes));
-              last_issued = k;
-            }
-          }
-          if (!__shfl_sync(0xffffffffu, ok, 0)) {
-            stop = true;
-            break;
-          }
-          // lanes 0 and 1 issue one page each
-          const int32_t my_page = lane == 0 ? page[0] : page[1];
-          const int my_in = lane == 0 ? in[0] : in[1];
-          if (lane < 2 && my_in) {
-            uint8_t* const sp = stage(s);
-            tma_3d(smem_addr(sp + kStPayload + lane * kPayloadBytes), &kmap, 0, 0, my_page, fb);
-            bulk_copy(smem_addr(sp + kStExp + lane * kExpBytes),
-                      p.cache + (int64_t)my_page * kPageBytes + kPayloadBytes, kExpBytes, fb);
-          }
-          s += kProducers;
-          if (s >= S) {
-            s -= S;
-            ph ^= 1u;
-          }
-        }
-        cur_id = nxt_id;
-        cur_in = nxt_in;
+        const int left = min(lw.hi - 1 - lw.t, n - 1 - m);  // the segment's tiles here after m
+        const int owners = min(kIssuers, left + 1);           // at its first tile here
+        dsc.hdr = (uint32_t)(lw.qi % QB) | ((((uint32_t)(lw.qi / QB)) & 1u) << 2) |
+                  (lw.pos < kIssuers ? kHdrFirst : 0u) | (left < kIssuers ? kHdrLast : 0u) |
+                  (lw.first ? kHdrSegFirst : 0u) | ((uint32_t)owners << 6) |
+                  ((uint32_t)(lw.q.ntok * p.H) << 8);
+        dsc.qrow = lw.q.qt0 * p.H;
       }
-      fill.run(p, st, pn, lane);  // any left (an aborted loop)
-    } else if (pi == 1) {  // no work tiles for this producer: its -inf half only
-      const int pn_all = start[5];
-      Filler fill;
-      fill.init(p, st, start[3], start[4], pn_all);
-      fill.run(p, st, pn_all / 2, lane, false);
-      fill.run(p, st, pn_all, lane);
+      return dsc;
+    };
+    const uint32_t q_bytes = (uint32_t)R * 64u;
+    // A segment's first tile here: its query operand and scale words, on the
+    // query buffer's own barrier, in segment order; then the releases of the
+    // buffer that issuers without a tile in the segment will not make.
+    auto load_q = [&](uint32_t hdr, int32_t qrow) -> bool {
+      const int qb = (int)(hdr & 3u);
+      const uint32_t qpar = (hdr >> 2) & 1u;
+      if (!wait_phase(bar_qempty(qb), qpar ^ 1u, abort)) return false;
+      const uint32_t qf = bar_qfull(qb);
+      const uint32_t sw_bytes = ((hdr >> 8) & 0xFFu) * 4u;
+      mbar_expect_tx(qf, q_bytes + sw_bytes);
+      tma_2d(smem_addr(sQ + (uint32_t)qb * q_bytes), &qmap, 0, qrow, qf);
+      bulk_copy(smem_addr(sQs + qb * 128), p.q_scale + (int64_t)qrow * 4, sw_bytes, qf);
+      q_issued[qb] = (int)qpar;
+      for (int o = (int)((hdr >> 6) & 3u); o < kIssuers; ++o) mbar_arrive(bar_qempty(qb));
+      return true;
+    };
+    // Lanes 4h .. 4h + 3 copy tile h of the pair: lanes 4h and 4h + 1 the
+    // two page payloads (TMA, 64-byte swizzled, the layout the MMA reads),
+    // lanes 4h + 2 and 4h + 3 the pages' exponent words (bulk copies).
+    const int th = (lane >> 2) & 1, pg = lane & 1;
+    const bool exps = (lane & 2) != 0;
+    Desc cur = describe(0), nxt = {-1, 0, 0u, 0};
+    int ps = 0;
+    uint32_t ph = 0;
+    bool stop = false;
+    for (int m0 = 0; m0 < n && !stop; m0 += 16) {
+      if (m0 + 16 < n) nxt = describe(m0 + 16);
+      for (int i = 0; i < 16 && m0 + i < n; i += 2) {
+        const int k = m0 + i;
+        const bool two = k + 1 < n;
+        const bool active = lane < 4 || (lane < 8 && two);
+        const int src = 2 * (i + th) + pg;
+        const int32_t my_page = __shfl_sync(0xffffffffu, cur.id, src);
+        int my_in = __shfl_sync(0xffffffffu, cur.in, src);
+        const uint32_t hdr0 = __shfl_sync(0xffffffffu, cur.hdr, 2 * i);
+        const uint32_t hdr1 = __shfl_sync(0xffffffffu, cur.hdr, 2 * i + 2);
+        const int32_t qrow0 = __shfl_sync(0xffffffffu, cur.qrow, 2 * i);
+        const int32_t qrow1 = __shfl_sync(0xffffffffu, cur.qrow, 2 * i + 2);
+        if (my_in && (my_page < 0 || my_page >= p.num_blocks)) {  // not read
+          if (active && !exps) flag_error(p.err, FP4IDX_ERRFLAG_PAGE);
+          my_in = 0;
+        }
+        // pages read, lanes 0, 1 (tile 0) and 4, 5 (tile 1)
+        const uint32_t rd = __ballot_sync(0xffffffffu, active && !exps && my_in);
+        // every lane that writes the stage observes its release itself
+        int ok = __all_sync(0xffffffffu, !active || wait_phase(bar_empty(ps), ph ^ 1u, abort));
+        uint8_t* const sp = stage(ps);
+        if (ok && lane == 0) {
+          ok = (!(hdr0 & kHdrSegFirst) || load_q(hdr0, qrow0)) &&
+               (!two || !(hdr1 & kHdrSegFirst) || load_q(hdr1, qrow1));
+          if (ok) {
+            *reinterpret_cast<uint2*>(sp + kPsHdr) = make_uint2(hdr0, hdr1);
+            mbar_expect_tx(bar_full(ps), (uint32_t)__popc(rd & 0x33u) * (kPayloadBytes + kExpBytes));
+            last_issued = k >> 1;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          stop = true;
+          break;
+        }
+        if (active && my_in) {
+          const uint32_t fb = bar_full(ps);
+          if (!exps)
+            tma_3d(smem_addr(sp + th * kTilePayload + pg * kPayloadBytes), &kmap, 0, 0, my_page, fb);
+          else
+            bulk_copy(smem_addr(sp + kPsExp + th * 512 + pg * kExpBytes),
+                      p.cache + (int64_t)my_page * kPageBytes + kPayloadBytes, kExpBytes, fb);
+        }
+        if (++ps == S) {
+          ps = 0;
+          ph ^= 1u;
+        }
+      }
+      cur = nxt;
     }
   } else if (n > 0 && warp >= kIssuerWarp && warp < kIssuerWarp + kIssuers) {
-    // ---- issuers: tile k belongs to issuer k % 2 ----------------------------
+    // ---- issuers: tile k belongs to issuer k % 3, which owns accumulator k % 3 --
     const int m = warp - kIssuerWarp;
-    Walk w;
-    w.init(p, st, start[0], start[1]);
-    int wk = 0;
-    uint32_t qv[4];  // this lane's query words of segment qv_g
-    int qv_g = -1;
-    auto load_qwords = [&](int g) {
-      const SegQ q = seg_q(p, g);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int r = 32 * j + lane;
-        qv[j] = (g < p.nseg && r < q.ntok * p.H)
-                    ? __ldg(reinterpret_cast<const uint32_t*>(p.q_scale) + (int64_t)q.qt0 * p.H + r)
-                    : 0x7F7F7F7Fu;
-      }
-      qv_g = g;
-    };
-    const int n_own = n > m ? (n - m + 1) / 2 : 0;
     const uint32_t id0 = mxf4_idesc(R, 0), id1 = mxf4_idesc(R, 2);
     const uint32_t q_bytes = (uint32_t)R * 64u;
-    int s = m, a = m % A, last = -1;
-    uint32_t ph = 0, pa = (uint32_t)(m / A) & 1u;
-    for (int i = 0; i < n_own; ++i) {
-      const int k = m + 2 * i;
-      while (wk < k) {
-        w.advance(p, st);
-        ++wk;
-      }
-      // Every lane reads the landed exponent words, so every lane observes
-      // the barrier's completion itself (acquire); a wait by one lane alone
-      // does not order the other lanes' reads after the copy.
-      int ok = __all_sync(0xffffffffu, wait_phase(bar_full(s), ph, abort));
+    const uint32_t d = tmem + (uint32_t)m * (uint32_t)R;
+    const uint32_t sfa = tmem + sfa_col0 + kSfCols * (uint32_t)m;
+    int issued = 0;
+    for (int k = m; k < n; k += kIssuers) {
+      const int j = k >> 1, h = k & 1, ps = j % S;
+      const uint32_t ph = (uint32_t)(j / S) & 1u;
+      // Lane 0 waits; then every lane, which reads the landed words, observes
+      // the completed phase itself (acquire): a wait by one lane alone does
+      // not order the other lanes' reads after the copy.
+      int ok = __shfl_sync(0xffffffffu, lane == 0 ? (int)wait_phase(bar_full(ps), ph, abort) : 0, 0);
       if (!ok) break;
-      uint8_t* const sp = stage(s);
+      (void)wait_phase(bar_full(ps), ph, abort);  // complete: returns at once
+      uint8_t* const sp = stage(ps);
+      const uint32_t hdr = *reinterpret_cast<const uint32_t*>(sp + kPsHdr + 4 * h);
+      const int qb = (int)(hdr & 3u);
+      const bool first = (hdr & kHdrFirst) != 0;
       {  // the keys' words: row l holds tokens l, l+32, l+64, l+96
-        const uint32_t* ew = reinterpret_cast<const uint32_t*>(sp + kStExp);
-        *reinterpret_cast<uint4*>(sp + kStSfa + 16 * lane) =
+        const uint32_t* ew = reinterpret_cast<const uint32_t*>(sp + kPsExp + 512 * h);
+        *reinterpret_cast<uint4*>(sp + kPsSfa + 512 * h + 16 * lane) =
             make_uint4(ew[lane], ew[lane + 32], ew[lane + 64], ew[lane + 96]);
       }
-      const bool seg_first = w.pos < 2;  // this issuer's first tile of the segment
-      if (seg_first) {  // the queries' words, rows 0-127 then 128-255
-        if (qv_g != w.g) load_qwords(w.g);
-        *reinterpret_cast<uint4*>(sp + kStSfb + 16 * lane) = make_uint4(qv[0], qv[1], qv[2], qv[3]);
-        SegRange r;
-        load_qwords(st.next(p, w.g, r));  // the next segment's, ahead of time
+      if (first) {  // this issuer's first tile of the segment: the queries' words
+        const uint32_t qpar = (hdr >> 2) & 1u;
+        ok = __shfl_sync(0xffffffffu, lane == 0 ? (int)wait_phase(bar_qfull(qb), qpar, abort) : 0, 0);
+        if (!ok) break;
+        (void)wait_phase(bar_qfull(qb), qpar, abort);  // complete: returns at once
+        const int rows = (int)(hdr >> 8) & 0xFF;
+        const uint32_t* qw = sQs + qb * 128;
+        uint32_t v[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) v[c] = 32 * c + lane < rows ? qw[32 * c + lane] : 0x7F7F7F7Fu;
+        *reinterpret_cast<uint4*>(sp + kPsSfb + 512 * h + 16 * lane) = make_uint4(v[0], v[1], v[2], v[3]);
       }
+      // generic-proxy writes, read next by tcgen05.cp (async proxy)
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) {
-        const int qb = w.qi % QB;
-        ok = (k < A || wait_phase(bar_acce(a), pa ^ 1u, abort)) &&
-             (!seg_first || wait_phase(bar_qfull(qb), (uint32_t)(w.qi / QB) & 1u, abort));
+        // accumulator m has been read out (this issuer's previous tile)
+        ok = issued == 0 || wait_phase(bar_acce(m), ((uint32_t)issued & 1u) ^ 1u, abort);
         if (ok) {
           asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-          const uint32_t sfa = tmem + sfa_col0 + kSfCols * (uint32_t)a;
           const uint32_t sfb = tmem + sfb_col0 + kSfCols * (uint32_t)(m * QB + qb);
-          cp_32x128b_x4(sfa, cp_desc(smem_addr(sp + kStSfa)));
-          if (seg_first) {
-            cp_32x128b_x4(sfb, cp_desc(smem_addr(sp + kStSfb)));
-          }
+          cp_32x128b_x4(sfa, cp_desc(smem_addr(sp + kPsSfa + 512 * h)));
+          if (first) cp_32x128b_x4(sfb, cp_desc(smem_addr(sp + kPsSfb + 512 * h)));
           // operand descriptors built from the buffers' own addresses
-          const uint64_t adesc = sw64_desc(smem_addr(sp + kStPayload));
+          const uint64_t adesc = sw64_desc(smem_addr(sp + h * kTilePayload));
           const uint64_t qdesc = sw64_desc(smem_addr(sQ + (uint32_t)qb * q_bytes));
-          const uint32_t d = tmem + (uint32_t)a * (uint32_t)R;
           mma_mxf4(d, adesc, qdesc, id0, sfa, sfb, 0u);
           mma_mxf4(d, adesc + 2, qdesc + 2, id1, sfa, sfb, 1u);
-          mma_commit(bar_accf(a));
-          last = k;
+          // Each commit tracks every earlier MMA of this thread: the
+          // accumulator is full, this tile's half of the pair stage can be
+          // refilled, and after this issuer's last tile of the segment, its
+          // share of the query buffer is released.
+          mma_commit(bar_accf(m));
+          mma_commit(bar_empty(ps));
+          if (hdr & kHdrLast) mma_commit(bar_qempty(qb));
         }
       }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      s += 2;
-      if (s >= S) {
-        s -= S;
-        ph ^= 1u;
-      }
-      a += 2;
-      while (a >= A) {
-        a -= A;
-        pa ^= 1u;
-      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      ++issued;
     }
-    if (lane == 0) misc[8 + m] = (uint32_t)(last + 1);  // for the drain after an abort
+    if (lane == 0) misc[8 + m] = (uint32_t)issued;  // for the drain after an abort
   } else if (n > 0 && warp >= kEpiWarp) {
-    // ---- epilogue -------------------------------------------------------------
-    // Warp (quad, wq) reads chunks [c0, c1) of every accumulator for the 32
-    // tokens of its lane quadrant.  Its chunks hold whole query tokens: one
-    // token, or two single-chunk tokens when H = 32 (cpj == 1, CPW <= 2).
-    const int quad = warp & 3, wq = (warp - kEpiWarp) >> 2;  // TMEM lanes: warp id % 4
-    const int nch = R / 32, cpj = p.H / 32;
-    const int c0 = wq * p.cpw, cw = min(p.cpw, nch - c0);
-    if (cw > 0) {
-      const int row = quad * 32 + lane;  // the tile's token = TMEM lane
-      const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-      float* const wts = sW + (quad * kMaxChunks + c0) * 32;  // this warp's chunk weights
-      const int tok0 = c0 / cpj;                               // first query token
-      const bool two = cpj == 1 && cw == 2;
-      Walk w;
-      w.init(p, st, start[0], start[1]);
-      // per segment: this warp's weights (and in prefill its tokens' key
-      // ranges), the next segment's loaded one segment ahead
-      float wn[CPW];
-      int an[2], bn[2], ac[2] = {0, 0}, bc[2] = {0, 0};
-      auto load_seg = [&](int g) {
-        const SegQ q = seg_q(p, g);
-        const bool live = g < p.nseg;
+    // ---- epilogue ---------------------------------------------------------------
+    // Group j (warps 4+4j .. 7+4j) reads accumulator j, i.e. tiles k = j
+    // (mod 3); its warp w reads TMEM lane quadrant w % 4 (tile keys
+    // 32(w%4) .. +31, one per thread) across every query row of the segment.
+    const int grp = (warp - kEpiWarp) >> 2, quad = warp & 3;
+    const int row = quad * 32 + lane;  // the tile's key = TMEM lane
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    float* const wts = sW + (warp - kEpiWarp) * kMaxRows;  // this warp's copy of the weights
+    Walk w;
+    w.init(p, st, start[0], start[1]);
+    int wk = 0;                        // w's tile
+    int cur_g = -1;                    // segment whose weights are in wts
+    int ac[kMaxTps] = {0, 0, 0, 0}, bc[kMaxTps] = {0, 0, 0, 0};  // prefill key ranges
+    uint32_t pu = 0;                   // parity of this group's next use of accumulator grp
+    // This warp's share of the -inf tiles, spread over its group's tiles: a
+    // group mostly waits for its accumulator, so the stores cost little.
+    const int e = warp - kEpiWarp, pn_all = start[5];
+    const bool leader = (e & 3) == 0;
+    volatile uint32_t* const gflag = misc + 16;  // [group][parity]: the leader's verdict
+    const int f_lo = (int)((long long)pn_all * e / kEpiWarps);
+    const int f_hi = (int)((long long)pn_all * (e + 1) / kEpiWarps), pn = f_hi - f_lo;
+    const int n_grp = (n - grp + kEpiGroups - 1) / kEpiGroups;  // this group's tiles
+    Filler fill;
+    fill.init(p, st, start[3], start[4], f_hi);
+    fill.run(p, st, f_lo, lane, false);  // step over the earlier warps' shares
+    int j_own = 0;
+    for (int k = grp; k < n; k += kEpiGroups) {
+      for (; wk < k; ++wk) w.advance(p, st);
+      const int ntok = w.q.ntok;
+      if (w.g != cur_g) {  // a new segment: its weights (and key ranges)
+        float wr[kMaxChunks];
 #pragma unroll
-        for (int i = 0; i < CPW; ++i) {
-          const int r = 32 * (c0 + i) + lane;  // the segment's query row
-          wn[i] = (i < cw && live && r < q.ntok * p.H)
-                      ? __ldg(p.weights + (int64_t)q.qt0 * p.H + r)
-                      : 0.0f;
+        for (int c = 0; c < kMaxChunks; ++c) {
+          const int r = 32 * c + lane;
+          wr[c] = r < ntok * p.H ? __ldg(p.weights + (int64_t)w.q.qt0 * p.H + r) : 0.0f;
         }
         if (p.mode == kModePrefill) {
 #pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            const int t = q.qt0 + tok0 + i;
-            const bool in = live && tok0 + i < q.ntok;
-            an[i] = in ? min(max(__ldg(p.ks + t), 0), p.ncols) : 0;
-            bn[i] = in ? min(max(__ldg(p.ke + t), 0), p.ncols) : 0;
+          for (int t = 0; t < kMaxTps; ++t) {
+            const bool in = t < ntok;
+            ac[t] = in ? min(max(__ldg(p.ks + w.q.qt0 + t), 0), p.ncols) : 0;
+            bc[t] = in ? min(max(__ldg(p.ke + w.q.qt0 + t), 0), p.ncols) : 0;
           }
         }
-      };
-      auto enter_seg = [&](int g) {
+        __syncwarp();  // the previous segment's reads of wts are done
 #pragma unroll
-        for (int i = 0; i < CPW; ++i)
-          if (i < cw) wts[i * 32 + lane] = wn[i];
-        ac[0] = an[0];
-        ac[1] = an[1];
-        bc[0] = bn[0];
-        bc[1] = bn[1];
+        for (int c = 0; c < kMaxChunks; ++c) wts[32 * c + lane] = wr[c];
         __syncwarp();
-        SegRange r;
-        load_seg(st.next(p, g, r));
-      };
-      // decode: this warp's page of the tile (-1 past the context), loaded a
-      // tile ahead and only compared when the tile is stored, so the load's
-      // latency stays off the per-tile chain
-      auto page_id = [&](const Walk& x) -> int32_t {
-        if (p.mode != kModeDecode) return 0;
-        const int pidx = x.t * 2 + (quad >> 1);
-        if (pidx * kKvBlock >= x.lim) return -1;
-        return __ldg(p.block_table + (int64_t)x.q.b * p.bt_stride + pidx);
-      };
-      load_seg(w.g);
-      Walk nw = w;
-      int32_t pid = page_id(w), pid_next = -1;
-      int a = 0, se = 0;
-      uint32_t pa = 0;
-      for (int k = 0; k < n; ++k) {
-        if (w.first) enter_seg(w.g);
-        if (k + 1 < n) {
-          nw.advance(p, st);
-          pid_next = page_id(nw);
-        }
-        if (!__all_sync(0xffffffffu, wait_phase(bar_accf(a), pa, abort))) break;
-        // The tile's MMAs have completed, so its stage (and, after a
-        // segment's last tile, the segment's query buffer) can be refilled.
-        if (warp == kEpiWarp && lane == 0) {
-          mbar_arrive(bar_empty(se));
-          if (k + 1 == n || w.last_of_segment()) mbar_arrive(bar_qempty(w.qi % QB));
-        }
-        if (++se == S) se = 0;
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        float v0 = 0.0f, v1 = 0.0f;
-        const uint32_t col = lane_base + (uint32_t)a * (uint32_t)R + 32u * (uint32_t)c0;
+        cur_g = w.g;
+      }
+      // decode: this warp's page of the tile (-1 past the context), loaded
+      // before the wait so that its latency is hidden behind it
+      int32_t pid = 0;
+      if (p.mode == kModeDecode) {
+        const int pidx = w.t * 2 + (quad >> 1);
+        pid = pidx * kKvBlock < w.lim
+                  ? __ldg(p.block_table + (int64_t)w.q.b * p.bt_stride + pidx)
+                  : -1;
+      }
+      // One warp of the group waits for the accumulator; the others wait at
+      // the group's named barrier, which takes no issue slots (spinning warps
+      // would take them from the issuers and the producer).  The leader's
+      // verdict goes through shared memory, one slot per parity, so that all
+      // four warps leave together.
+      if (leader) {
+        const bool ok = __all_sync(0xffffffffu, wait_phase(bar_accf(grp), pu, abort));
+        if (lane == 0) gflag[2 * grp + pu] = ok ? 1u : 0u;
+      }
+      asm volatile("bar.sync %0, 128;" ::"r"(1 + grp) : "memory");
+      if (!gflag[2 * grp + pu]) break;
+      pu ^= 1u;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const int nv = ntok * CPJ;  // accumulator chunks holding this segment's rows
+      const uint32_t col = tmem + lane_base + (uint32_t)grp * (uint32_t)R;
+      float v[kMaxTps];
 #pragma unroll
-        for (int i = 0; i < CPW; ++i) {
-          if (i < cw) {
-            uint32_t x[32];
-            tmem_ld32(tmem + col + 32u * i, x);
-            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-            if (i == cw - 1) {  // every load of the tile done: release the accumulator
-              asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-              __syncwarp();
-              if (lane == 0) mbar_arrive(bar_acce(a));
-            }
-            const float part = weighted_relu_sum(x, wts + i * 32);
-            if (i == 0)
-              v0 = part;
-            else if (two)
-              v1 = part;
+      for (int c = 0; c < kMaxChunks; c += 2) {
+        if (c < nv) {
+          uint32_t xa[32], xb[32];
+          tmem_ld32(col + 32u * c, xa);
+          if (c + 1 < nv) tmem_ld32(col + 32u * (c + 1), xb);
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+          if (c + 2 >= nv) {  // every load of the tile done: release the accumulator
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_acce(grp));
+          }
+          const float pa_ = weighted_relu_sum(xa, wts + 32 * c);
+          if (c % CPJ == 0)
+            v[c / CPJ] = pa_;
+          else
+            v[c / CPJ] = __fadd_rn(v[c / CPJ], pa_);
+          if (c + 1 < nv) {
+            const float pb_ = weighted_relu_sum(xb, wts + 32 * (c + 1));
+            if ((c + 1) % CPJ == 0)
+              v[(c + 1) / CPJ] = pb_;
             else
-              v0 = __fadd_rn(v0, part);
+              v[(c + 1) / CPJ] = __fadd_rn(v[(c + 1) / CPJ], pb_);
           }
         }
-        const int s_tok = w.t * kTile + row;
-        const bool pok = pid >= 0 && pid < p.num_blocks;
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          if (i == 1 && !two) break;
-          const int qt = w.q.qt0 + tok0 + i;  // query token
-          const bool valid = p.mode == kModeDecode ? (s_tok < w.lim && pok)
-                                                   : (s_tok >= ac[i] && s_tok < bc[i]);
-          if (tok0 + i < w.q.ntok && s_tok < p.ncols)
-            __stcs(p.logits + (int64_t)qt * p.logits_stride + s_tok,
-                   valid ? (i == 0 ? v0 : v1) : -INFINITY);
-        }
-        if (++a == A) {
-          a = 0;
-          pa ^= 1u;
-        }
-        w = nw;
-        pid = pid_next;
       }
+      const int s_tok = w.t * kTile + row;
+      const bool pok = pid >= 0 && pid < p.num_blocks;
+#pragma unroll
+      for (int t = 0; t < kMaxTps; ++t) {
+        if (t < ntok && s_tok < p.ncols) {
+          const bool valid = p.mode == kModeDecode ? (s_tok < w.lim && pok)
+                                                   : (s_tok >= ac[t] && s_tok < bc[t]);
+          __stcs(p.logits + (int64_t)(w.q.qt0 + t) * p.logits_stride + s_tok,
+                 valid ? v[t] : -INFINITY);
+        }
+      }
+      const long long f0 = (long long)pn * j_own / n_grp, f1 = (long long)pn * (j_own + 1) / n_grp;
+      fill.run(p, st, (int)(f1 - f0), lane);
+      ++j_own;
     }
+    fill.run(p, st, pn, lane);  // any left (a group without tiles, an aborted loop)
   } else if (n == 0 && warp == kProducerWarp) {
     // ---- no work tiles: only this CTA's share of the -inf tiles -------------
     Filler fill;
@@ -1015,21 +1013,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < QB; ++b)
           if (q_issued[b] >= 0) wait_phase_drain(bar_qfull(b), (uint32_t)q_issued[b]);
       }
-      // MMAs in flight land before TMEM is released.  (Without an abort the
-      // epilogue has waited for every one.)  With one accumulator, tile k's
-      // MMAs start only after tile k-1's completed, so only the later of the
-      // two issuers' last tiles can be in flight: waiting on the other's
-      // phase could match a newer phase of the same parity.
+      // MMAs in flight land before TMEM is released: an issuer's last
+      // commit tracks all its earlier MMAs, and its accumulator cannot be two
+      // phases behind it (its previous tile was read out before it was issued).
       if (warp >= kIssuerWarp && warp < kIssuerWarp + kIssuers && lane == 0) {
-        const int m = warp - kIssuerWarp;
-        const int last = (int)misc[8 + m] - 1, other = (int)misc[9 - m] - 1;
-        if (last >= 0 && (A > 1 || last > other))
-          wait_phase_drain(bar_accf(last % A), (uint32_t)(last / A) & 1u);
+        const int m = warp - kIssuerWarp, cnt = (int)misc[8 + m];
+        if (cnt > 0) wait_phase_drain(bar_accf(m), (uint32_t)(cnt - 1) & 1u);
       }
       if (tid == 0) flag_error(p.err, FP4IDX_ERRFLAG_TIMEOUT);
       __syncthreads();
     }
-    if (warp == 0)
+    __syncwarp();
+    if (warp == kIssuerWarp)
       asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                    "r"(kTmemCols)
                    : "memory");
@@ -1080,6 +1075,8 @@ fp4idx_status device_setup(DeviceInfo& out, EncodeTiledFn& enc) {
                              t.smem_optin) != cudaSuccess ||
         cudaFuncSetAttribute(scorer_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              t.smem_optin) != cudaSuccess ||
+        cudaFuncSetAttribute(scorer_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             t.smem_optin) != cudaSuccess ||
         cudaFuncSetAttribute(scorer_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              t.smem_optin) != cudaSuccess)
       return FP4IDX_ERR_CUDA;
@@ -1095,8 +1092,7 @@ fp4idx_status device_setup(DeviceInfo& out, EncodeTiledFn& enc) {
 // at least one query token's heads).
 bool heads_ok(int64_t H) { return H >= 32 && H % 32 == 0 && H <= kMaxRows; }
 
-// Fills the launch-shape fields of p (accumulators, query buffers, chunks
-// per epilogue warp, stages) and launches.
+// Fills the launch-shape fields of p (stages, tiles) and launches.
 fp4idx_status launch(ScorerParams& p, const uint8_t* q_fp4, const uint8_t* kv_cache,
                      cudaStream_t stream) {
   DeviceInfo di;
@@ -1104,11 +1100,8 @@ fp4idx_status launch(ScorerParams& p, const uint8_t* q_fp4, const uint8_t* kv_ca
   const fp4idx_status ds = device_setup(di, encode);
   if (ds != FP4IDX_OK) return ds;
   const int R = p.R;  // <= 128: 3 accumulators + scale words fit 512 TMEM columns
-  const int nch = R / 32, cpj = p.H / 32;
-  (void)nch;
-  p.cpw = cpj;  // chunks per epilogue warp: one query token's heads
-  int S = kMaxStages;
-  while (S > kProducers && (int)make_layout(S, R).total + 1024 > di.smem_optin) S -= kProducers;
+  int S = kMaxPairs;
+  while (S > 1 && (int)make_layout(S, R).total + 1024 > di.smem_optin) --S;
   if ((int)make_layout(S, R).total + 1024 > di.smem_optin) return FP4IDX_ERR_SHAPE;
   p.stages = S;
   const int smem_bytes = (int)make_layout(S, R).total + 1024;
@@ -1142,7 +1135,11 @@ fp4idx_status launch(ScorerParams& p, const uint8_t* q_fp4, const uint8_t* kv_ca
       return FP4IDX_ERR_CUDA;
   }
   if (cudaPeekAtLastError() != cudaSuccess) return FP4IDX_ERR_CUDA;  // an earlier error
-  auto kern = p.cpw <= 1 ? scorer_kernel<1> : p.cpw <= 2 ? scorer_kernel<2> : scorer_kernel<4>;
+  const int cpj = p.H / 32;
+  auto kern = cpj == 1 ? scorer_kernel<1>
+              : cpj == 2 ? scorer_kernel<2>
+              : cpj == 3 ? scorer_kernel<3>
+                         : scorer_kernel<4>;
   kern<<<(unsigned)di.sms, kThreads, smem_bytes, stream>>>(p, kmap, qmap);
   return cudaPeekAtLastError() == cudaSuccess ? FP4IDX_OK : FP4IDX_ERR_CUDA;
 }
@@ -1164,7 +1161,7 @@ extern "C" fp4idx_status fp4idx_paged_mqa_logits(
       logits_stride < max_context ||
       block_table_stride < (max_context + kKvBlock - 1) / kKvBlock)
     return FP4IDX_ERR_SHAPE;
-  if (!aligned(q_fp4, 16) || !aligned(q_scale, 4) || !aligned(weights, 4) ||
+  if (!aligned(q_fp4, 16) || !aligned(q_scale, 16) || !aligned(weights, 4) ||
       !aligned(kv_cache, 16) || !aligned(block_table, 4) || !aligned(context_lens, 4) ||
       !aligned(logits, 4) || (err_flags && !aligned(err_flags, 4)))
     return FP4IDX_ERR_ALIGN;
@@ -1207,7 +1204,7 @@ extern "C" fp4idx_status fp4idx_mqa_logits_prefill(
       num_keys > num_blocks * (int64_t)kKvBlock || num_tokens >= (1ll << 31) / num_heads ||
       logits_stride < num_keys)
     return FP4IDX_ERR_SHAPE;
-  if (!aligned(q_fp4, 16) || !aligned(q_scale, 4) || !aligned(weights, 4) ||
+  if (!aligned(q_fp4, 16) || !aligned(q_scale, 16) || !aligned(weights, 4) ||
       !aligned(kv_cache, 16) || !aligned(ks, 4) || !aligned(ke, 4) || !aligned(logits, 4) ||
       (err_flags && !aligned(err_flags, 4)))
     return FP4IDX_ERR_ALIGN;

@@ -323,7 +323,7 @@ fp4idx_status fp4idx_rope_fake_quant(
  *
  *   q_fp4        bytes [batch*next_n, num_heads, 64], dense, 16-byte aligned
  *                (the q_fp4 output of the calls above).
- *   q_scale      bytes [batch*next_n, num_heads, 4], dense, 4-byte aligned.
+ *   q_scale      bytes [batch*next_n, num_heads, 4], dense, 16-byte aligned.
  *   weights      fp32 [batch*next_n, num_heads], dense.
  *   kv_cache     bytes [num_blocks, 4352], 16-byte aligned, read only.
  *                Exponent bytes must be <= 254 (255 is NaN on the tensor

@@ -2,7 +2,8 @@
 through the pre-pass (keys into a shuffled paged cache, queries packed with
 their head weights) and then the paged scorer, all through the public API,
 against the same pipeline in the oracle.  The intermediate bytes must match
-exactly, the logits within the scorer's error bound; on the logits the test
+exactly (the fp32 head weights within 1 ulp), the logits within the scorer's
+error bound; on the logits the test
 also asserts cosine >= 0.999999 and a top-64 overlap of 1.0 per row, and
 prints how far the FP4 path is from the unquantised fp64 score (which sets
 what the format itself costs, not a kernel error).  Sources: "[HIP] Add FP4
@@ -14,7 +15,7 @@ import pytest
 import bench
 import oracle
 from fp4_sparse_attention_fp4idx_gb300 import workloads as wl
-from tests.gpu_util import F, SCORER_TOL
+from tests.gpu_util import F, SCORER_TOL, assert_weights
 
 pytestmark = pytest.mark.gpu
 
@@ -49,7 +50,9 @@ def test_indexer_end_to_end(H, next_n):
 
     assert np.array_equal(g_cache, o_cache), "paged cache bytes differ"
     assert np.array_equal(g_qf, o_qf) and np.array_equal(g_qs, o_qs), "query bytes differ"
-    assert np.array_equal(g_wt.view(np.uint32), o_wt.view(np.uint32)), "head weights differ"
+    # fp32(w * H^-1/2 * 128^-1/2): the library rounds the scale to fp32 first,
+    # the oracle forms the product in double (1 ulp apart at most)
+    assert_weights(g_wt, o_wt)
 
     assert np.all(np.isfinite(got)) and np.all(np.isfinite(want))
     err = np.abs(got.astype(np.float64) - want)
