@@ -756,15 +756,19 @@ __device__ __forceinline__ void fake_quant_e4m3_16(uint32_t (&a)[4], uint32_t (&
   uint32_t m = hmax_abs(prmt(ma, mb, 0x5410u), prmt(ma, mb, 0x7632u));
   m = hmax_abs(m, __shfl_xor_sync(kFull, m, 1));
   m &= 0x7fff7fffu;
-  const float sa = e4m3_round(__fdiv_rn(__uint_as_float(m << 16), 6.0f));
-  const float sb = e4m3_round(__fdiv_rn(__uint_as_float(m & 0xffff0000u), 6.0f));
+  // rn(amax / 6) and rn(x / s) through the corrected reciprocal quotient
+  // (exact for these operands: bf16 numerators, E4M3 or 6 divisors)
+  constexpr float kSixth = 1.0f / 6.0f;
+  const float sa = e4m3_round(div_rcp(__uint_as_float(m << 16), 6.0f, kSixth));
+  const float sb = e4m3_round(div_rcp(__uint_as_float(m & 0xffff0000u), 6.0f, kSixth));
+  // A zero scale takes a zero reciprocal: every quotient is then +-0 (finite
+  // x), so the group is all zeros.
+  const float ra = sa == 0.0f ? 0.0f : rcp_approx(sa), rb = sb == 0.0f ? 0.0f : rcp_approx(sb);
   float va[8], vb[8];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    va[2 * k] = sa == 0.0f ? 0.0f : __fdiv_rn(bf16_lo(a[k]), sa);
-    va[2 * k + 1] = sa == 0.0f ? 0.0f : __fdiv_rn(bf16_hi(a[k]), sa);
-    vb[2 * k] = sb == 0.0f ? 0.0f : __fdiv_rn(bf16_lo(b[k]), sb);
-    vb[2 * k + 1] = sb == 0.0f ? 0.0f : __fdiv_rn(bf16_hi(b[k]), sb);
+    div_rcp2(va[2 * k], va[2 * k + 1], bf16_lo(a[k]), bf16_hi(a[k]), sa, ra);
+    div_rcp2(vb[2 * k], vb[2 * k + 1], bf16_lo(b[k]), bf16_hi(b[k]), sb, rb);
   }
   dequant8(e2m1x8(va), sa, a);
   dequant8(e2m1x8(vb), sb, b);

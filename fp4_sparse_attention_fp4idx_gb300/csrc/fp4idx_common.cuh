@@ -118,6 +118,43 @@ __device__ __forceinline__ float4 ld_f4(const float* p) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// x / s rounded to nearest even, given rs = rn(1/s): q = rn(x * rs), the
+// residual x - q*s (exact in one fma), then q + residual * rs rounded once
+// (Markstein's correction of a reciprocal quotient, "IA-64 and Elementary
+// Functions", 2000).  For every bf16 x and every positive E4M3 s (and for
+// s = 6), the result equals the correctly rounded quotient; the GPU tests
+// check all of those pairs against the IEEE division.
+__device__ __forceinline__ float div_rcp(float x, float s, float rs) {
+  const float q = __fmul_rn(x, rs);
+  const float r = __fmaf_rn(-q, s, x);
+  return __fmaf_rn(r, rs, q);
+}
+
+// The hardware's approximate reciprocal (rcp.approx.ftz.f32).  With it as
+// rs, div_rcp still gives the correctly rounded x / s for the quantiser's
+// operands (bf16 x, positive E4M3 s): the GPU tests check every such pair.
+__device__ __forceinline__ float rcp_approx(float s) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
+  return r;
+}
+
+// (x0 / s, x1 / s) by div_rcp's three steps on f32x2 pairs (the residual as
+// rn(q * -s + x), the same exact value).
+__device__ __forceinline__ void div_rcp2(float& r0, float& r1, float x0, float x1, float s,
+                                         float rs) {
+  asm("{\n\t.reg .b64 rx, rr, rm, rq, rd, ro;\n\t"
+      "mov.b64 rx, {%2, %3};\n\t"
+      "mov.b64 rr, {%5, %5};\n\t"
+      "mov.b64 rm, {%4, %4};\n\t"
+      "mul.rn.f32x2 rq, rx, rr;\n\t"
+      "fma.rn.f32x2 rd, rq, rm, rx;\n\t"
+      "fma.rn.f32x2 ro, rd, rr, rq;\n\t"
+      "mov.b64 {%0, %1}, ro;\n\t}"
+      : "=f"(r0), "=f"(r1)
+      : "f"(x0), "f"(x1), "f"(-s), "f"(rs));
+}
+
 // fp32 pair -> bf16x2 word (lo in bits 0..15), round to nearest even.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t d;

@@ -281,7 +281,8 @@ fp4idx_status fp4idx_indexer_prepass_ex(
  *                s = E4M3(rn32(amax/6)) (round half to even, saturating at
  *                448), codes the nearest E2M1 of rn32(x/s) (ties to even,
  *                saturating at 6), values code*s; a group whose s rounds to
- *                0 becomes zeros.  No output is -0.
+ *                0 becomes zeros.  No output is -0.  Rows holding an inf
+ *                or NaN give unspecified values.
  *   out          bf16 [num_rows, 128], dense, 16-byte aligned.
  *   err_flags    FP4IDX_ERRFLAG_POSITION for a row whose position is out of
  *                range (that row is left untouched).
