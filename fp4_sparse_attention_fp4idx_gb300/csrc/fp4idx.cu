@@ -1145,6 +1145,17 @@ const char* fp4idx_version(void) { return "fp4idx 0.5.0 sm_103a"; }
 
 // H^-1/2 * D^-1/2 with D = 128, evaluated in double and rounded once to fp32;
 // 0 for a non-positive head count.
+fp4idx_status fp4idx_test_withhold_next(int kernel, int64_t index) {
+  if (index < 0) return FP4IDX_ERR_ARG;
+  if (kernel == FP4IDX_TEST_PREPASS)
+    fp4idx_impl::stream_withhold_next(index);
+  else if (kernel == FP4IDX_TEST_SCORER)
+    fp4idx_impl::scorer_withhold_next(index);
+  else
+    return FP4IDX_ERR_ARG;
+  return FP4IDX_OK;
+}
+
 float fp4idx_default_weight_scale(int64_t num_heads) {
   if (num_heads < 1) return 0.0f;
   return (float)(1.0 / sqrt((double)num_heads * (double)FP4IDX_HEAD_DIM));

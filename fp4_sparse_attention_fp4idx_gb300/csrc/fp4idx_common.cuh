@@ -329,4 +329,9 @@ namespace fp4idx_impl {
 bool stream_eligible(bool queries, int64_t H);
 fp4idx_status launch_stream(const KArgs& ka, const QArgs& qa, const Shared& sh, bool keys,
                             bool queries, int rope_style, int rotate, int fp8, void* stream);
+// The testing hook (fp4idx_test_withhold_next): the next launch of the
+// streaming kernel, or of a scorer, withholds the copies of work item `index`
+// of CTA 0 (a 64-row unit; a 128-key tile).
+void stream_withhold_next(int64_t index);
+void scorer_withhold_next(int64_t index);
 }  // namespace fp4idx_impl

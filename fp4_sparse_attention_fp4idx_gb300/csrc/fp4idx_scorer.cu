@@ -78,6 +78,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "fp4idx.h"
@@ -153,6 +154,7 @@ struct ScorerParams {
   int32_t ncols;        // logits columns (decode max_context, prefill key count)
   int32_t tiles_total;  // ceil(ncols / 128)
   int32_t stages;       // pair stages
+  int32_t withhold;     // testing: a tile of CTA 0 whose copies are not issued (-1: none)
 };
 
 struct Layout {
@@ -781,7 +783,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // every lane that writes the stage observes its release itself
         int ok = __all_sync(0xffffffffu, !active || wait_phase(bar_empty(ps), ph ^ 1u, abort));
         uint8_t* const sp = stage(ps);
-        if (ok && lane == 0) {
+        // testing hook (see fp4idx_test_withhold_next): this pair's copies and
+        // its arrival are withheld, so the waits for it run out
+        const bool withheld =
+            blockIdx.x == 0 && (k == p.withhold || (two && k + 1 == p.withhold));
+        if (ok && lane == 0 && !withheld) {
           ok = (!(hdr0 & kHdrSegFirst) || load_q(hdr0, qrow0)) &&
                (!two || !(hdr1 & kHdrSegFirst) || load_q(hdr1, qrow1));
           if (ok) {
@@ -795,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           stop = true;
           break;
         }
-        if (active && my_in) {
+        if (active && my_in && !withheld) {
           const uint32_t fb = bar_full(ps);
           if (!exps)
             tma_3d(smem_addr(sp + th * kTilePayload + pg * kPayloadBytes), &kmap, 0, 0, my_page, fb);
@@ -1088,6 +1094,10 @@ fp4idx_status device_setup(DeviceInfo& out, EncodeTiledFn& enc) {
   return enc ? FP4IDX_OK : FP4IDX_ERR_CUDA;
 }
 
+// Testing hook: the tile of CTA 0 whose copies the next scorer launch
+// withholds (-1: none), taken once.
+std::atomic<int64_t> g_withhold{-1};
+
 // Heads both scorers accept: a multiple of 32, at most 128 (a segment holds
 // at least one query token's heads).
 bool heads_ok(int64_t H) { return H >= 32 && H % 32 == 0 && H <= kMaxRows; }
@@ -1106,6 +1116,10 @@ fp4idx_status launch(ScorerParams& p, const uint8_t* q_fp4, const uint8_t* kv_ca
   p.stages = S;
   const int smem_bytes = (int)make_layout(S, R).total + 1024;
   p.tiles_total = (p.ncols + kTile - 1) / kTile;
+  {
+    const int64_t w = g_withhold.exchange(-1);
+    p.withhold = w >= 0 && w < (1ll << 30) ? (int32_t)w : -1;
+  }
 
   // The cache as a 3-D byte tensor: 64 payload bytes x 64 slots x pages.
   alignas(64) CUtensorMap kmap;
@@ -1229,3 +1243,9 @@ extern "C" fp4idx_status fp4idx_mqa_logits_prefill(
   p.ncols = (int32_t)num_keys;
   return launch(p, q_fp4, kv_cache, static_cast<cudaStream_t>(stream));
 }
+
+// The testing hook's scorer half (the C entry point, in fp4idx.cu, routes
+// here): the next scorer launch withholds the copies of tile `index` of CTA 0.
+namespace fp4idx_impl {
+void scorer_withhold_next(int64_t index) { g_withhold.store(index); }
+}  // namespace fp4idx_impl

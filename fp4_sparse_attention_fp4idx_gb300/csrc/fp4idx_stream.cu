@@ -62,6 +62,8 @@
 //  * Every wait is bounded (1 s); a timeout sets FP4IDX_ERRFLAG_TIMEOUT and
 //    the CTA drains its copies in flight before it exits.
 
+#include <atomic>
+
 #include "fp4idx_common.cuh"
 
 namespace fp4idx_impl {
@@ -119,6 +121,7 @@ struct SWork {
   int k_contig;    // key rows contiguous
   int w_bulk;      // head weights dense ([T, H]) and 16-byte aligned
   int meta_bulk;   // positions and slots 16-byte aligned
+  int withhold;    // testing: a unit of CTA 0 whose copies are not issued (-1: none)
 };
 
 __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
@@ -894,7 +897,11 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     // The first own unit's rows go out at once; every later unit's rows go
     // out together with its metadata (the first metadata waits for the
     // positions, and should not queue behind a whole ring of rows).
-    if (n_own > 0) issue_rows(p, u, wk, ka, qa, ring + (uint32_t)p * kStageBytesS, full0 + 8u * p);
+    // (testing hook, see fp4idx_test_withhold_next: a withheld unit's copies
+    // and arrival are skipped, so the waits for it run out)
+    const int held = blockIdx.x == 0 ? wk.withhold : -1;
+    if (n_own > 0 && p != held)
+      issue_rows(p, u, wk, ka, qa, ring + (uint32_t)p * kStageBytesS, full0 + 8u * p);
     for (int m = 0; m < n_own; ++m) {
       if (m % kBatch == 0) {
         if (m > 0) pos_cur = pos_next;
@@ -912,8 +919,8 @@ __global__ void __launch_bounds__(kThreadsS, 1)
           break;
         }
       }
-      if (m > 0) issue_rows(i, u, wk, ka, qa, stage, bar);
-      issue_meta(i, m % kBatch, u, wk, ka, qa, sh, pos_cur, stage, bar);
+      if (m > 0 && i != held) issue_rows(i, u, wk, ka, qa, stage, bar);
+      if (i != held) issue_meta(i, m % kBatch, u, wk, ka, qa, sh, pos_cur, stage, bar);
       issued = m + 1;
     }
     __syncwarp();
@@ -995,6 +1002,10 @@ void launch_style(unsigned grid, cudaStream_t s, const KArgs& ka, const QArgs& q
     stream_kernel<kStyle, true, true><<<grid, kThreadsS, kSmemS, s>>>(ka, qa, sh, wk);
 }
 
+// Testing hook: the unit of CTA 0 whose copies the next launch withholds
+// (-1: none), taken once.
+std::atomic<int64_t> g_stream_withhold{-1};
+
 int stream_sms() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesS) return 0;
@@ -1009,6 +1020,8 @@ int stream_sms() {
 }
 
 }  // namespace
+
+void stream_withhold_next(int64_t index) { g_stream_withhold.store(index); }
 
 bool stream_eligible(bool queries, int64_t H) { return !queries || H % kSliceRows == 0; }
 
@@ -1030,6 +1043,10 @@ fp4idx_status launch_stream(const KArgs& ka, const QArgs& qa, const Shared& sh, 
   wk.w_bulk = queries && qa.w_tstride == H && (reinterpret_cast<uintptr_t>(qa.w) % 16) == 0;
   wk.meta_bulk = keys && (reinterpret_cast<uintptr_t>(sh.pos) % 16) == 0 &&
                  (reinterpret_cast<uintptr_t>(ka.slots) % 16) == 0;
+  {
+    const int64_t w = g_stream_withhold.exchange(-1);
+    wk.withhold = w >= 0 && w < (1ll << 30) ? (int32_t)w : -1;
+  }
   const int64_t total = (int64_t)wk.nk + wk.nq;
   if (total == 0) return FP4IDX_OK;
   const int sms = stream_sms();

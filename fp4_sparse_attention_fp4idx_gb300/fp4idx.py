@@ -70,6 +70,7 @@ _SIGS = {
     "fp4idx_mqa_logits_prefill": (
         _INT, [_P, _P, _P, _P, _I64, _I64, _P, _P, _P, _I64, _I64, _I64, _P, _P]),
     "fp4idx_default_weight_scale": (_F, [_I64]),
+    "fp4idx_test_withhold_next": (_INT, [_INT, _I64]),
     "fp4idx_status_string": (ctypes.c_char_p, [_INT]),
     "fp4idx_version": (ctypes.c_char_p, []),
 }
@@ -137,6 +138,17 @@ def rope_style_code(style) -> int:
     if style in (ROPE_INTERLEAVED, "interleaved", "gptj"):
         return ROPE_INTERLEAVED
     raise ValueError(f"unknown rope style {style!r}")
+
+
+TEST_PREPASS = 0
+TEST_SCORER = 1
+
+
+def test_withhold_next(kernel: int, index: int) -> None:
+    """Testing hook: the next launch of `kernel` (TEST_PREPASS: the streaming
+    pre-pass; TEST_SCORER: the scorers) leaves out the copies of work item
+    `index` of its first CTA, so its bounded waits run out (TIMEOUT flag)."""
+    _check(_lib.fp4idx_test_withhold_next(int(kernel), int(index)), "fp4idx_test_withhold_next")
 
 
 def default_weight_scale(num_heads: int) -> float:

@@ -398,6 +398,24 @@ fp4idx_status fp4idx_mqa_logits_prefill(
  */
 float fp4idx_default_weight_scale(int64_t num_heads);
 
+/*
+ * Testing hook for the bounded waits (no counterpart in the pages: it exists
+ * so that the timeout path can be exercised without faulting the GPU).  The
+ * next launch of the given kernel, on any thread, leaves out the copies of
+ * one work item of its first CTA: a 64-row unit of the streaming pre-pass
+ * kernel (FP4IDX_TEST_PREPASS; units count key units first, then query
+ * units; head counts that are a multiple of 16), or a 128-key tile of the
+ * scorers (FP4IDX_TEST_SCORER; tiles count in that CTA's order, and a tile's
+ * partner in its stage pair is left out with it).  The waits for it then
+ * run out after their 1 s limit: that launch raises FP4IDX_ERRFLAG_TIMEOUT,
+ * leaves part of its outputs unwritten, drains its copies in flight and
+ * returns; later launches are unaffected.  The hook is taken by that one
+ * launch (an index past the CTA's work withholds nothing).  Returns
+ * FP4IDX_ERR_ARG for an unknown kernel or a negative index.
+ */
+enum { FP4IDX_TEST_PREPASS = 0, FP4IDX_TEST_SCORER = 1 };
+fp4idx_status fp4idx_test_withhold_next(int kernel, int64_t index);
+
 /* Static, NUL-terminated description of a status code. */
 const char* fp4idx_status_string(fp4idx_status status);
 

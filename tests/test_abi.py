@@ -32,7 +32,8 @@ def test_exports_every_declared_symbol(F):
                           "fp4idx_k_norm_rope_pack_store_ex", "fp4idx_q_rope_pack_weights_ex",
                           "fp4idx_indexer_prepass_ex", "fp4idx_rope_fake_quant",
                           "fp4idx_mqa_logits_prefill", "fp4idx_default_weight_scale",
-                          "fp4idx_status_string", "fp4idx_version"}
+                          "fp4idx_test_withhold_next", "fp4idx_status_string",
+                          "fp4idx_version"}
     out = subprocess.run(["nm", "-D", "--defined-only", F.LIB_PATH], capture_output=True,
                          text=True, check=True).stdout
     exported = set(re.findall(r"\bT (fp4idx_\w+)", out))
@@ -399,3 +400,14 @@ def test_default_weight_scale_closed_form(F):
         exact = 1.0 / (H * 128) ** 0.5
         assert abs(Fraction(got) - Fraction(exact)) <= Fraction(float(np.spacing(want))) / 2 * (1 + 1e-9)
     assert F.default_weight_scale(0) == 0.0
+
+
+def test_withhold_hook_argument_checks(F):
+    """The testing hook only arms itself for a known kernel and a
+    non-negative index (host-side, no launch); index 2^40 withholds nothing
+    (it is past any CTA's work) and is taken by the next launch."""
+    L = F.lib()
+    assert L.fp4idx_test_withhold_next(7, 0) == F.ERR_ARG
+    assert L.fp4idx_test_withhold_next(F.TEST_SCORER, -1) == F.ERR_ARG
+    assert L.fp4idx_test_withhold_next(F.TEST_PREPASS, 1 << 40) == F.OK
+    assert L.fp4idx_test_withhold_next(F.TEST_SCORER, 1 << 40) == F.OK
