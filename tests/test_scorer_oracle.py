@@ -221,3 +221,24 @@ def test_prefill_single_element_closed_form():
                                        np.array([70], np.int32), np.array([72], np.int32), 80)
     assert out[0, 70] == 12.0 and out[0, 71] == 0.0
     assert np.all(np.isneginf(out[0, :70])) and np.all(np.isneginf(out[0, 72:]))
+
+
+def test_prefill_matches_paged_scorer_on_identity_table():
+    """With every token's range the whole chunk, the prefill scorer is the
+    paged scorer of one sequence whose block table is the identity (key s in
+    page s/64) and whose next_n is the token count."""
+    rng = np.random.Generator(np.random.PCG64(45))
+    T, H, nk = 5, 32, 200
+    pages = -(-nk // 64)
+    cache = rng.integers(0, 256, (pages, 4352), dtype=np.uint8)
+    cache[:, 4096:] = rng.integers(118, 137, (pages, 256), dtype=np.uint8)
+    q = rng.integers(0, 256, (T, H, 64), dtype=np.uint8)
+    qs = rng.integers(118, 137, (T, H, 4), dtype=np.uint8)
+    w = rng.standard_normal((T, H)).astype(np.float32)
+    pre, st = oracle.mqa_logits_prefill(q, qs, w, cache, np.zeros(T, np.int32),
+                                        np.full(T, nk, np.int32), nk)
+    assert st == 0
+    paged, st = oracle.paged_mqa_logits(q, qs, w, cache, np.arange(pages, dtype=np.int32)[None],
+                                        np.array([nk], np.int32), T, nk)
+    assert st == 0
+    assert np.array_equal(pre.view(np.uint32), paged.view(np.uint32))
