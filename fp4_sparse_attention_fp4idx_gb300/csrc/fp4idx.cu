@@ -59,6 +59,9 @@
 //     otherwise (and always when e1 == 1, where the floor holds) stage 2
 //     reproduces stage 1.
 
+#include <atomic>
+#include <mutex>
+
 #include "fp4idx_common.cuh"
 
 namespace {
@@ -815,10 +818,11 @@ __global__ void __launch_bounds__(256) fake_quant_kernel(FQArgs fa) {
 // --------------------------------------------------------------- host side
 constexpr int kMaxDevices = 64;
 struct DeviceInfo {
-  int sm_count = 0;
+  std::atomic<int> sm_count{0};     // published (release) after blocks_per_sm
   int blocks_per_sm[2][2][2] = {};  // [style][rotate][fp8]
 };
 DeviceInfo g_devices[kMaxDevices];
+std::mutex g_setup_mutex;  // one thread sets a device up; the others wait
 
 template <int kStyle, bool kRotate, bool kFp8>
 int setup_kernel() {
@@ -838,7 +842,10 @@ int resident_ctas(int style, int rotate, int fp8) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
   DeviceInfo& di = g_devices[dev];
-  if (di.sm_count == 0) {
+  if (di.sm_count.load(std::memory_order_acquire) == 0) {
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    if (di.sm_count.load(std::memory_order_relaxed) != 0)
+      return di.sm_count.load(std::memory_order_relaxed) * di.blocks_per_sm[style][rotate][fp8];
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return 0;
@@ -857,9 +864,9 @@ int resident_ctas(int style, int rotate, int fp8) {
           if (n[a][b][c] < 1) return 0;
           di.blocks_per_sm[a][b][c] = n[a][b][c];
         }
-    di.sm_count = sms;
+    di.sm_count.store(sms, std::memory_order_release);
   }
-  return di.sm_count * di.blocks_per_sm[style][rotate][fp8];
+  return di.sm_count.load(std::memory_order_acquire) * di.blocks_per_sm[style][rotate][fp8];
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -903,9 +910,10 @@ fp4idx_status check_queries(const void* q, int64_t q_tstride, int64_t q_hstride,
 }
 
 template <int kStyle, bool kRotate, bool kFp8>
-void launch_one(unsigned grid, cudaStream_t s, const KArgs& ka, const QArgs& qa, const Shared& sh,
-                const Work& wk) {
-  prepass_kernel<kStyle, kRotate, kFp8><<<grid, kThreads, kSmemBytes, s>>>(ka, qa, sh, wk);
+cudaError_t launch_one(unsigned grid, cudaStream_t s, const KArgs& ka, const QArgs& qa,
+                       const Shared& sh, const Work& wk) {
+  return launch_kernel(prepass_kernel<kStyle, kRotate, kFp8>, grid, kThreads, kSmemBytes, s, ka,
+                       qa, sh, wk);
 }
 
 fp4idx_status launch(const KArgs& ka, const QArgs& qa, const Shared& sh, bool keys, bool queries,
@@ -930,17 +938,18 @@ fp4idx_status launch(const KArgs& ka, const QArgs& qa, const Shared& sh, bool ke
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const unsigned g = (unsigned)grid;
   const int which = (rope_style == FP4IDX_ROPE_NEOX ? 0 : 4) + (rotate ? 2 : 0) + (fp8 ? 1 : 0);
+  cudaError_t e;
   switch (which) {
-    case 0: launch_one<FP4IDX_ROPE_NEOX, false, false>(g, s, ka, qa, sh, wk); break;
-    case 1: launch_one<FP4IDX_ROPE_NEOX, false, true>(g, s, ka, qa, sh, wk); break;
-    case 2: launch_one<FP4IDX_ROPE_NEOX, true, false>(g, s, ka, qa, sh, wk); break;
-    case 3: launch_one<FP4IDX_ROPE_NEOX, true, true>(g, s, ka, qa, sh, wk); break;
-    case 4: launch_one<FP4IDX_ROPE_INTERLEAVED, false, false>(g, s, ka, qa, sh, wk); break;
-    case 5: launch_one<FP4IDX_ROPE_INTERLEAVED, false, true>(g, s, ka, qa, sh, wk); break;
-    case 6: launch_one<FP4IDX_ROPE_INTERLEAVED, true, false>(g, s, ka, qa, sh, wk); break;
-    default: launch_one<FP4IDX_ROPE_INTERLEAVED, true, true>(g, s, ka, qa, sh, wk); break;
+    case 0: e = launch_one<FP4IDX_ROPE_NEOX, false, false>(g, s, ka, qa, sh, wk); break;
+    case 1: e = launch_one<FP4IDX_ROPE_NEOX, false, true>(g, s, ka, qa, sh, wk); break;
+    case 2: e = launch_one<FP4IDX_ROPE_NEOX, true, false>(g, s, ka, qa, sh, wk); break;
+    case 3: e = launch_one<FP4IDX_ROPE_NEOX, true, true>(g, s, ka, qa, sh, wk); break;
+    case 4: e = launch_one<FP4IDX_ROPE_INTERLEAVED, false, false>(g, s, ka, qa, sh, wk); break;
+    case 5: e = launch_one<FP4IDX_ROPE_INTERLEAVED, false, true>(g, s, ka, qa, sh, wk); break;
+    case 6: e = launch_one<FP4IDX_ROPE_INTERLEAVED, true, false>(g, s, ka, qa, sh, wk); break;
+    default: e = launch_one<FP4IDX_ROPE_INTERLEAVED, true, true>(g, s, ka, qa, sh, wk); break;
   }
-  return cudaGetLastError() == cudaSuccess ? FP4IDX_OK : FP4IDX_ERR_CUDA;
+  return e == cudaSuccess ? FP4IDX_OK : FP4IDX_ERR_CUDA;
 }
 
 // Options: NULL means the defaults (compress ratio 1, no rotation, FP4).
@@ -1120,13 +1129,12 @@ fp4idx_status fp4idx_rope_fake_quant(const void* x, int64_t row_stride, int64_t 
   if (grid > (int64_t)sms * 8) grid = (int64_t)sms * 8;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int which = (rope_style == FP4IDX_ROPE_NEOX ? 0 : 2) + scale_mode;
-  switch (which) {
-    case 0: fake_quant_kernel<FP4IDX_ROPE_NEOX, 0><<<(unsigned)grid, 256, 0, s>>>(fa); break;
-    case 1: fake_quant_kernel<FP4IDX_ROPE_NEOX, 1><<<(unsigned)grid, 256, 0, s>>>(fa); break;
-    case 2: fake_quant_kernel<FP4IDX_ROPE_INTERLEAVED, 0><<<(unsigned)grid, 256, 0, s>>>(fa); break;
-    default: fake_quant_kernel<FP4IDX_ROPE_INTERLEAVED, 1><<<(unsigned)grid, 256, 0, s>>>(fa);
-  }
-  return cudaGetLastError() == cudaSuccess ? FP4IDX_OK : FP4IDX_ERR_CUDA;
+  auto kern = which == 0   ? fake_quant_kernel<FP4IDX_ROPE_NEOX, 0>
+              : which == 1 ? fake_quant_kernel<FP4IDX_ROPE_NEOX, 1>
+              : which == 2 ? fake_quant_kernel<FP4IDX_ROPE_INTERLEAVED, 0>
+                           : fake_quant_kernel<FP4IDX_ROPE_INTERLEAVED, 1>;
+  return launch_kernel(kern, (unsigned)grid, 256, 0, s, fa) == cudaSuccess ? FP4IDX_OK
+                                                                            : FP4IDX_ERR_CUDA;
 }
 
 const char* fp4idx_status_string(fp4idx_status status) {

@@ -8,6 +8,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include <cuda_fp16.h>
 
 #include "fp4idx.h"
@@ -324,6 +326,20 @@ inline FastDiv make_fastdiv(uint32_t d) {
 }  // namespace fp4idx_impl
 
 namespace fp4idx_impl {
+// Launches kern on stream s and returns this launch's own status:
+// cudaLaunchKernelEx reports its result directly, without reading or
+// clearing an error that the caller's own work left in the runtime.
+template <typename... Params, typename... Args>
+inline cudaError_t launch_kernel(void (*kern)(Params...), unsigned grid, unsigned block,
+                                 size_t smem, cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 // The streaming kernel (fp4idx_stream.cu): every output mode, with or
 // without the rotation; for queries a head count that is a multiple of 16.
 bool stream_eligible(bool queries, int64_t H);

@@ -1148,14 +1148,20 @@ fp4idx_status launch(ScorerParams& p, const uint8_t* q_fp4, const uint8_t* kv_ca
         CUDA_SUCCESS)
       return FP4IDX_ERR_CUDA;
   }
-  if (cudaPeekAtLastError() != cudaSuccess) return FP4IDX_ERR_CUDA;  // an earlier error
   const int cpj = p.H / 32;
   auto kern = cpj == 1 ? scorer_kernel<1>
               : cpj == 2 ? scorer_kernel<2>
               : cpj == 3 ? scorer_kernel<3>
                          : scorer_kernel<4>;
-  kern<<<(unsigned)di.sms, kThreads, smem_bytes, stream>>>(p, kmap, qmap);
-  return cudaPeekAtLastError() == cudaSuccess ? FP4IDX_OK : FP4IDX_ERR_CUDA;
+  // cudaLaunchKernelEx reports this launch's own status, without reading or
+  // clearing an error that the caller's own work left in the runtime
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)di.sms);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem_bytes;
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, kern, p, kmap, qmap) == cudaSuccess ? FP4IDX_OK
+                                                                        : FP4IDX_ERR_CUDA;
 }
 
 }  // namespace

@@ -63,6 +63,7 @@
 //    the CTA drains its copies in flight before it exits.
 
 #include <atomic>
+#include <mutex>
 
 #include "fp4idx_common.cuh"
 
@@ -968,7 +969,10 @@ __global__ void __launch_bounds__(kThreadsS, 1)
 
 // --------------------------------------------------------------- host side
 constexpr int kMaxDevicesS = 64;
-int g_sms[kMaxDevicesS];  // 0: not set up yet (a failed set-up is retried)
+// 0: not set up yet (a failed set-up is retried); published with release
+// once the kernel attributes are set, under g_sms_mutex
+std::atomic<int> g_sms[kMaxDevicesS];
+std::mutex g_sms_mutex;
 
 template <int kStyle, bool kRotate, bool kFp8>
 bool setup_stream() {
@@ -988,18 +992,15 @@ bool setup_style() {
          setup_stream<kStyle, true, false>() && setup_stream<kStyle, true, true>();
 }
 
-// The kernel for (rotate, fp8).
+// The kernel for (rotate, fp8); returns the launch's own status.
 template <int kStyle>
-void launch_style(unsigned grid, cudaStream_t s, const KArgs& ka, const QArgs& qa,
-                  const Shared& sh, const SWork& wk, int rotate, int fp8) {
-  if (!rotate && !fp8)
-    stream_kernel<kStyle, false, false><<<grid, kThreadsS, kSmemS, s>>>(ka, qa, sh, wk);
-  else if (!rotate)
-    stream_kernel<kStyle, false, true><<<grid, kThreadsS, kSmemS, s>>>(ka, qa, sh, wk);
-  else if (!fp8)
-    stream_kernel<kStyle, true, false><<<grid, kThreadsS, kSmemS, s>>>(ka, qa, sh, wk);
-  else
-    stream_kernel<kStyle, true, true><<<grid, kThreadsS, kSmemS, s>>>(ka, qa, sh, wk);
+cudaError_t launch_style(unsigned grid, cudaStream_t s, const KArgs& ka, const QArgs& qa,
+                         const Shared& sh, const SWork& wk, int rotate, int fp8) {
+  auto kern = !rotate && !fp8 ? stream_kernel<kStyle, false, false>
+              : !rotate       ? stream_kernel<kStyle, false, true>
+              : !fp8          ? stream_kernel<kStyle, true, false>
+                              : stream_kernel<kStyle, true, true>;
+  return launch_kernel(kern, grid, kThreadsS, kSmemS, s, ka, qa, sh, wk);
 }
 
 // Testing hook: the unit of CTA 0 whose copies the next launch withholds
@@ -1009,14 +1010,17 @@ std::atomic<int64_t> g_stream_withhold{-1};
 int stream_sms() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesS) return 0;
-  if (g_sms[dev] == 0) {
+  const int known = g_sms[dev].load(std::memory_order_acquire);
+  if (known != 0) return known;
+  std::lock_guard<std::mutex> lock(g_sms_mutex);
+  if (g_sms[dev].load(std::memory_order_relaxed) == 0) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         !setup_style<FP4IDX_ROPE_NEOX>() || !setup_style<FP4IDX_ROPE_INTERLEAVED>())
       return 0;
-    g_sms[dev] = sms;
+    g_sms[dev].store(sms, std::memory_order_release);
   }
-  return g_sms[dev];
+  return g_sms[dev].load(std::memory_order_relaxed);
 }
 
 }  // namespace
@@ -1053,11 +1057,11 @@ fp4idx_status launch_stream(const KArgs& ka, const QArgs& qa, const Shared& sh, 
   if (sms <= 0) return FP4IDX_ERR_CUDA;
   const unsigned grid = (unsigned)(total < sms ? total : sms);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (rope_style == FP4IDX_ROPE_NEOX)
-    launch_style<FP4IDX_ROPE_NEOX>(grid, s, ka, qa, sh, wk, rotate, fp8);
-  else
-    launch_style<FP4IDX_ROPE_INTERLEAVED>(grid, s, ka, qa, sh, wk, rotate, fp8);
-  return cudaGetLastError() == cudaSuccess ? FP4IDX_OK : FP4IDX_ERR_CUDA;
+  const cudaError_t e =
+      rope_style == FP4IDX_ROPE_NEOX
+          ? launch_style<FP4IDX_ROPE_NEOX>(grid, s, ka, qa, sh, wk, rotate, fp8)
+          : launch_style<FP4IDX_ROPE_INTERLEAVED>(grid, s, ka, qa, sh, wk, rotate, fp8);
+  return e == cudaSuccess ? FP4IDX_OK : FP4IDX_ERR_CUDA;
 }
 
 }  // namespace fp4idx_impl

@@ -17,6 +17,7 @@ from __future__ import annotations
 import ctypes
 import os
 import re
+import threading
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfp4idx.so")
@@ -345,9 +346,12 @@ class _HostPipe:
         self.ev_in = [torch.cuda.Event() for _ in range(2)]
         self.ev_run = [torch.cuda.Event() for _ in range(2)]
         self.ev_out = [torch.cuda.Event() for _ in range(2)]
+        # one call enqueues at a time (the events below order the GPU work)
+        self.lock = threading.Lock()
 
 
 _HOST_PIPES = {}
+_HOST_PIPES_LOCK = threading.Lock()
 
 
 def _need_host(t, dtype, name, ndim):
@@ -404,13 +408,31 @@ def indexer_prepass_host(k, gamma, slot_mapping, kv_cache, q, w, positions, cos_
     dev = kv_cache.device
     chunk = min(int(chunk_tokens), max(T, 1))
     key = (dev.index, chunk, H)
-    pipe = _HOST_PIPES.get(key)
-    if pipe is None:
-        pipe = _HOST_PIPES[key] = _HostPipe(dev, chunk, H)
+    with _HOST_PIPES_LOCK:
+        pipe = _HOST_PIPES.get(key)
+        if pipe is None:
+            pipe = _HOST_PIPES[key] = _HostPipe(dev, chunk, H)
     caller = stream if stream is not None else torch.cuda.current_stream(dev)
-    # everything already queued on the caller's stream comes first
+    with pipe.lock:
+        _host_pipeline(pipe, caller, chunk, T, k, gamma, slot_mapping, kv_cache, q, w,
+                       positions, cos_cache, sin_cache, eps, rope_style, weight_scale, q_fp4,
+                       q_scale, weights, err_flags)
+    return q_fp4, q_scale, weights
+
+
+def _host_pipeline(pipe, caller, chunk, T, k, gamma, slot_mapping, kv_cache, q, w, positions,
+                   cos_cache, sin_cache, eps, rope_style, weight_scale, q_fp4, q_scale, weights,
+                   err_flags):
+    torch = _torch()
+    # everything already queued on the caller's stream comes first, and so
+    # does an earlier call on this pipe: its kernels read the staging inputs
+    # (ev_run) and its downloads read the staging outputs (ev_out) that this
+    # call's first chunks overwrite (an event never recorded is no wait)
     for s in (pipe.s_in, pipe.s_run, pipe.s_out):
         s.wait_stream(caller)
+    for b in range(2):
+        pipe.s_in.wait_event(pipe.ev_run[b])
+        pipe.s_run.wait_event(pipe.ev_out[b])
     for c in range((T + chunk - 1) // chunk):
         b, t0 = c & 1, c * chunk
         t1 = min(T, t0 + chunk)
