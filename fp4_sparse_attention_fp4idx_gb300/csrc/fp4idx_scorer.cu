@@ -36,28 +36,28 @@
 // The tile rate of a one-CTA-per-SM pipeline is set by the longest serial
 // chain of dependent instructions that one warp runs per tile, not by the
 // copy latency: an mbarrier operation costs one thread on the order of a
-// hundred cycles and a copy issue about fifty.  So consecutive tiles are
-// taken in pairs that share one stage and one full / empty barrier pair,
-// and issuer m, accumulator m and epilogue group m form a private pipeline
-// for the tiles k = m (mod 3).
-//   warp 3       producer, a pair per step.  Every 16 tiles, a batch ahead,
-//                its lanes describe the batch's tiles in parallel (page ids,
-//                a header word per tile, the segment's first query row).  Per
-//                pair, lanes 4h .. 4h + 3 wait for the stage, then issue the
-//                TMA tensor copies of tile h's two page payloads (64-byte
-//                swizzled, the layout the MMA reads) and the bulk copies of
-//                their exponent words; lane 0 first writes the two header
-//                words and, at a segment's first tile, loads the segment's
+// hundred cycles and a copy issue about fifty.  So four consecutive tiles
+// share one stage and one full / empty barrier pair, and issuer m,
+// accumulator m and epilogue group m form a private pipeline for the tiles
+// k = m (mod 3).
+//   warp 3       producer, a stage of four tiles per step.  Every 16 tiles,
+//                a batch ahead, its lanes describe the batch's tiles in
+//                parallel (page ids, a header word per tile, the segment's
+//                first query row).  Per stage, lanes 4h .. 4h + 3 wait for it,
+//                then issue the TMA tensor copies of tile h's two page
+//                payloads (64-byte swizzled, the layout the MMA reads) and the
+//                bulk copies of their exponent words; lane 0 first writes the
+//                four header words and, at a segment's first tile, loads the segment's
 //                query operand and scale words into a query buffer (in
 //                segment order) and makes the buffer releases of the issuers
 //                that have no tile in the segment.
-//   warps 0-2    issuers: tile k belongs to issuer m = k % 3.  Once the pair
+//   warps 0-2    issuers: tile k belongs to issuer m = k % 3.  Once the stage
 //                has landed, the warp transposes the tile's 128 exponent
 //                words (and at its first tile of a segment the queries'
 //                words) into the 32 x 128-bit blocks tcgen05.cp reads; lane
 //                0 then issues tcgen05.cp into TMEM, the two MMAs into
 //                accumulator m and commits that mark the accumulator full,
-//                the tile's half of the stage free and, after the issuer's
+//                the tile's share of the stage free and, after the issuer's
 //                last tile of a segment, its share of the segment's query
 //                buffer free (a buffer is free once three releases came).
 //   warps 4-15   epilogue: group m = (w - 4) / 4 reads accumulator m; one
@@ -107,20 +107,21 @@ constexpr int kMaxChunks = kMaxRows / 32;
 constexpr int kMaxTps = kMaxRows / 32;         // query tokens per segment (H >= 32)
 constexpr int kMaxAccs = kEpiGroups;           // TMEM accumulators
 constexpr int kQBufs = 4;                      // query operand buffers
-constexpr int kMaxPairs = 8;                   // pair stages (two tiles each)
+constexpr int kTps = 4;                        // tiles per stage
+constexpr int kMaxStages = 4;                  // stages (kTps tiles each)
 constexpr int kSegTab = 512;                   // segment ranges kept in shared memory
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCols = 8;                // TMEM columns per scale-word slot
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
-// Offsets inside a pair stage: tiles h = 0, 1 of a pair share one stage,
-// one full and one empty barrier.
+// Offsets inside a stage: tiles h = 0 .. kTps-1 share one stage, one full
+// and one empty barrier.
 constexpr uint32_t kTilePayload = 2 * kPayloadBytes;  // 8192: tile h's two swizzled payloads at +8192h
-constexpr uint32_t kPsExp = 2 * kTilePayload;         // tile h's 2 x 256 exponent words at +512h
-constexpr uint32_t kPsSfa = kPsExp + 1024;            // tile h's keys' words, transposed, at +512h
-constexpr uint32_t kPsSfb = kPsSfa + 1024;            // tile h's queries' words, transposed, at +512h
-constexpr uint32_t kPsHdr = kPsSfb + 1024;            // one header word per tile
-constexpr uint32_t kPairBytes = 20480;                // a multiple of 1024
+constexpr uint32_t kPsExp = kTps * kTilePayload;      // tile h's 2 x 256 exponent words at +512h
+constexpr uint32_t kPsSfa = kPsExp + kTps * 512;      // tile h's keys' words, transposed, at +512h
+constexpr uint32_t kPsSfb = kPsSfa + kTps * 512;      // tile h's queries' words, transposed, at +512h
+constexpr uint32_t kPsHdr = kPsSfb + kTps * 512;      // one header word per tile
+constexpr uint32_t kStageBytes = (kPsHdr + 4 * kTps + 1023) / 1024 * 1024;  // a multiple of 1024
 // A tile's header word (written by the producer, read by the tile's issuer):
 // query buffer (bits 0-1), its fill parity (bit 2), the issuer's first
 // (bit 3) and last (bit 4) tile of the segment here, the segment's first
@@ -153,7 +154,7 @@ struct ScorerParams {
   int32_t R;            // tps * H
   int32_t ncols;        // logits columns (decode max_context, prefill key count)
   int32_t tiles_total;  // ceil(ncols / 128)
-  int32_t stages;       // pair stages
+  int32_t stages;       // stages of kTps tiles
   int32_t withhold;     // testing: a tile of CTA 0 whose copies are not issued (-1: none)
 };
 
@@ -161,13 +162,13 @@ struct Layout {
   uint32_t q, qs, w, tab, bars, misc, total;
 };
 
-// mbarriers: full and empty per pair stage; full and empty per accumulator;
+// mbarriers: full and empty per stage; full and empty per accumulator;
 // empty and full per query buffer.
 __host__ __device__ constexpr int kBarriers(int P) { return 2 * P + 2 * kMaxAccs + 2 * kQBufs; }
 
 __host__ __device__ inline Layout make_layout(int P, int R) {
   Layout L;
-  L.q = (uint32_t)P * kPairBytes;                   // kQBufs x R x 64 swizzled queries
+  L.q = (uint32_t)P * kStageBytes;                   // kQBufs x R x 64 swizzled queries
   L.qs = L.q + (uint32_t)kQBufs * R * 64;           // kQBufs x 128 query scale words
   L.w = L.qs + (uint32_t)kQBufs * 512u;             // per epilogue warp: kMaxRows weights
   L.tab = L.w + (uint32_t)kEpiWarps * kMaxRows * 4u;  // kSegTab x (lo, hi, lim)
@@ -568,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* const misc = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile uint32_t* const abort = misc + 1;
   int32_t* const start = reinterpret_cast<int32_t*>(misc + 2);  // g0, toff, n, pg0, poff, pn
-  auto stage = [&](int s) { return smem + (uint32_t)s * kPairBytes; };
+  auto stage = [&](int s) { return smem + (uint32_t)s * kStageBytes; };
   auto bar_full = [&](int s) { return bars + 8u * (uint32_t)s; };
   auto bar_empty = [&](int s) { return bars + 8u * (uint32_t)(S + s); };
   auto bar_accf = [&](int a) { return bars + 8u * (uint32_t)(2 * S + a); };
@@ -669,10 +670,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (n > 0) {
     if (tid == 0) {
       for (int i = 0; i < kBarriers(S); ++i) {
-        // a pair stage's empty takes one arrival per tile, acc_empty one per
+        // a stage's empty takes one arrival per tile, acc_empty one per
         // warp of its epilogue group, a query buffer's empty one per issuer
         const int j = i - 2 * S;
-        const int cnt = i >= S && i < 2 * S                             ? 2
+        const int cnt = i >= S && i < 2 * S                             ? kTps
                         : j >= kMaxAccs && j < 2 * kMaxAccs                ? 4
                         : j >= 2 * kMaxAccs && j < 2 * kMaxAccs + kQBufs ? kIssuers
                                                                          : 1;
@@ -697,11 +698,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // accumulator a at A*R + 8a; the queries' words of buffer b for issuer m
   // at A*R + 8A + 8(m*QB + b) (each issuer copies its own).
   const uint32_t sfa_col0 = (uint32_t)A * R, sfb_col0 = sfa_col0 + kMaxAccs * kSfCols;
-  int last_issued = -1;  // producer: the last pair whose copies were issued
+  int last_issued = -1;  // producer: the last stage use whose copies were issued
   int q_issued[4] = {-1, -1, -1, -1};  // producers: parity of the last query copy per buffer
 
   if (n > 0 && warp == kProducerWarp) {
-    // ---- producer: a pair of tiles per step -----------------------------------
+    // ---- producer: a stage of kTps tiles per step ------------------------------
     // Per batch of 16 tiles, a batch ahead, lane L describes half L % 2 of
     // tile m0 + L / 2: the page id (and whether the page is read), the tile's
     // header word and the first query row of its segment.
@@ -752,10 +753,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int o = (int)((hdr >> 6) & 3u); o < kIssuers; ++o) mbar_arrive(bar_qempty(qb));
       return true;
     };
-    // Lanes 4h .. 4h + 3 copy tile h of the pair: lanes 4h and 4h + 1 the
+    // Lanes 4h .. 4h + 3 copy tile h of a stage: lanes 4h and 4h + 1 the
     // two page payloads (TMA, 64-byte swizzled, the layout the MMA reads),
     // lanes 4h + 2 and 4h + 3 the pages' exponent words (bulk copies).
-    const int th = (lane >> 2) & 1, pg = lane & 1;
+    const int th = lane >> 2, pg = lane & 1;
     const bool exps = (lane & 2) != 0;
     Desc cur = describe(0), nxt = {-1, 0, 0u, 0};
     int ps = 0;
@@ -763,37 +764,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool stop = false;
     for (int m0 = 0; m0 < n && !stop; m0 += 16) {
       if (m0 + 16 < n) nxt = describe(m0 + 16);
-      for (int i = 0; i < 16 && m0 + i < n; i += 2) {
+      for (int i = 0; i < 16 && m0 + i < n; i += kTps) {
         const int k = m0 + i;
-        const bool two = k + 1 < n;
-        const bool active = lane < 4 || (lane < 8 && two);
+        const int nt = min(kTps, n - k);  // tiles in this stage
+        // lanes 4h .. 4h + 3 copy tile h: its two payloads, then its two
+        // exponent-word arrays
+        const bool active = th < nt;
         const int src = 2 * (i + th) + pg;
         const int32_t my_page = __shfl_sync(0xffffffffu, cur.id, src);
         int my_in = __shfl_sync(0xffffffffu, cur.in, src);
-        const uint32_t hdr0 = __shfl_sync(0xffffffffu, cur.hdr, 2 * i);
-        const uint32_t hdr1 = __shfl_sync(0xffffffffu, cur.hdr, 2 * i + 2);
-        const int32_t qrow0 = __shfl_sync(0xffffffffu, cur.qrow, 2 * i);
-        const int32_t qrow1 = __shfl_sync(0xffffffffu, cur.qrow, 2 * i + 2);
+        uint32_t hdr[kTps];
+        int32_t qrow[kTps];
+#pragma unroll
+        for (int t = 0; t < kTps; ++t) {
+          hdr[t] = __shfl_sync(0xffffffffu, cur.hdr, 2 * (i + t));
+          qrow[t] = __shfl_sync(0xffffffffu, cur.qrow, 2 * (i + t));
+        }
         if (my_in && (my_page < 0 || my_page >= p.num_blocks)) {  // not read
           if (active && !exps) flag_error(p.err, FP4IDX_ERRFLAG_PAGE);
           my_in = 0;
         }
-        // pages read, lanes 0, 1 (tile 0) and 4, 5 (tile 1)
+        // pages read: lanes 4h and 4h + 1 of each tile h
         const uint32_t rd = __ballot_sync(0xffffffffu, active && !exps && my_in);
         // every lane that writes the stage observes its release itself
         int ok = __all_sync(0xffffffffu, !active || wait_phase(bar_empty(ps), ph ^ 1u, abort));
         uint8_t* const sp = stage(ps);
-        // testing hook (see fp4idx_test_withhold_next): this pair's copies and
+        // testing hook (see fp4idx_test_withhold_next): this stage's copies and
         // its arrival are withheld, so the waits for it run out
-        const bool withheld =
-            blockIdx.x == 0 && (k == p.withhold || (two && k + 1 == p.withhold));
+        const bool withheld = blockIdx.x == 0 && p.withhold >= k && p.withhold < k + nt;
         if (ok && lane == 0 && !withheld) {
-          ok = (!(hdr0 & kHdrSegFirst) || load_q(hdr0, qrow0)) &&
-               (!two || !(hdr1 & kHdrSegFirst) || load_q(hdr1, qrow1));
+#pragma unroll
+          for (int t = 0; t < kTps; ++t)
+            if (ok && t < nt && (hdr[t] & kHdrSegFirst)) ok = load_q(hdr[t], qrow[t]);
           if (ok) {
-            *reinterpret_cast<uint2*>(sp + kPsHdr) = make_uint2(hdr0, hdr1);
-            mbar_expect_tx(bar_full(ps), (uint32_t)__popc(rd & 0x33u) * (kPayloadBytes + kExpBytes));
-            last_issued = k >> 1;
+#pragma unroll
+            for (int t = 0; t < kTps; ++t)
+              reinterpret_cast<uint32_t*>(sp + kPsHdr)[t] = hdr[t];
+            mbar_expect_tx(bar_full(ps), (uint32_t)__popc(rd & 0x33333333u) * (kPayloadBytes + kExpBytes));
+            last_issued = k / kTps;
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -825,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sfa = tmem + sfa_col0 + kSfCols * (uint32_t)m;
     int issued = 0;
     for (int k = m; k < n; k += kIssuers) {
-      const int j = k >> 1, h = k & 1, ps = j % S;
+      const int j = k / kTps, h = k % kTps, ps = j % S;
       const uint32_t ph = (uint32_t)(j / S) & 1u;
       // Lane 0 waits; then every lane, which reads the landed words, observes
       // the completed phase itself (acquire): a wait by one lane alone does
@@ -871,7 +879,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_mxf4(d, adesc, qdesc, id0, sfa, sfb, 0u);
           mma_mxf4(d, adesc + 2, qdesc + 2, id1, sfa, sfb, 1u);
           // Each commit tracks every earlier MMA of this thread: the
-          // accumulator is full, this tile's half of the pair stage can be
+          // accumulator is full, this tile's share of the stage can be
           // refilled, and after this issuer's last tile of the segment, its
           // share of the query buffer is released.
           mma_commit(bar_accf(m));
@@ -1110,7 +1118,7 @@ fp4idx_status launch(ScorerParams& p, const uint8_t* q_fp4, const uint8_t* kv_ca
   const fp4idx_status ds = device_setup(di, encode);
   if (ds != FP4IDX_OK) return ds;
   const int R = p.R;  // <= 128: 3 accumulators + scale words fit 512 TMEM columns
-  int S = kMaxPairs;
+  int S = kMaxStages;
   while (S > 1 && (int)make_layout(S, R).total + 1024 > di.smem_optin) --S;
   if ((int)make_layout(S, R).total + 1024 > di.smem_optin) return FP4IDX_ERR_SHAPE;
   p.stages = S;
