@@ -14,7 +14,7 @@ import sys
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 SRCS = [os.path.join(PKG, "csrc", name)
-        for name in ("fp4idx.cu", "fp4idx_stream.cu", "fp4idx_scorer.cu")]
+        for name in ("fp4idx.cu", "fp4idx_stream.cu", "fp4idx_scorer.cu", "fp4idx_host.cu")]
 HDRS = [os.path.join(ROOT, "include", "fp4idx.h"), os.path.join(PKG, "csrc", "fp4idx_common.cuh")]
 LIB = os.path.join(PKG, "libfp4idx.so")
 

@@ -971,6 +971,28 @@ fp4idx_status check_options(const fp4idx_options* o, int64_t& pos_mask, int& rot
 
 }  // namespace
 
+namespace fp4idx_impl {
+fp4idx_status prepass_check(const void* k, int64_t k_token_stride, const void* gamma, float eps,
+                            const int64_t* slot_mapping, const uint8_t* kv_cache,
+                            int64_t num_blocks, const void* q, int64_t q_token_stride,
+                            int64_t q_head_stride, const void* w, float weight_scale,
+                            const uint8_t* q_fp4, const uint8_t* q_scale,
+                            const float* weights_out, int64_t num_heads,
+                            const int64_t* positions, const float* cos_cache,
+                            const float* sin_cache, int64_t max_pos, int rope_style,
+                            int64_t num_tokens, const uint32_t* err_flags, int fp8) {
+  fp4idx_status st = check_shared(positions, cos_cache, sin_cache, max_pos, rope_style);
+  if (st != FP4IDX_OK) return st;
+  st = check_keys(k, k_token_stride, gamma, eps, slot_mapping, kv_cache, num_blocks);
+  if (st != FP4IDX_OK) return st;
+  st = check_queries(q, q_token_stride, q_head_stride, w, weight_scale, q_fp4, q_scale,
+                     weights_out, num_tokens, num_heads, fp8);
+  if (st != FP4IDX_OK) return st;
+  if (err_flags && !aligned(err_flags, 4)) return FP4IDX_ERR_ALIGN;
+  return FP4IDX_OK;
+}
+}  // namespace fp4idx_impl
+
 // ------------------------------------------------------------------- C ABI
 extern "C" {
 
@@ -1061,18 +1083,15 @@ fp4idx_status fp4idx_indexer_prepass_ex(
     const fp4idx_options* options, uint32_t* err_flags, void* stream) {
   if (num_tokens < 0) return FP4IDX_ERR_SHAPE;
   if (num_tokens == 0) return FP4IDX_OK;
-  fp4idx_status st = check_shared(positions, cos_cache, sin_cache, max_pos, rope_style);
-  if (st != FP4IDX_OK) return st;
-  st = check_keys(k, k_token_stride, gamma, eps, slot_mapping, kv_cache, num_blocks);
-  if (st != FP4IDX_OK) return st;
   int64_t pos_mask;
   int rotate, fp8;
-  st = check_options(options, pos_mask, rotate, fp8);
+  fp4idx_status st = check_options(options, pos_mask, rotate, fp8);
   if (st != FP4IDX_OK) return st;
-  st = check_queries(q, q_token_stride, q_head_stride, w, weight_scale, q_fp4, q_scale,
-                     weights_out, num_tokens, num_heads, fp8);
+  st = prepass_check(k, k_token_stride, gamma, eps, slot_mapping, kv_cache, num_blocks, q,
+                     q_token_stride, q_head_stride, w, weight_scale, q_fp4, q_scale,
+                     weights_out, num_heads, positions, cos_cache, sin_cache, max_pos,
+                     rope_style, num_tokens, err_flags, fp8);
   if (st != FP4IDX_OK) return st;
-  if (err_flags && !aligned(err_flags, 4)) return FP4IDX_ERR_ALIGN;
 
   KArgs ka{static_cast<const uint16_t*>(k), k_token_stride, static_cast<const uint16_t*>(gamma),
            eps, slot_mapping, kv_cache, num_blocks,

@@ -1,6 +1,6 @@
 // fp4idx_common.cuh -- constants, PTX wrappers, arithmetic helpers and
 // argument blocks shared by the pre-pass kernels (fp4idx.cu and
-// fp4idx_stream.cu).  Internal to the library; the public contract is
+// fp4idx_stream.cu) and the host-buffer pipeline (fp4idx_host.cu).  Internal to the library; the public contract is
 // include/fp4idx.h.
 #pragma once
 
@@ -350,4 +350,16 @@ fp4idx_status launch_stream(const KArgs& ka, const QArgs& qa, const Shared& sh, 
 // of CTA 0 (a 64-row unit; a 128-key tile).
 void stream_withhold_next(int64_t index);
 void scorer_withhold_next(int64_t index);
+
+// The host-side checks of fp4idx_indexer_prepass(_ex) without the launch
+// (fp8: the FP8 output mode, where q_scale may be NULL).
+fp4idx_status prepass_check(const void* k, int64_t k_token_stride, const void* gamma, float eps,
+                            const int64_t* slot_mapping, const uint8_t* kv_cache,
+                            int64_t num_blocks, const void* q, int64_t q_token_stride,
+                            int64_t q_head_stride, const void* w, float weight_scale,
+                            const uint8_t* q_fp4, const uint8_t* q_scale,
+                            const float* weights_out, int64_t num_heads,
+                            const int64_t* positions, const float* cos_cache,
+                            const float* sin_cache, int64_t max_pos, int rope_style,
+                            int64_t num_tokens, const uint32_t* err_flags, int fp8);
 }  // namespace fp4idx_impl

@@ -70,6 +70,10 @@ _SIGS = {
         _INT, [_P, _P, _P, _P, _I64, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _I64, _P, _P]),
     "fp4idx_mqa_logits_prefill": (
         _INT, [_P, _P, _P, _P, _I64, _I64, _P, _P, _P, _I64, _I64, _I64, _P, _P]),
+    "fp4idx_indexer_prepass_host": (
+        _INT, [_P, _P, _P, _F, _P, _I64, _P, _P, _I64, _F, _P, _P, _P, _P, _P, _P, _I64,
+               _INT, _I64, _I64, _P, _P, _P]),
+    "fp4idx_host_staging_bytes": (ctypes.c_size_t, [_I64, _I64]),
     "fp4idx_default_weight_scale": (_F, [_I64]),
     "fp4idx_test_withhold_next": (_INT, [_INT, _I64]),
     "fp4idx_status_string": (ctypes.c_char_p, [_INT]),
@@ -325,33 +329,8 @@ def indexer_prepass(k, gamma, slot_mapping, kv_cache, q, w, positions, cos_cache
 
 
 # ------------------------------------------------------- host-buffer pipeline
-class _HostPipe:
-    """Device staging for two chunks, three streams and their events."""
-
-    def __init__(self, device, chunk: int, H: int):
-        torch = _torch()
-        self.s_in, self.s_run, self.s_out = (torch.cuda.Stream(device) for _ in range(3))
-
-        def two(shape, dt):
-            return [torch.empty(shape, dtype=dt, device=device) for _ in range(2)]
-
-        self.q = two((chunk, H, HEAD_DIM), torch.bfloat16)
-        self.k = two((chunk, HEAD_DIM), torch.bfloat16)
-        self.w = two((chunk, H), torch.bfloat16)
-        self.pos = two((chunk,), torch.int64)
-        self.slots = two((chunk,), torch.int64)
-        self.qf = two((chunk, H, 64), torch.uint8)
-        self.qs = two((chunk, H, 4), torch.uint8)
-        self.wt = two((chunk, H), torch.float32)
-        self.ev_in = [torch.cuda.Event() for _ in range(2)]
-        self.ev_run = [torch.cuda.Event() for _ in range(2)]
-        self.ev_out = [torch.cuda.Event() for _ in range(2)]
-        # one call enqueues at a time (the events below order the GPU work)
-        self.lock = threading.Lock()
-
-
-_HOST_PIPES = {}
-_HOST_PIPES_LOCK = threading.Lock()
+_STAGING = {}  # (device index, chunk_tokens, H) -> device staging tensor
+_STAGING_LOCK = threading.Lock()
 
 
 def _need_host(t, dtype, name, ndim):
@@ -367,19 +346,34 @@ def _need_host(t, dtype, name, ndim):
     return t
 
 
+def _staging(device, chunk: int, H: int):
+    """The device staging buffer of fp4idx_indexer_prepass_host, allocated
+    once per (device, chunk, H) and kept (its contents are scratch)."""
+    torch = _torch()
+    nbytes = int(_lib.fp4idx_host_staging_bytes(chunk, H))
+    if nbytes == 0:
+        raise ValueError(f"chunk_tokens {chunk} x num_heads {H} is too large")
+    key = (device.index, chunk, H)
+    with _STAGING_LOCK:
+        buf = _STAGING.get(key)
+        if buf is None:
+            buf = _STAGING[key] = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return buf
+
+
 def indexer_prepass_host(k, gamma, slot_mapping, kv_cache, q, w, positions, cos_cache,
                          sin_cache, *, eps: float = 1e-6, rope_style="neox", weight_scale=None,
                          q_fp4=None, q_scale=None, weights=None, chunk_tokens: int = 4096,
                          err_flags=None, stream=None):
-    """indexer_prepass for inputs and outputs in host memory: k [T,128], q
-    [T,H,128], w [T,H] (bf16), positions and slot_mapping [T] (int64) are
-    contiguous host tensors, pinned for the copies to overlap; gamma, the
-    cos/sin caches and kv_cache are device tensors.  The tokens go through in
-    chunks of chunk_tokens on three streams, so that the upload of chunk c+1,
-    the fused pre-pass of chunk c (one C-ABI launch) and the download of
-    chunk c-1 overlap.  Returns host tensors (q_fp4, q_scale, weights),
-    allocated pinned when not given; they are complete once the caller's
-    stream (which waits for the pipeline) has reached this point."""
+    """indexer_prepass for inputs and outputs in host memory, through the
+    C-ABI call fp4idx_indexer_prepass_host: k [T,128], q [T,H,128], w [T,H]
+    (bf16), positions and slot_mapping [T] (int64) are contiguous host
+    tensors, pinned for the copies to overlap; gamma, the cos/sin caches and
+    kv_cache are device tensors.  The library pipelines the tokens in chunks
+    of chunk_tokens (upload of chunk c+1, fused launch of chunk c, download of
+    chunk c-1) on its own streams.  Returns host tensors (q_fp4, q_scale,
+    weights), allocated pinned when not given; they are complete once the
+    caller's stream (which waits for the pipeline) has reached this point."""
     torch = _torch()
     _need_host(k, torch.bfloat16, "k", 2)
     _need_host(q, torch.bfloat16, "q", 3)
@@ -387,11 +381,20 @@ def indexer_prepass_host(k, gamma, slot_mapping, kv_cache, q, w, positions, cos_
     _need_host(positions, torch.int64, "positions", 1)
     _need_host(slot_mapping, torch.int64, "slot_mapping", 1)
     _need(kv_cache, torch.uint8, "kv_cache", 2)
+    _need(gamma, torch.bfloat16, "gamma", 1)
     T, H, D = q.shape
     if D != HEAD_DIM or tuple(k.shape) != (T, HEAD_DIM) or tuple(w.shape) != (T, H):
         raise ValueError("k must be [T,128], q [T,H,128], w [T,H]")
     if positions.shape[0] != T or slot_mapping.shape[0] != T:
         raise ValueError("positions and slot_mapping must have T entries")
+    if gamma.shape[0] != HEAD_DIM or not gamma.is_contiguous():
+        raise ValueError("gamma must be contiguous [128]")
+    if kv_cache.shape[1] != PAGE_BYTES or not kv_cache.is_contiguous():
+        raise ValueError("kv_cache must be contiguous [num_blocks, 4352]")
+    for t, name in ((cos_cache, "cos_cache"), (sin_cache, "sin_cache")):
+        _need(t, torch.float32, name, 2)
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
     if chunk_tokens < 1:
         raise ValueError("chunk_tokens must be >= 1")
     outs = []
@@ -405,64 +408,21 @@ def indexer_prepass_host(k, gamma, slot_mapping, kv_cache, q, w, positions, cos_
             raise ValueError(f"{name} must be {shape}")
         outs.append(t)
     q_fp4, q_scale, weights = outs
+    if T == 0:
+        return q_fp4, q_scale, weights
     dev = kv_cache.device
-    chunk = min(int(chunk_tokens), max(T, 1))
-    key = (dev.index, chunk, H)
-    with _HOST_PIPES_LOCK:
-        pipe = _HOST_PIPES.get(key)
-        if pipe is None:
-            pipe = _HOST_PIPES[key] = _HostPipe(dev, chunk, H)
+    chunk = min(int(chunk_tokens), T)
+    staging = _staging(dev, chunk, H)
+    ws = default_weight_scale(H) if weight_scale is None else float(weight_scale)
     caller = stream if stream is not None else torch.cuda.current_stream(dev)
-    with pipe.lock:
-        _host_pipeline(pipe, caller, chunk, T, k, gamma, slot_mapping, kv_cache, q, w,
-                       positions, cos_cache, sin_cache, eps, rope_style, weight_scale, q_fp4,
-                       q_scale, weights, err_flags)
-    return q_fp4, q_scale, weights
-
-
-def _host_pipeline(pipe, caller, chunk, T, k, gamma, slot_mapping, kv_cache, q, w, positions,
-                   cos_cache, sin_cache, eps, rope_style, weight_scale, q_fp4, q_scale, weights,
-                   err_flags):
-    torch = _torch()
-    # everything already queued on the caller's stream comes first, and so
-    # does an earlier call on this pipe: its kernels read the staging inputs
-    # (ev_run) and its downloads read the staging outputs (ev_out) that this
-    # call's first chunks overwrite (an event never recorded is no wait)
-    for s in (pipe.s_in, pipe.s_run, pipe.s_out):
-        s.wait_stream(caller)
-    for b in range(2):
-        pipe.s_in.wait_event(pipe.ev_run[b])
-        pipe.s_run.wait_event(pipe.ev_out[b])
-    for c in range((T + chunk - 1) // chunk):
-        b, t0 = c & 1, c * chunk
-        t1 = min(T, t0 + chunk)
-        n = t1 - t0
-        if c >= 2:  # slot b's inputs are free once chunk c-2 has run
-            pipe.s_in.wait_event(pipe.ev_run[b])
-        with torch.cuda.stream(pipe.s_in):
-            pipe.q[b][:n].copy_(q[t0:t1], non_blocking=True)
-            pipe.k[b][:n].copy_(k[t0:t1], non_blocking=True)
-            pipe.w[b][:n].copy_(w[t0:t1], non_blocking=True)
-            pipe.pos[b][:n].copy_(positions[t0:t1], non_blocking=True)
-            pipe.slots[b][:n].copy_(slot_mapping[t0:t1], non_blocking=True)
-            pipe.ev_in[b].record(pipe.s_in)
-        pipe.s_run.wait_event(pipe.ev_in[b])
-        if c >= 2:  # slot b's outputs are free once chunk c-2 is downloaded
-            pipe.s_run.wait_event(pipe.ev_out[b])
-        indexer_prepass(pipe.k[b][:n], gamma, pipe.slots[b][:n], kv_cache, pipe.q[b][:n],
-                        pipe.w[b][:n], pipe.pos[b][:n], cos_cache, sin_cache, eps=eps,
-                        rope_style=rope_style, weight_scale=weight_scale, q_fp4=pipe.qf[b][:n],
-                        q_scale=pipe.qs[b][:n], weights=pipe.wt[b][:n], err_flags=err_flags,
-                        stream=pipe.s_run)
-        pipe.ev_run[b].record(pipe.s_run)
-        pipe.s_out.wait_event(pipe.ev_run[b])
-        with torch.cuda.stream(pipe.s_out):
-            q_fp4[t0:t1].copy_(pipe.qf[b][:n], non_blocking=True)
-            q_scale[t0:t1].copy_(pipe.qs[b][:n], non_blocking=True)
-            weights[t0:t1].copy_(pipe.wt[b][:n], non_blocking=True)
-            pipe.ev_out[b].record(pipe.s_out)
-    caller.wait_stream(pipe.s_run)
-    caller.wait_stream(pipe.s_out)
+    with torch.cuda.device(dev):
+        st = _lib.fp4idx_indexer_prepass_host(
+            _ptr(k), _ptr(slot_mapping), _ptr(gamma), float(eps), _ptr(kv_cache),
+            kv_cache.shape[0], _ptr(q), _ptr(w), H, ws, _ptr(q_fp4), _ptr(q_scale),
+            _ptr(weights), _ptr(positions), _ptr(cos_cache), _ptr(sin_cache),
+            cos_cache.shape[0], rope_style_code(rope_style), T, chunk, _ptr(staging),
+            _ptr(err_flags), _stream_ptr(caller))
+    _check(st, "fp4idx_indexer_prepass_host")
     return q_fp4, q_scale, weights
 
 

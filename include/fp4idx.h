@@ -36,10 +36,13 @@
  *
  * Conventions for every call:
  *   - All data pointers are DEVICE pointers (cudaMalloc / torch CUDA memory)
- *     on the current device.  bf16 tensors are passed as const void*.
+ *     on the current device, except where fp4idx_indexer_prepass_host says
+ *     HOST.  bf16 tensors are passed as const void*.
  *   - The caller owns every buffer.  The library allocates nothing, keeps no
  *     per-call state, never synchronises, and enqueues one kernel on
- *     `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *     `stream` (a cudaStream_t; NULL = the legacy default stream);
+ *     fp4idx_indexer_prepass_host enqueues one per chunk, on streams of its
+ *     own that it orders after and before `stream`.
  *   - Host-side checks run before anything is enqueued; a failing check
  *     returns its status and enqueues nothing.  num_tokens == 0 returns
  *     FP4IDX_OK and enqueues nothing.
@@ -58,6 +61,7 @@
 #ifndef FP4IDX_H
 #define FP4IDX_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -260,6 +264,52 @@ fp4idx_status fp4idx_indexer_prepass_ex(
     const int64_t* positions, const float* cos_cache, const float* sin_cache,
     int64_t max_pos, int rope_style, int64_t num_tokens,
     const fp4idx_options* options, uint32_t* err_flags, void* stream);
+
+/*
+ * fp4idx_indexer_prepass for inputs and query outputs in HOST memory.  The
+ * operation is fp4idx_indexer_prepass (same source, same results, bytes
+ * identical); the pages give no host-memory form of it, so this call only
+ * adds the copies.  The tokens go through in chunks of chunk_tokens: the
+ * upload of chunk c+1, the fused launch of chunk c and the download of chunk
+ * c-1 overlap on three streams that the library creates once per device and
+ * keeps.  Every copy is one cudaMemcpyAsync.
+ *
+ *   k, q, w      HOST bf16, dense: k [num_tokens, 128], q [num_tokens,
+ *                num_heads, 128], w [num_tokens, num_heads].
+ *   slot_mapping, positions   HOST int64 [num_tokens].
+ *   q_fp4, q_scale, weights_out   HOST outputs, dense, as for
+ *                fp4idx_q_rope_pack_weights.
+ *                Host buffers should be page-locked (cudaHostAlloc or
+ *                cudaHostRegister) for the copies to overlap; pageable
+ *                memory works, without overlap.
+ *   gamma, kv_cache, cos_cache, sin_cache, err_flags   DEVICE, as for
+ *                fp4idx_indexer_prepass.
+ *   staging      DEVICE scratch of fp4idx_host_staging_bytes(chunk_tokens,
+ *                num_heads) bytes, 256-byte aligned, owned by the caller (the
+ *                library allocates nothing).  Its contents are not kept.
+ *   stream       the caller's stream: the pipeline starts after the work
+ *                already queued on it, and the work queued on it after this
+ *                call runs once every launch and download is done.  The host
+ *                outputs are complete, and the host inputs may be reused,
+ *                once the caller's stream has reached that point.
+ *
+ * Calls are serialised by a lock while they enqueue, and a call's first
+ * chunks wait until the previous call on the same device no longer reads or
+ * writes its staging buffer.  Checks: those of fp4idx_indexer_prepass (run before anything is
+ * enqueued), chunk_tokens >= 1 and num_heads * chunk_tokens below 2^30
+ * (FP4IDX_ERR_SHAPE), staging NULL (FP4IDX_ERR_NULL) or misaligned
+ * (FP4IDX_ERR_ALIGN).  FP4IDX_ERR_CUDA: a stream, event or copy call failed;
+ * what was enqueued before it stays enqueued.
+ */
+size_t fp4idx_host_staging_bytes(int64_t chunk_tokens, int64_t num_heads);
+
+fp4idx_status fp4idx_indexer_prepass_host(
+    const void* k, const int64_t* slot_mapping, const void* gamma, float eps,
+    uint8_t* kv_cache, int64_t num_blocks, const void* q, const void* w,
+    int64_t num_heads, float weight_scale, uint8_t* q_fp4, uint8_t* q_scale,
+    float* weights_out, const int64_t* positions, const float* cos_cache,
+    const float* sin_cache, int64_t max_pos, int rope_style, int64_t num_tokens,
+    int64_t chunk_tokens, void* staging, uint32_t* err_flags, void* stream);
 
 /*
  * Torch-shaped fake quantisation: RoPE, then every value replaced by its

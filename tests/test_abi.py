@@ -33,7 +33,8 @@ def test_exports_every_declared_symbol(F):
                           "fp4idx_indexer_prepass_ex", "fp4idx_rope_fake_quant",
                           "fp4idx_mqa_logits_prefill", "fp4idx_default_weight_scale",
                           "fp4idx_test_withhold_next", "fp4idx_status_string",
-                          "fp4idx_version"}
+                          "fp4idx_version", "fp4idx_indexer_prepass_host",
+                          "fp4idx_host_staging_bytes"}
     out = subprocess.run(["nm", "-D", "--defined-only", F.LIB_PATH], capture_output=True,
                          text=True, check=True).stdout
     exported = set(re.findall(r"\bT (fp4idx_\w+)", out))
@@ -344,6 +345,65 @@ def test_fake_quant_host_checks(F, over, code):
         a["mode"], a["out"], a["n"], a["err"], a["stream"]) == getattr(F, code)
 
 
+# fp4idx_indexer_prepass_host: k, q, w, slots, positions and the outputs are
+# host pointers, the rest device pointers; none is touched before a defect.
+def _h_args(**over):
+    a = dict(k=A[0], slots=A[5], gamma=A[1], eps=1e-6, cache=A[6], num_blocks=4, q=A[7],
+             w=A[8], H=32, ws=0.125, qf=A[9], qs=A[10], wt=A[11], pos=A[2], cos=A[3],
+             sin=A[4], max_pos=64, style=0, T=100, chunk=32, staging=A[12], err=None,
+             stream=None)
+    a.update(over)
+    return a
+
+
+def _call_h(F, a):
+    return F.lib().fp4idx_indexer_prepass_host(
+        a["k"], a["slots"], a["gamma"], a["eps"], a["cache"], a["num_blocks"], a["q"], a["w"],
+        a["H"], a["ws"], a["qf"], a["qs"], a["wt"], a["pos"], a["cos"], a["sin"], a["max_pos"],
+        a["style"], a["T"], a["chunk"], a["staging"], a["err"], a["stream"])
+
+
+H_DEFECTS = [
+    (dict(T=-1), "ERR_SHAPE"),
+    (dict(H=0), "ERR_SHAPE"),
+    (dict(chunk=0), "ERR_SHAPE"),
+    (dict(chunk=1 << 30), "ERR_SHAPE"),
+    (dict(H=1 << 20, chunk=1 << 10), "ERR_SHAPE"),
+    (dict(max_pos=0), "ERR_SHAPE"),
+    (dict(num_blocks=0), "ERR_SHAPE"),
+    *[(dict([(n, None)]), "ERR_NULL") for n in ("k", "slots", "gamma", "cache", "q", "w",
+                                                 "qf", "qs", "wt", "pos", "cos", "sin",
+                                                 "staging")],
+    (dict(staging=A[12] + 16), "ERR_ALIGN"),
+    (dict(gamma=A[1] + 2), "ERR_ALIGN"),
+    (dict(cos=A[3] + 4), "ERR_ALIGN"),
+    (dict(cache=A[6] + 4), "ERR_ALIGN"),
+    (dict(err=A[13] + 2), "ERR_ALIGN"),
+    (dict(eps=0.0), "ERR_ARG"),
+    (dict(style=3), "ERR_ARG"),
+    (dict(ws=float("nan")), "ERR_ARG"),
+]
+
+
+@pytest.mark.fake_ptr
+@pytest.mark.parametrize("over,code", H_DEFECTS, ids=_ids(H_DEFECTS))
+def test_host_pipeline_host_checks(F, over, code):
+    assert _call_h(F, _h_args(**over)) == getattr(F, code)
+
+
+def test_host_staging_bytes(F):
+    L = F.lib()
+    # two slots, each the chunk's inputs and query outputs in 256-byte
+    # aligned pieces: q 64*32*256, k 64*256, w 64*32*2, positions and slots
+    # 64*8 each, q_fp4 64*32*64, q_scale and weights 64*32*4 each
+    assert L.fp4idx_host_staging_bytes(64, 32) == 2 * (524288 + 16384 + 4096 + 512 + 512
+                                                      + 131072 + 8192 + 8192)
+    # a ragged size rounds every piece up to 256 bytes
+    assert L.fp4idx_host_staging_bytes(1, 1) == 2 * 8 * 256
+    for c, h in ((0, 32), (32, 0), (-1, 1), (1 << 30, 1), (1 << 15, 1 << 15)):
+        assert L.fp4idx_host_staging_bytes(c, h) == 0
+
+
 @pytest.mark.fake_ptr
 def test_zero_tokens_is_ok_without_touching_cuda(F):
     # All pointers NULL, T == 0: returns OK before any check or CUDA call.
@@ -352,6 +412,7 @@ def test_zero_tokens_is_ok_without_touching_cuda(F):
     assert _call_fused(F, _k_args(T=0), _q_args(T=0)) == F.OK
     assert _call_s(F, _s_args(batch=0, qf=None, cache=None)) == F.OK
     assert _call_s(F, _s_args(max_ctx=0, out=None)) == F.OK
+    assert _call_h(F, _h_args(T=0, k=None, q=None, staging=None)) == F.OK
 
 
 def test_binding_fails_loudly_without_the_library(tmp_path):
