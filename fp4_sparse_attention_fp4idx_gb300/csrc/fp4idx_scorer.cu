@@ -88,12 +88,12 @@ namespace {
 // Warp roles.  The warps on a tile's critical chains (issuer, stager,
 // producers) take the lowest warp ids: among ready warps the schedulers
 // favour the oldest, so the epilogue's bulk work does not delay them.
-constexpr int kIssuers = 3;                               // one per accumulator
-constexpr int kIssuerWarp = 0;                            // warps 0-2
-constexpr int kProducers = 1;
-constexpr int kProducerWarp = kIssuerWarp + kIssuers;     // warp 3
+constexpr int kIssuers = 2;                               // tile k: issuer k % 2
+constexpr int kIssuerWarp = 0;                            // warps 0-1
+constexpr int kProducers = 2;                             // stage j: producer j % 2
+constexpr int kProducerWarp = kIssuerWarp + kIssuers;     // warps 2-3
 constexpr int kEpiWarp = kProducerWarp + kProducers;      // warps 4-15
-constexpr int kEpiGroups = kIssuers;                      // one per accumulator
+constexpr int kEpiGroups = 3;                             // one per accumulator
 constexpr int kEpiWarps = 4 * kEpiGroups;
 constexpr int kWarps = kEpiWarp + kEpiWarps;              // 16: four per SM sub-partition
 constexpr int kThreads = kWarps * 32;                    // 512
@@ -113,6 +113,10 @@ constexpr int kSegTab = 512;                   // segment ranges kept in shared 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCols = 8;                // TMEM columns per scale-word slot
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+static_assert(kMaxStages % kProducers == 0, "stage slots are split evenly between the producers");
+static_assert(kQBufs == 4, "a header word holds the query buffer in two bits");
+static_assert(kMaxAccs * kMaxRows + (kMaxAccs + kIssuers * kQBufs) * kSfCols <= kTmemCols,
+              "accumulators and scale words fit the TMEM columns");
 
 // Offsets inside a stage: tiles h = 0 .. kTps-1 share one stage, one full
 // and one empty barrier.
@@ -126,7 +130,8 @@ constexpr uint32_t kStageBytes = (kPsHdr + 4 * kTps + 1023) / 1024 * 1024;  // a
 // query buffer (bits 0-1), its fill parity (bit 2), the issuer's first
 // (bit 3) and last (bit 4) tile of the segment here, the segment's first
 // tile here (bit 5), the number of issuers with tiles in the segment here
-// (bits 6-7), the segment's query rows (bits 8-15).
+// (bits 6-7), the segment's query rows (bits 8-15), the segment's ordinal in
+// this CTA modulo 2^16 (bits 16-31; the buffer is its low two bits).
 constexpr uint32_t kHdrFirst = 1u << 3, kHdrLast = 1u << 4, kHdrSegFirst = 1u << 5;
 
 enum { kModeDecode = 0, kModePrefill = 1 };
@@ -162,9 +167,9 @@ struct Layout {
   uint32_t q, qs, w, tab, bars, misc, total;
 };
 
-// mbarriers: full and empty per stage; full and empty per accumulator;
-// empty and full per query buffer.
-__host__ __device__ constexpr int kBarriers(int P) { return 2 * P + 2 * kMaxAccs + 2 * kQBufs; }
+// mbarriers: full and empty per stage; full per accumulator and two empty
+// ones (for its even and its odd uses); empty and full per query buffer.
+__host__ __device__ constexpr int kBarriers(int P) { return 2 * P + 3 * kMaxAccs + 2 * kQBufs; }
 
 __host__ __device__ inline Layout make_layout(int P, int R) {
   Layout L;
@@ -211,6 +216,23 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
   for (;;) {
     for (int k = 0; k < 8; ++k)
       if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      *abort = 1u;
+      return false;
+    }
+  }
+}
+
+// Waits until *w == v (a word another warp of the CTA writes); gives up like
+// wait_phase.
+__device__ __forceinline__ bool wait_word(volatile uint32_t* w, uint32_t v,
+                                          volatile uint32_t* abort) {
+  if (*w == v) return true;
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    __nanosleep(64);
+    if (*w == v) return true;
     if (*abort) return false;
     if (global_ns() - t0 > kWaitLimitNs) {
       *abort = 1u;
@@ -550,7 +572,7 @@ __device__ __forceinline__ void warp_scan2(long long& a, long long& b, int lane)
 
 // ---------------------------------------------------------------- the kernel
 // CPJ: accumulator chunks of 32 columns per query token, H / 32.
-template <int CPJ>
+template <int CPJ, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     scorer_kernel(const __grid_constant__ ScorerParams p, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap qmap) {
@@ -568,15 +590,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bars = smem_addr(smem + L.bars);
   uint32_t* const misc = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile uint32_t* const abort = misc + 1;
+  volatile uint32_t* const qseq = misc + 24;  // per query buffer: loads made (mod 2^14)
   int32_t* const start = reinterpret_cast<int32_t*>(misc + 2);  // g0, toff, n, pg0, poff, pn
   auto stage = [&](int s) { return smem + (uint32_t)s * kStageBytes; };
   auto bar_full = [&](int s) { return bars + 8u * (uint32_t)s; };
   auto bar_empty = [&](int s) { return bars + 8u * (uint32_t)(S + s); };
   auto bar_accf = [&](int a) { return bars + 8u * (uint32_t)(2 * S + a); };
-  auto bar_acce = [&](int a) { return bars + 8u * (uint32_t)(2 * S + kMaxAccs + a); };
-  auto bar_qempty = [&](int b) { return bars + 8u * (uint32_t)(2 * S + 2 * kMaxAccs + b); };
+  // Accumulator a's readout of its use v arrives on bar_acce(a, v & 1): the
+  // two issuers take turns on an accumulator, and one barrier per use parity
+  // keeps every wait on it within one phase of the barrier's state.
+  auto bar_acce = [&](int a, int par) {
+    return bars + 8u * (uint32_t)(2 * S + kMaxAccs + 2 * a + par);
+  };
+  auto bar_qempty = [&](int b) { return bars + 8u * (uint32_t)(2 * S + 3 * kMaxAccs + b); };
   auto bar_qfull = [&](int b) {
-    return bars + 8u * (uint32_t)(2 * S + 2 * kMaxAccs + kQBufs + b);
+    return bars + 8u * (uint32_t)(2 * S + 3 * kMaxAccs + kQBufs + b);
   };
 
   // ---- this CTA's shares of the work tiles and of the -inf tiles ----------
@@ -598,7 +626,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       *abort = 0u;
       start[2] = 0;
       start[5] = 0;
-      misc[8] = misc[9] = misc[10] = 0u;
+      misc[8] = misc[9] = 0u;
+      for (int b = 0; b < kQBufs; ++b) misc[24 + b] = 0u;
     }
     if (lane == 31) {
       scanw[warp] = wi;
@@ -674,8 +703,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // warp of its epilogue group, a query buffer's empty one per issuer
         const int j = i - 2 * S;
         const int cnt = i >= S && i < 2 * S                             ? kTps
-                        : j >= kMaxAccs && j < 2 * kMaxAccs                ? 4
-                        : j >= 2 * kMaxAccs && j < 2 * kMaxAccs + kQBufs ? kIssuers
+                        : j >= kMaxAccs && j < 3 * kMaxAccs                ? 4
+                        : j >= 3 * kMaxAccs && j < 3 * kMaxAccs + kQBufs ? kIssuers
                                                                          : 1;
         asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bars + 8u * i), "r"(cnt)
                      : "memory");
@@ -701,48 +730,63 @@ __global__ void __launch_bounds__(kThreads, 1)
   int last_issued = -1;  // producer: the last stage use whose copies were issued
   int q_issued[4] = {-1, -1, -1, -1};  // producers: parity of the last query copy per buffer
 
-  if (n > 0 && warp == kProducerWarp) {
-    // ---- producer: a stage of kTps tiles per step ------------------------------
-    // Per batch of 16 tiles, a batch ahead, lane L describes half L % 2 of
-    // tile m0 + L / 2: the page id (and whether the page is read), the tile's
-    // header word and the first query row of its segment.
+  if (n > 0 && warp >= kProducerWarp && warp < kProducerWarp + kProducers) {
+    // ---- producers: stage j (tiles kTps*j ..) belongs to producer j % 2 ------
+    // Per batch of the producer's next four stages, a batch ahead, lane L
+    // describes half L % 2 of the batch's tile L / 2: the page to read (or
+    // none), the tile's header word and the first query row of its segment.
+    // Lane 0 then issues every copy of a stage itself: one warp's copies are
+    // accepted at a bounded rate, and a loop in one lane beats lanes that
+    // each issue one.
+    const int pr = warp - kProducerWarp;
     Walk lw;  // this lane's walker, at its tile of the batch being described
     lw.init(p, st, start[0], start[1]);
     int lk = 0;  // lw's tile index
     struct Desc {
-      int32_t id, in;
+      int32_t page;  // page to read; -1: none (past the context, or a bad entry)
       uint32_t hdr;
       int32_t qrow;
     };
-    auto describe = [&](int m0) -> Desc {
-      const int m = m0 + (lane >> 1);
-      Desc dsc = {-1, 0, 0u, 0};
+    // first stage of the producer's batch b; tile of slot s (0..15) in it
+    auto batch_stage = [&](int b) { return pr + kProducers * 4 * b; };
+    auto describe = [&](int b) -> Desc {
+      const int sl = lane >> 1;
+      const int m = kTps * (batch_stage(b) + kProducers * (sl / kTps)) + sl % kTps;
+      Desc dsc = {-1, 0u, 0};
       if (m < n) {
         for (; lk < m; ++lk) lw.advance(p, st);
         const int pidx = lw.t * 2 + (lane & 1);
         if (pidx * kKvBlock < lw.lim) {
-          dsc.in = 1;
-          dsc.id = p.mode == kModeDecode
-                       ? __ldg(p.block_table + (int64_t)lw.q.b * p.bt_stride + pidx)
-                       : pidx;
+          const int32_t id = MODE == kModeDecode
+                                 ? __ldg(p.block_table + (int64_t)lw.q.b * p.bt_stride + pidx)
+                                 : pidx;
+          if (id >= 0 && id < p.num_blocks)
+            dsc.page = id;
+          else
+            flag_error(p.err, FP4IDX_ERRFLAG_PAGE);  // not read: those keys score -inf
         }
         const int left = min(lw.hi - 1 - lw.t, n - 1 - m);  // the segment's tiles here after m
         const int owners = min(kIssuers, left + 1);           // at its first tile here
         dsc.hdr = (uint32_t)(lw.qi % QB) | ((((uint32_t)(lw.qi / QB)) & 1u) << 2) |
                   (lw.pos < kIssuers ? kHdrFirst : 0u) | (left < kIssuers ? kHdrLast : 0u) |
                   (lw.first ? kHdrSegFirst : 0u) | ((uint32_t)owners << 6) |
-                  ((uint32_t)(lw.q.ntok * p.H) << 8);
+                  ((uint32_t)(lw.q.ntok * p.H) << 8) | ((uint32_t)(lw.qi & 0xFFFF) << 16);
         dsc.qrow = lw.q.qt0 * p.H;
       }
       return dsc;
     };
     const uint32_t q_bytes = (uint32_t)R * 64u;
     // A segment's first tile here: its query operand and scale words, on the
-    // query buffer's own barrier, in segment order; then the releases of the
-    // buffer that issuers without a tile in the segment will not make.
+    // query buffer's own barrier; then the releases of the buffer that
+    // issuers without a tile in the segment will not make.  The loads into a
+    // buffer go in segment order, whichever producer makes them: a load
+    // first waits until the buffer's previous segment has been loaded, so the
+    // release it then waits for is the barrier's current phase, never one
+    // two phases back (which the parity alone cannot tell apart).
     auto load_q = [&](uint32_t hdr, int32_t qrow) -> bool {
       const int qb = (int)(hdr & 3u);
-      const uint32_t qpar = (hdr >> 2) & 1u;
+      const uint32_t qpar = (hdr >> 2) & 1u, use = (hdr >> 18) & 0x3FFFu;
+      if (!wait_word(qseq + qb, use, abort)) return false;
       if (!wait_phase(bar_qempty(qb), qpar ^ 1u, abort)) return false;
       const uint32_t qf = bar_qfull(qb);
       const uint32_t sw_bytes = ((hdr >> 8) & 0xFFu) * 4u;
@@ -751,57 +795,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       bulk_copy(smem_addr(sQs + qb * 128), p.q_scale + (int64_t)qrow * 4, sw_bytes, qf);
       q_issued[qb] = (int)qpar;
       for (int o = (int)((hdr >> 6) & 3u); o < kIssuers; ++o) mbar_arrive(bar_qempty(qb));
+      qseq[qb] = (use + 1u) & 0x3FFFu;
       return true;
     };
-    // Lanes 4h .. 4h + 3 copy tile h of a stage: lanes 4h and 4h + 1 the
-    // two page payloads (TMA, 64-byte swizzled, the layout the MMA reads),
-    // lanes 4h + 2 and 4h + 3 the pages' exponent words (bulk copies).
-    const int th = lane >> 2, pg = lane & 1;
-    const bool exps = (lane & 2) != 0;
-    Desc cur = describe(0), nxt = {-1, 0, 0u, 0};
-    int ps = 0;
-    uint32_t ph = 0;
+    Desc cur = describe(0), nxt = {-1, 0u, 0};
     bool stop = false;
-    for (int m0 = 0; m0 < n && !stop; m0 += 16) {
-      if (m0 + 16 < n) nxt = describe(m0 + 16);
-      for (int i = 0; i < 16 && m0 + i < n; i += kTps) {
-        const int k = m0 + i;
+    for (int b = 0; !stop && kTps * batch_stage(b) < n; ++b) {
+      if (kTps * batch_stage(b + 1) < n) nxt = describe(b + 1);
+      for (int i = 0; i < 4; ++i) {
+        const int j = batch_stage(b) + kProducers * i, k = kTps * j;
+        if (k >= n) break;
         const int nt = min(kTps, n - k);  // tiles in this stage
-        // lanes 4h .. 4h + 3 copy tile h: its two payloads, then its two
-        // exponent-word arrays
-        const bool active = th < nt;
-        const int src = 2 * (i + th) + pg;
-        const int32_t my_page = __shfl_sync(0xffffffffu, cur.id, src);
-        int my_in = __shfl_sync(0xffffffffu, cur.in, src);
+        const int ps = j % S;
+        const uint32_t ph = (uint32_t)(j / S) & 1u;
+        int32_t page[kTps][2];
         uint32_t hdr[kTps];
         int32_t qrow[kTps];
 #pragma unroll
         for (int t = 0; t < kTps; ++t) {
-          hdr[t] = __shfl_sync(0xffffffffu, cur.hdr, 2 * (i + t));
-          qrow[t] = __shfl_sync(0xffffffffu, cur.qrow, 2 * (i + t));
+          page[t][0] = __shfl_sync(0xffffffffu, cur.page, 2 * (kTps * i + t));
+          page[t][1] = __shfl_sync(0xffffffffu, cur.page, 2 * (kTps * i + t) + 1);
+          hdr[t] = __shfl_sync(0xffffffffu, cur.hdr, 2 * (kTps * i + t));
+          qrow[t] = __shfl_sync(0xffffffffu, cur.qrow, 2 * (kTps * i + t));
         }
-        if (my_in && (my_page < 0 || my_page >= p.num_blocks)) {  // not read
-          if (active && !exps) flag_error(p.err, FP4IDX_ERRFLAG_PAGE);
-          my_in = 0;
-        }
-        // pages read: lanes 4h and 4h + 1 of each tile h
-        const uint32_t rd = __ballot_sync(0xffffffffu, active && !exps && my_in);
-        // every lane that writes the stage observes its release itself
-        int ok = __all_sync(0xffffffffu, !active || wait_phase(bar_empty(ps), ph ^ 1u, abort));
-        uint8_t* const sp = stage(ps);
-        // testing hook (see fp4idx_test_withhold_next): this stage's copies and
-        // its arrival are withheld, so the waits for it run out
-        const bool withheld = blockIdx.x == 0 && p.withhold >= k && p.withhold < k + nt;
-        if (ok && lane == 0 && !withheld) {
-#pragma unroll
-          for (int t = 0; t < kTps; ++t)
-            if (ok && t < nt && (hdr[t] & kHdrSegFirst)) ok = load_q(hdr[t], qrow[t]);
-          if (ok) {
+        int ok = 1;
+        if (lane == 0) {
+          ok = wait_phase(bar_empty(ps), ph ^ 1u, abort);
+          // testing hook (see fp4idx_test_withhold_next): this stage's copies
+          // and its arrival are withheld, so the waits for it run out
+          const bool withheld = blockIdx.x == 0 && p.withhold >= k && p.withhold < k + nt;
+          if (ok && !withheld) {
 #pragma unroll
             for (int t = 0; t < kTps; ++t)
+              if (ok && t < nt && (hdr[t] & kHdrSegFirst)) ok = load_q(hdr[t], qrow[t]);
+          }
+          if (ok && !withheld) {
+            uint8_t* const sp = stage(ps);
+            uint32_t reads = 0;
+#pragma unroll
+            for (int t = 0; t < kTps; ++t) {
               reinterpret_cast<uint32_t*>(sp + kPsHdr)[t] = hdr[t];
-            mbar_expect_tx(bar_full(ps), (uint32_t)__popc(rd & 0x33333333u) * (kPayloadBytes + kExpBytes));
-            last_issued = k / kTps;
+              reads += (t < nt && page[t][0] >= 0) + (t < nt && page[t][1] >= 0);
+            }
+            const uint32_t fb = bar_full(ps);
+            mbar_expect_tx(fb, reads * (kPayloadBytes + kExpBytes));
+#pragma unroll
+            for (int t = 0; t < kTps; ++t)
+#pragma unroll
+              for (int pg = 0; pg < 2; ++pg)
+                if (t < nt && page[t][pg] >= 0) {
+                  const int32_t id = page[t][pg];
+                  tma_3d(smem_addr(sp + t * kTilePayload + pg * kPayloadBytes), &kmap, 0, 0, id, fb);
+                  bulk_copy(smem_addr(sp + kPsExp + t * 512 + pg * kExpBytes),
+                            p.cache + (int64_t)id * kPageBytes + kPayloadBytes, kExpBytes, fb);
+                }
+            last_issued = j;
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -809,30 +857,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           stop = true;
           break;
         }
-        if (active && my_in && !withheld) {
-          const uint32_t fb = bar_full(ps);
-          if (!exps)
-            tma_3d(smem_addr(sp + th * kTilePayload + pg * kPayloadBytes), &kmap, 0, 0, my_page, fb);
-          else
-            bulk_copy(smem_addr(sp + kPsExp + th * 512 + pg * kExpBytes),
-                      p.cache + (int64_t)my_page * kPageBytes + kPayloadBytes, kExpBytes, fb);
-        }
-        if (++ps == S) {
-          ps = 0;
-          ph ^= 1u;
-        }
       }
       cur = nxt;
     }
   } else if (n > 0 && warp >= kIssuerWarp && warp < kIssuerWarp + kIssuers) {
-    // ---- issuers: tile k belongs to issuer k % 3, which owns accumulator k % 3 --
+    // ---- issuers: tile k belongs to issuer k % 2 and accumulator k % 3 -------
     const int m = warp - kIssuerWarp;
     const uint32_t id0 = mxf4_idesc(R, 0), id1 = mxf4_idesc(R, 2);
     const uint32_t q_bytes = (uint32_t)R * 64u;
-    const uint32_t d = tmem + (uint32_t)m * (uint32_t)R;
-    const uint32_t sfa = tmem + sfa_col0 + kSfCols * (uint32_t)m;
-    int issued = 0;
+    int issued = 0;  // tiles issued by this issuer
     for (int k = m; k < n; k += kIssuers) {
+      const int a = k % kMaxAccs, use = k / kMaxAccs;  // accumulator and its use
+      const uint32_t d = tmem + (uint32_t)a * (uint32_t)R;
+      const uint32_t sfa = tmem + sfa_col0 + kSfCols * (uint32_t)a;
       const int j = k / kTps, h = k % kTps, ps = j % S;
       const uint32_t ph = (uint32_t)(j / S) & 1u;
       // Lane 0 waits; then every lane, which reads the landed words, observes
@@ -866,8 +903,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) {
-        // accumulator m has been read out (this issuer's previous tile)
-        ok = issued == 0 || wait_phase(bar_acce(m), ((uint32_t)issued & 1u) ^ 1u, abort);
+        // accumulator a has been read out (its previous use, tile k - 3, which
+        // the other issuer made).  That barrier cannot be two phases behind:
+        // this issuer made tile k - 6 only after the readout of tile k - 9.
+        ok = use == 0 || wait_phase(bar_acce(a, (use - 1) & 1), (uint32_t)((use - 1) >> 1) & 1u,
+                                    abort);
         if (ok) {
           asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
           const uint32_t sfb = tmem + sfb_col0 + kSfCols * (uint32_t)(m * QB + qb);
@@ -882,7 +922,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // accumulator is full, this tile's share of the stage can be
           // refilled, and after this issuer's last tile of the segment, its
           // share of the query buffer is released.
-          mma_commit(bar_accf(m));
+          mma_commit(bar_accf(a));
           mma_commit(bar_empty(ps));
           if (hdr & kHdrLast) mma_commit(bar_qempty(qb));
         }
@@ -891,7 +931,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       ++issued;
     }
-    if (lane == 0) misc[8 + m] = (uint32_t)issued;  // for the drain after an abort
+    // for the drain after an abort: 1 + this issuer's last tile issued
+    if (lane == 0) misc[8 + m] = issued > 0 ? (uint32_t)(m + kIssuers * (issued - 1) + 1) : 0u;
   } else if (n > 0 && warp >= kEpiWarp) {
     // ---- epilogue ---------------------------------------------------------------
     // Group j (warps 4+4j .. 7+4j) reads accumulator j, i.e. tiles k = j
@@ -919,6 +960,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fill.init(p, st, start[3], start[4], f_hi);
     fill.run(p, st, f_lo, lane, false);  // step over the earlier warps' shares
     int j_own = 0;
+    int facc = 0;  // -inf tiles spread evenly over the group's tiles, without a division
     for (int k = grp; k < n; k += kEpiGroups) {
       for (; wk < k; ++wk) w.advance(p, st);
       const int ntok = w.q.ntok;
@@ -929,7 +971,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int r = 32 * c + lane;
           wr[c] = r < ntok * p.H ? __ldg(p.weights + (int64_t)w.q.qt0 * p.H + r) : 0.0f;
         }
-        if (p.mode == kModePrefill) {
+        if (MODE == kModePrefill) {
 #pragma unroll
           for (int t = 0; t < kMaxTps; ++t) {
             const bool in = t < ntok;
@@ -946,7 +988,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // decode: this warp's page of the tile (-1 past the context), loaded
       // before the wait so that its latency is hidden behind it
       int32_t pid = 0;
-      if (p.mode == kModeDecode) {
+      if (MODE == kModeDecode) {
         const int pidx = w.t * 2 + (quad >> 1);
         pid = pidx * kKvBlock < w.lim
                   ? __ldg(p.block_table + (int64_t)w.q.b * p.bt_stride + pidx)
@@ -978,7 +1020,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (c + 2 >= nv) {  // every load of the tile done: release the accumulator
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_acce(grp));
+            if (lane == 0) mbar_arrive(bar_acce(grp, j_own & 1));
           }
           const float pa_ = weighted_relu_sum(xa, wts + 32 * c);
           if (c % CPJ == 0)
@@ -999,14 +1041,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int t = 0; t < kMaxTps; ++t) {
         if (t < ntok && s_tok < p.ncols) {
-          const bool valid = p.mode == kModeDecode ? (s_tok < w.lim && pok)
+          const bool valid = MODE == kModeDecode ? (s_tok < w.lim && pok)
                                                    : (s_tok >= ac[t] && s_tok < bc[t]);
           __stcs(p.logits + (int64_t)(w.q.qt0 + t) * p.logits_stride + s_tok,
                  valid ? v[t] : -INFINITY);
         }
       }
-      const long long f0 = (long long)pn * j_own / n_grp, f1 = (long long)pn * (j_own + 1) / n_grp;
-      fill.run(p, st, (int)(f1 - f0), lane);
+      int items = 0;
+      for (facc += pn; facc >= n_grp; facc -= n_grp) ++items;
+      fill.run(p, st, items, lane);
       ++j_own;
     }
     fill.run(p, st, pn, lane);  // any left (a group without tiles, an aborted loop)
@@ -1028,11 +1071,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (q_issued[b] >= 0) wait_phase_drain(bar_qfull(b), (uint32_t)q_issued[b]);
       }
       // MMAs in flight land before TMEM is released: an issuer's last
-      // commit tracks all its earlier MMAs, and its accumulator cannot be two
-      // phases behind it (its previous tile was read out before it was issued).
+      // commit tracks all its earlier MMAs, and that accumulator cannot be
+      // two phases behind it (its previous use was read out before the tile
+      // was issued).
       if (warp >= kIssuerWarp && warp < kIssuerWarp + kIssuers && lane == 0) {
-        const int m = warp - kIssuerWarp, cnt = (int)misc[8 + m];
-        if (cnt > 0) wait_phase_drain(bar_accf(m), (uint32_t)(cnt - 1) & 1u);
+        const int last = (int)misc[8 + (warp - kIssuerWarp)] - 1;
+        if (last >= 0)
+          wait_phase_drain(bar_accf(last % kMaxAccs), (uint32_t)(last / kMaxAccs) & 1u);
       }
       if (tid == 0) flag_error(p.err, FP4IDX_ERRFLAG_TIMEOUT);
       __syncthreads();
@@ -1052,6 +1097,23 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+typedef void (*ScorerKernel)(ScorerParams, CUtensorMap, CUtensorMap);
+// [mode][H / 32 - 1]
+constexpr ScorerKernel kKernels[2][4] = {
+    {scorer_kernel<1, kModeDecode>, scorer_kernel<2, kModeDecode>, scorer_kernel<3, kModeDecode>,
+     scorer_kernel<4, kModeDecode>},
+    {scorer_kernel<1, kModePrefill>, scorer_kernel<2, kModePrefill>,
+     scorer_kernel<3, kModePrefill>, scorer_kernel<4, kModePrefill>}};
+
+bool set_smem_limits(int bytes) {
+  for (const auto& row : kKernels)
+    for (ScorerKernel k : row)
+      if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+          cudaSuccess)
+        return false;
+  return true;
+}
 
 struct DeviceInfo {
   bool ready = false;
@@ -1085,14 +1147,7 @@ fp4idx_status device_setup(DeviceInfo& out, EncodeTiledFn& enc) {
     if (cudaDeviceGetAttribute(&t.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&t.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
             cudaSuccess ||
-        cudaFuncSetAttribute(scorer_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             t.smem_optin) != cudaSuccess ||
-        cudaFuncSetAttribute(scorer_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             t.smem_optin) != cudaSuccess ||
-        cudaFuncSetAttribute(scorer_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             t.smem_optin) != cudaSuccess ||
-        cudaFuncSetAttribute(scorer_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             t.smem_optin) != cudaSuccess)
+        !set_smem_limits(t.smem_optin))
       return FP4IDX_ERR_CUDA;
     t.ready = true;
     di = t;
@@ -1118,8 +1173,10 @@ fp4idx_status launch(ScorerParams& p, const uint8_t* q_fp4, const uint8_t* kv_ca
   const fp4idx_status ds = device_setup(di, encode);
   if (ds != FP4IDX_OK) return ds;
   const int R = p.R;  // <= 128: 3 accumulators + scale words fit 512 TMEM columns
+  // a multiple of the producer count: producer j % kProducers owns the
+  // stage slots j % S, so no slot is shared between producers
   int S = kMaxStages;
-  while (S > 1 && (int)make_layout(S, R).total + 1024 > di.smem_optin) --S;
+  while (S > kProducers && (int)make_layout(S, R).total + 1024 > di.smem_optin) S -= kProducers;
   if ((int)make_layout(S, R).total + 1024 > di.smem_optin) return FP4IDX_ERR_SHAPE;
   p.stages = S;
   const int smem_bytes = (int)make_layout(S, R).total + 1024;
@@ -1156,11 +1213,7 @@ fp4idx_status launch(ScorerParams& p, const uint8_t* q_fp4, const uint8_t* kv_ca
         CUDA_SUCCESS)
       return FP4IDX_ERR_CUDA;
   }
-  const int cpj = p.H / 32;
-  auto kern = cpj == 1 ? scorer_kernel<1>
-              : cpj == 2 ? scorer_kernel<2>
-              : cpj == 3 ? scorer_kernel<3>
-                         : scorer_kernel<4>;
+  const auto kern = kKernels[p.mode == kModePrefill ? 1 : 0][p.H / 32 - 1];
   // cudaLaunchKernelEx reports this launch's own status, without reading or
   // clearing an error that the caller's own work left in the runtime
   cudaLaunchConfig_t cfg = {};
