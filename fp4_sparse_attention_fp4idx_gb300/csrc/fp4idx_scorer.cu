@@ -114,6 +114,8 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCols = 8;                // TMEM columns per scale-word slot
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 static_assert(kMaxStages % kProducers == 0, "stage slots are split evenly between the producers");
+static_assert(kIssuers == 2 && kMaxAccs == 3 && kTps % kIssuers == 0,
+              "two issuers take turns over a stage's tiles and the three accumulators");
 static_assert(kQBufs == 4, "a header word holds the query buffer in two bits");
 static_assert(kMaxAccs * kMaxRows + (kMaxAccs + kIssuers * kQBufs) * kSfCols <= kTmemCols,
               "accumulators and scale words fit the TMEM columns");
@@ -699,10 +701,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (n > 0) {
     if (tid == 0) {
       for (int i = 0; i < kBarriers(S); ++i) {
-        // a stage's empty takes one arrival per tile, acc_empty one per
+        // a stage's empty takes one arrival per issuer, acc_empty one per
         // warp of its epilogue group, a query buffer's empty one per issuer
         const int j = i - 2 * S;
-        const int cnt = i >= S && i < 2 * S                             ? kTps
+        const int cnt = i >= S && i < 2 * S                             ? kIssuers
                         : j >= kMaxAccs && j < 3 * kMaxAccs                ? 4
                         : j >= 3 * kMaxAccs && j < 3 * kMaxAccs + kQBufs ? kIssuers
                                                                          : 1;
@@ -866,18 +868,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t id0 = mxf4_idesc(R, 0), id1 = mxf4_idesc(R, 2);
     const uint32_t q_bytes = (uint32_t)R * 64u;
     int issued = 0;  // tiles issued by this issuer
+    // tile k's accumulator a = k % 3 and its use k / 3; its stage j = k / kTps
+    // (slot ps = j % S, parity ph) and place h = k % kTps there, all stepped
+    // along with k
+    int a = m % kMaxAccs, use = m / kMaxAccs, h = m % kTps, ps = (m / kTps) % S;
+    uint32_t ph = (uint32_t)((m / kTps) / S) & 1u;
     for (int k = m; k < n; k += kIssuers) {
-      const int a = k % kMaxAccs, use = k / kMaxAccs;  // accumulator and its use
       const uint32_t d = tmem + (uint32_t)a * (uint32_t)R;
       const uint32_t sfa = tmem + sfa_col0 + kSfCols * (uint32_t)a;
-      const int j = k / kTps, h = k % kTps, ps = j % S;
-      const uint32_t ph = (uint32_t)(j / S) & 1u;
-      // Lane 0 waits; then every lane, which reads the landed words, observes
-      // the completed phase itself (acquire): a wait by one lane alone does
-      // not order the other lanes' reads after the copy.
-      int ok = __shfl_sync(0xffffffffu, lane == 0 ? (int)wait_phase(bar_full(ps), ph, abort) : 0, 0);
+      // Every lane, which reads the landed words, observes the completed
+      // phase itself (acquire).
+      int ok = __all_sync(0xffffffffu, wait_phase(bar_full(ps), ph, abort));
       if (!ok) break;
-      (void)wait_phase(bar_full(ps), ph, abort);  // complete: returns at once
       uint8_t* const sp = stage(ps);
       const uint32_t hdr = *reinterpret_cast<const uint32_t*>(sp + kPsHdr + 4 * h);
       const int qb = (int)(hdr & 3u);
@@ -923,13 +925,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           // refilled, and after this issuer's last tile of the segment, its
           // share of the query buffer is released.
           mma_commit(bar_accf(a));
-          mma_commit(bar_empty(ps));
+          // the stage is free once both issuers' tiles there are done: each
+          // releases it after its last one (the stage's empty barrier takes
+          // kIssuers arrivals; a partial last stage is never refilled)
+          if (h >= kTps - kIssuers) mma_commit(bar_empty(ps));
           if (hdr & kHdrLast) mma_commit(bar_qempty(qb));
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       ++issued;
+      a += kIssuers;
+      if (a >= kMaxAccs) {
+        a -= kMaxAccs;
+        ++use;
+      }
+      h += kIssuers;
+      if (h >= kTps) {
+        h -= kTps;
+        if (++ps == S) {
+          ps = 0;
+          ph ^= 1u;
+        }
+      }
     }
     // for the drain after an abort: 1 + this issuer's last tile issued
     if (lane == 0) misc[8 + m] = issued > 0 ? (uint32_t)(m + kIssuers * (issued - 1) + 1) : 0u;
