@@ -36,38 +36,42 @@
 // The tile rate of a one-CTA-per-SM pipeline is set by the longest serial
 // chain of dependent instructions that one warp runs per tile, not by the
 // copy latency: an mbarrier operation costs one thread on the order of a
-// hundred cycles and a copy issue about fifty.  So four consecutive tiles
-// share one stage and one full / empty barrier pair, and issuer m,
-// accumulator m and epilogue group m form a private pipeline for the tiles
-// k = m (mod 3).
-//   warp 3       producer, a stage of four tiles per step.  Every 16 tiles,
-//                a batch ahead, its lanes describe the batch's tiles in
-//                parallel (page ids, a header word per tile, the segment's
-//                first query row).  Per stage, lanes 4h .. 4h + 3 wait for it,
-//                then issue the TMA tensor copies of tile h's two page
-//                payloads (64-byte swizzled, the layout the MMA reads) and the
-//                bulk copies of their exponent words; lane 0 first writes the
-//                four header words and, at a segment's first tile, loads the segment's
-//                query operand and scale words into a query buffer (in
-//                segment order) and makes the buffer releases of the issuers
-//                that have no tile in the segment.
-//   warps 0-2    issuers: tile k belongs to issuer m = k % 3.  Once the stage
-//                has landed, the warp transposes the tile's 128 exponent
-//                words (and at its first tile of a segment the queries'
-//                words) into the 32 x 128-bit blocks tcgen05.cp reads; lane
-//                0 then issues tcgen05.cp into TMEM, the two MMAs into
-//                accumulator m and commits that mark the accumulator full,
-//                the tile's share of the stage free and, after the issuer's
-//                last tile of a segment, its share of the segment's query
-//                buffer free (a buffer is free once three releases came).
+// hundred cycles, and one warp's copies are accepted at about one 8.7 KB
+// tile per thousand cycles whatever their number or kind.  So four
+// consecutive tiles share one stage and one full / empty barrier pair, the
+// stages alternate between two producer warps, the tiles between two issuer
+// warps, and accumulator m and epilogue group m form a pipeline for the
+// tiles k = m (mod 3).
+//   warps 2-3    producers: stage j belongs to producer j % 2.  For its next
+//                four stages, a batch ahead, a producer's lanes describe the
+//                batch's 16 tiles in parallel (page ids, a header word per
+//                tile, the segment's first query row).  Per stage, lane 0
+//                waits for it, writes the four header words, at a segment's
+//                first tile loads the segment's query operand and scale
+//                words into a query buffer (the loads into one buffer in
+//                segment order, whichever producer makes them) and makes the
+//                buffer releases of the issuers that have no tile in the
+//                segment, then issues the TMA tensor copies of the page
+//                payloads (64-byte swizzled, the layout the MMA reads) and
+//                the bulk copies of their exponent words.  Between stages the
+//                warp writes its share of the -inf columns outside every
+//                segment's range.
+//   warps 0-1    issuers: tile k belongs to issuer k % 2 and accumulator
+//                k % 3.  Once the stage has landed, the warp transposes the
+//                tile's 128 exponent words (and at its first tile of a
+//                segment the queries' words) into the 32 x 128-bit blocks
+//                tcgen05.cp reads; lane 0 then issues tcgen05.cp into TMEM,
+//                the two MMAs into the accumulator and commits that mark the
+//                accumulator full, after its last tile of a stage its share
+//                of the stage free and, after its last tile of a segment, its
+//                share of the segment's query buffer free (a buffer is free
+//                once two releases came).
 //   warps 4-15   epilogue: group m = (w - 4) / 4 reads accumulator m; one
 //                warp of the group waits for it while the others wait at the
 //                group's named barrier; warp w of the group reads TMEM lane
 //                quadrant w % 4 (keys 32(w%4) .. +31 of the tile, one per
 //                thread) over every query row, frees the accumulator once its
-//                loads are done, then forms and stores the logits.  Between
-//                tiles each warp writes its share of the -inf columns outside
-//                every segment's range.
+//                loads are done, then forms and stores the logits.
 // Every wait is bounded (1 s) and a shared abort flag stops every role;
 // copies and MMAs in flight are waited for before TMEM and shared memory are
 // released.  Each E2M1 product is exact; the tensor core accumulates in
@@ -800,6 +804,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       qseq[qb] = (use + 1u) & 0x3FFFu;
       return true;
     };
+    // This producer's share of the CTA's -inf tiles, spread over its stages
+    // (the producers run well ahead of the tensor cores, the epilogue does
+    // not).
+    const int pn_all = start[5];
+    const int f_lo = (int)((long long)pn_all * pr / kProducers);
+    const int f_hi = (int)((long long)pn_all * (pr + 1) / kProducers), pn = f_hi - f_lo;
+    const int n_st = ((n + kTps - 1) / kTps - pr + kProducers - 1) / kProducers;  // its stages
+    Filler fill;
+    fill.init(p, st, start[3], start[4], f_hi);
+    fill.run(p, st, f_lo, lane, false);  // step over the other producer's share
+    int facc = 0;  // Bresenham: f_hi - f_lo tiles over n_st stages, without a division
     Desc cur = describe(0), nxt = {-1, 0u, 0};
     bool stop = false;
     for (int b = 0; !stop && kTps * batch_stage(b) < n; ++b) {
@@ -859,9 +874,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           stop = true;
           break;
         }
+        int items = 0;
+        for (facc += pn; facc >= n_st; facc -= n_st) ++items;
+        fill.run(p, st, items, lane);
       }
       cur = nxt;
     }
+    fill.run(p, st, pn, lane);  // any left (an aborted loop)
   } else if (n > 0 && warp >= kIssuerWarp && warp < kIssuerWarp + kIssuers) {
     // ---- issuers: tile k belongs to issuer k % 2 and accumulator k % 3 -------
     const int m = warp - kIssuerWarp;
@@ -966,19 +985,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int cur_g = -1;                    // segment whose weights are in wts
     int ac[kMaxTps] = {0, 0, 0, 0}, bc[kMaxTps] = {0, 0, 0, 0};  // prefill key ranges
     uint32_t pu = 0;                   // parity of this group's next use of accumulator grp
-    // This warp's share of the -inf tiles, spread over its group's tiles: a
-    // group mostly waits for its accumulator, so the stores cost little.
-    const int e = warp - kEpiWarp, pn_all = start[5];
-    const bool leader = (e & 3) == 0;
+    const bool leader = quad == 0;
     volatile uint32_t* const gflag = misc + 16;  // [group][parity]: the leader's verdict
-    const int f_lo = (int)((long long)pn_all * e / kEpiWarps);
-    const int f_hi = (int)((long long)pn_all * (e + 1) / kEpiWarps), pn = f_hi - f_lo;
-    const int n_grp = (n - grp + kEpiGroups - 1) / kEpiGroups;  // this group's tiles
-    Filler fill;
-    fill.init(p, st, start[3], start[4], f_hi);
-    fill.run(p, st, f_lo, lane, false);  // step over the earlier warps' shares
     int j_own = 0;
-    int facc = 0;  // -inf tiles spread evenly over the group's tiles, without a division
     for (int k = grp; k < n; k += kEpiGroups) {
       for (; wk < k; ++wk) w.advance(p, st);
       const int ntok = w.q.ntok;
@@ -1065,12 +1074,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                  valid ? v[t] : -INFINITY);
         }
       }
-      int items = 0;
-      for (facc += pn; facc >= n_grp; facc -= n_grp) ++items;
-      fill.run(p, st, items, lane);
       ++j_own;
     }
-    fill.run(p, st, pn, lane);  // any left (a group without tiles, an aborted loop)
   } else if (n == 0 && warp == kProducerWarp) {
     // ---- no work tiles: only this CTA's share of the -inf tiles -------------
     Filler fill;
