@@ -118,8 +118,12 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCols = 8;                // TMEM columns per scale-word slot
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 static_assert(kMaxStages % kProducers == 0, "stage slots are split evenly between the producers");
-static_assert(kIssuers == 2 && kMaxAccs == 3 && kTps % kIssuers == 0,
-              "two issuers take turns over a stage's tiles and the three accumulators");
+static_assert(kIssuers >= 2 && kIssuers <= kMaxAccs && (kIssuers == kMaxAccs || kIssuers == 2),
+              "an accumulator is used by one issuer, or by two in turn");
+// Each issuer releases a stage once, after its last tile there, when the
+// issuers split every stage evenly; otherwise every tile releases its share.
+constexpr bool kReleasePerIssuer = kTps % kIssuers == 0;
+constexpr int kStageReleases = kReleasePerIssuer ? kIssuers : kTps;
 static_assert(kQBufs == 4, "a header word holds the query buffer in two bits");
 static_assert(kMaxAccs * kMaxRows + (kMaxAccs + kIssuers * kQBufs) * kSfCols <= kTmemCols,
               "accumulators and scale words fit the TMEM columns");
@@ -632,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       *abort = 0u;
       start[2] = 0;
       start[5] = 0;
-      misc[8] = misc[9] = 0u;
+      for (int m = 0; m < kIssuers; ++m) misc[8 + m] = 0u;
       for (int b = 0; b < kQBufs; ++b) misc[24 + b] = 0u;
     }
     if (lane == 31) {
@@ -708,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // a stage's empty takes one arrival per issuer, acc_empty one per
         // warp of its epilogue group, a query buffer's empty one per issuer
         const int j = i - 2 * S;
-        const int cnt = i >= S && i < 2 * S                             ? kIssuers
+        const int cnt = i >= S && i < 2 * S                             ? kStageReleases
                         : j >= kMaxAccs && j < 3 * kMaxAccs                ? 4
                         : j >= 3 * kMaxAccs && j < 3 * kMaxAccs + kQBufs ? kIssuers
                                                                          : 1;
@@ -947,7 +951,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the stage is free once both issuers' tiles there are done: each
           // releases it after its last one (the stage's empty barrier takes
           // kIssuers arrivals; a partial last stage is never refilled)
-          if (h >= kTps - kIssuers) mma_commit(bar_empty(ps));
+          if (!kReleasePerIssuer || h >= kTps - kIssuers) mma_commit(bar_empty(ps));
           if (hdr & kHdrLast) mma_commit(bar_qempty(qb));
         }
       }
@@ -1036,30 +1040,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const int nv = ntok * CPJ;  // accumulator chunks holding this segment's rows
       const uint32_t col = tmem + lane_base + (uint32_t)grp * (uint32_t)R;
-      float v[kMaxTps];
+      float v[kMaxTps] = {0.0f, 0.0f, 0.0f, 0.0f};
+      // chunk c's weighted head sum, added to its query token's score
+      auto take = [&](int c, const uint32_t(&x)[32]) {
+        const float sc = weighted_relu_sum(x, wts + 32 * c);
+        v[c / CPJ] = c % CPJ == 0 ? sc : __fadd_rn(v[c / CPJ], sc);
+      };
+      // every load of the tile has landed: the accumulator is free
+      auto release = [&]() {
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_acce(grp, j_own & 1));
+      };
+      // Chunk c + 1 is loaded while chunk c is summed; tcgen05.wait::ld waits
+      // for every load in flight, so each wait follows the sum before it.
+      uint32_t xa[32], xb[32];
+      tmem_ld32(col, xa);
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
       for (int c = 0; c < kMaxChunks; c += 2) {
-        if (c < nv) {
-          uint32_t xa[32], xb[32];
-          tmem_ld32(col + 32u * c, xa);
-          if (c + 1 < nv) tmem_ld32(col + 32u * (c + 1), xb);
-          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-          if (c + 2 >= nv) {  // every load of the tile done: release the accumulator
-            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_acce(grp, j_own & 1));
-          }
-          const float pa_ = weighted_relu_sum(xa, wts + 32 * c);
-          if (c % CPJ == 0)
-            v[c / CPJ] = pa_;
+        if (c < nv) {  // xa holds chunk c
+          if (c + 1 < nv)
+            tmem_ld32(col + 32u * (c + 1), xb);
           else
-            v[c / CPJ] = __fadd_rn(v[c / CPJ], pa_);
+            release();
+          take(c, xa);
           if (c + 1 < nv) {
-            const float pb_ = weighted_relu_sum(xb, wts + 32 * (c + 1));
-            if ((c + 1) % CPJ == 0)
-              v[(c + 1) / CPJ] = pb_;
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            if (c + 2 < nv)
+              tmem_ld32(col + 32u * (c + 2), xa);
             else
-              v[(c + 1) / CPJ] = __fadd_rn(v[(c + 1) / CPJ], pb_);
+              release();
+            take(c + 1, xb);
+            if (c + 2 < nv) asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
           }
         }
       }
