@@ -124,6 +124,7 @@ static_assert(kIssuers >= 2 && kIssuers <= kMaxAccs && (kIssuers == kMaxAccs || 
 // issuers split every stage evenly; otherwise every tile releases its share.
 constexpr bool kReleasePerIssuer = kTps % kIssuers == 0;
 constexpr int kStageReleases = kReleasePerIssuer ? kIssuers : kTps;
+static_assert(kReleasePerIssuer, "an issuer handles its tiles of a stage together");
 static_assert(kQBufs == 4, "a header word holds the query buffer in two bits");
 static_assert(kMaxAccs * kMaxRows + (kMaxAccs + kIssuers * kQBufs) * kSfCols <= kTmemCols,
               "accumulators and scale words fit the TMEM columns");
@@ -899,24 +900,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = m; k < n; k += kIssuers) {
       const uint32_t d = tmem + (uint32_t)a * (uint32_t)R;
       const uint32_t sfa = tmem + sfa_col0 + kSfCols * (uint32_t)a;
-      // Every lane, which reads the landed words, observes the completed
-      // phase itself (acquire).
-      int ok = __all_sync(0xffffffffu, wait_phase(bar_full(ps), ph, abort));
-      if (!ok) break;
       uint8_t* const sp = stage(ps);
+      // At its first tile of a stage the issuer waits for the stage (every
+      // lane, which reads the landed words, observes the completed phase
+      // itself: acquire) and transposes the keys' words of both its tiles
+      // there; row l of a tile's block holds tokens l, l+32, l+64, l+96.
+      const bool stage_first = h < kIssuers;
+      int ok = 1;
+      if (stage_first) {
+        ok = __all_sync(0xffffffffu, wait_phase(bar_full(ps), ph, abort));
+        if (!ok) break;
+#pragma unroll
+        for (int t = 0; t < kTps / kIssuers; ++t) {
+          const int ht = h + kIssuers * t;
+          if (t == 0 || k + kIssuers * t < n) {
+            const uint32_t* ew = reinterpret_cast<const uint32_t*>(sp + kPsExp + 512 * ht);
+            *reinterpret_cast<uint4*>(sp + kPsSfa + 512 * ht + 16 * lane) =
+                make_uint4(ew[lane], ew[lane + 32], ew[lane + 64], ew[lane + 96]);
+          }
+        }
+      }
       const uint32_t hdr = *reinterpret_cast<const uint32_t*>(sp + kPsHdr + 4 * h);
       const int qb = (int)(hdr & 3u);
       const bool first = (hdr & kHdrFirst) != 0;
-      {  // the keys' words: row l holds tokens l, l+32, l+64, l+96
-        const uint32_t* ew = reinterpret_cast<const uint32_t*>(sp + kPsExp + 512 * h);
-        *reinterpret_cast<uint4*>(sp + kPsSfa + 512 * h + 16 * lane) =
-            make_uint4(ew[lane], ew[lane + 32], ew[lane + 64], ew[lane + 96]);
-      }
       if (first) {  // this issuer's first tile of the segment: the queries' words
         const uint32_t qpar = (hdr >> 2) & 1u;
-        ok = __shfl_sync(0xffffffffu, lane == 0 ? (int)wait_phase(bar_qfull(qb), qpar, abort) : 0, 0);
+        ok = __all_sync(0xffffffffu, wait_phase(bar_qfull(qb), qpar, abort));
         if (!ok) break;
-        (void)wait_phase(bar_qfull(qb), qpar, abort);  // complete: returns at once
         const int rows = (int)(hdr >> 8) & 0xFF;
         const uint32_t* qw = sQs + qb * 128;
         uint32_t v[4];
@@ -925,7 +935,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint4*>(sp + kPsSfb + 512 * h + 16 * lane) = make_uint4(v[0], v[1], v[2], v[3]);
       }
       // generic-proxy writes, read next by tcgen05.cp (async proxy)
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      if (stage_first || first) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) {
         // accumulator a has been read out (its previous use, tile k - 3, which
