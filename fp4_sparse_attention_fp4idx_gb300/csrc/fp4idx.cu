@@ -1164,6 +1164,7 @@ const char* fp4idx_status_string(fp4idx_status status) {
     case FP4IDX_ERR_ALIGN: return "a pointer or stride breaks its alignment rule";
     case FP4IDX_ERR_ARG: return "invalid argument (rope_style, eps, weight_scale or an option)";
     case FP4IDX_ERR_CUDA: return "CUDA launch failed";
+    case FP4IDX_ERR_SCRATCH: return "the request needs more than the library's static scratch";
   }
   return "unknown status";
 }

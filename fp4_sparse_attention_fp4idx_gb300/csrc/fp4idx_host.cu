@@ -77,6 +77,12 @@ bool make_pipe(Pipe& p) {
   return true;
 }
 
+// The staging of fp4idx_indexer_prepass_host_static: one buffer per device
+// (a module global), never allocated by a call.  Its address is looked up
+// once per device, under the pipeline lock.
+__device__ __align__(256) uint8_t g_static_staging[FP4IDX_STATIC_STAGING_BYTES];
+void* g_static_addr[kMaxDevicesH];
+
 }  // namespace
 
 extern "C" {
@@ -181,6 +187,36 @@ fp4idx_status fp4idx_indexer_prepass_host(
   chk(cudaStreamWaitEvent(caller, p.ev_end_out, 0));
   if (st != FP4IDX_OK) return st;
   return ok ? FP4IDX_OK : FP4IDX_ERR_CUDA;
+}
+
+fp4idx_status fp4idx_indexer_prepass_host_static(
+    const void* k, const int64_t* slot_mapping, const void* gamma, float eps, uint8_t* kv_cache,
+    int64_t num_blocks, const void* q, const void* w, int64_t num_heads, float weight_scale,
+    uint8_t* q_fp4, uint8_t* q_scale, float* weights_out, const int64_t* positions,
+    const float* cos_cache, const float* sin_cache, int64_t max_pos, int rope_style,
+    int64_t num_tokens, int64_t chunk_tokens, uint32_t* err_flags, void* stream) {
+  if (num_tokens < 0 || num_heads < 1 || chunk_tokens < 1) return FP4IDX_ERR_SHAPE;
+  if (num_tokens == 0) return FP4IDX_OK;
+  const size_t need = fp4idx_host_staging_bytes(chunk_tokens, num_heads);
+  if (need == 0) return FP4IDX_ERR_SHAPE;
+  if (need > (size_t)FP4IDX_STATIC_STAGING_BYTES) return FP4IDX_ERR_SCRATCH;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesH) return FP4IDX_ERR_CUDA;
+  void* staging = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_pipe_mutex);
+    if (g_static_addr[dev] == nullptr) {
+      void* a = nullptr;
+      if (cudaGetSymbolAddress(&a, g_static_staging) != cudaSuccess || a == nullptr)
+        return FP4IDX_ERR_CUDA;
+      g_static_addr[dev] = a;
+    }
+    staging = g_static_addr[dev];
+  }
+  return fp4idx_indexer_prepass_host(k, slot_mapping, gamma, eps, kv_cache, num_blocks, q, w,
+                                     num_heads, weight_scale, q_fp4, q_scale, weights_out,
+                                     positions, cos_cache, sin_cache, max_pos, rope_style,
+                                     num_tokens, chunk_tokens, staging, err_flags, stream);
 }
 
 }  // extern "C"

@@ -32,7 +32,8 @@ ERRFLAG_SLOT = 0x2
 ERRFLAG_TIMEOUT = 0x4
 ERRFLAG_PAGE = 0x8
 
-OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_ARG, ERR_CUDA = range(6)
+OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_ARG, ERR_CUDA, ERR_SCRATCH = range(7)
+STATIC_STAGING_BYTES = 64 << 20  # FP4IDX_STATIC_STAGING_BYTES
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
@@ -74,6 +75,9 @@ _SIGS = {
         _INT, [_P, _P, _P, _F, _P, _I64, _P, _P, _I64, _F, _P, _P, _P, _P, _P, _P, _I64,
                _INT, _I64, _I64, _P, _P, _P]),
     "fp4idx_host_staging_bytes": (ctypes.c_size_t, [_I64, _I64]),
+    "fp4idx_indexer_prepass_host_static": (
+        _INT, [_P, _P, _P, _F, _P, _I64, _P, _P, _I64, _F, _P, _P, _P, _P, _P, _P, _I64,
+               _INT, _I64, _I64, _P, _P]),
     "fp4idx_default_weight_scale": (_F, [_I64]),
     "fp4idx_test_withhold_next": (_INT, [_INT, _I64]),
     "fp4idx_status_string": (ctypes.c_char_p, [_INT]),
@@ -361,19 +365,11 @@ def _staging(device, chunk: int, H: int):
     return buf
 
 
-def indexer_prepass_host(k, gamma, slot_mapping, kv_cache, q, w, positions, cos_cache,
-                         sin_cache, *, eps: float = 1e-6, rope_style="neox", weight_scale=None,
-                         q_fp4=None, q_scale=None, weights=None, chunk_tokens: int = 4096,
-                         err_flags=None, stream=None):
-    """indexer_prepass for inputs and outputs in host memory, through the
-    C-ABI call fp4idx_indexer_prepass_host: k [T,128], q [T,H,128], w [T,H]
-    (bf16), positions and slot_mapping [T] (int64) are contiguous host
-    tensors, pinned for the copies to overlap; gamma, the cos/sin caches and
-    kv_cache are device tensors.  The library pipelines the tokens in chunks
-    of chunk_tokens (upload of chunk c+1, fused launch of chunk c, download of
-    chunk c-1) on its own streams.  Returns host tensors (q_fp4, q_scale,
-    weights), allocated pinned when not given; they are complete once the
-    caller's stream (which waits for the pipeline) has reached this point."""
+def _host_args(k, gamma, slot_mapping, kv_cache, q, w, positions, cos_cache, sin_cache,
+               weight_scale, q_fp4, q_scale, weights, chunk_tokens):
+    """Checks of the host-buffer calls; returns (T, H, chunk, q_fp4, q_scale,
+    weights, weight_scale) with the host outputs allocated pinned when not
+    given."""
     torch = _torch()
     _need_host(k, torch.bfloat16, "k", 2)
     _need_host(q, torch.bfloat16, "q", 3)
@@ -407,13 +403,31 @@ def indexer_prepass_host(k, gamma, slot_mapping, kv_cache, q, w, positions, cos_
         if tuple(t.shape) != shape:
             raise ValueError(f"{name} must be {shape}")
         outs.append(t)
-    q_fp4, q_scale, weights = outs
+    ws = default_weight_scale(H) if weight_scale is None else float(weight_scale)
+    return T, H, min(int(chunk_tokens), max(T, 1)), outs[0], outs[1], outs[2], ws
+
+
+def indexer_prepass_host(k, gamma, slot_mapping, kv_cache, q, w, positions, cos_cache,
+                         sin_cache, *, eps: float = 1e-6, rope_style="neox", weight_scale=None,
+                         q_fp4=None, q_scale=None, weights=None, chunk_tokens: int = 4096,
+                         err_flags=None, stream=None):
+    """indexer_prepass for inputs and outputs in host memory, through the
+    C-ABI call fp4idx_indexer_prepass_host: k [T,128], q [T,H,128], w [T,H]
+    (bf16), positions and slot_mapping [T] (int64) are contiguous host
+    tensors, pinned for the copies to overlap; gamma, the cos/sin caches and
+    kv_cache are device tensors.  The library pipelines the tokens in chunks
+    of chunk_tokens (upload of chunk c+1, fused launch of chunk c, download of
+    chunk c-1) on its own streams.  Returns host tensors (q_fp4, q_scale,
+    weights), allocated pinned when not given; they are complete once the
+    caller's stream (which waits for the pipeline) has reached this point."""
+    torch = _torch()
+    T, H, chunk, q_fp4, q_scale, weights, ws = _host_args(
+        k, gamma, slot_mapping, kv_cache, q, w, positions, cos_cache, sin_cache, weight_scale,
+        q_fp4, q_scale, weights, chunk_tokens)
     if T == 0:
         return q_fp4, q_scale, weights
     dev = kv_cache.device
-    chunk = min(int(chunk_tokens), T)
     staging = _staging(dev, chunk, H)
-    ws = default_weight_scale(H) if weight_scale is None else float(weight_scale)
     caller = stream if stream is not None else torch.cuda.current_stream(dev)
     with torch.cuda.device(dev):
         st = _lib.fp4idx_indexer_prepass_host(
@@ -423,6 +437,33 @@ def indexer_prepass_host(k, gamma, slot_mapping, kv_cache, q, w, positions, cos_
             cos_cache.shape[0], rope_style_code(rope_style), T, chunk, _ptr(staging),
             _ptr(err_flags), _stream_ptr(caller))
     _check(st, "fp4idx_indexer_prepass_host")
+    return q_fp4, q_scale, weights
+
+
+def indexer_prepass_host_static(k, gamma, slot_mapping, kv_cache, q, w, positions, cos_cache,
+                                sin_cache, *, eps: float = 1e-6, rope_style="neox",
+                                weight_scale=None, q_fp4=None, q_scale=None, weights=None,
+                                chunk_tokens: int = 1024, err_flags=None, stream=None):
+    """indexer_prepass_host with the staging in the library's static device
+    buffer (fp4idx_indexer_prepass_host_static): nothing is allocated on the
+    device; chunk_tokens must keep the staging within STATIC_STAGING_BYTES
+    (ERR_SCRATCH otherwise)."""
+    torch = _torch()
+    T, H, chunk, q_fp4, q_scale, weights, ws = _host_args(
+        k, gamma, slot_mapping, kv_cache, q, w, positions, cos_cache, sin_cache, weight_scale,
+        q_fp4, q_scale, weights, chunk_tokens)
+    if T == 0:
+        return q_fp4, q_scale, weights
+    dev = kv_cache.device
+    caller = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        st = _lib.fp4idx_indexer_prepass_host_static(
+            _ptr(k), _ptr(slot_mapping), _ptr(gamma), float(eps), _ptr(kv_cache),
+            kv_cache.shape[0], _ptr(q), _ptr(w), H, ws, _ptr(q_fp4), _ptr(q_scale),
+            _ptr(weights), _ptr(positions), _ptr(cos_cache), _ptr(sin_cache),
+            cos_cache.shape[0], rope_style_code(rope_style), T, chunk, _ptr(err_flags),
+            _stream_ptr(caller))
+    _check(st, "fp4idx_indexer_prepass_host_static")
     return q_fp4, q_scale, weights
 
 

@@ -76,7 +76,9 @@ typedef enum fp4idx_status {
   FP4IDX_ERR_ALIGN = 3, /* a pointer or stride breaks its alignment rule    */
   FP4IDX_ERR_ARG = 4,   /* bad rope_style, eps not finite and > 0, a
                            non-finite weight_scale, or a bad option          */
-  FP4IDX_ERR_CUDA = 5   /* the kernel launch failed                          */
+  FP4IDX_ERR_CUDA = 5,  /* the kernel launch failed                          */
+  FP4IDX_ERR_SCRATCH = 6 /* the request needs more than the library's static
+                            scratch (fp4idx_indexer_prepass_host_static)     */
 } fp4idx_status;
 
 enum {
@@ -310,6 +312,40 @@ fp4idx_status fp4idx_indexer_prepass_host(
     float* weights_out, const int64_t* positions, const float* cos_cache,
     const float* sin_cache, int64_t max_pos, int rope_style, int64_t num_tokens,
     int64_t chunk_tokens, void* staging, uint32_t* err_flags, void* stream);
+
+/*
+ * fp4idx_indexer_prepass_host with the device staging in a static buffer of
+ * the library instead of one the caller passes.  The pages have no
+ * counterpart: this is a convenience form of the host-buffer call for
+ * callers that own no device scratch.  It allocates nothing (no cudaMalloc,
+ * cudaFree or allocating library routine): the staging is one file-scope
+ * __device__ array of FP4IDX_STATIC_STAGING_BYTES per device, whose address
+ * is looked up once per device (cudaGetSymbolAddress).
+ *
+ * Arguments, results and checks are those of fp4idx_indexer_prepass_host
+ * without `staging`.  A request whose staging
+ * (fp4idx_host_staging_bytes(chunk_tokens, num_heads)) exceeds the static
+ * buffer returns FP4IDX_ERR_SCRATCH before anything is enqueued: choose
+ * chunk_tokens with chunk_tokens * (660 * num_heads + 544) + 4096 <=
+ * FP4IDX_STATIC_STAGING_BYTES (e.g. 1,536 tokens at 64 heads).  A failed
+ * symbol lookup returns FP4IDX_ERR_CUDA.  Nothing in the buffer needs to
+ * start at zero: every chunk's inputs are uploaded before its launch reads
+ * them, and its outputs written before they are downloaded.
+ *
+ * Overlapping calls would race on the one buffer.  The library orders them
+ * instead: calls enqueue under a lock, and each call's first uploads wait
+ * until the previous call on the device no longer reads or writes the
+ * staging, so concurrent callers run one after the other on the GPU.
+ */
+enum { FP4IDX_STATIC_STAGING_BYTES = 64 << 20 };
+
+fp4idx_status fp4idx_indexer_prepass_host_static(
+    const void* k, const int64_t* slot_mapping, const void* gamma, float eps,
+    uint8_t* kv_cache, int64_t num_blocks, const void* q, const void* w,
+    int64_t num_heads, float weight_scale, uint8_t* q_fp4, uint8_t* q_scale,
+    float* weights_out, const int64_t* positions, const float* cos_cache,
+    const float* sin_cache, int64_t max_pos, int rope_style, int64_t num_tokens,
+    int64_t chunk_tokens, uint32_t* err_flags, void* stream);
 
 /*
  * Torch-shaped fake quantisation: RoPE, then every value replaced by its

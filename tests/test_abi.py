@@ -34,7 +34,7 @@ def test_exports_every_declared_symbol(F):
                           "fp4idx_mqa_logits_prefill", "fp4idx_default_weight_scale",
                           "fp4idx_test_withhold_next", "fp4idx_status_string",
                           "fp4idx_version", "fp4idx_indexer_prepass_host",
-                          "fp4idx_host_staging_bytes"}
+                          "fp4idx_host_staging_bytes", "fp4idx_indexer_prepass_host_static"}
     out = subprocess.run(["nm", "-D", "--defined-only", F.LIB_PATH], capture_output=True,
                          text=True, check=True).stdout
     exported = set(re.findall(r"\bT (fp4idx_\w+)", out))
@@ -52,8 +52,8 @@ def test_library_is_built_for_sm103a(F):
 
 
 def test_status_strings_and_version(F):
-    texts = [F.status_string(s) for s in range(6)]
-    assert texts[0] == "ok" and len(set(texts)) == 6
+    texts = [F.status_string(s) for s in range(7)]
+    assert texts[0] == "ok" and len(set(texts)) == 7
     assert F.status_string(99) == "unknown status"
     assert F.version().startswith("fp4idx ") and "sm_103a" in F.version()
 
@@ -402,6 +402,43 @@ def test_host_staging_bytes(F):
     assert L.fp4idx_host_staging_bytes(1, 1) == 2 * 8 * 256
     for c, h in ((0, 32), (32, 0), (-1, 1), (1 << 30, 1), (1 << 15, 1 << 15)):
         assert L.fp4idx_host_staging_bytes(c, h) == 0
+
+
+def _call_hs(F, a):
+    return F.lib().fp4idx_indexer_prepass_host_static(
+        a["k"], a["slots"], a["gamma"], a["eps"], a["cache"], a["num_blocks"], a["q"], a["w"],
+        a["H"], a["ws"], a["qf"], a["qs"], a["wt"], a["pos"], a["cos"], a["sin"], a["max_pos"],
+        a["style"], a["T"], a["chunk"], a["err"], a["stream"])
+
+
+@pytest.mark.fake_ptr
+@pytest.mark.parametrize("over,code", [
+    (dict(T=-1), "ERR_SHAPE"), (dict(H=0), "ERR_SHAPE"), (dict(chunk=0), "ERR_SHAPE"),
+    (dict(chunk=1 << 30), "ERR_SHAPE"),
+    (dict(chunk=4096, H=64), "ERR_SCRATCH"),       # 168 MB of staging
+    (dict(chunk=1569, H=64), "ERR_SCRATCH"),       # just past the buffer (1568 fit)
+    (dict(chunk=100000, H=1), "ERR_SCRATCH"),
+    (dict(T=0, k=None, q=None), "OK"),
+], ids=["T", "H", "chunk0", "chunk_overflow", "4096x64", "1569x64", "100000x1", "empty"])
+def test_static_staging_host_checks(F, over, code):
+    """The static-staging call rejects a request its buffer cannot hold
+    before it looks the buffer up or enqueues anything."""
+    assert _call_hs(F, _h_args(**over)) == getattr(F, code)
+
+
+def test_static_staging_bound(F):
+    """The header's sufficient condition for a chunk to fit the static
+    buffer, c * (660 H + 544) + 4096 <= FP4IDX_STATIC_STAGING_BYTES, holds
+    against the library's staging size, and its example fits."""
+    text = open(F.HEADER_PATH).read()
+    assert "FP4IDX_STATIC_STAGING_BYTES = 64 << 20" in text
+    L = F.lib()
+    for c, h in ((1536, 64), (3072, 32), (1, 1), (777, 17), (12000, 8)):
+        exact = L.fp4idx_host_staging_bytes(c, h)
+        assert c * (660 * h + 544) <= exact <= c * (660 * h + 544) + 4096
+    assert L.fp4idx_host_staging_bytes(1536, 64) <= F.STATIC_STAGING_BYTES
+    assert L.fp4idx_host_staging_bytes(1568, 64) <= F.STATIC_STAGING_BYTES
+    assert L.fp4idx_host_staging_bytes(1569, 64) > F.STATIC_STAGING_BYTES
 
 
 @pytest.mark.fake_ptr
