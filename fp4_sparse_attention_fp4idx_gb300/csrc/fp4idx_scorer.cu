@@ -66,9 +66,8 @@
 //                of the stage free and, after its last tile of a segment, its
 //                share of the segment's query buffer free (a buffer is free
 //                once two releases came).
-//   warps 4-15   epilogue: group m = (w - 4) / 4 reads accumulator m; one
-//                warp of the group waits for it while the others wait at the
-//                group's named barrier; warp w of the group reads TMEM lane
+//   warps 4-15   epilogue: group m = (w - 4) / 4 reads accumulator m; each
+//                warp of the group waits for it; warp w of the group reads TMEM lane
 //                quadrant w % 4 (keys 32(w%4) .. +31 of the tile, one per
 //                thread) over every query row, frees the accumulator once its
 //                loads are done, then forms and stores the logits.
@@ -999,8 +998,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     int cur_g = -1;                    // segment whose weights are in wts
     int ac[kMaxTps] = {0, 0, 0, 0}, bc[kMaxTps] = {0, 0, 0, 0};  // prefill key ranges
     uint32_t pu = 0;                   // parity of this group's next use of accumulator grp
-    const bool leader = quad == 0;
-    volatile uint32_t* const gflag = misc + 16;  // [group][parity]: the leader's verdict
     int j_own = 0;
     for (int k = grp; k < n; k += kEpiGroups) {
       for (; wk < k; ++wk) w.advance(p, st);
@@ -1035,17 +1032,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                   ? __ldg(p.block_table + (int64_t)w.q.b * p.bt_stride + pidx)
                   : -1;
       }
-      // One warp of the group waits for the accumulator; the others wait at
-      // the group's named barrier, which takes no issue slots (spinning warps
-      // would take them from the issuers and the producer).  The leader's
-      // verdict goes through shared memory, one slot per parity, so that all
-      // four warps leave together.
-      if (leader) {
-        const bool ok = __all_sync(0xffffffffu, wait_phase(bar_accf(grp), pu, abort));
-        if (lane == 0) gflag[2 * grp + pu] = ok ? 1u : 0u;
-      }
-      asm volatile("bar.sync %0, 128;" ::"r"(1 + grp) : "memory");
-      if (!gflag[2 * grp + pu]) break;
+      // Every warp of the group waits for the accumulator itself (a warp
+      // suspended in mbarrier.try_wait takes no issue slots) and so observes
+      // its completion (acquire).
+      if (!__all_sync(0xffffffffu, wait_phase(bar_accf(grp), pu, abort))) break;
       pu ^= 1u;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const int nv = ntok * CPJ;  // accumulator chunks holding this segment's rows
