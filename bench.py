@@ -492,6 +492,8 @@ def _scorer_record(name, ms_list, nbytes, flops, peak, extra, alu=None):
     ms = sp["median"]
     achieved = nbytes / (ms / 1e3) / 1e9
     tr = traffic_record(name)
+    if tr and tr.get("workload_name") != extra.get("workload"):
+        tr = None  # the counters were taken on another workload
     rec = dict(extra)
     hbm = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
            "unit": "GB/s", "frac": round(achieved / peak, 4), "kernel": name,
