@@ -443,12 +443,20 @@ def indexer_prepass_host(k, gamma, slot_mapping, kv_cache, q, w, positions, cos_
 def indexer_prepass_host_static(k, gamma, slot_mapping, kv_cache, q, w, positions, cos_cache,
                                 sin_cache, *, eps: float = 1e-6, rope_style="neox",
                                 weight_scale=None, q_fp4=None, q_scale=None, weights=None,
-                                chunk_tokens: int = 1024, err_flags=None, stream=None):
+                                chunk_tokens=None, err_flags=None, stream=None):
     """indexer_prepass_host with the staging in the library's static device
     buffer (fp4idx_indexer_prepass_host_static): nothing is allocated on the
     device; chunk_tokens must keep the staging within STATIC_STAGING_BYTES
-    (ERR_SCRATCH otherwise)."""
+    (ERR_SCRATCH otherwise).  By default it is the largest power-of-two
+    share of 1024 tokens whose staging fits."""
     torch = _torch()
+    if chunk_tokens is None:
+        H = q.shape[1] if hasattr(q, "shape") and q.dim() == 3 else 1
+        chunk_tokens = 1024
+        while chunk_tokens > 1 and (
+                _lib.fp4idx_host_staging_bytes(chunk_tokens, H) == 0 or
+                _lib.fp4idx_host_staging_bytes(chunk_tokens, H) > STATIC_STAGING_BYTES):
+            chunk_tokens //= 2
     T, H, chunk, q_fp4, q_scale, weights, ws = _host_args(
         k, gamma, slot_mapping, kv_cache, q, w, positions, cos_cache, sin_cache, weight_scale,
         q_fp4, q_scale, weights, chunk_tokens)

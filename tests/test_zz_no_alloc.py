@@ -68,3 +68,21 @@ def test_static_staging_refuses_oversize_chunk():
     with pytest.raises(F().Fp4idxError) as e:
         _call(w, _inputs(w), cache, chunk=2000)  # 2000 x 64 rows need ~85 MB of staging
     assert e.value.status == F().ERR_SCRATCH
+
+
+def test_static_staging_default_chunk_fits_128_heads():
+    """Without chunk_tokens the binding picks a chunk whose staging fits the
+    static buffer (512 tokens at 128 heads), and the bytes are the oracle's."""
+    w = wl.make_random(600, 128, wl.ROPE_INTERLEAVED, seed=4245)
+    rc, rqf, rqs, rwt = run_oracle(w)
+    d = _inputs(w)
+    cache = dev(w.cache_init)
+    gamma, cos, sin = d
+    qf, qs, wt = F().indexer_prepass_host_static(
+        host_bf16(w.k), gamma, host(w.slot_mapping), cache, host_bf16(w.q), host_bf16(w.w),
+        host(w.positions), cos, sin, eps=w.eps, rope_style=w.rope_style)
+    torch.cuda.synchronize()
+    assert_bytes_equal(cache.cpu().numpy(), rc, "kv_cache")
+    assert_bytes_equal(qf.numpy(), rqf, "q_fp4")
+    assert_bytes_equal(qs.numpy(), rqs, "q_scale")
+    assert_weights(wt.numpy(), rwt)
