@@ -60,3 +60,44 @@ def test_host_pipeline_repeated_calls_share_staging():
         assert_bytes_equal(qf.numpy(), rqf, "q_fp4")
         assert_bytes_equal(qs.numpy(), rqs, "q_scale")
         assert_weights(wt.numpy(), rwt)
+
+
+def test_host_pipeline_two_threads_share_staging():
+    """Two host threads, each on its own stream, call the host-buffer pre-pass
+    three times each with the same chunking (so they share the library's
+    pipeline and the binding's staging buffer); every result is the
+    oracle's.  The calls enqueue one at a time and each waits until the
+    previous one no longer uses the staging."""
+    import threading
+    ws = [wl.make_random(180, 32, wl.ROPE_NEOX, seed=901),
+          wl.make_random(150, 32, wl.ROPE_INTERLEAVED, seed=902)]
+    refs = [run_oracle(w) for w in ws]
+    errors = []
+
+    def worker(w, ref):
+        try:
+            s = torch.cuda.Stream()
+            gamma = torch.from_numpy(w.gamma.view(np.int16)).view(torch.bfloat16).cuda()
+            cos, sin = dev(w.cos), dev(w.sin)
+            args = (host_bf16(w.k), gamma, host(w.slot_mapping))
+            for _ in range(3):
+                with torch.cuda.stream(s):
+                    cache = dev(w.cache_init)
+                    s.synchronize()
+                    qf, qs, wt = F().indexer_prepass_host(
+                        *args, cache, host_bf16(w.q), host_bf16(w.w), host(w.positions), cos, sin,
+                        eps=w.eps, rope_style=w.rope_style, chunk_tokens=40, stream=s)
+                    s.synchronize()
+                assert_bytes_equal(cache.cpu().numpy(), ref[0], "kv_cache")
+                assert_bytes_equal(qf.numpy(), ref[1], "q_fp4")
+                assert_bytes_equal(qs.numpy(), ref[2], "q_scale")
+                assert_weights(wt.numpy(), ref[3])
+        except Exception as e:  # reported on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(w, r)) for w, r in zip(ws, refs)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
