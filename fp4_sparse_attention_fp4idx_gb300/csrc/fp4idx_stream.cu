@@ -90,6 +90,9 @@ constexpr int kConsumers = FP4IDX_STREAM_CONSUMERS;
 constexpr int kProducers = FP4IDX_STREAM_PRODUCERS;
 constexpr int kThreadsS = (kConsumers + kProducers) * 32;
 constexpr int kStagesS = FP4IDX_STREAM_STAGES;
+// A producer's share of units up to which no rows go out ahead of the first
+// metadata.
+constexpr int kShortShare = 32;
 static_assert(kStagesS % kProducers == 0, "each producer owns kStagesS / kProducers stages");
 // Stage: rows | a cos row and a sin row per token of a query unit (at most
 // 4: slices never straddle tokens), or 64 positions and 64 slots (key unit)
@@ -895,13 +898,16 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     const int n_own = n_units > p ? (n_units - p + kProducers - 1) / kProducers : 0;
     int issued = 0;  // own units issued
     int64_t pos_cur = pos_first, pos_next = 0;
-    // The first own unit's rows go out at once; every later unit's rows go
-    // out together with its metadata (the first metadata waits for the
-    // positions, and should not queue behind a whole ring of rows).
+    // On a long share the first own unit's rows go out at once; every other
+    // unit's rows go out together with its metadata.  The first metadata
+    // waits for the positions and should not queue behind a ring of rows; on
+    // a short share (a prefill-sized step) not even behind one unit's rows
+    // (T=8192: 36.0 against 36.4 us; T=65536 keeps the early rows, 0.6%).
     // (testing hook, see fp4idx_test_withhold_next: a withheld unit's copies
     // and arrival are skipped, so the waits for it run out)
     const int held = blockIdx.x == 0 ? wk.withhold : -1;
-    if (n_own > 0 && p != held)
+    const int rows_first = n_own > kShortShare ? 1 : 0;  // own units whose rows go out first
+    if (rows_first && p != held)
       issue_rows(p, u, wk, ka, qa, ring + (uint32_t)p * kStageBytesS, full0 + 8u * p);
     for (int m = 0; m < n_own; ++m) {
       if (m % kBatch == 0) {
@@ -920,7 +926,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
           break;
         }
       }
-      if (m > 0 && i != held) issue_rows(i, u, wk, ka, qa, stage, bar);
+      if (m >= rows_first && i != held) issue_rows(i, u, wk, ka, qa, stage, bar);
       if (i != held) issue_meta(i, m % kBatch, u, wk, ka, qa, sh, pos_cur, stage, bar);
       issued = m + 1;
     }
