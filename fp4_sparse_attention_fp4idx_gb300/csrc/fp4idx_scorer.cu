@@ -1000,6 +1000,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t pu = 0;                   // parity of this group's next use of accumulator grp
     int j_own = 0;
     for (int k = grp; k < n; k += kEpiGroups) {
+      if (k > wk && w.t + (k - wk) < w.hi) {  // the common case: the same segment
+        w.t += k - wk;
+        w.pos += k - wk;
+        w.first = false;
+        wk = k;
+      }
       for (; wk < k; ++wk) w.advance(p, st);
       const int ntok = w.q.ntok;
       if (w.g != cur_g) {  // a new segment: its weights (and key ranges)
@@ -1077,14 +1083,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const int s_tok = w.t * kTile + row;
+      float* const rowp = p.logits + (int64_t)w.q.qt0 * p.logits_stride;  // first row
       const bool pok = pid >= 0 && pid < p.num_blocks;
 #pragma unroll
       for (int t = 0; t < kMaxTps; ++t) {
         if (t < ntok && s_tok < p.ncols) {
           const bool valid = MODE == kModeDecode ? (s_tok < w.lim && pok)
                                                    : (s_tok >= ac[t] && s_tok < bc[t]);
-          __stcs(p.logits + (int64_t)(w.q.qt0 + t) * p.logits_stride + s_tok,
-                 valid ? v[t] : -INFINITY);
+          __stcs(rowp + (int64_t)t * p.logits_stride + s_tok, valid ? v[t] : -INFINITY);
         }
       }
       ++j_own;
