@@ -996,6 +996,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     w.init(p, st, start[0], start[1]);
     int wk = 0;                        // w's tile
     int cur_g = -1;                    // segment whose weights are in wts
+    float* rowp = p.logits;            // the segment's first logits row
+    const int32_t* btrow = p.block_table;  // decode: the segment's block-table row
     int ac[kMaxTps] = {0, 0, 0, 0}, bc[kMaxTps] = {0, 0, 0, 0};  // prefill key ranges
     uint32_t pu = 0;                   // parity of this group's next use of accumulator grp
     int j_own = 0;
@@ -1009,6 +1011,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (; wk < k; ++wk) w.advance(p, st);
       const int ntok = w.q.ntok;
       if (w.g != cur_g) {  // a new segment: its weights (and key ranges)
+        rowp = p.logits + (int64_t)w.q.qt0 * p.logits_stride;
+        if (MODE == kModeDecode) btrow = p.block_table + (int64_t)w.q.b * p.bt_stride;
         float wr[kMaxChunks];
 #pragma unroll
         for (int c = 0; c < kMaxChunks; ++c) {
@@ -1035,7 +1039,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (MODE == kModeDecode) {
         const int pidx = w.t * 2 + (quad >> 1);
         pid = pidx * kKvBlock < w.lim
-                  ? __ldg(p.block_table + (int64_t)w.q.b * p.bt_stride + pidx)
+                  ? __ldg(btrow + pidx)
                   : -1;
       }
       // Every warp of the group waits for the accumulator itself (a warp
@@ -1083,7 +1087,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const int s_tok = w.t * kTile + row;
-      float* const rowp = p.logits + (int64_t)w.q.qt0 * p.logits_stride;  // first row
       const bool pok = pid >= 0 && pid < p.num_blocks;
 #pragma unroll
       for (int t = 0; t < kMaxTps; ++t) {
