@@ -764,6 +764,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int m = kTps * (batch_stage(b) + kProducers * (sl / kTps)) + sl % kTps;
       Desc dsc = {-1, 0u, 0};
       if (m < n) {
+        if (m > lk && lw.t + (m - lk) < lw.hi) {  // the common case: the same segment
+          lw.t += m - lk;
+          lw.pos += m - lk;
+          lw.first = false;
+          lk = m;
+        }
         for (; lk < m; ++lk) lw.advance(p, st);
         const int pidx = lw.t * 2 + (lane & 1);
         if (pidx * kKvBlock < lw.lim) {
