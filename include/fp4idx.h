@@ -320,7 +320,10 @@ fp4idx_status fp4idx_indexer_prepass_host(
  * callers that own no device scratch.  It allocates nothing (no cudaMalloc,
  * cudaFree or allocating library routine): the staging is one file-scope
  * __device__ array of FP4IDX_STATIC_STAGING_BYTES per device, whose address
- * is looked up once per device (cudaGetSymbolAddress).
+ * is looked up once per device (cudaGetSymbolAddress).  The array occupies
+ * device memory from the time the library's module is loaded on a device:
+ * with the CUDA runtime's lazy module loading (its default), the first call
+ * of this function there; with eager loading, context creation.
  *
  * Arguments, results and checks are those of fp4idx_indexer_prepass_host
  * without `staging`.  A request whose staging
