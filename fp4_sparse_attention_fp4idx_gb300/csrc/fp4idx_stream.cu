@@ -26,7 +26,8 @@
 //    flattened (token, head) row space, a key unit 64 consecutive tokens.
 //    Every CTA takes an equal contiguous slice of each list, key units first.
 //  * kProducers producer warps per CTA fill a ring of kStagesS shared-memory
-//    stages with cp.async.bulk (producer p owns units p, p + kProducers, ...
+//    stages (kShortStages on a short step) with cp.async.bulk (producer p
+//    owns units p, p + kProducers, ...
 //    and so every kProducers-th stage): a unit's rows (one 16 KB copy when
 //    they are contiguous in memory) and, for a query unit, the cos/sin rows
 //    of each distinct token.  A warp waits a few hundred cycles for each bulk
@@ -76,6 +77,9 @@ namespace {
 #ifndef FP4IDX_STREAM_STAGES
 #define FP4IDX_STREAM_STAGES 12
 #endif
+#ifndef FP4IDX_STREAM_SHORT_STAGES
+#define FP4IDX_STREAM_SHORT_STAGES 8
+#endif
 #ifndef FP4IDX_STREAM_PRODUCERS
 #define FP4IDX_STREAM_PRODUCERS 4
 #endif
@@ -93,7 +97,17 @@ constexpr int kStagesS = FP4IDX_STREAM_STAGES;
 // A producer's share of units up to which no rows go out ahead of the first
 // metadata.
 constexpr int kShortShare = 32;
-static_assert(kStagesS % kProducers == 0, "each producer owns kStagesS / kProducers stages");
+// The largest producer share of a launch up to which the ring is
+// kShortStages deep instead of kStagesS.  On a short step the first units'
+// copies then queue behind fewer rows (T=8192 at 64 heads, shares of 14:
+// 35.2 against 35.6 us; MTP, shares of 4: 16.8 against 17.1 us); from
+// shares of ~28 up the deeper ring keeps HBM busier (T=16384: 61.9 against
+// 60.9 us; T=65536: 212.5 against 217.3 us with 8 stages throughout).
+constexpr int kShallowShare = 16;
+constexpr int kShortStages = FP4IDX_STREAM_SHORT_STAGES;
+static_assert(kStagesS % kProducers == 0 && kShortStages % kProducers == 0 &&
+                  kShortStages >= kProducers && kShortStages <= kStagesS,
+              "each producer owns a whole number of stages");
 // Stage: rows | a cos row and a sin row per token of a query unit (at most
 // 4: slices never straddle tokens), or 64 positions and 64 slots (key unit)
 // | header | 64 head weights (query unit).
@@ -126,7 +140,16 @@ struct SWork {
   int w_bulk;      // head weights dense ([T, H]) and 16-byte aligned
   int meta_bulk;   // positions and slots 16-byte aligned
   int withhold;    // testing: a unit of CTA 0 whose copies are not issued (-1: none)
+  int stages;      // ring depth S of this launch: kShortStages or kStagesS
+  uint32_t smul;   // ceil(2^32 / S)
 };
+
+// Uses of unit i's stage before unit i, i / S (the stage is i - uses * S):
+// S * ceil(2^32 / S) = 2^32 + d with d < S, so the high word of i * smul is
+// the quotient for every i below 2^32 / S, far above any unit count.
+__device__ __forceinline__ uint32_t stage_uses(int i, const SWork& wk) {
+  return __umulhi((uint32_t)i, wk.smul);
+}
 
 __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
   uint16_t v;
@@ -179,12 +202,12 @@ __device__ __forceinline__ uint32_t lds_volatile(uint32_t addr) {
 
 // A consumer's wait for unit i in stage `stage` (all 32 lanes call).  Slices
 // are claimed ahead of the producers, so the stage may still be waiting for
-// unit i - kStagesS or older; a parity wait alone would then alias an older
+// unit i - stages or older; a parity wait alone would then alias an older
 // phase.  So first wait (bounded) until the producer has tagged the stage's
 // header with i -- it does so only after the previous unit in the stage was
 // released, i.e. once the stage's barrier is in unit i's phase -- and only
 // then wait for that phase.
-__device__ __forceinline__ bool wait_unit(uint32_t stage, uint32_t bar, int i,
+__device__ __forceinline__ bool wait_unit(uint32_t stage, uint32_t bar, int i, const SWork& wk,
                                           const volatile int* abort) {
   bool ok = (lds_volatile(stage + kHdrOff) >> 2) == (uint32_t)i;
   if (!ok) {
@@ -199,7 +222,7 @@ __device__ __forceinline__ bool wait_unit(uint32_t stage, uint32_t bar, int i,
     }
   }
   if (!__all_sync(kFull, ok)) return false;
-  return wait_or_abort(bar, (uint32_t)((i / kStagesS) & 1), abort);
+  return wait_or_abort(bar, stage_uses(i, wk) & 1u, abort);
 }
 
 // RoPE coefficients of one lane, in the order of its registers A (parts
@@ -878,7 +901,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   int64_t pos_first = 0;
   if (warp >= kConsumers) pos_first = slice_pos(warp - kConsumers, 0, u, wk, sh);
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStagesS; ++s) {
+    for (int s = 0; s < wk.stages; ++s) {
       mbar_init(full0 + 8u * s, 1);
       mbar_init(empty0 + 8u * s, kSlices);
       asm volatile("st.shared.u32 [%0], %1;" ::"r"(ring + (uint32_t)s * kStageBytesS + kHdrOff),
@@ -891,6 +914,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   }
   __syncthreads();
   const int n_units = u.total();
+  const int S = wk.stages;
 
   if (warp >= kConsumers) {
     // ---------------- producers: producer p issues units p, p + kProducers, ...
@@ -915,10 +939,11 @@ __global__ void __launch_bounds__(kThreadsS, 1)
         pos_next = slice_pos(p, m + kBatch, u, wk, sh);
       }
       const int i = p + kProducers * m;
-      const int s = i % kStagesS;
+      const uint32_t ph = stage_uses(i, wk);
+      const int s = i - (int)ph * S;
       const uint32_t stage = ring + (uint32_t)s * kStageBytesS, bar = full0 + 8u * s;
-      if (i >= kStagesS) {
-        if (!wait_or_abort(empty0 + 8u * s, (uint32_t)((i / kStagesS - 1) & 1), &abort_flag)) {
+      if (ph > 0) {
+        if (!wait_or_abort(empty0 + 8u * s, (ph - 1) & 1u, &abort_flag)) {
           if (lane == 0) {
             flag_error(sh.err, FP4IDX_ERRFLAG_TIMEOUT);
             abort_flag = 1;
@@ -938,9 +963,10 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     // The drain ignores the abort flag: only the time limit ends it.
     __syncthreads();
     const int no_abort = 0;
-    for (int m = max(issued - kStagesS / kProducers, 0); m < issued; ++m) {
+    for (int m = max(issued - S / kProducers, 0); m < issued; ++m) {
       const int i = p + kProducers * m;
-      wait_or_abort(full0 + 8u * (i % kStagesS), (uint32_t)((i / kStagesS) & 1), &no_abort);
+      const uint32_t ph = stage_uses(i, wk);
+      wait_or_abort(full0 + 8u * (uint32_t)(i - (int)ph * S), ph & 1u, &no_abort);
     }
     return;
   }
@@ -952,9 +978,10 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     k = __shfl_sync(kFull, k, 0);
     const int i = k / kSlices, sl = k % kSlices;
     if (i >= n_units) break;
-    const int s = i % kStagesS;
+    const uint32_t ph = stage_uses(i, wk);
+    const int s = i - (int)ph * wk.stages;
     const uint32_t stage = ring + (uint32_t)s * kStageBytesS;
-    if (!wait_unit(stage, full0 + 8u * s, i, &abort_flag)) {
+    if (!wait_unit(stage, full0 + 8u * s, i, wk, &abort_flag)) {
       if (lane == 0) {
         flag_error(sh.err, FP4IDX_ERRFLAG_TIMEOUT);
         abort_flag = 1;
@@ -968,7 +995,9 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     else
       query_slice<kStyle, kRotate, kFp8>(stage, (int32_t)hdr[1], (int)hdr[2], hdr[3], sl, wk, qa, sh);
     __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8u * s);
+    // (the stage's index again from its address: one register fewer live
+    // across the slice, which one variant would otherwise spill)
+    if (lane == 0) mbar_arrive(empty0 + 8u * ((stage - ring) / (uint32_t)kStageBytesS));
   }
   __syncthreads();
 }
@@ -1006,7 +1035,8 @@ cudaError_t launch_style(unsigned grid, cudaStream_t s, const KArgs& ka, const Q
               : !rotate       ? stream_kernel<kStyle, false, true>
               : !fp8          ? stream_kernel<kStyle, true, false>
                               : stream_kernel<kStyle, true, true>;
-  return launch_kernel(kern, grid, kThreadsS, kSmemS, s, ka, qa, sh, wk);
+  return launch_kernel(kern, grid, kThreadsS, (unsigned)(wk.stages * kStageBytesS), s, ka, qa,
+                       sh, wk);
 }
 
 // Testing hook: the unit of CTA 0 whose copies the next launch withholds
@@ -1062,6 +1092,10 @@ fp4idx_status launch_stream(const KArgs& ka, const QArgs& qa, const Shared& sh, 
   const int sms = stream_sms();
   if (sms <= 0) return FP4IDX_ERR_CUDA;
   const unsigned grid = (unsigned)(total < sms ? total : sms);
+  // the largest producer share of this launch decides the ring depth
+  const int64_t per_cta = (total + grid - 1) / grid;
+  wk.stages = (per_cta + kProducers - 1) / kProducers <= kShallowShare ? kShortStages : kStagesS;
+  wk.smul = (uint32_t)(((1ull << 32) + (uint64_t)wk.stages - 1) / (uint64_t)wk.stages);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const cudaError_t e =
       rope_style == FP4IDX_ROPE_NEOX
