@@ -80,15 +80,16 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def traffic_record(kernel: str):
+def traffic_record(kernel: str, workload: str, mode: str = "fused"):
     """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel's source file changed since the counters were taken."""
+    counters were taken on another workload or launch mode, or the kernel's
+    source file changed since."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
         rec = d.get(kernel)
-        if not rec:
+        if not rec or rec.get("workload_name") != workload or rec.get("mode", "fused") != mode:
             return None
         with open(os.path.join(ROOT, rec["source_file"]), "rb") as f:
             h = hashlib.sha256(f.read()).hexdigest()
@@ -491,9 +492,7 @@ def _scorer_record(name, ms_list, nbytes, flops, peak, extra, alu=None):
     sp = spread(ms_list)
     ms = sp["median"]
     achieved = nbytes / (ms / 1e3) / 1e9
-    tr = traffic_record(name)
-    if tr and tr.get("workload_name") != extra.get("workload"):
-        tr = None  # the counters were taken on another workload
+    tr = traffic_record(name, extra.get("workload"))
     rec = dict(extra)
     hbm = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
            "unit": "GB/s", "frac": round(achieved / peak, 4), "kernel": name,
@@ -768,7 +767,7 @@ def run_ours(args):
     else:
         kbytes, kms = ab["q_call"], float(np.median(r["q_ms"]))
     achieved = kbytes / (kms / 1e3) / 1e9
-    tr = traffic_record(kname)
+    tr = traffic_record(kname, w.name, args.mode)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                 "kernel": kname, "algorithmic_bytes_per_launch": kbytes,

@@ -102,3 +102,23 @@ def test_scorer_bytes_match_array_sizes():
         reads += ctx * slot_bytes + pages.nbytes
     logits = np.empty((sw.batch * sw.next_n, sw.max_context), np.float32)
     assert bench.scorer_bytes(sw) == reads + logits.nbytes
+
+
+def test_traffic_record_only_for_its_workload_and_mode():
+    """A committed DRAM-counter record is reported only beside the workload
+    and launch mode it was captured on, and only while its kernel's source
+    is the one that was captured."""
+    sys.path.insert(0, ROOT)
+    import json
+
+    import bench
+    with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+        d = json.load(f)
+    for kernel, rec in d.items():
+        name, mode = rec["workload_name"], rec.get("mode", "fused")
+        assert bench.traffic_record(kernel, name + "_other", mode) is None
+        assert bench.traffic_record(kernel, name, "separate") is None or mode == "separate"
+        got = bench.traffic_record(kernel, name, mode)
+        if got is not None:  # None only while the source differs from the capture's
+            assert got["dram_bytes_per_launch"] == rec["dram_bytes_read"] + rec["dram_bytes_write"]
+    assert bench.traffic_record("no_such_kernel", "large_prefill") is None
