@@ -20,6 +20,12 @@
  *
  * Where the pages leave a step open, the reading used is stated beside the
  * function that takes it.
+ *
+ * Parity unpinned: two readings have no page fact to pin them, so the tests
+ * fix the oracle's behaviour under them but cannot confirm them: the
+ * summation order of the sum of squares in oracle_rmsnorm_row, and the
+ * placement of a slot's 68 bytes in a 4352-byte cache page (64 payload
+ * bytes at 64 o, the exponent word at 4096 + 4 o) in the cache store.
  */
 #ifndef FP4IDX_ORACLE_H
 #define FP4IDX_ORACLE_H
