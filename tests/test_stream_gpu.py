@@ -35,6 +35,21 @@ def test_stream_ragged(T, H, style, hadamard):
         assert int(d.err.item()) == 0
 
 
+@pytest.mark.parametrize("T", [9578, 9579])
+def test_stream_ring_depth_boundary(T):
+    """The ring is 8 stages deep while the largest producer share of a
+    launch is at most 16 units, else 12.  At 64 heads on 152 SMs the fused
+    launch crosses that line between T = 9578 (150 key + 9578 query units:
+    64 per CTA, shares of 16) and T = 9579 (9729 units: 65 per CTA, a share
+    of 17); both depths wrap their ring many times and must give the same
+    bytes as the oracle."""
+    w = wl.make_random(T, 64, wl.ROPE_NEOX, seed=2500 + T)
+    ref = run_oracle(w)
+    d = DeviceWorkload(w)
+    assert_same(w, d.run("fused"), ref)
+    assert int(d.err.item()) == 0
+
+
 @pytest.mark.parametrize("hadamard", [False, True], ids=["plain", "rotated"])
 @pytest.mark.parametrize("style", STYLES)
 @pytest.mark.parametrize("scale", [1.0, 40.0, 1e-3, 3e4])
